@@ -1,0 +1,147 @@
+"""fp64 CPU oracle for ragged softmax attention -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this package.  The CUDA library never calls it and shares no
+code with it.
+
+Two parts:
+  * ``paged_decode`` / ``varlen_prefill``: the plain definition of softmax
+    attention over a paged or packed KV store, computed in fp64 by ``oracle.c``
+    (see the header there for the passages each step follows);
+  * ``planning``: the pages' bookkeeping formulas (task mapping, page/stack
+    counts, query folding, packed-query tiles, split-KV workspace size, the
+    static-anchor budget), restated independently of the library's planner.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so with gcc (plain C, no vector intrinsics)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-pthread", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        I = ctypes.c_int
+        L = ctypes.c_int64
+        D = ctypes.c_double
+        lib.oracle_paged_decode.restype = I
+        lib.oracle_paged_decode.argtypes = [P, P, P, P, P, P, P, L, P, I, I, I, I, I, I, I, I, I, D,
+                                            P, L, P, P, I]
+        lib.oracle_varlen_prefill.restype = I
+        lib.oracle_varlen_prefill.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, D,
+                                              P, L, P, P, I]
+        _lib = lib
+    return _lib
+
+
+def _bf16(t: torch.Tensor) -> torch.Tensor:
+    t = t.detach()
+    if t.device.type != "cpu":
+        t = t.cpu()
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"oracle expects bfloat16 inputs, got {t.dtype}")
+    return t
+
+
+def _strides(t: torch.Tensor) -> np.ndarray:
+    return np.ascontiguousarray(np.array(t.stride(), dtype=np.int64))
+
+
+def _i32(t) -> np.ndarray:
+    if isinstance(t, torch.Tensor):
+        t = t.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(t, dtype=np.int32))
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def paged_decode(q, k_cache, v_cache, block_table, seq_lens, scale, rows=None, threads=None):
+    """Softmax attention of every (b, t, h) query row over its paged keys.
+
+    q [B, q_len, Hq, Dk], k_cache [P, ps, Hkv, Dk], v_cache [P, ps, Hkv, Dv]
+    (bfloat16, any strides), block_table [B, max_pages] int32, seq_lens [B].
+    rows: optional flat row ids (b * q_len + t) * Hq + h to compute; default all.
+    Returns (out [n_rows, Dv] float64, lse [n_rows] float64, natural log).
+    """
+    lib = _load()
+    q, k_cache, v_cache = _bf16(q), _bf16(k_cache), _bf16(v_cache)
+    B, q_len, Hq, Dk = q.shape
+    P, ps, Hkv, Dk2 = k_cache.shape
+    Dv = v_cache.shape[3]
+    assert Dk2 == Dk and tuple(v_cache.shape[:3]) == (P, ps, Hkv)
+    bt = _i32(block_table)
+    sl = _i32(seq_lens)
+    assert bt.ndim == 2 and bt.shape[0] == B and sl.shape == (B,)
+    if rows is None:
+        rows_arr = np.arange(B * q_len * Hq, dtype=np.int64)
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    n = rows_arr.size
+    out = np.zeros((n, Dv), dtype=np.float64)
+    lse = np.zeros((n,), dtype=np.float64)
+    qs, ks, vs = _strides(q), _strides(k_cache), _strides(v_cache)
+    rc = lib.oracle_paged_decode(
+        q.data_ptr(), qs.ctypes.data, k_cache.data_ptr(), ks.ctypes.data,
+        v_cache.data_ptr(), vs.ctypes.data, bt.ctypes.data, bt.shape[1], sl.ctypes.data,
+        B, q_len, Hq, Hkv, Dk, Dv, ps, P, bt.shape[1], float(scale),
+        rows_arr.ctypes.data, n, out.ctypes.data, lse.ctypes.data,
+        int(threads or default_threads()))
+    if rc != 0:
+        raise ValueError(f"oracle_paged_decode failed with code {rc}")
+    return out, lse
+
+
+def varlen_prefill(q, k, v, cu_seqlens_q, cu_seqlens_k, causal, scale, rows=None, threads=None):
+    """Softmax attention of every packed query row over its own sequence's keys.
+
+    q [total_q, Hq, Dk], k [total_k, Hkv, Dk], v [total_k, Hkv, Dv] bfloat16;
+    cu_seqlens_q / cu_seqlens_k [B+1].  rows: optional flat ids token * Hq + h.
+    Returns (out [n_rows, Dv] float64, lse [n_rows] float64, natural log).
+    """
+    lib = _load()
+    q, k, v = _bf16(q), _bf16(k), _bf16(v)
+    total_q, Hq, Dk = q.shape
+    total_k, Hkv, Dk2 = k.shape
+    Dv = v.shape[2]
+    assert Dk2 == Dk and tuple(v.shape[:2]) == (total_k, Hkv)
+    cq, ck = _i32(cu_seqlens_q), _i32(cu_seqlens_k)
+    B = cq.size - 1
+    assert ck.size == B + 1 and cq[-1] == total_q and ck[-1] <= total_k
+    if rows is None:
+        rows_arr = np.arange(total_q * Hq, dtype=np.int64)
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    n = rows_arr.size
+    out = np.zeros((n, Dv), dtype=np.float64)
+    lse = np.zeros((n,), dtype=np.float64)
+    qs, ks, vs = _strides(q), _strides(k), _strides(v)
+    rc = lib.oracle_varlen_prefill(
+        q.data_ptr(), qs.ctypes.data, k.data_ptr(), ks.ctypes.data, v.data_ptr(), vs.ctypes.data,
+        cq.ctypes.data, ck.ctypes.data, B, Hq, Hkv, Dk, Dv, int(bool(causal)), float(scale),
+        rows_arr.ctypes.data, n, out.ctypes.data, lse.ctypes.data,
+        int(threads or default_threads()))
+    if rc != 0:
+        raise ValueError(f"oracle_varlen_prefill failed with code {rc}")
+    return out, lse

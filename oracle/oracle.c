@@ -1,0 +1,263 @@
+/*
+ * Plain fp64 CPU oracle for ragged softmax attention.  TEST INFRASTRUCTURE
+ * ONLY: the tests, the smoke check and the benchmark's CPU baseline call it;
+ * the product path never does.  It shares no code with the CUDA library.
+ *
+ * What it computes is the plain definition of softmax attention, per query
+ * row, written out with no blocking, no online recurrence and no KV split:
+ *
+ *   s_j  = scale * <q, k_j>                       (scores; "Flywheel Attention",
+ *                                                   section 1, P = softmax(QK^T);
+ *                                                   "Writing Page Attention with
+ *                                                   PyPTO", section 1.1, QK^T/sqrt(128))
+ *   m    = max_j s_j
+ *   l    = sum_j exp(s_j - m)
+ *   out  = sum_j exp(s_j - m) v_j / l             (O = PV)
+ *   lse  = m + ln l                               (natural-log log-sum-exp)
+ *
+ * over the keys the row may see.  Rows with no visible key give out = 0 and
+ * lse = -inf ("TokenSpeed-MLA 2.0.1", SM107 decode section: rows with no
+ * visible keys produce zero output and -inf LSE).
+ *
+ * Paged decode ("Writing Page Attention with PyPTO", sections 1.2-1.3 and 5.2):
+ *   query head h reads KV head h / G with G = Hq / Hkv (consecutive query heads
+ *   share a KV head: KV head 1 serves query heads 5-9 when G = 5); logical key
+ *   j of batch row b lives in physical page block_table[b, j / page_size] at
+ *   slot j % page_size.  With q_len > 1 query tokens the rows are causal and
+ *   bottom-right aligned: token t sees keys 0 .. n - q_len + t.
+ *
+ * Varlen prefill ("TokenSpeed-MLA 2.0.1", capability summary: ragged varlen
+ * prefill without padding, Q and KV packs described by separate cumulative
+ * sequence lengths, causal or not):
+ *   sequence i owns query rows cu_q[i] .. cu_q[i+1]-1 and keys cu_k[i] ..
+ *   cu_k[i+1]-1; with causal masking row r (0-based inside the sequence) sees
+ *   keys 0 .. r + Lk - Lq (bottom-right alignment, as the page's benchmark
+ *   command selects with --bottom_right_align).
+ *
+ * Inputs are BF16 bit patterns (uint16); each is widened exactly to double.
+ * Strides are in elements.  Every function returns 0 on success or a negative
+ * code for an out-of-range index (an invalid page number, a bad row id).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+static double bf16_to_double(uint16_t bits) {
+    uint32_t w = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return (double)f;
+}
+
+/* One query row against an explicit list of key/value row pointers. */
+static void attend_row(const uint16_t *q, int64_t q_dstride,
+                       const uint16_t *const *krows, int64_t k_dstride,
+                       const uint16_t *const *vrows, int64_t v_dstride,
+                       int64_t nkeys, int dk, int dv, double scale,
+                       double *s /* scratch [nkeys] */, double *out, double *lse) {
+    if (nkeys <= 0) {
+        for (int d = 0; d < dv; ++d) out[d] = 0.0;
+        *lse = -INFINITY;
+        return;
+    }
+    double m = -INFINITY;
+    for (int64_t j = 0; j < nkeys; ++j) {
+        double acc = 0.0;
+        for (int d = 0; d < dk; ++d)
+            acc += bf16_to_double(q[d * q_dstride]) * bf16_to_double(krows[j][d * k_dstride]);
+        s[j] = scale * acc;
+        if (s[j] > m) m = s[j];
+    }
+    double l = 0.0;
+    for (int d = 0; d < dv; ++d) out[d] = 0.0;
+    for (int64_t j = 0; j < nkeys; ++j) {
+        double p = exp(s[j] - m);
+        l += p;
+        for (int d = 0; d < dv; ++d) out[d] += p * bf16_to_double(vrows[j][d * v_dstride]);
+    }
+    for (int d = 0; d < dv; ++d) out[d] /= l;
+    *lse = m + log(l);
+}
+
+/* ------------------------------------------------------------------ decode */
+
+typedef struct {
+    const uint16_t *q; const int64_t *qs;        /* [B, q_len, Hq, Dk] */
+    const uint16_t *k; const int64_t *ks;        /* [P, ps, Hkv, Dk]   */
+    const uint16_t *v; const int64_t *vs;        /* [P, ps, Hkv, Dv]   */
+    const int32_t *bt; int64_t bt_stride;        /* [B, max_pages]     */
+    const int32_t *seq_lens;                     /* [B]                */
+    int B, q_len, Hq, Hkv, Dk, Dv, ps, num_pages, max_pages;
+    double scale;
+    const int64_t *rows; int64_t n_rows;
+    double *out, *lse;
+    int64_t begin, end;
+    int status;
+} decode_job;
+
+static void *decode_worker(void *arg) {
+    decode_job *J = (decode_job *)arg;
+    int G = J->Hq / J->Hkv;
+    int64_t cap = (int64_t)J->max_pages * J->ps;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(cap > 0 ? cap : 1));
+    const uint16_t **kr = (const uint16_t **)malloc(sizeof(void *) * (size_t)(cap > 0 ? cap : 1));
+    const uint16_t **vr = (const uint16_t **)malloc(sizeof(void *) * (size_t)(cap > 0 ? cap : 1));
+    if (!s || !kr || !vr) { J->status = -3; goto done; }
+    for (int64_t i = J->begin; i < J->end; ++i) {
+        int64_t row = J->rows ? J->rows[i] : i;
+        if (row < 0 || row >= (int64_t)J->B * J->q_len * J->Hq) { J->status = -2; break; }
+        int h = (int)(row % J->Hq);
+        int t = (int)((row / J->Hq) % J->q_len);
+        int b = (int)(row / ((int64_t)J->Hq * J->q_len));
+        int g = h / G;                                   /* consecutive heads share a KV head */
+        int64_t n = J->seq_lens[b];
+        int64_t visible = n - J->q_len + t + 1;          /* bottom-right causal for q_len > 1 */
+        if (visible > n) visible = n;
+        if (visible < 0) visible = 0;
+        if (n > cap) { J->status = -1; break; }
+        for (int64_t j = 0; j < visible; ++j) {
+            int32_t page = J->bt[(int64_t)b * J->bt_stride + j / J->ps];
+            if (page < 0 || page >= J->num_pages) { J->status = -1; goto done; }
+            int64_t slot = j % J->ps;
+            kr[j] = J->k + page * J->ks[0] + slot * J->ks[1] + (int64_t)g * J->ks[2];
+            vr[j] = J->v + page * J->vs[0] + slot * J->vs[1] + (int64_t)g * J->vs[2];
+        }
+        const uint16_t *qrow = J->q + b * J->qs[0] + t * J->qs[1] + h * J->qs[2];
+        attend_row(qrow, J->qs[3], kr, J->ks[3], vr, J->vs[3], visible, J->Dk, J->Dv,
+                   J->scale, s, J->out + i * J->Dv, J->lse + i);
+    }
+done:
+    free(s); free(kr); free(vr);
+    return NULL;
+}
+
+int oracle_paged_decode(const uint16_t *q, const int64_t *q_stride,
+                        const uint16_t *k_cache, const int64_t *k_stride,
+                        const uint16_t *v_cache, const int64_t *v_stride,
+                        const int32_t *block_table, int64_t bt_stride,
+                        const int32_t *seq_lens,
+                        int B, int q_len, int Hq, int Hkv, int Dk, int Dv,
+                        int page_size, int num_pages, int max_pages, double scale,
+                        const int64_t *rows, int64_t n_rows,
+                        double *out, double *lse, int n_threads) {
+    if (Hkv <= 0 || Hq % Hkv != 0 || page_size <= 0) return -4;
+    if (n_threads < 1) n_threads = 1;
+    if (n_rows < n_threads) n_threads = (int)(n_rows > 0 ? n_rows : 1);
+    decode_job *jobs = (decode_job *)calloc((size_t)n_threads, sizeof(decode_job));
+    pthread_t *tid = (pthread_t *)calloc((size_t)n_threads, sizeof(pthread_t));
+    if (!jobs || !tid) { free(jobs); free(tid); return -3; }
+    for (int w = 0; w < n_threads; ++w) {
+        decode_job *J = &jobs[w];
+        J->q = q; J->qs = q_stride; J->k = k_cache; J->ks = k_stride; J->v = v_cache; J->vs = v_stride;
+        J->bt = block_table; J->bt_stride = bt_stride; J->seq_lens = seq_lens;
+        J->B = B; J->q_len = q_len; J->Hq = Hq; J->Hkv = Hkv; J->Dk = Dk; J->Dv = Dv;
+        J->ps = page_size; J->num_pages = num_pages; J->max_pages = max_pages; J->scale = scale;
+        J->rows = rows; J->n_rows = n_rows; J->out = out; J->lse = lse;
+        J->begin = n_rows * w / n_threads; J->end = n_rows * (w + 1) / n_threads;
+        pthread_create(&tid[w], NULL, decode_worker, J);
+    }
+    int status = 0;
+    for (int w = 0; w < n_threads; ++w) {
+        pthread_join(tid[w], NULL);
+        if (jobs[w].status) status = jobs[w].status;
+    }
+    free(jobs); free(tid);
+    return status;
+}
+
+/* ----------------------------------------------------------------- prefill */
+
+typedef struct {
+    const uint16_t *q; const int64_t *qs;        /* [total_q, Hq, Dk]  */
+    const uint16_t *k; const int64_t *ks;        /* [total_k, Hkv, Dk] */
+    const uint16_t *v; const int64_t *vs;        /* [total_k, Hkv, Dv] */
+    const int32_t *cu_q, *cu_k;                  /* [B + 1]            */
+    int B, Hq, Hkv, Dk, Dv, causal;
+    int64_t total_q, max_k;
+    double scale;
+    const int64_t *rows; int64_t n_rows;
+    double *out, *lse;
+    int64_t begin, end;
+    int status;
+} prefill_job;
+
+static void *prefill_worker(void *arg) {
+    prefill_job *J = (prefill_job *)arg;
+    int G = J->Hq / J->Hkv;
+    int64_t cap = J->max_k > 0 ? J->max_k : 1;
+    double *s = (double *)malloc(sizeof(double) * (size_t)cap);
+    const uint16_t **kr = (const uint16_t **)malloc(sizeof(void *) * (size_t)cap);
+    const uint16_t **vr = (const uint16_t **)malloc(sizeof(void *) * (size_t)cap);
+    if (!s || !kr || !vr) { J->status = -3; goto done; }
+    for (int64_t i = J->begin; i < J->end; ++i) {
+        int64_t row = J->rows ? J->rows[i] : i;
+        if (row < 0 || row >= J->total_q * J->Hq) { J->status = -2; break; }
+        int h = (int)(row % J->Hq);
+        int64_t tok = row / J->Hq;
+        int seq = -1;
+        for (int b = 0; b < J->B; ++b)
+            if (tok >= J->cu_q[b] && tok < J->cu_q[b + 1]) { seq = b; break; }
+        if (seq < 0) { J->status = -2; break; }
+        int64_t Lq = J->cu_q[seq + 1] - J->cu_q[seq];
+        int64_t Lk = J->cu_k[seq + 1] - J->cu_k[seq];
+        int64_t r = tok - J->cu_q[seq];
+        int64_t visible = Lk;
+        if (J->causal) {
+            visible = r + Lk - Lq + 1;                   /* bottom-right alignment */
+            if (visible > Lk) visible = Lk;
+            if (visible < 0) visible = 0;
+        }
+        int g = h / G;
+        for (int64_t j = 0; j < visible; ++j) {
+            int64_t kt = J->cu_k[seq] + j;
+            kr[j] = J->k + kt * J->ks[0] + (int64_t)g * J->ks[1];
+            vr[j] = J->v + kt * J->vs[0] + (int64_t)g * J->vs[1];
+        }
+        const uint16_t *qrow = J->q + tok * J->qs[0] + (int64_t)h * J->qs[1];
+        attend_row(qrow, J->qs[2], kr, J->ks[2], vr, J->vs[2], visible, J->Dk, J->Dv,
+                   J->scale, s, J->out + i * J->Dv, J->lse + i);
+    }
+done:
+    free(s); free(kr); free(vr);
+    return NULL;
+}
+
+int oracle_varlen_prefill(const uint16_t *q, const int64_t *q_stride,
+                          const uint16_t *k, const int64_t *k_stride,
+                          const uint16_t *v, const int64_t *v_stride,
+                          const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                          int B, int Hq, int Hkv, int Dk, int Dv, int causal, double scale,
+                          const int64_t *rows, int64_t n_rows,
+                          double *out, double *lse, int n_threads) {
+    if (Hkv <= 0 || Hq % Hkv != 0) return -4;
+    int64_t max_k = 0;
+    for (int b = 0; b < B; ++b) {
+        int64_t L = (int64_t)cu_seqlens_k[b + 1] - cu_seqlens_k[b];
+        if (L < 0 || cu_seqlens_q[b + 1] < cu_seqlens_q[b]) return -1;
+        if (L > max_k) max_k = L;
+    }
+    if (n_threads < 1) n_threads = 1;
+    if (n_rows < n_threads) n_threads = (int)(n_rows > 0 ? n_rows : 1);
+    prefill_job *jobs = (prefill_job *)calloc((size_t)n_threads, sizeof(prefill_job));
+    pthread_t *tid = (pthread_t *)calloc((size_t)n_threads, sizeof(pthread_t));
+    if (!jobs || !tid) { free(jobs); free(tid); return -3; }
+    for (int w = 0; w < n_threads; ++w) {
+        prefill_job *J = &jobs[w];
+        J->q = q; J->qs = q_stride; J->k = k; J->ks = k_stride; J->v = v; J->vs = v_stride;
+        J->cu_q = cu_seqlens_q; J->cu_k = cu_seqlens_k;
+        J->B = B; J->Hq = Hq; J->Hkv = Hkv; J->Dk = Dk; J->Dv = Dv; J->causal = causal;
+        J->total_q = cu_seqlens_q[B]; J->max_k = max_k; J->scale = scale;
+        J->rows = rows; J->n_rows = n_rows; J->out = out; J->lse = lse;
+        J->begin = n_rows * w / n_threads; J->end = n_rows * (w + 1) / n_threads;
+        pthread_create(&tid[w], NULL, prefill_worker, J);
+    }
+    int status = 0;
+    for (int w = 0; w < n_threads; ++w) {
+        pthread_join(tid[w], NULL);
+        if (jobs[w].status) status = jobs[w].status;
+    }
+    free(jobs); free(tid);
+    return status;
+}
