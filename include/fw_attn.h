@@ -1,0 +1,210 @@
+/*
+ * fw_attn.h -- C ABI of the GB300 (sm_103a) ragged softmax attention library.
+ *
+ * Two operations, both fused online-softmax attention that never materialises
+ * the probability matrix (running max m, running sum l and a rescaled output
+ * accumulator o, "Flywheel Attention: Attention Kernels Built for the TPU",
+ * section 1, the FlashAttention recurrence):
+ *
+ *   fw_paged_decode    -- grouped-query decode over a paged, ragged KV cache
+ *                         addressed through block_table[batch, logical_page]
+ *                         ("Writing Page Attention with PyPTO", sections 1.2-1.3
+ *                         and 5.2), with split-KV partials merged by a
+ *                         log-sum-exp combine ("TokenSpeed-MLA 2.0.1", decode:
+ *                         a split-KV attention kernel plus a reduction kernel).
+ *   fw_varlen_prefill  -- ragged varlen prefill without padding, Q and KV packs
+ *                         given by cumulative sequence lengths, causal or not
+ *                         ("TokenSpeed-MLA 2.0.1", capability summary, MLA Prefill).
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are passed as fw_tensor_t: a DEVICE pointer, a dtype, up to 5
+ *     dimensions and strides IN ELEMENTS.  The caller owns every tensor; the
+ *     library never frees or retains them past the call.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  They never synchronise the host and never copy device data to
+ *     the host; split planning uses shapes only (max_pages * page_size bounds
+ *     every sequence).
+ *   - Arithmetic: BF16 inputs, FP32 accumulation and softmax state, BF16 output
+ *     rounded to nearest even, FP32 LSE.  LSE is the NATURAL log of
+ *     sum_j exp(scale * <q, k_j>) over the visible keys.
+ *   - Grouped-query heads: query head h reads KV head h / (Hq / Hkv), so
+ *     consecutive query heads share a KV head (PyPTO section 1.3: KV head 1
+ *     serves query heads 5-9 at 40 Q / 8 KV heads).
+ *   - Rows with no visible key produce a zero output row and LSE = -inf
+ *     ("TokenSpeed-MLA 2.0.1", SM107 decode section).
+ *   - Errors: invalid shapes, dtypes, strides or alignment return a status and
+ *     launch nothing; fw_last_error() then describes the problem.  A CUDA
+ *     launch failure returns FW_ERR_CUDA.  A device-side wait that exceeds its
+ *     time limit does not trap: the kernel records FW_ERR_DEVICE_TIMEOUT in a
+ *     device status word and exits; read it with fw_get_device_status().
+ */
+#ifndef FW_ATTN_H
+#define FW_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *fw_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+    FW_OK = 0,
+    FW_ERR_INVALID_ARG = 1,     /* inconsistent shapes / dtypes / strides / NULL data */
+    FW_ERR_UNSUPPORTED = 2,     /* valid but not implemented (head dim, page size, ...) */
+    FW_ERR_WORKSPACE = 3,       /* caller workspace too small, or allocation failed */
+    FW_ERR_CUDA = 4,            /* a CUDA runtime / driver call failed */
+    FW_ERR_DEVICE_TIMEOUT = 5   /* a kernel gave up waiting (reported by fw_get_device_status) */
+} fw_status_t;
+
+typedef enum { FW_BF16 = 0, FW_F32 = 1, FW_I32 = 2 } fw_dtype_t;
+
+typedef struct {
+    void *data;          /* device pointer (may be NULL only when every extent is 0) */
+    int32_t dtype;       /* fw_dtype_t */
+    int32_t ndim;        /* 1..5 */
+    int64_t shape[5];
+    int64_t stride[5];   /* in elements */
+} fw_tensor_t;
+
+/*
+ * Paged grouped-query decode.
+ *
+ *   q           [B, q_len, Hq, Dk]            BF16, last dim contiguous
+ *   k_cache     [num_pages, ps, Hkv, Dk]      BF16, last dim contiguous
+ *   v_cache     [num_pages, ps, Hkv, Dv]      BF16, last dim contiguous; may be a
+ *                                             strided view of k_cache (latent heads:
+ *                                             V = the first Dv columns of each K row)
+ *   block_table [B, max_pages]                I32; entry [b, p] is the physical page of
+ *                                             logical page p of row b.  Entries at or
+ *                                             past ceil(seq_lens[b] / ps) are never read
+ *                                             (PyPTO section 9.1) and may hold anything.
+ *   seq_lens    [B]                           I32; keys of row b, including the q_len
+ *                                             new tokens; 0 <= seq_lens[b] <= max_pages*ps.
+ *   scale       softmax scale applied to <q, k> before the max (PyPTO section 6.2).
+ *   out         [B, q_len, Hq, Dv]            BF16, written.
+ *   lse         [B, q_len, Hq]                F32, written; may be NULL.
+ *
+ * With q_len > 1 the query tokens are causal and bottom-right aligned: token
+ * t sees keys 0 .. seq_lens[b] - q_len + t.  With q_len = 1 every key is seen.
+ *
+ * Supported: Dk = Dv in {128, 256}; Hq % Hkv == 0 (any group size); page sizes
+ * 8, 16, 32, 64, 128 or any multiple of 128;
+ * 1 <= q_len <= 4; strides multiples of 8 elements and 16-byte aligned base
+ * pointers (tensor-memory-accelerator addressing).
+ *
+ * Split-KV: the library cuts each row's keys into chunks sized from shapes
+ * only and merges the FP32 partials (normalised output + log2-sum-exp per
+ * row per split) with a second kernel.  The partials live in a workspace:
+ * caller-provided through fw_set_workspace(), else an internal buffer grown
+ * on demand with cudaMalloc (grow it once, outside any stream capture, by an
+ * initial call with the largest shapes).
+ */
+fw_status_t fw_paged_decode(const fw_tensor_t *q, const fw_tensor_t *k_cache,
+                            const fw_tensor_t *v_cache, const fw_tensor_t *block_table,
+                            const fw_tensor_t *seq_lens, float scale,
+                            fw_tensor_t *out, fw_tensor_t *lse, fw_stream_t stream);
+
+/*
+ * Workspace bytes fw_paged_decode needs for these shapes (data pointers are
+ * not read).  Writes the size to *bytes; 0 when no row is ever split.
+ * The size is rows * splits * (Dv + 1) * 4 bytes, with rows = B * q_len * Hq:
+ * one FP32 partial output row plus one FP32 LSE per row per split
+ * ("TokenSpeed-MLA 2.0.1", packed-query paragraph, 513 floats per row at Dv 512).
+ */
+fw_status_t fw_paged_decode_workspace_size(const fw_tensor_t *q, const fw_tensor_t *k_cache,
+                                           const fw_tensor_t *v_cache,
+                                           const fw_tensor_t *block_table, size_t *bytes);
+
+/*
+ * Ragged varlen prefill.
+ *
+ *   q            [total_q, Hq, Dk]   BF16
+ *   k            [total_k, Hkv, Dk]  BF16
+ *   v            [total_k, Hkv, Dv]  BF16
+ *   cu_seqlens_q [B + 1]             I32 prefix sums of the query lengths (cu[0] = 0)
+ *   cu_seqlens_k [B + 1]             I32 prefix sums of the key lengths; may differ from Q's
+ *   causal       nonzero: row r of a sequence (0-based) sees keys 0 .. r + Lk - Lq
+ *                (bottom-right alignment); zero: every key of its sequence.
+ *   out          [total_q, Hq, Dv]   BF16, written
+ *   lse          [total_q, Hq]       F32, written; may be NULL
+ *
+ * Supported: Dk = Dv in {128, 256}; Hq % Hkv == 0; strides multiples of 8
+ * elements, 16-byte aligned base pointers.  cu_seqlens_q[B] must equal total_q
+ * and cu_seqlens_k[B] must not exceed total_k (checked on the device: a
+ * sequence reaching past the packed tensors is skipped and flagged in the
+ * device status word as FW_ERR_INVALID_ARG).
+ */
+fw_status_t fw_varlen_prefill(const fw_tensor_t *q, const fw_tensor_t *k, const fw_tensor_t *v,
+                              const fw_tensor_t *cu_seqlens_q, const fw_tensor_t *cu_seqlens_k,
+                              int causal, float scale, fw_tensor_t *out, fw_tensor_t *lse,
+                              fw_stream_t stream);
+
+/*
+ * Caller-owned workspace for the CURRENT device (ptr = NULL, bytes = 0 returns
+ * to the internal buffer).  The library never frees it.  Calls on one device
+ * that share the workspace must be ordered (same stream, or synchronised).
+ */
+fw_status_t fw_set_workspace(void *ptr, size_t bytes, fw_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word of the
+ * current device: 0 when every kernel since the last read finished normally,
+ * else the fw_status_t code of the first failure (FW_ERR_DEVICE_TIMEOUT when a
+ * kernel abandoned a wait, FW_ERR_INVALID_ARG for a bad sequence extent).
+ */
+fw_status_t fw_get_device_status(fw_stream_t stream, int32_t *code);
+
+/* Message for the last failing call on this host thread ("" if none). */
+const char *fw_last_error(void);
+
+/* Tunables, mostly for tests and measurement. */
+typedef enum {
+    FW_OPT_DECODE_CHUNK_TOKENS = 0, /* force the split-KV chunk (multiple of 128; 0 = auto) */
+    FW_OPT_WAIT_TIMEOUT_MS = 1,     /* device wait limit before giving up (default 2000) */
+    FW_OPT_KERNEL_TIMING = 2,       /* 1: record CUDA events around each attention kernel */
+    FW_OPT_MAX_CTAS = 3             /* cap on persistent CTAs (0 = one per SM) */
+} fw_option_t;
+
+fw_status_t fw_set_option(int32_t option, int64_t value);
+
+/*
+ * With FW_OPT_KERNEL_TIMING on, the summed device time (ms) of the attention
+ * kernels (decode or prefill main kernel, not the combine) since the last
+ * read and the number of such launches.  Synchronises the device.  Resets the
+ * accumulators.
+ */
+fw_status_t fw_kernel_timing_read(double *total_ms, int64_t *launches);
+
+/* Total kernels this library has launched in this process (all kinds). */
+int64_t fw_launch_count(void);
+
+/*
+ * Host-side decode plan for given shapes (no device access), exposed so the
+ * planner can be checked without a GPU.  num_sms <= 0 queries the current
+ * device.  Fields are written on success.
+ */
+typedef struct {
+    int32_t group;            /* G = Hq / Hkv */
+    int32_t rows_per_unit;    /* NQ: MMA N extent holding the (token, head) rows of one unit */
+    int32_t tokens_per_unit;  /* query tokens one unit covers (whole head groups) */
+    int32_t heads_per_unit;   /* query heads one unit covers */
+    int32_t row_groups;       /* units per (batch, kv head, split) */
+    int32_t chunk_tokens;     /* keys per split (multiple of 128) */
+    int32_t max_splits;       /* ceil(max_pages * ps / chunk_tokens) */
+    int64_t num_units;        /* B * Hkv * row_groups * max_splits (upper bound) */
+    int64_t workspace_bytes;  /* 0 when max_splits == 1 */
+    int32_t grid;             /* persistent CTAs launched */
+} fw_decode_plan_t;
+
+fw_status_t fw_plan_decode(int32_t batch, int32_t q_len, int32_t num_q_heads,
+                           int32_t num_kv_heads, int32_t head_dim_v, int64_t max_kv_len,
+                           int32_t num_sms, fw_decode_plan_t *plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FW_ATTN_H */

@@ -1,0 +1,522 @@
+// C ABI of the library: argument validation, planning, tensor-map encoding,
+// workspace and status-word management, and kernel launches.  Every entry
+// point is declared and documented in include/fw_attn.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/fw_attn.h"
+#include "fw_internal.h"
+
+namespace {
+
+__device__ int g_fw_status = 0;
+
+constexpr int kMaxDevices = 64;
+
+thread_local char t_error[512] = "";
+
+fw_status_t fail(fw_status_t st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_error, sizeof t_error, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+fw_status_t ok() {
+    t_error[0] = '\0';
+    return FW_OK;
+}
+
+struct DeviceState {
+    bool init = false;
+    int num_sms = 0;
+    int *status = nullptr;          // device address of g_fw_status
+    void *ws = nullptr;             // internal workspace
+    size_t ws_bytes = 0;
+    void *user_ws = nullptr;        // caller workspace
+    size_t user_ws_bytes = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+std::atomic<int64_t> g_launches{0};
+int64_t g_opt_chunk = 0;
+int64_t g_opt_timeout_ms = 2000;
+int64_t g_opt_timing = 0;
+int64_t g_opt_max_ctas = 0;
+
+struct TimedLaunch { cudaEvent_t a, b; };
+std::vector<TimedLaunch> g_timed;      // pending event pairs
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t pooled_event() {
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+fw_status_t device_state(DeviceState **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(FW_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(FW_ERR_UNSUPPORTED, "device index %d out of range", dev);
+    DeviceState &d = g_dev[dev];
+    if (!d.init) {
+        e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return fail(FW_ERR_CUDA, "multiprocessor count: %s", cudaGetErrorString(e));
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (major != 10 || minor != 3)
+            return fail(FW_ERR_UNSUPPORTED, "this library is built for sm_103a (GB300); device %d is sm_%d%d",
+                        dev, major, minor);
+        e = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.status), g_fw_status);
+        if (e != cudaSuccess) return fail(FW_ERR_CUDA, "status word address: %s", cudaGetErrorString(e));
+        d.init = true;
+    }
+    *out = &d;
+    return FW_OK;
+}
+
+// ---------------------------------------------------------------- tensor maps
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+fw_status_t get_encoder() {
+    if (g_encode) return FW_OK;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return fail(FW_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return FW_OK;
+}
+
+// BF16 tensor map with 128-byte swizzle; dims/strides innermost first,
+// strides in bytes for dims 1..rank-1.
+fw_status_t encode_bf16(CUtensorMap *tm, const void *base, int rank, const uint64_t *dims,
+                        const uint64_t *strides_bytes, const uint32_t *box, const char *what) {
+    if (fw_status_t s = get_encoder()) return s;
+    uint32_t elem[5] = {1, 1, 1, 1, 1};
+    CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base),
+                          dims, strides_bytes, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(FW_ERR_INVALID_ARG, "tensor map for %s rejected (CUresult %d)", what, (int)r);
+    return FW_OK;
+}
+
+// ----------------------------------------------------------------- validation
+
+const char *dtype_name(int32_t d) {
+    switch (d) { case FW_BF16: return "bf16"; case FW_F32: return "f32"; case FW_I32: return "i32"; default: return "?"; }
+}
+
+fw_status_t check_tensor(const fw_tensor_t *t, const char *name, int ndim, int32_t dtype, bool allow_null = false) {
+    if (!t) return allow_null ? FW_OK : fail(FW_ERR_INVALID_ARG, "%s is NULL", name);
+    if (t->ndim != ndim) return fail(FW_ERR_INVALID_ARG, "%s: expected %d dims, got %d", name, ndim, t->ndim);
+    if (t->dtype != dtype)
+        return fail(FW_ERR_INVALID_ARG, "%s: expected dtype %s, got %s", name, dtype_name(dtype), dtype_name(t->dtype));
+    int64_t numel = 1;
+    for (int i = 0; i < ndim; ++i) {
+        if (t->shape[i] < 0) return fail(FW_ERR_INVALID_ARG, "%s: negative extent", name);
+        if (t->stride[i] < 0) return fail(FW_ERR_INVALID_ARG, "%s: negative stride", name);
+        numel *= t->shape[i];
+    }
+    if (numel > 0 && !t->data) return fail(FW_ERR_INVALID_ARG, "%s: NULL data", name);
+    if (numel > 0 && t->stride[ndim - 1] != 1 && t->shape[ndim - 1] > 1)
+        return fail(FW_ERR_INVALID_ARG, "%s: last dimension must be contiguous", name);
+    return FW_OK;
+}
+
+// Tensors read through the tensor memory accelerator: 16-byte aligned base,
+// every outer stride a multiple of 8 BF16 elements (16 bytes).
+fw_status_t check_tma_layout(const fw_tensor_t *t, const char *name) {
+    if (reinterpret_cast<uintptr_t>(t->data) % 16 != 0)
+        return fail(FW_ERR_INVALID_ARG, "%s: base pointer must be 16-byte aligned", name);
+    for (int i = 0; i + 1 < t->ndim; ++i)
+        if (t->stride[i] % 8 != 0)
+            return fail(FW_ERR_INVALID_ARG, "%s: stride[%d] = %lld is not a multiple of 8 elements", name, i,
+                        (long long)t->stride[i]);
+    return FW_OK;
+}
+
+fw_status_t check_output_layout(const fw_tensor_t *t, const char *name) {
+    if (reinterpret_cast<uintptr_t>(t->data) % 16 != 0)
+        return fail(FW_ERR_INVALID_ARG, "%s: base pointer must be 16-byte aligned", name);
+    for (int i = 0; i + 1 < t->ndim; ++i)
+        if (t->stride[i] % 2 != 0)
+            return fail(FW_ERR_INVALID_ARG, "%s: stride[%d] must be even", name, i);
+    return FW_OK;
+}
+
+bool supported_page_size(int64_t ps) {
+    if (ps == 8 || ps == 16 || ps == 32 || ps == 64 || ps == 128) return true;
+    return ps > 128 && ps % 128 == 0 && ps <= (1 << 20);
+}
+
+// --------------------------------------------------------------------- planner
+
+fw_status_t plan_decode(int32_t B, int32_t q_len, int32_t Hq, int32_t Hkv, int32_t Dv, int64_t max_kv_len,
+                        int32_t num_sms, fw_decode_plan_t *pl) {
+    if (B < 0 || q_len < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || max_kv_len < 0 || Dv < 1)
+        return fail(FW_ERR_INVALID_ARG, "invalid decode shapes");
+    if (num_sms <= 0) return fail(FW_ERR_INVALID_ARG, "num_sms must be positive");
+    fw_decode_plan_t p{};
+    const int G = Hq / Hkv;
+    p.group = G;
+    // Fold query tokens next to the heads of a KV group: the largest F that
+    // divides q_len with G * F within the 32-row N budget ("TokenSpeed-MLA
+    // 2.0.1", fold_sq_factor, with 32 rows instead of 128 because here the
+    // query rows sit on the MMA N axis).  Groups wider than 32 heads are cut
+    // into 32-head chunks, one token each.
+    if (G <= 32) {
+        int F = 1;
+        for (int f = 1; f <= q_len; ++f)
+            if (q_len % f == 0 && G * f <= 32) F = f;
+        p.tokens_per_unit = F;
+        p.heads_per_unit = G;
+        p.rows_per_unit = G * F <= 16 ? 16 : 32;
+        p.row_groups = q_len / F;
+    } else {
+        p.tokens_per_unit = 1;
+        p.heads_per_unit = 32;
+        p.rows_per_unit = 32;
+        p.row_groups = q_len * ((G + 31) / 32);
+    }
+    const int64_t units_base = (int64_t)B * Hkv * p.row_groups;
+    const int64_t tiles_max = (max_kv_len + fw::kKvTile - 1) / fw::kKvTile;
+    int64_t chunk_tiles;
+    if (g_opt_chunk > 0) {
+        chunk_tiles = (g_opt_chunk + fw::kKvTile - 1) / fw::kKvTile;
+    } else {
+        // Aim for ~32 units per persistent CTA when every row is at the length
+        // bound, but never below 8 tiles (1024 keys) per split.
+        const int64_t target = 32LL * num_sms;
+        const int64_t want = units_base > 0 ? (target + units_base - 1) / units_base : 1;
+        chunk_tiles = tiles_max > 0 ? (tiles_max + want - 1) / want : 1;
+        if (chunk_tiles < 8) chunk_tiles = 8;
+    }
+    if (tiles_max > 0 && chunk_tiles > tiles_max) chunk_tiles = tiles_max;
+    if (chunk_tiles < 1) chunk_tiles = 1;
+    p.chunk_tokens = (int32_t)(chunk_tiles * fw::kKvTile);
+    p.max_splits = max_kv_len > 0 ? (int32_t)((max_kv_len + p.chunk_tokens - 1) / p.chunk_tokens) : 1;
+    p.num_units = units_base * p.max_splits;
+    const int64_t rows = (int64_t)B * q_len * Hq;
+    p.workspace_bytes = p.max_splits > 1 ? rows * p.max_splits * (int64_t)(Dv + 1) * 4 + 256 : 0;
+    int64_t grid = num_sms;
+    if (g_opt_max_ctas > 0 && grid > g_opt_max_ctas) grid = g_opt_max_ctas;
+    if (grid > p.num_units) grid = p.num_units;
+    p.grid = (int32_t)grid;
+    *pl = p;
+    return FW_OK;
+}
+
+fw_status_t get_workspace(DeviceState *d, size_t bytes, cudaStream_t stream, void **ptr) {
+    *ptr = nullptr;
+    if (bytes == 0) return FW_OK;
+    if (d->user_ws) {
+        if (d->user_ws_bytes < bytes)
+            return fail(FW_ERR_WORKSPACE, "caller workspace holds %zu bytes, %zu needed", d->user_ws_bytes, bytes);
+        *ptr = d->user_ws;
+        return FW_OK;
+    }
+    if (d->ws_bytes < bytes) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        cudaStreamIsCapturing(stream, &cs);
+        if (cs != cudaStreamCaptureStatusNone)
+            return fail(FW_ERR_WORKSPACE, "workspace must grow to %zu bytes during stream capture; "
+                        "make one call with these shapes before capturing", bytes);
+        if (d->ws) cudaFree(d->ws);
+        d->ws = nullptr;
+        d->ws_bytes = 0;
+        cudaError_t e = cudaMalloc(&d->ws, bytes);
+        if (e != cudaSuccess) return fail(FW_ERR_WORKSPACE, "cudaMalloc(%zu): %s", bytes, cudaGetErrorString(e));
+        d->ws_bytes = bytes;
+    }
+    *ptr = d->ws;
+    return FW_OK;
+}
+
+void timing_begin(cudaStream_t stream, cudaEvent_t *a) {
+    *a = nullptr;
+    if (!g_opt_timing) return;
+    *a = pooled_event();
+    cudaEventRecord(*a, stream);
+}
+
+void timing_end(cudaStream_t stream, cudaEvent_t a) {
+    if (!a) return;
+    cudaEvent_t b = pooled_event();
+    cudaEventRecord(b, stream);
+    g_timed.push_back({a, b});
+}
+
+}  // namespace
+
+// ============================================================== entry points
+
+extern "C" {
+
+const char *fw_last_error(void) { return t_error; }
+
+int64_t fw_launch_count(void) { return g_launches.load(); }
+
+fw_status_t fw_set_option(int32_t option, int64_t value) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    switch (option) {
+        case FW_OPT_DECODE_CHUNK_TOKENS:
+            if (value < 0 || value % fw::kKvTile) return fail(FW_ERR_INVALID_ARG, "chunk must be a multiple of 128");
+            g_opt_chunk = value; return ok();
+        case FW_OPT_WAIT_TIMEOUT_MS:
+            if (value < 1) return fail(FW_ERR_INVALID_ARG, "timeout must be positive");
+            g_opt_timeout_ms = value; return ok();
+        case FW_OPT_KERNEL_TIMING: g_opt_timing = value ? 1 : 0; return ok();
+        case FW_OPT_MAX_CTAS:
+            if (value < 0) return fail(FW_ERR_INVALID_ARG, "max CTAs must be >= 0");
+            g_opt_max_ctas = value; return ok();
+        default: return fail(FW_ERR_INVALID_ARG, "unknown option %d", option);
+    }
+}
+
+fw_status_t fw_kernel_timing_read(double *total_ms, int64_t *launches) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    double sum = 0.0;
+    int64_t n = 0;
+    for (auto &t : g_timed) {
+        cudaError_t e = cudaEventSynchronize(t.b);
+        float ms = 0.f;
+        if (e == cudaSuccess && cudaEventElapsedTime(&ms, t.a, t.b) == cudaSuccess) { sum += ms; ++n; }
+        g_event_pool.push_back(t.a);
+        g_event_pool.push_back(t.b);
+    }
+    g_timed.clear();
+    if (total_ms) *total_ms = sum;
+    if (launches) *launches = n;
+    return ok();
+}
+
+fw_status_t fw_plan_decode(int32_t batch, int32_t q_len, int32_t num_q_heads, int32_t num_kv_heads,
+                           int32_t head_dim_v, int64_t max_kv_len, int32_t num_sms, fw_decode_plan_t *plan) {
+    if (!plan) return fail(FW_ERR_INVALID_ARG, "plan is NULL");
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (num_sms <= 0) {
+        DeviceState *d = nullptr;
+        if (fw_status_t s = device_state(&d)) return s;
+        num_sms = d->num_sms;
+    }
+    if (fw_status_t s = plan_decode(batch, q_len, num_q_heads, num_kv_heads, head_dim_v, max_kv_len, num_sms, plan))
+        return s;
+    return ok();
+}
+
+fw_status_t fw_set_workspace(void *ptr, size_t bytes, fw_stream_t stream) {
+    (void)stream;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState *d = nullptr;
+    if (fw_status_t s = device_state(&d)) return s;
+    if (!ptr && bytes) return fail(FW_ERR_INVALID_ARG, "NULL workspace with nonzero size");
+    if (ptr && reinterpret_cast<uintptr_t>(ptr) % 256 != 0)
+        return fail(FW_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    d->user_ws = ptr;
+    d->user_ws_bytes = ptr ? bytes : 0;
+    return ok();
+}
+
+fw_status_t fw_get_device_status(fw_stream_t stream, int32_t *code) {
+    if (!code) return fail(FW_ERR_INVALID_ARG, "code is NULL");
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState *d = nullptr;
+    if (fw_status_t s = device_state(&d)) return s;
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(FW_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
+    int v = 0;
+    e = cudaMemcpy(&v, d->status, sizeof v, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail(FW_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+    const int zero = 0;
+    cudaMemcpy(d->status, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    *code = v;
+    return ok();
+}
+
+static fw_status_t decode_shapes(const fw_tensor_t *q, const fw_tensor_t *k_cache, const fw_tensor_t *v_cache,
+                                 const fw_tensor_t *block_table) {
+    if (fw_status_t s = check_tensor(q, "q", 4, FW_BF16)) return s;
+    if (fw_status_t s = check_tensor(k_cache, "k_cache", 4, FW_BF16)) return s;
+    if (fw_status_t s = check_tensor(v_cache, "v_cache", 4, FW_BF16)) return s;
+    if (fw_status_t s = check_tensor(block_table, "block_table", 2, FW_I32)) return s;
+    const int64_t B = q->shape[0], Hq = q->shape[2], Dk = q->shape[3];
+    const int64_t P = k_cache->shape[0], ps = k_cache->shape[1], Hkv = k_cache->shape[2];
+    if (k_cache->shape[3] != Dk) return fail(FW_ERR_INVALID_ARG, "k_cache head dim %lld != q head dim %lld",
+                                             (long long)k_cache->shape[3], (long long)Dk);
+    if (v_cache->shape[0] != P || v_cache->shape[1] != ps || v_cache->shape[2] != Hkv)
+        return fail(FW_ERR_INVALID_ARG, "v_cache [P, ps, Hkv] must match k_cache");
+    if (block_table->shape[0] != B) return fail(FW_ERR_INVALID_ARG, "block_table rows != batch");
+    if (block_table->shape[1] > 0 && block_table->stride[1] != 1)
+        return fail(FW_ERR_INVALID_ARG, "block_table rows must be contiguous");
+    if (Hkv < 1 || Hq % Hkv != 0) return fail(FW_ERR_INVALID_ARG, "Hq (%lld) must be a multiple of Hkv (%lld)",
+                                              (long long)Hq, (long long)Hkv);
+    if (ps < 1) return fail(FW_ERR_INVALID_ARG, "page size must be positive");
+    return FW_OK;
+}
+
+fw_status_t fw_paged_decode_workspace_size(const fw_tensor_t *q, const fw_tensor_t *k_cache,
+                                           const fw_tensor_t *v_cache, const fw_tensor_t *block_table,
+                                           size_t *bytes) {
+    if (!bytes) return fail(FW_ERR_INVALID_ARG, "bytes is NULL");
+    if (fw_status_t s = decode_shapes(q, k_cache, v_cache, block_table)) return s;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState *d = nullptr;
+    if (fw_status_t s = device_state(&d)) return s;
+    fw_decode_plan_t pl;
+    const int64_t max_kv = block_table->shape[1] * k_cache->shape[1];
+    if (fw_status_t s = plan_decode((int32_t)q->shape[0], (int32_t)q->shape[1], (int32_t)q->shape[2],
+                                    (int32_t)k_cache->shape[2], (int32_t)v_cache->shape[3], max_kv, d->num_sms, &pl))
+        return s;
+    *bytes = (size_t)pl.workspace_bytes;
+    return ok();
+}
+
+fw_status_t fw_paged_decode(const fw_tensor_t *q, const fw_tensor_t *k_cache, const fw_tensor_t *v_cache,
+                            const fw_tensor_t *block_table, const fw_tensor_t *seq_lens, float scale,
+                            fw_tensor_t *out, fw_tensor_t *lse, fw_stream_t stream_) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (fw_status_t s = decode_shapes(q, k_cache, v_cache, block_table)) return s;
+    if (fw_status_t s = check_tensor(seq_lens, "seq_lens", 1, FW_I32)) return s;
+    if (fw_status_t s = check_tensor(out, "out", 4, FW_BF16)) return s;
+    if (fw_status_t s = check_tensor(lse, "lse", 3, FW_F32, true)) return s;
+    const int64_t B = q->shape[0], q_len = q->shape[1], Hq = q->shape[2], Dk = q->shape[3];
+    const int64_t P = k_cache->shape[0], ps = k_cache->shape[1], Hkv = k_cache->shape[2];
+    const int64_t Dv = v_cache->shape[3];
+    const int64_t max_pages = block_table->shape[1];
+    if (seq_lens->shape[0] != B || (B > 0 && seq_lens->stride[0] != 1))
+        return fail(FW_ERR_INVALID_ARG, "seq_lens must be a contiguous [B] vector");
+    if (out->shape[0] != B || out->shape[1] != q_len || out->shape[2] != Hq || out->shape[3] != Dv)
+        return fail(FW_ERR_INVALID_ARG, "out must be [B, q_len, Hq, Dv]");
+    if (lse && (lse->shape[0] != B || lse->shape[1] != q_len || lse->shape[2] != Hq))
+        return fail(FW_ERR_INVALID_ARG, "lse must be [B, q_len, Hq]");
+    if (!std::isfinite(scale)) return fail(FW_ERR_INVALID_ARG, "scale must be finite");
+    if (!(Dk == Dv && (Dk == 128 || Dk == 256)))
+        return fail(FW_ERR_UNSUPPORTED, "decode head dims (Dk=%lld, Dv=%lld): supported Dk = Dv in {128, 256}",
+                    (long long)Dk, (long long)Dv);
+    if (q_len < 1 || q_len > 4) return fail(FW_ERR_UNSUPPORTED, "q_len must be in [1, 4]");
+    if (!supported_page_size(ps))
+        return fail(FW_ERR_UNSUPPORTED, "page size %lld: supported 8, 16, 32, 64, 128 or multiples of 128",
+                    (long long)ps);
+    if (B == 0) return ok();
+    if (P < 1 || max_pages < 1) return fail(FW_ERR_INVALID_ARG, "empty page pool or block table");
+    if (P > (1LL << 31) - 1 || max_pages * ps > (1LL << 30))
+        return fail(FW_ERR_UNSUPPORTED, "page pool or sequence bound too large");
+    if (fw_status_t s = check_tma_layout(q, "q")) return s;
+    if (fw_status_t s = check_tma_layout(k_cache, "k_cache")) return s;
+    if (fw_status_t s = check_tma_layout(v_cache, "v_cache")) return s;
+    if (fw_status_t s = check_output_layout(out, "out")) return s;
+    if (lse && reinterpret_cast<uintptr_t>(lse->data) % 4) return fail(FW_ERR_INVALID_ARG, "lse misaligned");
+
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState *d = nullptr;
+    if (fw_status_t s = device_state(&d)) return s;
+    fw_decode_plan_t pl;
+    if (fw_status_t s = plan_decode((int32_t)B, (int32_t)q_len, (int32_t)Hq, (int32_t)Hkv, (int32_t)Dv,
+                                    max_pages * ps, d->num_sms, &pl))
+        return s;
+    void *ws = nullptr;
+    if (fw_status_t s = get_workspace(d, (size_t)pl.workspace_bytes, stream, &ws)) return s;
+
+    fw::DecodeParams p{};
+    p.B = (int)B; p.q_len = (int)q_len; p.Hq = (int)Hq; p.Hkv = (int)Hkv; p.G = pl.group;
+    p.ps = (int)ps; p.max_pages = (int)max_pages; p.num_pages = (int)P;
+    p.rows = pl.rows_per_unit;
+    p.head_mode = pl.group <= 32 ? 0 : 1;
+    p.tokens_per_unit = pl.tokens_per_unit;
+    p.heads_per_unit = pl.heads_per_unit;
+    p.head_chunks = p.head_mode ? (pl.group + 31) / 32 : 1;
+    p.row_groups = pl.row_groups;
+    p.chunk_tokens = pl.chunk_tokens;
+    p.max_splits = pl.max_splits;
+    p.num_units = pl.num_units;
+    p.block_table = static_cast<const int32_t *>(block_table->data);
+    p.bt_stride = block_table->stride[0];
+    p.seq_lens = static_cast<const int32_t *>(seq_lens->data);
+    p.out = out->data;
+    for (int i = 0; i < 4; ++i) p.out_stride[i] = out->stride[i];
+    p.lse = lse ? static_cast<float *>(lse->data) : nullptr;
+    if (lse) for (int i = 0; i < 3; ++i) p.lse_stride[i] = lse->stride[i];
+    const int64_t rows = B * q_len * Hq;
+    p.ws_o = static_cast<float *>(ws);
+    p.ws_lse = ws ? reinterpret_cast<float *>(static_cast<char *>(ws) +
+                                              ((rows * pl.max_splits * Dv * 4 + 255) / 256) * 256)
+                  : nullptr;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.timeout_ns = (uint64_t)g_opt_timeout_ms * 1000000ull;
+    p.status = d->status;
+
+    CUtensorMap tq, tk, tv;
+    {
+        const uint32_t box_h = p.head_mode == 0 ? (uint32_t)pl.group : 32u;
+        const uint32_t box_t = p.head_mode == 0 ? (uint32_t)pl.tokens_per_unit : 1u;
+        const uint64_t dims[4] = {(uint64_t)Dk, (uint64_t)Hq, (uint64_t)q_len, (uint64_t)B};
+        const uint64_t strides[3] = {(uint64_t)q->stride[2] * 2, (uint64_t)q->stride[1] * 2, (uint64_t)q->stride[0] * 2};
+        const uint32_t box[4] = {64, box_h, box_t, 1};
+        if (fw_status_t s = encode_bf16(&tq, q->data, 4, dims, strides, box, "q")) return s;
+    }
+    {
+        const uint32_t rows_box = (uint32_t)(ps < fw::kKvTile ? ps : fw::kKvTile);
+        const uint64_t dk[4] = {(uint64_t)Dk, (uint64_t)Hkv, (uint64_t)ps, (uint64_t)P};
+        const uint64_t sk[3] = {(uint64_t)k_cache->stride[2] * 2, (uint64_t)k_cache->stride[1] * 2,
+                                (uint64_t)k_cache->stride[0] * 2};
+        const uint32_t box[4] = {64, 1, rows_box, 1};
+        if (fw_status_t s = encode_bf16(&tk, k_cache->data, 4, dk, sk, box, "k_cache")) return s;
+        const uint64_t dv[4] = {(uint64_t)Dv, (uint64_t)Hkv, (uint64_t)ps, (uint64_t)P};
+        const uint64_t sv[3] = {(uint64_t)v_cache->stride[2] * 2, (uint64_t)v_cache->stride[1] * 2,
+                                (uint64_t)v_cache->stride[0] * 2};
+        if (fw_status_t s = encode_bf16(&tv, v_cache->data, 4, dv, sv, box, "v_cache")) return s;
+    }
+    cudaEvent_t ev = nullptr;
+    timing_begin(stream, &ev);
+    cudaError_t e = fw::launch_decode(p, tq, tk, tv, (int)Dk, pl.grid, stream);
+    if (e != cudaSuccess) return fail(FW_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+    timing_end(stream, ev);
+    g_launches.fetch_add(1);
+    if (pl.max_splits > 1) {
+        fw::CombineParams c{};
+        c.B = (int)B; c.q_len = (int)q_len; c.Hq = (int)Hq; c.Dv = (int)Dv;
+        c.chunk_tokens = pl.chunk_tokens; c.max_splits = pl.max_splits;
+        c.seq_lens = p.seq_lens; c.ws_o = p.ws_o; c.ws_lse = p.ws_lse;
+        c.out = out->data;
+        for (int i = 0; i < 4; ++i) c.out_stride[i] = out->stride[i];
+        c.lse = p.lse;
+        if (lse) for (int i = 0; i < 3; ++i) c.lse_stride[i] = lse->stride[i];
+        c.max_kv_len = (int)(max_pages * ps);
+        e = fw::launch_combine(c, stream);
+        if (e != cudaSuccess) return fail(FW_ERR_CUDA, "combine launch: %s", cudaGetErrorString(e));
+        g_launches.fetch_add(1);
+    }
+    return ok();
+}
+
+fw_status_t fw_varlen_prefill(const fw_tensor_t *q, const fw_tensor_t *k, const fw_tensor_t *v,
+                              const fw_tensor_t *cu_seqlens_q, const fw_tensor_t *cu_seqlens_k, int causal,
+                              float scale, fw_tensor_t *out, fw_tensor_t *lse, fw_stream_t stream) {
+    (void)q; (void)k; (void)v; (void)cu_seqlens_q; (void)cu_seqlens_k; (void)causal; (void)scale;
+    (void)out; (void)lse; (void)stream;
+    return fail(FW_ERR_UNSUPPORTED, "varlen prefill is not built yet");
+}
+
+}  // extern "C"

@@ -1,0 +1,626 @@
+// Paged grouped-query decode, sm_103a.
+//
+// The work unit is (batch row b, KV head g, row group, KV split): the query
+// rows a unit holds are the (token, head) pairs of the query heads that share
+// KV head g ("Writing Page Attention with PyPTO", section 1.3: one task = one
+// batch row + one KV head + its five query heads; "TokenSpeed-MLA 2.0.1":
+// query tokens folded next to the heads), and its keys are one chunk of the
+// row's paged KV range (split-KV, merged afterwards by the combine kernel).
+//
+// Orientation.  A decode unit has few query rows (5 at 40 Q / 8 KV heads), so
+// the KV tile takes the 128-wide MMA M axis and the padded query rows take N:
+//   S^T [128 keys x NQ]  = K_tile [128 x D]  * Q^T            (tcgen05, TMEM)
+//   O^T [D x NQ]        += V_tile^T [D x 128] * P^T [128 x NQ] (tcgen05, TMEM)
+// Every softmax thread then owns one key of the tile and holds that key's
+// score for every query row, so exp2 work spreads over 128 threads.
+//
+// Warp roles (192 threads, one CTA per SM, persistent over units):
+//   warp 0     TMA producer: walks block_table[b, logical_page] and loads the
+//              K and V pages of each 128-key tile into separate smem rings
+//              (PyPTO section 5.2 page lookup; "TokenSpeed-MLA 2.0.1": K and V
+//              loads do not wait on each other), plus the unit's Q rows.
+//   warp 1     MMA issuer (one thread) and TMEM owner.
+//   warps 2-5  online softmax in base 2 with a conditional rescale (the base
+//              moves only when a row's max rises by more than 8 log2 units,
+//              "TokenSpeed-MLA 2.0.1", softmax precision paragraph), P^T to
+//              smem, O^T correction in TMEM when the base moves, epilogue.
+// Handoffs are mbarriers: k_full/k_empty, v_full/v_empty, q_full/q_empty,
+// s_full/s_free, p_full/p_free, pv_done -- the READY events of PyPTO
+// section 8.3 with the double-buffered S and P slots playing its ring.
+#include <cuda_bf16.h>
+
+#include "fw_internal.h"
+#include "fw_ptx.cuh"
+
+namespace fw {
+
+namespace {
+
+constexpr float kNegInf = -__builtin_huge_valf();
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
+
+template <int D, int NQ>
+struct DecodeCfg {
+    static constexpr int kChunks = D / 64;                 // 128-byte swizzle column blocks
+    static constexpr int kChunkBytes = kKvTile * 128;       // one 64-column block of a tile
+    static constexpr int kTileBytes = kKvTile * D * 2;
+    static constexpr int kKStages = (D == 128) ? 3 : (NQ == 16 ? 2 : 1);
+    static constexpr int kVStages = (D == 128) ? 3 : 1;
+    static constexpr int kQBytes = NQ * D * 2;
+    static constexpr int kPBytes = NQ * kKvTile * 2;
+    static constexpr int kDvTiles = D / 128;
+    static constexpr int kTmemNeed = (2 + kDvTiles) * NQ;
+    static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128 : 256;
+    // shared memory map (offsets from a 1024-aligned base)
+    static constexpr int kOffK = 0;
+    static constexpr int kOffV = kOffK + kKStages * kTileBytes;
+    static constexpr int kOffQ = kOffV + kVStages * kTileBytes;
+    static constexpr int kOffP = kOffQ + 2 * kQBytes;
+    static constexpr int kOffBar = kOffP + 2 * kPBytes;
+    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + 2 + 2 + 2 + 1 + 1;
+    static constexpr int kOffRedMax = kOffBar + kNumBars * 8;
+    static constexpr int kOffRedSum = kOffRedMax + 2 * 4 * NQ * 4;
+    static constexpr int kOffMisc = kOffRedSum + 4 * NQ * 4;
+    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
+    static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA exceeded");
+    static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, NQ, false, false);
+    static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, NQ, true, false);
+};
+
+struct Unit {
+    int b, g, rg, s, n, k_begin, k_end, ntiles;
+    bool single;
+};
+
+__device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
+
+__device__ __forceinline__ bool fetch_unit(const DecodeParams &p, int64_t u, Unit &x) {
+    x.rg = (int)(u % p.row_groups);
+    int64_t t = u / p.row_groups;
+    x.g = (int)(t % p.Hkv);
+    t /= p.Hkv;
+    x.b = (int)(t % p.B);
+    x.s = (int)(t / p.B);
+    int n = __ldg(p.seq_lens + x.b);
+    const int cap = p.max_pages * p.ps;
+    n = n < 0 ? 0 : (n > cap ? cap : n);
+    x.n = n;
+    const int nsplit = n > 0 ? ceil_div_i(n, p.chunk_tokens) : 1;
+    if (x.s >= nsplit) return false;
+    x.single = (nsplit == 1);
+    x.k_begin = x.s * p.chunk_tokens;
+    x.k_end = min(n, x.k_begin + p.chunk_tokens);
+    x.ntiles = n > 0 ? ceil_div_i(x.k_end - x.k_begin, kKvTile) : 0;
+    return true;
+}
+
+// Query row r of unit x -> (token t, head h); false if the row is padding.
+__device__ __forceinline__ bool unit_row(const DecodeParams &p, const Unit &x, int r, int &t, int &h) {
+    if (p.head_mode == 0) {
+        const int tt = r / p.G;
+        t = x.rg * p.tokens_per_unit + tt;
+        h = x.g * p.G + (r - tt * p.G);
+        return tt < p.tokens_per_unit && t < p.q_len;
+    }
+    t = x.rg / p.head_chunks;
+    const int hh = (x.rg % p.head_chunks) * p.rows + r;
+    h = x.g * p.G + hh;
+    return hh < p.G;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// One lane waits, the whole warp learns the outcome (keeps the warp converged).
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const WaitCtx &w, int lane) {
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(bar, parity, w) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+template <int D, int NQ>
+__global__ void __launch_bounds__(192, 1)
+paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
+    using C = DecodeCfg<D, NQ>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sK = smem + C::kOffK;
+    uint8_t *sV = smem + C::kOffV;
+    uint8_t *sQ = smem + C::kOffQ;
+    uint8_t *sP = smem + C::kOffP;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
+    uint64_t *k_full = bars;
+    uint64_t *k_empty = k_full + C::kKStages;
+    uint64_t *v_full = k_empty + C::kKStages;
+    uint64_t *v_empty = v_full + C::kVStages;
+    uint64_t *q_full = v_empty + C::kVStages;
+    uint64_t *q_empty = q_full + 2;
+    uint64_t *s_full = q_empty + 2;
+    uint64_t *s_free = s_full + 2;
+    uint64_t *p_full = s_free + 2;
+    uint64_t *p_free = p_full + 2;
+    uint64_t *pv_done = p_free + 2;
+    uint64_t *drain = pv_done + 1;
+    float *red_max = reinterpret_cast<float *>(smem + C::kOffRedMax);   // [2][4][NQ]
+    float *red_sum = reinterpret_cast<float *>(smem + C::kOffRedSum);   // [4][NQ]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::kKStages; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 1); }
+        for (int i = 0; i < C::kVStages; ++i) { mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], 1); }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1);
+            mbar_init(&s_full[i], 1); mbar_init(&s_free[i], 4);
+            mbar_init(&p_full[i], 4); mbar_init(&p_free[i], 1);
+        }
+        mbar_init(pv_done, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_q); tma_prefetch_desc(&tm_k); tma_prefetch_desc(&tm_v);
+    }
+    if (warp == 1) { tmem_alloc(tmem_slot, C::kTmemCols); tmem_relinquish(); }
+    // Zero the Q and P slots once: padding rows then contribute exact zeros.
+    for (int i = threadIdx.x; i < (2 * C::kQBytes + 2 * C::kPBytes) / 16; i += blockDim.x)
+        reinterpret_cast<uint4 *>(sQ)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtx wc{p.status, p.timeout_ns, abort_flag};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        int jt = 0, ju = 0, issued_k = 0, issued_v = 0;
+        const int box_rows = p.ps < kKvTile ? p.ps : kKvTile;
+        const int pages_per_tile = p.ps < kKvTile ? kKvTile / p.ps : 1;
+        const uint32_t q_rows = p.head_mode == 0 ? (uint32_t)(p.G * p.tokens_per_unit) : (uint32_t)p.rows;
+        for (int64_t u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+            Unit x;
+            if (!fetch_unit(p, u, x) || x.ntiles == 0) continue;
+            const int qs = ju & 1;
+            if (!warp_wait(&q_empty[qs], ((ju >> 1) & 1) ^ 1, wc, lane)) goto producer_done;
+            if (lane == 0) {
+                int h0, t0;
+                if (p.head_mode == 0) { h0 = x.g * p.G; t0 = x.rg * p.tokens_per_unit; }
+                else { t0 = x.rg / p.head_chunks; h0 = x.g * p.G + (x.rg % p.head_chunks) * p.rows; }
+                mbar_arrive_expect_tx(&q_full[qs], C::kChunks * q_rows * 128u);
+#pragma unroll
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_4d(smem_u32(sQ + qs * C::kQBytes + c * NQ * 128), &tm_q, &q_full[qs],
+                                c * 64, h0, t0, x.b);
+            }
+            __syncwarp();
+            for (int i = 0; i < x.ntiles; ++i, ++jt) {
+                const int ts = x.k_begin + i * kKvTile;
+                const int first_lp = ts / p.ps;
+                const int slot0 = p.ps < kKvTile ? 0 : ts % p.ps;
+                int npages = 1;
+                if (p.ps < kKvTile) npages = min(pages_per_tile, ceil_div_i(x.k_end - ts, p.ps));
+                int phys = 0;
+                if (lane < npages) {
+                    phys = __ldg(p.block_table + (int64_t)x.b * p.bt_stride + first_lp + lane);
+                    if ((unsigned)phys >= (unsigned)p.num_pages) { record_error(p.status, 1); phys = 0; }
+                }
+                const uint32_t bytes = (uint32_t)(npages * box_rows * 128 * C::kChunks);
+                const int ks = jt % C::kKStages;
+                if (!warp_wait(&k_empty[ks], ((jt / C::kKStages) & 1) ^ 1, wc, lane)) goto producer_done;
+                if (lane == 0) mbar_arrive_expect_tx(&k_full[ks], bytes);
+                __syncwarp();
+                if (lane < npages) {
+#pragma unroll
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_4d(smem_u32(sK + ks * C::kTileBytes + c * C::kChunkBytes + lane * box_rows * 128),
+                                    &tm_k, &k_full[ks], c * 64, x.g, slot0, phys);
+                }
+                issued_k = jt + 1;
+                const int vs = jt % C::kVStages;
+                if (!warp_wait(&v_empty[vs], ((jt / C::kVStages) & 1) ^ 1, wc, lane)) goto producer_done;
+                if (lane == 0) mbar_arrive_expect_tx(&v_full[vs], bytes);
+                __syncwarp();
+                if (lane < npages) {
+#pragma unroll
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_4d(smem_u32(sV + vs * C::kTileBytes + c * C::kChunkBytes + lane * box_rows * 128),
+                                    &tm_v, &v_full[vs], c * 64, x.g, slot0, phys);
+                }
+                issued_v = jt + 1;
+            }
+            ++ju;
+        }
+    producer_done:
+        // Do not leave the CTA while copies it issued may still land.
+        if (lane == 0) {
+            for (int k = 0; k < C::kKStages && k < issued_k; ++k) {
+                const int j = issued_k - 1 - k;
+                mbar_wait_drain(&k_full[j % C::kKStages], (j / C::kKStages) & 1, wc);
+            }
+            for (int k = 0; k < C::kVStages && k < issued_v; ++k) {
+                const int j = issued_v - 1 - k;
+                mbar_wait_drain(&v_full[j % C::kVStages], (j / C::kVStages) & 1, wc);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ----------------------------------------------------------------- MMA
+        if (lane == 0) {
+            int jt = 0, ju = 0, pend = -1;
+            bool pend_first = false;
+            auto issue_pv = [&](int jj, bool first) -> bool {
+                const int vs = jj % C::kVStages;
+                const int pb = jj & 1;
+                if (!mbar_wait(&v_full[vs], (jj / C::kVStages) & 1, wc)) return false;
+                if (!mbar_wait(&p_full[pb], (jj >> 1) & 1, wc)) return false;
+                tc_fence_after();
+                const uint32_t v_base = smem_u32(sV + vs * C::kTileBytes);
+                const uint32_t p_base = smem_u32(sP + pb * C::kPBytes);
+#pragma unroll
+                for (int dvt = 0; dvt < C::kDvTiles; ++dvt) {
+#pragma unroll
+                    for (int kk = 0; kk < kKvTile / 16; ++kk) {
+                        const uint64_t a = sdesc_sw128(v_base + (2 * dvt) * C::kChunkBytes + kk * 16 * 128,
+                                                       C::kChunkBytes, 1024);
+                        const uint64_t b = sdesc_sw128(p_base + (kk >> 2) * NQ * 128 + (kk & 3) * 32, 16, 1024);
+                        mma_bf16_ss(tmem + 2 * NQ + dvt * NQ, a, b, C::kIdescPV, (first && kk == 0) ? 0u : 1u);
+                    }
+                }
+                mma_commit(&v_empty[vs]);
+                mma_commit(&p_free[pb]);
+                mma_commit(pv_done);
+                return true;
+            };
+            for (int64_t u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+                Unit x;
+                if (!fetch_unit(p, u, x) || x.ntiles == 0) continue;
+                const int qs = ju & 1;
+                if (!mbar_wait(&q_full[qs], (ju >> 1) & 1, wc)) goto mma_done;
+                for (int i = 0; i < x.ntiles; ++i, ++jt) {
+                    const int ks = jt % C::kKStages;
+                    const int sb = jt & 1;
+                    if (!mbar_wait(&k_full[ks], (jt / C::kKStages) & 1, wc)) goto mma_done;
+                    if (!mbar_wait(&s_free[sb], ((jt >> 1) & 1) ^ 1, wc)) goto mma_done;
+                    tc_fence_after();
+                    const uint32_t k_base = smem_u32(sK + ks * C::kTileBytes);
+                    const uint32_t q_base = smem_u32(sQ + qs * C::kQBytes);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t a = sdesc_sw128(k_base + (kk >> 2) * C::kChunkBytes + (kk & 3) * 32, 16, 1024);
+                        const uint64_t b = sdesc_sw128(q_base + (kk >> 2) * NQ * 128 + (kk & 3) * 32, 16, 1024);
+                        mma_bf16_ss(tmem + sb * NQ, a, b, C::kIdescQK, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&k_empty[ks]);
+                    mma_commit(&s_full[sb]);
+                    if (i == x.ntiles - 1) mma_commit(&q_empty[qs]);
+                    if (pend >= 0 && !issue_pv(pend, pend_first)) goto mma_done;
+                    pend = jt;
+                    pend_first = (i == 0);
+                }
+                ++ju;
+            }
+            if (pend >= 0) issue_pv(pend, pend_first);
+        mma_done:
+            mma_commit(drain);
+            mbar_wait_drain(drain, 0, wc);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------- softmax / epilogue
+        // These 128 threads meet at named barriers, which cannot time out, so
+        // a failed wait does not leave the loop: after an abort every wait
+        // returns at once and the warps run through their remaining (bounded)
+        // iterations in lockstep, producing garbage that the recorded status
+        // word disowns.
+        const int q4 = warp & 3;                       // TMEM lane quadrant of this warp
+        const int row_in_tile = q4 * 32 + lane;        // key of the tile / dv lane this thread owns
+        const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+        int jt = 0;
+        for (int64_t u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+            Unit x;
+            if (!fetch_unit(p, u, x)) continue;
+            int lim[NQ];
+            int nrows = 0;
+#pragma unroll
+            for (int r = 0; r < NQ; ++r) {
+                int t, h;
+                const bool ok = unit_row(p, x, r, t, h);
+                lim[r] = ok ? min(x.n, x.n - p.q_len + t + 1) : 0;
+                if (ok) nrows = r + 1;
+            }
+            if (x.ntiles == 0) {
+                // No keys at all: zero output rows and -inf LSE.
+#pragma unroll
+                for (int r = 0; r < NQ; ++r) {
+                    int t, h;
+                    if (!unit_row(p, x, r, t, h)) continue;
+                    __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(p.out) + x.b * p.out_stride[0] +
+                                       t * p.out_stride[1] + h * p.out_stride[2];
+                    for (int dv = row_in_tile; dv < D; dv += 128) o[dv] = __float2bfloat16(0.f);
+                    if (row_in_tile == 0 && p.lse)
+                        p.lse[x.b * p.lse_stride[0] + t * p.lse_stride[1] + h * p.lse_stride[2]] = kNegInf;
+                }
+                continue;
+            }
+            float m_ref[NQ], l_part[NQ];
+#pragma unroll
+            for (int r = 0; r < NQ; ++r) { m_ref[r] = kNegInf; l_part[r] = 0.f; }
+            for (int i = 0; i < x.ntiles; ++i, ++jt) {
+                const int ts = x.k_begin + i * kKvTile;
+                const int tok = ts + row_in_tile;
+                const int sb = jt & 1;
+                mbar_wait(&s_full[sb], (jt >> 1) & 1, wc);
+                tc_fence_after();
+                float s[NQ];
+#pragma unroll
+                for (int c = 0; c < NQ; c += 16)
+                    tmem_ld16(tmem + lane_off + sb * NQ + c, *reinterpret_cast<float(*)[16]>(&s[c]));
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_free[sb]);
+                float* rm = red_max + (jt & 1) * 4 * NQ;
+#pragma unroll
+                for (int r = 0; r < NQ; ++r) {
+                    s[r] = (tok < lim[r]) ? s[r] * p.scale_log2 : kNegInf;
+                    if (r < nrows) {
+                        const float v = warp_max(s[r]);
+                        if (lane == 0) rm[q4 * NQ + r] = v;
+                    }
+                }
+                named_bar_sync(1, 128);
+                bool need = false;
+                float mx[NQ];
+#pragma unroll
+                for (int r = 0; r < NQ; ++r) {
+                    mx[r] = kNegInf;
+                    if (r < nrows)
+                        mx[r] = fmaxf(fmaxf(rm[r], rm[NQ + r]), fmaxf(rm[2 * NQ + r], rm[3 * NQ + r]));
+                    need |= mx[r] > m_ref[r] + kRescaleThreshold;
+                }
+                if (need) {
+                    float alpha[NQ];
+#pragma unroll
+                    for (int r = 0; r < NQ; ++r) {
+                        const float mn = fmaxf(m_ref[r], mx[r]);
+                        alpha[r] = (mn == kNegInf) ? 1.f : ex2_approx(m_ref[r] - mn);
+                        l_part[r] *= alpha[r];
+                        m_ref[r] = mn;
+                    }
+                    if (i > 0) {
+                        // Rescale the accumulated O^T once the previous PV has landed.
+                        mbar_wait(pv_done, (jt - 1) & 1, wc);
+                        tc_fence_after();
+#pragma unroll
+                        for (int dvt = 0; dvt < C::kDvTiles; ++dvt) {
+#pragma unroll
+                            for (int c = 0; c < NQ; c += 16) {
+                                float o[16];
+                                const uint32_t ta = tmem + lane_off + 2 * NQ + dvt * NQ + c;
+                                tmem_ld16(ta, o);
+                                tmem_wait_ld();
+#pragma unroll
+                                for (int k = 0; k < 16; ++k) o[k] *= alpha[c + k];
+                                tmem_st16(ta, o);
+                            }
+                        }
+                        tmem_wait_st();
+                    }
+                }
+                if (ts + kKvTile > x.n) {
+                    // Keys past the row's end: their V rows may hold anything
+                    // (unloaded pages, poisoned slots).  Zero them so that the
+                    // exact-zero probabilities cannot meet a NaN in the MMA.
+                    const int vs = jt % C::kVStages;
+                    mbar_wait(&v_full[vs], (jt / C::kVStages) & 1, wc);
+                    if (tok >= x.n) {
+#pragma unroll
+                        for (int c = 0; c < C::kChunks; ++c) {
+                            uint4 *row = reinterpret_cast<uint4 *>(sV + vs * C::kTileBytes + c * C::kChunkBytes +
+                                                                   row_in_tile * 128);
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) row[k] = make_uint4(0, 0, 0, 0);
+                        }
+                    }
+                }
+                const int pb = jt & 1;
+                mbar_wait(&p_free[pb], ((jt >> 1) & 1) ^ 1, wc);
+                uint8_t *pbuf = sP + pb * C::kPBytes;
+#pragma unroll
+                for (int r = 0; r < NQ; ++r) {
+                    float pr = 0.f;
+                    if (r < nrows) {
+                        const float mu = (m_ref[r] == kNegInf) ? 0.f : m_ref[r];
+                        pr = ex2_approx(s[r] - mu);
+                        l_part[r] += pr;
+                    }
+                    *reinterpret_cast<__nv_bfloat16 *>(pbuf + sw128_offset(r, row_in_tile, NQ)) = __float2bfloat16_rn(pr);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[pb]);
+            }
+            // ------------------------------------------------------ epilogue
+            {
+#pragma unroll
+                for (int r = 0; r < NQ; ++r) {
+                    if (r < nrows) {
+                        const float v = warp_sum(l_part[r]);
+                        if (lane == 0) red_sum[q4 * NQ + r] = v;
+                    }
+                }
+                named_bar_sync(1, 128);
+                float L[NQ];
+#pragma unroll
+                for (int r = 0; r < NQ; ++r)
+                    L[r] = (r < nrows) ? (red_sum[r] + red_sum[NQ + r]) + (red_sum[2 * NQ + r] + red_sum[3 * NQ + r]) : 0.f;
+                mbar_wait(pv_done, (jt - 1) & 1, wc);
+                tc_fence_after();
+#pragma unroll
+                for (int dvt = 0; dvt < C::kDvTiles; ++dvt) {
+                    float o[NQ];
+#pragma unroll
+                    for (int c = 0; c < NQ; c += 16)
+                        tmem_ld16(tmem + lane_off + 2 * NQ + dvt * NQ + c, *reinterpret_cast<float(*)[16]>(&o[c]));
+                    tmem_wait_ld();
+                    const int dv = dvt * 128 + row_in_tile;
+#pragma unroll
+                    for (int r = 0; r < NQ; ++r) {
+                        int t, h;
+                        if (r >= nrows || !unit_row(p, x, r, t, h)) continue;
+                        const float val = L[r] > 0.f ? o[r] / L[r] : 0.f;
+                        if (x.single) {
+                            __nv_bfloat16 *op = reinterpret_cast<__nv_bfloat16 *>(p.out) + x.b * p.out_stride[0] +
+                                                t * p.out_stride[1] + h * p.out_stride[2];
+                            op[dv] = __float2bfloat16_rn(val);
+                        } else {
+                            const int64_t row = ((int64_t)x.b * p.q_len + t) * p.Hq + h;
+                            p.ws_o[(row * p.max_splits + x.s) * D + dv] = val;
+                        }
+                    }
+                }
+                if (row_in_tile < nrows) {
+                    const int r = row_in_tile;
+                    int t, h;
+                    if (unit_row(p, x, r, t, h)) {
+                        float lse2 = kNegInf;
+#pragma unroll
+                        for (int k = 0; k < NQ; ++k)
+                            if (k == r && L[k] > 0.f) lse2 = m_ref[k] + __log2f(L[k]);
+                        if (x.single) {
+                            if (p.lse)
+                                p.lse[x.b * p.lse_stride[0] + t * p.lse_stride[1] + h * p.lse_stride[2]] =
+                                    lse2 * 0.69314718055994531f;
+                        } else {
+                            const int64_t row = ((int64_t)x.b * p.q_len + t) * p.Hq + h;
+                            p.ws_lse[row * p.max_splits + x.s] = lse2;
+                        }
+                    }
+                }
+                tc_fence_before();
+                named_bar_sync(1, 128);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+template <int D, int NQ>
+cudaError_t launch_t(const DecodeParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                     const CUtensorMap &tv, int grid, cudaStream_t stream) {
+    using C = DecodeCfg<D, NQ>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<D, NQ>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    paged_decode_kernel<D, NQ><<<grid, 192, C::kSmemBytes, stream>>>(p, tq, tk, tv);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t decode_smem_bytes(int head_dim, int rows) {
+    if (head_dim == 128) return rows == 16 ? DecodeCfg<128, 16>::kSmemBytes : DecodeCfg<128, 32>::kSmemBytes;
+    return rows == 16 ? DecodeCfg<256, 16>::kSmemBytes : DecodeCfg<256, 32>::kSmemBytes;
+}
+
+cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                          const CUtensorMap &tv, int head_dim, int grid, cudaStream_t stream) {
+    if (head_dim == 128 && p.rows == 16) return launch_t<128, 16>(p, tq, tk, tv, grid, stream);
+    if (head_dim == 128 && p.rows == 32) return launch_t<128, 32>(p, tq, tk, tv, grid, stream);
+    if (head_dim == 256 && p.rows == 16) return launch_t<256, 16>(p, tq, tk, tv, grid, stream);
+    if (head_dim == 256 && p.rows == 32) return launch_t<256, 32>(p, tq, tk, tv, grid, stream);
+    return cudaErrorInvalidValue;
+}
+
+// ------------------------------------------------------------------ combine
+//
+// Merge the split-KV partials of each query row: with per-split normalised
+// outputs o_i and log2-sum-exp values e_i, L = log2 sum_i 2^{e_i} and
+// out = sum_i 2^{e_i - L} o_i.  This is the rescale of the online recurrence
+// applied across whole splits ("Flywheel Attention", section 1; the reduction
+// kernel of "TokenSpeed-MLA 2.0.1", decode).  One warp per row, float4 loads.
+
+template <int D>
+__global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ CombineParams p) {
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = (int64_t)p.B * p.q_len * p.Hq;
+    const int64_t row = (int64_t)blockIdx.x * 4 + warp;
+    if (row >= rows) return;
+    const int h = (int)(row % p.Hq);
+    const int t = (int)((row / p.Hq) % p.q_len);
+    const int b = (int)(row / ((int64_t)p.Hq * p.q_len));
+    int n = __ldg(p.seq_lens + b);
+    n = n < 0 ? 0 : (n > p.max_kv_len ? p.max_kv_len : n);
+    const int nsplit = n > 0 ? (n + p.chunk_tokens - 1) / p.chunk_tokens : 1;
+    if (nsplit <= 1) return;                         // written directly by the attention kernel
+    const float *lse_row = p.ws_lse + row * p.max_splits;
+    float m = kNegInf;
+    for (int i = lane; i < nsplit; i += 32) m = fmaxf(m, lse_row[i]);
+    m = warp_max(m);
+    constexpr int V = D / 32;                        // floats per lane
+    float acc[V];
+#pragma unroll
+    for (int k = 0; k < V; ++k) acc[k] = 0.f;
+    float wsum = 0.f;
+    if (m != kNegInf) {
+        for (int i = 0; i < nsplit; ++i) {
+            const float e = lse_row[i];
+            const float w = ex2_approx(e - m);       // 0 for an empty split (e = -inf)
+            wsum += w;
+            const float4 *src = reinterpret_cast<const float4 *>(p.ws_o + (row * p.max_splits + i) * D) + lane * (V / 4);
+#pragma unroll
+            for (int k = 0; k < V / 4; ++k) {
+                const float4 v = src[k];
+                acc[4 * k + 0] += w * v.x; acc[4 * k + 1] += w * v.y;
+                acc[4 * k + 2] += w * v.z; acc[4 * k + 3] += w * v.w;
+            }
+        }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(p.out) + b * p.out_stride[0] + t * p.out_stride[1] +
+                       h * p.out_stride[2] + lane * V;
+#pragma unroll
+    for (int k = 0; k < V; k += 2) {
+        __nv_bfloat162 v2 = __floats2bfloat162_rn(acc[k] * inv, acc[k + 1] * inv);
+        *reinterpret_cast<__nv_bfloat162 *>(o + k) = v2;
+    }
+    if (lane == 0 && p.lse)
+        p.lse[b * p.lse_stride[0] + t * p.lse_stride[1] + h * p.lse_stride[2]] =
+            (m == kNegInf) ? kNegInf : (m + __log2f(wsum)) * 0.69314718055994531f;
+}
+
+cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream) {
+    const int64_t rows = (int64_t)p.B * p.q_len * p.Hq;
+    const unsigned grid = (unsigned)((rows + 3) / 4);
+    if (grid == 0) return cudaSuccess;
+    if (p.Dv == 128) combine_kernel<128><<<grid, 128, 0, stream>>>(p);
+    else if (p.Dv == 256) combine_kernel<256><<<grid, 128, 0, stream>>>(p);
+    else return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+}  // namespace fw

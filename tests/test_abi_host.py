@@ -1,0 +1,190 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+  * libfw_attn.so builds, loads and exports every function include/*.h declares;
+  * the decode planner's folding, split sizing and workspace size agree with
+    the pages' formulas as restated independently in oracle/planning.py;
+  * invalid arguments are rejected with the documented status before any
+    CUDA call, and a valid call without a usable GPU fails loudly.
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from oracle import planning
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def fwlib():
+    from ragged_softmax_attention_gb300 import build
+    import ragged_softmax_attention_gb300 as fw
+    path = build.build()
+    fw.load_library(path)
+    return fw
+
+
+def declared_functions():
+    names = set()
+    for hdr in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(hdr).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b(fw_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("fw_paged_decode", "fw_varlen_prefill", "fw_paged_decode_workspace_size",
+                     "fw_set_workspace", "fw_get_device_status", "fw_last_error"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(fwlib):
+    lib = ctypes.CDLL(fwlib._binding.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"declared but not exported: {missing}"
+
+
+def test_missing_library_fails_loudly():
+    from ragged_softmax_attention_gb300 import _binding
+    saved = _binding._lib
+    _binding._lib = None
+    try:
+        with pytest.raises(RuntimeError, match="not built"):
+            _binding.load_library("/nonexistent/libfw_attn.so")
+    finally:
+        _binding._lib = saved
+
+
+@pytest.mark.parametrize("G,q_len", [(5, 1), (4, 1), (8, 4), (5, 4), (16, 4), (12, 4), (32, 2), (3, 3), (1, 4)])
+def test_planner_folds_like_tokenspeed_rule(fwlib, G, q_len):
+    p = fwlib.plan_decode(2, q_len, G * 2, 2, 128, 4096, num_sms=152)
+    F = planning.fold_factor(G, q_len, max_rows=32)
+    assert p["tokens_per_unit"] == F
+    assert p["row_groups"] == q_len // F
+    assert p["rows_per_unit"] == (16 if G * F <= 16 else 32)
+
+
+def test_planner_wide_groups_are_chunked(fwlib):
+    p = fwlib.plan_decode(2, 4, 128, 1, 512, 81920, num_sms=152)
+    assert p["heads_per_unit"] == 32 and p["row_groups"] == 4 * 4
+
+
+def test_planner_workspace_matches_pages_formula(fwlib):
+    """Dv + 1 FP32 values per row per split: at H*q_len a multiple of 128 this is
+    exactly TokenSpeed's B*128*ceil(H*q_len/128)*split*513*4 bytes (+256 alignment)."""
+    p = fwlib.plan_decode(2, 4, 128, 1, 512, 81920, num_sms=152)
+    assert p["max_splits"] > 1
+    assert p["workspace_bytes"] == planning.split_workspace_bytes(2, 128, 4, p["max_splits"], 512) + 256
+    p1 = fwlib.plan_decode(2, 1, 8, 2, 128, 200, num_sms=152)
+    assert p1["max_splits"] == 1 and p1["workspace_bytes"] == 0
+
+
+def test_planner_splits_cover_the_length_bound(fwlib):
+    for max_len in (1, 127, 128, 129, 4096, 32768, 81920):
+        p = fwlib.plan_decode(64, 1, 40, 8, 128, max_len, num_sms=152)
+        assert p["chunk_tokens"] % 128 == 0 and p["chunk_tokens"] >= 128
+        assert p["max_splits"] == -(-max_len // p["chunk_tokens"])
+        assert p["num_units"] == 64 * 8 * p["row_groups"] * p["max_splits"]
+        assert 1 <= p["grid"] <= 152
+
+
+def test_qwen3_14b_plan(fwlib):
+    """40 Q / 8 KV heads, q_len 1: one unit holds the five query heads of a KV
+    head (PyPTO section 1.3), padded to a 16-row MMA N extent."""
+    p = fwlib.plan_decode(64, 1, 40, 8, 128, 32768, num_sms=152)
+    assert p["group"] == 5 and p["heads_per_unit"] == 5 and p["rows_per_unit"] == 16
+    assert p["row_groups"] == 1
+
+
+def test_forced_chunk_option(fwlib):
+    fwlib.set_option(fwlib.FW_OPT_DECODE_CHUNK_TOKENS, 256)
+    try:
+        p = fwlib.plan_decode(2, 1, 8, 2, 128, 1000, num_sms=152)
+        assert p["chunk_tokens"] == 256 and p["max_splits"] == 4
+    finally:
+        fwlib.set_option(fwlib.FW_OPT_DECODE_CHUNK_TOKENS, 0)
+    with pytest.raises(fwlib.FwError):
+        fwlib.set_option(fwlib.FW_OPT_DECODE_CHUNK_TOKENS, 100)
+
+
+# ------------------------------------------------------- validation, no GPU
+
+def fake(shape, dtype, ptr=0x10000, strides=None):
+    from ragged_softmax_attention_gb300._binding import FwTensor
+    t = FwTensor()
+    t.data = ptr
+    t.dtype = dtype
+    t.ndim = len(shape)
+    if strides is None:
+        strides = []
+        acc = 1
+        for s in reversed(shape):
+            strides.insert(0, acc)
+            acc *= s
+    for i, (s, st) in enumerate(zip(shape, strides)):
+        t.shape[i] = s
+        t.stride[i] = st
+    return t
+
+
+def call_decode(fwlib, q, k, v, bt, sl, out, lse=None, scale=0.1):
+    lib = fwlib.load_library()
+    r = lambda x: ctypes.byref(x) if x is not None else None
+    return lib.fw_paged_decode(r(q), r(k), r(v), r(bt), r(sl), ctypes.c_float(scale), r(out), r(lse), None)
+
+
+def decode_args(B=2, q_len=1, Hq=8, Hkv=2, D=128, P=10, ps=16, max_pages=4):
+    BF, F32, I32 = 0, 1, 2
+    return dict(q=fake([B, q_len, Hq, D], BF), k=fake([P, ps, Hkv, D], BF), v=fake([P, ps, Hkv, D], BF),
+                bt=fake([B, max_pages], I32), sl=fake([B], I32), out=fake([B, q_len, Hq, D], BF),
+                lse=fake([B, q_len, Hq], F32))
+
+
+@pytest.mark.parametrize("mutate,status", [
+    (lambda a: a["q"].__setattr__("dtype", 1), 1),                 # q not bf16
+    (lambda a: a["k"].__setattr__("ndim", 3), 1),                  # wrong rank
+    (lambda a: a["out"].shape.__setitem__(3, 64), 1),              # out head dim mismatch
+    (lambda a: a["sl"].shape.__setitem__(0, 3), 1),                # seq_lens length
+    (lambda a: a["q"].__setattr__("data", 0x10002), 1),            # misaligned base
+    (lambda a: a["k"].stride.__setitem__(1, 2 * 128 + 4), 1),      # stride not 16-byte multiple
+    (lambda a: a["bt"].stride.__setitem__(1, 2), 1),               # non-contiguous table rows
+    (lambda a: a["lse"].shape.__setitem__(2, 5), 1),               # lse shape
+])
+def test_invalid_decode_arguments(fwlib, mutate, status):
+    a = decode_args()
+    mutate(a)
+    rc = call_decode(fwlib, a["q"], a["k"], a["v"], a["bt"], a["sl"], a["out"], a["lse"])
+    assert rc == status, fwlib.load_library().fw_last_error()
+
+
+def test_unsupported_shapes(fwlib):
+    a = decode_args(D=64)
+    assert call_decode(fwlib, a["q"], a["k"], a["v"], a["bt"], a["sl"], a["out"], a["lse"]) == 2
+    a = decode_args(ps=24)
+    assert call_decode(fwlib, a["q"], a["k"], a["v"], a["bt"], a["sl"], a["out"], a["lse"]) == 2
+    a = decode_args(q_len=5)
+    assert call_decode(fwlib, a["q"], a["k"], a["v"], a["bt"], a["sl"], a["out"], a["lse"]) == 2
+    a = decode_args(Hq=6, Hkv=4)
+    assert call_decode(fwlib, a["q"], a["k"], a["v"], a["bt"], a["sl"], a["out"], a["lse"]) == 1
+
+
+def test_nonfinite_scale_rejected(fwlib):
+    a = decode_args()
+    assert call_decode(fwlib, a["q"], a["k"], a["v"], a["bt"], a["sl"], a["out"], a["lse"],
+                       scale=float("nan")) == 1
+
+
+def test_valid_call_without_gpu_fails_loudly(fwlib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    a = decode_args()
+    rc = call_decode(fwlib, a["q"], a["k"], a["v"], a["bt"], a["sl"], a["out"], a["lse"])
+    assert rc in (2, 4)              # FW_ERR_UNSUPPORTED / FW_ERR_CUDA: no device, nothing launched
+    assert fwlib.launch_count() == 0
