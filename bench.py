@@ -1,0 +1,470 @@
+"""Benchmark: paged GQA decode KV GB/s (and varlen prefill TFLOP/s) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is one fw_paged_decode call (split-KV attention kernel + combine
+kernel) over the Qwen3-14B-shaped workload: batch 64, 40 Q / 8 KV heads,
+head_dim 128, 128-token pages, seq_lens uniform in [512, 32768], BF16 ~N(0,1)
+in shuffled physical pages.  The KV cache (4.4 GB) is far larger than L2, so
+no flush is needed between steps.  `value` is KV bytes read per step divided
+by the step time (CUDA events on the launching stream, inputs resident).
+The prefill object times fw_varlen_prefill on the causal varlen GQA workload
+(16 sequences, lengths uniform in [256, 8192], 32 Q / 8 KV heads, hd 128).
+
+With N > 1 (torchrun, one rank per GPU) every rank runs its own replica of
+the workload (no collective on the data path: decode units are independent),
+so scaling is weak; the reported time is the max over ranks.
+
+--impl reference times the fp64 CPU oracle (the only other implementation of
+this method in the repository) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode KV GB/s (% of HBM peak); prefill TFLOP/s (% of BF16 peak)"
+DECODE_WL = "qwen3_14b_paged_decode"
+PREFILL_WL = "varlen_gqa_prefill"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": pk["hbm_gbs"], "bf16_tflops": pk["bf16_tflops"],
+                "bf16_tflops_sustained": pk.get("bf16_tflops_sustained", pk["bf16_tflops"]),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during a timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.device = device_index
+
+    def __enter__(self):
+        import torch
+        target = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.device).uuid)
+            target = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        except Exception:
+            target = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
+        if target:
+            cmd += ["-i", target]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        self.samples = []
+        if self.proc is None:
+            return False
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                self.samples.append({"sm": float(parts[1]), "max": float(parts[2]), "power": float(parts[3]),
+                                     "hw_slowdown": parts[5], "hw_thermal": parts[6],
+                                     "sw_thermal": parts[7], "sw_power_cap": parts[8]})
+            except ValueError:
+                continue
+        return False
+
+    def summary(self):
+        s = getattr(self, "samples", [])
+        if not s:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        reasons = set()
+        for x in s:
+            for key, name in (("hw_slowdown", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"), ("sw_power_cap", "sw_power_cap")):
+                if x[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(x["sm"] for x in s), "sm_max_mhz": max(x["max"] for x in s),
+                "reasons": sorted(reasons), "samples": len(s),
+                "power_w_max": max(x["power"] for x in s)}
+
+
+def source_sha(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "ragged_softmax_attention_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def ncu_traffic(profile_name, sources, units):
+    """DRAM bytes per launch from a committed ncu summary, scaled to `units`
+    of work; None when the kernel source changed since the capture."""
+    path = os.path.join(ROOT, "profiles", profile_name)
+    try:
+        with open(path) as f:
+            prof = json.load(f)
+    except Exception:
+        return None
+    if prof.get("source_sha256") != source_sha(*sources):
+        return None
+    per_unit = prof["dram_bytes_per_launch"] / prof["units_per_launch"]
+    return per_unit * units
+
+
+# ----------------------------------------------------------------- decode
+
+def decode_work(inp, wl):
+    lens = inp["seq_lens"].long().cpu()
+    kv = int(lens.sum()) * wl.num_kv_heads * (wl.head_dim_qk + wl.head_dim_v) * 2
+    rows = wl.batch * wl.q_len * wl.num_q_heads
+    pages = int(((lens + wl.page_size - 1) // wl.page_size).sum())
+    other = rows * wl.head_dim_qk * 2 + rows * wl.head_dim_v * 2 + rows * 4 + pages * 4 + wl.batch * 4
+    return kv, kv + other, int(lens.sum())
+
+
+def bench_decode(fw, torch, steps, warmup, device, peaks, batch=None, do_e2e=True):
+    import dataclasses
+    from ragged_softmax_attention_gb300.workloads import WORKLOADS, make_decode_inputs, workload_seq_lens
+    wl = WORKLOADS[DECODE_WL]
+    if batch:   # a prefix of the same batch (profiling captures on a smaller case)
+        lens = workload_seq_lens(wl)[:batch]
+        wl = dataclasses.replace(wl, batch=batch, seq_len_range=None, seq_lens=tuple(lens))
+    d = make_decode_inputs(wl, device)
+    kv_bytes, alg_bytes, tokens = decode_work(d, wl)
+    out, lse = fw.paged_decode(d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["seq_lens"], d["scale"])
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    def step():
+        fw.paged_decode(d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["seq_lens"], d["scale"],
+                        out=out, lse=lse)
+
+    for _ in range(max(3, warmup)):
+        step()
+    torch.cuda.synchronize()
+    fw.set_option(fw.FW_OPT_KERNEL_TIMING, 1)
+    fw.kernel_timing_read()
+    launches0 = fw.launch_count()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        torch.cuda.synchronize()
+        start.record(stream)
+        for _ in range(steps):
+            step()
+        stop.record(stream)
+        torch.cuda.synchronize()
+    elapsed_ms = start.elapsed_time(stop)
+    launches = fw.launch_count() - launches0
+    kernel_ms, kernel_n = fw.kernel_timing_read()
+    fw.set_option(fw.FW_OPT_KERNEL_TIMING, 0)
+    status = fw.device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} during the decode benchmark")
+    per_launch_ms = kernel_ms / max(1, kernel_n)
+    achieved = alg_bytes / (per_launch_ms * 1e-3) / 1e9
+    traffic = ncu_traffic("paged_decode_qwen3_14b_ncu.json", ["decode_kernel.cu", "fw_ptx.cuh"], tokens)
+    roof = {"kernel": "paged_decode_kernel<128,16>", "bound": "hbm", "achieved": round(achieved, 1),
+            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "traffic": traffic, "peak_source": peaks["source"],
+            "algorithmic_bytes_per_launch": alg_bytes, "kernel_ms_per_launch": round(per_launch_ms, 4)}
+
+    cfg = {"workload": DECODE_WL, "batch": wl.batch, "q_len": wl.q_len, "num_q_heads": wl.num_q_heads,
+           "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim_qk, "page_size": wl.page_size,
+           "seq_len_range": [512, 32768], "total_kv_tokens": tokens,
+           "kv_bytes_per_step": kv_bytes, "l2": "inputs larger than L2 (KV cache 4.4 GB), no flush",
+           "scale": wl.scale}
+    res = {"elapsed_ms": elapsed_ms, "kv_bytes": kv_bytes, "launches": launches, "roofline": roof,
+           "clocks": clk.summary(), "config": cfg, "inputs": d, "wl": wl,
+           "e2e_ms": float("nan"), "h2d": 0, "d2h": 0, "e2e_steps": 0}
+    if not do_e2e:
+        return res
+
+    # End to end through the public API from pinned host buffers.
+    host = {k: (v.cpu().pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    dev = {k: (torch.empty_like(v, device=device) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+    if wl.latent:
+        raise RuntimeError("latent workload not expected here")
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if isinstance(v, torch.Tensor))
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    e2e_steps = max(3, min(steps, 10))
+
+    def e2e_step():
+        for k, v in host.items():
+            if isinstance(v, torch.Tensor):
+                dev[k].copy_(v, non_blocking=True)
+        o, l_ = fw.paged_decode(dev["q"], dev["k_cache"], dev["v_cache"], dev["block_table"], dev["seq_lens"],
+                                dev["scale"], out=out, lse=lse)
+        out_h.copy_(o, non_blocking=True)
+        lse_h.copy_(l_, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    stop.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = start.elapsed_time(stop) / e2e_steps
+    del dev, host
+    res.update(e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, e2e_steps=e2e_steps)
+    return res
+
+
+# ---------------------------------------------------------------- prefill
+
+def prefill_flops(cu_q, cu_k, hq, dk, dv, causal):
+    total = 0
+    for i in range(len(cu_q) - 1):
+        lq = cu_q[i + 1] - cu_q[i]
+        lk = cu_k[i + 1] - cu_k[i]
+        if causal:
+            pairs = sum(max(0, min(lk, r + lk - lq + 1)) for r in range(lq)) if lq != lk else lq * (lq + 1) // 2
+        else:
+            pairs = lq * lk
+        total += pairs
+    return total * hq * 2 * (dk + dv)
+
+
+def bench_prefill(fw, torch, steps, warmup, device, peaks):
+    from ragged_softmax_attention_gb300.workloads import WORKLOADS, make_prefill_inputs
+    wl = WORKLOADS[PREFILL_WL]
+    d = make_prefill_inputs(wl, device)
+    cu_q = d["cu_seqlens_q"].cpu().tolist()
+    cu_k = d["cu_seqlens_k"].cpu().tolist()
+    flops = prefill_flops(cu_q, cu_k, wl.num_q_heads, wl.head_dim_qk, wl.head_dim_v, wl.causal)
+    try:
+        out, lse = fw.varlen_prefill(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], wl.causal,
+                                     wl.scale)
+    except fw.FwError as e:
+        if e.status == 2:
+            return {"workload": PREFILL_WL, "value": None, "unit": "TFLOP/s", "unavailable": str(e)}
+        raise
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, warmup)):
+        fw.varlen_prefill(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], wl.causal, wl.scale,
+                          out=out, lse=lse)
+    torch.cuda.synchronize()
+    fw.set_option(fw.FW_OPT_KERNEL_TIMING, 1)
+    fw.kernel_timing_read()
+    n = max(3, min(steps, 50))
+    l0 = fw.launch_count()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(n):
+        fw.varlen_prefill(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], wl.causal, wl.scale,
+                          out=out, lse=lse)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(stop) / n
+    kms, kn = fw.kernel_timing_read()
+    fw.set_option(fw.FW_OPT_KERNEL_TIMING, 0)
+    if fw.device_status() != 0:
+        raise RuntimeError("device status nonzero during the prefill benchmark")
+    per = kms / max(1, kn)
+    ach = flops / (per * 1e-3) / 1e12
+    traffic = ncu_traffic("varlen_prefill_gqa_ncu.json", ["prefill_kernel.cu", "fw_ptx.cuh"], flops)
+    return {"workload": PREFILL_WL, "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 4), "steps": n, "flops_per_step": flops,
+            "gpu_launches": fw.launch_count() - l0,
+            "config": {"num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads, "num_kv_heads": wl.num_kv_heads,
+                       "head_dim": wl.head_dim_qk, "causal": wl.causal, "total_tokens": cu_q[-1],
+                       "seq_len_range": list(wl.seq_len_range)},
+            "roofline": {"kernel": "varlen_prefill_kernel<128>", "bound": "tensor", "achieved": round(ach, 1),
+                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": round(ach / peaks["bf16_tflops"], 4),
+                         "frac_of_sustained": round(ach / peaks["bf16_tflops_sustained"], 4),
+                         "traffic": traffic, "peak_source": peaks["source"], "kernel_ms_per_launch": round(per, 4)}}
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def oracle_sample_rate(torch, inp, wl, rows_b, heads, threads):
+    """Run the fp64 oracle on batch rows `rows_b` x query heads `heads`;
+    returns (KV bytes those rows read, seconds)."""
+    import oracle
+    lens = inp["seq_lens"].cpu()
+    bt = inp["block_table"].cpu()
+    G = wl.num_q_heads // wl.num_kv_heads
+    total_bytes = 0
+    total_s = 0.0
+    for b in rows_b:
+        npg = -(-int(lens[b]) // wl.page_size)
+        pages = bt[b, :npg].long()
+        k = inp["k_cache"][pages.to(inp["k_cache"].device)].cpu()
+        v = inp["v_cache"][pages.to(inp["v_cache"].device)].cpu()
+        sub_bt = torch.arange(npg, dtype=torch.int32).unsqueeze(0)
+        q = inp["q"][b:b + 1].cpu()
+        t0 = time.perf_counter()
+        oracle.paged_decode(q, k, v, sub_bt, lens[b:b + 1], wl.scale, rows=list(heads), threads=threads)
+        total_s += time.perf_counter() - t0
+        kv_heads = sorted({h // G for h in heads})
+        total_bytes += int(lens[b]) * len(kv_heads) * (wl.head_dim_qk + wl.head_dim_v) * 2
+    return total_bytes, total_s
+
+
+def cpu_baseline(torch, inp, wl, budget_s=15.0):
+    threads = max(1, os.cpu_count() or 1)
+    heads = list(range(wl.num_q_heads))
+    b_cal, s_cal = oracle_sample_rate(torch, inp, wl, [0], heads, threads)
+    nrows = max(1, min(wl.batch - 1, int(budget_s / max(s_cal, 1e-3))))
+    rows = list(range(1, 1 + nrows))
+    by, s = oracle_sample_rate(torch, inp, wl, rows, heads, threads)
+    return {"value": round(by / s / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"batch rows 1..{nrows} of {wl.batch}, all {wl.num_q_heads} query heads "
+                      f"({s:.1f} s of fp64 CPU work, {threads} threads)"}
+
+
+def run_reference(args):
+    import torch
+    world, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    from ragged_softmax_attention_gb300.workloads import WORKLOADS, make_decode_inputs
+    wl = WORKLOADS[DECODE_WL]
+    # Inputs are drawn where they are cheapest to draw (the GPU when present);
+    # only the oracle call itself is timed, on the host cores.
+    inp = make_decode_inputs(wl, "cuda" if torch.cuda.is_available() else "cpu")
+    threads = max(1, os.cpu_count() or 1)
+    G = wl.num_q_heads // wl.num_kv_heads
+    total_bytes, total_s = 0, 0.0
+    for i in range(args.warmup + args.steps):
+        b = i % wl.batch
+        g = (i // wl.batch) % wl.num_kv_heads
+        by, s = oracle_sample_rate(torch, inp, wl, [b], range(g * G, (g + 1) * G), threads)
+        if i >= args.warmup:
+            total_bytes += by
+            total_s += s
+    value = total_bytes / total_s / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_s / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": DECODE_WL, "batch": wl.batch,
+                                            "num_q_heads": wl.num_q_heads, "num_kv_heads": wl.num_kv_heads,
+                                            "head_dim": wl.head_dim_qk, "page_size": wl.page_size},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": "each step: one (batch row, KV head group) of the workload, "
+                                       "cycling through rows"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--only", choices=["all", "decode", "prefill"], default="all",
+                    help="profiling runs: time one path only")
+    ap.add_argument("--decode-batch", type=int, default=0,
+                    help="profiling runs: a prefix of the decode batch (smaller capture)")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import ragged_softmax_attention_gb300 as fw
+    from ragged_softmax_attention_gb300 import build as fwbuild
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        pg = dist
+    if rank == 0:
+        fwbuild.build()
+    if pg:
+        pg.barrier()
+    fw.load_library()
+    peaks = load_peaks()
+
+    if pg:
+        pg.barrier()
+    if args.only == "prefill":
+        pre = bench_prefill(fw, torch, args.steps, args.warmup, device, peaks)
+        if rank == 0:
+            print(json.dumps({"prefill": pre}), flush=True)
+        return 0
+    dec = bench_decode(fw, torch, args.steps, args.warmup, device, peaks, batch=args.decode_batch or None,
+                       do_e2e=not args.no_e2e)
+    pre = None if args.only == "decode" else bench_prefill(fw, torch, args.steps, args.warmup, device, peaks)
+    t = torch.tensor([dec["elapsed_ms"], dec["e2e_ms"]], dtype=torch.float64, device=device)
+    if pg:
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    elapsed_ms, e2e_ms = t.tolist()
+    value = dec["kv_bytes"] * args.steps * world / (elapsed_ms * 1e-3) / 1e9
+    e2e_value = dec["kv_bytes"] * world / (e2e_ms * 1e-3) / 1e9 if e2e_ms == e2e_ms else None
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return 0
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": dict(dec["config"], parallelism=f"replicas{world}" if world > 1 else "single"),
+            "frac_of_hbm_peak": round(value / world / peaks["hbm_gbs"], 4),
+            "roofline": dec["roofline"], "clocks": dec["clocks"], "gpu_launches": dec["launches"],
+            "e2e": {"value": round(e2e_value, 1) if e2e_value else None, "unit": "GB/s", "h2d_bytes_per_step": dec["h2d"],
+                    "d2h_bytes_per_step": dec["d2h"], "steps": dec["e2e_steps"],
+                    "note": "inputs (incl. the KV cache) copied from pinned host memory every step"},
+            "prefill": pre}
+    if world == 1 and not args.no_cpu_baseline and not args.decode_batch:
+        try:
+            line["cpu_baseline"] = cpu_baseline(torch, dec["inputs"], dec["wl"])
+        except Exception as e:   # the baseline is context; report why it is missing
+            line["cpu_baseline"] = {"value": None, "unit": "GB/s", "kind": "oracle", "error": str(e)}
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

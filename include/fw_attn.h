@@ -95,9 +95,10 @@ typedef struct {
  * 1 <= q_len <= 4; strides multiples of 8 elements and 16-byte aligned base
  * pointers (tensor-memory-accelerator addressing).
  *
- * Split-KV: the library cuts each row's keys into chunks sized from shapes
- * only and merges the FP32 partials (normalised output + log2-sum-exp per
- * row per split) with a second kernel.  The partials live in a workspace:
+ * Split-KV: the keys of a row may be cut across CTAs (see fw_decode_plan_t);
+ * the FP32 partials (normalised output + log2-sum-exp per row per piece) are
+ * merged by a combine kernel.  Three launches per call: plan (one block),
+ * attention, combine.  The plan and the partials live in a workspace:
  * caller-provided through fw_set_workspace(), else an internal buffer grown
  * on demand with cudaMalloc (grow it once, outside any stream capture, by an
  * initial call with the largest shapes).
@@ -109,10 +110,11 @@ fw_status_t fw_paged_decode(const fw_tensor_t *q, const fw_tensor_t *k_cache,
 
 /*
  * Workspace bytes fw_paged_decode needs for these shapes (data pointers are
- * not read).  Writes the size to *bytes; 0 when no row is ever split.
- * The size is rows * splits * (Dv + 1) * 4 bytes, with rows = B * q_len * Hq:
- * one FP32 partial output row plus one FP32 LSE per row per split
- * ("TokenSpeed-MLA 2.0.1", packed-query paragraph, 513 floats per row at Dv 512).
+ * not read).  Writes the size to *bytes.  It holds the tile prefix table
+ * (B + 3 int32) and rows * max_pieces * (Dv + 1) * 4 bytes of partials, with
+ * rows = B * q_len * Hq: one FP32 partial output row plus one FP32 LSE per
+ * row per split ("TokenSpeed-MLA 2.0.1", packed-query paragraph, 513 floats
+ * per row at Dv 512).
  */
 fw_status_t fw_paged_decode_workspace_size(const fw_tensor_t *q, const fw_tensor_t *k_cache,
                                            const fw_tensor_t *v_cache,
@@ -162,7 +164,7 @@ const char *fw_last_error(void);
 
 /* Tunables, mostly for tests and measurement. */
 typedef enum {
-    FW_OPT_DECODE_CHUNK_TOKENS = 0, /* force the split-KV chunk (multiple of 128; 0 = auto) */
+    FW_OPT_DECODE_CHUNK_TOKENS = 0, /* force the keys per CTA range (multiple of 128; 0 = auto) */
     FW_OPT_WAIT_TIMEOUT_MS = 1,     /* device wait limit before giving up (default 2000) */
     FW_OPT_KERNEL_TIMING = 2,       /* 1: record CUDA events around each attention kernel */
     FW_OPT_MAX_CTAS = 3             /* cap on persistent CTAs (0 = one per SM) */
@@ -185,17 +187,25 @@ int64_t fw_launch_count(void);
  * Host-side decode plan for given shapes (no device access), exposed so the
  * planner can be checked without a GPU.  num_sms <= 0 queries the current
  * device.  Fields are written on success.
+ *
+ * Scheduling: the (batch row, KV head, row group) units are laid end to end
+ * in the order of their 128-key tiles; each persistent CTA takes equal
+ * contiguous tile ranges (span decided on the device from seq_lens, never
+ * below min_span_tiles unless forced), so CTAs differ by at most one tile of
+ * work.  A unit cut by range boundaries becomes pieces whose FP32 partials a
+ * combine kernel merges.
  */
 typedef struct {
     int32_t group;            /* G = Hq / Hkv */
     int32_t rows_per_unit;    /* NQ: MMA N extent holding the (token, head) rows of one unit */
     int32_t tokens_per_unit;  /* query tokens one unit covers (whole head groups) */
     int32_t heads_per_unit;   /* query heads one unit covers */
-    int32_t row_groups;       /* units per (batch, kv head, split) */
-    int32_t chunk_tokens;     /* keys per split (multiple of 128) */
-    int32_t max_splits;       /* ceil(max_pages * ps / chunk_tokens) */
-    int64_t num_units;        /* B * Hkv * row_groups * max_splits (upper bound) */
-    int64_t workspace_bytes;  /* 0 when max_splits == 1 */
+    int32_t row_groups;       /* units per (batch row, KV head) */
+    int32_t min_span_tiles;   /* fewest KV tiles in one CTA range (the forced span when set) */
+    int32_t max_pieces;       /* upper bound of split-KV pieces of one unit */
+    int64_t num_units;        /* B * Hkv * row_groups */
+    int64_t partial_bytes;    /* rows * max_pieces * (Dv + 1) * 4: FP32 partial rows + LSE */
+    int64_t workspace_bytes;  /* partial_bytes + the tile prefix table + alignment */
     int32_t grid;             /* persistent CTAs launched */
 } fw_decode_plan_t;
 

@@ -39,9 +39,10 @@ class FwTensor(ctypes.Structure):
 class FwDecodePlan(ctypes.Structure):
     _fields_ = [("group", ctypes.c_int32), ("rows_per_unit", ctypes.c_int32),
                 ("tokens_per_unit", ctypes.c_int32), ("heads_per_unit", ctypes.c_int32),
-                ("row_groups", ctypes.c_int32), ("chunk_tokens", ctypes.c_int32),
-                ("max_splits", ctypes.c_int32), ("num_units", ctypes.c_int64),
-                ("workspace_bytes", ctypes.c_int64), ("grid", ctypes.c_int32)]
+                ("row_groups", ctypes.c_int32), ("min_span_tiles", ctypes.c_int32),
+                ("max_pieces", ctypes.c_int32), ("num_units", ctypes.c_int64),
+                ("partial_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
+                ("grid", ctypes.c_int32)]
 
 
 _lib = None

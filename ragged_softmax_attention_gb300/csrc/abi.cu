@@ -200,30 +200,22 @@ fw_status_t plan_decode(int32_t B, int32_t q_len, int32_t Hq, int32_t Hkv, int32
         p.rows_per_unit = 32;
         p.row_groups = q_len * ((G + 31) / 32);
     }
-    const int64_t units_base = (int64_t)B * Hkv * p.row_groups;
+    p.num_units = (int64_t)B * Hkv * p.row_groups;
     const int64_t tiles_max = (max_kv_len + fw::kKvTile - 1) / fw::kKvTile;
-    int64_t chunk_tiles;
-    if (g_opt_chunk > 0) {
-        chunk_tiles = (g_opt_chunk + fw::kKvTile - 1) / fw::kKvTile;
-    } else {
-        // Aim for ~32 units per persistent CTA when every row is at the length
-        // bound, but never below 8 tiles (1024 keys) per split.
-        const int64_t target = 32LL * num_sms;
-        const int64_t want = units_base > 0 ? (target + units_base - 1) / units_base : 1;
-        chunk_tiles = tiles_max > 0 ? (tiles_max + want - 1) / want : 1;
-        if (chunk_tiles < 8) chunk_tiles = 8;
-    }
-    if (tiles_max > 0 && chunk_tiles > tiles_max) chunk_tiles = tiles_max;
-    if (chunk_tiles < 1) chunk_tiles = 1;
-    p.chunk_tokens = (int32_t)(chunk_tiles * fw::kKvTile);
-    p.max_splits = max_kv_len > 0 ? (int32_t)((max_kv_len + p.chunk_tokens - 1) / p.chunk_tokens) : 1;
-    p.num_units = units_base * p.max_splits;
+    if (p.num_units * (tiles_max > 0 ? tiles_max : 1) >= (1LL << 31))
+        return fail(FW_ERR_UNSUPPORTED, "decode too large for 32-bit tile indices");
+    int64_t span = g_opt_chunk > 0 ? (g_opt_chunk + fw::kKvTile - 1) / fw::kKvTile : fw::kDecodeMinSpan;
+    p.min_span_tiles = (int32_t)span;
+    // A unit of t tiles meets at most ceil(t / span) + 1 ranges.
+    p.max_pieces = (int32_t)((tiles_max + span - 1) / span + 1);
     const int64_t rows = (int64_t)B * q_len * Hq;
-    p.workspace_bytes = p.max_splits > 1 ? rows * p.max_splits * (int64_t)(Dv + 1) * 4 + 256 : 0;
+    p.partial_bytes = rows * p.max_pieces * (int64_t)(Dv + 1) * 4;
+    const int64_t plan_bytes = ((B + 3) * 4 + 255) / 256 * 256;
+    const int64_t o_bytes = (rows * p.max_pieces * (int64_t)Dv * 4 + 255) / 256 * 256;
+    p.workspace_bytes = plan_bytes + o_bytes + rows * p.max_pieces * 4;
     int64_t grid = num_sms;
     if (g_opt_max_ctas > 0 && grid > g_opt_max_ctas) grid = g_opt_max_ctas;
-    if (grid > p.num_units) grid = p.num_units;
-    p.grid = (int32_t)grid;
+    p.grid = (int32_t)(grid > 0 ? grid : 1);
     *pl = p;
     return FW_OK;
 }
@@ -252,20 +244,6 @@ fw_status_t get_workspace(DeviceState *d, size_t bytes, cudaStream_t stream, voi
     }
     *ptr = d->ws;
     return FW_OK;
-}
-
-void timing_begin(cudaStream_t stream, cudaEvent_t *a) {
-    *a = nullptr;
-    if (!g_opt_timing) return;
-    *a = pooled_event();
-    cudaEventRecord(*a, stream);
-}
-
-void timing_end(cudaStream_t stream, cudaEvent_t a) {
-    if (!a) return;
-    cudaEvent_t b = pooled_event();
-    cudaEventRecord(b, stream);
-    g_timed.push_back({a, b});
 }
 
 }  // namespace
@@ -448,9 +426,12 @@ fw_status_t fw_paged_decode(const fw_tensor_t *q, const fw_tensor_t *k_cache, co
     p.heads_per_unit = pl.heads_per_unit;
     p.head_chunks = p.head_mode ? (pl.group + 31) / 32 : 1;
     p.row_groups = pl.row_groups;
-    p.chunk_tokens = pl.chunk_tokens;
-    p.max_splits = pl.max_splits;
-    p.num_units = pl.num_units;
+    p.units_per_row = (int)Hkv * pl.row_groups;
+    p.forced_span = g_opt_chunk > 0 ? pl.min_span_tiles : 0;
+    p.min_span = pl.min_span_tiles;
+    p.max_pieces = pl.max_pieces;
+    p.grid = pl.grid;
+    p.Dv = (int)Dv;
     p.block_table = static_cast<const int32_t *>(block_table->data);
     p.bt_stride = block_table->stride[0];
     p.seq_lens = static_cast<const int32_t *>(seq_lens->data);
@@ -459,10 +440,12 @@ fw_status_t fw_paged_decode(const fw_tensor_t *q, const fw_tensor_t *k_cache, co
     p.lse = lse ? static_cast<float *>(lse->data) : nullptr;
     if (lse) for (int i = 0; i < 3; ++i) p.lse_stride[i] = lse->stride[i];
     const int64_t rows = B * q_len * Hq;
-    p.ws_o = static_cast<float *>(ws);
-    p.ws_lse = ws ? reinterpret_cast<float *>(static_cast<char *>(ws) +
-                                              ((rows * pl.max_splits * Dv * 4 + 255) / 256) * 256)
-                  : nullptr;
+    char *wsb = static_cast<char *>(ws);
+    const int64_t plan_bytes = ((B + 3) * 4 + 255) / 256 * 256;
+    const int64_t o_bytes = (rows * pl.max_pieces * Dv * 4 + 255) / 256 * 256;
+    p.plan = reinterpret_cast<int32_t *>(wsb);
+    p.ws_o = reinterpret_cast<float *>(wsb + plan_bytes);
+    p.ws_lse = reinterpret_cast<float *>(wsb + plan_bytes + o_bytes);
     p.scale_log2 = scale * 1.4426950408889634f;
     p.timeout_ns = (uint64_t)g_opt_timeout_ms * 1000000ull;
     p.status = d->status;
@@ -488,26 +471,13 @@ fw_status_t fw_paged_decode(const fw_tensor_t *q, const fw_tensor_t *k_cache, co
                                 (uint64_t)v_cache->stride[0] * 2};
         if (fw_status_t s = encode_bf16(&tv, v_cache->data, 4, dv, sv, box, "v_cache")) return s;
     }
-    cudaEvent_t ev = nullptr;
-    timing_begin(stream, &ev);
-    cudaError_t e = fw::launch_decode(p, tq, tk, tv, (int)Dk, pl.grid, stream);
+    cudaEvent_t ev0 = nullptr, ev1 = nullptr;
+    if (g_opt_timing) { ev0 = pooled_event(); ev1 = pooled_event(); }
+    int launched = 0;
+    cudaError_t e = fw::launch_decode(p, tq, tk, tv, (int)Dk, stream, ev0, ev1, &launched);
+    g_launches.fetch_add(launched);
     if (e != cudaSuccess) return fail(FW_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
-    timing_end(stream, ev);
-    g_launches.fetch_add(1);
-    if (pl.max_splits > 1) {
-        fw::CombineParams c{};
-        c.B = (int)B; c.q_len = (int)q_len; c.Hq = (int)Hq; c.Dv = (int)Dv;
-        c.chunk_tokens = pl.chunk_tokens; c.max_splits = pl.max_splits;
-        c.seq_lens = p.seq_lens; c.ws_o = p.ws_o; c.ws_lse = p.ws_lse;
-        c.out = out->data;
-        for (int i = 0; i < 4; ++i) c.out_stride[i] = out->stride[i];
-        c.lse = p.lse;
-        if (lse) for (int i = 0; i < 3; ++i) c.lse_stride[i] = lse->stride[i];
-        c.max_kv_len = (int)(max_pages * ps);
-        e = fw::launch_combine(c, stream);
-        if (e != cudaSuccess) return fail(FW_ERR_CUDA, "combine launch: %s", cudaGetErrorString(e));
-        g_launches.fetch_add(1);
-    }
+    if (ev0) g_timed.push_back({ev0, ev1});
     return ok();
 }
 

@@ -1,11 +1,14 @@
 // Paged grouped-query decode, sm_103a.
 //
-// The work unit is (batch row b, KV head g, row group, KV split): the query
-// rows a unit holds are the (token, head) pairs of the query heads that share
-// KV head g ("Writing Page Attention with PyPTO", section 1.3: one task = one
-// batch row + one KV head + its five query heads; "TokenSpeed-MLA 2.0.1":
-// query tokens folded next to the heads), and its keys are one chunk of the
-// row's paged KV range (split-KV, merged afterwards by the combine kernel).
+// The work unit is (batch row b, KV head g, row group): the query rows a unit
+// holds are the (token, head) pairs of the query heads that share KV head g
+// ("Writing Page Attention with PyPTO", section 1.3: one task = one batch row
+// + one KV head + its five query heads; "TokenSpeed-MLA 2.0.1": query tokens
+// folded next to the heads).  Units are laid end to end in the global order
+// of their 128-key tiles and every persistent CTA takes equal contiguous tile
+// ranges, so the work per CTA differs by at most one tile however ragged the
+// batch is.  A unit cut by a range boundary becomes several pieces whose
+// FP32 partials (split-KV) the combine kernel merges.
 //
 // Orientation.  A decode unit has few query rows (5 at 40 Q / 8 KV heads), so
 // the KV tile takes the 128-wide MMA M axis and the padded query rows take N:
@@ -67,32 +70,75 @@ struct DecodeCfg {
     static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, NQ, true, false);
 };
 
-struct Unit {
-    int b, g, rg, s, n, k_begin, k_end, ntiles;
+struct Unit {                 // one piece: a unit's tiles inside one CTA range
+    int b, g, rg, n, k_begin, k_end, ntiles;
+    int k, npieces;
     bool single;
 };
 
 __device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
 
-__device__ __forceinline__ bool fetch_unit(const DecodeParams &p, int64_t u, Unit &x) {
-    x.rg = (int)(u % p.row_groups);
-    int64_t t = u / p.row_groups;
-    x.g = (int)(t % p.Hkv);
-    t /= p.Hkv;
-    x.b = (int)(t % p.B);
-    x.s = (int)(t / p.B);
-    int n = __ldg(p.seq_lens + x.b);
+__device__ __forceinline__ int clamp_len(const DecodeParams &p, int n) {
     const int cap = p.max_pages * p.ps;
-    n = n < 0 ? 0 : (n > cap ? cap : n);
-    x.n = n;
-    const int nsplit = n > 0 ? ceil_div_i(n, p.chunk_tokens) : 1;
-    if (x.s >= nsplit) return false;
-    x.single = (nsplit == 1);
-    x.k_begin = x.s * p.chunk_tokens;
-    x.k_end = min(n, x.k_begin + p.chunk_tokens);
-    x.ntiles = n > 0 ? ceil_div_i(x.k_end - x.k_begin, kKvTile) : 0;
-    return true;
+    return n < 0 ? 0 : (n > cap ? cap : n);
 }
+
+// Walks the pieces of this CTA's tile ranges; every role runs its own copy
+// and sees the same sequence.
+struct PieceIter {
+    int T, span, range, pos, end, b;
+
+    __device__ void init(const DecodeParams &p) {
+        T = __ldg(p.plan + 0);
+        span = max(1, __ldg(p.plan + 1));
+        range = blockIdx.x;
+        pos = 0;
+        end = 0;
+        b = -1;
+        open_range();
+    }
+    __device__ void open_range() {
+        const long long lo = (long long)range * span;
+        pos = lo < T ? (int)lo : T;
+        end = (int)min((long long)T, lo + span);
+        b = -1;
+    }
+    __device__ bool next(const DecodeParams &p, Unit &x) {
+        const int32_t *PB = p.plan + 2;
+        while (pos >= end) {
+            range += gridDim.x;
+            if ((long long)range * span >= T) return false;
+            open_range();
+        }
+        if (b < 0 || pos >= __ldg(PB + b + 1)) {
+            int lo = 0, hi = p.B - 1;              // largest b with PB[b] <= pos
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (__ldg(PB + mid) <= pos) lo = mid; else hi = mid - 1;
+            }
+            b = lo;
+        }
+        const int pb0 = __ldg(PB + b);
+        const int tb = (__ldg(PB + b + 1) - pb0) / p.units_per_row;
+        const int off = pos - pb0;
+        const int u = off / tb;
+        const int tl = off - u * tb;
+        const int th = min(tb, tl + (end - pos));
+        const int pstart = pb0 + u * tb;
+        x.b = b;
+        x.g = u / p.row_groups;
+        x.rg = u - x.g * p.row_groups;
+        x.n = clamp_len(p, __ldg(p.seq_lens + b));
+        x.k_begin = tl * kKvTile;
+        x.k_end = min(x.n, th * kKvTile);
+        x.ntiles = th - tl;
+        x.k = (pstart + tl) / span - pstart / span;
+        x.npieces = (pstart + tb - 1) / span - pstart / span + 1;
+        x.single = (x.npieces == 1);
+        pos += th - tl;
+        return true;
+    }
+};
 
 // Query row r of unit x -> (token t, head h); false if the row is padding.
 __device__ __forceinline__ bool unit_row(const DecodeParams &p, const Unit &x, int r, int &t, int &h) {
@@ -191,9 +237,10 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
         const int box_rows = p.ps < kKvTile ? p.ps : kKvTile;
         const int pages_per_tile = p.ps < kKvTile ? kKvTile / p.ps : 1;
         const uint32_t q_rows = p.head_mode == 0 ? (uint32_t)(p.G * p.tokens_per_unit) : (uint32_t)p.rows;
-        for (int64_t u = blockIdx.x; u < p.num_units; u += gridDim.x) {
-            Unit x;
-            if (!fetch_unit(p, u, x) || x.ntiles == 0) continue;
+        PieceIter it;
+        it.init(p);
+        Unit x;
+        while (it.next(p, x)) {
             const int qs = ju & 1;
             if (!warp_wait(&q_empty[qs], ((ju >> 1) & 1) ^ 1, wc, lane)) goto producer_done;
             if (lane == 0) {
@@ -207,17 +254,32 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
                                 c * 64, h0, t0, x.b);
             }
             __syncwarp();
+            // Physical page numbers of the piece, 64 logical pages at a time in
+            // two 32-entry register windows (lane l holds page win + l and
+            // win + 32 + l); the next window is fetched while the current one
+            // is in use, so no tile waits on a block-table read.  Entries past
+            // the row's last page are never read (PyPTO section 9.1).
+            const int32_t *bt_row = p.block_table + (int64_t)x.b * p.bt_stride;
+            const int lp_end = ceil_div_i(x.k_end, p.ps);
+            int win = x.k_begin / p.ps;
+            int cur = (win + lane < lp_end) ? __ldg(bt_row + win + lane) : 0;
+            int nxt = (win + 32 + lane < lp_end) ? __ldg(bt_row + win + 32 + lane) : 0;
             for (int i = 0; i < x.ntiles; ++i, ++jt) {
                 const int ts = x.k_begin + i * kKvTile;
-                const int first_lp = ts / p.ps;
+                const int lp0 = ts / p.ps;
                 const int slot0 = p.ps < kKvTile ? 0 : ts % p.ps;
                 int npages = 1;
                 if (p.ps < kKvTile) npages = min(pages_per_tile, ceil_div_i(x.k_end - ts, p.ps));
-                int phys = 0;
-                if (lane < npages) {
-                    phys = __ldg(p.block_table + (int64_t)x.b * p.bt_stride + first_lp + lane);
-                    if ((unsigned)phys >= (unsigned)p.num_pages) { record_error(p.status, 1); phys = 0; }
+                if (lp0 >= win + 32) {
+                    win += 32;
+                    cur = nxt;
+                    nxt = (win + 32 + lane < lp_end) ? __ldg(bt_row + win + 32 + lane) : 0;
                 }
+                const int idx = lp0 + lane - win;          // < 64 since npages <= 16
+                const int from_cur = __shfl_sync(0xffffffffu, cur, idx & 31);
+                const int from_nxt = __shfl_sync(0xffffffffu, nxt, idx & 31);
+                int phys = idx < 32 ? from_cur : from_nxt;
+                if (lane < npages && (unsigned)phys >= (unsigned)p.num_pages) { record_error(p.status, 1); phys = 0; }
                 const uint32_t bytes = (uint32_t)(npages * box_rows * 128 * C::kChunks);
                 const int ks = jt % C::kKStages;
                 if (!warp_wait(&k_empty[ks], ((jt / C::kKStages) & 1) ^ 1, wc, lane)) goto producer_done;
@@ -285,9 +347,10 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
                 mma_commit(pv_done);
                 return true;
             };
-            for (int64_t u = blockIdx.x; u < p.num_units; u += gridDim.x) {
-                Unit x;
-                if (!fetch_unit(p, u, x) || x.ntiles == 0) continue;
+            PieceIter it;
+            it.init(p);
+            Unit x;
+            while (it.next(p, x)) {
                 const int qs = ju & 1;
                 if (!mbar_wait(&q_full[qs], (ju >> 1) & 1, wc)) goto mma_done;
                 for (int i = 0; i < x.ntiles; ++i, ++jt) {
@@ -330,9 +393,10 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
         const int row_in_tile = q4 * 32 + lane;        // key of the tile / dv lane this thread owns
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         int jt = 0;
-        for (int64_t u = blockIdx.x; u < p.num_units; u += gridDim.x) {
-            Unit x;
-            if (!fetch_unit(p, u, x)) continue;
+        PieceIter it;
+        it.init(p);
+        Unit x;
+        while (it.next(p, x)) {
             int lim[NQ];
             int nrows = 0;
 #pragma unroll
@@ -341,20 +405,6 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
                 const bool ok = unit_row(p, x, r, t, h);
                 lim[r] = ok ? min(x.n, x.n - p.q_len + t + 1) : 0;
                 if (ok) nrows = r + 1;
-            }
-            if (x.ntiles == 0) {
-                // No keys at all: zero output rows and -inf LSE.
-#pragma unroll
-                for (int r = 0; r < NQ; ++r) {
-                    int t, h;
-                    if (!unit_row(p, x, r, t, h)) continue;
-                    __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(p.out) + x.b * p.out_stride[0] +
-                                       t * p.out_stride[1] + h * p.out_stride[2];
-                    for (int dv = row_in_tile; dv < D; dv += 128) o[dv] = __float2bfloat16(0.f);
-                    if (row_in_tile == 0 && p.lse)
-                        p.lse[x.b * p.lse_stride[0] + t * p.lse_stride[1] + h * p.lse_stride[2]] = kNegInf;
-                }
-                continue;
             }
             float m_ref[NQ], l_part[NQ];
 #pragma unroll
@@ -490,7 +540,7 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
                             op[dv] = __float2bfloat16_rn(val);
                         } else {
                             const int64_t row = ((int64_t)x.b * p.q_len + t) * p.Hq + h;
-                            p.ws_o[(row * p.max_splits + x.s) * D + dv] = val;
+                            p.ws_o[(row * p.max_pieces + x.k) * D + dv] = val;
                         }
                     }
                 }
@@ -508,7 +558,7 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
                                     lse2 * 0.69314718055994531f;
                         } else {
                             const int64_t row = ((int64_t)x.b * p.q_len + t) * p.Hq + h;
-                            p.ws_lse[row * p.max_splits + x.s] = lse2;
+                            p.ws_lse[row * p.max_pieces + x.k] = lse2;
                         }
                     }
                 }
@@ -526,7 +576,7 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
 
 template <int D, int NQ>
 cudaError_t launch_t(const DecodeParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
-                     const CUtensorMap &tv, int grid, cudaStream_t stream) {
+                     const CUtensorMap &tv, cudaStream_t stream) {
     using C = DecodeCfg<D, NQ>;
     static bool configured = false;
     if (!configured) {
@@ -535,36 +585,84 @@ cudaError_t launch_t(const DecodeParams &p, const CUtensorMap &tq, const CUtenso
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    paged_decode_kernel<D, NQ><<<grid, 192, C::kSmemBytes, stream>>>(p, tq, tk, tv);
+    paged_decode_kernel<D, NQ><<<p.grid, 192, C::kSmemBytes, stream>>>(p, tq, tk, tv);
     return cudaGetLastError();
 }
 
-}  // namespace
-
-size_t decode_smem_bytes(int head_dim, int rows) {
-    if (head_dim == 128) return rows == 16 ? DecodeCfg<128, 16>::kSmemBytes : DecodeCfg<128, 32>::kSmemBytes;
-    return rows == 16 ? DecodeCfg<256, 16>::kSmemBytes : DecodeCfg<256, 32>::kSmemBytes;
-}
-
-cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
-                          const CUtensorMap &tv, int head_dim, int grid, cudaStream_t stream) {
-    if (head_dim == 128 && p.rows == 16) return launch_t<128, 16>(p, tq, tk, tv, grid, stream);
-    if (head_dim == 128 && p.rows == 32) return launch_t<128, 32>(p, tq, tk, tv, grid, stream);
-    if (head_dim == 256 && p.rows == 16) return launch_t<256, 16>(p, tq, tk, tv, grid, stream);
-    if (head_dim == 256 && p.rows == 32) return launch_t<256, 32>(p, tq, tk, tv, grid, stream);
-    return cudaErrorInvalidValue;
+// ------------------------------------------------------------------- plan
+//
+// One block: exclusive prefix PB[b] of the KV tiles each batch row puts in
+// the global order (ceil(n_b / 128) tiles for each of its units), the total
+// T and the range span; rows with no keys get their zero output and -inf LSE
+// here, since no range ever covers them.
+__global__ void __launch_bounds__(1024) decode_plan_kernel(const __grid_constant__ DecodeParams p) {
+    __shared__ int warp_sums[32];
+    __shared__ int carry_s;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int32_t *PB = p.plan + 2;
+    if (tid == 0) carry_s = 0;
+    __syncthreads();
+    for (int base = 0; base < p.B; base += 1024) {
+        const int b = base + tid;
+        const int n = b < p.B ? clamp_len(p, __ldg(p.seq_lens + b)) : 0;
+        const int t = ceil_div_i(n, kKvTile) * p.units_per_row;
+        int incl = t;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) warp_sums[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            int w = warp_sums[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += v;
+            }
+            warp_sums[lane] = w;                     // inclusive over warps
+        }
+        __syncthreads();
+        const int before = (warp > 0 ? warp_sums[warp - 1] : 0) + incl - t;
+        if (b < p.B) PB[b] = carry_s + before;
+        __syncthreads();
+        if (tid == 0) carry_s += warp_sums[31];
+        __syncthreads();
+    }
+    if (tid == 0) {
+        const int T = carry_s;
+        PB[p.B] = T;
+        int span = p.forced_span;
+        if (span <= 0) span = max(p.min_span, ceil_div_i(T, max(1, p.grid)));
+        p.plan[0] = T;
+        p.plan[1] = span;
+    }
+    // Empty rows.
+    const int64_t rows = (int64_t)p.B * p.q_len * p.Hq;
+    for (int64_t r = tid; r < rows; r += blockDim.x) {
+        const int b = (int)(r / ((int64_t)p.q_len * p.Hq));
+        if (clamp_len(p, __ldg(p.seq_lens + b)) != 0) continue;
+        const int h = (int)(r % p.Hq);
+        const int t = (int)((r / p.Hq) % p.q_len);
+        __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(p.out) + b * p.out_stride[0] + t * p.out_stride[1] +
+                           h * p.out_stride[2];
+        for (int dv = 0; dv < p.Dv; ++dv) o[dv] = __float2bfloat16(0.f);
+        if (p.lse) p.lse[b * p.lse_stride[0] + t * p.lse_stride[1] + h * p.lse_stride[2]] = kNegInf;
+    }
 }
 
 // ------------------------------------------------------------------ combine
 //
-// Merge the split-KV partials of each query row: with per-split normalised
+// Merge the split-KV partials of each query row: with per-piece normalised
 // outputs o_i and log2-sum-exp values e_i, L = log2 sum_i 2^{e_i} and
 // out = sum_i 2^{e_i - L} o_i.  This is the rescale of the online recurrence
-// applied across whole splits ("Flywheel Attention", section 1; the reduction
-// kernel of "TokenSpeed-MLA 2.0.1", decode).  One warp per row, float4 loads.
+// applied across whole pieces ("Flywheel Attention", section 1; the reduction
+// kernel of "TokenSpeed-MLA 2.0.1", decode).  One warp per row, float4 loads;
+// rows whose unit fits one range were written by the attention kernel.
 
 template <int D>
-__global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ CombineParams p) {
+__global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ DecodeParams p) {
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int64_t rows = (int64_t)p.B * p.q_len * p.Hq;
@@ -573,13 +671,20 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ Co
     const int h = (int)(row % p.Hq);
     const int t = (int)((row / p.Hq) % p.q_len);
     const int b = (int)(row / ((int64_t)p.Hq * p.q_len));
-    int n = __ldg(p.seq_lens + b);
-    n = n < 0 ? 0 : (n > p.max_kv_len ? p.max_kv_len : n);
-    const int nsplit = n > 0 ? (n + p.chunk_tokens - 1) / p.chunk_tokens : 1;
-    if (nsplit <= 1) return;                         // written directly by the attention kernel
-    const float *lse_row = p.ws_lse + row * p.max_splits;
+    const int32_t *PB = p.plan + 2;
+    const int span = max(1, __ldg(p.plan + 1));
+    const int pb0 = __ldg(PB + b);
+    const int tb = (__ldg(PB + b + 1) - pb0) / p.units_per_row;
+    if (tb == 0) return;                             // empty row: written by the plan kernel
+    const int g = h / p.G;
+    const int rg = p.head_mode == 0 ? t / p.tokens_per_unit
+                                    : t * p.head_chunks + (h - g * p.G) / p.rows;
+    const int pstart = pb0 + (g * p.row_groups + rg) * tb;
+    const int npieces = (pstart + tb - 1) / span - pstart / span + 1;
+    if (npieces <= 1) return;
+    const float *lse_row = p.ws_lse + row * p.max_pieces;
     float m = kNegInf;
-    for (int i = lane; i < nsplit; i += 32) m = fmaxf(m, lse_row[i]);
+    for (int i = lane; i < npieces; i += 32) m = fmaxf(m, lse_row[i]);
     m = warp_max(m);
     constexpr int V = D / 32;                        // floats per lane
     float acc[V];
@@ -587,11 +692,10 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ Co
     for (int k = 0; k < V; ++k) acc[k] = 0.f;
     float wsum = 0.f;
     if (m != kNegInf) {
-        for (int i = 0; i < nsplit; ++i) {
-            const float e = lse_row[i];
-            const float w = ex2_approx(e - m);       // 0 for an empty split (e = -inf)
+        for (int i = 0; i < npieces; ++i) {
+            const float w = ex2_approx(lse_row[i] - m);  // 0 for an empty piece (e = -inf)
             wsum += w;
-            const float4 *src = reinterpret_cast<const float4 *>(p.ws_o + (row * p.max_splits + i) * D) + lane * (V / 4);
+            const float4 *src = reinterpret_cast<const float4 *>(p.ws_o + (row * p.max_pieces + i) * D) + lane * (V / 4);
 #pragma unroll
             for (int k = 0; k < V / 4; ++k) {
                 const float4 v = src[k];
@@ -604,23 +708,47 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ Co
     __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(p.out) + b * p.out_stride[0] + t * p.out_stride[1] +
                        h * p.out_stride[2] + lane * V;
 #pragma unroll
-    for (int k = 0; k < V; k += 2) {
-        __nv_bfloat162 v2 = __floats2bfloat162_rn(acc[k] * inv, acc[k + 1] * inv);
-        *reinterpret_cast<__nv_bfloat162 *>(o + k) = v2;
-    }
+    for (int k = 0; k < V; k += 2)
+        *reinterpret_cast<__nv_bfloat162 *>(o + k) = __floats2bfloat162_rn(acc[k] * inv, acc[k + 1] * inv);
     if (lane == 0 && p.lse)
         p.lse[b * p.lse_stride[0] + t * p.lse_stride[1] + h * p.lse_stride[2]] =
             (m == kNegInf) ? kNegInf : (m + __log2f(wsum)) * 0.69314718055994531f;
 }
 
-cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream) {
-    const int64_t rows = (int64_t)p.B * p.q_len * p.Hq;
-    const unsigned grid = (unsigned)((rows + 3) / 4);
-    if (grid == 0) return cudaSuccess;
-    if (p.Dv == 128) combine_kernel<128><<<grid, 128, 0, stream>>>(p);
-    else if (p.Dv == 256) combine_kernel<256><<<grid, 128, 0, stream>>>(p);
+}  // namespace
+
+size_t decode_smem_bytes(int head_dim, int rows) {
+    if (head_dim == 128) return rows == 16 ? DecodeCfg<128, 16>::kSmemBytes : DecodeCfg<128, 32>::kSmemBytes;
+    return rows == 16 ? DecodeCfg<256, 16>::kSmemBytes : DecodeCfg<256, 32>::kSmemBytes;
+}
+
+cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                          const CUtensorMap &tv, int head_dim, cudaStream_t stream,
+                          cudaEvent_t timing_start, cudaEvent_t timing_stop, int *launches) {
+    *launches = 0;
+    decode_plan_kernel<<<1, 1024, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    ++*launches;
+    if (timing_start) cudaEventRecord(timing_start, stream);
+    if (head_dim == 128 && p.rows == 16) e = launch_t<128, 16>(p, tq, tk, tv, stream);
+    else if (head_dim == 128 && p.rows == 32) e = launch_t<128, 32>(p, tq, tk, tv, stream);
+    else if (head_dim == 256 && p.rows == 16) e = launch_t<256, 16>(p, tq, tk, tv, stream);
+    else if (head_dim == 256 && p.rows == 32) e = launch_t<256, 32>(p, tq, tk, tv, stream);
     else return cudaErrorInvalidValue;
-    return cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    ++*launches;
+    if (timing_stop) cudaEventRecord(timing_stop, stream);
+    if (p.max_pieces > 1) {
+        const int64_t rows = (int64_t)p.B * p.q_len * p.Hq;
+        const unsigned grid = (unsigned)((rows + 3) / 4);
+        if (head_dim == 128) combine_kernel<128><<<grid, 128, 0, stream>>>(p);
+        else combine_kernel<256><<<grid, 128, 0, stream>>>(p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        ++*launches;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace fw

@@ -10,33 +10,38 @@ namespace fw {
 constexpr int kKvTile = 128;          // keys per KV tile (MMA M extent in decode, N in prefill)
 constexpr int kSoftmaxStartWarp = 2;  // decode: warps 2..5 run the softmax / epilogue
 
+constexpr int kDecodeMinSpan = 8;     // decode: fewest KV tiles one CTA range holds (auto mode)
+
 // One decode launch, fully resolved on the host.
+//
+// Scheduling: the (batch row, KV head, row group) units are laid end to end
+// in that order, each contributing ceil(n_b / 128) KV tiles; the plan kernel
+// writes the exclusive prefix PB[b] of these tile counts per batch row, the
+// total T and the range span.  CTA c then processes the global tile ranges
+// [r * span, (r + 1) * span) for r = c, c + grid, ...; the part of a unit
+// inside one range is a "piece" and writes a split-KV partial unless the unit
+// fits in a single range.
 struct DecodeParams {
     int B, q_len, Hq, Hkv, G, ps, max_pages, num_pages;
     int head_mode;        // 0: a unit holds whole head groups for tokens_per_unit tokens;
                           // 1: a unit holds `rows` consecutive heads of one token
     int rows;             // NQ: padded MMA N extent
-    int tokens_per_unit, heads_per_unit, head_chunks, row_groups;
-    int chunk_tokens, max_splits;
-    int64_t num_units;
+    int tokens_per_unit, heads_per_unit, head_chunks, row_groups, units_per_row;
+    int forced_span;      // KV tiles per range, 0 = auto
+    int min_span;         // lower bound of the auto span
+    int max_pieces;       // workspace slots per query row
+    int grid;             // CTAs of the attention kernel
+    int Dv;
+    int32_t *plan;        // [0] = T, [1] = span, [2 .. 2 + B] = PB
     const int32_t *block_table; int64_t bt_stride;
     const int32_t *seq_lens;
     void *out; int64_t out_stride[4];          // [B, q_len, Hq, Dv] bf16
     float *lse; int64_t lse_stride[3];         // [B, q_len, Hq] or nullptr
-    float *ws_o;                               // [B*q_len*Hq, max_splits, Dv]
-    float *ws_lse;                             // [B*q_len*Hq, max_splits] (log2 units)
+    float *ws_o;                               // [B*q_len*Hq, max_pieces, Dv]
+    float *ws_lse;                             // [B*q_len*Hq, max_pieces] (log2 units)
     float scale_log2;                          // scale * log2(e)
     uint64_t timeout_ns;
     int *status;                               // device status word
-};
-
-struct CombineParams {
-    int B, q_len, Hq, Dv, chunk_tokens, max_splits;
-    const int32_t *seq_lens;
-    const float *ws_o, *ws_lse;
-    void *out; int64_t out_stride[4];
-    float *lse; int64_t lse_stride[3];
-    int max_kv_len;
 };
 
 struct PrefillParams {
@@ -54,9 +59,10 @@ struct PrefillParams {
     int max_q_tiles;
 };
 
+// plan kernel + attention kernel + combine kernel, in stream order
 cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                          const CUtensorMap &tm_v, int head_dim, int grid, cudaStream_t stream);
-cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
+                          const CUtensorMap &tm_v, int head_dim, cudaStream_t stream,
+                          cudaEvent_t timing_start, cudaEvent_t timing_stop, int *launches);
 size_t decode_smem_bytes(int head_dim, int rows);
 
 cudaError_t launch_prefill(const PrefillParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,

@@ -76,22 +76,37 @@ def test_planner_wide_groups_are_chunked(fwlib):
 
 
 def test_planner_workspace_matches_pages_formula(fwlib):
-    """Dv + 1 FP32 values per row per split: at H*q_len a multiple of 128 this is
-    exactly TokenSpeed's B*128*ceil(H*q_len/128)*split*513*4 bytes (+256 alignment)."""
+    """Dv + 1 FP32 values per row per split: at H*q_len a multiple of 128 the
+    partials take exactly TokenSpeed's B*128*ceil(H*q_len/128)*split*513*4 bytes."""
     p = fwlib.plan_decode(2, 4, 128, 1, 512, 81920, num_sms=152)
-    assert p["max_splits"] > 1
-    assert p["workspace_bytes"] == planning.split_workspace_bytes(2, 128, 4, p["max_splits"], 512) + 256
+    assert p["max_pieces"] > 1
+    assert p["partial_bytes"] == planning.split_workspace_bytes(2, 128, 4, p["max_pieces"], 512)
+    assert p["workspace_bytes"] >= p["partial_bytes"] + (2 + 3) * 4
     p1 = fwlib.plan_decode(2, 1, 8, 2, 128, 200, num_sms=152)
-    assert p1["max_splits"] == 1 and p1["workspace_bytes"] == 0
+    assert p1["partial_bytes"] == 2 * 8 * p1["max_pieces"] * 129 * 4
 
 
-def test_planner_splits_cover_the_length_bound(fwlib):
+def test_planner_piece_bound(fwlib):
+    """A unit of t tiles meets at most ceil(t / span) + 1 CTA ranges."""
     for max_len in (1, 127, 128, 129, 4096, 32768, 81920):
         p = fwlib.plan_decode(64, 1, 40, 8, 128, max_len, num_sms=152)
-        assert p["chunk_tokens"] % 128 == 0 and p["chunk_tokens"] >= 128
-        assert p["max_splits"] == -(-max_len // p["chunk_tokens"])
-        assert p["num_units"] == 64 * 8 * p["row_groups"] * p["max_splits"]
-        assert 1 <= p["grid"] <= 152
+        tiles = -(-max_len // 128)
+        assert p["min_span_tiles"] == 8
+        assert p["max_pieces"] == -(-tiles // 8) + 1
+        assert p["num_units"] == 64 * 8 * p["row_groups"]
+        assert p["grid"] == 152
+
+
+def piece_count(start, tiles, span):
+    """Ranges [r*span, (r+1)*span) that tiles [start, start + tiles) meet."""
+    return len({t // span for t in range(start, start + tiles)})
+
+
+def test_piece_bound_holds_for_any_alignment():
+    for span in (1, 3, 8, 100):
+        for tiles in (1, 2, 7, 8, 9, 64, 257):
+            worst = max(piece_count(s, tiles, span) for s in range(span))
+            assert worst <= -(-tiles // span) + 1
 
 
 def test_qwen3_14b_plan(fwlib):
@@ -106,7 +121,7 @@ def test_forced_chunk_option(fwlib):
     fwlib.set_option(fwlib.FW_OPT_DECODE_CHUNK_TOKENS, 256)
     try:
         p = fwlib.plan_decode(2, 1, 8, 2, 128, 1000, num_sms=152)
-        assert p["chunk_tokens"] == 256 and p["max_splits"] == 4
+        assert p["min_span_tiles"] == 2 and p["max_pieces"] == 4 + 1
     finally:
         fwlib.set_option(fwlib.FW_OPT_DECODE_CHUNK_TOKENS, 0)
     with pytest.raises(fwlib.FwError):
