@@ -109,6 +109,37 @@ fw_status_t fw_paged_decode(const fw_tensor_t *q, const fw_tensor_t *k_cache,
                             fw_tensor_t *out, fw_tensor_t *lse, fw_stream_t stream);
 
 /*
+ * fw_paged_decode for callers that cannot allocate device memory.  The pages
+ * have no counterpart to this entry point; it exists for users of the library.
+ *
+ * Who needs it: code that runs where cudaMalloc is off limits -- a plugin whose
+ * host runtime owns every byte of device memory and forbids allocation in its
+ * execute step, or a latency-critical loop that cannot take the implicit
+ * device synchronisation or the out-of-memory failure an allocation may
+ * bring.  fw_paged_decode may grow an internal workspace with cudaMalloc the
+ * first time it sees larger shapes; this variant never allocates anything.
+ *
+ * Arguments, layouts, supported shapes and results are those of
+ * fw_paged_decode; a workspace set with fw_set_workspace() is not used.  Its
+ * scratch (the tile prefix table and the split-KV partials) is a fixed
+ * 64 MiB array in the library's device image, held by every GPU that loads
+ * the library until the process exits.  Shapes whose scratch
+ * (fw_decode_plan_t.workspace_bytes) exceeds 64 MiB return FW_ERR_WORKSPACE
+ * and launch nothing.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  Every call shares the one array and nothing in
+ * it needs to start at zero (each value is written before it is read within a
+ * call), but calls whose kernels overlap on the GPU -- different streams, or
+ * several host threads -- race on it: order them.
+ */
+fw_status_t fw_paged_decode_noalloc(const fw_tensor_t *q, const fw_tensor_t *k_cache,
+                                    const fw_tensor_t *v_cache, const fw_tensor_t *block_table,
+                                    const fw_tensor_t *seq_lens, float scale,
+                                    fw_tensor_t *out, fw_tensor_t *lse, fw_stream_t stream);
+
+/*
  * Workspace bytes fw_paged_decode needs for these shapes (data pointers are
  * not read).  Writes the size to *bytes.  It holds the tile prefix table
  * (B + 3 int32) and rows * max_pieces * (Dv + 1) * 4 bytes of partials, with

@@ -62,6 +62,8 @@ def load_library(path: Optional[str] = None):
     S = ctypes.c_int
     lib.fw_paged_decode.restype = S
     lib.fw_paged_decode.argtypes = [P, P, P, P, P, ctypes.c_float, P, P, ctypes.c_void_p]
+    lib.fw_paged_decode_noalloc.restype = S
+    lib.fw_paged_decode_noalloc.argtypes = [P, P, P, P, P, ctypes.c_float, P, P, ctypes.c_void_p]
     lib.fw_paged_decode_workspace_size.restype = S
     lib.fw_paged_decode_workspace_size.argtypes = [P, P, P, P, ctypes.POINTER(ctypes.c_size_t)]
     lib.fw_varlen_prefill.restype = S
@@ -132,6 +134,22 @@ def paged_decode(q, k_cache, v_cache, block_table, seq_lens, scale, out=None, ls
     fo, fl = as_fw_tensor(out), as_fw_tensor(lse)
     _check(lib.fw_paged_decode(*[_ref(a) for a in args], ctypes.c_float(scale), _ref(fo), _ref(fl),
                                _stream_handle(stream)))
+    return out, lse
+
+
+def paged_decode_noalloc(q, k_cache, v_cache, block_table, seq_lens, scale, out, lse=None, stream=None):
+    """fw_paged_decode_noalloc: the same decode without any device allocation.
+
+    For callers that may not allocate device memory (a runtime that owns the
+    whole pool, a loop that cannot afford cudaMalloc's synchronisation): the
+    output buffers are the caller's, and the scratch is the library's fixed
+    64 MiB device array.  Calls overlapping on the GPU race on that array.
+    """
+    lib = load_library()
+    args = [as_fw_tensor(x) for x in (q, k_cache, v_cache, block_table, seq_lens)]
+    fo, fl = as_fw_tensor(out), as_fw_tensor(lse)
+    _check(lib.fw_paged_decode_noalloc(*[_ref(a) for a in args], ctypes.c_float(scale), _ref(fo), _ref(fl),
+                                       _stream_handle(stream)))
     return out, lse
 
 

@@ -45,6 +45,7 @@ struct DeviceState {
     size_t ws_bytes = 0;
     void *user_ws = nullptr;        // caller workspace
     size_t user_ws_bytes = 0;
+    void *noalloc_scratch = nullptr; // device address of g_noalloc_scratch on this device
 };
 
 std::mutex g_mu;
@@ -371,9 +372,14 @@ fw_status_t fw_paged_decode_workspace_size(const fw_tensor_t *q, const fw_tensor
     return ok();
 }
 
-fw_status_t fw_paged_decode(const fw_tensor_t *q, const fw_tensor_t *k_cache, const fw_tensor_t *v_cache,
-                            const fw_tensor_t *block_table, const fw_tensor_t *seq_lens, float scale,
-                            fw_tensor_t *out, fw_tensor_t *lse, fw_stream_t stream_) {
+// Shared body of the decode entry points.  `fixed_ws` selects where the
+// scratch comes from: nullptr = the workspace fw_set_workspace() set or the
+// internal buffer (fw_paged_decode); otherwise that device range of
+// `fixed_bytes` bytes, which is never grown (fw_paged_decode_noalloc).
+static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_cache, const fw_tensor_t *v_cache,
+                                     const fw_tensor_t *block_table, const fw_tensor_t *seq_lens, float scale,
+                                     fw_tensor_t *out, fw_tensor_t *lse, fw_stream_t stream_,
+                                     void *(*fixed_ws)(DeviceState *, fw_status_t *), size_t fixed_bytes) {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     if (fw_status_t s = decode_shapes(q, k_cache, v_cache, block_table)) return s;
     if (fw_status_t s = check_tensor(seq_lens, "seq_lens", 1, FW_I32)) return s;
@@ -415,7 +421,16 @@ fw_status_t fw_paged_decode(const fw_tensor_t *q, const fw_tensor_t *k_cache, co
                                     max_pages * ps, d->num_sms, &pl))
         return s;
     void *ws = nullptr;
-    if (fw_status_t s = get_workspace(d, (size_t)pl.workspace_bytes, stream, &ws)) return s;
+    if (fixed_ws) {
+        if ((size_t)pl.workspace_bytes > fixed_bytes)
+            return fail(FW_ERR_WORKSPACE, "these shapes need %lld bytes of decode scratch; the fixed scratch "
+                        "holds %zu bytes", (long long)pl.workspace_bytes, fixed_bytes);
+        fw_status_t st = FW_OK;
+        ws = fixed_ws(d, &st);
+        if (st != FW_OK) return st;
+    } else if (fw_status_t s = get_workspace(d, (size_t)pl.workspace_bytes, stream, &ws)) {
+        return s;
+    }
 
     fw::DecodeParams p{};
     p.B = (int)B; p.q_len = (int)q_len; p.Hq = (int)Hq; p.Hkv = (int)Hkv; p.G = pl.group;
@@ -479,6 +494,48 @@ fw_status_t fw_paged_decode(const fw_tensor_t *q, const fw_tensor_t *k_cache, co
     if (e != cudaSuccess) return fail(FW_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
     if (ev0) g_timed.push_back({ev0, ev1});
     return ok();
+}
+
+fw_status_t fw_paged_decode(const fw_tensor_t *q, const fw_tensor_t *k_cache, const fw_tensor_t *v_cache,
+                            const fw_tensor_t *block_table, const fw_tensor_t *seq_lens, float scale,
+                            fw_tensor_t *out, fw_tensor_t *lse, fw_stream_t stream) {
+    return paged_decode_impl(q, k_cache, v_cache, block_table, seq_lens, scale, out, lse, stream, nullptr, 0);
+}
+
+// ----------------------------------------------------- decode without allocation
+//
+// Fixed decode scratch for fw_paged_decode_noalloc: the tile prefix table and
+// the split-KV partials of one call.  It is part of the library's device
+// image, so every GPU that loads the library holds these 64 MiB until the
+// process exits.  Host code must not hand the array's name to a kernel (on
+// the host it is only a stand-in symbol); the device address is looked up
+// below, once per device, and cached.
+}  // extern "C"
+
+static constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+static void *noalloc_scratch(DeviceState *d, fw_status_t *st) {
+    if (!d->noalloc_scratch) {
+        void *ptr = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess || !ptr) {
+            *st = fail(FW_ERR_CUDA, "device address of the fixed decode scratch: %s", cudaGetErrorString(e));
+            return nullptr;
+        }
+        d->noalloc_scratch = ptr;
+    }
+    *st = FW_OK;
+    return d->noalloc_scratch;
+}
+
+extern "C" {
+
+fw_status_t fw_paged_decode_noalloc(const fw_tensor_t *q, const fw_tensor_t *k_cache, const fw_tensor_t *v_cache,
+                                    const fw_tensor_t *block_table, const fw_tensor_t *seq_lens, float scale,
+                                    fw_tensor_t *out, fw_tensor_t *lse, fw_stream_t stream) {
+    return paged_decode_impl(q, k_cache, v_cache, block_table, seq_lens, scale, out, lse, stream,
+                             noalloc_scratch, kNoAllocScratchBytes);
 }
 
 fw_status_t fw_varlen_prefill(const fw_tensor_t *q, const fw_tensor_t *k, const fw_tensor_t *v,
