@@ -540,10 +540,100 @@ fw_status_t fw_paged_decode_noalloc(const fw_tensor_t *q, const fw_tensor_t *k_c
 
 fw_status_t fw_varlen_prefill(const fw_tensor_t *q, const fw_tensor_t *k, const fw_tensor_t *v,
                               const fw_tensor_t *cu_seqlens_q, const fw_tensor_t *cu_seqlens_k, int causal,
-                              float scale, fw_tensor_t *out, fw_tensor_t *lse, fw_stream_t stream) {
-    (void)q; (void)k; (void)v; (void)cu_seqlens_q; (void)cu_seqlens_k; (void)causal; (void)scale;
-    (void)out; (void)lse; (void)stream;
-    return fail(FW_ERR_UNSUPPORTED, "varlen prefill is not built yet");
+                              float scale, fw_tensor_t *out, fw_tensor_t *lse, fw_stream_t stream_) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (fw_status_t s = check_tensor(q, "q", 3, FW_BF16)) return s;
+    if (fw_status_t s = check_tensor(k, "k", 3, FW_BF16)) return s;
+    if (fw_status_t s = check_tensor(v, "v", 3, FW_BF16)) return s;
+    if (fw_status_t s = check_tensor(cu_seqlens_q, "cu_seqlens_q", 1, FW_I32)) return s;
+    if (fw_status_t s = check_tensor(cu_seqlens_k, "cu_seqlens_k", 1, FW_I32)) return s;
+    if (fw_status_t s = check_tensor(out, "out", 3, FW_BF16)) return s;
+    if (fw_status_t s = check_tensor(lse, "lse", 2, FW_F32, true)) return s;
+    const int64_t total_q = q->shape[0], Hq = q->shape[1], Dk = q->shape[2];
+    const int64_t total_k = k->shape[0], Hkv = k->shape[1];
+    const int64_t Dv = v->shape[2];
+    const int64_t B = cu_seqlens_q->shape[0] - 1;
+    if (k->shape[2] != Dk) return fail(FW_ERR_INVALID_ARG, "k head dim must match q");
+    if (v->shape[0] != total_k || v->shape[1] != Hkv) return fail(FW_ERR_INVALID_ARG, "v must be [total_k, Hkv, Dv]");
+    if (B < 0 || cu_seqlens_k->shape[0] != B + 1)
+        return fail(FW_ERR_INVALID_ARG, "cu_seqlens_q and cu_seqlens_k must both hold B + 1 entries");
+    if ((B >= 0 && cu_seqlens_q->stride[0] != 1 && B + 1 > 1) || (cu_seqlens_k->stride[0] != 1 && B + 1 > 1))
+        return fail(FW_ERR_INVALID_ARG, "cu_seqlens must be contiguous");
+    if (out->shape[0] != total_q || out->shape[1] != Hq || out->shape[2] != Dv)
+        return fail(FW_ERR_INVALID_ARG, "out must be [total_q, Hq, Dv]");
+    if (lse && (lse->shape[0] != total_q || lse->shape[1] != Hq))
+        return fail(FW_ERR_INVALID_ARG, "lse must be [total_q, Hq]");
+    if (Hkv < 1 || Hq % Hkv != 0) return fail(FW_ERR_INVALID_ARG, "Hq must be a multiple of Hkv");
+    if (!std::isfinite(scale)) return fail(FW_ERR_INVALID_ARG, "scale must be finite");
+    if (!(Dk == Dv && (Dk == 128 || Dk == 256)))
+        return fail(FW_ERR_UNSUPPORTED, "prefill head dims (Dk=%lld, Dv=%lld): supported Dk = Dv in {128, 256}",
+                    (long long)Dk, (long long)Dv);
+    if (total_q >= (1LL << 31) || total_k >= (1LL << 31)) return fail(FW_ERR_UNSUPPORTED, "too many tokens");
+    if (B == 0 || total_q == 0) return ok();
+    if (fw_status_t s = check_tma_layout(q, "q")) return s;
+    if (fw_status_t s = check_tma_layout(k, "k")) return s;
+    if (fw_status_t s = check_tma_layout(v, "v")) return s;
+    if (fw_status_t s = check_tma_layout(out, "out")) return s;   // rows are written as 16-byte vectors
+    if (lse && reinterpret_cast<uintptr_t>(lse->data) % 4) return fail(FW_ERR_INVALID_ARG, "lse misaligned");
+    const int64_t capacity = ((total_q + 127) / 128 + B) * Hq;
+    if (capacity >= (1LL << 31)) return fail(FW_ERR_UNSUPPORTED, "too many query tiles");
+
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState *d = nullptr;
+    if (fw_status_t s = device_state(&d)) return s;
+    const int64_t plan_bytes = ((B + 3) * 4 + 255) / 256 * 256;
+    const int64_t ws_bytes = plan_bytes + capacity * 4;
+    void *ws = nullptr;
+    if (fw_status_t s = get_workspace(d, (size_t)ws_bytes, stream, &ws)) return s;
+
+    fw::PrefillParams p{};
+    p.B = (int)B; p.Hq = (int)Hq; p.Hkv = (int)Hkv; p.G = (int)(Hq / Hkv); p.causal = causal ? 1 : 0;
+    p.Dv = (int)Dv;
+    p.total_q = total_q; p.total_k = total_k;
+    p.cu_q = static_cast<const int32_t *>(cu_seqlens_q->data);
+    p.cu_k = static_cast<const int32_t *>(cu_seqlens_k->data);
+    p.out = out->data;
+    for (int i = 0; i < 3; ++i) p.out_stride[i] = out->stride[i];
+    p.lse = lse ? static_cast<float *>(lse->data) : nullptr;
+    if (lse) for (int i = 0; i < 2; ++i) p.lse_stride[i] = lse->stride[i];
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.timeout_ns = (uint64_t)g_opt_timeout_ms * 1000000ull;
+    p.status = d->status;
+    p.plan = static_cast<int32_t *>(ws);
+    p.list = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + plan_bytes);
+    p.list_capacity = capacity;
+    int64_t grid = d->num_sms;
+    if (g_opt_max_ctas > 0 && grid > g_opt_max_ctas) grid = g_opt_max_ctas;
+    p.grid = (int)grid;
+
+    CUtensorMap tq, tk, tv;
+    {
+        const uint64_t dq[3] = {(uint64_t)Dk, (uint64_t)Hq, (uint64_t)total_q};
+        const uint64_t sq[2] = {(uint64_t)q->stride[1] * 2, (uint64_t)q->stride[0] * 2};
+        const uint32_t box[3] = {64, 1, 128};
+        if (fw_status_t s = encode_bf16(&tq, q->data, 3, dq, sq, box, "q")) return s;
+        if (total_k > 0) {
+            const uint64_t dk[3] = {(uint64_t)Dk, (uint64_t)Hkv, (uint64_t)total_k};
+            const uint64_t sk[2] = {(uint64_t)k->stride[1] * 2, (uint64_t)k->stride[0] * 2};
+            if (fw_status_t s = encode_bf16(&tk, k->data, 3, dk, sk, box, "k")) return s;
+            const uint64_t dv[3] = {(uint64_t)Dv, (uint64_t)Hkv, (uint64_t)total_k};
+            const uint64_t sv[2] = {(uint64_t)v->stride[1] * 2, (uint64_t)v->stride[0] * 2};
+            if (fw_status_t s = encode_bf16(&tv, v->data, 3, dv, sv, box, "v")) return s;
+        } else {
+            // No keys anywhere: every query tile walks zero KV tiles, so these
+            // maps are never used; they only need to be valid descriptors.
+            tk = tq;
+            tv = tq;
+        }
+    }
+    cudaEvent_t ev0 = nullptr, ev1 = nullptr;
+    if (g_opt_timing) { ev0 = pooled_event(); ev1 = pooled_event(); }
+    int launched = 0;
+    cudaError_t e = fw::launch_prefill(p, tq, tk, tv, (int)Dk, stream, ev0, ev1, &launched);
+    g_launches.fetch_add(launched);
+    if (e != cudaSuccess) return fail(FW_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
+    if (ev0) g_timed.push_back({ev0, ev1});
+    return ok();
 }
 
 }  // extern "C"

@@ -44,19 +44,23 @@ struct DecodeParams {
     int *status;                               // device status word
 };
 
+// One varlen prefill launch.  The plan kernel lists the units (sequence,
+// query head, pair of consecutive 128-row query tiles) longest first; CTA c
+// takes list entries c, 2*grid-1-c, 2*grid+c, ... (a snake over the sorted
+// list, which balances the sums).
 struct PrefillParams {
-    int B, Hq, Hkv, G, causal;
+    int B, Hq, Hkv, G, causal, Dv;
     int64_t total_q, total_k;
     const int32_t *cu_q, *cu_k;
     void *out; int64_t out_stride[3];          // [total_q, Hq, Dv] bf16
-    float *lse; int64_t lse_stride[2];
+    float *lse; int64_t lse_stride[2];         // [total_q, Hq] or nullptr
     float scale_log2;
     uint64_t timeout_ns;
     int *status;
-    int32_t *work_counter;                      // zeroed before launch
-    const int32_t *work_list;                   // planned (seq, q_tile) list, longest first
-    int32_t *work_count;                        // number of entries (device)
-    int max_q_tiles;
+    int32_t *plan;        // [0] = entries, [1] = pairs, [2 .. 2 + B] = pair prefix PP
+    int32_t *list;        // entries pair_index * Hq + head, sorted by cost, longest first
+    int64_t list_capacity;
+    int grid;
 };
 
 // plan kernel + attention kernel + combine kernel, in stream order
@@ -65,10 +69,9 @@ cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &tm_q, const 
                           cudaEvent_t timing_start, cudaEvent_t timing_stop, int *launches);
 size_t decode_smem_bytes(int head_dim, int rows);
 
+// plan kernel + attention kernel, in stream order
 cudaError_t launch_prefill(const PrefillParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                           const CUtensorMap &tm_v, int head_dim, int grid, int64_t plan_entries,
-                           cudaStream_t stream);
-cudaError_t launch_prefill_plan(const PrefillParams &p, int32_t *work_list, int32_t *work_count,
-                                int64_t capacity, cudaStream_t stream);
+                           const CUtensorMap &tm_v, int head_dim, cudaStream_t stream,
+                           cudaEvent_t timing_start, cudaEvent_t timing_stop, int *launches);
 
 }  // namespace fw

@@ -1,0 +1,589 @@
+// Ragged (varlen) prefill, sm_103a: packed Q [total_q, Hq, D], K/V
+// [total_k, Hkv, D] described by cumulative sequence lengths, causal
+// (bottom-right aligned) or not ("TokenSpeed-MLA 2.0.1", MLA Prefill: ragged
+// varlen FMHA without padding, Q and KV packs may differ).
+//
+// Orientation: a 128-row query tile is the MMA M axis, a 128-key tile is N:
+//   S [128 x 128]  = Q_tile * K_tile^T          (tcgen05, FP32 in TMEM)
+//   O [128 x D]   += P [128 x 128] * V_tile      (tcgen05, FP32 in TMEM)
+// with the online softmax of "Flywheel Attention", section 1, in base 2 and
+// with a conditional rescale (the base moves only when a row max rises by
+// more than 8 log2 units).
+//
+// D = 128: a unit is two consecutive query tiles of one head that share every
+// K/V tile load; S and O of both live in TMEM (4 x 128 columns) and two
+// softmax warpgroups alternate with the tensor core: while one group turns
+// its S into P, the MMA warp runs the other tile's PV and QK ("Flywheel
+// Attention", section 1: two compute groups alternate so that one's softmax
+// overlaps the other's matmuls).  D = 256: one query tile per unit, S double
+// buffered (2 x 128 columns) next to O (256 columns).
+//
+// Warp roles: warp 0 TMA producer (Q tiles, then K_j / V_j through a ring of
+// shared-memory slots), warp 1 MMA issuer and TMEM owner, then one warpgroup
+// per query tile (thread = query row: the row max and sum are thread-local).
+#include <cuda_bf16.h>
+
+#include "fw_internal.h"
+#include "fw_ptx.cuh"
+
+namespace fw {
+namespace {
+
+constexpr float kNegInf = -__builtin_huge_valf();
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
+constexpr int kQTile = 128;
+constexpr int kCostBins = 4096;
+
+template <int D>
+struct PrefillCfg {
+    static constexpr int kNumQ = (D == 128) ? 2 : 1;           // query tiles per unit
+    static constexpr int kChunks = D / 64;
+    static constexpr int kChunkBytes = 128 * 128;              // 128 rows x 64 bf16 columns
+    static constexpr int kTileBytes = 128 * D * 2;              // one Q, K or V tile
+    static constexpr int kSlots = (D == 128) ? 3 : 2;           // K/V ring slots
+    static constexpr int kPBytes = 128 * kKvTile * 2;
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffRing = kOffQ + kNumQ * kTileBytes;
+    static constexpr int kOffP = kOffRing + kSlots * kTileBytes;
+    static constexpr int kOffBar = kOffP + kNumQ * kPBytes;
+    static constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 1;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+    static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA exceeded");
+    static constexpr int kThreads = 64 + kNumQ * 128;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kKvTile, false, false);
+    static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, false, true);
+    // TMEM columns: S buffers then O accumulators
+    __device__ static constexpr uint32_t s_col(int tile, uint32_t cnt) {
+        return kNumQ == 2 ? (uint32_t)tile * 128u : (cnt & 1u) * 128u;
+    }
+    __device__ static constexpr uint32_t o_col(int tile) { return 256u + (uint32_t)tile * 128u; }
+};
+
+__device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
+
+struct Seq {
+    int q0, k0, Lq, Lk;
+    bool ok;
+};
+
+__device__ __forceinline__ Seq load_seq(const PrefillParams &p, int i) {
+    Seq s;
+    s.q0 = __ldg(p.cu_q + i);
+    s.k0 = __ldg(p.cu_k + i);
+    const int q1 = __ldg(p.cu_q + i + 1);
+    const int k1 = __ldg(p.cu_k + i + 1);
+    s.ok = s.q0 >= 0 && s.k0 >= 0 && q1 >= s.q0 && k1 >= s.k0 && q1 <= p.total_q && k1 <= p.total_k;
+    s.Lq = s.ok ? q1 - s.q0 : 0;
+    s.Lk = s.ok ? k1 - s.k0 : 0;
+    return s;
+}
+
+// Keys a query tile sees: [0, kv_limit); the last row decides for causal.
+__device__ __forceinline__ int tile_kv_limit(const PrefillParams &p, const Seq &s, int t) {
+    if (t * kQTile >= s.Lq) return 0;
+    if (!p.causal) return s.Lk;
+    const int q_last = min(s.Lq, (t + 1) * kQTile) - 1;
+    return max(0, min(s.Lk, q_last + s.Lk - s.Lq + 1));
+}
+
+__device__ __forceinline__ int tile_kv_tiles(const PrefillParams &p, const Seq &s, int t) {
+    return ceil_div_i(tile_kv_limit(p, s, t), kKvTile);
+}
+
+// One unit of work: (sequence, head, pair of query tiles 2*pair and 2*pair+1).
+struct PUnit {
+    int seq, h, g;
+    Seq s;
+    int tile[2];       // query tile index, -1 if absent
+    int nkv[2];        // KV tiles each query tile walks
+    int nmax;
+};
+
+__device__ __forceinline__ void decode_entry(const PrefillParams &p, int e, PUnit &u, int num_q) {
+    const int32_t *PP = p.plan + 2;
+    const int gp = e / p.Hq;
+    u.h = e - gp * p.Hq;
+    u.g = u.h / p.G;
+    int lo = 0, hi = p.B - 1;                          // largest seq with PP[seq] <= gp
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(PP + mid) <= gp) lo = mid; else hi = mid - 1;
+    }
+    u.seq = lo;
+    u.s = load_seq(p, lo);
+    const int pair = gp - __ldg(PP + lo);
+    const int nqt = ceil_div_i(u.s.Lq, kQTile);
+    u.nmax = 0;
+    for (int x = 0; x < 2; ++x) {
+        const int t = num_q == 2 ? 2 * pair + x : (x == 0 ? pair : -1);
+        u.tile[x] = (t >= 0 && t < nqt) ? t : -1;
+        u.nkv[x] = u.tile[x] >= 0 ? tile_kv_tiles(p, u.s, t) : 0;
+        u.nmax = max(u.nmax, u.nkv[x]);
+    }
+}
+
+// Static snake over the cost-sorted list: entry index of this CTA's k-th unit.
+__device__ __forceinline__ int snake_index(int k, int grid) {
+    return k * grid + ((k & 1) ? (grid - 1 - (int)blockIdx.x) : (int)blockIdx.x);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+template <int D>
+__global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
+varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
+    using C = PrefillCfg<D>;
+    constexpr int NQ = C::kNumQ;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sQ = smem + C::kOffQ;
+    uint8_t *sRing = smem + C::kOffRing;
+    uint8_t *sP = smem + C::kOffP;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
+    uint64_t *slot_full = bars;
+    uint64_t *slot_empty = slot_full + C::kSlots;
+    uint64_t *q_full = slot_empty + C::kSlots;      // [1]
+    uint64_t *q_empty = q_full + 2;                  // [1]
+    uint64_t *s_full = q_empty + 2;                  // [2]
+    uint64_t *p_full = s_full + 2;                   // [2]
+    uint64_t *pv_done = p_full + 2;                  // [2]
+    uint64_t *drain = pv_done + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int count = __ldg(p.plan + 0);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::kSlots; ++i) { mbar_init(&slot_full[i], 1); mbar_init(&slot_empty[i], 1); }
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
+        for (int i = 0; i < 2; ++i) { mbar_init(&s_full[i], 1); mbar_init(&p_full[i], 4); mbar_init(&pv_done[i], 1); }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_q); tma_prefetch_desc(&tm_k); tma_prefetch_desc(&tm_v);
+    }
+    if (warp == 1) { tmem_alloc(tmem_slot, C::kTmemCols); tmem_relinquish(); }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtx wc{p.status, p.timeout_ns, abort_flag};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            uint32_t rp = 0, nu = 0, issued = 0;
+            bool ok = true;
+            for (int k = 0; ok; ++k, ++nu) {
+                const int idx = snake_index(k, p.grid);
+                if (idx >= count) break;
+                PUnit u;
+                decode_entry(p, __ldg(p.list + idx), u, NQ);
+                if (!mbar_wait(q_empty, (nu & 1) ^ 1, wc)) break;
+                uint32_t bytes = 0;
+                for (int x = 0; x < NQ; ++x) if (u.tile[x] >= 0) bytes += C::kTileBytes;
+                mbar_arrive_expect_tx(q_full, bytes);
+                for (int x = 0; x < NQ; ++x) {
+                    if (u.tile[x] < 0) continue;
+#pragma unroll
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_3d(smem_u32(sQ + x * C::kTileBytes + c * C::kChunkBytes), &tm_q, q_full,
+                                    c * 64, u.h, u.s.q0 + u.tile[x] * kQTile);
+                }
+                // K_j and V_j of the unit, in that order, through the slot ring.
+                for (int j = 0; j < u.nmax && ok; ++j) {
+                    for (int kv = 0; kv < 2; ++kv, ++rp) {
+                        const int sl = rp % C::kSlots;
+                        ok = mbar_wait(&slot_empty[sl], ((rp / C::kSlots) & 1) ^ 1, wc);
+                        if (!ok) break;
+                        mbar_arrive_expect_tx(&slot_full[sl], C::kTileBytes);
+#pragma unroll
+                        for (int c = 0; c < C::kChunks; ++c)
+                            tma_load_3d(smem_u32(sRing + sl * C::kTileBytes + c * C::kChunkBytes),
+                                        kv == 0 ? (const void *)&tm_k : (const void *)&tm_v, &slot_full[sl],
+                                        c * 64, u.g, u.s.k0 + j * kKvTile);
+                        issued = rp + 1;
+                    }
+                }
+            }
+            for (uint32_t k = 0; k < (uint32_t)C::kSlots && k < issued; ++k) {
+                const uint32_t r = issued - 1 - k;
+                mbar_wait_drain(&slot_full[r % C::kSlots], (r / C::kSlots) & 1, wc);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ----------------------------------------------------------------- MMA
+        if (lane == 0) {
+            uint32_t rp = 0, nu = 0;
+            uint32_t qk_cnt[2] = {0, 0}, pv_cnt[2] = {0, 0};
+            auto wait_slot = [&](uint32_t r) {
+                return mbar_wait(&slot_full[r % C::kSlots], (r / C::kSlots) & 1, wc);
+            };
+            auto issue_qk = [&](int x, uint32_t r_k) {
+                const uint32_t sc = C::s_col(x, qk_cnt[x]);
+                const uint32_t q_base = smem_u32(sQ + x * C::kTileBytes);
+                const uint32_t k_base = smem_u32(sRing + (r_k % C::kSlots) * C::kTileBytes);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t a = sdesc_sw128(q_base + (kk >> 2) * C::kChunkBytes + (kk & 3) * 32, 16, 1024);
+                    const uint64_t b = sdesc_sw128(k_base + (kk >> 2) * C::kChunkBytes + (kk & 3) * 32, 16, 1024);
+                    mma_bf16_ss(tmem + sc, a, b, C::kIdescQK, kk > 0 ? 1u : 0u);
+                }
+                const int sb = NQ == 2 ? x : (int)(qk_cnt[x] & 1u);
+                mma_commit(&s_full[sb]);
+                ++qk_cnt[x];
+            };
+            auto issue_pv = [&](int x, uint32_t r_v, bool first) -> bool {
+                const uint32_t pc = pv_cnt[x];
+                if (!mbar_wait(&p_full[NQ == 2 ? x : 0], (pc & 1), wc)) return false;
+                tc_fence_after();
+                const uint32_t p_base = smem_u32(sP + x * C::kPBytes);
+                const uint32_t v_base = smem_u32(sRing + (r_v % C::kSlots) * C::kTileBytes);
+#pragma unroll
+                for (int kk = 0; kk < kKvTile / 16; ++kk) {
+                    const uint64_t a = sdesc_sw128(p_base + (kk >> 2) * C::kChunkBytes + (kk & 3) * 32, 16, 1024);
+                    const uint64_t b = sdesc_sw128(v_base + kk * 16 * 128, C::kChunkBytes, 1024);
+                    mma_bf16_ss(tmem + C::o_col(x), a, b, C::kIdescPV, (first && kk == 0) ? 0u : 1u);
+                }
+                mma_commit(&pv_done[x]);
+                ++pv_cnt[x];
+                return true;
+            };
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int idx = snake_index(k, p.grid);
+                if (idx >= count) break;
+                PUnit u;
+                decode_entry(p, __ldg(p.list + idx), u, NQ);
+                if (!mbar_wait(q_full, nu & 1, wc)) break;
+                tc_fence_after();
+                // K_j sits at ring position r0 + 2j, V_j at r0 + 2j + 1.  A slot is
+                // released (commit) right after the last MMA reading it is issued,
+                // so the in-order producer never waits on a slot the MMA warp
+                // still needs to reach.
+                const uint32_t r0 = rp;
+                // the query tile that reads KV tile jj last (tile 1 walks at least as far)
+                auto last_user = [&](int jj) { return (NQ == 2 && jj < u.nkv[1]) ? 1 : 0; };
+                if (u.nmax > 0) {
+                    if (!wait_slot(r0)) break;
+                    tc_fence_after();
+                    for (int x = 0; x < NQ; ++x)
+                        if (u.nkv[x] > 0) issue_qk(x, r0);
+                    mma_commit(&slot_empty[r0 % C::kSlots]);
+                    if (NQ == 1 && u.nkv[0] > 1) {
+                        if (!wait_slot(r0 + 2)) break;
+                        tc_fence_after();
+                        issue_qk(0, r0 + 2);
+                        mma_commit(&slot_empty[(r0 + 2) % C::kSlots]);
+                    }
+                }
+                for (int j = 0; j < u.nmax && ok; ++j) {
+                    const uint32_t rv = r0 + 2 * j + 1;
+                    if (!wait_slot(rv)) { ok = false; break; }
+                    tc_fence_after();
+                    for (int x = 0; x < NQ; ++x) {
+                        if (j >= u.nkv[x]) continue;
+                        if (!issue_pv(x, rv, j == 0)) { ok = false; break; }
+                        if (x == last_user(j)) mma_commit(&slot_empty[rv % C::kSlots]);
+                        const int jn = NQ == 2 ? j + 1 : j + 2;    // next QK of this tile
+                        if (jn < u.nkv[x]) {
+                            const uint32_t rk = r0 + 2 * jn;
+                            if (!wait_slot(rk)) { ok = false; break; }
+                            tc_fence_after();
+                            issue_qk(x, rk);
+                            if (x == last_user(jn)) mma_commit(&slot_empty[rk % C::kSlots]);
+                        }
+                    }
+                }
+                if (!ok) break;
+                rp = r0 + 2 * u.nmax;
+                mma_commit(q_empty);
+                ++nu;
+            }
+            mma_commit(drain);
+            mbar_wait_drain(drain, 0, wc);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------- softmax / epilogue
+        // Warpgroup x owns query tile x of each unit; thread = one query row.
+        // A failed wait does not change the control flow (no block-level
+        // barriers here; each warp arrives on its own), so aborts wind down
+        // through the remaining bounded iterations.
+        const int x = (warp - 2) >> 2;
+        const int q4 = warp & 3;
+        const int row = q4 * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+        uint8_t *pbuf = sP + x * C::kPBytes;
+        uint32_t s_cnt = 0, pv_cnt = 0;
+        for (int k = 0;; ++k) {
+            const int idx = snake_index(k, p.grid);
+            if (idx >= count) break;
+            PUnit u;
+            decode_entry(p, __ldg(p.list + idx), u, NQ);
+            if (u.tile[x] < 0) continue;
+            const int q_row = u.tile[x] * kQTile + row;          // row within the sequence
+            const bool row_valid = q_row < u.s.Lq;
+            const int lim = !p.causal ? u.s.Lk : max(0, min(u.s.Lk, q_row + u.s.Lk - u.s.Lq + 1));
+            const int nkv = u.nkv[x];
+            float m_ref = kNegInf, l_sum = 0.f;
+            for (int j = 0; j < nkv; ++j, ++s_cnt) {
+                const int sb = NQ == 2 ? x : (int)(s_cnt & 1u);
+                const uint32_t spar = NQ == 2 ? (s_cnt & 1u) : ((s_cnt >> 1) & 1u);
+                mbar_wait(&s_full[sb], spar, wc);
+                tc_fence_after();
+                const uint32_t sa = tmem + lane_off + C::s_col(x, s_cnt);
+                const int key0 = j * kKvTile;
+                const bool full = key0 + kKvTile <= lim;
+                // pass 1: row max of the scaled scores
+                float mx = kNegInf;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float v[32];
+                    tmem_ld32(sa + c * 32, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float sv = (full || key0 + c * 32 + i < lim) ? v[i] * p.scale_log2 : kNegInf;
+                        mx = fmaxf(mx, sv);
+                    }
+                }
+                // The previous PV of this tile must have landed before O is
+                // rescaled or P is overwritten.
+                if (j > 0) {
+                    mbar_wait(&pv_done[x], (pv_cnt + j - 1) & 1, wc);
+                    tc_fence_after();
+                }
+                const float m_new = fmaxf(m_ref, mx);
+                const bool need = m_new > m_ref + kRescaleThreshold;
+                float alpha = 1.f;
+                if (need) {
+                    alpha = (m_ref == kNegInf) ? 0.f : ex2_approx(m_ref - m_new);
+                    l_sum *= alpha;
+                    m_ref = m_new;
+                }
+                if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        float o[32];
+                        const uint32_t oa = tmem + lane_off + C::o_col(x) + c * 32;
+                        tmem_ld32(oa, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                        tmem_st32(oa, o);
+                    }
+                    tmem_wait_st();
+                }
+                const float mu = (m_ref == kNegInf) ? 0.f : m_ref;
+                // pass 2: P = 2^(s * scale_log2 - m) as BF16 into the swizzled P tile
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float v[32];
+                    tmem_ld32(sa + c * 32, v);
+                    tmem_wait_ld();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        const bool in0 = full || key0 + c * 32 + i < lim;
+                        const bool in1 = full || key0 + c * 32 + i + 1 < lim;
+                        const float p0 = in0 ? ex2_approx(fmaf(v[i], p.scale_log2, -mu)) : 0.f;
+                        const float p1 = in1 ? ex2_approx(fmaf(v[i + 1], p.scale_log2, -mu)) : 0.f;
+                        l_sum += p0 + p1;
+                        pk[i >> 1] = pack_bf16x2(p0, p1);
+                    }
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const int unit = c * 4 + w;                 // 16-byte unit of the row: keys 8*unit..
+                        const int chunk = unit >> 3;
+                        const int phys = (unit & 7) ^ (row & 7);
+                        uint4 *dst = reinterpret_cast<uint4 *>(pbuf + chunk * C::kChunkBytes + row * 128 + phys * 16);
+                        *dst = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[NQ == 2 ? x : 0]);
+            }
+            // ------------------------------------------------------ epilogue
+            __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(p.out) +
+                                  (int64_t)(u.s.q0 + q_row) * p.out_stride[0] + (int64_t)u.h * p.out_stride[1];
+            if (nkv > 0) {
+                mbar_wait(&pv_done[x], (pv_cnt + nkv - 1) & 1, wc);
+                tc_fence_after();
+                const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    float o[32];
+                    tmem_ld32(tmem + lane_off + C::o_col(x) + c * 32, o);
+                    tmem_wait_ld();
+                    if (row_valid) {
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            uint4 v;
+                            v.x = pack_bf16x2(o[8 * w + 0] * inv, o[8 * w + 1] * inv);
+                            v.y = pack_bf16x2(o[8 * w + 2] * inv, o[8 * w + 3] * inv);
+                            v.z = pack_bf16x2(o[8 * w + 4] * inv, o[8 * w + 5] * inv);
+                            v.w = pack_bf16x2(o[8 * w + 6] * inv, o[8 * w + 7] * inv);
+                            *reinterpret_cast<uint4 *>(orow + c * 32 + w * 8) = v;
+                        }
+                    }
+                }
+                tc_fence_before();
+            } else if (row_valid) {
+                for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4 *>(orow)[c] = make_uint4(0, 0, 0, 0);
+            }
+            if (row_valid && p.lse)
+                p.lse[(int64_t)(u.s.q0 + q_row) * p.lse_stride[0] + (int64_t)u.h * p.lse_stride[1]] =
+                    l_sum > 0.f ? (m_ref + __log2f(l_sum)) * 0.69314718055994531f : kNegInf;
+            pv_cnt += nkv;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+// ------------------------------------------------------------------- plan
+//
+// One block.  PP[i] = exclusive prefix of the unit pairs per sequence; each
+// (pair, head) entry goes into the list ordered by its KV-tile cost, largest
+// first (counting sort), so that the snake assignment balances the CTAs.
+// Sequences whose cumulative lengths reach past the packed tensors are left
+// out and reported in the status word.
+__global__ void __launch_bounds__(1024) prefill_plan_kernel(const __grid_constant__ PrefillParams p, int num_q) {
+    __shared__ int warp_sums[32];
+    __shared__ int carry_s;
+    __shared__ int bins[kCostBins];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int32_t *PP = p.plan + 2;
+    if (tid == 0) carry_s = 0;
+    for (int i = tid; i < kCostBins; i += blockDim.x) bins[i] = 0;
+    __syncthreads();
+    for (int base = 0; base < p.B; base += 1024) {
+        const int i = base + tid;
+        int pairs = 0;
+        if (i < p.B) {
+            const Seq s = load_seq(p, i);
+            if (!s.ok) record_error(p.status, 1);
+            const int nqt = ceil_div_i(s.Lq, kQTile);
+            pairs = num_q == 2 ? (nqt + 1) / 2 : nqt;
+        }
+        int incl = pairs;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) warp_sums[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            int w = warp_sums[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += v;
+            }
+            warp_sums[lane] = w;
+        }
+        __syncthreads();
+        if (i < p.B) PP[i] = carry_s + (warp > 0 ? warp_sums[warp - 1] : 0) + incl - pairs;
+        __syncthreads();
+        if (tid == 0) carry_s += warp_sums[31];
+        __syncthreads();
+    }
+    const int NP = carry_s;
+    if (tid == 0) PP[p.B] = NP;
+    __syncthreads();
+    // cost of a pair: KV tiles of both of its query tiles
+    auto pair_bin = [&](int gp, int &seq_out) {
+        int lo = 0, hi = p.B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (PP[mid] <= gp) lo = mid; else hi = mid - 1;
+        }
+        seq_out = lo;
+        const Seq s = load_seq(p, lo);
+        const int pair = gp - PP[lo];
+        int cost = 0;
+        if (num_q == 2) {
+            cost = tile_kv_tiles(p, s, 2 * pair) + tile_kv_tiles(p, s, 2 * pair + 1);
+        } else {
+            cost = 2 * tile_kv_tiles(p, s, pair);
+        }
+        return kCostBins - 1 - min(cost, kCostBins - 1);     // largest cost first
+    };
+    for (int gp = tid; gp < NP; gp += blockDim.x) {
+        int sq;
+        atomicAdd(&bins[pair_bin(gp, sq)], 1);
+    }
+    __syncthreads();
+    if (tid == 0) {                                  // exclusive scan of the bins (4096 adds)
+        int acc = 0;
+        for (int i = 0; i < kCostBins; ++i) { const int c = bins[i]; bins[i] = acc; acc += c; }
+    }
+    __syncthreads();
+    for (int gp = tid; gp < NP; gp += blockDim.x) {
+        int sq;
+        const int pos = atomicAdd(&bins[pair_bin(gp, sq)], 1);
+        if ((int64_t)(pos + 1) * p.Hq <= p.list_capacity)
+            for (int h = 0; h < p.Hq; ++h) p.list[(int64_t)pos * p.Hq + h] = gp * p.Hq + h;
+    }
+    if (tid == 0) {
+        p.plan[0] = (int64_t)NP * p.Hq <= p.list_capacity ? NP * p.Hq : 0;
+        p.plan[1] = NP;
+        if ((int64_t)NP * p.Hq > p.list_capacity) record_error(p.status, 3);
+    }
+}
+
+template <int D>
+cudaError_t launch_t(const PrefillParams &p, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                     cudaStream_t stream) {
+    using C = PrefillCfg<D>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(varlen_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    varlen_prefill_kernel<D><<<p.grid, C::kThreads, C::kSmemBytes, stream>>>(p, tq, tk, tv);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                           const CUtensorMap &tv, int head_dim, cudaStream_t stream,
+                           cudaEvent_t timing_start, cudaEvent_t timing_stop, int *launches) {
+    *launches = 0;
+    prefill_plan_kernel<<<1, 1024, 0, stream>>>(p, head_dim == 128 ? 2 : 1);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    ++*launches;
+    if (timing_start) cudaEventRecord(timing_start, stream);
+    if (head_dim == 128) e = launch_t<128>(p, tq, tk, tv, stream);
+    else if (head_dim == 256) e = launch_t<256>(p, tq, tk, tv, stream);
+    else return cudaErrorInvalidValue;
+    if (e != cudaSuccess) return e;
+    ++*launches;
+    if (timing_stop) cudaEventRecord(timing_stop, stream);
+    return cudaSuccess;
+}
+
+}  // namespace fw

@@ -1,0 +1,129 @@
+"""Varlen prefill on the GPU, through the C ABI, against the fp64 oracle.
+
+Ragged packs (TokenSpeed-MLA capability summary: no padding, Q and KV packs
+may differ), causal bottom-right and non-causal, GQA and MHA, head dims 128
+and 256, tile-boundary lengths, empty sequences and rows with no visible key,
+and the two full-size workloads (varlen GQA prefill, dense causal MHA at head
+dim 256) on sampled rows in the launch configuration the benchmark times.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from ragged_softmax_attention_gb300.workloads import WORKLOADS, PrefillWorkload, make_prefill_inputs
+from tests.gpu_common import built_library, compare, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fw():
+    return built_library()
+
+
+def wl_prefill(hq=8, hkv=2, d=128, causal=True, seed=31):
+    return PrefillWorkload("p", num_seqs=0, num_q_heads=hq, num_kv_heads=hkv, head_dim_qk=d, head_dim_v=d,
+                           causal=causal, scale=1.0 / math.sqrt(d), value_seed=seed)
+
+
+def run_case(fw, wl, lq, lk=None, rows=None):
+    inp = make_prefill_inputs(wl, "cpu", lq, lk)
+    ref_o, ref_l = oracle.varlen_prefill(inp["q"], inp["k"], inp["v"], inp["cu_seqlens_q"], inp["cu_seqlens_k"],
+                                         wl.causal, wl.scale, rows=rows)
+    d = to_device(inp)
+    out, lse = fw.varlen_prefill(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], wl.causal, wl.scale)
+    torch.cuda.synchronize()
+    assert fw.device_status() == 0
+    o = out.reshape(-1, out.shape[-1])
+    l_ = lse.reshape(-1)
+    if rows is not None:
+        o, l_ = o[rows], l_[rows]
+    return compare(o, l_, ref_o, ref_l, what=f"lq={lq} lk={lk}")
+
+
+@pytest.mark.parametrize("L", [1, 2, 127, 128, 129, 255, 256, 257, 300, 511, 600])
+def test_causal_single_sequence_lengths(fw, L):
+    run_case(fw, wl_prefill(), [L])
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_ragged_batch(fw, causal):
+    run_case(fw, wl_prefill(causal=causal), [130, 1, 257, 64, 0, 400])
+
+
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 1), (32, 8), (12, 3)])
+def test_gqa_groups(fw, hq, hkv):
+    run_case(fw, wl_prefill(hq=hq, hkv=hkv), [200, 333])
+
+
+@pytest.mark.parametrize("lq,lk", [([100, 5, 300], [500, 5, 300]), ([256, 40], [100, 40]), ([7, 129], [0, 600])])
+@pytest.mark.parametrize("causal", [True, False])
+def test_different_q_and_kv_packs(fw, lq, lk, causal):
+    """Chunked-prefill shape (Lq < Lk), Lq > Lk (rows without visible keys when causal), empty KV."""
+    run_case(fw, wl_prefill(causal=causal), lq, lk)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_head_dim_256(fw, causal):
+    run_case(fw, wl_prefill(hq=4, hkv=2, d=256, causal=causal), [129, 300, 1])
+
+
+def test_many_units_balance_path(fw):
+    """More units than CTAs: the snake schedule over the longest-first list."""
+    wl = wl_prefill(hq=16, hkv=4)
+    lens = [int(x) for x in np.random.default_rng(3).integers(1, 700, size=24)]
+    total = sum(lens) * 16
+    rows = np.random.default_rng(4).choice(total, size=min(total, 3000), replace=False)
+    run_case(fw, wl, lens, rows=np.sort(rows))
+
+
+def test_output_guard_and_lse_optional(fw):
+    wl = wl_prefill(hq=4, hkv=2)
+    inp = to_device(make_prefill_inputs(wl, "cpu", [150, 20]))
+    big = torch.full((172, 4, 128), 3.0, dtype=torch.bfloat16, device="cuda")
+    out = big[1:171]
+    fw.varlen_prefill(inp["q"], inp["k"], inp["v"], inp["cu_seqlens_q"], inp["cu_seqlens_k"], True, wl.scale,
+                      out=out, return_lse=False)
+    torch.cuda.synchronize()
+    assert torch.all(big[0] == 3.0) and torch.all(big[171] == 3.0)
+    ref_o, _ = oracle.varlen_prefill(inp["q"].cpu(), inp["k"].cpu(), inp["v"].cpu(), inp["cu_seqlens_q"].cpu(),
+                                     inp["cu_seqlens_k"].cpu(), True, wl.scale)
+    compare(out.reshape(-1, 128), None, ref_o, None, "guard")
+
+
+def test_invalid_prefill_arguments(fw):
+    wl = wl_prefill(hq=4, hkv=2)
+    d = to_device(make_prefill_inputs(wl, "cpu", [10, 20]))
+    before = fw.launch_count()
+    with pytest.raises(fw.FwError):
+        fw.varlen_prefill(d["q"], d["k"], d["v"], d["cu_seqlens_q"][:2], d["cu_seqlens_k"], True, 0.1)
+    with pytest.raises(fw.FwError):
+        fw.varlen_prefill(d["q"][..., :64], d["k"][..., :64], d["v"][..., :64], d["cu_seqlens_q"],
+                          d["cu_seqlens_k"], True, 0.1)
+    with pytest.raises(fw.FwError):
+        fw.varlen_prefill(d["q"][:, :3], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], True, 0.1)
+    assert fw.launch_count() == before
+
+
+@pytest.mark.parametrize("name", ["varlen_gqa_prefill", "dense_causal_mha_hd256"])
+def test_full_size_workloads_sampled_rows(fw, name):
+    """The benchmark workloads at full size; 512 sampled rows checked against the oracle."""
+    wl = WORKLOADS[name]
+    d = make_prefill_inputs(wl, "cuda")
+    out, lse = fw.varlen_prefill(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], wl.causal, wl.scale)
+    torch.cuda.synchronize()
+    assert fw.device_status() == 0
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    total = d["q"].shape[0] * wl.num_q_heads
+    rows = np.sort(np.random.default_rng(9).choice(total, size=512, replace=False))
+    ref_o, ref_l = oracle.varlen_prefill(d["q"].cpu(), d["k"].cpu(), d["v"].cpu(), d["cu_seqlens_q"].cpu(),
+                                         d["cu_seqlens_k"].cpu(), wl.causal, wl.scale, rows=rows)
+    compare(out.reshape(-1, out.shape[-1])[rows], lse.reshape(-1)[rows], ref_o, ref_l, name)
+
+
+def test_no_keys_at_all(fw):
+    """Every KV length zero: all rows give zero output and -inf LSE."""
+    run_case(fw, wl_prefill(hq=4, hkv=2), [5, 130], [0, 0])
