@@ -19,8 +19,9 @@
 // buffered (2 x 128 columns) next to O (256 columns).
 //
 // Warp roles: warp 0 TMA producer (Q tiles, then K_j / V_j through a ring of
-// shared-memory slots), warp 1 MMA issuer and TMEM owner, then one warpgroup
-// per query tile (thread = query row: the row max and sum are thread-local).
+// shared-memory slots), warp 1 MMA issuer and TMEM owner (warps 2-3 idle),
+// then one warpgroup per query tile (thread = query row: the row max and sum
+// are thread-local; the row of S stays in registers).
 #include <cuda_bf16.h>
 
 #include "fw_internal.h"
@@ -50,7 +51,14 @@ struct PrefillCfg {
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA exceeded");
-    static constexpr int kThreads = 64 + kNumQ * 128;
+    // warpgroup 0: producer (warp 0), MMA (warp 1), two idle warps; then one
+    // softmax warpgroup per query tile
+    static constexpr int kThreads = 128 + kNumQ * 128;
+    // hd 128 launches 384 threads at 168 registers (64512 in all); the split
+    // below gives 128 x 72 + 256 x 216 = 64512 <= 64512.
+    static constexpr uint32_t kRegsControl = 72;
+    static constexpr uint32_t kRegsSoftmax = 216;
+    static_assert(kNumQ == 1 || 128 * kRegsControl + 256 * kRegsSoftmax <= 384 * 168, "register split");
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kKvTile, false, false);
     static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, false, true);
@@ -180,7 +188,9 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
     const uint32_t tmem = *tmem_slot;
     const WaitCtx wc{p.status, p.timeout_ns, abort_flag};
 
-    if (warp == 0) {
+    if (warp < 4) {
+      if constexpr (NQ == 2) setmaxnreg_dec<C::kRegsControl>();
+      if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             uint32_t rp = 0, nu = 0, issued = 0;
@@ -223,7 +233,7 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
+      } else if (warp == 1) {
         // ----------------------------------------------------------------- MMA
         if (lane == 0) {
             uint32_t rp = 0, nu = 0;
@@ -279,6 +289,7 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                 if (u.nmax > 0) {
                     if (!wait_slot(r0)) break;
                     tc_fence_after();
+#pragma unroll
                     for (int x = 0; x < NQ; ++x)
                         if (u.nkv[x] > 0) issue_qk(x, r0);
                     mma_commit(&slot_empty[r0 % C::kSlots]);
@@ -293,6 +304,7 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                     const uint32_t rv = r0 + 2 * j + 1;
                     if (!wait_slot(rv)) { ok = false; break; }
                     tc_fence_after();
+#pragma unroll
                     for (int x = 0; x < NQ; ++x) {
                         if (j >= u.nkv[x]) continue;
                         if (!issue_pv(x, rv, j == 0)) { ok = false; break; }
@@ -316,17 +328,20 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
             mbar_wait_drain(drain, 0, wc);
         }
         __syncwarp();
+      }
     } else {
+        if constexpr (NQ == 2) setmaxnreg_inc<C::kRegsSoftmax>();
         // ------------------------------------------------- softmax / epilogue
         // Warpgroup x owns query tile x of each unit; thread = one query row.
         // A failed wait does not change the control flow (no block-level
         // barriers here; each warp arrives on its own), so aborts wind down
         // through the remaining bounded iterations.
-        const int x = (warp - 2) >> 2;
+        const int x = (warp - 4) >> 2;
         const int q4 = warp & 3;
         const int row = q4 * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         uint8_t *pbuf = sP + x * C::kPBytes;
+        const bool scale_pos = p.scale_log2 >= 0.f;
         uint32_t s_cnt = 0, pv_cnt = 0;
         for (int k = 0;; ++k) {
             const int idx = snake_index(k, p.grid);
@@ -346,20 +361,36 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                 tc_fence_after();
                 const uint32_t sa = tmem + lane_off + C::s_col(x, s_cnt);
                 const int key0 = j * kKvTile;
-                const bool full = key0 + kKvTile <= lim;
-                // pass 1: row max of the scaled scores
-                float mx = kNegInf;
+                // The whole row of S in registers with one TMEM round trip.
+                float sv[kKvTile];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float v[32];
-                    tmem_ld32(sa + c * 32, v);
-                    tmem_wait_ld();
+                for (int c = 0; c < kKvTile / 32; ++c) tmem_ld32(sa + c * 32, sv + c * 32);
+                tmem_wait_ld();
+                // Masked keys (past the causal limit or the sequence end) get the
+                // value that exponentiates to 0 for this scale's sign, so the
+                // exponent pass below needs no second test.
+                if (key0 + kKvTile > lim) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float sv = (full || key0 + c * 32 + i < lim) ? v[i] * p.scale_log2 : kNegInf;
-                        mx = fmaxf(mx, sv);
-                    }
+                    for (int i = 0; i < kKvTile; ++i)
+                        if (key0 + i >= lim) sv[i] = scale_pos ? kNegInf : -kNegInf;
                 }
+                // Row extreme of the raw scores (max for a positive scale), 8
+                // independent chains; the scaled max is extreme * scale * log2(e).
+                float e8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) e8[i] = sv[i];
+                if (scale_pos) {
+#pragma unroll
+                    for (int i = 8; i < kKvTile; ++i) e8[i & 7] = fmaxf(e8[i & 7], sv[i]);
+                } else {
+#pragma unroll
+                    for (int i = 8; i < kKvTile; ++i) e8[i & 7] = fminf(e8[i & 7], sv[i]);
+                }
+                float ext = scale_pos ? fmaxf(fmaxf(fmaxf(e8[0], e8[1]), fmaxf(e8[2], e8[3])),
+                                              fmaxf(fmaxf(e8[4], e8[5]), fmaxf(e8[6], e8[7])))
+                                      : fminf(fminf(fminf(e8[0], e8[1]), fminf(e8[2], e8[3])),
+                                              fminf(fminf(e8[4], e8[5]), fminf(e8[6], e8[7])));
+                const float mx = (ext == kNegInf || ext == -kNegInf) ? kNegInf : ext * p.scale_log2;
                 // The previous PV of this tile must have landed before O is
                 // rescaled or P is overwritten.
                 if (j > 0) {
@@ -388,20 +419,19 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                     tmem_wait_st();
                 }
                 const float mu = (m_ref == kNegInf) ? 0.f : m_ref;
-                // pass 2: P = 2^(s * scale_log2 - m) as BF16 into the swizzled P tile
+                // P = 2^(s * scale * log2(e) - m) as BF16 into the swizzled P tile;
+                // the row sum runs in 8 independent chains.
+                float a8[8];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float v[32];
-                    tmem_ld32(sa + c * 32, v);
-                    tmem_wait_ld();
+                for (int i = 0; i < 8; ++i) a8[i] = 0.f;
+#pragma unroll
+                for (int c = 0; c < kKvTile / 32; ++c) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 32; i += 2) {
-                        const bool in0 = full || key0 + c * 32 + i < lim;
-                        const bool in1 = full || key0 + c * 32 + i + 1 < lim;
-                        const float p0 = in0 ? ex2_approx(fmaf(v[i], p.scale_log2, -mu)) : 0.f;
-                        const float p1 = in1 ? ex2_approx(fmaf(v[i + 1], p.scale_log2, -mu)) : 0.f;
-                        l_sum += p0 + p1;
+                        const float p0 = ex2_approx(fmaf(sv[c * 32 + i], p.scale_log2, -mu));
+                        const float p1 = ex2_approx(fmaf(sv[c * 32 + i + 1], p.scale_log2, -mu));
+                        a8[(i >> 1) & 7] += p0 + p1;
                         pk[i >> 1] = pack_bf16x2(p0, p1);
                     }
 #pragma unroll
@@ -413,6 +443,7 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                         *dst = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
                     }
                 }
+                l_sum += ((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]));
                 fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
