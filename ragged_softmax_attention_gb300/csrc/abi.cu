@@ -13,7 +13,7 @@
 #include <mutex>
 #include <vector>
 
-#include "../../include/fw_attn.h"
+#include "fw_attn.h"
 #include "fw_internal.h"
 
 namespace {

@@ -6,9 +6,11 @@
 // Orientation: a 128-row query tile is the MMA M axis, a 128-key tile is N:
 //   S [128 x 128]  = Q_tile * K_tile^T          (tcgen05, FP32 in TMEM)
 //   O [128 x D]   += P [128 x 128] * V_tile      (tcgen05, FP32 in TMEM)
-// with the online softmax of "Flywheel Attention", section 1, in base 2 and
-// with a conditional rescale (the base moves only when a row max rises by
-// more than 8 log2 units).
+// with the static-anchor softmax of "Flywheel Attention", section 3.1 and
+// appendix A, in base 2: each row's anchor is the max of its first visible
+// tile, P = 2^(s - anchor) needs no running max, and a check of the running
+// sum after each tile replays the tile with the online rescale (section 1
+// recurrence) when a score could have outgrown the anchor.
 //
 // D = 128: a unit is two consecutive query tiles of one head that share every
 // K/V tile load; S and O of both live in TMEM (4 x 128 columns) and two
@@ -19,7 +21,8 @@
 // buffered (2 x 128 columns) next to O (256 columns).
 //
 // Warp roles: warp 0 TMA producer (Q tiles, then K_j / V_j through a ring of
-// shared-memory slots), warp 1 MMA issuer and TMEM owner (warps 2-3 idle),
+// shared-memory slots), warp 1 MMA issuer of query tile 0 and TMEM owner,
+// warp 2 MMA issuer of query tile 1 (warp 3 idle),
 // then one warpgroup per query tile (thread = query row: the row max and sum
 // are thread-local; the row of S stays in registers).
 #include <cuda_bf16.h>
@@ -31,7 +34,10 @@ namespace fw {
 namespace {
 
 constexpr float kNegInf = -__builtin_huge_valf();
-constexpr float kRescaleThreshold = 8.0f;   // log2 units
+// Budget on a row's running sum of 2^(s - anchor): 2^32 keeps l and every
+// entry of O (|O| <= l * max|v|) far inside FP32 for |v| < 2^90; Flywheel's
+// appendix A derives its budget the same way, in natural-log units.
+constexpr float kAnchorBudget = 4294967296.0f;
 constexpr int kQTile = 128;
 constexpr int kCostBins = 4096;
 
@@ -41,13 +47,11 @@ struct PrefillCfg {
     static constexpr int kChunks = D / 64;
     static constexpr int kChunkBytes = 128 * 128;              // 128 rows x 64 bf16 columns
     static constexpr int kTileBytes = 128 * D * 2;              // one Q, K or V tile
-    static constexpr int kSlots = (D == 128) ? 3 : 2;           // K/V ring slots
-    static constexpr int kPBytes = 128 * kKvTile * 2;
+    static constexpr int kSlots = (D == 128) ? 4 : 2;           // K/V ring slots
     static constexpr int kOffQ = 0;
     static constexpr int kOffRing = kOffQ + kNumQ * kTileBytes;
-    static constexpr int kOffP = kOffRing + kSlots * kTileBytes;
-    static constexpr int kOffBar = kOffP + kNumQ * kPBytes;
-    static constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 1;
+    static constexpr int kOffBar = kOffRing + kSlots * kTileBytes;
+    static constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 2;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA exceeded");
@@ -152,7 +156,6 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sQ = smem + C::kOffQ;
     uint8_t *sRing = smem + C::kOffRing;
-    uint8_t *sP = smem + C::kOffP;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
     uint64_t *slot_full = bars;
     uint64_t *slot_empty = slot_full + C::kSlots;
@@ -161,7 +164,7 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
     uint64_t *s_full = q_empty + 2;                  // [2]
     uint64_t *p_full = s_full + 2;                   // [2]
     uint64_t *pv_done = p_full + 2;                  // [2]
-    uint64_t *drain = pv_done + 2;
+    uint64_t *drain = pv_done + 2;                   // [2]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
 
@@ -170,11 +173,12 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
     const int count = __ldg(p.plan + 0);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < C::kSlots; ++i) { mbar_init(&slot_full[i], 1); mbar_init(&slot_empty[i], 1); }
+        for (int i = 0; i < C::kSlots; ++i) { mbar_init(&slot_full[i], 1); mbar_init(&slot_empty[i], NQ); }
         mbar_init(q_full, 1);
-        mbar_init(q_empty, 1);
-        for (int i = 0; i < 2; ++i) { mbar_init(&s_full[i], 1); mbar_init(&p_full[i], 4); mbar_init(&pv_done[i], 1); }
-        mbar_init(drain, 1);
+        mbar_init(q_empty, NQ);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s_full[i], 1); mbar_init(&p_full[i], 4); mbar_init(&pv_done[i], 1); mbar_init(&drain[i], 1);
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -233,16 +237,18 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
             }
         }
         __syncwarp();
-      } else if (warp == 1) {
+      } else if (warp == 1 || (NQ == 2 && warp == 2)) {
         // ----------------------------------------------------------------- MMA
+        // One issuing thread per query tile, so neither tile's MMAs queue
+        // behind the other's issue: warp 1 drives tile 0, warp 2 tile 1.
         if (lane == 0) {
-            uint32_t rp = 0, nu = 0;
-            uint32_t qk_cnt[2] = {0, 0}, pv_cnt[2] = {0, 0};
+            const int x = warp - 1;
+            uint32_t rp = 0, nu = 0, qk_cnt = 0, pv_cnt = 0;
             auto wait_slot = [&](uint32_t r) {
                 return mbar_wait(&slot_full[r % C::kSlots], (r / C::kSlots) & 1, wc);
             };
-            auto issue_qk = [&](int x, uint32_t r_k) {
-                const uint32_t sc = C::s_col(x, qk_cnt[x]);
+            auto issue_qk = [&](uint32_t r_k) {
+                const uint32_t sc = C::s_col(x, qk_cnt);
                 const uint32_t q_base = smem_u32(sQ + x * C::kTileBytes);
                 const uint32_t k_base = smem_u32(sRing + (r_k % C::kSlots) * C::kTileBytes);
 #pragma unroll
@@ -251,24 +257,34 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                     const uint64_t b = sdesc_sw128(k_base + (kk >> 2) * C::kChunkBytes + (kk & 3) * 32, 16, 1024);
                     mma_bf16_ss(tmem + sc, a, b, C::kIdescQK, kk > 0 ? 1u : 0u);
                 }
-                const int sb = NQ == 2 ? x : (int)(qk_cnt[x] & 1u);
-                mma_commit(&s_full[sb]);
-                ++qk_cnt[x];
+                mma_commit(&s_full[NQ == 2 ? x : (int)(qk_cnt & 1u)]);
+                ++qk_cnt;
             };
-            auto issue_pv = [&](int x, uint32_t r_v, bool first) -> bool {
-                const uint32_t pc = pv_cnt[x];
-                if (!mbar_wait(&p_full[NQ == 2 ? x : 0], (pc & 1), wc)) return false;
+            auto issue_pv = [&](uint32_t r_v, bool first) -> bool {
+                if (!mbar_wait(&p_full[NQ == 2 ? x : 0], (pv_cnt & 1), wc)) return false;
                 tc_fence_after();
-                const uint32_t p_base = smem_u32(sP + x * C::kPBytes);
+                // P was written over the first 64 columns of this tile's S buffer
+                // (two BF16 per 32-bit column): A operand straight from TMEM.
+                const uint32_t p_col = C::s_col(x, pv_cnt);
                 const uint32_t v_base = smem_u32(sRing + (r_v % C::kSlots) * C::kTileBytes);
 #pragma unroll
                 for (int kk = 0; kk < kKvTile / 16; ++kk) {
-                    const uint64_t a = sdesc_sw128(p_base + (kk >> 2) * C::kChunkBytes + (kk & 3) * 32, 16, 1024);
                     const uint64_t b = sdesc_sw128(v_base + kk * 16 * 128, C::kChunkBytes, 1024);
-                    mma_bf16_ss(tmem + C::o_col(x), a, b, C::kIdescPV, (first && kk == 0) ? 0u : 1u);
+                    mma_bf16_ts(tmem + C::o_col(x), tmem + p_col + kk * 8, b, C::kIdescPV,
+                                (first && kk == 0) ? 0u : 1u);
                 }
                 mma_commit(&pv_done[x]);
-                ++pv_cnt[x];
+                ++pv_cnt;
+                return true;
+            };
+            // Each issuing thread releases every ring position of the unit
+            // exactly once (slot_empty counts one arrival per issuer): right
+            // after its last MMA reading the slot, or -- for a KV tile this
+            // query tile does not reach -- once the load has landed, so that no
+            // release can run a full ring ahead of the producer.
+            auto release = [&](uint32_t r, bool used) -> bool {
+                if (!used && !wait_slot(r)) return false;
+                mma_commit(&slot_empty[r % C::kSlots]);
                 return true;
             };
             bool ok = true;
@@ -279,44 +295,36 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                 decode_entry(p, __ldg(p.list + idx), u, NQ);
                 if (!mbar_wait(q_full, nu & 1, wc)) break;
                 tc_fence_after();
-                // K_j sits at ring position r0 + 2j, V_j at r0 + 2j + 1.  A slot is
-                // released (commit) right after the last MMA reading it is issued,
-                // so the in-order producer never waits on a slot the MMA warp
-                // still needs to reach.
-                const uint32_t r0 = rp;
-                // the query tile that reads KV tile jj last (tile 1 walks at least as far)
-                auto last_user = [&](int jj) { return (NQ == 2 && jj < u.nkv[1]) ? 1 : 0; };
-                if (u.nmax > 0) {
-                    if (!wait_slot(r0)) break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int x = 0; x < NQ; ++x)
-                        if (u.nkv[x] > 0) issue_qk(x, r0);
-                    mma_commit(&slot_empty[r0 % C::kSlots]);
-                    if (NQ == 1 && u.nkv[0] > 1) {
-                        if (!wait_slot(r0 + 2)) break;
+                const uint32_t r0 = rp;                       // K_j at r0 + 2j, V_j at r0 + 2j + 1
+                const int n = u.nkv[x];
+                const int step = NQ == 2 ? 1 : 2;             // QKs run this far ahead of PVs
+                // prologue: the first `step` QKs
+                for (int j = 0; j < step && j < u.nmax && ok; ++j) {
+                    const uint32_t rk = r0 + 2 * j;
+                    if (j < n) {
+                        if (!wait_slot(rk)) { ok = false; break; }
                         tc_fence_after();
-                        issue_qk(0, r0 + 2);
-                        mma_commit(&slot_empty[(r0 + 2) % C::kSlots]);
+                        issue_qk(rk);
                     }
+                    ok = release(rk, j < n);
                 }
                 for (int j = 0; j < u.nmax && ok; ++j) {
                     const uint32_t rv = r0 + 2 * j + 1;
-                    if (!wait_slot(rv)) { ok = false; break; }
-                    tc_fence_after();
-#pragma unroll
-                    for (int x = 0; x < NQ; ++x) {
-                        if (j >= u.nkv[x]) continue;
-                        if (!issue_pv(x, rv, j == 0)) { ok = false; break; }
-                        if (x == last_user(j)) mma_commit(&slot_empty[rv % C::kSlots]);
-                        const int jn = NQ == 2 ? j + 1 : j + 2;    // next QK of this tile
-                        if (jn < u.nkv[x]) {
-                            const uint32_t rk = r0 + 2 * jn;
+                    if (j < n) {
+                        if (!wait_slot(rv)) { ok = false; break; }
+                        tc_fence_after();
+                        if (!issue_pv(rv, j == 0)) { ok = false; break; }
+                    }
+                    if (!release(rv, j < n)) { ok = false; break; }
+                    const int jn = j + step;
+                    if (jn < u.nmax) {
+                        const uint32_t rk = r0 + 2 * jn;
+                        if (jn < n) {
                             if (!wait_slot(rk)) { ok = false; break; }
                             tc_fence_after();
-                            issue_qk(x, rk);
-                            if (x == last_user(jn)) mma_commit(&slot_empty[rk % C::kSlots]);
+                            issue_qk(rk);
                         }
+                        if (!release(rk, jn < n)) { ok = false; break; }
                     }
                 }
                 if (!ok) break;
@@ -324,8 +332,8 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                 mma_commit(q_empty);
                 ++nu;
             }
-            mma_commit(drain);
-            mbar_wait_drain(drain, 0, wc);
+            mma_commit(&drain[x]);
+            mbar_wait_drain(&drain[x], 0, wc);
         }
         __syncwarp();
       }
@@ -340,7 +348,6 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
         const int q4 = warp & 3;
         const int row = q4 * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-        uint8_t *pbuf = sP + x * C::kPBytes;
         const bool scale_pos = p.scale_log2 >= 0.f;
         uint32_t s_cnt = 0, pv_cnt = 0;
         for (int k = 0;; ++k) {
@@ -367,84 +374,96 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                 for (int c = 0; c < kKvTile / 32; ++c) tmem_ld32(sa + c * 32, sv + c * 32);
                 tmem_wait_ld();
                 // Masked keys (past the causal limit or the sequence end) get the
-                // value that exponentiates to 0 for this scale's sign, so the
-                // exponent pass below needs no second test.
+                // value that exponentiates to 0 for this scale's sign.
                 if (key0 + kKvTile > lim) {
 #pragma unroll
                     for (int i = 0; i < kKvTile; ++i)
                         if (key0 + i >= lim) sv[i] = scale_pos ? kNegInf : -kNegInf;
                 }
-                // Row extreme of the raw scores (max for a positive scale), 8
-                // independent chains; the scaled max is extreme * scale * log2(e).
-                float e8[8];
+                // Scaled row max of this tile (-inf when every key is masked),
+                // 8 independent chains over the raw scores.
+                auto row_max = [&]() -> float {
+                    float e8[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) e8[i] = sv[i];
-                if (scale_pos) {
+                    for (int i = 0; i < 8; ++i) e8[i] = sv[i];
+                    if (scale_pos) {
 #pragma unroll
-                    for (int i = 8; i < kKvTile; ++i) e8[i & 7] = fmaxf(e8[i & 7], sv[i]);
-                } else {
+                        for (int i = 8; i < kKvTile; ++i) e8[i & 7] = fmaxf(e8[i & 7], sv[i]);
+                    } else {
 #pragma unroll
-                    for (int i = 8; i < kKvTile; ++i) e8[i & 7] = fminf(e8[i & 7], sv[i]);
-                }
-                float ext = scale_pos ? fmaxf(fmaxf(fmaxf(e8[0], e8[1]), fmaxf(e8[2], e8[3])),
-                                              fmaxf(fmaxf(e8[4], e8[5]), fmaxf(e8[6], e8[7])))
-                                      : fminf(fminf(fminf(e8[0], e8[1]), fminf(e8[2], e8[3])),
-                                              fminf(fminf(e8[4], e8[5]), fminf(e8[6], e8[7])));
-                const float mx = (ext == kNegInf || ext == -kNegInf) ? kNegInf : ext * p.scale_log2;
-                // The previous PV of this tile must have landed before O is
-                // rescaled or P is overwritten.
+                        for (int i = 8; i < kKvTile; ++i) e8[i & 7] = fminf(e8[i & 7], sv[i]);
+                    }
+                    const float ext = scale_pos
+                        ? fmaxf(fmaxf(fmaxf(e8[0], e8[1]), fmaxf(e8[2], e8[3])), fmaxf(fmaxf(e8[4], e8[5]), fmaxf(e8[6], e8[7])))
+                        : fminf(fminf(fminf(e8[0], e8[1]), fminf(e8[2], e8[3])), fminf(fminf(e8[4], e8[5]), fminf(e8[6], e8[7])));
+                    return (ext == kNegInf || ext == -kNegInf) ? kNegInf : ext * p.scale_log2;
+                };
+                // P = 2^(s * scale * log2(e) - anchor) as BF16, packed two per
+                // 32-bit column over the first 64 columns of this tile's S buffer
+                // (its scores are already in registers); returns the tile's row
+                // sum (8 independent chains).  Warp-collective (TMEM stores).
+                auto write_p = [&](float anchor) -> float {
+                    const float mu = (anchor == kNegInf) ? 0.f : anchor;
+                    float a8[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) a8[i] = 0.f;
+#pragma unroll
+                    for (int c = 0; c < kKvTile / 32; ++c) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            const float p0 = ex2_approx(fmaf(sv[c * 32 + i], p.scale_log2, -mu));
+                            const float p1 = ex2_approx(fmaf(sv[c * 32 + i + 1], p.scale_log2, -mu));
+                            a8[(i >> 1) & 7] += p0 + p1;
+                            pk[i >> 1] = pack_bf16x2(p0, p1);
+                        }
+                        tmem_st16u(sa + c * 16, pk);
+                    }
+                    return ((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]));
+                };
+                // The previous PV of this tile must have landed before its P is
+                // overwritten or O is rescaled.
                 if (j > 0) {
                     mbar_wait(&pv_done[x], (pv_cnt + j - 1) & 1, wc);
                     tc_fence_after();
                 }
-                const float m_new = fmaxf(m_ref, mx);
-                const bool need = m_new > m_ref + kRescaleThreshold;
-                float alpha = 1.f;
-                if (need) {
-                    alpha = (m_ref == kNegInf) ? 0.f : ex2_approx(m_ref - m_new);
-                    l_sum *= alpha;
-                    m_ref = m_new;
-                }
-                if (j > 0 && __any_sync(0xffffffffu, need)) {
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        float o[32];
-                        const uint32_t oa = tmem + lane_off + C::o_col(x) + c * 32;
-                        tmem_ld32(oa, o);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                        tmem_st32(oa, o);
+                // Static anchor ("Flywheel Attention", section 3.1 and appendix
+                // A): a row's anchor is the max of the first tile in which it sees
+                // a key and does not move on the fast path, so the exponent pass
+                // needs no running max.
+                if (m_ref == kNegInf) m_ref = row_max();
+                float tsum = write_p(m_ref);
+                // The check: every p <= l, so a running sum within the budget
+                // proves no score rose more than log2(budget) above the anchor
+                // (appendix A, claim 2).  A row that fails (or overflowed) replays
+                // the tile with the rescaling softmax: its anchor moves to the new
+                // max, l and O are rescaled, P is recomputed before the MMA sees it.
+                const bool over = !(l_sum + tsum <= kAnchorBudget);
+                if (__any_sync(0xffffffffu, over)) {
+                    float alpha = 1.f;
+                    if (over) {
+                        const float m_new = fmaxf(m_ref, row_max());
+                        alpha = ex2_approx(m_ref - m_new);
+                        l_sum *= alpha;
+                        m_ref = m_new;
                     }
-                    tmem_wait_st();
-                }
-                const float mu = (m_ref == kNegInf) ? 0.f : m_ref;
-                // P = 2^(s * scale * log2(e) - m) as BF16 into the swizzled P tile;
-                // the row sum runs in 8 independent chains.
-                float a8[8];
+                    if (j > 0) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) a8[i] = 0.f;
+                        for (int c = 0; c < D / 32; ++c) {
+                            float o[32];
+                            const uint32_t oa = tmem + lane_off + C::o_col(x) + c * 32;
+                            tmem_ld32(oa, o);
+                            tmem_wait_ld();
 #pragma unroll
-                for (int c = 0; c < kKvTile / 32; ++c) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        const float p0 = ex2_approx(fmaf(sv[c * 32 + i], p.scale_log2, -mu));
-                        const float p1 = ex2_approx(fmaf(sv[c * 32 + i + 1], p.scale_log2, -mu));
-                        a8[(i >> 1) & 7] += p0 + p1;
-                        pk[i >> 1] = pack_bf16x2(p0, p1);
+                            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                            tmem_st32(oa, o);
+                        }
+                        tmem_wait_st();
                     }
-#pragma unroll
-                    for (int w = 0; w < 4; ++w) {
-                        const int unit = c * 4 + w;                 // 16-byte unit of the row: keys 8*unit..
-                        const int chunk = unit >> 3;
-                        const int phys = (unit & 7) ^ (row & 7);
-                        uint4 *dst = reinterpret_cast<uint4 *>(pbuf + chunk * C::kChunkBytes + row * 128 + phys * 16);
-                        *dst = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
-                    }
+                    tsum = write_p(m_ref);         // all lanes: unchanged rows rewrite the same P
                 }
-                l_sum += ((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]));
-                fence_proxy_async_smem();
+                l_sum += tsum;
+                tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[NQ == 2 ? x : 0]);

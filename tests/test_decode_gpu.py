@@ -107,6 +107,14 @@ def test_split_count_invariance(fw):
         assert (l - outs[0][1]).abs().max().item() <= 1e-3
 
 
+@pytest.mark.parametrize("scale", [1.0, -0.2])
+def test_scale_extremes_exercise_rescale(fw, scale):
+    """Large or negative scales move the running max far and often."""
+    wl = wl_decode(batch=3, hq=40, hkv=8, ps=64, lens=(900, 130, 2000))
+    import dataclasses
+    run_case(fw, dataclasses.replace(wl, scale=scale), chunk=256)
+
+
 def test_empty_rows(fw):
     """n = 0 rows and causal rows with no visible key: zero output, -inf LSE."""
     run_case(fw, wl_decode(batch=3, q_len=4, lens=(0, 2, 40), ps=16))

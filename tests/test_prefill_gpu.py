@@ -127,3 +127,14 @@ def test_full_size_workloads_sampled_rows(fw, name):
 def test_no_keys_at_all(fw):
     """Every KV length zero: all rows give zero output and -inf LSE."""
     run_case(fw, wl_prefill(hq=4, hkv=2), [5, 130], [0, 0])
+
+
+@pytest.mark.parametrize("scale", [1.0, 2.0, -0.2])
+@pytest.mark.parametrize("d", [128, 256])
+def test_scale_extremes_exercise_anchor_replay(fw, scale, d):
+    """Large scales spread scores over ~100 log2 units, so later tiles outgrow the
+    first tile's anchor and the running-sum check replays them (Flywheel appendix
+    A); a negative scale exercises the sign-aware masking."""
+    wl = PrefillWorkload("s", num_seqs=0, num_q_heads=4, num_kv_heads=2, head_dim_qk=d, head_dim_v=d,
+                         causal=True, scale=scale, value_seed=41)
+    run_case(fw, wl, [300, 700, 129])
