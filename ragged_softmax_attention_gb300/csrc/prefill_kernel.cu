@@ -51,7 +51,7 @@ struct PrefillCfg {
     static constexpr int kOffQ = 0;
     static constexpr int kOffRing = kOffQ + kNumQ * kTileBytes;
     static constexpr int kOffBar = kOffRing + kSlots * kTileBytes;
-    static constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 2;
+    static constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 2 + 2;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA exceeded");
@@ -165,6 +165,7 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
     uint64_t *p_full = s_full + 2;                   // [2]
     uint64_t *pv_done = p_full + 2;                  // [2]
     uint64_t *drain = pv_done + 2;                   // [2]
+    uint64_t *issued = drain + 2;                    // [2]: step handoff between the two issuers
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
 
@@ -178,6 +179,7 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
         mbar_init(q_empty, NQ);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1); mbar_init(&p_full[i], 4); mbar_init(&pv_done[i], 1); mbar_init(&drain[i], 1);
+            mbar_init(&issued[i], 1);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -247,7 +249,10 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
             auto wait_slot = [&](uint32_t r) {
                 return mbar_wait(&slot_full[r % C::kSlots], (r / C::kSlots) & 1, wc);
             };
-            auto issue_qk = [&](uint32_t r_k) {
+            // Pushes only: a thread's tcgen05.mma issue advances at the tensor
+            // core's pace, and any wait between pushes lets the pipe drain, so
+            // each step waits for everything first and commits afterwards.
+            auto push_qk = [&](uint32_t r_k) {
                 const uint32_t sc = C::s_col(x, qk_cnt);
                 const uint32_t q_base = smem_u32(sQ + x * C::kTileBytes);
                 const uint32_t k_base = smem_u32(sRing + (r_k % C::kSlots) * C::kTileBytes);
@@ -257,14 +262,14 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                     const uint64_t b = sdesc_sw128(k_base + (kk >> 2) * C::kChunkBytes + (kk & 3) * 32, 16, 1024);
                     mma_bf16_ss(tmem + sc, a, b, C::kIdescQK, kk > 0 ? 1u : 0u);
                 }
+            };
+            auto commit_qk = [&]() {
                 mma_commit(&s_full[NQ == 2 ? x : (int)(qk_cnt & 1u)]);
                 ++qk_cnt;
             };
-            auto issue_pv = [&](uint32_t r_v, bool first) -> bool {
-                if (!mbar_wait(&p_full[NQ == 2 ? x : 0], (pv_cnt & 1), wc)) return false;
-                tc_fence_after();
-                // P was written over the first 64 columns of this tile's S buffer
-                // (two BF16 per 32-bit column): A operand straight from TMEM.
+            // P was written over the first 64 columns of this tile's S buffer
+            // (two BF16 per 32-bit column): A operand straight from TMEM.
+            auto push_pv = [&](uint32_t r_v, bool first) {
                 const uint32_t p_col = C::s_col(x, pv_cnt);
                 const uint32_t v_base = smem_u32(sRing + (r_v % C::kSlots) * C::kTileBytes);
 #pragma unroll
@@ -273,20 +278,28 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                     mma_bf16_ts(tmem + C::o_col(x), tmem + p_col + kk * 8, b, C::kIdescPV,
                                 (first && kk == 0) ? 0u : 1u);
                 }
+            };
+            auto commit_pv = [&]() {
                 mma_commit(&pv_done[x]);
                 ++pv_cnt;
-                return true;
             };
             // Each issuing thread releases every ring position of the unit
-            // exactly once (slot_empty counts one arrival per issuer): right
-            // after its last MMA reading the slot, or -- for a KV tile this
-            // query tile does not reach -- once the load has landed, so that no
-            // release can run a full ring ahead of the producer.
-            auto release = [&](uint32_t r, bool used) -> bool {
-                if (!used && !wait_slot(r)) return false;
+            // exactly once (slot_empty counts one arrival per issuer): after its
+            // last MMA reading the slot, or -- for a KV tile this query tile
+            // does not reach -- once the load has landed, so that no release
+            // can run a full ring ahead of the producer.
+            auto release_unused = [&](uint32_t r) -> bool {
+                if (!wait_slot(r)) return false;
                 mma_commit(&slot_empty[r % C::kSlots]);
                 return true;
             };
+            // Alternation (two issuers): step j of tile 1 is issued only after
+            // step j of tile 0, and step j of tile 0 only after step j-1 of tile
+            // 1, so the tensor core runs the tiles' PV+QK groups in turns while
+            // the other tile's softmax works -- the two-group ping-pong.  The
+            // skew between the issuers stays within one step, so each waits on
+            // at most the newest phase of the other's `issued` barrier.
+            uint32_t other = 0;                            // steps the other tile issued so far
             bool ok = true;
             for (int k = 0; ok; ++k) {
                 const int idx = snake_index(k, p.grid);
@@ -297,6 +310,7 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                 tc_fence_after();
                 const uint32_t r0 = rp;                       // K_j at r0 + 2j, V_j at r0 + 2j + 1
                 const int n = u.nkv[x];
+                const int n_other = NQ == 2 ? u.nkv[1 - x] : 0;
                 const int step = NQ == 2 ? 1 : 2;             // QKs run this far ahead of PVs
                 // prologue: the first `step` QKs
                 for (int j = 0; j < step && j < u.nmax && ok; ++j) {
@@ -304,30 +318,51 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                     if (j < n) {
                         if (!wait_slot(rk)) { ok = false; break; }
                         tc_fence_after();
-                        issue_qk(rk);
+                        push_qk(rk);
+                        commit_qk();
+                        mma_commit(&slot_empty[rk % C::kSlots]);
+                    } else {
+                        ok = release_unused(rk);
                     }
-                    ok = release(rk, j < n);
                 }
                 for (int j = 0; j < u.nmax && ok; ++j) {
                     const uint32_t rv = r0 + 2 * j + 1;
-                    if (j < n) {
-                        if (!wait_slot(rv)) { ok = false; break; }
-                        tc_fence_after();
-                        if (!issue_pv(rv, j == 0)) { ok = false; break; }
-                    }
-                    if (!release(rv, j < n)) { ok = false; break; }
                     const int jn = j + step;
-                    if (jn < u.nmax) {
-                        const uint32_t rk = r0 + 2 * jn;
-                        if (jn < n) {
+                    const uint32_t rk = r0 + 2 * jn;
+                    const bool mine = j < n, next_mine = jn < n;
+                    if (mine) {
+                        if (NQ == 2) {
+                            // tile 1 follows tile 0's step j; tile 0 follows tile 1's step j-1
+                            const int dep = x == 1 ? j : j - 1;
+                            if (dep >= 0 && dep < n_other && !mbar_wait(&issued[1 - x], (other + dep) & 1, wc)) {
+                                ok = false; break;
+                            }
+                        }
+                        // With at least 3 ring slots K_{j+step} can land before V_j is
+                        // released, so PV and QK go out back to back; with 2 slots the
+                        // producer needs V_j's slot first (K and V alternate slots).
+                        constexpr bool kEarlyK = C::kSlots >= 3;
+                        if (!wait_slot(rv) || (kEarlyK && next_mine && !wait_slot(rk)) ||
+                            !mbar_wait(&p_full[NQ == 2 ? x : 0], (pv_cnt & 1), wc)) { ok = false; break; }
+                        tc_fence_after();
+                        push_pv(rv, j == 0);
+                        if (kEarlyK && next_mine) push_qk(rk);
+                        if (NQ == 2) mbar_arrive(&issued[x]);    // step j handed over
+                        commit_pv();
+                        mma_commit(&slot_empty[rv % C::kSlots]);
+                        if (!kEarlyK && next_mine) {
                             if (!wait_slot(rk)) { ok = false; break; }
                             tc_fence_after();
-                            issue_qk(rk);
+                            push_qk(rk);
                         }
-                        if (!release(rk, jn < n)) { ok = false; break; }
+                        if (next_mine) { commit_qk(); mma_commit(&slot_empty[rk % C::kSlots]); }
+                    } else if (!release_unused(rv)) {
+                        ok = false; break;
                     }
+                    if (jn < u.nmax && !next_mine && !release_unused(rk)) { ok = false; break; }
                 }
                 if (!ok) break;
+                other += n_other;
                 rp = r0 + 2 * u.nmax;
                 mma_commit(q_empty);
                 ++nu;
