@@ -343,16 +343,19 @@ def oracle_sample_rate(torch, inp, wl, rows_b, heads, threads):
     return total_bytes, total_s
 
 
-def cpu_baseline(torch, inp, wl, budget_s=15.0):
+def cpu_baseline(torch, inp, wl, budget_s=12.0):
+    """The oracle, as it stands, on the host cores: whole batch rows (all query
+    heads) in batch order, cycling through the batch until about `budget_s`
+    seconds of oracle time have accumulated."""
     threads = max(1, os.cpu_count() or 1)
     heads = list(range(wl.num_q_heads))
-    b_cal, s_cal = oracle_sample_rate(torch, inp, wl, [0], heads, threads)
-    nrows = max(1, min(wl.batch - 1, int(budget_s / max(s_cal, 1e-3))))
-    rows = list(range(1, 1 + nrows))
-    by, s = oracle_sample_rate(torch, inp, wl, rows, heads, threads)
+    by, s, n = 0, 0.0, 0
+    while s < budget_s and n < 64 * wl.batch:
+        b_by, b_s = oracle_sample_rate(torch, inp, wl, [n % wl.batch], heads, threads)
+        by, s, n = by + b_by, s + b_s, n + 1
     return {"value": round(by / s / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"batch rows 1..{nrows} of {wl.batch}, all {wl.num_q_heads} query heads "
-                      f"({s:.1f} s of fp64 CPU work, {threads} threads)"}
+            "sample": f"{n} batch rows in batch order ({n / wl.batch:.1f} passes over the {wl.batch}-row batch), "
+                      f"all {wl.num_q_heads} query heads ({s:.1f} s of fp64 CPU work, {threads} threads)"}
 
 
 def run_reference(args):

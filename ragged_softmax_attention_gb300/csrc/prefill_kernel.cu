@@ -657,7 +657,7 @@ cudaError_t launch_prefill(const PrefillParams &p, const CUtensorMap &tq, const 
                            const CUtensorMap &tv, int head_dim, cudaStream_t stream,
                            cudaEvent_t timing_start, cudaEvent_t timing_stop, int *launches) {
     *launches = 0;
-    prefill_plan_kernel<<<1, 1024, 0, stream>>>(p, head_dim == 128 ? 2 : 1);
+    prefill_plan_kernel<<<1, 1024, 0, stream>>>(p, head_dim == 128 ? PrefillCfg<128>::kNumQ : PrefillCfg<256>::kNumQ);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     ++*launches;
