@@ -36,6 +36,7 @@ sys.path.insert(0, ROOT)
 METRIC = "decode KV GB/s (% of HBM peak); prefill TFLOP/s (% of BF16 peak)"
 DECODE_WL = "qwen3_14b_paged_decode"
 PREFILL_WL = "varlen_gqa_prefill"
+PREFILL_HD256_WL = "dense_causal_mha_hd256"
 
 
 def load_peaks():
@@ -48,6 +49,24 @@ def load_peaks():
                 "source": "measured"}
     except Exception:
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def max_over_ranks(dist, values, device):
+    """Element-wise maximum of `values` over all ranks (the slowest rank sets
+    the time); `dist` is torch.distributed with an initialised group, or None."""
+    import torch
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(bytes_per_step_per_rank, steps, world, elapsed_ms):
+    """Aggregate GB/s over all ranks: every rank processes the same per-step
+    bytes (weak scaling), over the slowest rank's time."""
+    if not (elapsed_ms == elapsed_ms) or elapsed_ms <= 0:
+        return None
+    return bytes_per_step_per_rank * steps * world / (elapsed_ms * 1e-3) / 1e9
 
 
 def dist_env():
@@ -158,7 +177,7 @@ def decode_work(inp, wl):
     return kv, kv + other, int(lens.sum())
 
 
-def bench_decode(fw, torch, steps, warmup, device, peaks, batch=None, do_e2e=True):
+def bench_decode(fw, torch, steps, warmup, device, peaks, batch=None, do_e2e=True, barrier=lambda: None):
     import dataclasses
     from ragged_softmax_attention_gb300.workloads import WORKLOADS, make_decode_inputs, workload_seq_lens
     wl = WORKLOADS[DECODE_WL]
@@ -184,12 +203,14 @@ def bench_decode(fw, torch, steps, warmup, device, peaks, batch=None, do_e2e=Tru
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
     with ClockSampler(torch.cuda.current_device()) as clk:
+        barrier()
         torch.cuda.synchronize()
         start.record(stream)
         for _ in range(steps):
             step()
         stop.record(stream)
         torch.cuda.synchronize()
+        barrier()
     elapsed_ms = start.elapsed_time(stop)
     launches = fw.launch_count() - launches0
     kernel_ms, kernel_n = fw.kernel_timing_read()
@@ -237,12 +258,14 @@ def bench_decode(fw, torch, steps, warmup, device, peaks, batch=None, do_e2e=Tru
         lse_h.copy_(l_, non_blocking=True)
 
     e2e_step()
+    barrier()
     torch.cuda.synchronize()
     start.record(stream)
     for _ in range(e2e_steps):
         e2e_step()
     stop.record(stream)
     torch.cuda.synchronize()
+    barrier()
     e2e_ms = start.elapsed_time(stop) / e2e_steps
     del dev, host
     res.update(e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, e2e_steps=e2e_steps)
@@ -264,9 +287,10 @@ def prefill_flops(cu_q, cu_k, hq, dk, dv, causal):
     return total * hq * 2 * (dk + dv)
 
 
-def bench_prefill(fw, torch, steps, warmup, device, peaks):
+def bench_prefill(fw, torch, steps, warmup, device, peaks, name=None):
     from ragged_softmax_attention_gb300.workloads import WORKLOADS, make_prefill_inputs
-    wl = WORKLOADS[PREFILL_WL]
+    name = name or PREFILL_WL
+    wl = WORKLOADS[name]
     d = make_prefill_inputs(wl, device)
     cu_q = d["cu_seqlens_q"].cpu().tolist()
     cu_k = d["cu_seqlens_k"].cpu().tolist()
@@ -276,7 +300,7 @@ def bench_prefill(fw, torch, steps, warmup, device, peaks):
                                      wl.scale)
     except fw.FwError as e:
         if e.status == 2:
-            return {"workload": PREFILL_WL, "value": None, "unit": "TFLOP/s", "unavailable": str(e)}
+            return {"workload": name, "value": None, "unit": "TFLOP/s", "unavailable": str(e)}
         raise
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
@@ -303,14 +327,16 @@ def bench_prefill(fw, torch, steps, warmup, device, peaks):
         raise RuntimeError("device status nonzero during the prefill benchmark")
     per = kms / max(1, kn)
     ach = flops / (per * 1e-3) / 1e12
-    traffic = ncu_traffic("varlen_prefill_gqa_ncu.json", ["prefill_kernel.cu", "fw_ptx.cuh"], flops)
-    return {"workload": PREFILL_WL, "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+    traffic = (ncu_traffic("varlen_prefill_gqa_ncu.json", ["prefill_kernel.cu", "fw_ptx.cuh"], flops)
+               if name == PREFILL_WL else None)
+    return {"workload": name, "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 4), "steps": n, "flops_per_step": flops,
             "gpu_launches": fw.launch_count() - l0,
             "config": {"num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads, "num_kv_heads": wl.num_kv_heads,
                        "head_dim": wl.head_dim_qk, "causal": wl.causal, "total_tokens": cu_q[-1],
-                       "seq_len_range": list(wl.seq_len_range)},
-            "roofline": {"kernel": "varlen_prefill_kernel<128>", "bound": "tensor", "achieved": round(ach, 1),
+                       "seq_len_range": list(wl.seq_len_range) if wl.seq_len_range else None,
+                       "seq_lens": list(wl.seq_lens) if wl.seq_lens else None, "scale": wl.scale},
+            "roofline": {"kernel": f"varlen_prefill_kernel<{wl.head_dim_qk}>", "bound": "tensor", "achieved": round(ach, 1),
                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": round(ach / peaks["bf16_tflops"], 4),
                          "frac_of_sustained": round(ach / peaks["bf16_tflops_sustained"], 4),
@@ -436,14 +462,13 @@ def main():
             print(json.dumps({"prefill": pre}), flush=True)
         return 0
     dec = bench_decode(fw, torch, args.steps, args.warmup, device, peaks, batch=args.decode_batch or None,
-                       do_e2e=not args.no_e2e)
+                       do_e2e=not args.no_e2e, barrier=(pg.barrier if pg else (lambda: None)))
     pre = None if args.only == "decode" else bench_prefill(fw, torch, args.steps, args.warmup, device, peaks)
-    t = torch.tensor([dec["elapsed_ms"], dec["e2e_ms"]], dtype=torch.float64, device=device)
-    if pg:
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-    elapsed_ms, e2e_ms = t.tolist()
-    value = dec["kv_bytes"] * args.steps * world / (elapsed_ms * 1e-3) / 1e9
-    e2e_value = dec["kv_bytes"] * world / (e2e_ms * 1e-3) / 1e9 if e2e_ms == e2e_ms else None
+    pre256 = (None if args.only == "decode" else
+              bench_prefill(fw, torch, args.steps, args.warmup, device, peaks, name=PREFILL_HD256_WL))
+    elapsed_ms, e2e_ms = max_over_ranks(pg, [dec["elapsed_ms"], dec["e2e_ms"]], device)
+    value = whole_job_rate(dec["kv_bytes"], args.steps, world, elapsed_ms)
+    e2e_value = whole_job_rate(dec["kv_bytes"], 1, world, e2e_ms)
     if rank != 0:
         if pg:
             pg.destroy_process_group()
@@ -457,7 +482,7 @@ def main():
             "e2e": {"value": round(e2e_value, 1) if e2e_value else None, "unit": "GB/s", "h2d_bytes_per_step": dec["h2d"],
                     "d2h_bytes_per_step": dec["d2h"], "steps": dec["e2e_steps"],
                     "note": "inputs (incl. the KV cache) copied from pinned host memory every step"},
-            "prefill": pre}
+            "prefill": pre, "prefill_hd256": pre256}
     if world == 1 and not args.no_cpu_baseline and not args.decode_batch:
         try:
             line["cpu_baseline"] = cpu_baseline(torch, dec["inputs"], dec["wl"])
