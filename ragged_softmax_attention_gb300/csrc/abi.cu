@@ -182,6 +182,20 @@ fw_status_t plan_decode(int32_t B, int32_t q_len, int32_t Hq, int32_t Hkv, int32
     fw_decode_plan_t p{};
     const int G = Hq / Hkv;
     p.group = G;
+    const bool latent = (Dv == 512);
+    if (latent) {
+        // Latent heads (Dk = 576, Dv = 512): 64 query heads of one token per
+        // CTA; the q_len * G / 64 row groups of a unit share its tile ranges
+        // and ride on the CTA index.
+        if (G % fw::kLatentRows != 0)
+            return fail(FW_ERR_UNSUPPORTED, "latent decode needs the query heads per KV head (%d) to be a "
+                        "multiple of %d", G, fw::kLatentRows);
+        p.tokens_per_unit = 1;
+        p.heads_per_unit = fw::kLatentRows;
+        p.rows_per_unit = fw::kLatentRows;
+        p.row_groups = q_len * (G / fw::kLatentRows);
+        if (p.row_groups > num_sms) return fail(FW_ERR_UNSUPPORTED, "more row groups than SMs");
+    } else
     // Fold query tokens next to the heads of a KV group: the largest F that
     // divides q_len with G * F within the 32-row N budget ("TokenSpeed-MLA
     // 2.0.1", fold_sq_factor, with 32 rows instead of 128 because here the
@@ -205,7 +219,8 @@ fw_status_t plan_decode(int32_t B, int32_t q_len, int32_t Hq, int32_t Hkv, int32
     const int64_t tiles_max = (max_kv_len + fw::kKvTile - 1) / fw::kKvTile;
     if (p.num_units * (tiles_max > 0 ? tiles_max : 1) >= (1LL << 31))
         return fail(FW_ERR_UNSUPPORTED, "decode too large for 32-bit tile indices");
-    int64_t span = g_opt_chunk > 0 ? (g_opt_chunk + fw::kKvTile - 1) / fw::kKvTile : fw::kDecodeMinSpan;
+    int64_t span = g_opt_chunk > 0 ? (g_opt_chunk + fw::kKvTile - 1) / fw::kKvTile
+                                   : (latent ? fw::kLatentMinSpan : fw::kDecodeMinSpan);
     p.min_span_tiles = (int32_t)span;
     // A unit of t tiles meets at most ceil(t / span) + 1 ranges.
     p.max_pieces = (int32_t)((tiles_max + span - 1) / span + 1);
@@ -216,6 +231,10 @@ fw_status_t plan_decode(int32_t B, int32_t q_len, int32_t Hq, int32_t Hkv, int32
     p.workspace_bytes = plan_bytes + o_bytes + rows * p.max_pieces * 4;
     int64_t grid = num_sms;
     if (g_opt_max_ctas > 0 && grid > g_opt_max_ctas) grid = g_opt_max_ctas;
+    if (latent) {
+        grid = grid / p.row_groups * p.row_groups;         // whole groups of row-group CTAs
+        if (grid < p.row_groups) grid = p.row_groups;
+    }
     p.grid = (int32_t)(grid > 0 ? grid : 1);
     *pl = p;
     return FW_OK;
@@ -396,9 +415,12 @@ static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_
     if (lse && (lse->shape[0] != B || lse->shape[1] != q_len || lse->shape[2] != Hq))
         return fail(FW_ERR_INVALID_ARG, "lse must be [B, q_len, Hq]");
     if (!std::isfinite(scale)) return fail(FW_ERR_INVALID_ARG, "scale must be finite");
-    if (!(Dk == Dv && (Dk == 128 || Dk == 256)))
-        return fail(FW_ERR_UNSUPPORTED, "decode head dims (Dk=%lld, Dv=%lld): supported Dk = Dv in {128, 256}",
-                    (long long)Dk, (long long)Dv);
+    const bool latent = (Dk == 576 && Dv == 512);
+    if (!latent && !(Dk == Dv && (Dk == 128 || Dk == 256)))
+        return fail(FW_ERR_UNSUPPORTED, "decode head dims (Dk=%lld, Dv=%lld): supported Dk = Dv in {128, 256} "
+                    "and the latent (576, 512)", (long long)Dk, (long long)Dv);
+    if (!latent && Dv == 512)
+        return fail(FW_ERR_UNSUPPORTED, "Dv = 512 is served for the latent layout (Dk = 576) only");
     if (q_len < 1 || q_len > 4) return fail(FW_ERR_UNSUPPORTED, "q_len must be in [1, 4]");
     if (!supported_page_size(ps))
         return fail(FW_ERR_UNSUPPORTED, "page size %lld: supported 8, 16, 32, 64, 128 or multiples of 128",
@@ -436,12 +458,13 @@ static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_
     p.B = (int)B; p.q_len = (int)q_len; p.Hq = (int)Hq; p.Hkv = (int)Hkv; p.G = pl.group;
     p.ps = (int)ps; p.max_pages = (int)max_pages; p.num_pages = (int)P;
     p.rows = pl.rows_per_unit;
-    p.head_mode = pl.group <= 32 ? 0 : 1;
+    p.head_mode = (latent || pl.group > 32) ? 1 : 0;
     p.tokens_per_unit = pl.tokens_per_unit;
     p.heads_per_unit = pl.heads_per_unit;
-    p.head_chunks = p.head_mode ? (pl.group + 31) / 32 : 1;
+    p.head_chunks = p.head_mode ? (pl.group + pl.heads_per_unit - 1) / pl.heads_per_unit : 1;
     p.row_groups = pl.row_groups;
-    p.units_per_row = (int)Hkv * pl.row_groups;
+    p.units_per_row = latent ? (int)Hkv : (int)Hkv * pl.row_groups;
+    p.range_groups = latent ? pl.row_groups : 1;
     p.forced_span = g_opt_chunk > 0 ? pl.min_span_tiles : 0;
     p.min_span = pl.min_span_tiles;
     p.max_pieces = pl.max_pieces;
@@ -467,7 +490,7 @@ static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_
 
     CUtensorMap tq, tk, tv;
     {
-        const uint32_t box_h = p.head_mode == 0 ? (uint32_t)pl.group : 32u;
+        const uint32_t box_h = p.head_mode == 0 ? (uint32_t)pl.group : (uint32_t)pl.heads_per_unit;
         const uint32_t box_t = p.head_mode == 0 ? (uint32_t)pl.tokens_per_unit : 1u;
         const uint64_t dims[4] = {(uint64_t)Dk, (uint64_t)Hq, (uint64_t)q_len, (uint64_t)B};
         const uint64_t strides[3] = {(uint64_t)q->stride[2] * 2, (uint64_t)q->stride[1] * 2, (uint64_t)q->stride[0] * 2};
@@ -489,7 +512,8 @@ static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_
     cudaEvent_t ev0 = nullptr, ev1 = nullptr;
     if (g_opt_timing) { ev0 = pooled_event(); ev1 = pooled_event(); }
     int launched = 0;
-    cudaError_t e = fw::launch_decode(p, tq, tk, tv, (int)Dk, stream, ev0, ev1, &launched);
+    cudaError_t e = latent ? fw::launch_latent_decode(p, tq, tk, tv, stream, ev0, ev1, &launched)
+                           : fw::launch_decode(p, tq, tk, tv, (int)Dk, stream, ev0, ev1, &launched);
     g_launches.fetch_add(launched);
     if (e != cudaSuccess) return fail(FW_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
     if (ev0) g_timed.push_back({ev0, ev1});

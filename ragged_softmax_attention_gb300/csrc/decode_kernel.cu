@@ -634,7 +634,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const __grid_constant
         const int T = carry_s;
         PB[p.B] = T;
         int span = p.forced_span;
-        if (span <= 0) span = max(p.min_span, ceil_div_i(T, max(1, p.grid)));
+        if (span <= 0) span = max(p.min_span, ceil_div_i(T, max(1, p.grid / max(1, p.range_groups))));
         p.plan[0] = T;
         p.plan[1] = span;
     }
@@ -677,9 +677,11 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ De
     const int tb = (__ldg(PB + b + 1) - pb0) / p.units_per_row;
     if (tb == 0) return;                             // empty row: written by the plan kernel
     const int g = h / p.G;
-    const int rg = p.head_mode == 0 ? t / p.tokens_per_unit
+    // Row groups that ride on the CTA index share their unit's tile range.
+    const int rg = p.range_groups > 1 ? 0
+                 : p.head_mode == 0 ? t / p.tokens_per_unit
                                     : t * p.head_chunks + (h - g * p.G) / p.rows;
-    const int pstart = pb0 + (g * p.row_groups + rg) * tb;
+    const int pstart = pb0 + (g * (p.range_groups > 1 ? 1 : p.row_groups) + rg) * tb;
     const int npieces = (pstart + tb - 1) / span - pstart / span + 1;
     if (npieces <= 1) return;
     const float *lse_row = p.ws_lse + row * p.max_pieces;
@@ -722,12 +724,26 @@ size_t decode_smem_bytes(int head_dim, int rows) {
     return rows == 16 ? DecodeCfg<256, 16>::kSmemBytes : DecodeCfg<256, 32>::kSmemBytes;
 }
 
+cudaError_t launch_decode_plan(const DecodeParams &p, cudaStream_t stream) {
+    decode_plan_kernel<<<1, 1024, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_combine(const DecodeParams &p, int head_dim_v, cudaStream_t stream) {
+    const int64_t rows = (int64_t)p.B * p.q_len * p.Hq;
+    const unsigned grid = (unsigned)((rows + 3) / 4);
+    if (head_dim_v == 128) combine_kernel<128><<<grid, 128, 0, stream>>>(p);
+    else if (head_dim_v == 256) combine_kernel<256><<<grid, 128, 0, stream>>>(p);
+    else if (head_dim_v == 512) combine_kernel<512><<<grid, 128, 0, stream>>>(p);
+    else return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
 cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                           const CUtensorMap &tv, int head_dim, cudaStream_t stream,
                           cudaEvent_t timing_start, cudaEvent_t timing_stop, int *launches) {
     *launches = 0;
-    decode_plan_kernel<<<1, 1024, 0, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_decode_plan(p, stream);
     if (e != cudaSuccess) return e;
     ++*launches;
     if (timing_start) cudaEventRecord(timing_start, stream);
@@ -740,11 +756,7 @@ cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &tq, const CU
     ++*launches;
     if (timing_stop) cudaEventRecord(timing_stop, stream);
     if (p.max_pieces > 1) {
-        const int64_t rows = (int64_t)p.B * p.q_len * p.Hq;
-        const unsigned grid = (unsigned)((rows + 3) / 4);
-        if (head_dim == 128) combine_kernel<128><<<grid, 128, 0, stream>>>(p);
-        else combine_kernel<256><<<grid, 128, 0, stream>>>(p);
-        e = cudaGetLastError();
+        e = launch_decode_combine(p, head_dim, stream);
         if (e != cudaSuccess) return e;
         ++*launches;
     }

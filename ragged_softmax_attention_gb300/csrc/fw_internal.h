@@ -11,6 +11,8 @@ constexpr int kKvTile = 128;          // keys per KV tile (MMA M extent in decod
 constexpr int kSoftmaxStartWarp = 2;  // decode: warps 2..5 run the softmax / epilogue
 
 constexpr int kDecodeMinSpan = 8;     // decode: fewest KV tiles one CTA range holds (auto mode)
+constexpr int kLatentMinSpan = 32;    // latent-head decode: the same, for its heavier tiles
+constexpr int kLatentRows = 64;       // latent-head decode: query heads per CTA (MMA N)
 
 // One decode launch, fully resolved on the host.
 //
@@ -31,6 +33,9 @@ struct DecodeParams {
     int min_span;         // lower bound of the auto span
     int max_pieces;       // workspace slots per query row
     int grid;             // CTAs of the attention kernel
+    int range_groups;     // 1: CTA c takes ranges c, c + grid, ...; R > 1: the R row groups of
+                          // a unit ride on the CTA index (CTA c runs row group c % R over ranges
+                          // c / R, c / R + grid / R, ...), so they read the same keys together
     int Dv;
     int32_t *plan;        // [0] = T, [1] = span, [2 .. 2 + B] = PB
     const int32_t *block_table; int64_t bt_stride;
@@ -68,6 +73,15 @@ cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &tm_q, const 
                           const CUtensorMap &tm_v, int head_dim, cudaStream_t stream,
                           cudaEvent_t timing_start, cudaEvent_t timing_stop, int *launches);
 size_t decode_smem_bytes(int head_dim, int rows);
+cudaError_t launch_decode_plan(const DecodeParams &p, cudaStream_t stream);
+cudaError_t launch_decode_combine(const DecodeParams &p, int head_dim_v, cudaStream_t stream);
+
+// Latent-head decode (Dk = 576, Dv = 512, row groups of 64 query heads):
+// plan kernel + attention kernel + combine kernel, in stream order
+cudaError_t launch_latent_decode(const DecodeParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                                 const CUtensorMap &tm_v, cudaStream_t stream, cudaEvent_t timing_start,
+                                 cudaEvent_t timing_stop, int *launches);
+size_t latent_decode_smem_bytes();
 
 // plan kernel + attention kernel, in stream order
 cudaError_t launch_prefill(const PrefillParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,

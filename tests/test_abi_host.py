@@ -71,8 +71,27 @@ def test_planner_folds_like_tokenspeed_rule(fwlib, G, q_len):
 
 
 def test_planner_wide_groups_are_chunked(fwlib):
-    p = fwlib.plan_decode(2, 4, 128, 1, 512, 81920, num_sms=152)
+    p = fwlib.plan_decode(2, 4, 128, 1, 128, 81920, num_sms=152)
     assert p["heads_per_unit"] == 32 and p["row_groups"] == 4 * 4
+
+
+@pytest.mark.parametrize("q_len,hq,hkv,sms,grid", [(4, 128, 1, 152, 152), (3, 128, 1, 152, 150),
+                                                    (1, 64, 1, 152, 152), (2, 128, 2, 148, 148)])
+def test_planner_latent_row_groups_ride_on_the_grid(fwlib, q_len, hq, hkv, sms, grid):
+    """Latent heads (Dv 512): 64 heads of one token per CTA; the row groups of a
+    unit are q_len * G / 64 consecutive CTAs, so the grid is a whole multiple."""
+    p = fwlib.plan_decode(32, q_len, hq, hkv, 512, 81920, num_sms=sms)
+    G = hq // hkv
+    assert p["heads_per_unit"] == 64 and p["rows_per_unit"] == 64 and p["tokens_per_unit"] == 1
+    assert p["row_groups"] == q_len * G // 64
+    assert p["grid"] == grid and p["grid"] % p["row_groups"] == 0
+    assert p["min_span_tiles"] == 32
+    assert p["max_pieces"] == -(-640 // 32) + 1
+
+
+def test_planner_latent_rejects_partial_head_blocks(fwlib):
+    with pytest.raises(fwlib.FwError):
+        fwlib.plan_decode(2, 1, 96, 1, 512, 4096, num_sms=152)
 
 
 def test_planner_workspace_matches_pages_formula(fwlib):
