@@ -37,6 +37,7 @@ METRIC = "decode KV GB/s (% of HBM peak); prefill TFLOP/s (% of BF16 peak)"
 DECODE_WL = "qwen3_14b_paged_decode"
 PREFILL_WL = "varlen_gqa_prefill"
 PREFILL_HD256_WL = "dense_causal_mha_hd256"
+LATENT_WL = "latent_paged_decode"
 
 
 def load_peaks():
@@ -343,6 +344,67 @@ def bench_prefill(fw, torch, steps, warmup, device, peaks, name=None):
                          "traffic": traffic, "peak_source": peaks["source"], "kernel_ms_per_launch": round(per, 4)}}
 
 
+# ------------------------------------------------------- latent decode
+
+def latent_work(lens, wl):
+    """FLOPs (each query token t of a row with n keys sees n - q_len + t + 1)
+    and KV bytes (the 576-wide key rows; values are a view of them)."""
+    flops = 0
+    for n in lens:
+        for t in range(wl.q_len):
+            flops += max(0, min(n, n - wl.q_len + t + 1)) * wl.num_q_heads * 2 * (wl.head_dim_qk + wl.head_dim_v)
+    kv = sum(lens) * wl.num_kv_heads * wl.head_dim_qk * 2
+    return flops, kv
+
+
+def bench_latent(fw, torch, steps, warmup, device, peaks, batch=None):
+    import dataclasses
+    from ragged_softmax_attention_gb300.workloads import WORKLOADS, make_decode_inputs
+    wl = WORKLOADS[LATENT_WL]
+    if batch:   # a prefix of the same batch (profiling captures on a smaller case)
+        wl = dataclasses.replace(wl, batch=batch, seq_lens=wl.seq_lens[:batch])
+    d = make_decode_inputs(wl, device)
+    lens = d["seq_lens"].cpu().tolist()
+    flops, kv = latent_work(lens, wl)
+    args = (d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["seq_lens"], d["scale"])
+    out, lse = fw.paged_decode(*args)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, warmup)):
+        fw.paged_decode(*args, out=out, lse=lse)
+    torch.cuda.synchronize()
+    fw.set_option(fw.FW_OPT_KERNEL_TIMING, 1)
+    fw.kernel_timing_read()
+    n = max(3, min(steps, 50))
+    l0 = fw.launch_count()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(n):
+        fw.paged_decode(*args, out=out, lse=lse)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(stop) / n
+    kms, kn = fw.kernel_timing_read()
+    fw.set_option(fw.FW_OPT_KERNEL_TIMING, 0)
+    if fw.device_status() != 0:
+        raise RuntimeError("device status nonzero during the latent decode benchmark")
+    per = kms / max(1, kn)
+    ach = flops / (per * 1e-3) / 1e12
+    return {"workload": LATENT_WL, "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "kv_gbs": round(kv / (ms * 1e-3) / 1e9, 1), "ms_per_step": round(ms, 4), "steps": n,
+            "flops_per_step": flops, "kv_bytes_per_step": kv, "gpu_launches": fw.launch_count() - l0,
+            "config": {"batch": wl.batch, "q_len": wl.q_len, "num_q_heads": wl.num_q_heads,
+                       "num_kv_heads": wl.num_kv_heads, "head_dim_qk": wl.head_dim_qk,
+                       "head_dim_v": wl.head_dim_v, "page_size": wl.page_size, "seq_lens": "81920 each",
+                       "scale": wl.scale, "v": "first 512 columns of the key cache"},
+            "roofline": {"kernel": "latent_decode_kernel", "bound": "tensor", "achieved": round(ach, 1),
+                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": round(ach / peaks["bf16_tflops"], 4),
+                         "frac_of_sustained": round(ach / peaks["bf16_tflops_sustained"], 4),
+                         "traffic": None, "peak_source": peaks["source"], "kernel_ms_per_launch": round(per, 4)}}
+
+
 # ------------------------------------------------------------ CPU oracle
 
 def oracle_sample_rate(torch, inp, wl, rows_b, heads, threads):
@@ -427,10 +489,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--only", choices=["all", "decode", "prefill"], default="all",
+    ap.add_argument("--only", choices=["all", "decode", "prefill", "latent"], default="all",
                     help="profiling runs: time one path only")
     ap.add_argument("--decode-batch", type=int, default=0,
                     help="profiling runs: a prefix of the decode batch (smaller capture)")
+    ap.add_argument("--latent-batch", type=int, default=0,
+                    help="profiling runs: a prefix of the latent decode batch (smaller capture)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -461,11 +525,17 @@ def main():
         if rank == 0:
             print(json.dumps({"prefill": pre}), flush=True)
         return 0
+    if args.only == "latent":
+        lat = bench_latent(fw, torch, args.steps, args.warmup, device, peaks, batch=args.latent_batch or None)
+        if rank == 0:
+            print(json.dumps({"latent_decode": lat}), flush=True)
+        return 0
     dec = bench_decode(fw, torch, args.steps, args.warmup, device, peaks, batch=args.decode_batch or None,
                        do_e2e=not args.no_e2e, barrier=(pg.barrier if pg else (lambda: None)))
     pre = None if args.only == "decode" else bench_prefill(fw, torch, args.steps, args.warmup, device, peaks)
     pre256 = (None if args.only == "decode" else
               bench_prefill(fw, torch, args.steps, args.warmup, device, peaks, name=PREFILL_HD256_WL))
+    lat = None if args.only == "decode" else bench_latent(fw, torch, args.steps, args.warmup, device, peaks)
     elapsed_ms, e2e_ms = max_over_ranks(pg, [dec["elapsed_ms"], dec["e2e_ms"]], device)
     value = whole_job_rate(dec["kv_bytes"], args.steps, world, elapsed_ms)
     e2e_value = whole_job_rate(dec["kv_bytes"], 1, world, e2e_ms)
@@ -482,7 +552,7 @@ def main():
             "e2e": {"value": round(e2e_value, 1) if e2e_value else None, "unit": "GB/s", "h2d_bytes_per_step": dec["h2d"],
                     "d2h_bytes_per_step": dec["d2h"], "steps": dec["e2e_steps"],
                     "note": "inputs (incl. the KV cache) copied from pinned host memory every step"},
-            "prefill": pre, "prefill_hd256": pre256}
+            "prefill": pre, "prefill_hd256": pre256, "latent_decode": lat}
     if world == 1 and not args.no_cpu_baseline and not args.decode_batch:
         try:
             line["cpu_baseline"] = cpu_baseline(torch, dec["inputs"], dec["wl"])
