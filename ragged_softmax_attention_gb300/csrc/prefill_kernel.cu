@@ -293,12 +293,13 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                 mma_commit(&slot_empty[r % C::kSlots]);
                 return true;
             };
-            // Alternation (two issuers): step j of tile 1 is issued only after
-            // step j of tile 0, and step j of tile 0 only after step j-1 of tile
-            // 1, so the tensor core runs the tiles' PV+QK groups in turns while
-            // the other tile's softmax works -- the two-group ping-pong.  The
-            // skew between the issuers stays within one step, so each waits on
-            // at most the newest phase of the other's `issued` barrier.
+            // Alternation (two issuers): step j of tile 1 starts once tile 0 has
+            // pushed the PV of its step j, and step j of tile 0 once tile 1 has
+            // pushed the PV of its step j-1, so the tensor core runs the tiles'
+            // PV+QK groups in turns while the other tile's softmax works -- the
+            // two-group ping-pong.  The skew between the issuers stays within
+            // one step, so each waits on at most the newest phase of the other's
+            // `issued` barrier.
             uint32_t other = 0;                            // steps the other tile issued so far
             bool ok = true;
             for (int k = 0; ok; ++k) {
@@ -346,8 +347,12 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                             !mbar_wait(&p_full[NQ == 2 ? x : 0], (pv_cnt & 1), wc)) { ok = false; break; }
                         tc_fence_after();
                         push_pv(rv, j == 0);
+                        // Hand the turn over while this step's QK is still being
+                        // pushed: the other issuer's waits then overlap that push,
+                        // and its PV queues right behind it instead of after an
+                        // empty pipe.
+                        if (NQ == 2) mbar_arrive(&issued[x]);
                         if (kEarlyK && next_mine) push_qk(rk);
-                        if (NQ == 2) mbar_arrive(&issued[x]);    // step j handed over
                         commit_pv();
                         mma_commit(&slot_empty[rv % C::kSlots]);
                         if (!kEarlyK && next_mine) {
