@@ -47,10 +47,14 @@ struct PrefillCfg {
     static constexpr int kChunks = D / 64;
     static constexpr int kChunkBytes = 128 * 128;              // 128 rows x 64 bf16 columns
     static constexpr int kTileBytes = 128 * D * 2;              // one Q, K or V tile
-    static constexpr int kSlots = (D == 128) ? 4 : 2;           // K/V ring slots
+    // The K/V ring moves items of 128 keys x 128 columns (two 64-column
+    // blocks); a tile is D / 128 items.
+    static constexpr int kItems = D / 128;
+    static constexpr int kSlotBytes = 2 * kChunkBytes;
+    static constexpr int kSlots = (D == 128) ? 4 : 5;           // K/V ring slots (items)
     static constexpr int kOffQ = 0;
     static constexpr int kOffRing = kOffQ + kNumQ * kTileBytes;
-    static constexpr int kOffBar = kOffRing + kSlots * kTileBytes;
+    static constexpr int kOffBar = kOffRing + kSlots * kSlotBytes;
     static constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 2 + 2;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
@@ -65,7 +69,7 @@ struct PrefillCfg {
     static_assert(kNumQ == 1 || 128 * kRegsControl + 256 * kRegsSoftmax <= 384 * 168, "register split");
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kKvTile, false, false);
-    static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, false, true);
+    static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, false, true);   // one item of V
     // TMEM columns: S buffers then O accumulators
     __device__ static constexpr uint32_t s_col(int tile, uint32_t cnt) {
         return kNumQ == 2 ? (uint32_t)tile * 128u : (cnt & 1u) * 128u;
@@ -74,6 +78,23 @@ struct PrefillCfg {
 };
 
 __device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
+
+// Ring order of a unit's K and V tiles, in blocks of kItems ring items.
+// Two query tiles (one item per tile): K_0 V_0 K_1 V_1 ..., the order the
+// two issuers' steps need them.  One query tile, whose QKs run two tiles
+// ahead of its PVs: K_0 K_1, then V_j followed by K_{j+2} -- the order its
+// single issuer consumes them, so a ring of a few items always holds the
+// next loads.
+template <int NQ>
+__device__ __forceinline__ int ring_block_v(int j, int n) {
+    if constexpr (NQ == 2) return 2 * j + 1;
+    return min(2, n) + j + min(j, max(0, n - 2));
+}
+template <int NQ>
+__device__ __forceinline__ int ring_block_k(int j, int n) {
+    if constexpr (NQ == 2) return 2 * j;
+    return j < 2 ? j : ring_block_v<NQ>(j - 2, n) + 1;
+}
 
 struct Seq {
     int q0, k0, Lq, Lk;
@@ -217,19 +238,29 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                         tma_load_3d(smem_u32(sQ + x * C::kTileBytes + c * C::kChunkBytes), &tm_q, q_full,
                                     c * 64, u.h, u.s.q0 + u.tile[x] * kQTile);
                 }
-                // K_j and V_j of the unit, in that order, through the slot ring.
-                for (int j = 0; j < u.nmax && ok; ++j) {
-                    for (int kv = 0; kv < 2; ++kv, ++rp) {
+                // The unit's K and V tiles through the ring, item by item, in
+                // ring order (ring_block_k / ring_block_v).
+                auto load_tile = [&](bool is_v, int j) {
+                    for (int h = 0; h < C::kItems && ok; ++h, ++rp) {
                         const int sl = rp % C::kSlots;
                         ok = mbar_wait(&slot_empty[sl], ((rp / C::kSlots) & 1) ^ 1, wc);
                         if (!ok) break;
-                        mbar_arrive_expect_tx(&slot_full[sl], C::kTileBytes);
+                        mbar_arrive_expect_tx(&slot_full[sl], C::kSlotBytes);
 #pragma unroll
-                        for (int c = 0; c < C::kChunks; ++c)
-                            tma_load_3d(smem_u32(sRing + sl * C::kTileBytes + c * C::kChunkBytes),
-                                        kv == 0 ? (const void *)&tm_k : (const void *)&tm_v, &slot_full[sl],
-                                        c * 64, u.g, u.s.k0 + j * kKvTile);
+                        for (int c = 0; c < 2; ++c)
+                            tma_load_3d(smem_u32(sRing + sl * C::kSlotBytes + c * C::kChunkBytes),
+                                        is_v ? (const void *)&tm_v : (const void *)&tm_k, &slot_full[sl],
+                                        (2 * h + c) * 64, u.g, u.s.k0 + j * kKvTile);
                         issued = rp + 1;
+                    }
+                };
+                if constexpr (NQ == 2) {
+                    for (int j = 0; j < u.nmax && ok; ++j) { load_tile(false, j); load_tile(true, j); }
+                } else {
+                    for (int j = 0; j < 2 && j < u.nmax && ok; ++j) load_tile(false, j);
+                    for (int j = 0; j < u.nmax && ok; ++j) {
+                        load_tile(true, j);
+                        if (j + 2 < u.nmax) load_tile(false, j + 2);
                     }
                 }
             }
@@ -252,14 +283,24 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
             // Pushes only: a thread's tcgen05.mma issue advances at the tensor
             // core's pace, and any wait between pushes lets the pipe drain, so
             // each step waits for everything first and commits afterwards.
+            // A tile at ring position r occupies items r .. r + kItems - 1.
+            auto wait_tile = [&](uint32_t r) {
+                for (int h = 0; h < C::kItems; ++h)
+                    if (!wait_slot(r + h)) return false;
+                return true;
+            };
+            auto release_tile = [&](uint32_t r) {
+                for (int h = 0; h < C::kItems; ++h) mma_commit(&slot_empty[(r + h) % C::kSlots]);
+            };
             auto push_qk = [&](uint32_t r_k) {
                 const uint32_t sc = C::s_col(x, qk_cnt);
                 const uint32_t q_base = smem_u32(sQ + x * C::kTileBytes);
-                const uint32_t k_base = smem_u32(sRing + (r_k % C::kSlots) * C::kTileBytes);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t k_base = smem_u32(sRing + ((r_k + (kk >> 3)) % C::kSlots) * C::kSlotBytes);
+                    const int kl = kk & 7;
                     const uint64_t a = sdesc_sw128(q_base + (kk >> 2) * C::kChunkBytes + (kk & 3) * 32, 16, 1024);
-                    const uint64_t b = sdesc_sw128(k_base + (kk >> 2) * C::kChunkBytes + (kk & 3) * 32, 16, 1024);
+                    const uint64_t b = sdesc_sw128(k_base + (kl >> 2) * C::kChunkBytes + (kl & 3) * 32, 16, 1024);
                     mma_bf16_ss(tmem + sc, a, b, C::kIdescQK, kk > 0 ? 1u : 0u);
                 }
             };
@@ -269,18 +310,23 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
             };
             // P was written over the first 64 columns of this tile's S buffer
             // (two BF16 per 32-bit column): A operand straight from TMEM.
+            // Each item of V (128 value columns) accumulates into its own
+            // 128 columns of O.
             auto push_pv = [&](uint32_t r_v, bool first) {
                 const uint32_t p_col = C::s_col(x, pv_cnt);
-                const uint32_t v_base = smem_u32(sRing + (r_v % C::kSlots) * C::kTileBytes);
 #pragma unroll
-                for (int kk = 0; kk < kKvTile / 16; ++kk) {
-                    const uint64_t b = sdesc_sw128(v_base + kk * 16 * 128, C::kChunkBytes, 1024);
-                    mma_bf16_ts(tmem + C::o_col(x), tmem + p_col + kk * 8, b, C::kIdescPV,
-                                (first && kk == 0) ? 0u : 1u);
+                for (int h = 0; h < C::kItems; ++h) {
+                    const uint32_t v_base = smem_u32(sRing + ((r_v + h) % C::kSlots) * C::kSlotBytes);
+#pragma unroll
+                    for (int kk = 0; kk < kKvTile / 16; ++kk) {
+                        const uint64_t b = sdesc_sw128(v_base + kk * 16 * 128, C::kChunkBytes, 1024);
+                        mma_bf16_ts(tmem + C::o_col(x) + h * 128, tmem + p_col + kk * 8, b, C::kIdescPV,
+                                    (first && kk == 0) ? 0u : 1u);
+                    }
                 }
             };
             auto commit_pv = [&]() {
-                mma_commit(&pv_done[x]);
+                mma_commit(&pv_done[NQ == 2 ? x : (int)(pv_cnt & 1u)]);
                 ++pv_cnt;
             };
             // Each issuing thread releases every ring position of the unit
@@ -289,8 +335,8 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
             // does not reach -- once the load has landed, so that no release
             // can run a full ring ahead of the producer.
             auto release_unused = [&](uint32_t r) -> bool {
-                if (!wait_slot(r)) return false;
-                mma_commit(&slot_empty[r % C::kSlots]);
+                if (!wait_tile(r)) return false;
+                release_tile(r);
                 return true;
             };
             // Alternation (two issuers): step j of tile 1 starts once tile 0 has
@@ -309,27 +355,29 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                 decode_entry(p, __ldg(p.list + idx), u, NQ);
                 if (!mbar_wait(q_full, nu & 1, wc)) break;
                 tc_fence_after();
-                const uint32_t r0 = rp;                       // K_j at r0 + 2j, V_j at r0 + 2j + 1
+                const uint32_t r0 = rp;
+                auto pos_k = [&](int j) { return r0 + (uint32_t)(C::kItems * ring_block_k<NQ>(j, u.nmax)); };
+                auto pos_v = [&](int j) { return r0 + (uint32_t)(C::kItems * ring_block_v<NQ>(j, u.nmax)); };
                 const int n = u.nkv[x];
                 const int n_other = NQ == 2 ? u.nkv[1 - x] : 0;
                 const int step = NQ == 2 ? 1 : 2;             // QKs run this far ahead of PVs
                 // prologue: the first `step` QKs
                 for (int j = 0; j < step && j < u.nmax && ok; ++j) {
-                    const uint32_t rk = r0 + 2 * j;
+                    const uint32_t rk = pos_k(j);
                     if (j < n) {
-                        if (!wait_slot(rk)) { ok = false; break; }
+                        if (!wait_tile(rk)) { ok = false; break; }
                         tc_fence_after();
                         push_qk(rk);
                         commit_qk();
-                        mma_commit(&slot_empty[rk % C::kSlots]);
+                        release_tile(rk);
                     } else {
                         ok = release_unused(rk);
                     }
                 }
                 for (int j = 0; j < u.nmax && ok; ++j) {
-                    const uint32_t rv = r0 + 2 * j + 1;
                     const int jn = j + step;
-                    const uint32_t rk = r0 + 2 * jn;
+                    const uint32_t rv = pos_v(j);
+                    const uint32_t rk = jn < u.nmax ? pos_k(jn) : 0u;
                     const bool mine = j < n, next_mine = jn < n;
                     if (mine) {
                         if (NQ == 2) {
@@ -339,12 +387,14 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                                 ok = false; break;
                             }
                         }
-                        // With at least 3 ring slots K_{j+step} can land before V_j is
-                        // released, so PV and QK go out back to back; with 2 slots the
-                        // producer needs V_j's slot first (K and V alternate slots).
-                        constexpr bool kEarlyK = C::kSlots >= 3;
-                        if (!wait_slot(rv) || (kEarlyK && next_mine && !wait_slot(rk)) ||
-                            !mbar_wait(&p_full[NQ == 2 ? x : 0], (pv_cnt & 1), wc)) { ok = false; break; }
+                        // The ring holds K_{j+step} before V_j is released (its items
+                        // need only older items consumed), so PV and QK go out back
+                        // to back.
+                        if (!wait_tile(rv) || (next_mine && !wait_tile(rk)) ||
+                            !mbar_wait(&p_full[NQ == 2 ? x : (int)(pv_cnt & 1u)],
+                                       NQ == 2 ? (pv_cnt & 1u) : ((pv_cnt >> 1) & 1u), wc)) {
+                            ok = false; break;
+                        }
                         tc_fence_after();
                         push_pv(rv, j == 0);
                         // Hand the turn over while this step's QK is still being
@@ -352,15 +402,10 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                         // and its PV queues right behind it instead of after an
                         // empty pipe.
                         if (NQ == 2) mbar_arrive(&issued[x]);
-                        if (kEarlyK && next_mine) push_qk(rk);
+                        if (next_mine) push_qk(rk);
                         commit_pv();
-                        mma_commit(&slot_empty[rv % C::kSlots]);
-                        if (!kEarlyK && next_mine) {
-                            if (!wait_slot(rk)) { ok = false; break; }
-                            tc_fence_after();
-                            push_qk(rk);
-                        }
-                        if (next_mine) { commit_qk(); mma_commit(&slot_empty[rk % C::kSlots]); }
+                        release_tile(rv);
+                        if (next_mine) { commit_qk(); release_tile(rk); }
                     } else if (!release_unused(rv)) {
                         ok = false; break;
                     }
@@ -368,7 +413,7 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                 }
                 if (!ok) break;
                 other += n_other;
-                rp = r0 + 2 * u.nmax;
+                rp = r0 + (uint32_t)(2 * C::kItems * u.nmax);
                 mma_commit(q_empty);
                 ++nu;
             }
@@ -390,6 +435,14 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         const bool scale_pos = p.scale_log2 >= 0.f;
         uint32_t s_cnt = 0, pv_cnt = 0;
+        // Completion of this tile's PV number i.  With one query tile the
+        // softmax may run a tile ahead of the PVs, so PVs alternate between two
+        // barriers (like the S buffers) to keep every wait within one phase.
+        auto wait_pv = [&](uint32_t i) {
+            if constexpr (NQ == 2) mbar_wait(&pv_done[x], i & 1u, wc);
+            else mbar_wait(&pv_done[i & 1u], (i >> 1) & 1u, wc);
+            tc_fence_after();
+        };
         for (int k = 0;; ++k) {
             const int idx = snake_index(k, p.grid);
             if (idx >= count) break;
@@ -461,12 +514,12 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                     }
                     return ((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]));
                 };
-                // The previous PV of this tile must have landed before its P is
-                // overwritten or O is rescaled.
-                if (j > 0) {
-                    mbar_wait(&pv_done[x], (pv_cnt + j - 1) & 1, wc);
-                    tc_fence_after();
-                }
+                // With two query tiles P overwrites the tile's only S buffer,
+                // which the previous PV reads, so that PV must have landed first.
+                // With one tile P(j) goes to S buffer j & 1, which PV(j-1) does
+                // not read (PV(j-2) did, and it finished before QK(j) wrote S(j));
+                // there only a rescale of O has to wait for the previous PV.
+                if (NQ == 2 && j > 0) wait_pv(pv_cnt + j - 1);
                 // Static anchor ("Flywheel Attention", section 3.1 and appendix
                 // A): a row's anchor is the max of the first tile in which it sees
                 // a key and does not move on the fast path, so the exponent pass
@@ -488,6 +541,7 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                         m_ref = m_new;
                     }
                     if (j > 0) {
+                        if (NQ == 1) wait_pv(pv_cnt + j - 1);
 #pragma unroll
                         for (int c = 0; c < D / 32; ++c) {
                             float o[32];
@@ -506,14 +560,13 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&p_full[NQ == 2 ? x : 0]);
+                if (lane == 0) mbar_arrive(&p_full[NQ == 2 ? x : (int)(s_cnt & 1u)]);
             }
             // ------------------------------------------------------ epilogue
             __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(p.out) +
                                   (int64_t)(u.s.q0 + q_row) * p.out_stride[0] + (int64_t)u.h * p.out_stride[1];
             if (nkv > 0) {
-                mbar_wait(&pv_done[x], (pv_cnt + nkv - 1) & 1, wc);
-                tc_fence_after();
+                wait_pv(pv_cnt + nkv - 1);
                 const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
