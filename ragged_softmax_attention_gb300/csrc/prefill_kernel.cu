@@ -79,6 +79,12 @@ struct PrefillCfg {
 
 __device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
 
+// Bulk prefetch of one tensor-map box into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void l2_prefetch_3d(const void *tmap, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
+                 :: "l"(tmap), "r"(c0), "r"(c1), "r"(c2) : "memory");
+}
+
 // Ring order of a unit's K and V tiles, in blocks of kItems ring items.
 // Two query tiles (one item per tile): K_0 V_0 K_1 V_1 ..., the order the
 // two issuers' steps need them.  One query tile, whose QKs run two tiles
@@ -240,7 +246,21 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                 }
                 // The unit's K and V tiles through the ring, item by item, in
                 // ring order (ring_block_k / ring_block_v).
+                // One query tile (head dim 256): the ring holds little more than
+                // one step of items, and the concurrently running units touch
+                // about as much K/V as L2 holds, so tiles are also prefetched
+                // into L2 two steps ahead of their ring loads.
+                constexpr int kL2Ahead = NQ == 1 ? 2 : 0;
+                auto prefetch_tile = [&](int j) {
+                    if (j >= u.nmax) return;
+                    for (int c = 0; c < C::kChunks; ++c) {
+                        l2_prefetch_3d(&tm_k, c * 64, u.g, u.s.k0 + j * kKvTile);
+                        l2_prefetch_3d(&tm_v, c * 64, u.g, u.s.k0 + j * kKvTile);
+                    }
+                };
+                for (int j = 0; j < kL2Ahead; ++j) prefetch_tile(j);
                 auto load_tile = [&](bool is_v, int j) {
+                    if (kL2Ahead > 0 && is_v) prefetch_tile(j + kL2Ahead);
                     for (int h = 0; h < C::kItems && ok; ++h, ++rp) {
                         const int sl = rp % C::kSlots;
                         ok = mbar_wait(&slot_empty[sl], ((rp / C::kSlots) & 1) ^ 1, wc);
