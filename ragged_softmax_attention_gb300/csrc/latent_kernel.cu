@@ -238,19 +238,24 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
         // end are not loaded; with `zero_tail`, rows at or past k_end are
         // cleared once the copy has landed (their V values may be anything,
         // and a zero probability times a NaN would still be NaN).
-        auto load_chunk = [&](int b, int g, int ts, int k_end, const CUtensorMap *tm, int c, bool zero_tail) -> bool {
+        // Physical pages of the 128-key tile at key ts of row b: lane l holds
+        // the tile's l-th page (l < pages in the tile).  Read one tile ahead
+        // of use, so no chunk load waits on the block table.
+        auto tile_pages = [&](int b, int ts, int k_end) {
+            int npages = 1;
+            if (p.ps < kKvTile) npages = min(kKvTile / p.ps, ceil_div_i(k_end - ts, p.ps));
+            int phys = 0;
+            if (lane < npages) phys = __ldg(p.block_table + (int64_t)b * p.bt_stride + ts / p.ps + lane);
+            return phys;
+        };
+        auto load_chunk = [&](int g, int ts, int k_end, int phys, const CUtensorMap *tm, int c, bool zero_tail) -> bool {
             const uint32_t s = m % kSlots;
             if (!warp_wait(&slot_empty[s], ((m / kSlots) & 1) ^ 1, wc, lane)) return false;
             const int halves = c < 4 ? 2 : 1;
             int npages = 1, slot0 = 0;
             if (p.ps < kKvTile) npages = min(kKvTile / p.ps, ceil_div_i(k_end - ts, p.ps));
             else slot0 = ts % p.ps;
-            const int lp0 = ts / p.ps;
-            int phys = 0;
-            if (lane < npages) {
-                phys = __ldg(p.block_table + (int64_t)b * p.bt_stride + lp0 + lane);
-                if ((unsigned)phys >= (unsigned)p.num_pages) { record_error(p.status, 1); phys = 0; }
-            }
+            if (lane < npages && (unsigned)phys >= (unsigned)p.num_pages) { record_error(p.status, 1); phys = 0; }
             const bool zero = zero_tail && ts + kKvTile > k_end;
             uint64_t *bar = zero ? tail_bar : &slot_full[s];
             const uint32_t bytes = (uint32_t)(npages * box_rows * 128 * halves);
@@ -284,7 +289,7 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
             return true;
         };
         bool ok = true;
-        int pb = -1, pg = 0, pts = 0, pend_end = 0;       // the tile whose PV is still to be fed
+        int pb = -1, pg = 0, pts = 0, pend_end = 0, pphys = 0;   // the tile whose PV is still to be fed
         LatIter it;
         it.init(p);
         LatPiece x;
@@ -297,16 +302,20 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
             }
             __syncwarp();
             ++nq;
+            int nphys = tile_pages(x.b, x.k_begin, x.k_end);
             for (int i = 0; i < x.ntiles && ok; ++i) {
                 const int ts = x.k_begin + i * kKvTile;
-                for (int c = 0; c < kQkChunks && ok; ++c) ok = load_chunk(x.b, x.g, ts, x.k_end, &tm_k, c, false);
+                const int phys = nphys;
+                if (i + 1 < x.ntiles) nphys = tile_pages(x.b, ts + kKvTile, x.k_end);
+                for (int c = 0; c < kQkChunks && ok; ++c) ok = load_chunk(x.g, ts, x.k_end, phys, &tm_k, c, false);
                 if (pb >= 0)
-                    for (int c = 0; c < kPvChunks && ok; ++c) ok = load_chunk(pb, pg, pts, pend_end, &tm_v, c, true);
-                pb = x.b; pg = x.g; pts = ts; pend_end = x.k_end;
+                    for (int c = 0; c < kPvChunks && ok; ++c)
+                        ok = load_chunk(pg, pts, pend_end, pphys, &tm_v, c, true);
+                pb = x.b; pg = x.g; pts = ts; pend_end = x.k_end; pphys = phys;
             }
         }
         if (ok && pb >= 0)
-            for (int c = 0; c < kPvChunks && ok; ++c) ok = load_chunk(pb, pg, pts, pend_end, &tm_v, c, true);
+            for (int c = 0; c < kPvChunks && ok; ++c) ok = load_chunk(pg, pts, pend_end, pphys, &tm_v, c, true);
         // Do not leave the CTA while copies it issued may still land.
         if (lane == 0) {
             for (uint32_t k = 0; k < (uint32_t)kSlots && k < m; ++k) {
