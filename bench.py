@@ -328,8 +328,8 @@ def bench_prefill(fw, torch, steps, warmup, device, peaks, name=None):
         raise RuntimeError("device status nonzero during the prefill benchmark")
     per = kms / max(1, kn)
     ach = flops / (per * 1e-3) / 1e12
-    traffic = (ncu_traffic("varlen_prefill_gqa_ncu.json", ["prefill_kernel.cu", "fw_ptx.cuh"], flops)
-               if name == PREFILL_WL else None)
+    profile = {PREFILL_WL: "varlen_prefill_gqa_ncu.json", PREFILL_HD256_WL: "varlen_prefill_hd256_ncu.json"}[name]
+    traffic = ncu_traffic(profile, ["prefill_kernel.cu", "fw_ptx.cuh"], flops)
     return {"workload": name, "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 4), "steps": n, "flops_per_step": flops,
             "gpu_launches": fw.launch_count() - l0,
@@ -402,7 +402,8 @@ def bench_latent(fw, torch, steps, warmup, device, peaks, batch=None):
                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": round(ach / peaks["bf16_tflops"], 4),
                          "frac_of_sustained": round(ach / peaks["bf16_tflops_sustained"], 4),
-                         "traffic": None, "peak_source": peaks["source"], "kernel_ms_per_launch": round(per, 4)}}
+                         "traffic": ncu_traffic("latent_decode_ncu.json", ["latent_kernel.cu", "fw_ptx.cuh"],
+                                                sum(lens)), "peak_source": peaks["source"], "kernel_ms_per_launch": round(per, 4)}}
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -489,7 +490,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--only", choices=["all", "decode", "prefill", "latent"], default="all",
+    ap.add_argument("--only", choices=["all", "decode", "prefill", "prefill256", "latent"], default="all",
                     help="profiling runs: time one path only")
     ap.add_argument("--decode-batch", type=int, default=0,
                     help="profiling runs: a prefix of the decode batch (smaller capture)")
@@ -520,10 +521,12 @@ def main():
 
     if pg:
         pg.barrier()
-    if args.only == "prefill":
-        pre = bench_prefill(fw, torch, args.steps, args.warmup, device, peaks)
+    if args.only in ("prefill", "prefill256"):
+        key = "prefill" if args.only == "prefill" else "prefill_hd256"
+        pre = bench_prefill(fw, torch, args.steps, args.warmup, device, peaks,
+                            name=PREFILL_WL if args.only == "prefill" else PREFILL_HD256_WL)
         if rank == 0:
-            print(json.dumps({"prefill": pre}), flush=True)
+            print(json.dumps({key: pre}), flush=True)
         return 0
     if args.only == "latent":
         lat = bench_latent(fw, torch, args.steps, args.warmup, device, peaks, batch=args.latent_batch or None)
