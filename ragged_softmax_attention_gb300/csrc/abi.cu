@@ -628,6 +628,7 @@ fw_status_t fw_varlen_prefill(const fw_tensor_t *q, const fw_tensor_t *k, const 
     p.list_capacity = capacity;
     int64_t grid = d->num_sms;
     if (g_opt_max_ctas > 0 && grid > g_opt_max_ctas) grid = g_opt_max_ctas;
+    if (Dk == 256) grid = grid < 2 ? 2 : grid & ~int64_t(1);   // whole CTA pairs
     p.grid = (int)grid;
 
     CUtensorMap tq, tk, tv;
@@ -639,7 +640,9 @@ fw_status_t fw_varlen_prefill(const fw_tensor_t *q, const fw_tensor_t *k, const 
         if (total_k > 0) {
             const uint64_t dk[3] = {(uint64_t)Dk, (uint64_t)Hkv, (uint64_t)total_k};
             const uint64_t sk[2] = {(uint64_t)k->stride[1] * 2, (uint64_t)k->stride[0] * 2};
-            if (fw_status_t s = encode_bf16(&tk, k->data, 3, dk, sk, box, "k")) return s;
+            // Head dim 256 runs on CTA pairs that each load half (64 keys) of a K tile.
+            const uint32_t kbox[3] = {64, 1, Dk == 256 ? 64u : 128u};
+            if (fw_status_t s = encode_bf16(&tk, k->data, 3, dk, sk, kbox, "k")) return s;
             const uint64_t dv[3] = {(uint64_t)Dv, (uint64_t)Hkv, (uint64_t)total_k};
             const uint64_t sv[2] = {(uint64_t)v->stride[1] * 2, (uint64_t)v->stride[0] * 2};
             if (fw_status_t s = encode_bf16(&tv, v->data, 3, dv, sv, box, "v")) return s;

@@ -17,8 +17,9 @@
 // softmax warpgroups alternate with the tensor core: while one group turns
 // its S into P, the MMA warp runs the other tile's PV and QK ("Flywheel
 // Attention", section 1: two compute groups alternate so that one's softmax
-// overlaps the other's matmuls).  D = 256: one query tile per unit, S double
-// buffered (2 x 128 columns) next to O (256 columns).
+// overlaps the other's matmuls).  D = 256: the same two query tiles run on a
+// pair of CTAs (varlen_prefill_pair_kernel below), one tile each, with
+// cta_group::2 MMAs whose K and V operands the pair splits between its SMs.
 //
 // Warp roles: warp 0 TMA producer (Q tiles, then K_j / V_j through a ring of
 // shared-memory slots), warp 1 MMA issuer of query tile 0 and TMEM owner,
@@ -622,6 +623,464 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
     if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
+// ------------------------------------------------- head dim 256, CTA pairs
+//
+// A cluster of two CTAs runs one unit of two consecutive 128-row query tiles
+// (tile 2u in CTA 0, tile 2u+1 in CTA 1) with tcgen05.mma.cta_group::2,
+// issued by CTA 0 for both:
+//   S [256 x 128]  = Q [256 x 256] * K_tile^T      M = 256 rows, N = 128 keys
+//   O [256 x 256] += P [256 x 128] * V_tile        M = 256 rows, N = 256 columns
+// Each CTA holds its own query tile (A) and its TMEM holds its own 128 rows
+// of S and O; the B operands are split between the pair: CTA r loads keys
+// [64r, 64r + 64) of each K tile and value columns [128r, 128r + 128) of each
+// V tile.  Every SM so moves 64 KiB of K/V per 128-key step instead of 128
+// KiB, which is what a one-tile CTA at head dim 256 was bound by.
+//
+// Synchronisation across the pair: both CTAs' copies complete on CTA 0's
+// barriers (slot_full, q_full); CTA 0's commits arrive on both CTAs'
+// barriers (multicast: slot_empty, q_empty, s_full, pv_done); both CTAs'
+// softmax warps arrive on CTA 0's p_full.
+
+constexpr int kPairSlots = 5;
+constexpr int kPairSlotBytes = 32768;          // half a K tile (64 x 256) or half a V tile (128 x 128)
+constexpr int kPairQBytes = 128 * 256 * 2;
+constexpr int kPairOffRing = kPairQBytes;
+constexpr int kPairOffBar = kPairOffRing + kPairSlots * kPairSlotBytes;
+constexpr int kPairNumBars = 2 * kPairSlots + 2 + 2 + 2 + 2 + 2 + 2;
+constexpr int kPairOffMisc = kPairOffBar + kPairNumBars * 8;
+constexpr int kPairSmemBytes = kPairOffMisc + 16 + 1024;
+static_assert(kPairSmemBytes <= 232448, "shared memory budget of one CTA exceeded");
+constexpr uint32_t kPairIdescQK = idesc_bf16_f32(256, 128, false, false);
+constexpr uint32_t kPairIdescPV = idesc_bf16_f32(256, 256, false, true);
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of this CTA's shared variable `p` in the shared memory of cluster CTA `cta`.
+__device__ __forceinline__ uint32_t cluster_addr(const void *p, uint32_t cta) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(cta));
+    return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(bar_cluster_addr) : "memory");
+}
+// TMA tile load into this CTA's shared memory whose completion is counted on
+// an mbarrier of either CTA of the pair.
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void *tmap, uint32_t bar_cluster_addr,
+                                                 int32_t c0, int32_t c1, int32_t c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];"
+        :: "r"(dst), "l"(tmap), "r"(bar_cluster_addr), "r"(c0), "r"(c1), "r"(c2) : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(smem_u32(dst)), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void mma_pair_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                 :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+__device__ __forceinline__ void mma_pair_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                 :: "r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+// Arrive on the mbarrier at this offset in both CTAs of the pair once all
+// MMAs issued so far have completed.
+__device__ __forceinline__ void mma_commit_pair(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+                 :: "r"(smem_u32(bar)), "h"((uint16_t)3) : "memory");
+}
+
+// Bounded wait (as mbar_wait) whose acquire reaches cluster scope: for
+// barriers that threads of the other CTA of the pair arrive on.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, const WaitCtx &w) {
+    const uint32_t a = smem_u32(bar);
+    auto try_once = [&]() {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok) : "r"(a), "r"(parity) : "memory");
+        return ok != 0;
+    };
+    if (try_once()) return true;
+    if (*w.abort_flag) return false;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (try_once()) return true;
+        if ((it & 255u) == 0) {
+            if (*w.abort_flag) return false;
+            if (global_timer_ns() - t0 > w.timeout_ns) {
+                record_error(w.status, 5 /* FW_ERR_DEVICE_TIMEOUT */);
+                *w.abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// Snake over the cost-sorted list, one entry per CTA pair.
+__device__ __forceinline__ int pair_snake_index(int k) {
+    const int nc = (int)gridDim.x >> 1, c = (int)blockIdx.x >> 1;
+    return k * nc + ((k & 1) ? (nc - 1 - c) : c);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
+varlen_prefill_pair_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tm_q,
+                           const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
+    constexpr int D = 256;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sQ = smem;
+    uint8_t *sRing = smem + kPairOffRing;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kPairOffBar);
+    uint64_t *slot_full = bars;                          // CTA 0's count both CTAs' copies
+    uint64_t *slot_empty = slot_full + kPairSlots;
+    uint64_t *q_full = slot_empty + kPairSlots;          // [1], CTA 0's counts both Q tiles
+    uint64_t *q_empty = q_full + 2;                      // [1]
+    uint64_t *s_full = q_empty + 2;                      // [2]
+    uint64_t *p_full = s_full + 2;                       // [2], CTA 0's counts both CTAs' warps
+    uint64_t *pv_done = p_full + 2;                      // [2]
+    uint64_t *drain = pv_done + 2;                       // [1]: CTA 0's MMAs all complete
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kPairOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kPairOffMisc + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const int count = __ldg(p.plan + 0);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kPairSlots; ++i) { mbar_init(&slot_full[i], 1); mbar_init(&slot_empty[i], 1); }
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
+        for (int i = 0; i < 2; ++i) { mbar_init(&s_full[i], 1); mbar_init(&p_full[i], 8); mbar_init(&pv_done[i], 1); }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_q); tma_prefetch_desc(&tm_k); tma_prefetch_desc(&tm_v);
+    }
+    if (warp == 1) { tmem_alloc_pair(tmem_slot, 512); tmem_relinquish_pair(); }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();                                  // both CTAs' barriers exist before any remote use
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtx wc{p.status, p.timeout_ns, abort_flag};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint32_t q_full0 = cluster_addr(q_full, 0);
+            uint32_t rp = 0, nu = 0;
+            bool ok = true;
+            for (int k = 0; ok; ++k, ++nu) {
+                const int idx = pair_snake_index(k);
+                if (idx >= count) break;
+                PUnit u;
+                decode_entry(p, __ldg(p.list + idx), u, 2);
+                if (!mbar_wait(q_empty, (nu & 1) ^ 1, wc)) break;
+                // A CTA whose tile does not exist loads its partner's rows
+                // (finite values; its outputs are never written).
+                const int tile = u.tile[rank] >= 0 ? u.tile[rank] : u.tile[0];
+                if (rank == 0) mbar_arrive_expect_tx(q_full, 2u * kPairQBytes);
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_3d_pair(smem_u32(sQ + c * 128 * 128), &tm_q, q_full0, c * 64, u.h,
+                                     u.s.q0 + tile * kQTile);
+                const int n = u.nmax;
+                auto prefetch_tile = [&](int j) {
+                    if (j >= n) return;
+                    const int key = u.s.k0 + j * kKvTile;
+                    for (int c = 0; c < D / 64; ++c) l2_prefetch_3d(&tm_k, c * 64, u.g, key + (int)rank * 64);
+                    for (int c = 0; c < 2; ++c) l2_prefetch_3d(&tm_v, (int)rank * 128 + c * 64, u.g, key);
+                };
+                for (int j = 0; j < 2; ++j) prefetch_tile(j);
+                // This CTA's half of K_j or V_j, as one ring item.
+                auto load_half = [&](bool is_v, int j) {
+                    const int sl = rp % kPairSlots;
+                    ok = mbar_wait(&slot_empty[sl], ((rp / kPairSlots) & 1) ^ 1, wc);
+                    if (!ok) return;
+                    if (rank == 0) mbar_arrive_expect_tx(&slot_full[sl], 2u * kPairSlotBytes);
+                    const uint32_t full0 = cluster_addr(&slot_full[sl], 0);
+                    const uint32_t dst = smem_u32(sRing + sl * kPairSlotBytes);
+                    const int key = u.s.k0 + j * kKvTile;
+                    if (!is_v) {
+#pragma unroll
+                        for (int c = 0; c < D / 64; ++c)          // 64 keys x 64 columns per box
+                            tma_load_3d_pair(dst + c * 64 * 128, &tm_k, full0, c * 64, u.g, key + (int)rank * 64);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 2; ++c)                // 128 keys x 64 columns per box
+                            tma_load_3d_pair(dst + c * 128 * 128, &tm_v, full0, (int)rank * 128 + c * 64, u.g, key);
+                        prefetch_tile(j + 2);
+                    }
+                    ++rp;
+                };
+                for (int j = 0; j < 2 && j < n && ok; ++j) load_half(false, j);
+                for (int j = 0; j < n && ok; ++j) {
+                    load_half(true, j);
+                    if (ok && j + 2 < n) load_half(false, j + 2);
+                }
+            }
+            // CTA 0's slot_full / q_full phases complete only once both CTAs'
+            // copies have landed; CTA 0 drains them below, before the pair's
+            // final cluster barrier, so neither CTA leaves with a copy in flight.
+            if (rank == 0) {
+                for (uint32_t k = 0; k < (uint32_t)kPairSlots && k < rp; ++k) {
+                    const uint32_t r = rp - 1 - k;
+                    mbar_wait_drain(&slot_full[r % kPairSlots], (r / kPairSlots) & 1, wc);
+                }
+                if (nu > 0) mbar_wait_drain(q_full, (nu - 1) & 1, wc);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // -------------------------------------------------- MMA (CTA 0 only)
+        if (rank == 0 && lane == 0) {
+            uint32_t rp = 0, nu = 0, qk_cnt = 0, pv_cnt = 0;
+            const uint32_t q_base = smem_u32(sQ);
+            auto wait_slot = [&](uint32_t r) {
+                return mbar_wait(&slot_full[r % kPairSlots], (r / kPairSlots) & 1, wc);
+            };
+            auto push_qk = [&](uint32_t r_k) {
+                const uint32_t sc = (qk_cnt & 1u) * 128u;
+                const uint32_t k_base = smem_u32(sRing + (r_k % kPairSlots) * kPairSlotBytes);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t a = sdesc_sw128(q_base + (kk >> 2) * 128 * 128 + (kk & 3) * 32, 16, 1024);
+                    const uint64_t b = sdesc_sw128(k_base + (kk >> 2) * 64 * 128 + (kk & 3) * 32, 16, 1024);
+                    mma_pair_ss(tmem + sc, a, b, kPairIdescQK, kk > 0 ? 1u : 0u);
+                }
+            };
+            auto commit_qk = [&]() { mma_commit_pair(&s_full[qk_cnt & 1u]); ++qk_cnt; };
+            // P sits over the first 64 columns of the tile's S buffer, two BF16
+            // per column, in each CTA's TMEM.
+            auto push_pv = [&](uint32_t r_v, bool first) {
+                const uint32_t p_col = (pv_cnt & 1u) * 128u;
+                const uint32_t v_base = smem_u32(sRing + (r_v % kPairSlots) * kPairSlotBytes);
+#pragma unroll
+                for (int kk = 0; kk < kKvTile / 16; ++kk) {
+                    const uint64_t b = sdesc_sw128(v_base + kk * 16 * 128, 128 * 128, 1024);
+                    mma_pair_ts(tmem + 256u, tmem + p_col + kk * 8, b, kPairIdescPV, (first && kk == 0) ? 0u : 1u);
+                }
+            };
+            auto commit_pv = [&]() { mma_commit_pair(&pv_done[pv_cnt & 1u]); ++pv_cnt; };
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int idx = pair_snake_index(k);
+                if (idx >= count) break;
+                PUnit u;
+                decode_entry(p, __ldg(p.list + idx), u, 2);
+                if (!mbar_wait(q_full, nu & 1, wc)) break;
+                tc_fence_after();
+                const uint32_t r0 = rp;
+                const int n = u.nmax;
+                auto pos_k = [&](int j) { return r0 + (uint32_t)ring_block_k<1>(j, n); };
+                auto pos_v = [&](int j) { return r0 + (uint32_t)ring_block_v<1>(j, n); };
+                for (int j = 0; j < 2 && j < n && ok; ++j) {
+                    const uint32_t rk = pos_k(j);
+                    if (!wait_slot(rk)) { ok = false; break; }
+                    tc_fence_after();
+                    push_qk(rk);
+                    commit_qk();
+                    mma_commit_pair(&slot_empty[rk % kPairSlots]);
+                }
+                for (int j = 0; j < n && ok; ++j) {
+                    const bool next = j + 2 < n;
+                    const uint32_t rv = pos_v(j);
+                    const uint32_t rk = next ? pos_k(j + 2) : 0u;
+                    if (!wait_slot(rv) || (next && !wait_slot(rk)) ||
+                        !mbar_wait_cluster(&p_full[pv_cnt & 1u], (pv_cnt >> 1) & 1u, wc)) {
+                        ok = false; break;
+                    }
+                    tc_fence_after();
+                    push_pv(rv, j == 0);
+                    if (next) push_qk(rk);
+                    commit_pv();
+                    mma_commit_pair(&slot_empty[rv % kPairSlots]);
+                    if (next) { commit_qk(); mma_commit_pair(&slot_empty[rk % kPairSlots]); }
+                }
+                if (!ok) break;
+                rp = r0 + (uint32_t)(2 * n);
+                mma_commit_pair(q_empty);
+                ++nu;
+            }
+            // No MMA of the pair may still run when the pair frees TMEM.
+            mma_commit_pair(drain);
+            mbar_wait_drain(drain, 0, wc);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------- softmax / epilogue
+        // Thread = one row of this CTA's query tile.  Every unit walks the
+        // pair's KV tiles; a tile past this CTA's causal reach is fully masked
+        // (zero probabilities).  A CTA whose tile does not exist still takes
+        // part (its P gates CTA 0's PV) and writes nothing.
+        const int q4 = warp & 3;
+        const int row = q4 * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+        const bool scale_pos = p.scale_log2 >= 0.f;
+        uint32_t s_cnt = 0, pv_cnt = 0;
+        auto wait_pv = [&](uint32_t i) {
+            mbar_wait(&pv_done[i & 1u], (i >> 1) & 1u, wc);
+            tc_fence_after();
+        };
+        for (int k = 0;; ++k) {
+            const int idx = pair_snake_index(k);
+            if (idx >= count) break;
+            PUnit u;
+            decode_entry(p, __ldg(p.list + idx), u, 2);
+            const bool tile_ok = u.tile[rank] >= 0;
+            const int q_row = (tile_ok ? u.tile[rank] : u.tile[0]) * kQTile + row;
+            const bool row_valid = tile_ok && q_row < u.s.Lq;
+            const int lim = !p.causal ? u.s.Lk : max(0, min(u.s.Lk, q_row + u.s.Lk - u.s.Lq + 1));
+            const int n = u.nmax;
+            float m_ref = kNegInf, l_sum = 0.f;
+            for (int j = 0; j < n; ++j, ++s_cnt) {
+                const uint32_t sb = s_cnt & 1u;
+                mbar_wait(&s_full[sb], (s_cnt >> 1) & 1u, wc);
+                tc_fence_after();
+                const uint32_t sa = tmem + lane_off + sb * 128u;
+                const int key0 = j * kKvTile;
+                float sv[kKvTile];
+#pragma unroll
+                for (int c = 0; c < kKvTile / 32; ++c) tmem_ld32(sa + c * 32, sv + c * 32);
+                tmem_wait_ld();
+                if (key0 + kKvTile > lim) {
+#pragma unroll
+                    for (int i = 0; i < kKvTile; ++i)
+                        if (key0 + i >= lim) sv[i] = scale_pos ? kNegInf : -kNegInf;
+                }
+                auto row_max = [&]() -> float {
+                    float e8[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) e8[i] = sv[i];
+                    if (scale_pos) {
+#pragma unroll
+                        for (int i = 8; i < kKvTile; ++i) e8[i & 7] = fmaxf(e8[i & 7], sv[i]);
+                    } else {
+#pragma unroll
+                        for (int i = 8; i < kKvTile; ++i) e8[i & 7] = fminf(e8[i & 7], sv[i]);
+                    }
+                    const float ext = scale_pos
+                        ? fmaxf(fmaxf(fmaxf(e8[0], e8[1]), fmaxf(e8[2], e8[3])), fmaxf(fmaxf(e8[4], e8[5]), fmaxf(e8[6], e8[7])))
+                        : fminf(fminf(fminf(e8[0], e8[1]), fminf(e8[2], e8[3])), fminf(fminf(e8[4], e8[5]), fminf(e8[6], e8[7])));
+                    return (ext == kNegInf || ext == -kNegInf) ? kNegInf : ext * p.scale_log2;
+                };
+                auto write_p = [&](float anchor) -> float {
+                    const float mu = (anchor == kNegInf) ? 0.f : anchor;
+                    float a8[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) a8[i] = 0.f;
+#pragma unroll
+                    for (int c = 0; c < kKvTile / 32; ++c) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            const float p0 = ex2_approx(fmaf(sv[c * 32 + i], p.scale_log2, -mu));
+                            const float p1 = ex2_approx(fmaf(sv[c * 32 + i + 1], p.scale_log2, -mu));
+                            a8[(i >> 1) & 7] += p0 + p1;
+                            pk[i >> 1] = pack_bf16x2(p0, p1);
+                        }
+                        tmem_st16u(sa + c * 16, pk);
+                    }
+                    return ((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]));
+                };
+                // Static anchor and the running-sum check, as in the one-CTA
+                // kernel; P(j) goes to S buffer j & 1, which PV(j-1) does not read.
+                if (m_ref == kNegInf) m_ref = row_max();
+                float tsum = write_p(m_ref);
+                const bool over = !(l_sum + tsum <= kAnchorBudget);
+                if (__any_sync(0xffffffffu, over)) {
+                    float alpha = 1.f;
+                    if (over) {
+                        const float m_new = fmaxf(m_ref, row_max());
+                        alpha = ex2_approx(m_ref - m_new);
+                        l_sum *= alpha;
+                        m_ref = m_new;
+                    }
+                    if (j > 0) {
+                        wait_pv(pv_cnt + j - 1);
+#pragma unroll
+                        for (int c = 0; c < D / 32; ++c) {
+                            float o[32];
+                            const uint32_t oa = tmem + lane_off + 256u + c * 32;
+                            tmem_ld32(oa, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                            tmem_st32(oa, o);
+                        }
+                        tmem_wait_st();
+                    }
+                    tsum = write_p(m_ref);
+                }
+                l_sum += tsum;
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(cluster_addr(&p_full[s_cnt & 1u], 0));
+            }
+            // ------------------------------------------------------ epilogue
+            __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(p.out) +
+                                  (int64_t)(u.s.q0 + q_row) * p.out_stride[0] + (int64_t)u.h * p.out_stride[1];
+            if (n > 0) {
+                wait_pv(pv_cnt + n - 1);
+                const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    float o[32];
+                    tmem_ld32(tmem + lane_off + 256u + c * 32, o);
+                    tmem_wait_ld();
+                    if (row_valid) {
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            uint4 v;
+                            v.x = pack_bf16x2(o[8 * w + 0] * inv, o[8 * w + 1] * inv);
+                            v.y = pack_bf16x2(o[8 * w + 2] * inv, o[8 * w + 3] * inv);
+                            v.z = pack_bf16x2(o[8 * w + 4] * inv, o[8 * w + 5] * inv);
+                            v.w = pack_bf16x2(o[8 * w + 6] * inv, o[8 * w + 7] * inv);
+                            *reinterpret_cast<uint4 *>(orow + c * 32 + w * 8) = v;
+                        }
+                    }
+                }
+                tc_fence_before();
+            } else if (row_valid) {
+                for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4 *>(orow)[c] = make_uint4(0, 0, 0, 0);
+            }
+            if (row_valid && p.lse)
+                p.lse[(int64_t)(u.s.q0 + q_row) * p.lse_stride[0] + (int64_t)u.h * p.lse_stride[1]] =
+                    l_sum > 0.f ? (m_ref + __log2f(l_sum)) * 0.69314718055994531f : kNegInf;
+            pv_cnt += n;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();                                  // no MMA, copy or remote arrive of the pair is left
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem, 512);
+}
+
 // ------------------------------------------------------------------- plan
 //
 // One block.  PP[i] = exclusive prefix of the unit pairs per sequence; each
@@ -729,19 +1188,32 @@ cudaError_t launch_t(const PrefillParams &p, const CUtensorMap &tq, const CUtens
     return cudaGetLastError();
 }
 
+cudaError_t launch_pair(const PrefillParams &p, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                        cudaStream_t stream) {
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(varlen_prefill_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kPairSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    varlen_prefill_pair_kernel<<<p.grid & ~1, 256, kPairSmemBytes, stream>>>(p, tq, tk, tv);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                            const CUtensorMap &tv, int head_dim, cudaStream_t stream,
                            cudaEvent_t timing_start, cudaEvent_t timing_stop, int *launches) {
     *launches = 0;
-    prefill_plan_kernel<<<1, 1024, 0, stream>>>(p, head_dim == 128 ? PrefillCfg<128>::kNumQ : PrefillCfg<256>::kNumQ);
+    prefill_plan_kernel<<<1, 1024, 0, stream>>>(p, 2);           // units of two query tiles at both head dims
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     ++*launches;
     if (timing_start) cudaEventRecord(timing_start, stream);
     if (head_dim == 128) e = launch_t<128>(p, tq, tk, tv, stream);
-    else if (head_dim == 256) e = launch_t<256>(p, tq, tk, tv, stream);
+    else if (head_dim == 256) e = launch_pair(p, tq, tk, tv, stream);
     else return cudaErrorInvalidValue;
     if (e != cudaSuccess) return e;
     ++*launches;
