@@ -42,17 +42,15 @@ constexpr float kAnchorBudget = 4294967296.0f;
 constexpr int kQTile = 128;
 constexpr int kCostBins = 4096;
 
-template <int D>
+// Head dim 128, two query tiles per CTA.
 struct PrefillCfg {
-    static constexpr int kNumQ = (D == 128) ? 2 : 1;           // query tiles per unit
+    static constexpr int D = 128;
+    static constexpr int kNumQ = 2;                             // query tiles per unit
     static constexpr int kChunks = D / 64;
     static constexpr int kChunkBytes = 128 * 128;              // 128 rows x 64 bf16 columns
     static constexpr int kTileBytes = 128 * D * 2;              // one Q, K or V tile
-    // The K/V ring moves items of 128 keys x 128 columns (two 64-column
-    // blocks); a tile is D / 128 items.
-    static constexpr int kItems = D / 128;
-    static constexpr int kSlotBytes = 2 * kChunkBytes;
-    static constexpr int kSlots = (D == 128) ? 4 : 5;           // K/V ring slots (items)
+    static constexpr int kSlotBytes = kTileBytes;
+    static constexpr int kSlots = 4;                            // K/V ring slots
     static constexpr int kOffQ = 0;
     static constexpr int kOffRing = kOffQ + kNumQ * kTileBytes;
     static constexpr int kOffBar = kOffRing + kSlots * kSlotBytes;
@@ -67,14 +65,12 @@ struct PrefillCfg {
     // below gives 128 x 72 + 256 x 216 = 64512 <= 64512.
     static constexpr uint32_t kRegsControl = 72;
     static constexpr uint32_t kRegsSoftmax = 216;
-    static_assert(kNumQ == 1 || 128 * kRegsControl + 256 * kRegsSoftmax <= 384 * 168, "register split");
+    static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= 384 * 168, "register split");
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kKvTile, false, false);
-    static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, false, true);   // one item of V
-    // TMEM columns: S buffers then O accumulators
-    __device__ static constexpr uint32_t s_col(int tile, uint32_t cnt) {
-        return kNumQ == 2 ? (uint32_t)tile * 128u : (cnt & 1u) * 128u;
-    }
+    static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, false, true);
+    // TMEM columns: the two tiles' S buffers, then their O accumulators
+    __device__ static constexpr uint32_t s_col(int tile) { return (uint32_t)tile * 128u; }
     __device__ static constexpr uint32_t o_col(int tile) { return 256u + (uint32_t)tile * 128u; }
 };
 
@@ -86,21 +82,15 @@ __device__ __forceinline__ void l2_prefetch_3d(const void *tmap, int c0, int c1,
                  :: "l"(tmap), "r"(c0), "r"(c1), "r"(c2) : "memory");
 }
 
-// Ring order of a unit's K and V tiles, in blocks of kItems ring items.
-// Two query tiles (one item per tile): K_0 V_0 K_1 V_1 ..., the order the
-// two issuers' steps need them.  One query tile, whose QKs run two tiles
-// ahead of its PVs: K_0 K_1, then V_j followed by K_{j+2} -- the order its
-// single issuer consumes them, so a ring of a few items always holds the
-// next loads.
-template <int NQ>
-__device__ __forceinline__ int ring_block_v(int j, int n) {
-    if constexpr (NQ == 2) return 2 * j + 1;
+// Ring order of a unit's K and V tiles when one issuer's QKs run two tiles
+// ahead of its PVs (the CTA-pair kernel): K_0 K_1, then V_j followed by
+// K_{j+2} -- the order the issuer consumes them, so a ring of a few items
+// always holds the next loads.  (The two-tile kernel uses K_0 V_0 K_1 V_1 ...)
+__device__ __forceinline__ int ring_pos_v(int j, int n) {
     return min(2, n) + j + min(j, max(0, n - 2));
 }
-template <int NQ>
-__device__ __forceinline__ int ring_block_k(int j, int n) {
-    if constexpr (NQ == 2) return 2 * j;
-    return j < 2 ? j : ring_block_v<NQ>(j - 2, n) + 1;
+__device__ __forceinline__ int ring_pos_k(int j, int n) {
+    return j < 2 ? j : ring_pos_v(j - 2, n) + 1;
 }
 
 struct Seq {
@@ -174,11 +164,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-template <int D>
-__global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
+__global__ void __launch_bounds__(PrefillCfg::kThreads, 1)
 varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
-    using C = PrefillCfg<D>;
+    using C = PrefillCfg;
+    constexpr int D = C::D;
     constexpr int NQ = C::kNumQ;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -223,7 +213,7 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
     const WaitCtx wc{p.status, p.timeout_ns, abort_flag};
 
     if (warp < 4) {
-      if constexpr (NQ == 2) setmaxnreg_dec<C::kRegsControl>();
+      setmaxnreg_dec<C::kRegsControl>();
       if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
@@ -245,43 +235,19 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                         tma_load_3d(smem_u32(sQ + x * C::kTileBytes + c * C::kChunkBytes), &tm_q, q_full,
                                     c * 64, u.h, u.s.q0 + u.tile[x] * kQTile);
                 }
-                // The unit's K and V tiles through the ring, item by item, in
-                // ring order (ring_block_k / ring_block_v).
-                // One query tile (head dim 256): the ring holds little more than
-                // one step of items, and the concurrently running units touch
-                // about as much K/V as L2 holds, so tiles are also prefetched
-                // into L2 two steps ahead of their ring loads.
-                constexpr int kL2Ahead = NQ == 1 ? 2 : 0;
-                auto prefetch_tile = [&](int j) {
-                    if (j >= u.nmax) return;
-                    for (int c = 0; c < C::kChunks; ++c) {
-                        l2_prefetch_3d(&tm_k, c * 64, u.g, u.s.k0 + j * kKvTile);
-                        l2_prefetch_3d(&tm_v, c * 64, u.g, u.s.k0 + j * kKvTile);
-                    }
-                };
-                for (int j = 0; j < kL2Ahead; ++j) prefetch_tile(j);
-                auto load_tile = [&](bool is_v, int j) {
-                    if (kL2Ahead > 0 && is_v) prefetch_tile(j + kL2Ahead);
-                    for (int h = 0; h < C::kItems && ok; ++h, ++rp) {
+                // K_j and V_j of the unit, in that order, through the slot ring.
+                for (int j = 0; j < u.nmax && ok; ++j) {
+                    for (int kv = 0; kv < 2 && ok; ++kv, ++rp) {
                         const int sl = rp % C::kSlots;
                         ok = mbar_wait(&slot_empty[sl], ((rp / C::kSlots) & 1) ^ 1, wc);
                         if (!ok) break;
-                        mbar_arrive_expect_tx(&slot_full[sl], C::kSlotBytes);
+                        mbar_arrive_expect_tx(&slot_full[sl], C::kTileBytes);
 #pragma unroll
-                        for (int c = 0; c < 2; ++c)
+                        for (int c = 0; c < C::kChunks; ++c)
                             tma_load_3d(smem_u32(sRing + sl * C::kSlotBytes + c * C::kChunkBytes),
-                                        is_v ? (const void *)&tm_v : (const void *)&tm_k, &slot_full[sl],
-                                        (2 * h + c) * 64, u.g, u.s.k0 + j * kKvTile);
+                                        kv == 0 ? (const void *)&tm_k : (const void *)&tm_v, &slot_full[sl],
+                                        c * 64, u.g, u.s.k0 + j * kKvTile);
                         issued = rp + 1;
-                    }
-                };
-                if constexpr (NQ == 2) {
-                    for (int j = 0; j < u.nmax && ok; ++j) { load_tile(false, j); load_tile(true, j); }
-                } else {
-                    for (int j = 0; j < 2 && j < u.nmax && ok; ++j) load_tile(false, j);
-                    for (int j = 0; j < u.nmax && ok; ++j) {
-                        load_tile(true, j);
-                        if (j + 2 < u.nmax) load_tile(false, j + 2);
                     }
                 }
             }
@@ -291,7 +257,7 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
             }
         }
         __syncwarp();
-      } else if (warp == 1 || (NQ == 2 && warp == 2)) {
+      } else if (warp == 1 || warp == 2) {
         // ----------------------------------------------------------------- MMA
         // One issuing thread per query tile, so neither tile's MMAs queue
         // behind the other's issue: warp 1 drives tile 0, warp 2 tile 1.
@@ -304,50 +270,37 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
             // Pushes only: a thread's tcgen05.mma issue advances at the tensor
             // core's pace, and any wait between pushes lets the pipe drain, so
             // each step waits for everything first and commits afterwards.
-            // A tile at ring position r occupies items r .. r + kItems - 1.
-            auto wait_tile = [&](uint32_t r) {
-                for (int h = 0; h < C::kItems; ++h)
-                    if (!wait_slot(r + h)) return false;
-                return true;
-            };
-            auto release_tile = [&](uint32_t r) {
-                for (int h = 0; h < C::kItems; ++h) mma_commit(&slot_empty[(r + h) % C::kSlots]);
-            };
+            auto wait_tile = [&](uint32_t r) { return wait_slot(r); };
+            auto release_tile = [&](uint32_t r) { mma_commit(&slot_empty[r % C::kSlots]); };
             auto push_qk = [&](uint32_t r_k) {
-                const uint32_t sc = C::s_col(x, qk_cnt);
+                const uint32_t sc = C::s_col(x);
                 const uint32_t q_base = smem_u32(sQ + x * C::kTileBytes);
+                const uint32_t k_base = smem_u32(sRing + (r_k % C::kSlots) * C::kSlotBytes);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t k_base = smem_u32(sRing + ((r_k + (kk >> 3)) % C::kSlots) * C::kSlotBytes);
-                    const int kl = kk & 7;
                     const uint64_t a = sdesc_sw128(q_base + (kk >> 2) * C::kChunkBytes + (kk & 3) * 32, 16, 1024);
-                    const uint64_t b = sdesc_sw128(k_base + (kl >> 2) * C::kChunkBytes + (kl & 3) * 32, 16, 1024);
+                    const uint64_t b = sdesc_sw128(k_base + (kk >> 2) * C::kChunkBytes + (kk & 3) * 32, 16, 1024);
                     mma_bf16_ss(tmem + sc, a, b, C::kIdescQK, kk > 0 ? 1u : 0u);
                 }
             };
             auto commit_qk = [&]() {
-                mma_commit(&s_full[NQ == 2 ? x : (int)(qk_cnt & 1u)]);
+                mma_commit(&s_full[x]);
                 ++qk_cnt;
             };
             // P was written over the first 64 columns of this tile's S buffer
             // (two BF16 per 32-bit column): A operand straight from TMEM.
-            // Each item of V (128 value columns) accumulates into its own
-            // 128 columns of O.
             auto push_pv = [&](uint32_t r_v, bool first) {
-                const uint32_t p_col = C::s_col(x, pv_cnt);
+                const uint32_t p_col = C::s_col(x);
+                const uint32_t v_base = smem_u32(sRing + (r_v % C::kSlots) * C::kSlotBytes);
 #pragma unroll
-                for (int h = 0; h < C::kItems; ++h) {
-                    const uint32_t v_base = smem_u32(sRing + ((r_v + h) % C::kSlots) * C::kSlotBytes);
-#pragma unroll
-                    for (int kk = 0; kk < kKvTile / 16; ++kk) {
-                        const uint64_t b = sdesc_sw128(v_base + kk * 16 * 128, C::kChunkBytes, 1024);
-                        mma_bf16_ts(tmem + C::o_col(x) + h * 128, tmem + p_col + kk * 8, b, C::kIdescPV,
-                                    (first && kk == 0) ? 0u : 1u);
-                    }
+                for (int kk = 0; kk < kKvTile / 16; ++kk) {
+                    const uint64_t b = sdesc_sw128(v_base + kk * 16 * 128, C::kChunkBytes, 1024);
+                    mma_bf16_ts(tmem + C::o_col(x), tmem + p_col + kk * 8, b, C::kIdescPV,
+                                (first && kk == 0) ? 0u : 1u);
                 }
             };
             auto commit_pv = [&]() {
-                mma_commit(&pv_done[NQ == 2 ? x : (int)(pv_cnt & 1u)]);
+                mma_commit(&pv_done[x]);
                 ++pv_cnt;
             };
             // Each issuing thread releases every ring position of the unit
@@ -376,12 +329,12 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                 decode_entry(p, __ldg(p.list + idx), u, NQ);
                 if (!mbar_wait(q_full, nu & 1, wc)) break;
                 tc_fence_after();
-                const uint32_t r0 = rp;
-                auto pos_k = [&](int j) { return r0 + (uint32_t)(C::kItems * ring_block_k<NQ>(j, u.nmax)); };
-                auto pos_v = [&](int j) { return r0 + (uint32_t)(C::kItems * ring_block_v<NQ>(j, u.nmax)); };
+                const uint32_t r0 = rp;                       // K_j at r0 + 2j, V_j at r0 + 2j + 1
+                auto pos_k = [&](int j) { return r0 + 2u * (uint32_t)j; };
+                auto pos_v = [&](int j) { return r0 + 2u * (uint32_t)j + 1u; };
                 const int n = u.nkv[x];
-                const int n_other = NQ == 2 ? u.nkv[1 - x] : 0;
-                const int step = NQ == 2 ? 1 : 2;             // QKs run this far ahead of PVs
+                const int n_other = u.nkv[1 - x];
+                constexpr int step = 1;                       // QK_{j+1} goes out with PV_j
                 // prologue: the first `step` QKs
                 for (int j = 0; j < step && j < u.nmax && ok; ++j) {
                     const uint32_t rk = pos_k(j);
@@ -401,7 +354,7 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                     const uint32_t rk = jn < u.nmax ? pos_k(jn) : 0u;
                     const bool mine = j < n, next_mine = jn < n;
                     if (mine) {
-                        if (NQ == 2) {
+                        {
                             // tile 1 follows tile 0's step j; tile 0 follows tile 1's step j-1
                             const int dep = x == 1 ? j : j - 1;
                             if (dep >= 0 && dep < n_other && !mbar_wait(&issued[1 - x], (other + dep) & 1, wc)) {
@@ -412,8 +365,7 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                         // need only older items consumed), so PV and QK go out back
                         // to back.
                         if (!wait_tile(rv) || (next_mine && !wait_tile(rk)) ||
-                            !mbar_wait(&p_full[NQ == 2 ? x : (int)(pv_cnt & 1u)],
-                                       NQ == 2 ? (pv_cnt & 1u) : ((pv_cnt >> 1) & 1u), wc)) {
+                            !mbar_wait(&p_full[x], pv_cnt & 1u, wc)) {
                             ok = false; break;
                         }
                         tc_fence_after();
@@ -422,7 +374,7 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                         // pushed: the other issuer's waits then overlap that push,
                         // and its PV queues right behind it instead of after an
                         // empty pipe.
-                        if (NQ == 2) mbar_arrive(&issued[x]);
+                        mbar_arrive(&issued[x]);
                         if (next_mine) push_qk(rk);
                         commit_pv();
                         release_tile(rv);
@@ -434,7 +386,7 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                 }
                 if (!ok) break;
                 other += n_other;
-                rp = r0 + (uint32_t)(2 * C::kItems * u.nmax);
+                rp = r0 + (uint32_t)(2 * u.nmax);
                 mma_commit(q_empty);
                 ++nu;
             }
@@ -444,7 +396,7 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
         __syncwarp();
       }
     } else {
-        if constexpr (NQ == 2) setmaxnreg_inc<C::kRegsSoftmax>();
+        setmaxnreg_inc<C::kRegsSoftmax>();
         // ------------------------------------------------- softmax / epilogue
         // Warpgroup x owns query tile x of each unit; thread = one query row.
         // A failed wait does not change the control flow (no block-level
@@ -456,12 +408,9 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         const bool scale_pos = p.scale_log2 >= 0.f;
         uint32_t s_cnt = 0, pv_cnt = 0;
-        // Completion of this tile's PV number i.  With one query tile the
-        // softmax may run a tile ahead of the PVs, so PVs alternate between two
-        // barriers (like the S buffers) to keep every wait within one phase.
+        // Completion of this tile's PV number i.
         auto wait_pv = [&](uint32_t i) {
-            if constexpr (NQ == 2) mbar_wait(&pv_done[x], i & 1u, wc);
-            else mbar_wait(&pv_done[i & 1u], (i >> 1) & 1u, wc);
+            mbar_wait(&pv_done[x], i & 1u, wc);
             tc_fence_after();
         };
         for (int k = 0;; ++k) {
@@ -476,11 +425,9 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
             const int nkv = u.nkv[x];
             float m_ref = kNegInf, l_sum = 0.f;
             for (int j = 0; j < nkv; ++j, ++s_cnt) {
-                const int sb = NQ == 2 ? x : (int)(s_cnt & 1u);
-                const uint32_t spar = NQ == 2 ? (s_cnt & 1u) : ((s_cnt >> 1) & 1u);
-                mbar_wait(&s_full[sb], spar, wc);
+                mbar_wait(&s_full[x], s_cnt & 1u, wc);
                 tc_fence_after();
-                const uint32_t sa = tmem + lane_off + C::s_col(x, s_cnt);
+                const uint32_t sa = tmem + lane_off + C::s_col(x);
                 const int key0 = j * kKvTile;
                 // The whole row of S in registers with one TMEM round trip.
                 float sv[kKvTile];
@@ -535,12 +482,9 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                     }
                     return ((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]));
                 };
-                // With two query tiles P overwrites the tile's only S buffer,
-                // which the previous PV reads, so that PV must have landed first.
-                // With one tile P(j) goes to S buffer j & 1, which PV(j-1) does
-                // not read (PV(j-2) did, and it finished before QK(j) wrote S(j));
-                // there only a rescale of O has to wait for the previous PV.
-                if (NQ == 2 && j > 0) wait_pv(pv_cnt + j - 1);
+                // P overwrites the tile's only S buffer, which the previous PV
+                // reads, so that PV must have landed first.
+                if (j > 0) wait_pv(pv_cnt + j - 1);
                 // Static anchor ("Flywheel Attention", section 3.1 and appendix
                 // A): a row's anchor is the max of the first tile in which it sees
                 // a key and does not move on the fast path, so the exponent pass
@@ -562,7 +506,6 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                         m_ref = m_new;
                     }
                     if (j > 0) {
-                        if (NQ == 1) wait_pv(pv_cnt + j - 1);
 #pragma unroll
                         for (int c = 0; c < D / 32; ++c) {
                             float o[32];
@@ -581,7 +524,7 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&p_full[NQ == 2 ? x : (int)(s_cnt & 1u)]);
+                if (lane == 0) mbar_arrive(&p_full[x]);
             }
             // ------------------------------------------------------ epilogue
             __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(p.out) +
@@ -894,8 +837,8 @@ varlen_prefill_pair_kernel(const __grid_constant__ PrefillParams p, const __grid
                 tc_fence_after();
                 const uint32_t r0 = rp;
                 const int n = u.nmax;
-                auto pos_k = [&](int j) { return r0 + (uint32_t)ring_block_k<1>(j, n); };
-                auto pos_v = [&](int j) { return r0 + (uint32_t)ring_block_v<1>(j, n); };
+                auto pos_k = [&](int j) { return r0 + (uint32_t)ring_pos_k(j, n); };
+                auto pos_v = [&](int j) { return r0 + (uint32_t)ring_pos_v(j, n); };
                 for (int j = 0; j < 2 && j < n && ok; ++j) {
                     const uint32_t rk = pos_k(j);
                     if (!wait_slot(rk)) { ok = false; break; }
@@ -1155,9 +1098,36 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const __grid_constan
         atomicAdd(&bins[pair_bin(gp, sq)], 1);
     }
     __syncthreads();
-    if (tid == 0) {                                  // exclusive scan of the bins (4096 adds)
-        int acc = 0;
-        for (int i = 0; i < kCostBins; ++i) { const int c = bins[i]; bins[i] = acc; acc += c; }
+    {
+        // Exclusive scan of the bins: each thread scans its run of
+        // kCostBins / blockDim.x consecutive bins, then the run totals are
+        // scanned across the block (warp shuffles + one warp over warp sums).
+        constexpr int kPer = kCostBins / 1024;
+        static_assert(kCostBins % 1024 == 0, "bins per thread");
+        int run[kPer], tot = 0;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) { run[i] = bins[tid * kPer + i]; tot += run[i]; }
+        int incl = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) warp_sums[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            int w = warp_sums[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += v;
+            }
+            warp_sums[lane] = w;
+        }
+        __syncthreads();
+        int acc = (warp > 0 ? warp_sums[warp - 1] : 0) + incl - tot;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) { bins[tid * kPer + i] = acc; acc += run[i]; }
     }
     __syncthreads();
     for (int gp = tid; gp < NP; gp += blockDim.x) {
@@ -1173,18 +1143,17 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const __grid_constan
     }
 }
 
-template <int D>
-cudaError_t launch_t(const PrefillParams &p, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                     cudaStream_t stream) {
-    using C = PrefillCfg<D>;
+cudaError_t launch_tiles(const PrefillParams &p, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                         cudaStream_t stream) {
+    using C = PrefillCfg;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(varlen_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(varlen_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    varlen_prefill_kernel<D><<<p.grid, C::kThreads, C::kSmemBytes, stream>>>(p, tq, tk, tv);
+    varlen_prefill_kernel<<<p.grid, C::kThreads, C::kSmemBytes, stream>>>(p, tq, tk, tv);
     return cudaGetLastError();
 }
 
@@ -1212,7 +1181,7 @@ cudaError_t launch_prefill(const PrefillParams &p, const CUtensorMap &tq, const 
     if (e != cudaSuccess) return e;
     ++*launches;
     if (timing_start) cudaEventRecord(timing_start, stream);
-    if (head_dim == 128) e = launch_t<128>(p, tq, tk, tv, stream);
+    if (head_dim == 128) e = launch_tiles(p, tq, tk, tv, stream);
     else if (head_dim == 256) e = launch_pair(p, tq, tk, tv, stream);
     else return cudaErrorInvalidValue;
     if (e != cudaSuccess) return e;
