@@ -47,6 +47,11 @@ def _load():
         lib.oracle_paged_decode.restype = I
         lib.oracle_paged_decode.argtypes = [P, P, P, P, P, P, P, L, P, I, I, I, I, I, I, I, I, I, D,
                                             P, L, P, P, I]
+        lib.oracle_paged_decode_kv8.restype = I
+        lib.oracle_paged_decode_kv8.argtypes = [P, P, P, P, P, P, D, D, P, L, P, I, I, I, I, I, I, I, I, I, D,
+                                                P, L, P, P, I]
+        lib.oracle_e4m3_to_double.restype = D
+        lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
         lib.oracle_varlen_prefill.restype = I
         lib.oracle_varlen_prefill.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, D,
                                               P, L, P, P, I]
@@ -77,16 +82,32 @@ def default_threads() -> int:
     return max(1, os.cpu_count() or 1)
 
 
-def paged_decode(q, k_cache, v_cache, block_table, seq_lens, scale, rows=None, threads=None):
+def e4m3_to_double(byte: int) -> float:
+    """The oracle's decoding of one OCP FP8 E4M3 byte (NaN for S.1111.111)."""
+    return _load().oracle_e4m3_to_double(int(byte) & 0xFF)
+
+
+def paged_decode(q, k_cache, v_cache, block_table, seq_lens, scale, rows=None, threads=None,
+                 k_scale=1.0, v_scale=1.0):
     """Softmax attention of every (b, t, h) query row over its paged keys.
 
     q [B, q_len, Hq, Dk], k_cache [P, ps, Hkv, Dk], v_cache [P, ps, Hkv, Dv]
-    (bfloat16, any strides), block_table [B, max_pages] int32, seq_lens [B].
-    rows: optional flat row ids (b * q_len + t) * Hq + h to compute; default all.
+    (bfloat16, any strides; or float8_e4m3fn caches, whose values are taken
+    as k_scale * e4m3 and v_scale * e4m3), block_table [B, max_pages] int32,
+    seq_lens [B].  rows: optional flat row ids (b * q_len + t) * Hq + h to
+    compute; default all.
     Returns (out [n_rows, Dv] float64, lse [n_rows] float64, natural log).
     """
     lib = _load()
-    q, k_cache, v_cache = _bf16(q), _bf16(k_cache), _bf16(v_cache)
+    kv8 = k_cache.dtype == torch.float8_e4m3fn
+    if kv8:
+        if v_cache.dtype != torch.float8_e4m3fn:
+            raise TypeError("FP8 keys need FP8 values")
+        q = _bf16(q)
+        k_cache = k_cache.detach().cpu().view(torch.uint8)
+        v_cache = v_cache.detach().cpu().view(torch.uint8)
+    else:
+        q, k_cache, v_cache = _bf16(q), _bf16(k_cache), _bf16(v_cache)
     B, q_len, Hq, Dk = q.shape
     P, ps, Hkv, Dk2 = k_cache.shape
     Dv = v_cache.shape[3]
@@ -102,12 +123,21 @@ def paged_decode(q, k_cache, v_cache, block_table, seq_lens, scale, rows=None, t
     out = np.zeros((n, Dv), dtype=np.float64)
     lse = np.zeros((n,), dtype=np.float64)
     qs, ks, vs = _strides(q), _strides(k_cache), _strides(v_cache)
-    rc = lib.oracle_paged_decode(
-        q.data_ptr(), qs.ctypes.data, k_cache.data_ptr(), ks.ctypes.data,
-        v_cache.data_ptr(), vs.ctypes.data, bt.ctypes.data, bt.shape[1], sl.ctypes.data,
-        B, q_len, Hq, Hkv, Dk, Dv, ps, P, bt.shape[1], float(scale),
-        rows_arr.ctypes.data, n, out.ctypes.data, lse.ctypes.data,
-        int(threads or default_threads()))
+    if kv8:
+        rc = lib.oracle_paged_decode_kv8(
+            q.data_ptr(), qs.ctypes.data, k_cache.data_ptr(), ks.ctypes.data,
+            v_cache.data_ptr(), vs.ctypes.data, float(k_scale), float(v_scale),
+            bt.ctypes.data, bt.shape[1], sl.ctypes.data,
+            B, q_len, Hq, Hkv, Dk, Dv, ps, P, bt.shape[1], float(scale),
+            rows_arr.ctypes.data, n, out.ctypes.data, lse.ctypes.data,
+            int(threads or default_threads()))
+    else:
+        rc = lib.oracle_paged_decode(
+            q.data_ptr(), qs.ctypes.data, k_cache.data_ptr(), ks.ctypes.data,
+            v_cache.data_ptr(), vs.ctypes.data, bt.ctypes.data, bt.shape[1], sl.ctypes.data,
+            B, q_len, Hq, Hkv, Dk, Dv, ps, P, bt.shape[1], float(scale),
+            rows_arr.ctypes.data, n, out.ctypes.data, lse.ctypes.data,
+            int(threads or default_threads()))
     if rc != 0:
         raise ValueError(f"oracle_paged_decode failed with code {rc}")
     return out, lse

@@ -34,7 +34,13 @@
  *   keys 0 .. r + Lk - Lq (bottom-right alignment, as the page's benchmark
  *   command selects with --bottom_right_align).
  *
- * Inputs are BF16 bit patterns (uint16); each is widened exactly to double.
+ * FP8 KV cache (oracle_paged_decode_kv8; "TokenSpeed-MLA 2.0.1": decode on
+ * FP8 inputs writes BF16 output): keys and values are OCP FP8 E4M3 bytes with
+ * one scale each for the whole cache, k_j = k_scale * e4m3(K byte), v_j =
+ * v_scale * e4m3(V byte); the attention itself is the same definition.
+ *
+ * Inputs are BF16 bit patterns (uint16) or E4M3 bytes; each is widened
+ * exactly to double.
  * Strides are in elements.  Every function returns 0 on success or a negative
  * code for an out-of-range index (an invalid page number, a bad row id).
  */
@@ -49,6 +55,19 @@ static double bf16_to_double(uint16_t bits) {
     float f;
     memcpy(&f, &w, sizeof f);
     return (double)f;
+}
+
+/* OCP 8-bit floating point, E4M3 ("FN" variant): 1 sign bit, 4 exponent bits
+ * with bias 7, 3 mantissa bits; exponent 0 encodes subnormals m * 2^-9; the
+ * pattern S.1111.111 is NaN; there is no infinity (S.1111.110 = 448 is the
+ * largest finite value). */
+double oracle_e4m3_to_double(uint8_t b) {
+    int sign = b >> 7, e = (b >> 3) & 15, m = b & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);
+    else v = ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -v : v;
 }
 
 /* One query row against an explicit list of key/value row pointers. */
@@ -81,12 +100,43 @@ static void attend_row(const uint16_t *q, int64_t q_dstride,
     *lse = m + log(l);
 }
 
+/* The same row with FP8 E4M3 key and value rows and their scales. */
+static void attend_row_kv8(const uint16_t *q, int64_t q_dstride,
+                           const uint8_t *const *krows, int64_t k_dstride, double k_scale,
+                           const uint8_t *const *vrows, int64_t v_dstride, double v_scale,
+                           int64_t nkeys, int dk, int dv, double scale,
+                           double *s, double *out, double *lse) {
+    if (nkeys <= 0) {
+        for (int d = 0; d < dv; ++d) out[d] = 0.0;
+        *lse = -INFINITY;
+        return;
+    }
+    double m = -INFINITY;
+    for (int64_t j = 0; j < nkeys; ++j) {
+        double acc = 0.0;
+        for (int d = 0; d < dk; ++d)
+            acc += bf16_to_double(q[d * q_dstride]) * (k_scale * oracle_e4m3_to_double(krows[j][d * k_dstride]));
+        s[j] = scale * acc;
+        if (s[j] > m) m = s[j];
+    }
+    double l = 0.0;
+    for (int d = 0; d < dv; ++d) out[d] = 0.0;
+    for (int64_t j = 0; j < nkeys; ++j) {
+        double p = exp(s[j] - m);
+        l += p;
+        for (int d = 0; d < dv; ++d) out[d] += p * (v_scale * oracle_e4m3_to_double(vrows[j][d * v_dstride]));
+    }
+    for (int d = 0; d < dv; ++d) out[d] /= l;
+    *lse = m + log(l);
+}
+
 /* ------------------------------------------------------------------ decode */
 
 typedef struct {
     const uint16_t *q; const int64_t *qs;        /* [B, q_len, Hq, Dk] */
-    const uint16_t *k; const int64_t *ks;        /* [P, ps, Hkv, Dk]   */
-    const uint16_t *v; const int64_t *vs;        /* [P, ps, Hkv, Dv]   */
+    const void *k; const int64_t *ks;            /* [P, ps, Hkv, Dk]: BF16, or E4M3 when kv8 */
+    const void *v; const int64_t *vs;            /* [P, ps, Hkv, Dv]   */
+    int kv8; double k_scale, v_scale;
     const int32_t *bt; int64_t bt_stride;        /* [B, max_pages]     */
     const int32_t *seq_lens;                     /* [B]                */
     int B, q_len, Hq, Hkv, Dk, Dv, ps, num_pages, max_pages;
@@ -102,8 +152,9 @@ static void *decode_worker(void *arg) {
     int G = J->Hq / J->Hkv;
     int64_t cap = (int64_t)J->max_pages * J->ps;
     double *s = (double *)malloc(sizeof(double) * (size_t)(cap > 0 ? cap : 1));
-    const uint16_t **kr = (const uint16_t **)malloc(sizeof(void *) * (size_t)(cap > 0 ? cap : 1));
-    const uint16_t **vr = (const uint16_t **)malloc(sizeof(void *) * (size_t)(cap > 0 ? cap : 1));
+    const void **kr = (const void **)malloc(sizeof(void *) * (size_t)(cap > 0 ? cap : 1));
+    const void **vr = (const void **)malloc(sizeof(void *) * (size_t)(cap > 0 ? cap : 1));
+    const size_t esz = J->kv8 ? 1 : 2;                   /* bytes per K/V element */
     if (!s || !kr || !vr) { J->status = -3; goto done; }
     for (int64_t i = J->begin; i < J->end; ++i) {
         int64_t row = J->rows ? J->rows[i] : i;
@@ -121,27 +172,33 @@ static void *decode_worker(void *arg) {
             int32_t page = J->bt[(int64_t)b * J->bt_stride + j / J->ps];
             if (page < 0 || page >= J->num_pages) { J->status = -1; goto done; }
             int64_t slot = j % J->ps;
-            kr[j] = J->k + page * J->ks[0] + slot * J->ks[1] + (int64_t)g * J->ks[2];
-            vr[j] = J->v + page * J->vs[0] + slot * J->vs[1] + (int64_t)g * J->vs[2];
+            kr[j] = (const char *)J->k + esz * (size_t)(page * J->ks[0] + slot * J->ks[1] + (int64_t)g * J->ks[2]);
+            vr[j] = (const char *)J->v + esz * (size_t)(page * J->vs[0] + slot * J->vs[1] + (int64_t)g * J->vs[2]);
         }
         const uint16_t *qrow = J->q + b * J->qs[0] + t * J->qs[1] + h * J->qs[2];
-        attend_row(qrow, J->qs[3], kr, J->ks[3], vr, J->vs[3], visible, J->Dk, J->Dv,
-                   J->scale, s, J->out + i * J->Dv, J->lse + i);
+        if (J->kv8)
+            attend_row_kv8(qrow, J->qs[3], (const uint8_t *const *)kr, J->ks[3], J->k_scale,
+                           (const uint8_t *const *)vr, J->vs[3], J->v_scale, visible, J->Dk, J->Dv,
+                           J->scale, s, J->out + i * J->Dv, J->lse + i);
+        else
+            attend_row(qrow, J->qs[3], (const uint16_t *const *)kr, J->ks[3], (const uint16_t *const *)vr,
+                       J->vs[3], visible, J->Dk, J->Dv, J->scale, s, J->out + i * J->Dv, J->lse + i);
     }
 done:
     free(s); free(kr); free(vr);
     return NULL;
 }
 
-int oracle_paged_decode(const uint16_t *q, const int64_t *q_stride,
-                        const uint16_t *k_cache, const int64_t *k_stride,
-                        const uint16_t *v_cache, const int64_t *v_stride,
-                        const int32_t *block_table, int64_t bt_stride,
-                        const int32_t *seq_lens,
-                        int B, int q_len, int Hq, int Hkv, int Dk, int Dv,
-                        int page_size, int num_pages, int max_pages, double scale,
-                        const int64_t *rows, int64_t n_rows,
-                        double *out, double *lse, int n_threads) {
+static int paged_decode_any(const uint16_t *q, const int64_t *q_stride,
+                            const void *k_cache, const int64_t *k_stride,
+                            const void *v_cache, const int64_t *v_stride,
+                            int kv8, double k_scale, double v_scale,
+                            const int32_t *block_table, int64_t bt_stride,
+                            const int32_t *seq_lens,
+                            int B, int q_len, int Hq, int Hkv, int Dk, int Dv,
+                            int page_size, int num_pages, int max_pages, double scale,
+                            const int64_t *rows, int64_t n_rows,
+                            double *out, double *lse, int n_threads) {
     if (Hkv <= 0 || Hq % Hkv != 0 || page_size <= 0) return -4;
     if (n_threads < 1) n_threads = 1;
     if (n_rows < n_threads) n_threads = (int)(n_rows > 0 ? n_rows : 1);
@@ -151,6 +208,7 @@ int oracle_paged_decode(const uint16_t *q, const int64_t *q_stride,
     for (int w = 0; w < n_threads; ++w) {
         decode_job *J = &jobs[w];
         J->q = q; J->qs = q_stride; J->k = k_cache; J->ks = k_stride; J->v = v_cache; J->vs = v_stride;
+        J->kv8 = kv8; J->k_scale = k_scale; J->v_scale = v_scale;
         J->bt = block_table; J->bt_stride = bt_stride; J->seq_lens = seq_lens;
         J->B = B; J->q_len = q_len; J->Hq = Hq; J->Hkv = Hkv; J->Dk = Dk; J->Dv = Dv;
         J->ps = page_size; J->num_pages = num_pages; J->max_pages = max_pages; J->scale = scale;
@@ -165,6 +223,35 @@ int oracle_paged_decode(const uint16_t *q, const int64_t *q_stride,
     }
     free(jobs); free(tid);
     return status;
+}
+
+int oracle_paged_decode(const uint16_t *q, const int64_t *q_stride,
+                        const uint16_t *k_cache, const int64_t *k_stride,
+                        const uint16_t *v_cache, const int64_t *v_stride,
+                        const int32_t *block_table, int64_t bt_stride,
+                        const int32_t *seq_lens,
+                        int B, int q_len, int Hq, int Hkv, int Dk, int Dv,
+                        int page_size, int num_pages, int max_pages, double scale,
+                        const int64_t *rows, int64_t n_rows,
+                        double *out, double *lse, int n_threads) {
+    return paged_decode_any(q, q_stride, k_cache, k_stride, v_cache, v_stride, 0, 1.0, 1.0, block_table,
+                            bt_stride, seq_lens, B, q_len, Hq, Hkv, Dk, Dv, page_size, num_pages, max_pages,
+                            scale, rows, n_rows, out, lse, n_threads);
+}
+
+int oracle_paged_decode_kv8(const uint16_t *q, const int64_t *q_stride,
+                            const uint8_t *k_cache, const int64_t *k_stride,
+                            const uint8_t *v_cache, const int64_t *v_stride,
+                            double k_scale, double v_scale,
+                            const int32_t *block_table, int64_t bt_stride,
+                            const int32_t *seq_lens,
+                            int B, int q_len, int Hq, int Hkv, int Dk, int Dv,
+                            int page_size, int num_pages, int max_pages, double scale,
+                            const int64_t *rows, int64_t n_rows,
+                            double *out, double *lse, int n_threads) {
+    return paged_decode_any(q, q_stride, k_cache, k_stride, v_cache, v_stride, 1, k_scale, v_scale, block_table,
+                            bt_stride, seq_lens, B, q_len, Hq, Hkv, Dk, Dv, page_size, num_pages, max_pages,
+                            scale, rows, n_rows, out, lse, n_threads);
 }
 
 /* ----------------------------------------------------------------- prefill */

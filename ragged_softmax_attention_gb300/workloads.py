@@ -43,6 +43,7 @@ class DecodeWorkload:
     seq_lens: Optional[tuple] = None          # fixed lengths (one per batch row)
     seq_len_range: Optional[tuple] = None     # inclusive uniform integer range
     latent: bool = False                      # V = first head_dim_v columns of each K row
+    kv_fp8: bool = False                      # K/V caches in FP8 E4M3 with one scale each
     value_seed: int = 1234
     spare_pages: int = 3                      # NaN-filled pool pages no sequence uses
 
@@ -85,6 +86,10 @@ WORKLOADS = {
         "varlen_gqa_prefill", num_seqs=16, num_q_heads=32, num_kv_heads=8,
         head_dim_qk=128, head_dim_v=128, causal=True, scale=1.0 / math.sqrt(128),
         seq_len_range=(256, 8192), value_seed=1236),
+    "qwen3_14b_paged_decode_fp8": DecodeWorkload(
+        "qwen3_14b_paged_decode_fp8", batch=64, q_len=1, num_q_heads=40, num_kv_heads=8,
+        head_dim_qk=128, head_dim_v=128, page_size=128, scale=1.0 / math.sqrt(128.0),
+        seq_len_range=(512, 32768), kv_fp8=True, value_seed=1235),
     "dense_causal_mha_hd256": PrefillWorkload(
         "dense_causal_mha_hd256", num_seqs=1, num_q_heads=16, num_kv_heads=16,
         head_dim_qk=256, head_dim_v=256, causal=True, scale=1.0 / 16.0,
@@ -172,6 +177,14 @@ def make_decode_inputs(wl: DecodeWorkload, device="cpu", seq_lens=None, mapping=
         v_cache = k_cache[..., : wl.head_dim_v]
     else:
         v_cache = _randn((num_pages, wl.page_size, wl.num_kv_heads, wl.head_dim_v), gen, device)
+    k_scale = v_scale = 1.0
+    if wl.kv_fp8:
+        # One scale per cache: the largest magnitude maps to E4M3's largest
+        # finite value (448), so no value saturates.
+        k_scale = float(k_cache.float().abs().amax()) / 448.0
+        v_scale = float(v_cache.float().abs().amax()) / 448.0
+        k_cache = (k_cache.float() / k_scale).to(torch.float8_e4m3fn)
+        v_cache = (v_cache.float() / v_scale).to(torch.float8_e4m3fn)
     if poison:
         covered = torch.zeros((num_pages, wl.page_size), dtype=torch.bool)
         for b, n in enumerate(lens):
@@ -179,10 +192,15 @@ def make_decode_inputs(wl: DecodeWorkload, device="cpu", seq_lens=None, mapping=
                 cnt = min(wl.page_size, int(n) - j)
                 covered[int(bt[b, j // wl.page_size]), :cnt] = True
         mask = (~covered).to(device)
-        nan = float("nan")
-        k_cache[mask] = nan
-        if not wl.latent:
-            v_cache[mask] = nan
+        if wl.kv_fp8:                         # E4M3 NaN: S.1111.111
+            k_cache.view(torch.uint8)[mask] = 0x7F
+            if not wl.latent:
+                v_cache.view(torch.uint8)[mask] = 0x7F
+        else:
+            nan = float("nan")
+            k_cache[mask] = nan
+            if not wl.latent:
+                v_cache[mask] = nan
     return {
         "q": q,
         "k_cache": k_cache,
@@ -190,6 +208,8 @@ def make_decode_inputs(wl: DecodeWorkload, device="cpu", seq_lens=None, mapping=
         "block_table": bt.to(device),
         "seq_lens": torch.tensor(lens, dtype=torch.int32, device=device),
         "scale": float(wl.scale),
+        "k_scale": k_scale,
+        "v_scale": v_scale,
         "num_pages": num_pages,
     }
 

@@ -489,3 +489,73 @@ def test_flywheel_static_anchor_budget():
     # The refusal threshold is crossed only at N = exp(88.7 - ln Vmax - delta - 20) keys.
     n_star = math.exp(g["fp32_log_max"] - math.log(g["v_max"]) - g["delta"] - g["refuse_below"])
     assert planning.static_anchor_tau(n_star * 1.01) < g["refuse_below"] < planning.static_anchor_tau(n_star * 0.99)
+
+
+# ------------------------------------------------------------ FP8 KV cache
+
+def tiny_decode_fp8(batch=3, q_len=1, hq=8, hkv=2, d=32, ps=4, lens=(5, 1, 13), seed=13):
+    wl = DecodeWorkload("t8", batch=batch, q_len=q_len, num_q_heads=hq, num_kv_heads=hkv,
+                        head_dim_qk=d, head_dim_v=d, page_size=ps, scale=1.0 / math.sqrt(d),
+                        seq_lens=tuple(lens), value_seed=seed, spare_pages=2, kv_fp8=True)
+    return wl, make_decode_inputs(wl, "cpu")
+
+
+def test_e4m3_decoding_matches_torch_for_every_byte():
+    """The oracle's E4M3 decoder (written from the format definition) against
+    torch's float8_e4m3fn conversion, all 256 codes, NaN codes included."""
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).tolist()
+    for b in range(256):
+        v = oracle.e4m3_to_double(b)
+        assert (math.isnan(v) and math.isnan(ref[b])) or v == ref[b], b
+    # closed forms: 1.0, the largest finite value, the smallest subnormal, NaN
+    assert oracle.e4m3_to_double(0x38) == 1.0 and oracle.e4m3_to_double(0x7E) == 448.0
+    assert oracle.e4m3_to_double(0x01) == 2.0 ** -9 and oracle.e4m3_to_double(0xB8) == -1.0
+    assert math.isnan(oracle.e4m3_to_double(0x7F)) and math.isnan(oracle.e4m3_to_double(0xFF))
+
+
+def _dequantized_dense(inp, b, name, scale):
+    """Row b's keys or values as float64: bytes gathered through the block
+    table (plain indexing on the uint8 view), decoded by torch, times the scale."""
+    n = int(inp["seq_lens"][b])
+    ps = inp[name].shape[1]
+    pages = [int(inp["block_table"][b, j // ps]) for j in range(n)]
+    slots = [j % ps for j in range(n)]
+    raw = inp[name].view(torch.uint8)[pages, slots]
+    return raw.view(torch.float8_e4m3fn).to(torch.float64) * scale
+
+
+@pytest.mark.parametrize("q_len,lens", [(1, (5, 1, 13)), (3, (7, 9, 12))])
+def test_fp8_kv_decode_matches_sdpa_on_dequantized_copy(q_len, lens):
+    wl, inp = tiny_decode_fp8(q_len=q_len, lens=lens)
+    out, lse = oracle.paged_decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"],
+                                   inp["seq_lens"], inp["scale"], k_scale=inp["k_scale"], v_scale=inp["v_scale"])
+    hq, hkv = wl.num_q_heads, wl.num_kv_heads
+    for b in range(wl.batch):
+        k = _dequantized_dense(inp, b, "k_cache", inp["k_scale"]).repeat_interleave(hq // hkv, dim=1)
+        v = _dequantized_dense(inp, b, "v_cache", inp["v_scale"]).repeat_interleave(hq // hkv, dim=1)
+        q = inp["q"][b].double()
+        n = k.shape[0]
+        mask = torch.zeros(q_len, n, dtype=torch.bool)
+        for t in range(q_len):
+            mask[t, : max(0, n - q_len + t + 1)] = True
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            q.transpose(0, 1), k.transpose(0, 1), v.transpose(0, 1), attn_mask=mask, scale=inp["scale"])
+        sc = (torch.einsum("thd,nhd->htn", q, k) * inp["scale"]).masked_fill(~mask, float("-inf"))
+        rows = slice(b * q_len * hq, (b + 1) * q_len * hq)
+        np.testing.assert_allclose(out[rows], ref.transpose(0, 1).reshape(q_len * hq, -1).numpy(), atol=1e-12)
+        np.testing.assert_allclose(lse[rows], torch.logsumexp(sc, -1).transpose(0, 1).reshape(-1).numpy(),
+                                   atol=1e-12)
+
+
+def test_fp8_scales_fold_into_score_scale_and_output():
+    """k_scale multiplies every score like the softmax scale does; v_scale
+    multiplies the output and leaves the LSE alone."""
+    wl, inp = tiny_decode_fp8()
+    args = (inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"], inp["seq_lens"])
+    o1, l1 = oracle.paged_decode(*args, 0.3, k_scale=2.0, v_scale=1.0)
+    o2, l2 = oracle.paged_decode(*args, 0.6, k_scale=1.0, v_scale=1.0)
+    np.testing.assert_allclose(o1, o2, atol=1e-12)
+    np.testing.assert_allclose(l1, l2, atol=1e-12)
+    o3, l3 = oracle.paged_decode(*args, 0.3, k_scale=2.0, v_scale=3.0)
+    np.testing.assert_allclose(o3, 3.0 * o1, atol=1e-12)
+    np.testing.assert_allclose(l3, l1, atol=1e-12)
