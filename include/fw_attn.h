@@ -59,7 +59,7 @@ typedef enum {
     FW_ERR_DEVICE_TIMEOUT = 5   /* a kernel gave up waiting (reported by fw_get_device_status) */
 } fw_status_t;
 
-typedef enum { FW_BF16 = 0, FW_F32 = 1, FW_I32 = 2 } fw_dtype_t;
+typedef enum { FW_BF16 = 0, FW_F32 = 1, FW_I32 = 2, FW_FP8_E4M3 = 3 } fw_dtype_t;
 
 typedef struct {
     void *data;          /* device pointer (may be NULL only when every extent is 0) */
@@ -138,6 +138,30 @@ fw_status_t fw_paged_decode_noalloc(const fw_tensor_t *q, const fw_tensor_t *k_c
                                     const fw_tensor_t *v_cache, const fw_tensor_t *block_table,
                                     const fw_tensor_t *seq_lens, float scale,
                                     fw_tensor_t *out, fw_tensor_t *lse, fw_stream_t stream);
+
+/*
+ * fw_paged_decode over an FP8 KV cache ("TokenSpeed-MLA 2.0.1", decode: FP8
+ * inputs, BF16 output).
+ *
+ *   k_cache, v_cache  [num_pages, page_size, Hkv, 128]  FP8_E4M3 (OCP E4M3
+ *                     bytes); key j's values are k_scale * e4m3(byte) and
+ *                     v_scale * e4m3(byte), one scale per cache
+ *   q, block_table, seq_lens, scale, out, lse, stream: as fw_paged_decode
+ *                     (q BF16, out BF16, lse F32 natural log)
+ *
+ * Supported: Dk = Dv = 128, the query-head groupings, q_len 1-4 and page
+ * sizes of fw_paged_decode; cache strides multiples of 16 bytes.  The
+ * arithmetic is exact in the FP8 values: keys and values are widened to FP16
+ * on chip (every E4M3 value is an FP16 value), queries are converted from
+ * BF16 to FP16 (|q| must stay below 65504), scores and sums are FP32.  The
+ * same workspace as fw_paged_decode (fw_paged_decode_workspace_size with the
+ * same shapes); errors as fw_paged_decode, plus FW_ERR_INVALID_ARG for a
+ * non-finite or non-positive k_scale / v_scale.
+ */
+fw_status_t fw_paged_decode_fp8(const fw_tensor_t *q, const fw_tensor_t *k_cache,
+                                const fw_tensor_t *v_cache, const fw_tensor_t *block_table,
+                                const fw_tensor_t *seq_lens, float scale, float k_scale, float v_scale,
+                                fw_tensor_t *out, fw_tensor_t *lse, fw_stream_t stream);
 
 /*
  * Workspace bytes fw_paged_decode needs for these shapes (data pointers are

@@ -19,10 +19,11 @@ LIB_PATH = os.path.join(_HERE, "libfw_attn.so")
 FW_OK, FW_ERR_INVALID_ARG, FW_ERR_UNSUPPORTED, FW_ERR_WORKSPACE, FW_ERR_CUDA, FW_ERR_DEVICE_TIMEOUT = range(6)
 STATUS_NAMES = {0: "FW_OK", 1: "FW_ERR_INVALID_ARG", 2: "FW_ERR_UNSUPPORTED", 3: "FW_ERR_WORKSPACE",
                 4: "FW_ERR_CUDA", 5: "FW_ERR_DEVICE_TIMEOUT"}
-FW_BF16, FW_F32, FW_I32 = 0, 1, 2
+FW_BF16, FW_F32, FW_I32, FW_FP8_E4M3 = 0, 1, 2, 3
 FW_OPT_DECODE_CHUNK_TOKENS, FW_OPT_WAIT_TIMEOUT_MS, FW_OPT_KERNEL_TIMING, FW_OPT_MAX_CTAS = 0, 1, 2, 3
 
-_DTYPES = {torch.bfloat16: FW_BF16, torch.float32: FW_F32, torch.int32: FW_I32}
+_DTYPES = {torch.bfloat16: FW_BF16, torch.float32: FW_F32, torch.int32: FW_I32,
+           torch.float8_e4m3fn: FW_FP8_E4M3}
 
 
 class FwError(RuntimeError):
@@ -64,6 +65,9 @@ def load_library(path: Optional[str] = None):
     lib.fw_paged_decode.argtypes = [P, P, P, P, P, ctypes.c_float, P, P, ctypes.c_void_p]
     lib.fw_paged_decode_noalloc.restype = S
     lib.fw_paged_decode_noalloc.argtypes = [P, P, P, P, P, ctypes.c_float, P, P, ctypes.c_void_p]
+    lib.fw_paged_decode_fp8.restype = ctypes.c_int
+    lib.fw_paged_decode_fp8.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_float, ctypes.c_float, P, P,
+                                        ctypes.c_void_p]
     lib.fw_paged_decode_workspace_size.restype = S
     lib.fw_paged_decode_workspace_size.argtypes = [P, P, P, P, ctypes.POINTER(ctypes.c_size_t)]
     lib.fw_varlen_prefill.restype = S
@@ -134,6 +138,24 @@ def paged_decode(q, k_cache, v_cache, block_table, seq_lens, scale, out=None, ls
     fo, fl = as_fw_tensor(out), as_fw_tensor(lse)
     _check(lib.fw_paged_decode(*[_ref(a) for a in args], ctypes.c_float(scale), _ref(fo), _ref(fl),
                                _stream_handle(stream)))
+    return out, lse
+
+
+def paged_decode_fp8(q, k_cache, v_cache, block_table, seq_lens, scale, k_scale, v_scale, out=None, lse=None,
+                     return_lse=True, stream=None):
+    """fw_paged_decode_fp8: FP8 E4M3 caches (torch.float8_e4m3fn) with one scale
+    each; returns (out [B, q_len, Hq, Dv] bf16, lse [B, q_len, Hq] f32 or None)."""
+    lib = load_library()
+    B, q_len, Hq, _ = q.shape
+    Dv = v_cache.shape[3]
+    if out is None:
+        out = torch.empty((B, q_len, Hq, Dv), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, q_len, Hq), dtype=torch.float32, device=q.device)
+    args = [as_fw_tensor(x) for x in (q, k_cache, v_cache, block_table, seq_lens)]
+    fo, fl = as_fw_tensor(out), as_fw_tensor(lse)
+    _check(lib.fw_paged_decode_fp8(*[_ref(a) for a in args], ctypes.c_float(scale), ctypes.c_float(k_scale),
+                                   ctypes.c_float(v_scale), _ref(fo), _ref(fl), _stream_handle(stream)))
     return out, lse
 
 

@@ -109,13 +109,13 @@ fw_status_t get_encoder() {
     return FW_OK;
 }
 
-// BF16 tensor map with 128-byte swizzle; dims/strides innermost first,
-// strides in bytes for dims 1..rank-1.
-fw_status_t encode_bf16(CUtensorMap *tm, const void *base, int rank, const uint64_t *dims,
-                        const uint64_t *strides_bytes, const uint32_t *box, const char *what) {
+// Tensor map with 128-byte swizzle; dims/strides innermost first, strides
+// in bytes for dims 1..rank-1.
+fw_status_t encode_map(CUtensorMap *tm, CUtensorMapDataType type, const void *base, int rank, const uint64_t *dims,
+                       const uint64_t *strides_bytes, const uint32_t *box, const char *what) {
     if (fw_status_t s = get_encoder()) return s;
     uint32_t elem[5] = {1, 1, 1, 1, 1};
-    CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base),
+    CUresult r = g_encode(tm, type, (cuuint32_t)rank, const_cast<void *>(base),
                           dims, strides_bytes, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -123,10 +123,18 @@ fw_status_t encode_bf16(CUtensorMap *tm, const void *base, int rank, const uint6
     return FW_OK;
 }
 
+fw_status_t encode_bf16(CUtensorMap *tm, const void *base, int rank, const uint64_t *dims,
+                        const uint64_t *strides_bytes, const uint32_t *box, const char *what) {
+    return encode_map(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rank, dims, strides_bytes, box, what);
+}
+
 // ----------------------------------------------------------------- validation
 
 const char *dtype_name(int32_t d) {
-    switch (d) { case FW_BF16: return "bf16"; case FW_F32: return "f32"; case FW_I32: return "i32"; default: return "?"; }
+    switch (d) {
+        case FW_BF16: return "bf16"; case FW_F32: return "f32"; case FW_I32: return "i32";
+        case FW_FP8_E4M3: return "fp8_e4m3"; default: return "?";
+    }
 }
 
 fw_status_t check_tensor(const fw_tensor_t *t, const char *name, int ndim, int32_t dtype, bool allow_null = false) {
@@ -147,14 +155,15 @@ fw_status_t check_tensor(const fw_tensor_t *t, const char *name, int ndim, int32
 }
 
 // Tensors read through the tensor memory accelerator: 16-byte aligned base,
-// every outer stride a multiple of 8 BF16 elements (16 bytes).
+// every outer stride a multiple of 16 bytes (8 BF16 or 16 FP8 elements).
 fw_status_t check_tma_layout(const fw_tensor_t *t, const char *name) {
     if (reinterpret_cast<uintptr_t>(t->data) % 16 != 0)
         return fail(FW_ERR_INVALID_ARG, "%s: base pointer must be 16-byte aligned", name);
+    const int64_t per16 = t->dtype == FW_FP8_E4M3 ? 16 : 8;
     for (int i = 0; i + 1 < t->ndim; ++i)
-        if (t->stride[i] % 8 != 0)
-            return fail(FW_ERR_INVALID_ARG, "%s: stride[%d] = %lld is not a multiple of 8 elements", name, i,
-                        (long long)t->stride[i]);
+        if (t->stride[i] % per16 != 0)
+            return fail(FW_ERR_INVALID_ARG, "%s: stride[%d] = %lld is not a multiple of %lld elements", name, i,
+                        (long long)t->stride[i], (long long)per16);
     return FW_OK;
 }
 
@@ -356,8 +365,10 @@ fw_status_t fw_get_device_status(fw_stream_t stream, int32_t *code) {
 static fw_status_t decode_shapes(const fw_tensor_t *q, const fw_tensor_t *k_cache, const fw_tensor_t *v_cache,
                                  const fw_tensor_t *block_table) {
     if (fw_status_t s = check_tensor(q, "q", 4, FW_BF16)) return s;
-    if (fw_status_t s = check_tensor(k_cache, "k_cache", 4, FW_BF16)) return s;
-    if (fw_status_t s = check_tensor(v_cache, "v_cache", 4, FW_BF16)) return s;
+    // BF16 caches, or FP8 caches (fw_paged_decode_fp8): both of one type
+    const int32_t kv_type = k_cache && k_cache->dtype == FW_FP8_E4M3 ? FW_FP8_E4M3 : FW_BF16;
+    if (fw_status_t s = check_tensor(k_cache, "k_cache", 4, kv_type)) return s;
+    if (fw_status_t s = check_tensor(v_cache, "v_cache", 4, kv_type)) return s;
     if (fw_status_t s = check_tensor(block_table, "block_table", 2, FW_I32)) return s;
     const int64_t B = q->shape[0], Hq = q->shape[2], Dk = q->shape[3];
     const int64_t P = k_cache->shape[0], ps = k_cache->shape[1], Hkv = k_cache->shape[2];
@@ -398,9 +409,15 @@ fw_status_t fw_paged_decode_workspace_size(const fw_tensor_t *q, const fw_tensor
 static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_cache, const fw_tensor_t *v_cache,
                                      const fw_tensor_t *block_table, const fw_tensor_t *seq_lens, float scale,
                                      fw_tensor_t *out, fw_tensor_t *lse, fw_stream_t stream_,
-                                     void *(*fixed_ws)(DeviceState *, fw_status_t *), size_t fixed_bytes) {
+                                     void *(*fixed_ws)(DeviceState *, fw_status_t *), size_t fixed_bytes,
+                                     bool kv8 = false, float k_scale = 1.f, float v_scale = 1.f) {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     if (fw_status_t s = decode_shapes(q, k_cache, v_cache, block_table)) return s;
+    if (kv8 != (k_cache->dtype == FW_FP8_E4M3))
+        return fail(FW_ERR_INVALID_ARG, kv8 ? "fw_paged_decode_fp8 takes FP8_E4M3 caches"
+                                            : "FP8 caches go through fw_paged_decode_fp8");
+    if (kv8 && !(std::isfinite(k_scale) && std::isfinite(v_scale) && k_scale > 0.f && v_scale > 0.f))
+        return fail(FW_ERR_INVALID_ARG, "k_scale and v_scale must be finite and positive");
     if (fw_status_t s = check_tensor(seq_lens, "seq_lens", 1, FW_I32)) return s;
     if (fw_status_t s = check_tensor(out, "out", 4, FW_BF16)) return s;
     if (fw_status_t s = check_tensor(lse, "lse", 3, FW_F32, true)) return s;
@@ -415,7 +432,10 @@ static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_
     if (lse && (lse->shape[0] != B || lse->shape[1] != q_len || lse->shape[2] != Hq))
         return fail(FW_ERR_INVALID_ARG, "lse must be [B, q_len, Hq]");
     if (!std::isfinite(scale)) return fail(FW_ERR_INVALID_ARG, "scale must be finite");
-    const bool latent = (Dk == 576 && Dv == 512);
+    const bool latent = !kv8 && (Dk == 576 && Dv == 512);
+    if (kv8 && !(Dk == 128 && Dv == 128))
+        return fail(FW_ERR_UNSUPPORTED, "FP8 decode head dims (Dk=%lld, Dv=%lld): supported Dk = Dv = 128",
+                    (long long)Dk, (long long)Dv);
     if (!latent && !(Dk == Dv && (Dk == 128 || Dk == 256)))
         return fail(FW_ERR_UNSUPPORTED, "decode head dims (Dk=%lld, Dv=%lld): supported Dk = Dv in {128, 256} "
                     "and the latent (576, 512)", (long long)Dk, (long long)Dv);
@@ -484,7 +504,8 @@ static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_
     p.plan = reinterpret_cast<int32_t *>(wsb);
     p.ws_o = reinterpret_cast<float *>(wsb + plan_bytes);
     p.ws_lse = reinterpret_cast<float *>(wsb + plan_bytes + o_bytes);
-    p.scale_log2 = scale * 1.4426950408889634f;
+    p.scale_log2 = scale * (kv8 ? k_scale : 1.f) * 1.4426950408889634f;
+    p.out_scale = kv8 ? v_scale : 1.f;
     p.timeout_ns = (uint64_t)g_opt_timeout_ms * 1000000ull;
     p.status = d->status;
 
@@ -498,21 +519,26 @@ static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_
         if (fw_status_t s = encode_bf16(&tq, q->data, 4, dims, strides, box, "q")) return s;
     }
     {
+        // BF16: boxes of 64 columns (128 bytes); FP8: one box spans the whole
+        // 128-byte row of 128 E4M3 values.
         const uint32_t rows_box = (uint32_t)(ps < fw::kKvTile ? ps : fw::kKvTile);
+        const uint64_t esz = kv8 ? 1 : 2;
+        const CUtensorMapDataType type = kv8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
         const uint64_t dk[4] = {(uint64_t)Dk, (uint64_t)Hkv, (uint64_t)ps, (uint64_t)P};
-        const uint64_t sk[3] = {(uint64_t)k_cache->stride[2] * 2, (uint64_t)k_cache->stride[1] * 2,
-                                (uint64_t)k_cache->stride[0] * 2};
-        const uint32_t box[4] = {64, 1, rows_box, 1};
-        if (fw_status_t s = encode_bf16(&tk, k_cache->data, 4, dk, sk, box, "k_cache")) return s;
+        const uint64_t sk[3] = {(uint64_t)k_cache->stride[2] * esz, (uint64_t)k_cache->stride[1] * esz,
+                                (uint64_t)k_cache->stride[0] * esz};
+        const uint32_t box[4] = {kv8 ? 128u : 64u, 1, rows_box, 1};
+        if (fw_status_t s = encode_map(&tk, type, k_cache->data, 4, dk, sk, box, "k_cache")) return s;
         const uint64_t dv[4] = {(uint64_t)Dv, (uint64_t)Hkv, (uint64_t)ps, (uint64_t)P};
-        const uint64_t sv[3] = {(uint64_t)v_cache->stride[2] * 2, (uint64_t)v_cache->stride[1] * 2,
-                                (uint64_t)v_cache->stride[0] * 2};
-        if (fw_status_t s = encode_bf16(&tv, v_cache->data, 4, dv, sv, box, "v_cache")) return s;
+        const uint64_t sv[3] = {(uint64_t)v_cache->stride[2] * esz, (uint64_t)v_cache->stride[1] * esz,
+                                (uint64_t)v_cache->stride[0] * esz};
+        if (fw_status_t s = encode_map(&tv, type, v_cache->data, 4, dv, sv, box, "v_cache")) return s;
     }
     cudaEvent_t ev0 = nullptr, ev1 = nullptr;
     if (g_opt_timing) { ev0 = pooled_event(); ev1 = pooled_event(); }
     int launched = 0;
-    cudaError_t e = latent ? fw::launch_latent_decode(p, tq, tk, tv, stream, ev0, ev1, &launched)
+    cudaError_t e = kv8 ? fw::launch_decode_fp8(p, tq, tk, tv, stream, ev0, ev1, &launched)
+                  : latent ? fw::launch_latent_decode(p, tq, tk, tv, stream, ev0, ev1, &launched)
                            : fw::launch_decode(p, tq, tk, tv, (int)Dk, stream, ev0, ev1, &launched);
     g_launches.fetch_add(launched);
     if (e != cudaSuccess) return fail(FW_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
@@ -524,6 +550,14 @@ fw_status_t fw_paged_decode(const fw_tensor_t *q, const fw_tensor_t *k_cache, co
                             const fw_tensor_t *block_table, const fw_tensor_t *seq_lens, float scale,
                             fw_tensor_t *out, fw_tensor_t *lse, fw_stream_t stream) {
     return paged_decode_impl(q, k_cache, v_cache, block_table, seq_lens, scale, out, lse, stream, nullptr, 0);
+}
+
+fw_status_t fw_paged_decode_fp8(const fw_tensor_t *q, const fw_tensor_t *k_cache, const fw_tensor_t *v_cache,
+                                const fw_tensor_t *block_table, const fw_tensor_t *seq_lens, float scale,
+                                float k_scale, float v_scale, fw_tensor_t *out, fw_tensor_t *lse,
+                                fw_stream_t stream) {
+    return paged_decode_impl(q, k_cache, v_cache, block_table, seq_lens, scale, out, lse, stream, nullptr, 0,
+                             true, k_scale, v_scale);
 }
 
 // ----------------------------------------------------- decode without allocation

@@ -32,12 +32,15 @@
 // section 8.3 with the double-buffered S and P slots playing its ring.
 #include <cuda_bf16.h>
 
+#include "decode_common.cuh"
 #include "fw_internal.h"
 #include "fw_ptx.cuh"
 
 namespace fw {
 
 namespace {
+
+using namespace dec;
 
 constexpr float kNegInf = -__builtin_huge_valf();
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
@@ -69,108 +72,6 @@ struct DecodeCfg {
     static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, NQ, false, false);
     static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, NQ, true, false);
 };
-
-struct Unit {                 // one piece: a unit's tiles inside one CTA range
-    int b, g, rg, n, k_begin, k_end, ntiles;
-    int k, npieces;
-    bool single;
-};
-
-__device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
-
-__device__ __forceinline__ int clamp_len(const DecodeParams &p, int n) {
-    const int cap = p.max_pages * p.ps;
-    return n < 0 ? 0 : (n > cap ? cap : n);
-}
-
-// Walks the pieces of this CTA's tile ranges; every role runs its own copy
-// and sees the same sequence.
-struct PieceIter {
-    int T, span, range, pos, end, b;
-
-    __device__ void init(const DecodeParams &p) {
-        T = __ldg(p.plan + 0);
-        span = max(1, __ldg(p.plan + 1));
-        range = blockIdx.x;
-        pos = 0;
-        end = 0;
-        b = -1;
-        open_range();
-    }
-    __device__ void open_range() {
-        const long long lo = (long long)range * span;
-        pos = lo < T ? (int)lo : T;
-        end = (int)min((long long)T, lo + span);
-        b = -1;
-    }
-    __device__ bool next(const DecodeParams &p, Unit &x) {
-        const int32_t *PB = p.plan + 2;
-        while (pos >= end) {
-            range += gridDim.x;
-            if ((long long)range * span >= T) return false;
-            open_range();
-        }
-        if (b < 0 || pos >= __ldg(PB + b + 1)) {
-            int lo = 0, hi = p.B - 1;              // largest b with PB[b] <= pos
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (__ldg(PB + mid) <= pos) lo = mid; else hi = mid - 1;
-            }
-            b = lo;
-        }
-        const int pb0 = __ldg(PB + b);
-        const int tb = (__ldg(PB + b + 1) - pb0) / p.units_per_row;
-        const int off = pos - pb0;
-        const int u = off / tb;
-        const int tl = off - u * tb;
-        const int th = min(tb, tl + (end - pos));
-        const int pstart = pb0 + u * tb;
-        x.b = b;
-        x.g = u / p.row_groups;
-        x.rg = u - x.g * p.row_groups;
-        x.n = clamp_len(p, __ldg(p.seq_lens + b));
-        x.k_begin = tl * kKvTile;
-        x.k_end = min(x.n, th * kKvTile);
-        x.ntiles = th - tl;
-        x.k = (pstart + tl) / span - pstart / span;
-        x.npieces = (pstart + tb - 1) / span - pstart / span + 1;
-        x.single = (x.npieces == 1);
-        pos += th - tl;
-        return true;
-    }
-};
-
-// Query row r of unit x -> (token t, head h); false if the row is padding.
-__device__ __forceinline__ bool unit_row(const DecodeParams &p, const Unit &x, int r, int &t, int &h) {
-    if (p.head_mode == 0) {
-        const int tt = r / p.G;
-        t = x.rg * p.tokens_per_unit + tt;
-        h = x.g * p.G + (r - tt * p.G);
-        return tt < p.tokens_per_unit && t < p.q_len;
-    }
-    t = x.rg / p.head_chunks;
-    const int hh = (x.rg % p.head_chunks) * p.rows + r;
-    h = x.g * p.G + hh;
-    return hh < p.G;
-}
-
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
-// One lane waits, the whole warp learns the outcome (keeps the warp converged).
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const WaitCtx &w, int lane) {
-    int ok = 1;
-    if (lane == 0) ok = mbar_wait(bar, parity, w) ? 1 : 0;
-    return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
 
 template <int D, int NQ>
 __global__ void __launch_bounds__(192, 1)

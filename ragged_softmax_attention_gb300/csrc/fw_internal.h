@@ -44,7 +44,8 @@ struct DecodeParams {
     float *lse; int64_t lse_stride[3];         // [B, q_len, Hq] or nullptr
     float *ws_o;                               // [B*q_len*Hq, max_pieces, Dv]
     float *ws_lse;                             // [B*q_len*Hq, max_pieces] (log2 units)
-    float scale_log2;                          // scale * log2(e)
+    float scale_log2;                          // scale * log2(e) (times k_scale for an FP8 cache)
+    float out_scale;                           // v_scale for an FP8 cache, else 1
     uint64_t timeout_ns;
     int *status;                               // device status word
 };
@@ -82,6 +83,11 @@ cudaError_t launch_latent_decode(const DecodeParams &p, const CUtensorMap &tm_q,
                                  const CUtensorMap &tm_v, cudaStream_t stream, cudaEvent_t timing_start,
                                  cudaEvent_t timing_stop, int *launches);
 size_t latent_decode_smem_bytes();
+
+// Decode over an FP8 E4M3 KV cache (Dk = Dv = 128): plan + attention + combine
+cudaError_t launch_decode_fp8(const DecodeParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                              const CUtensorMap &tm_v, cudaStream_t stream, cudaEvent_t timing_start,
+                              cudaEvent_t timing_stop, int *launches);
 
 // plan kernel + attention kernel, in stream order
 cudaError_t launch_prefill(const PrefillParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
