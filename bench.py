@@ -38,6 +38,7 @@ DECODE_WL = "qwen3_14b_paged_decode"
 PREFILL_WL = "varlen_gqa_prefill"
 PREFILL_HD256_WL = "dense_causal_mha_hd256"
 LATENT_WL = "latent_paged_decode"
+DECODE_FP8_WL = "qwen3_14b_paged_decode_fp8"
 
 
 def load_peaks():
@@ -221,7 +222,8 @@ def bench_decode(fw, torch, steps, warmup, device, peaks, batch=None, do_e2e=Tru
         raise RuntimeError(f"device status {status} during the decode benchmark")
     per_launch_ms = kernel_ms / max(1, kernel_n)
     achieved = alg_bytes / (per_launch_ms * 1e-3) / 1e9
-    traffic = ncu_traffic("paged_decode_qwen3_14b_ncu.json", ["decode_kernel.cu", "fw_ptx.cuh"], tokens)
+    traffic = ncu_traffic("paged_decode_qwen3_14b_ncu.json", ["decode_kernel.cu", "decode_common.cuh", "fw_ptx.cuh"],
+                          tokens)
     roof = {"kernel": "paged_decode_kernel<128,16>", "bound": "hbm", "achieved": round(achieved, 1),
             "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
             "traffic": traffic, "peak_source": peaks["source"],
@@ -342,6 +344,62 @@ def bench_prefill(fw, torch, steps, warmup, device, peaks, name=None):
                          "frac": round(ach / peaks["bf16_tflops"], 4),
                          "frac_of_sustained": round(ach / peaks["bf16_tflops_sustained"], 4),
                          "traffic": traffic, "peak_source": peaks["source"], "kernel_ms_per_launch": round(per, 4)}}
+
+
+# ------------------------------------------------------ FP8 KV decode
+
+def bench_decode_fp8(fw, torch, steps, warmup, device, peaks, batch=None):
+    import dataclasses
+    from ragged_softmax_attention_gb300.workloads import WORKLOADS, make_decode_inputs, workload_seq_lens
+    wl = WORKLOADS[DECODE_FP8_WL]
+    if batch:   # a prefix of the same batch (profiling captures on a smaller case)
+        lens = workload_seq_lens(wl)[:batch]
+        wl = dataclasses.replace(wl, batch=batch, seq_len_range=None, seq_lens=tuple(lens))
+    d = make_decode_inputs(wl, device)
+    lens = d["seq_lens"].long().cpu()
+    tokens = int(lens.sum())
+    kv = tokens * wl.num_kv_heads * (wl.head_dim_qk + wl.head_dim_v)          # one byte per value
+    rows = wl.batch * wl.q_len * wl.num_q_heads
+    pages = int(((lens + wl.page_size - 1) // wl.page_size).sum())
+    alg = kv + rows * wl.head_dim_qk * 2 + rows * wl.head_dim_v * 2 + rows * 4 + pages * 4 + wl.batch * 4
+    args = (d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["seq_lens"], d["scale"], d["k_scale"],
+            d["v_scale"])
+    out, lse = fw.paged_decode_fp8(*args)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, warmup)):
+        fw.paged_decode_fp8(*args, out=out, lse=lse)
+    torch.cuda.synchronize()
+    fw.set_option(fw.FW_OPT_KERNEL_TIMING, 1)
+    fw.kernel_timing_read()
+    n = max(3, min(steps, 100))
+    l0 = fw.launch_count()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(n):
+        fw.paged_decode_fp8(*args, out=out, lse=lse)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(stop) / n
+    kms, kn = fw.kernel_timing_read()
+    fw.set_option(fw.FW_OPT_KERNEL_TIMING, 0)
+    if fw.device_status() != 0:
+        raise RuntimeError("device status nonzero during the FP8 decode benchmark")
+    per = kms / max(1, kn)
+    ach = alg / (per * 1e-3) / 1e9
+    return {"workload": DECODE_FP8_WL, "value": round(kv / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "kv_tokens_per_s": round(tokens / (ms * 1e-3), 1), "ms_per_step": round(ms, 4), "steps": n,
+            "kv_bytes_per_step": kv, "gpu_launches": fw.launch_count() - l0,
+            "config": {"batch": wl.batch, "q_len": wl.q_len, "num_q_heads": wl.num_q_heads,
+                       "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim_qk, "page_size": wl.page_size,
+                       "kv_dtype": "fp8_e4m3, one scale per cache", "total_kv_tokens": tokens},
+            "roofline": {"kernel": "paged_decode_fp8_kernel<16>", "bound": "hbm", "achieved": round(ach, 1),
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
+                         "traffic": ncu_traffic("paged_decode_fp8_ncu.json",
+                                                ["decode_fp8_kernel.cu", "decode_common.cuh", "fw_ptx.cuh"], tokens),
+                         "peak_source": peaks["source"], "algorithmic_bytes_per_launch": alg,
+                         "kernel_ms_per_launch": round(per, 4)}}
 
 
 # ------------------------------------------------------- latent decode
@@ -490,7 +548,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--only", choices=["all", "decode", "prefill", "prefill256", "latent"], default="all",
+    ap.add_argument("--only", choices=["all", "decode", "decode_fp8", "prefill", "prefill256", "latent"],
+                    default="all",
                     help="profiling runs: time one path only")
     ap.add_argument("--decode-batch", type=int, default=0,
                     help="profiling runs: a prefix of the decode batch (smaller capture)")
@@ -528,6 +587,11 @@ def main():
         if rank == 0:
             print(json.dumps({key: pre}), flush=True)
         return 0
+    if args.only == "decode_fp8":
+        f8 = bench_decode_fp8(fw, torch, args.steps, args.warmup, device, peaks, batch=args.decode_batch or None)
+        if rank == 0:
+            print(json.dumps({"decode_fp8": f8}), flush=True)
+        return 0
     if args.only == "latent":
         lat = bench_latent(fw, torch, args.steps, args.warmup, device, peaks, batch=args.latent_batch or None)
         if rank == 0:
@@ -539,6 +603,7 @@ def main():
     pre256 = (None if args.only == "decode" else
               bench_prefill(fw, torch, args.steps, args.warmup, device, peaks, name=PREFILL_HD256_WL))
     lat = None if args.only == "decode" else bench_latent(fw, torch, args.steps, args.warmup, device, peaks)
+    f8 = None if args.only == "decode" else bench_decode_fp8(fw, torch, args.steps, args.warmup, device, peaks)
     elapsed_ms, e2e_ms = max_over_ranks(pg, [dec["elapsed_ms"], dec["e2e_ms"]], device)
     value = whole_job_rate(dec["kv_bytes"], args.steps, world, elapsed_ms)
     e2e_value = whole_job_rate(dec["kv_bytes"], 1, world, e2e_ms)
@@ -555,7 +620,7 @@ def main():
             "e2e": {"value": round(e2e_value, 1) if e2e_value else None, "unit": "GB/s", "h2d_bytes_per_step": dec["h2d"],
                     "d2h_bytes_per_step": dec["d2h"], "steps": dec["e2e_steps"],
                     "note": "inputs (incl. the KV cache) copied from pinned host memory every step"},
-            "prefill": pre, "prefill_hd256": pre256, "latent_decode": lat}
+            "prefill": pre, "prefill_hd256": pre256, "latent_decode": lat, "decode_fp8": f8}
     if world == 1 and not args.no_cpu_baseline and not args.decode_batch:
         try:
             line["cpu_baseline"] = cpu_baseline(torch, dec["inputs"], dec["wl"])

@@ -104,6 +104,40 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Reduces each of the NQ per-lane values over the warp (max or sum) and
+// stores row r's result to dst[r].  Reduce-scatter: every butterfly stage
+// sends the half of the remaining rows that the partner lane keeps, so the
+// warp issues NQ - 1 + (5 - log2 NQ) shuffles instead of 5 NQ, and the
+// shuffles of one stage are independent of each other.
+template <int NQ, bool kMax>
+__device__ __forceinline__ void warp_rows_reduce(const float (&v)[NQ], int lane, float *dst) {
+    static_assert(NQ == 16 || NQ == 32, "rows per warp reduction");
+    float a[NQ];
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) a[i] = v[i];
+    int row = 0;
+#pragma unroll
+    for (int st = 0; st < 5; ++st) {
+        const int off = 16 >> st;
+        const int half = NQ >> (st + 1);
+        if (half >= 1) {
+            const bool hi = (lane & off) != 0;
+#pragma unroll
+            for (int i = 0; i < half; ++i) {
+                const float send = hi ? a[i] : a[half + i];
+                const float keep = hi ? a[half + i] : a[i];
+                const float got = __shfl_xor_sync(0xffffffffu, send, off);
+                a[i] = kMax ? fmaxf(keep, got) : keep + got;
+            }
+            row += hi ? half : 0;
+        } else {
+            const float got = __shfl_xor_sync(0xffffffffu, a[0], off);
+            a[0] = kMax ? fmaxf(a[0], got) : a[0] + got;
+        }
+    }
+    if ((lane & (32 / NQ - 1)) == 0) dst[row] = a[0];
+}
+
 // One lane waits, the whole warp learns the outcome (keeps the warp converged).
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const WaitCtx &w, int lane) {
     int ok = 1;

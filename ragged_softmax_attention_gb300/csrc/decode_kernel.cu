@@ -326,13 +326,8 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
                 if (lane == 0) mbar_arrive(&s_free[sb]);
                 float* rm = red_max + (jt & 1) * 4 * NQ;
 #pragma unroll
-                for (int r = 0; r < NQ; ++r) {
-                    s[r] = (tok < lim[r]) ? s[r] * p.scale_log2 : kNegInf;
-                    if (r < nrows) {
-                        const float v = warp_max(s[r]);
-                        if (lane == 0) rm[q4 * NQ + r] = v;
-                    }
-                }
+                for (int r = 0; r < NQ; ++r) s[r] = (tok < lim[r]) ? s[r] * p.scale_log2 : kNegInf;
+                warp_rows_reduce<NQ, true>(s, lane, rm + q4 * NQ);
                 named_bar_sync(1, 128);
                 bool need = false;
                 float mx[NQ];
@@ -408,13 +403,7 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
             }
             // ------------------------------------------------------ epilogue
             {
-#pragma unroll
-                for (int r = 0; r < NQ; ++r) {
-                    if (r < nrows) {
-                        const float v = warp_sum(l_part[r]);
-                        if (lane == 0) red_sum[q4 * NQ + r] = v;
-                    }
-                }
+                warp_rows_reduce<NQ, false>(l_part, lane, red_sum + q4 * NQ);
                 named_bar_sync(1, 128);
                 float L[NQ];
 #pragma unroll
