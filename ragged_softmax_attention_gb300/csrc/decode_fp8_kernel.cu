@@ -425,9 +425,8 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                 float mx[NQ];
 #pragma unroll
                 for (int r = 0; r < NQ; ++r) {
-                    mx[r] = kNegInf;
-                    if (r < nrows)
-                        mx[r] = fmaxf(fmaxf(rm[r], rm[NQ + r]), fmaxf(rm[2 * NQ + r], rm[3 * NQ + r]));
+                    // Padding rows hold -inf everywhere: mx = -inf, no rescale.
+                    mx[r] = fmaxf(fmaxf(rm[r], rm[NQ + r]), fmaxf(rm[2 * NQ + r], rm[3 * NQ + r]));
                     need |= mx[r] > m_ref[r] + kRescaleThreshold;
                 }
                 if (need) {
@@ -460,12 +459,10 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                 uint8_t *pbuf = sP + pb * C::kPBytes;
 #pragma unroll
                 for (int r = 0; r < NQ; ++r) {
-                    float pr = 0.f;
-                    if (r < nrows) {
-                        const float mu = (m_ref[r] == kNegInf) ? 0.f : m_ref[r] - kHeadroom;
-                        pr = ex2_approx(s[r] - mu);
-                        l_part[r] += pr;
-                    }
+                    // Masked keys and padding rows have s = -inf: p = 0 exactly.
+                    const float mu = (m_ref[r] == kNegInf) ? 0.f : m_ref[r] - kHeadroom;
+                    const float pr = ex2_approx(s[r] - mu);
+                    l_part[r] += pr;
                     *reinterpret_cast<__half *>(pbuf + sw128_offset(r, row_in_tile, NQ)) = __float2half_rn(pr);
                 }
                 fence_proxy_async_smem();
@@ -480,7 +477,7 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                 float L[NQ];
 #pragma unroll
                 for (int r = 0; r < NQ; ++r)
-                    L[r] = (r < nrows) ? (red_sum[r] + red_sum[NQ + r]) + (red_sum[2 * NQ + r] + red_sum[3 * NQ + r]) : 0.f;
+                    L[r] = (red_sum[r] + red_sum[NQ + r]) + (red_sum[2 * NQ + r] + red_sum[3 * NQ + r]);
                 mbar_wait(pv_done, (jt - 1) & 1, wc);
                 tc_fence_after();
                 float o[NQ];
