@@ -83,6 +83,7 @@ struct Fp8Cfg {
     static constexpr int kOffMisc = kOffRedSum + 4 * NQ * 4;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA exceeded");
+    static_assert(kOffRedMax % 16 == 0, "row maxima are read as float4");
     // TMEM: two FP16 K tiles (64 columns each), two S^T buffers, O^T
     static constexpr uint32_t kColK = 0;
     static constexpr uint32_t kColS = 128;
@@ -92,11 +93,14 @@ struct Fp8Cfg {
     static constexpr uint32_t kIdescPV = idesc_f16_f32(128, NQ, true, false);
 };
 
-template <int NQ>
+// NQ: query rows on the MMA N axis (16 or 32); R: rows the softmax carries
+// (8 when a unit holds at most 8 query rows, else NQ).
+template <int NQ, int R>
 __global__ void __launch_bounds__(320, 1)
 paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
     using C = Fp8Cfg<NQ>;
+    static_assert(R == 8 || R == NQ, "softmax rows");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sK8 = smem + C::kOffK8;
@@ -261,52 +265,55 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                 const uint32_t par8 = (jt / C::kStages8) & 1;
                 const int b16 = jt & 1;
                 const uint32_t par16 = ((jt >> 1) & 1) ^ 1;
-                // K row -> TMEM lane `key`, 64 columns of FP16 pairs
+                // K row -> TMEM lane `key`, 64 columns of FP16 pairs.  The
+                // loops stay rolled: the converter shares each SM sub-partition
+                // with a softmax warp, and a compact body keeps both in the
+                // instruction cache.
                 mbar_wait(&k8_full[s8], par8, wc);
-                uint4 raw[8];
-                const uint8_t *krow = sK8 + s8 * C::kTile8Bytes + key * 128;
-#pragma unroll
-                for (int u = 0; u < 8; ++u) raw[u] = *reinterpret_cast<const uint4 *>(krow + ((u ^ (key & 7)) << 4));
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&k8_empty[s8]);
                 mbar_wait(&k16_empty[b16], par16, wc);
                 tc_fence_after();
-#pragma unroll
+                const uint8_t *krow = sK8 + s8 * C::kTile8Bytes + key * 128;
+#pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
+                    uint4 r[2];
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        r[k] = *reinterpret_cast<const uint4 *>(krow + (((2 * c + k) ^ (key & 7)) << 4));
+                        if (!live) r[k] = make_uint4(0, 0, 0, 0);
+                    }
                     uint32_t w16[16];
 #pragma unroll
                     for (int k = 0; k < 2; ++k) {
-                        const uint4 r = raw[2 * c + k];
-                        const uint32_t wd[4] = {r.x, r.y, r.z, r.w};
+                        const uint32_t wd[4] = {r[k].x, r[k].y, r[k].z, r[k].w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            w16[8 * k + 2 * e] = live ? e4m3x2_to_f16x2((uint16_t)(wd[e] & 0xffffu)) : 0u;
-                            w16[8 * k + 2 * e + 1] = live ? e4m3x2_to_f16x2((uint16_t)(wd[e] >> 16)) : 0u;
+                            w16[8 * k + 2 * e] = e4m3x2_to_f16x2((uint16_t)(wd[e] & 0xffffu));
+                            w16[8 * k + 2 * e + 1] = e4m3x2_to_f16x2((uint16_t)(wd[e] >> 16));
                         }
                     }
                     tmem_st16u(tmem + lane_off + C::kColK + b16 * 64 + c * 16, w16);
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&k8_empty[s8]);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&k16_full[b16]);
                 // V row -> swizzled FP16 tile (two 64-column chunks)
                 mbar_wait(&v8_full[s8], par8, wc);
-                const uint8_t *vrow = sV8 + s8 * C::kTile8Bytes + key * 128;
-#pragma unroll
-                for (int u = 0; u < 8; ++u) raw[u] = *reinterpret_cast<const uint4 *>(vrow + ((u ^ (key & 7)) << 4));
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&v8_empty[s8]);
                 mbar_wait(&v16_empty[b16], par16, wc);
+                const uint8_t *vrow = sV8 + s8 * C::kTile8Bytes + key * 128;
                 uint8_t *v16 = sV16 + b16 * C::kTile16Bytes;
-#pragma unroll
+#pragma unroll 1
                 for (int u = 0; u < 8; ++u) {              // FP8 unit u = columns 16u .. 16u + 15
-                    const uint32_t wd[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+                    uint4 r = *reinterpret_cast<const uint4 *>(vrow + ((u ^ (key & 7)) << 4));
+                    if (!live) r = make_uint4(0, 0, 0, 0);
+                    const uint32_t wd[4] = {r.x, r.y, r.z, r.w};
                     uint32_t h[8];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        h[2 * e] = live ? e4m3x2_to_f16x2((uint16_t)(wd[e] & 0xffffu)) : 0u;
-                        h[2 * e + 1] = live ? e4m3x2_to_f16x2((uint16_t)(wd[e] >> 16)) : 0u;
+                        h[2 * e] = e4m3x2_to_f16x2((uint16_t)(wd[e] & 0xffffu));
+                        h[2 * e + 1] = e4m3x2_to_f16x2((uint16_t)(wd[e] >> 16));
                     }
                     const int chunk = u >> 2;                // 64 columns per chunk
                     const int unit = (u & 3) * 2;            // 8 FP16 columns per 16-byte unit
@@ -314,6 +321,8 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                     *reinterpret_cast<uint4 *>(rowp + ((unit ^ (key & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
                     *reinterpret_cast<uint4 *>(rowp + (((unit + 1) ^ (key & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&v8_empty[s8]);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&v16_full[b16]);
@@ -390,49 +399,55 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
         it.init(p);
         Unit x;
         while (it.next(p, x)) {
-            int lim[NQ];
+            int lim[R];
             int nrows = 0;
 #pragma unroll
-            for (int r = 0; r < NQ; ++r) {
+            for (int r = 0; r < R; ++r) {
                 int t, h;
                 const bool ok = unit_row(p, x, r, t, h);
                 lim[r] = ok ? min(x.n, x.n - p.q_len + t + 1) : 0;
                 if (ok) nrows = r + 1;
             }
-            float m_ref[NQ], l_part[NQ];
+            float m_ref[R], l_part[R];
 #pragma unroll
-            for (int r = 0; r < NQ; ++r) { m_ref[r] = kNegInf; l_part[r] = 0.f; }
+            for (int r = 0; r < R; ++r) { m_ref[r] = kNegInf; l_part[r] = 0.f; }
             for (int i = 0; i < x.ntiles; ++i, ++jt) {
                 const int ts = x.k_begin + i * kKvTile;
                 const int tok = ts + row_in_tile;
                 const int sb = jt & 1;
                 mbar_wait(&s_full[sb], (jt >> 1) & 1, wc);
                 tc_fence_after();
-                float s[NQ];
-#pragma unroll
-                for (int c = 0; c < NQ; c += 16)
-                    tmem_ld16(tmem + lane_off + C::kColS + sb * NQ + c, *reinterpret_cast<float(*)[16]>(&s[c]));
+                float s[R];
+                tmem_ld_cols<R>(tmem + lane_off + C::kColS + sb * NQ, s);
                 tmem_wait_ld();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s_free[sb]);
-                float *rm = red_max + (jt & 1) * 4 * NQ;
+                float *rm = red_max + (jt & 1) * 4 * R;
 #pragma unroll
-                for (int r = 0; r < NQ; ++r) s[r] = (tok < lim[r]) ? s[r] * p.scale_log2 : kNegInf;
-                warp_rows_reduce<NQ, true>(s, lane, rm + q4 * NQ);
+                for (int r = 0; r < R; ++r) s[r] = (tok < lim[r]) ? s[r] * p.scale_log2 : kNegInf;
+                warp_rows_reduce<R, true>(s, lane, rm + q4 * R);
                 named_bar_sync(1, 128);
                 bool need = false;
-                float mx[NQ];
+                float mx[R];
 #pragma unroll
-                for (int r = 0; r < NQ; ++r) {
+                for (int r = 0; r < R; r += 4) {
                     // Padding rows hold -inf everywhere: mx = -inf, no rescale.
-                    mx[r] = fmaxf(fmaxf(rm[r], rm[NQ + r]), fmaxf(rm[2 * NQ + r], rm[3 * NQ + r]));
-                    need |= mx[r] > m_ref[r] + kRescaleThreshold;
-                }
-                if (need) {
-                    float alpha[NQ];
+                    float4 m4 = *reinterpret_cast<const float4 *>(rm + r);
 #pragma unroll
-                    for (int r = 0; r < NQ; ++r) {
+                    for (int q = 1; q < 4; ++q) {
+                        const float4 o4 = *reinterpret_cast<const float4 *>(rm + q * R + r);
+                        m4.x = fmaxf(m4.x, o4.x); m4.y = fmaxf(m4.y, o4.y);
+                        m4.z = fmaxf(m4.z, o4.z); m4.w = fmaxf(m4.w, o4.w);
+                    }
+                    mx[r] = m4.x; mx[r + 1] = m4.y; mx[r + 2] = m4.z; mx[r + 3] = m4.w;
+                }
+#pragma unroll
+                for (int r = 0; r < R; ++r) need |= mx[r] > m_ref[r] + kRescaleThreshold;
+                if (need) {
+                    float alpha[R];
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
                         const float mn = fmaxf(m_ref[r], mx[r]);
                         alpha[r] = (mn == kNegInf) ? 1.f : ex2_approx(m_ref[r] - mn);
                         l_part[r] *= alpha[r];
@@ -441,16 +456,13 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                     if (i > 0) {
                         mbar_wait(pv_done, (jt - 1) & 1, wc);
                         tc_fence_after();
+                        float o[R];
+                        const uint32_t ta = tmem + lane_off + C::kColO;
+                        tmem_ld_cols<R>(ta, o);
+                        tmem_wait_ld();
 #pragma unroll
-                        for (int c = 0; c < NQ; c += 16) {
-                            float o[16];
-                            const uint32_t ta = tmem + lane_off + C::kColO + c;
-                            tmem_ld16(ta, o);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int k = 0; k < 16; ++k) o[k] *= alpha[c + k];
-                            tmem_st16(ta, o);
-                        }
+                        for (int k = 0; k < R; ++k) o[k] *= alpha[k];
+                        tmem_st_cols<R>(ta, o);
                         tmem_wait_st();
                     }
                 }
@@ -458,8 +470,9 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                 mbar_wait(&p_free[pb], ((jt >> 1) & 1) ^ 1, wc);
                 uint8_t *pbuf = sP + pb * C::kPBytes;
 #pragma unroll
-                for (int r = 0; r < NQ; ++r) {
+                for (int r = 0; r < R; ++r) {
                     // Masked keys and padding rows have s = -inf: p = 0 exactly.
+                    // Rows R..NQ-1 of P stay at the zeros written at start.
                     const float mu = (m_ref[r] == kNegInf) ? 0.f : m_ref[r] - kHeadroom;
                     const float pr = ex2_approx(s[r] - mu);
                     l_part[r] += pr;
@@ -472,22 +485,20 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
             }
             // ------------------------------------------------------ epilogue
             {
-                warp_rows_reduce<NQ, false>(l_part, lane, red_sum + q4 * NQ);
+                warp_rows_reduce<R, false>(l_part, lane, red_sum + q4 * R);
                 named_bar_sync(1, 128);
-                float L[NQ];
+                float L[R];
 #pragma unroll
-                for (int r = 0; r < NQ; ++r)
-                    L[r] = (red_sum[r] + red_sum[NQ + r]) + (red_sum[2 * NQ + r] + red_sum[3 * NQ + r]);
+                for (int r = 0; r < R; ++r)
+                    L[r] = (red_sum[r] + red_sum[R + r]) + (red_sum[2 * R + r] + red_sum[3 * R + r]);
                 mbar_wait(pv_done, (jt - 1) & 1, wc);
                 tc_fence_after();
-                float o[NQ];
-#pragma unroll
-                for (int c = 0; c < NQ; c += 16)
-                    tmem_ld16(tmem + lane_off + C::kColO + c, *reinterpret_cast<float(*)[16]>(&o[c]));
+                float o[R];
+                tmem_ld_cols<R>(tmem + lane_off + C::kColO, o);
                 tmem_wait_ld();
                 const int dv = row_in_tile;
 #pragma unroll
-                for (int r = 0; r < NQ; ++r) {
+                for (int r = 0; r < R; ++r) {
                     int t, h;
                     if (r >= nrows || !unit_row(p, x, r, t, h)) continue;
                     const float val = L[r] > 0.f ? o[r] / L[r] * p.out_scale : 0.f;
@@ -506,7 +517,7 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                     if (unit_row(p, x, r, t, h)) {
                         float lse2 = kNegInf;
 #pragma unroll
-                        for (int k = 0; k < NQ; ++k)
+                        for (int k = 0; k < R; ++k)
                             if (k == r && L[k] > 0.f) lse2 = m_ref[k] - kHeadroom + __log2f(L[k]);
                         if (x.single) {
                             if (p.lse)
@@ -530,18 +541,18 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
     if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-template <int NQ>
+template <int NQ, int R>
 cudaError_t launch_fp8_t(const DecodeParams &p, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                          cudaStream_t stream) {
     using C = Fp8Cfg<NQ>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(paged_decode_fp8_kernel<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(paged_decode_fp8_kernel<NQ, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    paged_decode_fp8_kernel<NQ><<<p.grid, 320, C::kSmemBytes, stream>>>(p, tq, tk, tv);
+    paged_decode_fp8_kernel<NQ, R><<<p.grid, 320, C::kSmemBytes, stream>>>(p, tq, tk, tv);
     return cudaGetLastError();
 }
 
@@ -555,8 +566,10 @@ cudaError_t launch_decode_fp8(const DecodeParams &p, const CUtensorMap &tq, cons
     if (e != cudaSuccess) return e;
     ++*launches;
     if (timing_start) cudaEventRecord(timing_start, stream);
-    if (p.rows == 16) e = launch_fp8_t<16>(p, tq, tk, tv, stream);
-    else if (p.rows == 32) e = launch_fp8_t<32>(p, tq, tk, tv, stream);
+    const bool narrow = p.head_mode == 0 && p.G * p.tokens_per_unit <= 8;
+    if (p.rows == 16 && narrow) e = launch_fp8_t<16, 8>(p, tq, tk, tv, stream);
+    else if (p.rows == 16) e = launch_fp8_t<16, 16>(p, tq, tk, tv, stream);
+    else if (p.rows == 32) e = launch_fp8_t<32, 32>(p, tq, tk, tv, stream);
     else return cudaErrorInvalidValue;
     if (e != cudaSuccess) return e;
     ++*launches;
