@@ -265,15 +265,12 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                 const uint32_t par8 = (jt / C::kStages8) & 1;
                 const int b16 = jt & 1;
                 const uint32_t par16 = ((jt >> 1) & 1) ^ 1;
-                // K row -> TMEM lane `key`, 64 columns of FP16 pairs.  The
-                // loops stay rolled: the converter shares each SM sub-partition
-                // with a softmax warp, and a compact body keeps both in the
-                // instruction cache.
+                // K row -> TMEM lane `key`, 64 columns of FP16 pairs.
                 mbar_wait(&k8_full[s8], par8, wc);
                 mbar_wait(&k16_empty[b16], par16, wc);
                 tc_fence_after();
                 const uint8_t *krow = sK8 + s8 * C::kTile8Bytes + key * 128;
-#pragma unroll 1
+#pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint4 r[2];
 #pragma unroll
@@ -304,7 +301,7 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                 mbar_wait(&v16_empty[b16], par16, wc);
                 const uint8_t *vrow = sV8 + s8 * C::kTile8Bytes + key * 128;
                 uint8_t *v16 = sV16 + b16 * C::kTile16Bytes;
-#pragma unroll 1
+#pragma unroll 4
                 for (int u = 0; u < 8; ++u) {              // FP8 unit u = columns 16u .. 16u + 15
                     uint4 r = *reinterpret_cast<const uint4 *>(vrow + ((u ^ (key & 7)) << 4));
                     if (!live) r = make_uint4(0, 0, 0, 0);
@@ -454,6 +451,9 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                         m_ref[r] = mn;
                     }
                     if (i > 0) {
+                        // PV(jt - 1) landed; s_full(jt) was committed after
+                        // PV(jt - 2) was issued, so pv_done is at most one
+                        // phase behind here.
                         mbar_wait(pv_done, (jt - 1) & 1, wc);
                         tc_fence_after();
                         float o[R];
@@ -491,7 +491,13 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
 #pragma unroll
                 for (int r = 0; r < R; ++r)
                     L[r] = (red_sum[r] + red_sum[R + r]) + (red_sum[2 * R + r] + red_sum[3 * R + r]);
-                mbar_wait(pv_done, (jt - 1) & 1, wc);
+                // O^T is final once PV(jt - 2) and PV(jt - 1), the unit's
+                // last, have landed.  These are the P-buffer waits of tiles jt
+                // and jt + 1: each buffer's phase is at most one behind, while
+                // a parity wait on pv_done alone could pass with PV(jt - 2)
+                // still in flight.
+                mbar_wait(&p_free[jt & 1], ((jt >> 1) & 1) ^ 1, wc);
+                mbar_wait(&p_free[(jt + 1) & 1], (((jt + 1) >> 1) & 1) ^ 1, wc);
                 tc_fence_after();
                 float o[R];
                 tmem_ld_cols<R>(tmem + lane_off + C::kColO, o);

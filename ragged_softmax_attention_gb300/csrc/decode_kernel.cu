@@ -347,7 +347,9 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
                         m_ref[r] = mn;
                     }
                     if (i > 0) {
-                        // Rescale the accumulated O^T once the previous PV has landed.
+                        // Rescale the accumulated O^T once PV(jt - 1) has landed.
+                        // s_full(jt) was committed after PV(jt - 2) was issued,
+                        // so pv_done is at most one phase behind here.
                         mbar_wait(pv_done, (jt - 1) & 1, wc);
                         tc_fence_after();
 #pragma unroll
@@ -406,7 +408,13 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
 #pragma unroll
                 for (int r = 0; r < NQ; ++r)
                     L[r] = (red_sum[r] + red_sum[NQ + r]) + (red_sum[2 * NQ + r] + red_sum[3 * NQ + r]);
-                mbar_wait(pv_done, (jt - 1) & 1, wc);
+                // O^T is final once PV(jt - 2) and PV(jt - 1), the unit's
+                // last, have landed.  These are the P-buffer waits of tiles jt
+                // and jt + 1: each buffer's phase is at most one behind, while
+                // a parity wait on pv_done alone could pass with PV(jt - 2)
+                // still in flight.
+                mbar_wait(&p_free[jt & 1], ((jt >> 1) & 1) ^ 1, wc);
+                mbar_wait(&p_free[(jt + 1) & 1], (((jt + 1) >> 1) & 1) ^ 1, wc);
                 tc_fence_after();
 #pragma unroll
                 for (int dvt = 0; dvt < C::kDvTiles; ++dvt) {

@@ -182,3 +182,25 @@ def test_qwen3_14b_decode_full_size_sampled_rows(fw):
         o_ref, l_ref = oracle.paged_decode(d["q"][b:b + 1].cpu(), k, v, sub_bt, lens[b:b + 1], wl.scale,
                                            rows=heads)
         compare(out[b, 0, heads], lse[b, 0, heads], o_ref, l_ref, f"b{b}")
+
+
+@pytest.mark.parametrize("chunk", [0, 512])
+def test_repeated_launches_are_bitwise_identical(fw, chunk):
+    """Every launch writes the same bytes.  An accumulator read before its last
+    MMA has landed, or a buffer refilled while still in use, shows up as drift
+    between launches.  Full-size Qwen3-14B-shaped workload, six launches, with
+    and without forced split-KV chunking."""
+    wl = WORKLOADS["qwen3_14b_paged_decode"]
+    d = make_decode_inputs(wl, "cuda")
+    args = (d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["seq_lens"], d["scale"])
+    fw.set_option(fw.FW_OPT_DECODE_CHUNK_TOKENS, chunk)
+    try:
+        out0, lse0 = fw.paged_decode(*args)
+        for _ in range(5):
+            out, lse = fw.paged_decode(*args)
+            torch.cuda.synchronize()
+            assert fw.device_status() == 0
+            assert torch.equal(out.view(torch.int16), out0.view(torch.int16))
+            assert torch.equal(lse.view(torch.int32), lse0.view(torch.int32))
+    finally:
+        fw.set_option(fw.FW_OPT_DECODE_CHUNK_TOKENS, 0)

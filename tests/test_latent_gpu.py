@@ -141,3 +141,19 @@ def test_invalid_latent_shapes_launch_nothing(fw):
         fw.paged_decode(d["q"][..., :512], d["k_cache"][..., :512], d["k_cache"][..., :512], d["block_table"],
                         d["seq_lens"], 0.1)
     assert fw.launch_count() == before
+
+
+def test_repeated_launches_are_bitwise_identical(fw):
+    """Every launch writes the same bytes (an accumulator read before its last
+    MMA has landed shows up as drift between launches).  Full-size latent
+    workload, four launches."""
+    wl = WORKLOADS["latent_paged_decode"]
+    d = make_decode_inputs(wl, "cuda")
+    args = (d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["seq_lens"], d["scale"])
+    out0, lse0 = fw.paged_decode(*args)
+    for _ in range(3):
+        out, lse = fw.paged_decode(*args)
+        torch.cuda.synchronize()
+        assert fw.device_status() == 0
+        assert torch.equal(out.view(torch.int16), out0.view(torch.int16))
+        assert torch.equal(lse.view(torch.int32), lse0.view(torch.int32))
