@@ -77,7 +77,7 @@ struct Fp8Cfg {
     static constexpr int kOffQ = kOffV16 + 2 * kTile16Bytes;
     static constexpr int kOffP = kOffQ + 2 * kQBytes;
     static constexpr int kOffBar = kOffP + 2 * kPBytes;
-    static constexpr int kNumBars = 4 * kStages8 + 2 * 2 + 2 * 2 + 2 + 2 + 2 + 2 + 2 + 2 + 2 + 1 + 1;
+    static constexpr int kNumBars = 4 * kStages8 + 2 * 2 + 2 * 2 + 2 + 2 + 2 + 2 + 2 + 1 + 1;
     static constexpr int kOffRedMax = kOffBar + kNumBars * 8;
     static constexpr int kOffRedSum = kOffRedMax + 2 * 4 * NQ * 4;
     static constexpr int kOffMisc = kOffRedSum + 4 * NQ * 4;
@@ -114,18 +114,20 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
     uint64_t *v8_full = k8_empty + C::kStages8;
     uint64_t *v8_empty = v8_full + C::kStages8;
     uint64_t *k16_full = v8_empty + C::kStages8;      // [2]
-    uint64_t *k16_empty = k16_full + 2;                // [2]
-    uint64_t *v16_full = k16_empty + 2;                // [2]
-    uint64_t *v16_empty = v16_full + 2;                // [2]
-    uint64_t *q_full = v16_empty + 2;                  // [2] BF16 Q landed
+    // One commit per MMA group: qk_done[b] (QK of tile j, b = j & 1) frees
+    // the FP16 K buffer b and publishes S buffer b; pv_done[b] (PV of tile j)
+    // frees the FP16 V buffer and the P buffer b.  A commit costs the tensor
+    // pipe about as much as an N = 16 MMA, so each event has one barrier,
+    // waited on by every role that needs it.
+    uint64_t *qk_done = k16_full + 2;                  // [2]
+    uint64_t *v16_full = qk_done + 2;                  // [2]
+    uint64_t *pv_done = v16_full + 2;                  // [2]
+    uint64_t *q_full = pv_done + 2;                    // [2] BF16 Q landed
     uint64_t *q16 = q_full + 2;                        // [2] Q converted to FP16
     uint64_t *q_empty = q16 + 2;                       // [2]
-    uint64_t *s_full = q_empty + 2;                    // [2]
-    uint64_t *s_free = s_full + 2;                     // [2]
+    uint64_t *s_free = q_empty + 2;                    // [2]
     uint64_t *p_full = s_free + 2;                     // [2]
-    uint64_t *p_free = p_full + 2;                     // [2]
-    uint64_t *pv_done = p_free + 2;                    // [1]
-    uint64_t *drain = pv_done + 1;                     // [1]
+    uint64_t *drain = p_full + 2;                      // [1]
     float *red_max = reinterpret_cast<float *>(smem + C::kOffRedMax);   // [2][4][NQ]
     float *red_sum = reinterpret_cast<float *>(smem + C::kOffRedSum);   // [4][NQ]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
@@ -140,13 +142,12 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
             mbar_init(&v8_full[i], 1); mbar_init(&v8_empty[i], 4);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&k16_full[i], 4); mbar_init(&k16_empty[i], 1);
-            mbar_init(&v16_full[i], 4); mbar_init(&v16_empty[i], 1);
+            mbar_init(&k16_full[i], 4); mbar_init(&qk_done[i], 1);
+            mbar_init(&v16_full[i], 4); mbar_init(&pv_done[i], 1);
             mbar_init(&q_full[i], 1); mbar_init(&q16[i], 4); mbar_init(&q_empty[i], 1);
-            mbar_init(&s_full[i], 1); mbar_init(&s_free[i], 4);
-            mbar_init(&p_full[i], 4); mbar_init(&p_free[i], 1);
+            mbar_init(&s_free[i], 4);
+            mbar_init(&p_full[i], 4);
         }
-        mbar_init(pv_done, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -267,7 +268,7 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                 const uint32_t par16 = ((jt >> 1) & 1) ^ 1;
                 // K row -> TMEM lane `key`, 64 columns of FP16 pairs.
                 mbar_wait(&k8_full[s8], par8, wc);
-                mbar_wait(&k16_empty[b16], par16, wc);
+                mbar_wait(&qk_done[b16], par16, wc);      // QK(jt - 2) read this buffer
                 tc_fence_after();
                 const uint8_t *krow = sK8 + s8 * C::kTile8Bytes + key * 128;
 #pragma unroll
@@ -298,7 +299,7 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                 if (lane == 0) mbar_arrive(&k16_full[b16]);
                 // V row -> swizzled FP16 tile (two 64-column chunks)
                 mbar_wait(&v8_full[s8], par8, wc);
-                mbar_wait(&v16_empty[b16], par16, wc);
+                mbar_wait(&pv_done[b16], par16, wc);      // PV(jt - 2) read this buffer
                 const uint8_t *vrow = sV8 + s8 * C::kTile8Bytes + key * 128;
                 uint8_t *v16 = sV16 + b16 * C::kTile16Bytes;
 #pragma unroll 4
@@ -345,9 +346,7 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                     const uint64_t b = sdesc_sw128(p_base + (kk >> 2) * NQ * 128 + (kk & 3) * 32, 16, 1024);
                     mma_bf16_ss(tmem + C::kColO, a, b, C::kIdescPV, (first && kk == 0) ? 0u : 1u);
                 }
-                mma_commit(&v16_empty[b16]);
-                mma_commit(&p_free[pb]);
-                mma_commit(pv_done);
+                mma_commit(&pv_done[b16]);
                 return true;
             };
             PieceIter it;
@@ -369,8 +368,7 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                         mma_bf16_ts(tmem + C::kColS + sb * NQ, tmem + C::kColK + b16 * 64 + kk * 8, b, C::kIdescQK,
                                     kk > 0 ? 1u : 0u);
                     }
-                    mma_commit(&k16_empty[b16]);
-                    mma_commit(&s_full[sb]);
+                    mma_commit(&qk_done[b16]);
                     if (i == x.ntiles - 1) mma_commit(&q_empty[qs]);
                     if (pend >= 0 && !issue_pv(pend, pend_first)) goto mma_done;
                     pend = jt;
@@ -412,7 +410,7 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                 const int ts = x.k_begin + i * kKvTile;
                 const int tok = ts + row_in_tile;
                 const int sb = jt & 1;
-                mbar_wait(&s_full[sb], (jt >> 1) & 1, wc);
+                mbar_wait(&qk_done[sb], (jt >> 1) & 1, wc);
                 tc_fence_after();
                 float s[R];
                 tmem_ld_cols<R>(tmem + lane_off + C::kColS + sb * NQ, s);
@@ -451,10 +449,10 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                         m_ref[r] = mn;
                     }
                     if (i > 0) {
-                        // PV(jt - 1) landed; s_full(jt) was committed after
-                        // PV(jt - 2) was issued, so pv_done is at most one
-                        // phase behind here.
-                        mbar_wait(pv_done, (jt - 1) & 1, wc);
+                        // Rescale once PV(jt - 1) has landed (the P-buffer wait
+                        // of tile jt + 1); PV(jt - 2) has, as qk_done(jt) was
+                        // committed after it was issued.
+                        mbar_wait(&pv_done[(jt + 1) & 1], (((jt + 1) >> 1) & 1) ^ 1, wc);
                         tc_fence_after();
                         float o[R];
                         const uint32_t ta = tmem + lane_off + C::kColO;
@@ -467,7 +465,7 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                     }
                 }
                 const int pb = jt & 1;
-                mbar_wait(&p_free[pb], ((jt >> 1) & 1) ^ 1, wc);
+                mbar_wait(&pv_done[pb], ((jt >> 1) & 1) ^ 1, wc);     // PV(jt - 2) read P buffer pb
                 uint8_t *pbuf = sP + pb * C::kPBytes;
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
@@ -492,12 +490,11 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                 for (int r = 0; r < R; ++r)
                     L[r] = (red_sum[r] + red_sum[R + r]) + (red_sum[2 * R + r] + red_sum[3 * R + r]);
                 // O^T is final once PV(jt - 2) and PV(jt - 1), the unit's
-                // last, have landed.  These are the P-buffer waits of tiles jt
-                // and jt + 1: each buffer's phase is at most one behind, while
-                // a parity wait on pv_done alone could pass with PV(jt - 2)
-                // still in flight.
-                mbar_wait(&p_free[jt & 1], ((jt >> 1) & 1) ^ 1, wc);
-                mbar_wait(&p_free[(jt + 1) & 1], (((jt + 1) >> 1) & 1) ^ 1, wc);
+                // last, have landed: the P-buffer waits of tiles jt and jt + 1.
+                // Each buffer's barrier is at most one phase behind its waiter,
+                // so the parity waits are unambiguous.
+                mbar_wait(&pv_done[jt & 1], ((jt >> 1) & 1) ^ 1, wc);
+                mbar_wait(&pv_done[(jt + 1) & 1], (((jt + 1) >> 1) & 1) ^ 1, wc);
                 tc_fence_after();
                 float o[R];
                 tmem_ld_cols<R>(tmem + lane_off + C::kColO, o);
