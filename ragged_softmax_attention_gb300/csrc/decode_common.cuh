@@ -111,7 +111,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 // shuffles of one stage are independent of each other.
 template <int NQ, bool kMax>
 __device__ __forceinline__ void warp_rows_reduce(const float (&v)[NQ], int lane, float *dst) {
-    static_assert(NQ == 8 || NQ == 16 || NQ == 32, "rows per warp reduction");
+    static_assert(NQ == 4 || NQ == 8 || NQ == 16 || NQ == 32, "rows per warp reduction");
     float a[NQ];
 #pragma unroll
     for (int i = 0; i < NQ; ++i) a[i] = v[i];
@@ -141,24 +141,30 @@ __device__ __forceinline__ void warp_rows_reduce(const float (&v)[NQ], int lane,
 // R consecutive 32-bit TMEM columns of this warp's lane quadrant.
 template <int R>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[R]) {
-    static_assert(R % 8 == 0, "columns in groups of 8");
+    static_assert(R % 4 == 0, "columns in groups of 4");
     if constexpr (R % 16 == 0) {
 #pragma unroll
         for (int c = 0; c < R; c += 16) tmem_ld16(taddr + c, *reinterpret_cast<float(*)[16]>(&v[c]));
-    } else {
+    } else if constexpr (R % 8 == 0) {
 #pragma unroll
         for (int c = 0; c < R; c += 8) tmem_ld8(taddr + c, *reinterpret_cast<float(*)[8]>(&v[c]));
+    } else {
+#pragma unroll
+        for (int c = 0; c < R; c += 4) tmem_ld4(taddr + c, *reinterpret_cast<float(*)[4]>(&v[c]));
     }
 }
 template <int R>
 __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const float (&v)[R]) {
-    static_assert(R % 8 == 0, "columns in groups of 8");
+    static_assert(R % 4 == 0, "columns in groups of 4");
     if constexpr (R % 16 == 0) {
 #pragma unroll
         for (int c = 0; c < R; c += 16) tmem_st16(taddr + c, *reinterpret_cast<const float(*)[16]>(&v[c]));
-    } else {
+    } else if constexpr (R % 8 == 0) {
 #pragma unroll
         for (int c = 0; c < R; c += 8) tmem_st8(taddr + c, *reinterpret_cast<const float(*)[8]>(&v[c]));
+    } else {
+#pragma unroll
+        for (int c = 0; c < R; c += 4) tmem_st4(taddr + c, *reinterpret_cast<const float(*)[4]>(&v[c]));
     }
 }
 

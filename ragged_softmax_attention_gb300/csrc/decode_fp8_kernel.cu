@@ -3,26 +3,40 @@
 // "TokenSpeed-MLA 2.0.1" (decode): FP8 inputs, BF16 output.  The cache holds
 // E4M3 bytes with one scale per cache (k = k_scale * e4m3, v = v_scale *
 // e4m3); HBM traffic per key is half that of a BF16 cache, which is what a
-// bandwidth-bound decode gains.  The arithmetic keeps 16-bit operands: every
-// E4M3 value is exact in FP16, so converter warps widen the K and V tiles to
-// FP16 next to the tensor core and the MMAs run kind::f16 with FP16 A and B
-// (queries converted from BF16 once per unit, probabilities written as FP16);
-// k_scale folds into the score scale, v_scale into the epilogue.
+// bandwidth-bound decode gains.
+//
+// The tensor cores read the E4M3 tiles as TMA lands them (kind::f8f6f4, 32
+// keys or dims per instruction): nothing widens K or V.  The 16-bit sides of
+// the two products enter as sums of 8-bit terms stacked along the MMA's N
+// axis, so one instruction covers all terms while reading its K or V slice
+// once:
+//   * Q: each BF16 query row is scaled by a power of two 2^e (its largest
+//     magnitude lands in [128, 256)) and split into hi + mid E4M3 terms.
+//     Every BF16 value of the row down to 2^-10 of that maximum is exactly
+//     hi + mid (8 significant bits = two 4-bit terms); S = S_hi + S_mid and
+//     2^-e folds into the row's score scale, k_scale too.
+//   * P: each probability is rounded to FP16 (as a 16-bit MMA would take it)
+//     and split into four E5M2 terms; E5M2 is FP16's upper byte, so the four
+//     terms (3 significant bits each) give the FP16 value exactly across
+//     FP16's range.  O = O_1 + O_2 + O_3 + O_4, v_scale in the epilogue.
+// The arithmetic therefore matches a kernel that widens K and V to FP16 and
+// runs FP16 MMAs on FP16 queries and probabilities.
 //
 // Layout and schedule follow the BF16 decode kernel (swap-AB: S^T [128 keys x
-// NQ] = K * Q^T, O^T [128 x NQ] += V^T * P^T; balanced tile ranges; split-KV
-// pieces merged by the combine kernel).  Differences:
-//   * warp 0 (TMA) loads 16 KiB FP8 tiles (128 keys x 128 bytes) into two
-//     byte rings, one for K and one for V;
-//   * warps 6-9 convert, one thread per key: the K row into TMEM as the A
-//     operand of QK^T (thread = key = TMEM lane, 2 FP16 per column), the V
-//     row into a swizzled FP16 tile in shared memory (the A operand of PV);
-//     keys past the piece's end become zeros, so NaN bytes in unused slots
-//     never meet the MMAs;
-//   * warp 1 issues the MMAs (QK^T in TS form), warps 2-5 run the softmax
-//     with the conditional rescale of the BF16 kernel.
+// 2 NQ] = K * [Q_hi; Q_mid]^T, O^T [128 x 4 NQ] += V^T * [P_1..P_4]^T with V^T
+// read MN-major straight from the 128-byte key rows; balanced tile ranges;
+// split-KV pieces merged by the combine kernel).  Roles:
+//   * warp 0 (TMA): per tile one ring stage holding the K and the V tile;
+//   * warp 1 issues QK^T (4 instructions) and PV (4 instructions), one
+//     commit each: qk_done publishes S; kv_empty frees the ring stage and the
+//     P buffer and, for the rescale and the epilogue, marks O^T;
+//   * warps 2-9: softmax, two warps per TMEM lane quadrant (thread = key),
+//     each with half of the unit's query rows; they also build the Q terms
+//     once per unit and zero the V rows of keys past a row's end, so NaN bytes
+//     in unused slots never meet an MMA.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "decode_common.cuh"
 #include "fw_internal.h"
@@ -36,100 +50,90 @@ using namespace dec;
 
 constexpr float kNegInf = -__builtin_huge_valf();
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: 2^(s - base) stays below 2^8
-// Probabilities go to the MMA as FP16, whose normal range starts at 2^-14;
-// they are taken relative to base - kHeadroom (at most 2^15, inside FP16's
-// 65504) so that small ones keep their precision.  l carries the same factor,
-// and the LSE subtracts it again.
+// Probabilities are taken relative to base - kHeadroom: at most 2^15, inside
+// FP16's (and E5M2's) range, with small ones clear of the subnormals.  l
+// carries the same factor and the LSE subtracts it again.
 constexpr float kHeadroom = 7.0f;
 constexpr int D = 128;
+constexpr int kQTerms = 2;   // E4M3 terms of a scaled BF16 query
+constexpr int kPTerms = 4;   // E5M2 terms of an FP16 probability
+constexpr int kSoftmaxThreads = 256;
 
-// Instruction descriptor, kind::f16 with FP16 A/B and FP32 accumulation.
-__host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N, bool a_mn_major, bool b_mn_major) {
-    return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) | ((N >> 3) << 17) |
-           ((M >> 4) << 24);
+// kind::f8f6f4 instruction descriptor: FP32 accumulation, A E4M3, B E4M3 (0)
+// or E5M2 (1), A K-major or MN-major, B K-major.
+__host__ __device__ constexpr uint32_t idesc_f8_f32(uint32_t M, uint32_t N, bool a_mn_major, uint32_t b_fmt) {
+    return (1u << 4) | (b_fmt << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
-// Two E4M3 bytes (the lower address in the low byte) to two FP16 values
-// (the lower address in the low half).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
-    uint32_t r;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(two));
-    return r;
+// Byte offset of (row, col) in a K-major tile of 128-byte rows, 128B swizzle.
+__device__ __forceinline__ uint32_t sw128_byte(uint32_t row, uint32_t col) {
+    return row * 128u + ((((col >> 4) ^ (row & 7u))) << 4) + (col & 15u);
 }
 
-__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
-    __half2 v = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&v);
-}
-
-template <int NQ>
-struct Fp8Cfg {
-    static constexpr int kStages8 = NQ == 16 ? 4 : 3;          // FP8 tiles in flight per ring
-    static constexpr int kTile8Bytes = kKvTile * D;             // 128 keys x 128 bytes
-    static constexpr int kChunkBytes = kKvTile * 128;           // 64 FP16 columns of a tile
-    static constexpr int kTile16Bytes = 2 * kChunkBytes;
-    static constexpr int kQBytes = NQ * D * 2;
-    static constexpr int kPBytes = NQ * kKvTile * 2;
+template <int NQ, int R>
+struct F8Cfg {
+    static constexpr int kStages = NQ == 16 ? 5 : 4;           // ring stages (K tile + V tile each)
+    static constexpr int kTileBytes = kKvTile * D;              // 128 keys x 128 E4M3 bytes
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kQ16Bytes = NQ * D * 2;                // BF16 query rows, two 64-column chunks
+    static constexpr int kQ8Bytes = kQTerms * NQ * D;           // B of QK^T: row = term * NQ + query row
+    static constexpr int kPBytes = kPTerms * NQ * kKvTile;      // B of PV: row = term * NQ + query row
+    static constexpr int kRH = R / 2;                           // query rows per softmax warp
     // shared memory map (offsets from a 1024-aligned base)
-    static constexpr int kOffK8 = 0;
-    static constexpr int kOffV8 = kOffK8 + kStages8 * kTile8Bytes;
-    static constexpr int kOffV16 = kOffV8 + kStages8 * kTile8Bytes;
-    static constexpr int kOffQ = kOffV16 + 2 * kTile16Bytes;
-    static constexpr int kOffP = kOffQ + 2 * kQBytes;
+    static constexpr int kOffRing = 0;
+    static constexpr int kOffQ16 = kOffRing + kStages * kStageBytes;
+    static constexpr int kOffQ8 = kOffQ16 + 2 * kQ16Bytes;
+    static constexpr int kOffP = kOffQ8 + 2 * kQ8Bytes;
     static constexpr int kOffBar = kOffP + 2 * kPBytes;
-    static constexpr int kNumBars = 4 * kStages8 + 2 * 2 + 2 * 2 + 2 + 2 + 2 + 2 + 2 + 1 + 1;
-    static constexpr int kOffRedMax = kOffBar + kNumBars * 8;
-    static constexpr int kOffRedSum = kOffRedMax + 2 * 4 * NQ * 4;
-    static constexpr int kOffMisc = kOffRedSum + 4 * NQ * 4;
+    static constexpr int kNumBars = 3 * kStages + 4 * 2 + 3 * 2 + 1;
+    static constexpr int kOffRedMax = (kOffBar + kNumBars * 8 + 15) / 16 * 16;
+    static constexpr int kOffRedSum = kOffRedMax + 2 * 4 * R * 4;
+    static constexpr int kOffQExp = kOffRedSum + 4 * R * 4;
+    static constexpr int kOffMisc = kOffQExp + 2 * NQ * 4;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA exceeded");
-    static_assert(kOffRedMax % 16 == 0, "row maxima are read as float4");
-    // TMEM: two FP16 K tiles (64 columns each), two S^T buffers, O^T
-    static constexpr uint32_t kColK = 0;
-    static constexpr uint32_t kColS = 128;
-    static constexpr uint32_t kColO = kColS + 2 * NQ;
-    static constexpr uint32_t kTmemCols = 256;
-    static constexpr uint32_t kIdescQK = idesc_f16_f32(128, NQ, false, false);
-    static constexpr uint32_t kIdescPV = idesc_f16_f32(128, NQ, true, false);
+    static_assert(kRH % 4 == 0, "softmax rows per warp");
+    // TMEM: two S^T buffers (Q terms side by side), then O^T (P terms side by side)
+    static constexpr uint32_t kColS = 0;
+    static constexpr uint32_t kSCols = kQTerms * NQ;
+    static constexpr uint32_t kColO = 2 * kSCols;
+    static constexpr uint32_t kTmemCols = (kColO + kPTerms * NQ) <= 128 ? 128 : 256;
+    static_assert(kColO + kPTerms * NQ <= kTmemCols, "TMEM columns");
+    static constexpr uint32_t kIdescQK = idesc_f8_f32(128, kQTerms * NQ, false, 0);
+    static constexpr uint32_t kIdescPV = idesc_f8_f32(128, kPTerms * NQ, true, 1);
 };
 
-// NQ: query rows on the MMA N axis (16 or 32); R: rows the softmax carries
-// (8 when a unit holds at most 8 query rows, else NQ).
+// NQ: query rows per unit on the MMA N axis (16 or 32); R: rows the softmax
+// carries (8 when a unit holds at most 8 query rows, else NQ).
 template <int NQ, int R>
 __global__ void __launch_bounds__(320, 1)
 paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
-    using C = Fp8Cfg<NQ>;
+    using C = F8Cfg<NQ, R>;
     static_assert(R == 8 || R == NQ, "softmax rows");
+    constexpr int S = C::kStages;
+    constexpr int RH = C::kRH;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sK8 = smem + C::kOffK8;
-    uint8_t *sV8 = smem + C::kOffV8;
-    uint8_t *sV16 = smem + C::kOffV16;
-    uint8_t *sQ = smem + C::kOffQ;
+    uint8_t *ring = smem + C::kOffRing;
+    uint8_t *sQ16 = smem + C::kOffQ16;
+    uint8_t *sQ8 = smem + C::kOffQ8;
     uint8_t *sP = smem + C::kOffP;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
-    uint64_t *k8_full = bars;
-    uint64_t *k8_empty = k8_full + C::kStages8;
-    uint64_t *v8_full = k8_empty + C::kStages8;
-    uint64_t *v8_empty = v8_full + C::kStages8;
-    uint64_t *k16_full = v8_empty + C::kStages8;      // [2]
-    // One commit per MMA group: qk_done[b] (QK of tile j, b = j & 1) frees
-    // the FP16 K buffer b and publishes S buffer b; pv_done[b] (PV of tile j)
-    // frees the FP16 V buffer and the P buffer b.  A commit costs the tensor
-    // pipe about as much as an N = 16 MMA, so each event has one barrier,
-    // waited on by every role that needs it.
-    uint64_t *qk_done = k16_full + 2;                  // [2]
-    uint64_t *v16_full = qk_done + 2;                  // [2]
-    uint64_t *pv_done = v16_full + 2;                  // [2]
-    uint64_t *q_full = pv_done + 2;                    // [2] BF16 Q landed
-    uint64_t *q16 = q_full + 2;                        // [2] Q converted to FP16
-    uint64_t *q_empty = q16 + 2;                       // [2]
-    uint64_t *s_free = q_empty + 2;                    // [2]
-    uint64_t *p_full = s_free + 2;                     // [2]
-    uint64_t *drain = p_full + 2;                      // [1]
-    float *red_max = reinterpret_cast<float *>(smem + C::kOffRedMax);   // [2][4][NQ]
-    float *red_sum = reinterpret_cast<float *>(smem + C::kOffRedSum);   // [4][NQ]
+    uint64_t *k_full = bars;                   // [S] K tile landed
+    uint64_t *v_full = k_full + S;             // [S] V tile landed
+    uint64_t *kv_empty = v_full + S;           // [S] PV of the stage's tile done: stage, P buffer, O^T
+    uint64_t *q16_full = kv_empty + S;         // [2] BF16 Q landed
+    uint64_t *q16_free = q16_full + 2;         // [2] BF16 Q read (softmax warps)
+    uint64_t *q8_full = q16_free + 2;          // [2] Q terms written (softmax warps)
+    uint64_t *q8_free = q8_full + 2;           // [2] the unit's last QK^T done
+    uint64_t *qk_done = q8_free + 2;           // [2] S buffer of tile j & 1 ready
+    uint64_t *s_free = qk_done + 2;            // [2] S buffer read (softmax warps)
+    uint64_t *p_full = s_free + 2;             // [2] P terms written (softmax warps)
+    uint64_t *drain = p_full + 2;              // [1]
+    float *red_max = reinterpret_cast<float *>(smem + C::kOffRedMax);   // [2][4][R]
+    float *red_sum = reinterpret_cast<float *>(smem + C::kOffRedSum);   // [4][R]
+    int *q_exp = reinterpret_cast<int *>(smem + C::kOffQExp);           // [2][NQ]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
 
@@ -137,16 +141,13 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < C::kStages8; ++i) {
-            mbar_init(&k8_full[i], 1); mbar_init(&k8_empty[i], 4);
-            mbar_init(&v8_full[i], 1); mbar_init(&v8_empty[i], 4);
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&k_full[i], 1); mbar_init(&v_full[i], 1); mbar_init(&kv_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&k16_full[i], 4); mbar_init(&qk_done[i], 1);
-            mbar_init(&v16_full[i], 4); mbar_init(&pv_done[i], 1);
-            mbar_init(&q_full[i], 1); mbar_init(&q16[i], 4); mbar_init(&q_empty[i], 1);
-            mbar_init(&s_free[i], 4);
-            mbar_init(&p_full[i], 4);
+            mbar_init(&q16_full[i], 1); mbar_init(&q16_free[i], 8);
+            mbar_init(&q8_full[i], 8); mbar_init(&q8_free[i], 1);
+            mbar_init(&qk_done[i], 1); mbar_init(&s_free[i], 8); mbar_init(&p_full[i], 8);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -156,9 +157,9 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
         tma_prefetch_desc(&tm_q); tma_prefetch_desc(&tm_k); tma_prefetch_desc(&tm_v);
     }
     if (warp == 1) { tmem_alloc(tmem_slot, C::kTmemCols); tmem_relinquish(); }
-    // Zero the Q and P slots once: padding rows then contribute exact zeros.
-    for (int i = threadIdx.x; i < (2 * C::kQBytes + 2 * C::kPBytes) / 16; i += blockDim.x)
-        reinterpret_cast<uint4 *>(sQ)[i] = make_uint4(0, 0, 0, 0);
+    // Zero the query and probability buffers once: padding rows stay exact zeros.
+    for (int i = threadIdx.x; i < (C::kOffBar - C::kOffQ16) / 16; i += blockDim.x)
+        reinterpret_cast<uint4 *>(sQ16)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -177,16 +178,16 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
         Unit x;
         while (it.next(p, x)) {
             const int qs = ju & 1;
-            if (!warp_wait(&q_empty[qs], ((ju >> 1) & 1) ^ 1, wc, lane)) goto producer_done;
+            if (!warp_wait(&q16_free[qs], ((ju >> 1) & 1) ^ 1, wc, lane)) goto producer_done;
             if (lane == 0) {
                 int h0, t0;
                 if (p.head_mode == 0) { h0 = x.g * p.G; t0 = x.rg * p.tokens_per_unit; }
                 else { t0 = x.rg / p.head_chunks; h0 = x.g * p.G + (x.rg % p.head_chunks) * p.rows; }
-                mbar_arrive_expect_tx(&q_full[qs], 2u * q_rows * 128u);
+                mbar_arrive_expect_tx(&q16_full[qs], 2u * q_rows * 128u);
 #pragma unroll
                 for (int c = 0; c < 2; ++c)
-                    tma_load_4d(smem_u32(sQ + qs * C::kQBytes + c * NQ * 128), &tm_q, &q_full[qs], c * 64, h0, t0,
-                                x.b);
+                    tma_load_4d(smem_u32(sQ16 + qs * C::kQ16Bytes + c * NQ * 128), &tm_q, &q16_full[qs], c * 64, h0,
+                                t0, x.b);
             }
             __syncwarp();
             {
@@ -202,20 +203,19 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                         if ((unsigned)phys >= (unsigned)p.num_pages) { record_error(p.status, 1); phys = 0; }
                     }
                     const uint32_t bytes = (uint32_t)(npages * box_rows * 128);
-                    const int s8 = jt % C::kStages8;
-                    const uint32_t par = ((jt / C::kStages8) & 1) ^ 1;
-                    if (!warp_wait(&k8_empty[s8], par, wc, lane)) goto producer_done;
-                    if (lane == 0) mbar_arrive_expect_tx(&k8_full[s8], bytes);
+                    const int s = jt % S;
+                    if (!warp_wait(&kv_empty[s], ((jt / S) & 1) ^ 1, wc, lane)) goto producer_done;
+                    uint8_t *stage = ring + s * C::kStageBytes;
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&k_full[s], bytes);
+                        mbar_arrive_expect_tx(&v_full[s], bytes);
+                    }
                     __syncwarp();
-                    if (lane < npages)
-                        tma_load_4d(smem_u32(sK8 + s8 * C::kTile8Bytes + lane * box_rows * 128), &tm_k, &k8_full[s8],
-                                    0, x.g, slot0, phys);
-                    if (!warp_wait(&v8_empty[s8], par, wc, lane)) goto producer_done;
-                    if (lane == 0) mbar_arrive_expect_tx(&v8_full[s8], bytes);
-                    __syncwarp();
-                    if (lane < npages)
-                        tma_load_4d(smem_u32(sV8 + s8 * C::kTile8Bytes + lane * box_rows * 128), &tm_v, &v8_full[s8],
-                                    0, x.g, slot0, phys);
+                    if (lane < npages) {
+                        tma_load_4d(smem_u32(stage + lane * box_rows * 128), &tm_k, &k_full[s], 0, x.g, slot0, phys);
+                        tma_load_4d(smem_u32(stage + C::kTileBytes + lane * box_rows * 128), &tm_v, &v_full[s], 0,
+                                    x.g, slot0, phys);
+                    }
                     issued = jt + 1;
                 }
             }
@@ -223,130 +223,34 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
         }
     producer_done:
         if (lane == 0) {
-            for (int k = 0; k < C::kStages8 && k < issued; ++k) {
+            for (int k = 0; k < S && k < issued; ++k) {
                 const int j = issued - 1 - k;
-                mbar_wait_drain(&k8_full[j % C::kStages8], (j / C::kStages8) & 1, wc);
-                mbar_wait_drain(&v8_full[j % C::kStages8], (j / C::kStages8) & 1, wc);
+                mbar_wait_drain(&k_full[j % S], (j / S) & 1, wc);
+                mbar_wait_drain(&v_full[j % S], (j / S) & 1, wc);
             }
         }
         __syncwarp();
-    } else if (warp >= 6) {
-        // ------------------------------------------------------------ convert
-        // Thread = key of the tile (its TMEM lane for K); keys at or past the
-        // piece's end become zeros.  Waits that fail do not change the control
-        // flow (each warp arrives on its own), so aborts wind down.
-        const int q4 = warp & 3;
-        const int key = q4 * 32 + lane;
-        const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-        const int tq = threadIdx.x - 192;                 // 0..127
-        int jt = 0, ju = 0;
-        PieceIter it;
-        it.init(p);
-        Unit x;
-        while (it.next(p, x)) {
-            // Q of this unit: BF16 -> FP16 in place (each element keeps its
-            // position, so the swizzled layout needs no remapping).
-            const int qs = ju & 1;
-            mbar_wait(&q_full[qs], (ju >> 1) & 1, wc);
-            {
-                uint32_t *qw = reinterpret_cast<uint32_t *>(sQ + qs * C::kQBytes);
-                for (int i = tq; i < C::kQBytes / 4; i += 128) {
-                    const uint32_t w = qw[i];
-                    const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
-                    qw[i] = pack_half2(lo, hi);
-                }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&q16[qs]);
-            for (int i = 0; i < x.ntiles; ++i, ++jt) {
-                const int valid = x.k_end - (x.k_begin + i * kKvTile);   // keys of the tile inside the piece
-                const bool live = key < valid;
-                const int s8 = jt % C::kStages8;
-                const uint32_t par8 = (jt / C::kStages8) & 1;
-                const int b16 = jt & 1;
-                const uint32_t par16 = ((jt >> 1) & 1) ^ 1;
-                // K row -> TMEM lane `key`, 64 columns of FP16 pairs.
-                mbar_wait(&k8_full[s8], par8, wc);
-                mbar_wait(&qk_done[b16], par16, wc);      // QK(jt - 2) read this buffer
-                tc_fence_after();
-                const uint8_t *krow = sK8 + s8 * C::kTile8Bytes + key * 128;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint4 r[2];
-#pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        r[k] = *reinterpret_cast<const uint4 *>(krow + (((2 * c + k) ^ (key & 7)) << 4));
-                        if (!live) r[k] = make_uint4(0, 0, 0, 0);
-                    }
-                    uint32_t w16[16];
-#pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        const uint32_t wd[4] = {r[k].x, r[k].y, r[k].z, r[k].w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            w16[8 * k + 2 * e] = e4m3x2_to_f16x2((uint16_t)(wd[e] & 0xffffu));
-                            w16[8 * k + 2 * e + 1] = e4m3x2_to_f16x2((uint16_t)(wd[e] >> 16));
-                        }
-                    }
-                    tmem_st16u(tmem + lane_off + C::kColK + b16 * 64 + c * 16, w16);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&k8_empty[s8]);
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&k16_full[b16]);
-                // V row -> swizzled FP16 tile (two 64-column chunks)
-                mbar_wait(&v8_full[s8], par8, wc);
-                mbar_wait(&pv_done[b16], par16, wc);      // PV(jt - 2) read this buffer
-                const uint8_t *vrow = sV8 + s8 * C::kTile8Bytes + key * 128;
-                uint8_t *v16 = sV16 + b16 * C::kTile16Bytes;
-#pragma unroll 4
-                for (int u = 0; u < 8; ++u) {              // FP8 unit u = columns 16u .. 16u + 15
-                    uint4 r = *reinterpret_cast<const uint4 *>(vrow + ((u ^ (key & 7)) << 4));
-                    if (!live) r = make_uint4(0, 0, 0, 0);
-                    const uint32_t wd[4] = {r.x, r.y, r.z, r.w};
-                    uint32_t h[8];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        h[2 * e] = e4m3x2_to_f16x2((uint16_t)(wd[e] & 0xffffu));
-                        h[2 * e + 1] = e4m3x2_to_f16x2((uint16_t)(wd[e] >> 16));
-                    }
-                    const int chunk = u >> 2;                // 64 columns per chunk
-                    const int unit = (u & 3) * 2;            // 8 FP16 columns per 16-byte unit
-                    uint8_t *rowp = v16 + chunk * C::kChunkBytes + key * 128;
-                    *reinterpret_cast<uint4 *>(rowp + ((unit ^ (key & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-                    *reinterpret_cast<uint4 *>(rowp + (((unit + 1) ^ (key & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&v8_empty[s8]);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&v16_full[b16]);
-            }
-            ++ju;
-        }
     } else if (warp == 1) {
         // ----------------------------------------------------------------- MMA
         if (lane == 0) {
             int jt = 0, ju = 0, pend = -1;
             bool pend_first = false;
             auto issue_pv = [&](int jj, bool first) -> bool {
-                const int b16 = jj & 1;
+                const int s = jj % S;
                 const int pb = jj & 1;
-                if (!mbar_wait(&v16_full[b16], (jj >> 1) & 1, wc)) return false;
+                if (!mbar_wait(&v_full[s], (jj / S) & 1, wc)) return false;
                 if (!mbar_wait(&p_full[pb], (jj >> 1) & 1, wc)) return false;
                 tc_fence_after();
-                const uint32_t v_base = smem_u32(sV16 + b16 * C::kTile16Bytes);
+                const uint32_t v_base = smem_u32(ring + s * C::kStageBytes + C::kTileBytes);
                 const uint32_t p_base = smem_u32(sP + pb * C::kPBytes);
 #pragma unroll
-                for (int kk = 0; kk < kKvTile / 16; ++kk) {
-                    const uint64_t a = sdesc_sw128(v_base + kk * 16 * 128, C::kChunkBytes, 1024);
-                    const uint64_t b = sdesc_sw128(p_base + (kk >> 2) * NQ * 128 + (kk & 3) * 32, 16, 1024);
-                    mma_bf16_ss(tmem + C::kColO, a, b, C::kIdescPV, (first && kk == 0) ? 0u : 1u);
+                for (int kk = 0; kk < kKvTile / 32; ++kk) {
+                    // A = V^T, MN-major: 32 key rows of 128 bytes per step.
+                    const uint64_t a = sdesc_sw128(v_base + kk * 32 * 128, 16, 1024);
+                    const uint64_t b = sdesc_sw128(p_base + kk * 32, 16, 1024);
+                    mma_f8_ss(tmem + C::kColO, a, b, C::kIdescPV, (first && kk == 0) ? 0u : 1u);
                 }
-                mma_commit(&pv_done[b16]);
+                mma_commit(&kv_empty[s]);
                 return true;
             };
             PieceIter it;
@@ -354,22 +258,30 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
             Unit x;
             while (it.next(p, x)) {
                 const int qs = ju & 1;
-                if (!mbar_wait(&q16[qs], (ju >> 1) & 1, wc)) goto mma_done;
+                // The previous unit's last PV goes out before this unit's Q
+                // terms are awaited: the softmax warps build them only after
+                // their epilogue, which waits for that PV.
+                if (pend >= 0) {
+                    if (!issue_pv(pend, pend_first)) goto mma_done;
+                    pend = -1;
+                }
+                if (!mbar_wait(&q8_full[qs], (ju >> 1) & 1, wc)) goto mma_done;
                 for (int i = 0; i < x.ntiles; ++i, ++jt) {
-                    const int b16 = jt & 1;
+                    const int s = jt % S;
                     const int sb = jt & 1;
-                    if (!mbar_wait(&k16_full[b16], (jt >> 1) & 1, wc)) goto mma_done;
+                    if (!mbar_wait(&k_full[s], (jt / S) & 1, wc)) goto mma_done;
                     if (!mbar_wait(&s_free[sb], ((jt >> 1) & 1) ^ 1, wc)) goto mma_done;
                     tc_fence_after();
-                    const uint32_t q_base = smem_u32(sQ + qs * C::kQBytes);
+                    const uint32_t k_base = smem_u32(ring + s * C::kStageBytes);
+                    const uint32_t q_base = smem_u32(sQ8 + qs * C::kQ8Bytes);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t b = sdesc_sw128(q_base + (kk >> 2) * NQ * 128 + (kk & 3) * 32, 16, 1024);
-                        mma_bf16_ts(tmem + C::kColS + sb * NQ, tmem + C::kColK + b16 * 64 + kk * 8, b, C::kIdescQK,
-                                    kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 32; ++kk) {
+                        const uint64_t a = sdesc_sw128(k_base + kk * 32, 16, 1024);
+                        const uint64_t b = sdesc_sw128(q_base + kk * 32, 16, 1024);
+                        mma_f8_ss(tmem + C::kColS + sb * C::kSCols, a, b, C::kIdescQK, kk > 0 ? 1u : 0u);
                     }
-                    mma_commit(&qk_done[b16]);
-                    if (i == x.ntiles - 1) mma_commit(&q_empty[qs]);
+                    mma_commit(&qk_done[sb]);
+                    if (i == x.ntiles - 1) mma_commit(&q8_free[qs]);
                     if (pend >= 0 && !issue_pv(pend, pend_first)) goto mma_done;
                     pend = jt;
                     pend_first = (i == 0);
@@ -382,99 +294,192 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
             mbar_wait_drain(drain, 0, wc);
         }
         __syncwarp();
-    } else if (warp >= 2) {
+    } else {
         // ------------------------------------------------- softmax / epilogue
-        // As in the BF16 decode kernel: thread = key of the tile, all NQ rows
-        // of its S^T column in registers, conditional rescale; P as FP16.
+        // Thread = key of the tile (TMEM lane) and, in the epilogue, value
+        // column; warp pair (w, w + 4) shares a lane quadrant and splits the
+        // rows.  Waits that fail do not change the control flow; the bounded
+        // iterations wind down under the recorded status.
         const int q4 = warp & 3;
-        const int row_in_tile = q4 * 32 + lane;
+        const int half = (warp - 2) >> 2;
+        const int r0 = half * RH;
+        const int key = q4 * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-        int jt = 0;
+        const int st = threadIdx.x - 64;                       // 0..255
+        int jt = 0, ju = 0;
         PieceIter it;
         it.init(p);
         Unit x;
         while (it.next(p, x)) {
-            int lim[R];
+            const int qs = ju & 1;
+            // ---- query terms: BF16 row * 2^e = hi + mid, both E4M3
+            mbar_wait(&q16_full[qs], (ju >> 1) & 1, wc);
+            mbar_wait(&q8_free[qs], ((ju >> 1) & 1) ^ 1, wc);
+            {
+                constexpr int TPR = kSoftmaxThreads / NQ;          // threads per query row
+                constexpr int EPT = D / TPR;                       // elements per thread (8 or 16)
+                const int rq = st / TPR;
+                const int c0 = (st % TPR) * EPT;
+                float y[EPT];
+                const uint8_t *q16 = sQ16 + qs * C::kQ16Bytes + (c0 >> 6) * NQ * 128 + rq * 128;
+#pragma unroll
+                for (int u = 0; u < EPT / 8; ++u) {
+                    const int unit = ((c0 & 63) >> 3) + u;
+                    const uint4 w = *reinterpret_cast<const uint4 *>(q16 + ((unit ^ (rq & 7)) << 4));
+                    const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        y[8 * u + 2 * e] = __uint_as_float(wd[e] << 16);
+                        y[8 * u + 2 * e + 1] = __uint_as_float(wd[e] & 0xffff0000u);
+                    }
+                }
+                float amax = 0.f;
+#pragma unroll
+                for (int e = 0; e < EPT; ++e) amax = fmaxf(amax, fabsf(y[e]));
+#pragma unroll
+                for (int o = TPR / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+                int ex = 0;
+                if (amax > 0.f && amax <= 3.0e38f) ex = min(100, max(-100, 7 - ilogbf(amax)));
+                const float mul = __int_as_float((ex + 127) << 23);     // 2^ex, exact
+                uint8_t hi[EPT], mid[EPT];
+#pragma unroll
+                for (int e = 0; e < EPT; e += 2) {
+                    const float a = y[e] * mul, b = y[e + 1] * mul;
+                    const __nv_fp8x2_storage_t h2 = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+                    const float2 hb = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(h2, __NV_E4M3)));
+                    const __nv_fp8x2_storage_t m2 =
+                        __nv_cvt_float2_to_fp8x2(make_float2(a - hb.x, b - hb.y), __NV_SATFINITE, __NV_E4M3);
+                    hi[e] = (uint8_t)(h2 & 0xff); hi[e + 1] = (uint8_t)(h2 >> 8);
+                    mid[e] = (uint8_t)(m2 & 0xff); mid[e + 1] = (uint8_t)(m2 >> 8);
+                }
+                uint8_t *q8 = sQ8 + qs * C::kQ8Bytes;
+#pragma unroll
+                for (int t = 0; t < kQTerms; ++t) {
+                    const uint8_t *src = t == 0 ? hi : mid;
+                    const uint32_t row = (uint32_t)(t * NQ + rq);
+#pragma unroll
+                    for (int e = 0; e < EPT; e += 8) {
+                        uint2 v;
+                        v.x = src[e] | (src[e + 1] << 8) | (src[e + 2] << 16) | ((uint32_t)src[e + 3] << 24);
+                        v.y = src[e + 4] | (src[e + 5] << 8) | (src[e + 6] << 16) | ((uint32_t)src[e + 7] << 24);
+                        *reinterpret_cast<uint2 *>(q8 + sw128_byte(row, (uint32_t)(c0 + e))) = v;
+                    }
+                }
+                if (st % TPR == 0) q_exp[qs * NQ + rq] = ex;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) { mbar_arrive(&q16_free[qs]); mbar_arrive(&q8_full[qs]); }
+            named_bar_sync(3, kSoftmaxThreads);                   // q_exp of this unit visible
+            int lim[RH];
+            float rs[RH];
             int nrows = 0;
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
+            for (int r = 0; r < RH; ++r) {
                 int t, h;
-                const bool ok = unit_row(p, x, r, t, h);
+                const bool ok = unit_row(p, x, r0 + r, t, h);
                 lim[r] = ok ? min(x.n, x.n - p.q_len + t + 1) : 0;
                 if (ok) nrows = r + 1;
+                rs[r] = p.scale_log2 * __int_as_float((127 - q_exp[qs * NQ + r0 + r]) << 23);
             }
-            float m_ref[R], l_part[R];
+            float m_ref[RH], l_part[RH];
 #pragma unroll
-            for (int r = 0; r < R; ++r) { m_ref[r] = kNegInf; l_part[r] = 0.f; }
+            for (int r = 0; r < RH; ++r) { m_ref[r] = kNegInf; l_part[r] = 0.f; }
             for (int i = 0; i < x.ntiles; ++i, ++jt) {
                 const int ts = x.k_begin + i * kKvTile;
-                const int tok = ts + row_in_tile;
+                const int tok = ts + key;
                 const int sb = jt & 1;
                 mbar_wait(&qk_done[sb], (jt >> 1) & 1, wc);
                 tc_fence_after();
-                float s[R];
-                tmem_ld_cols<R>(tmem + lane_off + C::kColS + sb * NQ, s);
+                float s[RH], sm[RH];
+                tmem_ld_cols<RH>(tmem + lane_off + C::kColS + sb * C::kSCols + r0, s);
+                tmem_ld_cols<RH>(tmem + lane_off + C::kColS + sb * C::kSCols + NQ + r0, sm);
                 tmem_wait_ld();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s_free[sb]);
                 float *rm = red_max + (jt & 1) * 4 * R;
 #pragma unroll
-                for (int r = 0; r < R; ++r) s[r] = (tok < lim[r]) ? s[r] * p.scale_log2 : kNegInf;
-                warp_rows_reduce<R, true>(s, lane, rm + q4 * R);
-                named_bar_sync(1, 128);
+                for (int r = 0; r < RH; ++r) s[r] = (tok < lim[r]) ? (s[r] + sm[r]) * rs[r] : kNegInf;
+                warp_rows_reduce<RH, true>(s, lane, rm + q4 * R + r0);
+                named_bar_sync(1 + half, 128);
                 bool need = false;
-                float mx[R];
+                float mx[RH];
 #pragma unroll
-                for (int r = 0; r < R; r += 4) {
+                for (int r = 0; r < RH; r += 4) {
                     // Padding rows hold -inf everywhere: mx = -inf, no rescale.
-                    float4 m4 = *reinterpret_cast<const float4 *>(rm + r);
+                    float4 m4 = *reinterpret_cast<const float4 *>(rm + r0 + r);
 #pragma unroll
                     for (int q = 1; q < 4; ++q) {
-                        const float4 o4 = *reinterpret_cast<const float4 *>(rm + q * R + r);
+                        const float4 o4 = *reinterpret_cast<const float4 *>(rm + q * R + r0 + r);
                         m4.x = fmaxf(m4.x, o4.x); m4.y = fmaxf(m4.y, o4.y);
                         m4.z = fmaxf(m4.z, o4.z); m4.w = fmaxf(m4.w, o4.w);
                     }
                     mx[r] = m4.x; mx[r + 1] = m4.y; mx[r + 2] = m4.z; mx[r + 3] = m4.w;
                 }
 #pragma unroll
-                for (int r = 0; r < R; ++r) need |= mx[r] > m_ref[r] + kRescaleThreshold;
+                for (int r = 0; r < RH; ++r) need |= mx[r] > m_ref[r] + kRescaleThreshold;
                 if (need) {
-                    float alpha[R];
+                    float alpha[RH];
 #pragma unroll
-                    for (int r = 0; r < R; ++r) {
+                    for (int r = 0; r < RH; ++r) {
                         const float mn = fmaxf(m_ref[r], mx[r]);
                         alpha[r] = (mn == kNegInf) ? 1.f : ex2_approx(m_ref[r] - mn);
                         l_part[r] *= alpha[r];
                         m_ref[r] = mn;
                     }
                     if (i > 0) {
-                        // Rescale once PV(jt - 1) has landed (the P-buffer wait
-                        // of tile jt + 1); PV(jt - 2) has, as qk_done(jt) was
-                        // committed after it was issued.
-                        mbar_wait(&pv_done[(jt + 1) & 1], (((jt + 1) >> 1) & 1) ^ 1, wc);
+                        // Rescale once PV(jt - 1) has landed; PV(jt - 2) has,
+                        // as qk_done(jt) was committed after it was issued.
+                        mbar_wait(&kv_empty[(jt - 1) % S], ((jt - 1) / S) & 1, wc);
                         tc_fence_after();
-                        float o[R];
-                        const uint32_t ta = tmem + lane_off + C::kColO;
-                        tmem_ld_cols<R>(ta, o);
-                        tmem_wait_ld();
 #pragma unroll
-                        for (int k = 0; k < R; ++k) o[k] *= alpha[k];
-                        tmem_st_cols<R>(ta, o);
+                        for (int t = 0; t < kPTerms; ++t) {
+                            float o[RH];
+                            const uint32_t ta = tmem + lane_off + C::kColO + t * NQ + r0;
+                            tmem_ld_cols<RH>(ta, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int k = 0; k < RH; ++k) o[k] *= alpha[k];
+                            tmem_st_cols<RH>(ta, o);
+                        }
                         tmem_wait_st();
                     }
                 }
+                if (half == 0 && ts + kKvTile > x.n) {
+                    // Keys past the row's end: their V rows may hold anything
+                    // (unloaded pages, poisoned slots).  Zero them so that the
+                    // exact-zero probabilities cannot meet a NaN in the MMA.
+                    const int s = jt % S;
+                    mbar_wait(&v_full[s], (jt / S) & 1, wc);
+                    if (tok >= x.n) {
+                        uint4 *row = reinterpret_cast<uint4 *>(ring + s * C::kStageBytes + C::kTileBytes + key * 128);
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) row[k] = make_uint4(0, 0, 0, 0);
+                    }
+                }
                 const int pb = jt & 1;
-                mbar_wait(&pv_done[pb], ((jt >> 1) & 1) ^ 1, wc);     // PV(jt - 2) read P buffer pb
+                if (jt >= 2) mbar_wait(&kv_empty[(jt - 2) % S], ((jt - 2) / S) & 1, wc);   // PV(jt - 2) read P buffer pb
                 uint8_t *pbuf = sP + pb * C::kPBytes;
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
+                for (int r = 0; r < RH; r += 2) {
                     // Masked keys and padding rows have s = -inf: p = 0 exactly.
-                    // Rows R..NQ-1 of P stay at the zeros written at start.
-                    const float mu = (m_ref[r] == kNegInf) ? 0.f : m_ref[r] - kHeadroom;
-                    const float pr = ex2_approx(s[r] - mu);
-                    l_part[r] += pr;
-                    *reinterpret_cast<__half *>(pbuf + sw128_offset(r, row_in_tile, NQ)) = __float2half_rn(pr);
+                    const float mu0 = (m_ref[r] == kNegInf) ? 0.f : m_ref[r] - kHeadroom;
+                    const float mu1 = (m_ref[r + 1] == kNegInf) ? 0.f : m_ref[r + 1] - kHeadroom;
+                    const float p0 = ex2_approx(s[r] - mu0);
+                    const float p1 = ex2_approx(s[r + 1] - mu1);
+                    l_part[r] += p0;
+                    l_part[r + 1] += p1;
+                    // FP16 value -> four E5M2 terms: round, subtract exactly, repeat.
+                    __half2 h = __floats2half2_rn(p0, p1);
+#pragma unroll
+                    for (int t = 0; t < kPTerms; ++t) {
+                        const __nv_fp8x2_storage_t e2 =
+                            __nv_cvt_halfraw2_to_fp8x2(__half2_raw(h), __NV_SATFINITE, __NV_E5M2);
+                        pbuf[sw128_byte((uint32_t)(t * NQ + r0 + r), (uint32_t)key)] = (uint8_t)(e2 & 0xff);
+                        pbuf[sw128_byte((uint32_t)(t * NQ + r0 + r + 1), (uint32_t)key)] = (uint8_t)(e2 >> 8);
+                        if (t + 1 < kPTerms) h = __hsub2(h, __half2(__nv_cvt_fp8x2_to_halfraw2(e2, __NV_E5M2)));
+                    }
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -483,27 +488,34 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
             }
             // ------------------------------------------------------ epilogue
             {
-                warp_rows_reduce<R, false>(l_part, lane, red_sum + q4 * R);
-                named_bar_sync(1, 128);
-                float L[R];
+                warp_rows_reduce<RH, false>(l_part, lane, red_sum + q4 * R + r0);
+                named_bar_sync(1 + half, 128);
+                float L[RH];
 #pragma unroll
-                for (int r = 0; r < R; ++r)
-                    L[r] = (red_sum[r] + red_sum[R + r]) + (red_sum[2 * R + r] + red_sum[3 * R + r]);
+                for (int r = 0; r < RH; ++r)
+                    L[r] = (red_sum[r0 + r] + red_sum[R + r0 + r]) + (red_sum[2 * R + r0 + r] + red_sum[3 * R + r0 + r]);
                 // O^T is final once PV(jt - 2) and PV(jt - 1), the unit's
-                // last, have landed: the P-buffer waits of tiles jt and jt + 1.
-                // Each buffer's barrier is at most one phase behind its waiter,
-                // so the parity waits are unambiguous.
-                mbar_wait(&pv_done[jt & 1], ((jt >> 1) & 1) ^ 1, wc);
-                mbar_wait(&pv_done[(jt + 1) & 1], (((jt + 1) >> 1) & 1) ^ 1, wc);
+                // last, have landed.  The softmax waits each stage's phases in
+                // order, so neither wait can be two phases behind.
+                if (jt >= 2) mbar_wait(&kv_empty[(jt - 2) % S], ((jt - 2) / S) & 1, wc);
+                mbar_wait(&kv_empty[(jt - 1) % S], ((jt - 1) / S) & 1, wc);
                 tc_fence_after();
-                float o[R];
-                tmem_ld_cols<R>(tmem + lane_off + C::kColO, o);
-                tmem_wait_ld();
-                const int dv = row_in_tile;
+                float o[RH];
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
+                for (int r = 0; r < RH; ++r) o[r] = 0.f;
+#pragma unroll
+                for (int t = 0; t < kPTerms; ++t) {
+                    float ot[RH];
+                    tmem_ld_cols<RH>(tmem + lane_off + C::kColO + t * NQ + r0, ot);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int r = 0; r < RH; ++r) o[r] += ot[r];
+                }
+                const int dv = key;
+#pragma unroll
+                for (int r = 0; r < RH; ++r) {
                     int t, h;
-                    if (r >= nrows || !unit_row(p, x, r, t, h)) continue;
+                    if (r >= nrows || !unit_row(p, x, r0 + r, t, h)) continue;
                     const float val = L[r] > 0.f ? o[r] / L[r] * p.out_scale : 0.f;
                     if (x.single) {
                         __nv_bfloat16 *op = reinterpret_cast<__nv_bfloat16 *>(p.out) + x.b * p.out_stride[0] +
@@ -514,13 +526,13 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                         p.ws_o[(row * p.max_pieces + x.k) * D + dv] = val;
                     }
                 }
-                if (row_in_tile < nrows) {
-                    const int r = row_in_tile;
+                if (q4 == 0 && lane < nrows) {
+                    const int r = lane;
                     int t, h;
-                    if (unit_row(p, x, r, t, h)) {
+                    if (unit_row(p, x, r0 + r, t, h)) {
                         float lse2 = kNegInf;
 #pragma unroll
-                        for (int k = 0; k < R; ++k)
+                        for (int k = 0; k < RH; ++k)
                             if (k == r && L[k] > 0.f) lse2 = m_ref[k] - kHeadroom + __log2f(L[k]);
                         if (x.single) {
                             if (p.lse)
@@ -533,8 +545,9 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                     }
                 }
                 tc_fence_before();
-                named_bar_sync(1, 128);
+                named_bar_sync(1 + half, 128);
             }
+            ++ju;
         }
     }
 
@@ -547,11 +560,11 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
 template <int NQ, int R>
 cudaError_t launch_fp8_t(const DecodeParams &p, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                          cudaStream_t stream) {
-    using C = Fp8Cfg<NQ>;
+    using C = F8Cfg<NQ, R>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(paged_decode_fp8_kernel<NQ, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(paged_decode_fp8_kernel<NQ, R>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured = true;
     }
