@@ -110,15 +110,16 @@ fw_status_t get_encoder() {
 }
 
 // Tensor map with 128-byte swizzle; dims/strides innermost first, strides
-// in bytes for dims 1..rank-1.
+// in bytes for dims 1..rank-1.  L2 fetches are promoted to 256 bytes unless
+// the caller knows the other half of each 256-byte block is someone else's.
 fw_status_t encode_map(CUtensorMap *tm, CUtensorMapDataType type, const void *base, int rank, const uint64_t *dims,
-                       const uint64_t *strides_bytes, const uint32_t *box, const char *what) {
+                       const uint64_t *strides_bytes, const uint32_t *box, const char *what,
+                       CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B) {
     if (fw_status_t s = get_encoder()) return s;
     uint32_t elem[5] = {1, 1, 1, 1, 1};
     CUresult r = g_encode(tm, type, (cuuint32_t)rank, const_cast<void *>(base),
                           dims, strides_bytes, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          CU_TENSOR_MAP_SWIZZLE_128B, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(FW_ERR_INVALID_ARG, "tensor map for %s rejected (CUresult %d)", what, (int)r);
     return FW_OK;
 }
@@ -528,11 +529,22 @@ static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_
         const uint64_t sk[3] = {(uint64_t)k_cache->stride[2] * esz, (uint64_t)k_cache->stride[1] * esz,
                                 (uint64_t)k_cache->stride[0] * esz};
         const uint32_t box[4] = {kv8 ? 128u : 64u, 1, rows_box, 1};
-        if (fw_status_t s = encode_map(&tk, type, k_cache->data, 4, dk, sk, box, "k_cache")) return s;
+        // A 128-byte FP8 row is followed in memory by another head's row
+        // unless the slots are 128 bytes apart (one KV head): promoting its
+        // fetch to 256 bytes would then pull that row through DRAM for another
+        // CTA that mostly comes too late (measured: 1.4x the algorithmic bytes
+        // with 8 KV heads).  BF16 rows of 256 bytes or more use both halves.
+        auto promo_for = [&](const fw_tensor_t *c) {
+            const bool narrow_row = kv8 && (uint64_t)Dk * esz == 128 && (uint64_t)c->stride[1] * esz != 128;
+            return narrow_row ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
+        };
+        if (fw_status_t s = encode_map(&tk, type, k_cache->data, 4, dk, sk, box, "k_cache", promo_for(k_cache)))
+            return s;
         const uint64_t dv[4] = {(uint64_t)Dv, (uint64_t)Hkv, (uint64_t)ps, (uint64_t)P};
         const uint64_t sv[3] = {(uint64_t)v_cache->stride[2] * esz, (uint64_t)v_cache->stride[1] * esz,
                                 (uint64_t)v_cache->stride[0] * esz};
-        if (fw_status_t s = encode_map(&tv, type, v_cache->data, 4, dv, sv, box, "v_cache")) return s;
+        if (fw_status_t s = encode_map(&tv, type, v_cache->data, 4, dv, sv, box, "v_cache", promo_for(v_cache)))
+            return s;
     }
     cudaEvent_t ev0 = nullptr, ev1 = nullptr;
     if (g_opt_timing) { ev0 = pooled_event(); ev1 = pooled_event(); }
