@@ -222,7 +222,7 @@ def bench_decode(fw, torch, steps, warmup, device, peaks, batch=None, do_e2e=Tru
         raise RuntimeError(f"device status {status} during the decode benchmark")
     per_launch_ms = kernel_ms / max(1, kernel_n)
     achieved = alg_bytes / (per_launch_ms * 1e-3) / 1e9
-    traffic = ncu_traffic("paged_decode_qwen3_14b_ncu.json", ["decode_kernel.cu", "decode_common.cuh", "fw_ptx.cuh"],
+    traffic = ncu_traffic("paged_decode_qwen3_14b_ncu.json", ["decode_kernel.cu", "decode_common.cuh", "fw_ptx.cuh", "abi.cu"],
                           tokens)
     roof = {"kernel": "paged_decode_kernel<128,16>", "bound": "hbm", "achieved": round(achieved, 1),
             "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
@@ -331,7 +331,7 @@ def bench_prefill(fw, torch, steps, warmup, device, peaks, name=None):
     per = kms / max(1, kn)
     ach = flops / (per * 1e-3) / 1e12
     profile = {PREFILL_WL: "varlen_prefill_gqa_ncu.json", PREFILL_HD256_WL: "varlen_prefill_hd256_ncu.json"}[name]
-    traffic = ncu_traffic(profile, ["prefill_kernel.cu", "fw_ptx.cuh"], flops)
+    traffic = ncu_traffic(profile, ["prefill_kernel.cu", "fw_ptx.cuh", "abi.cu"], flops)
     return {"workload": name, "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 4), "steps": n, "flops_per_step": flops,
             "gpu_launches": fw.launch_count() - l0,
@@ -339,7 +339,7 @@ def bench_prefill(fw, torch, steps, warmup, device, peaks, name=None):
                        "head_dim": wl.head_dim_qk, "causal": wl.causal, "total_tokens": cu_q[-1],
                        "seq_len_range": list(wl.seq_len_range) if wl.seq_len_range else None,
                        "seq_lens": list(wl.seq_lens) if wl.seq_lens else None, "scale": wl.scale},
-            "roofline": {"kernel": f"varlen_prefill_kernel<{wl.head_dim_qk}>", "bound": "tensor", "achieved": round(ach, 1),
+            "roofline": {"kernel": "varlen_prefill_kernel" if wl.head_dim_qk == 128 else "varlen_prefill_pair_kernel", "bound": "tensor", "achieved": round(ach, 1),
                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": round(ach / peaks["bf16_tflops"], 4),
                          "frac_of_sustained": round(ach / peaks["bf16_tflops_sustained"], 4),
@@ -394,10 +394,10 @@ def bench_decode_fp8(fw, torch, steps, warmup, device, peaks, batch=None):
             "config": {"batch": wl.batch, "q_len": wl.q_len, "num_q_heads": wl.num_q_heads,
                        "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim_qk, "page_size": wl.page_size,
                        "kv_dtype": "fp8_e4m3, one scale per cache", "total_kv_tokens": tokens},
-            "roofline": {"kernel": "paged_decode_fp8_kernel<16>", "bound": "hbm", "achieved": round(ach, 1),
+            "roofline": {"kernel": "paged_decode_fp8_kernel<16,8>", "bound": "hbm", "achieved": round(ach, 1),
                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
                          "traffic": ncu_traffic("paged_decode_fp8_ncu.json",
-                                                ["decode_fp8_kernel.cu", "decode_common.cuh", "fw_ptx.cuh"], tokens),
+                                                ["decode_fp8_kernel.cu", "decode_common.cuh", "fw_ptx.cuh", "abi.cu"], tokens),
                          "peak_source": peaks["source"], "algorithmic_bytes_per_launch": alg,
                          "kernel_ms_per_launch": round(per, 4)}}
 
@@ -460,7 +460,7 @@ def bench_latent(fw, torch, steps, warmup, device, peaks, batch=None):
                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": round(ach / peaks["bf16_tflops"], 4),
                          "frac_of_sustained": round(ach / peaks["bf16_tflops_sustained"], 4),
-                         "traffic": ncu_traffic("latent_decode_ncu.json", ["latent_kernel.cu", "fw_ptx.cuh"],
+                         "traffic": ncu_traffic("latent_decode_ncu.json", ["latent_kernel.cu", "fw_ptx.cuh", "abi.cu"],
                                                 sum(lens)), "peak_source": peaks["source"], "kernel_ms_per_launch": round(per, 4)}}
 
 
