@@ -26,6 +26,12 @@
  *   slot j % page_size.  With q_len > 1 query tokens the rows are causal and
  *   bottom-right aligned: token t sees keys 0 .. n - q_len + t.
  *
+ * Sliding window (oracle_paged_decode_window; "TokenSpeed-MLA 2.0.1",
+ *   window_left): with window_left = W >= 0, token t sees only keys
+ *   max(0, n - q_len + t - W) .. n - q_len + t, i.e. its own position and the
+ *   W positions before it.  Keys before the window are not gathered at all, so
+ *   their block-table entries are never read.  W < 0: no window.
+ *
  * Varlen prefill ("TokenSpeed-MLA 2.0.1", capability summary: ragged varlen
  * prefill without padding, Q and KV packs described by separate cumulative
  * sequence lengths, causal or not):
@@ -137,6 +143,7 @@ typedef struct {
     const void *k; const int64_t *ks;            /* [P, ps, Hkv, Dk]: BF16, or E4M3 when kv8 */
     const void *v; const int64_t *vs;            /* [P, ps, Hkv, Dv]   */
     int kv8; double k_scale, v_scale;
+    int window_left;                             /* < 0: none */
     const int32_t *bt; int64_t bt_stride;        /* [B, max_pages]     */
     const int32_t *seq_lens;                     /* [B]                */
     int B, q_len, Hq, Hkv, Dk, Dv, ps, num_pages, max_pages;
@@ -168,7 +175,12 @@ static void *decode_worker(void *arg) {
         if (visible > n) visible = n;
         if (visible < 0) visible = 0;
         if (n > cap) { J->status = -1; break; }
-        for (int64_t j = 0; j < visible; ++j) {
+        int64_t first = 0;                               /* sliding window: keys first .. visible - 1 */
+        if (J->window_left >= 0 && visible > 0) {
+            first = visible - 1 - J->window_left;
+            if (first < 0) first = 0;
+        }
+        for (int64_t j = first; j < visible; ++j) {
             int32_t page = J->bt[(int64_t)b * J->bt_stride + j / J->ps];
             if (page < 0 || page >= J->num_pages) { J->status = -1; goto done; }
             int64_t slot = j % J->ps;
@@ -177,12 +189,13 @@ static void *decode_worker(void *arg) {
         }
         const uint16_t *qrow = J->q + b * J->qs[0] + t * J->qs[1] + h * J->qs[2];
         if (J->kv8)
-            attend_row_kv8(qrow, J->qs[3], (const uint8_t *const *)kr, J->ks[3], J->k_scale,
-                           (const uint8_t *const *)vr, J->vs[3], J->v_scale, visible, J->Dk, J->Dv,
-                           J->scale, s, J->out + i * J->Dv, J->lse + i);
+            attend_row_kv8(qrow, J->qs[3], (const uint8_t *const *)(kr + first), J->ks[3], J->k_scale,
+                           (const uint8_t *const *)(vr + first), J->vs[3], J->v_scale, visible - first, J->Dk,
+                           J->Dv, J->scale, s, J->out + i * J->Dv, J->lse + i);
         else
-            attend_row(qrow, J->qs[3], (const uint16_t *const *)kr, J->ks[3], (const uint16_t *const *)vr,
-                       J->vs[3], visible, J->Dk, J->Dv, J->scale, s, J->out + i * J->Dv, J->lse + i);
+            attend_row(qrow, J->qs[3], (const uint16_t *const *)(kr + first), J->ks[3],
+                       (const uint16_t *const *)(vr + first), J->vs[3], visible - first, J->Dk, J->Dv, J->scale, s,
+                       J->out + i * J->Dv, J->lse + i);
     }
 done:
     free(s); free(kr); free(vr);
@@ -192,7 +205,7 @@ done:
 static int paged_decode_any(const uint16_t *q, const int64_t *q_stride,
                             const void *k_cache, const int64_t *k_stride,
                             const void *v_cache, const int64_t *v_stride,
-                            int kv8, double k_scale, double v_scale,
+                            int kv8, double k_scale, double v_scale, int window_left,
                             const int32_t *block_table, int64_t bt_stride,
                             const int32_t *seq_lens,
                             int B, int q_len, int Hq, int Hkv, int Dk, int Dv,
@@ -208,7 +221,7 @@ static int paged_decode_any(const uint16_t *q, const int64_t *q_stride,
     for (int w = 0; w < n_threads; ++w) {
         decode_job *J = &jobs[w];
         J->q = q; J->qs = q_stride; J->k = k_cache; J->ks = k_stride; J->v = v_cache; J->vs = v_stride;
-        J->kv8 = kv8; J->k_scale = k_scale; J->v_scale = v_scale;
+        J->kv8 = kv8; J->k_scale = k_scale; J->v_scale = v_scale; J->window_left = window_left;
         J->bt = block_table; J->bt_stride = bt_stride; J->seq_lens = seq_lens;
         J->B = B; J->q_len = q_len; J->Hq = Hq; J->Hkv = Hkv; J->Dk = Dk; J->Dv = Dv;
         J->ps = page_size; J->num_pages = num_pages; J->max_pages = max_pages; J->scale = scale;
@@ -234,7 +247,7 @@ int oracle_paged_decode(const uint16_t *q, const int64_t *q_stride,
                         int page_size, int num_pages, int max_pages, double scale,
                         const int64_t *rows, int64_t n_rows,
                         double *out, double *lse, int n_threads) {
-    return paged_decode_any(q, q_stride, k_cache, k_stride, v_cache, v_stride, 0, 1.0, 1.0, block_table,
+    return paged_decode_any(q, q_stride, k_cache, k_stride, v_cache, v_stride, 0, 1.0, 1.0, -1, block_table,
                             bt_stride, seq_lens, B, q_len, Hq, Hkv, Dk, Dv, page_size, num_pages, max_pages,
                             scale, rows, n_rows, out, lse, n_threads);
 }
@@ -249,9 +262,25 @@ int oracle_paged_decode_kv8(const uint16_t *q, const int64_t *q_stride,
                             int page_size, int num_pages, int max_pages, double scale,
                             const int64_t *rows, int64_t n_rows,
                             double *out, double *lse, int n_threads) {
-    return paged_decode_any(q, q_stride, k_cache, k_stride, v_cache, v_stride, 1, k_scale, v_scale, block_table,
+    return paged_decode_any(q, q_stride, k_cache, k_stride, v_cache, v_stride, 1, k_scale, v_scale, -1, block_table,
                             bt_stride, seq_lens, B, q_len, Hq, Hkv, Dk, Dv, page_size, num_pages, max_pages,
                             scale, rows, n_rows, out, lse, n_threads);
+}
+
+/* Either cache type (kv8 = 1: E4M3 bytes with scales) and a sliding window. */
+int oracle_paged_decode_window(const uint16_t *q, const int64_t *q_stride,
+                               const void *k_cache, const int64_t *k_stride,
+                               const void *v_cache, const int64_t *v_stride,
+                               int kv8, double k_scale, double v_scale, int window_left,
+                               const int32_t *block_table, int64_t bt_stride,
+                               const int32_t *seq_lens,
+                               int B, int q_len, int Hq, int Hkv, int Dk, int Dv,
+                               int page_size, int num_pages, int max_pages, double scale,
+                               const int64_t *rows, int64_t n_rows,
+                               double *out, double *lse, int n_threads) {
+    return paged_decode_any(q, q_stride, k_cache, k_stride, v_cache, v_stride, kv8, k_scale, v_scale, window_left,
+                            block_table, bt_stride, seq_lens, B, q_len, Hq, Hkv, Dk, Dv, page_size, num_pages,
+                            max_pages, scale, rows, n_rows, out, lse, n_threads);
 }
 
 /* ----------------------------------------------------------------- prefill */

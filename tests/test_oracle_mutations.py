@@ -28,6 +28,7 @@ MUTATIONS = {
     "missing_normalisation": ("for (int d = 0; d < dv; ++d) out[d] /= l;", ""),
     "fp8_value_scale_dropped": ("out[d] += p * (v_scale * oracle_e4m3_to_double", "out[d] += p * (oracle_e4m3_to_double"),
     "fp8_exponent_bias_off": ("else v = ldexp(1.0 + m / 8.0, e - 7);", "else v = ldexp(1.0 + m / 8.0, e - 8);"),
+    "window_off_by_one": ("first = visible - 1 - J->window_left;", "first = visible - J->window_left;"),
 }
 
 PIN_CHECKS = [
@@ -40,6 +41,8 @@ PIN_CHECKS = [
     pins.test_lse_bounds,
     pins.test_e4m3_decoding_matches_torch_for_every_byte,
     lambda: pins.test_fp8_kv_decode_matches_sdpa_on_dequantized_copy(1, (5, 1, 13)),
+    lambda: pins.test_window_matches_sdpa_on_dense_copy(2, (9, 30, 2), 4, 7),
+    pins.test_window_zero_sees_own_position_only,
 ]
 
 
@@ -60,7 +63,8 @@ def test_pins_catch_mutant(tmp_path, monkeypatch, name):
     oracle._load()                                   # fetch argtypes from the real library
     real = oracle._lib
     mutant = ctypes.CDLL(lib_path)
-    for fn in ("oracle_paged_decode", "oracle_paged_decode_kv8", "oracle_e4m3_to_double", "oracle_varlen_prefill"):
+    for fn in ("oracle_paged_decode", "oracle_paged_decode_kv8", "oracle_paged_decode_window", "oracle_e4m3_to_double",
+               "oracle_varlen_prefill"):
         getattr(mutant, fn).restype = getattr(real, fn).restype
         getattr(mutant, fn).argtypes = getattr(real, fn).argtypes
     monkeypatch.setattr(oracle, "_lib", mutant)

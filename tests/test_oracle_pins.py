@@ -559,3 +559,93 @@ def test_fp8_scales_fold_into_score_scale_and_output():
     o3, l3 = oracle.paged_decode(*args, 0.3, k_scale=2.0, v_scale=3.0)
     np.testing.assert_allclose(o3, 3.0 * o1, atol=1e-12)
     np.testing.assert_allclose(l3, l1, atol=1e-12)
+
+
+# ------------------------------------------------------------ sliding window
+# "TokenSpeed-MLA 2.0.1", window_left: token t of a row with n keys sees keys
+# max(0, n - q_len + t - W) .. n - q_len + t.
+
+def _window_mask(q_len, n, window_left):
+    mask = torch.zeros(q_len, n, dtype=torch.bool)
+    for t in range(q_len):
+        hi = n - q_len + t                         # last visible key (bottom-right causal)
+        if hi < 0:
+            continue
+        lo = max(0, hi - window_left)
+        mask[t, lo:hi + 1] = True
+    return mask
+
+
+@pytest.mark.parametrize("q_len,lens,ps,window", [
+    (1, (5, 1, 13), 4, 0), (1, (16, 17, 3), 8, 3), (2, (9, 30, 2), 4, 7), (4, (20, 6, 33), 8, 5),
+    (3, (40, 41, 12), 16, 16)])
+def test_window_matches_sdpa_on_dense_copy(q_len, lens, ps, window):
+    wl, inp = tiny_decode(q_len=q_len, lens=lens, ps=ps, seed=17)
+    out, lse = oracle.paged_decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"],
+                                   inp["seq_lens"], inp["scale"], window_left=window)
+    hq, hkv = wl.num_q_heads, wl.num_kv_heads
+    for b in range(wl.batch):
+        k, v = dense_kv(inp, b)
+        n = k.shape[0]
+        q = inp["q"][b].double()
+        k = k.double().repeat_interleave(hq // hkv, dim=1)
+        v = v.double().repeat_interleave(hq // hkv, dim=1)
+        mask = _window_mask(q_len, n, window)
+        sc = (torch.einsum("thd,nhd->htn", q, k) * inp["scale"]).masked_fill(~mask, float("-inf"))
+        w = torch.softmax(sc, -1).nan_to_num(0.0)  # rows with no visible key: zero output
+        ref = torch.einsum("htn,nhd->thd", w, v).reshape(q_len * hq, -1).numpy()
+        rows = slice(b * q_len * hq, (b + 1) * q_len * hq)
+        np.testing.assert_allclose(out[rows], ref, atol=1e-12)
+        np.testing.assert_allclose(lse[rows], torch.logsumexp(sc, -1).transpose(0, 1).reshape(-1).numpy(),
+                                   atol=1e-12)
+
+
+def test_window_zero_sees_own_position_only():
+    """W = 0: token t sees exactly key n - q_len + t, so out = that value row
+    and lse = that score (closed form)."""
+    wl, inp = tiny_decode(q_len=3, lens=(7, 12, 5), ps=4, seed=19)
+    out, lse = oracle.paged_decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"],
+                                   inp["seq_lens"], inp["scale"], window_left=0)
+    G = wl.num_q_heads // wl.num_kv_heads
+    for b in range(wl.batch):
+        k, v = dense_kv(inp, b)
+        n = k.shape[0]
+        for t in range(wl.q_len):
+            j = n - wl.q_len + t
+            for h in range(wl.num_q_heads):
+                r = (b * wl.q_len + t) * wl.num_q_heads + h
+                np.testing.assert_allclose(out[r], v[j, h // G].double().numpy(), atol=1e-12)
+                s = inp["scale"] * float((inp["q"][b, t, h].double() * k[j, h // G].double()).sum())
+                assert abs(lse[r] - s) < 1e-12
+
+
+def test_window_wider_than_row_is_no_window():
+    wl, inp = tiny_decode(q_len=2, lens=(9, 30, 2), ps=4, seed=21)
+    args = (inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"], inp["seq_lens"], inp["scale"])
+    o0, l0 = oracle.paged_decode(*args)
+    o1, l1 = oracle.paged_decode(*args, window_left=30)
+    np.testing.assert_array_equal(o0, o1)
+    np.testing.assert_array_equal(l0, l1)
+
+
+def test_window_never_reads_pages_before_it():
+    """Pages wholly before every token's window may be evicted: their table
+    entries can hold anything and their contents NaN (a cache that drops keys
+    leaving the window)."""
+    wl, inp = tiny_decode(q_len=2, lens=(40, 37, 9), ps=4, seed=23)
+    W = 6
+    args = (inp["q"], inp["k_cache"], inp["v_cache"])
+    o0, l0 = oracle.paged_decode(*args, inp["block_table"], inp["seq_lens"], inp["scale"], window_left=W)
+    bt = inp["block_table"].clone()
+    kc, vc = inp["k_cache"].clone(), inp["v_cache"].clone()
+    for b in range(wl.batch):
+        n = int(inp["seq_lens"][b])
+        first = max(0, n - wl.q_len - W)           # smallest lower bound of the row
+        for pg in range(first // wl.page_size):
+            kc[int(bt[b, pg])] = float("nan")
+            vc[int(bt[b, pg])] = float("nan")
+        for pg in range(first // wl.page_size):
+            bt[b, pg] = -1
+    o1, l1 = oracle.paged_decode(inp["q"], kc, vc, bt, inp["seq_lens"], inp["scale"], window_left=W)
+    np.testing.assert_array_equal(o0, o1)
+    np.testing.assert_array_equal(l0, l1)
