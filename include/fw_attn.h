@@ -151,17 +151,46 @@ fw_status_t fw_paged_decode_noalloc(const fw_tensor_t *q, const fw_tensor_t *k_c
  *
  * Supported: Dk = Dv = 128, the query-head groupings, q_len 1-4 and page
  * sizes of fw_paged_decode; cache strides multiples of 16 bytes.  The
- * arithmetic is exact in the FP8 values: keys and values are widened to FP16
- * on chip (every E4M3 value is an FP16 value), queries are converted from
- * BF16 to FP16 (|q| must stay below 65504), scores and sums are FP32.  The
- * same workspace as fw_paged_decode (fw_paged_decode_workspace_size with the
- * same shapes); errors as fw_paged_decode, plus FW_ERR_INVALID_ARG for a
- * non-finite or non-positive k_scale / v_scale.
+ * tensor cores read the E4M3 bytes as stored; the result is that of FP16
+ * products of the FP8 values with FP16-exact queries and probabilities and
+ * FP32 sums: each BF16 query row is scaled by a power of two and carried as
+ * two E4M3 terms (exact for every element down to 2^-10 of the row's largest
+ * magnitude), each probability is rounded to FP16 and carried as four E5M2
+ * terms (exact).  The same workspace as fw_paged_decode
+ * (fw_paged_decode_workspace_size with the same shapes); errors as
+ * fw_paged_decode, plus FW_ERR_INVALID_ARG for a non-finite or non-positive
+ * k_scale / v_scale.
  */
 fw_status_t fw_paged_decode_fp8(const fw_tensor_t *q, const fw_tensor_t *k_cache,
                                 const fw_tensor_t *v_cache, const fw_tensor_t *block_table,
                                 const fw_tensor_t *seq_lens, float scale, float k_scale, float v_scale,
                                 fw_tensor_t *out, fw_tensor_t *lse, fw_stream_t stream);
+
+/*
+ * Paged decode with a sliding window ("TokenSpeed-MLA 2.0.1", window_left),
+ * over a BF16 or an FP8_E4M3 cache (chosen by k_cache's dtype).
+ *
+ *   window_left  -1: no window (the call equals fw_paged_decode or
+ *                fw_paged_decode_fp8); W >= 0: query token t of row b sees only
+ *                keys max(0, n - q_len + t - W) .. n - q_len + t, n =
+ *                seq_lens[b] -- its own position and the W before it.
+ *   k_scale, v_scale  the FP8 cache scales; must be 1 for a BF16 cache.
+ *   other arguments   as fw_paged_decode / fw_paged_decode_fp8.
+ *
+ * The walk of a row starts at the KV tile holding its first visible key, so
+ * the work scales with the window, not the row.  Block-table entries of pages
+ * wholly before key max(0, n - q_len - W) are never read and those pages are
+ * never loaded: a cache may drop pages that left the window.  Supported: the
+ * grouped-query layouts of fw_paged_decode (Dk = Dv in {128, 256}) and of
+ * fw_paged_decode_fp8; the latent layout (Dk 576, Dv 512) returns
+ * FW_ERR_UNSUPPORTED when W >= 0.  FW_ERR_INVALID_ARG for W < -1 or BF16
+ * caches with scales other than 1.  Same workspace as fw_paged_decode.
+ */
+fw_status_t fw_paged_decode_window(const fw_tensor_t *q, const fw_tensor_t *k_cache,
+                                   const fw_tensor_t *v_cache, const fw_tensor_t *block_table,
+                                   const fw_tensor_t *seq_lens, float scale, float k_scale, float v_scale,
+                                   int32_t window_left, fw_tensor_t *out, fw_tensor_t *lse,
+                                   fw_stream_t stream);
 
 /*
  * Workspace bytes fw_paged_decode needs for these shapes (data pointers are

@@ -411,12 +411,17 @@ static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_
                                      const fw_tensor_t *block_table, const fw_tensor_t *seq_lens, float scale,
                                      fw_tensor_t *out, fw_tensor_t *lse, fw_stream_t stream_,
                                      void *(*fixed_ws)(DeviceState *, fw_status_t *), size_t fixed_bytes,
-                                     bool kv8 = false, float k_scale = 1.f, float v_scale = 1.f) {
+                                     bool kv8 = false, float k_scale = 1.f, float v_scale = 1.f,
+                                     int32_t window_left = -1, bool any_cache = false) {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     if (fw_status_t s = decode_shapes(q, k_cache, v_cache, block_table)) return s;
+    if (any_cache) kv8 = k_cache->dtype == FW_FP8_E4M3;
     if (kv8 != (k_cache->dtype == FW_FP8_E4M3))
         return fail(FW_ERR_INVALID_ARG, kv8 ? "fw_paged_decode_fp8 takes FP8_E4M3 caches"
                                             : "FP8 caches go through fw_paged_decode_fp8");
+    if (!kv8 && (k_scale != 1.f || v_scale != 1.f))
+        return fail(FW_ERR_INVALID_ARG, "k_scale and v_scale must be 1 for BF16 caches");
+    if (window_left < -1) return fail(FW_ERR_INVALID_ARG, "window_left must be -1 (no window) or >= 0");
     if (kv8 && !(std::isfinite(k_scale) && std::isfinite(v_scale) && k_scale > 0.f && v_scale > 0.f))
         return fail(FW_ERR_INVALID_ARG, "k_scale and v_scale must be finite and positive");
     if (fw_status_t s = check_tensor(seq_lens, "seq_lens", 1, FW_I32)) return s;
@@ -434,6 +439,8 @@ static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_
         return fail(FW_ERR_INVALID_ARG, "lse must be [B, q_len, Hq]");
     if (!std::isfinite(scale)) return fail(FW_ERR_INVALID_ARG, "scale must be finite");
     const bool latent = !kv8 && (Dk == 576 && Dv == 512);
+    if (latent && window_left >= 0)
+        return fail(FW_ERR_UNSUPPORTED, "sliding windows are served for Dk = Dv in {128, 256} (BF16) and 128 (FP8)");
     if (kv8 && !(Dk == 128 && Dv == 128))
         return fail(FW_ERR_UNSUPPORTED, "FP8 decode head dims (Dk=%lld, Dv=%lld): supported Dk = Dv = 128",
                     (long long)Dk, (long long)Dv);
@@ -491,6 +498,7 @@ static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_
     p.max_pieces = pl.max_pieces;
     p.grid = pl.grid;
     p.Dv = (int)Dv;
+    p.window_left = window_left;
     p.block_table = static_cast<const int32_t *>(block_table->data);
     p.bt_stride = block_table->stride[0];
     p.seq_lens = static_cast<const int32_t *>(seq_lens->data);
@@ -570,6 +578,14 @@ fw_status_t fw_paged_decode_fp8(const fw_tensor_t *q, const fw_tensor_t *k_cache
                                 fw_stream_t stream) {
     return paged_decode_impl(q, k_cache, v_cache, block_table, seq_lens, scale, out, lse, stream, nullptr, 0,
                              true, k_scale, v_scale);
+}
+
+fw_status_t fw_paged_decode_window(const fw_tensor_t *q, const fw_tensor_t *k_cache, const fw_tensor_t *v_cache,
+                                   const fw_tensor_t *block_table, const fw_tensor_t *seq_lens, float scale,
+                                   float k_scale, float v_scale, int32_t window_left, fw_tensor_t *out,
+                                   fw_tensor_t *lse, fw_stream_t stream) {
+    return paged_decode_impl(q, k_cache, v_cache, block_table, seq_lens, scale, out, lse, stream, nullptr, 0,
+                             false, k_scale, v_scale, window_left, true);
 }
 
 // ----------------------------------------------------- decode without allocation

@@ -10,7 +10,7 @@ namespace fw {
 namespace dec {
 
 struct Unit {                 // one piece: a unit's tiles inside one CTA range
-    int b, g, rg, n, k_begin, k_end, ntiles;
+    int b, g, rg, n, lo, k_begin, k_end, ntiles;   // lo: first key any row of the unit may see
     int k, npieces;
     bool single;
 };
@@ -20,6 +20,19 @@ __device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b
 __device__ __forceinline__ int clamp_len(const DecodeParams &p, int n) {
     const int cap = p.max_pages * p.ps;
     return n < 0 ? 0 : (n > cap ? cap : n);
+}
+
+// First key any query row of a row with n keys may see: max(0, n - q_len -
+// W) under a sliding window of W ("TokenSpeed-MLA 2.0.1", window_left), else
+// 0.  The row's walk starts at the tile holding it; pages wholly before it
+// are never read.
+__device__ __forceinline__ int window_first_key(const DecodeParams &p, int n) {
+    return p.window_left < 0 ? 0 : max(0, n - p.q_len - p.window_left);
+}
+
+// KV tiles a row with n keys walks (per unit).
+__device__ __forceinline__ int row_tiles(const DecodeParams &p, int n) {
+    return ceil_div_i(n, kKvTile) - window_first_key(p, n) / kKvTile;
 }
 
 // Walks the pieces of this CTA's tile ranges; every role runs its own copy
@@ -68,8 +81,10 @@ struct PieceIter {
         x.g = u / p.row_groups;
         x.rg = u - x.g * p.row_groups;
         x.n = clamp_len(p, __ldg(p.seq_lens + b));
-        x.k_begin = tl * kKvTile;
-        x.k_end = min(x.n, th * kKvTile);
+        x.lo = window_first_key(p, x.n);
+        const int t0 = x.lo / kKvTile;               // the walk starts at the window's first tile
+        x.k_begin = (t0 + tl) * kKvTile;
+        x.k_end = min(x.n, (t0 + th) * kKvTile);
         x.ntiles = th - tl;
         x.k = (pstart + tl) / span - pstart / span;
         x.npieces = (pstart + tb - 1) / span - pstart / span + 1;

@@ -197,12 +197,16 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                     const int slot0 = p.ps < kKvTile ? 0 : ts % p.ps;
                     int npages = 1;
                     if (p.ps < kKvTile) npages = min(pages_per_tile, ceil_div_i(x.k_end - ts, p.ps));
+                    // Leading pages wholly before the window are neither looked
+                    // up nor loaded (their rows are masked, their V rows zeroed).
+                    const int skip = min(npages, max(0, x.lo / p.ps - ts / p.ps));
+                    const bool load = lane >= skip && lane < npages;
                     int phys = 0;
-                    if (lane < npages) {
+                    if (load) {
                         phys = __ldg(bt_row + ts / p.ps + lane);
                         if ((unsigned)phys >= (unsigned)p.num_pages) { record_error(p.status, 1); phys = 0; }
                     }
-                    const uint32_t bytes = (uint32_t)(npages * box_rows * 128);
+                    const uint32_t bytes = (uint32_t)((npages - skip) * box_rows * 128);
                     const int s = jt % S;
                     if (!warp_wait(&kv_empty[s], ((jt / S) & 1) ^ 1, wc, lane)) goto producer_done;
                     uint8_t *stage = ring + s * C::kStageBytes;
@@ -211,7 +215,7 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                         mbar_arrive_expect_tx(&v_full[s], bytes);
                     }
                     __syncwarp();
-                    if (lane < npages) {
+                    if (load) {
                         tma_load_4d(smem_u32(stage + lane * box_rows * 128), &tm_k, &k_full[s], 0, x.g, slot0, phys);
                         tma_load_4d(smem_u32(stage + C::kTileBytes + lane * box_rows * 128), &tm_v, &v_full[s], 0,
                                     x.g, slot0, phys);
@@ -382,6 +386,9 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                 if (ok) nrows = r + 1;
                 rs[r] = p.scale_log2 * __int_as_float((127 - q_exp[qs * NQ + r0 + r]) << 23);
             }
+            // Sliding window: a row with visible-key bound lim sees keys
+            // lim - 1 - W .. lim - 1, i.e. lim - tok <= W + 1.
+            const int wp1 = p.window_left < 0 ? 0x7fffffff : p.window_left + 1;
             float m_ref[RH], l_part[RH];
 #pragma unroll
             for (int r = 0; r < RH; ++r) { m_ref[r] = kNegInf; l_part[r] = 0.f; }
@@ -400,7 +407,8 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                 if (lane == 0) mbar_arrive(&s_free[sb]);
                 float *rm = red_max + (jt & 1) * 4 * R;
 #pragma unroll
-                for (int r = 0; r < RH; ++r) s[r] = (tok < lim[r]) ? (s[r] + sm[r]) * rs[r] : kNegInf;
+                for (int r = 0; r < RH; ++r)
+                    s[r] = (tok < lim[r] && lim[r] - tok <= wp1) ? (s[r] + sm[r]) * rs[r] : kNegInf;
                 warp_rows_reduce<RH, true>(s, lane, rm + q4 * R + r0);
                 named_bar_sync(1 + half, 128);
                 bool need = false;
@@ -446,13 +454,14 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                         tmem_wait_st();
                     }
                 }
-                if (half == 0 && ts + kKvTile > x.n) {
-                    // Keys past the row's end: their V rows may hold anything
-                    // (unloaded pages, poisoned slots).  Zero them so that the
-                    // exact-zero probabilities cannot meet a NaN in the MMA.
+                if (half == 0 && (ts + kKvTile > x.n || ts < x.lo)) {
+                    // Keys past the row's end or before its window: their V
+                    // rows may hold anything (unloaded pages, poisoned slots).
+                    // Zero them so that the exact-zero probabilities cannot
+                    // meet a NaN in the MMA.
                     const int s = jt % S;
                     mbar_wait(&v_full[s], (jt / S) & 1, wc);
-                    if (tok >= x.n) {
+                    if (tok >= x.n || tok < x.lo) {
                         uint4 *row = reinterpret_cast<uint4 *>(ring + s * C::kStageBytes + C::kTileBytes + key * 128);
 #pragma unroll
                         for (int k = 0; k < 8; ++k) row[k] = make_uint4(0, 0, 0, 0);

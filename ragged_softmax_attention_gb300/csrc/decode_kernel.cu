@@ -159,12 +159,15 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
             // two 32-entry register windows (lane l holds page win + l and
             // win + 32 + l); the next window is fetched while the current one
             // is in use, so no tile waits on a block-table read.  Entries past
-            // the row's last page are never read (PyPTO section 9.1).
+            // the row's last page are never read (PyPTO section 9.1), nor, under
+            // a sliding window, those of pages wholly before the window.
             const int32_t *bt_row = p.block_table + (int64_t)x.b * p.bt_stride;
             const int lp_end = ceil_div_i(x.k_end, p.ps);
+            const int lp_first = x.lo / p.ps;
             int win = x.k_begin / p.ps;
-            int cur = (win + lane < lp_end) ? __ldg(bt_row + win + lane) : 0;
-            int nxt = (win + 32 + lane < lp_end) ? __ldg(bt_row + win + 32 + lane) : 0;
+            auto bt_at = [&](int lp) { return (lp >= lp_first && lp < lp_end) ? __ldg(bt_row + lp) : 0; };
+            int cur = bt_at(win + lane);
+            int nxt = bt_at(win + 32 + lane);
             for (int i = 0; i < x.ntiles; ++i, ++jt) {
                 const int ts = x.k_begin + i * kKvTile;
                 const int lp0 = ts / p.ps;
@@ -174,19 +177,23 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
                 if (lp0 >= win + 32) {
                     win += 32;
                     cur = nxt;
-                    nxt = (win + 32 + lane < lp_end) ? __ldg(bt_row + win + 32 + lane) : 0;
+                    nxt = bt_at(win + 32 + lane);
                 }
+                // Leading pages of the tile wholly before the window are not
+                // loaded (their rows are masked and their V rows zeroed).
+                const int skip = min(npages, max(0, lp_first - lp0));
+                const bool load = lane >= skip && lane < npages;
                 const int idx = lp0 + lane - win;          // < 64 since npages <= 16
                 const int from_cur = __shfl_sync(0xffffffffu, cur, idx & 31);
                 const int from_nxt = __shfl_sync(0xffffffffu, nxt, idx & 31);
                 int phys = idx < 32 ? from_cur : from_nxt;
-                if (lane < npages && (unsigned)phys >= (unsigned)p.num_pages) { record_error(p.status, 1); phys = 0; }
-                const uint32_t bytes = (uint32_t)(npages * box_rows * 128 * C::kChunks);
+                if (load && (unsigned)phys >= (unsigned)p.num_pages) { record_error(p.status, 1); phys = 0; }
+                const uint32_t bytes = (uint32_t)((npages - skip) * box_rows * 128 * C::kChunks);
                 const int ks = jt % C::kKStages;
                 if (!warp_wait(&k_empty[ks], ((jt / C::kKStages) & 1) ^ 1, wc, lane)) goto producer_done;
                 if (lane == 0) mbar_arrive_expect_tx(&k_full[ks], bytes);
                 __syncwarp();
-                if (lane < npages) {
+                if (load) {
 #pragma unroll
                     for (int c = 0; c < C::kChunks; ++c)
                         tma_load_4d(smem_u32(sK + ks * C::kTileBytes + c * C::kChunkBytes + lane * box_rows * 128),
@@ -197,7 +204,7 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
                 if (!warp_wait(&v_empty[vs], ((jt / C::kVStages) & 1) ^ 1, wc, lane)) goto producer_done;
                 if (lane == 0) mbar_arrive_expect_tx(&v_full[vs], bytes);
                 __syncwarp();
-                if (lane < npages) {
+                if (load) {
 #pragma unroll
                     for (int c = 0; c < C::kChunks; ++c)
                         tma_load_4d(smem_u32(sV + vs * C::kTileBytes + c * C::kChunkBytes + lane * box_rows * 128),
@@ -307,6 +314,9 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
                 lim[r] = ok ? min(x.n, x.n - p.q_len + t + 1) : 0;
                 if (ok) nrows = r + 1;
             }
+            // Sliding window: a row with visible-key bound lim sees keys
+            // lim - 1 - W .. lim - 1, i.e. lim - tok <= W + 1.
+            const int wp1 = p.window_left < 0 ? 0x7fffffff : p.window_left + 1;
             float m_ref[NQ], l_part[NQ];
 #pragma unroll
             for (int r = 0; r < NQ; ++r) { m_ref[r] = kNegInf; l_part[r] = 0.f; }
@@ -326,7 +336,7 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
                 if (lane == 0) mbar_arrive(&s_free[sb]);
                 float* rm = red_max + (jt & 1) * 4 * NQ;
 #pragma unroll
-                for (int r = 0; r < NQ; ++r) s[r] = (tok < lim[r]) ? s[r] * p.scale_log2 : kNegInf;
+                for (int r = 0; r < NQ; ++r) s[r] = (tok < lim[r] && lim[r] - tok <= wp1) ? s[r] * p.scale_log2 : kNegInf;
                 warp_rows_reduce<NQ, true>(s, lane, rm + q4 * NQ);
                 named_bar_sync(1, 128);
                 bool need = false;
@@ -368,13 +378,14 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
                         tmem_wait_st();
                     }
                 }
-                if (ts + kKvTile > x.n) {
-                    // Keys past the row's end: their V rows may hold anything
-                    // (unloaded pages, poisoned slots).  Zero them so that the
-                    // exact-zero probabilities cannot meet a NaN in the MMA.
+                if (ts + kKvTile > x.n || ts < x.lo) {
+                    // Keys past the row's end or before its window: their V
+                    // rows may hold anything (unloaded pages, poisoned slots).
+                    // Zero them so that the exact-zero probabilities cannot
+                    // meet a NaN in the MMA.
                     const int vs = jt % C::kVStages;
                     mbar_wait(&v_full[vs], (jt / C::kVStages) & 1, wc);
-                    if (tok >= x.n) {
+                    if (tok >= x.n || tok < x.lo) {
 #pragma unroll
                         for (int c = 0; c < C::kChunks; ++c) {
                             uint4 *row = reinterpret_cast<uint4 *>(sV + vs * C::kTileBytes + c * C::kChunkBytes +
@@ -487,7 +498,8 @@ cudaError_t launch_t(const DecodeParams &p, const CUtensorMap &tq, const CUtenso
 // ------------------------------------------------------------------- plan
 //
 // One block: exclusive prefix PB[b] of the KV tiles each batch row puts in
-// the global order (ceil(n_b / 128) tiles for each of its units), the total
+// the global order (the tiles from the window's first key, or from key 0,
+// to ceil(n_b / 128), for each of its units), the total
 // T and the range span; rows with no keys get their zero output and -inf LSE
 // here, since no range ever covers them.
 __global__ void __launch_bounds__(1024) decode_plan_kernel(const __grid_constant__ DecodeParams p) {
@@ -500,7 +512,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const __grid_constant
     for (int base = 0; base < p.B; base += 1024) {
         const int b = base + tid;
         const int n = b < p.B ? clamp_len(p, __ldg(p.seq_lens + b)) : 0;
-        const int t = ceil_div_i(n, kKvTile) * p.units_per_row;
+        const int t = row_tiles(p, n) * p.units_per_row;
         int incl = t;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {

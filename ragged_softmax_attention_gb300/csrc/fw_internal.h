@@ -37,6 +37,7 @@ struct DecodeParams {
                           // a unit ride on the CTA index (CTA c runs row group c % R over ranges
                           // c / R, c / R + grid / R, ...), so they read the same keys together
     int Dv;
+    int window_left;      // < 0: none; else token t sees keys max(0, n - q_len + t - W) .. n - q_len + t
     int32_t *plan;        // [0] = T, [1] = span, [2 .. 2 + B] = PB
     const int32_t *block_table; int64_t bt_stride;
     const int32_t *seq_lens;
