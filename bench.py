@@ -402,6 +402,59 @@ def bench_decode_fp8(fw, torch, steps, warmup, device, peaks, batch=None):
                          "kernel_ms_per_launch": round(per, 4)}}
 
 
+def bench_decode_window(fw, torch, steps, warmup, device, peaks, fp8=False, window=4096):
+    """Sliding-window decode ("TokenSpeed-MLA 2.0.1", window_left) on the
+    Qwen3-14B-shaped workload: each row reads only its last window + q_len keys.
+    The metric counts those keys' bytes (the window's own KV), so it compares
+    directly with the full-row decode's GB/s."""
+    from ragged_softmax_attention_gb300.workloads import WORKLOADS, make_decode_inputs
+    wl = WORKLOADS[DECODE_FP8_WL if fp8 else DECODE_WL]
+    d = make_decode_inputs(wl, device)
+    lens = d["seq_lens"].long().cpu()
+    first = (lens - wl.q_len - window).clamp(min=0)
+    tokens = int((lens - first).sum())
+    esz = 1 if fp8 else 2
+    kv = tokens * wl.num_kv_heads * (wl.head_dim_qk + wl.head_dim_v) * esz
+    rows = wl.batch * wl.q_len * wl.num_q_heads
+    pages = int((((lens + wl.page_size - 1) // wl.page_size) - first // wl.page_size).sum())
+    alg = kv + rows * wl.head_dim_qk * 2 + rows * wl.head_dim_v * 2 + rows * 4 + pages * 4 + wl.batch * 4
+    ks, vs = (d["k_scale"], d["v_scale"]) if fp8 else (1.0, 1.0)
+    args = (d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["seq_lens"], d["scale"], window)
+    out, lse = fw.paged_decode_window(*args, k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, warmup)):
+        fw.paged_decode_window(*args, k_scale=ks, v_scale=vs, out=out, lse=lse)
+    torch.cuda.synchronize()
+    fw.set_option(fw.FW_OPT_KERNEL_TIMING, 1)
+    fw.kernel_timing_read()
+    n = max(3, min(steps, 100))
+    l0 = fw.launch_count()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(n):
+        fw.paged_decode_window(*args, k_scale=ks, v_scale=vs, out=out, lse=lse)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(stop) / n
+    kms, kn = fw.kernel_timing_read()
+    fw.set_option(fw.FW_OPT_KERNEL_TIMING, 0)
+    if fw.device_status() != 0:
+        raise RuntimeError("device status nonzero during the sliding-window decode benchmark")
+    per = kms / max(1, kn)
+    ach = alg / (per * 1e-3) / 1e9
+    kernel = "paged_decode_fp8_kernel<16,8>" if fp8 else "paged_decode_kernel<128,16>"
+    return {"workload": (DECODE_FP8_WL if fp8 else DECODE_WL) + f", window_left {window}",
+            "value": round(kv / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "kv_tokens_per_s": round(tokens / (ms * 1e-3), 1), "ms_per_step": round(ms, 4), "steps": n,
+            "kv_bytes_per_step": kv, "window_kv_tokens": tokens, "gpu_launches": fw.launch_count() - l0,
+            "roofline": {"kernel": kernel, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": None,
+                         "peak_source": peaks["source"], "algorithmic_bytes_per_launch": alg,
+                         "kernel_ms_per_launch": round(per, 4)}}
+
+
 # ------------------------------------------------------- latent decode
 
 def latent_work(lens, wl):
@@ -548,7 +601,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--only", choices=["all", "decode", "decode_fp8", "prefill", "prefill256", "latent"],
+    ap.add_argument("--only", choices=["all", "decode", "decode_fp8", "decode_window", "prefill", "prefill256",
+                                       "latent"],
                     default="all",
                     help="profiling runs: time one path only")
     ap.add_argument("--decode-batch", type=int, default=0,
@@ -592,6 +646,12 @@ def main():
         if rank == 0:
             print(json.dumps({"decode_fp8": f8}), flush=True)
         return 0
+    if args.only == "decode_window":
+        w16 = bench_decode_window(fw, torch, args.steps, args.warmup, device, peaks, fp8=False)
+        w8 = bench_decode_window(fw, torch, args.steps, args.warmup, device, peaks, fp8=True)
+        if rank == 0:
+            print(json.dumps({"decode_window": w16, "decode_fp8_window": w8}), flush=True)
+        return 0
     if args.only == "latent":
         lat = bench_latent(fw, torch, args.steps, args.warmup, device, peaks, batch=args.latent_batch or None)
         if rank == 0:
@@ -604,6 +664,10 @@ def main():
               bench_prefill(fw, torch, args.steps, args.warmup, device, peaks, name=PREFILL_HD256_WL))
     lat = None if args.only == "decode" else bench_latent(fw, torch, args.steps, args.warmup, device, peaks)
     f8 = None if args.only == "decode" else bench_decode_fp8(fw, torch, args.steps, args.warmup, device, peaks)
+    w16 = (None if args.only == "decode" else
+           bench_decode_window(fw, torch, args.steps, args.warmup, device, peaks, fp8=False))
+    w8 = (None if args.only == "decode" else
+          bench_decode_window(fw, torch, args.steps, args.warmup, device, peaks, fp8=True))
     elapsed_ms, e2e_ms = max_over_ranks(pg, [dec["elapsed_ms"], dec["e2e_ms"]], device)
     value = whole_job_rate(dec["kv_bytes"], args.steps, world, elapsed_ms)
     e2e_value = whole_job_rate(dec["kv_bytes"], 1, world, e2e_ms)
@@ -620,7 +684,8 @@ def main():
             "e2e": {"value": round(e2e_value, 1) if e2e_value else None, "unit": "GB/s", "h2d_bytes_per_step": dec["h2d"],
                     "d2h_bytes_per_step": dec["d2h"], "steps": dec["e2e_steps"],
                     "note": "inputs (incl. the KV cache) copied from pinned host memory every step"},
-            "prefill": pre, "prefill_hd256": pre256, "latent_decode": lat, "decode_fp8": f8}
+            "prefill": pre, "prefill_hd256": pre256, "latent_decode": lat, "decode_fp8": f8,
+            "decode_window": w16, "decode_fp8_window": w8}
     if world == 1 and not args.no_cpu_baseline and not args.decode_batch:
         try:
             line["cpu_baseline"] = cpu_baseline(torch, dec["inputs"], dec["wl"])
