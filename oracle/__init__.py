@@ -53,6 +53,11 @@ def _load():
         lib.oracle_paged_decode_window.restype = I
         lib.oracle_paged_decode_window.argtypes = [P, P, P, P, P, P, I, D, D, I, P, L, P, I, I, I, I, I, I, I, I, I,
                                                    D, P, L, P, P, I]
+        lib.oracle_e4m3_from_float.restype = ctypes.c_uint8
+        lib.oracle_e4m3_from_float.argtypes = [ctypes.c_float]
+        lib.oracle_kv_append.restype = I
+        lib.oracle_kv_append.argtypes = [P, P, P, P, P, L, P, P, P, P, I, ctypes.c_float, ctypes.c_float,
+                                         I, I, I, I, I, I, L]
         lib.oracle_e4m3_to_double.restype = D
         lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
         lib.oracle_varlen_prefill.restype = I
@@ -154,6 +159,42 @@ def paged_decode(q, k_cache, v_cache, block_table, seq_lens, scale, rows=None, t
     if rc != 0:
         raise ValueError(f"oracle_paged_decode failed with code {rc}")
     return out, lse
+
+
+def e4m3_from_float(x: float) -> int:
+    """The oracle's E4M3 code of an FP32 value: nearest, ties to even,
+    saturating to +-448, NaN to S.1111.111."""
+    return int(_load().oracle_e4m3_from_float(float(x)))
+
+
+def kv_append(k_new, v_new, slot_mapping, layer_base_rows, k_cache, v_cache, k_scale=1.0, v_scale=1.0):
+    """KV-cache append ("Writing Page Attention with PyPTO", section 4.3): row
+    (b, t) of k_new / v_new [B, q_len, Hkv, D] (bfloat16) goes to token row
+    layer_base_rows + max(slot_mapping[b * q_len + t], 0) of the caches
+    [pages, ps, Hkv, D] (bfloat16, or float8_e4m3fn taking x / scale).
+    Returns updated copies (k_cache, v_cache); the inputs are not modified."""
+    lib = _load()
+    k_new, v_new = _bf16(k_new), _bf16(v_new)
+    kv8 = k_cache.dtype == torch.float8_e4m3fn
+    kc = k_cache.detach().cpu().clone()
+    vc = v_cache.detach().cpu().clone()
+    if kv8:
+        kc_raw, vc_raw = kc.view(torch.uint8), vc.view(torch.uint8)
+    else:
+        kc_raw, vc_raw = _bf16(kc), _bf16(vc)
+    B, q_len, Hkv, Dk = k_new.shape
+    Dv = v_new.shape[3]
+    P, ps = kc.shape[0], kc.shape[1]
+    sm = _i32(slot_mapping).reshape(-1)
+    assert sm.size == B * q_len
+    kns, vns, ks, vs = _strides(k_new), _strides(v_new), _strides(kc_raw), _strides(vc_raw)
+    rc = lib.oracle_kv_append(k_new.data_ptr(), kns.ctypes.data, v_new.data_ptr(), vns.ctypes.data,
+                              sm.ctypes.data, int(layer_base_rows), kc_raw.data_ptr(), ks.ctypes.data,
+                              vc_raw.data_ptr(), vs.ctypes.data, int(kv8), float(k_scale), float(v_scale),
+                              B, q_len, Hkv, Dk, Dv, ps, P)
+    if rc != 0:
+        raise ValueError(f"oracle_kv_append failed with code {rc}")
+    return kc, vc
 
 
 def varlen_prefill(q, k, v, cu_seqlens_q, cu_seqlens_k, causal, scale, rows=None, threads=None):

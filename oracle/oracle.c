@@ -377,3 +377,70 @@ int oracle_varlen_prefill(const uint16_t *q, const int64_t *q_stride,
     free(jobs); free(tid);
     return status;
 }
+
+/* ------------------------------------------------------------------ append
+ *
+ * KV-cache append ("Writing Page Attention with PyPTO", sections 4.2-4.3):
+ * the K and V rows of query token t of batch row b go to cache token row
+ *   layer_base + max(slot_mapping[b * q_len + t], 0)
+ * -- the warm-up slot -1 is clamped to 0 before the layer base is added, so a
+ * layer never writes into the previous layer's last row.  Token row r lives
+ * at page r / ps, slot r % ps of a [pages, ps, Hkv, D] cache.  A BF16 cache
+ * takes the BF16 bits unchanged.  An E4M3 cache takes the code of the FP32
+ * quotient x / scale (IEEE single-precision division) rounded to the nearest
+ * E4M3 value, ties to an even code, finite overflow saturating to +-448, NaN
+ * to S.1111.111 -- the plain reading of "FP8 inputs" with one scale per cache
+ * ("TokenSpeed-MLA 2.0.1", decode).  Writes go in (b, t) order; rows that
+ * several tokens address (repeated warm-up slots) keep the last one.
+ */
+uint8_t oracle_e4m3_from_float(float x) {
+    if (isnan(x)) return signbit(x) ? 0xFF : 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0;
+    double a = fabs((double)x);
+    if (a >= 448.0) return sign | 0x7E;
+    int best = 0;
+    double best_d = INFINITY;
+    for (int code = 0; code <= 0x7E; ++code) {        /* every finite non-negative code */
+        double d = fabs(oracle_e4m3_to_double((uint8_t)code) - a);
+        if (d < best_d || (d == best_d && (code & 1) == 0)) { best = code; best_d = d; }
+    }
+    return sign | (uint8_t)best;
+}
+
+int oracle_kv_append(const uint16_t *k_new, const int64_t *kn_stride,
+                     const uint16_t *v_new, const int64_t *vn_stride,
+                     const int32_t *slot_mapping, int64_t layer_base,
+                     void *k_cache, const int64_t *k_stride,
+                     void *v_cache, const int64_t *v_stride,
+                     int kv8, float k_scale, float v_scale,
+                     int B, int q_len, int Hkv, int Dk, int Dv, int ps, int64_t num_pages) {
+    for (int b = 0; b < B; ++b) {
+        for (int t = 0; t < q_len; ++t) {
+            int64_t slot = slot_mapping[(int64_t)b * q_len + t];
+            if (slot < 0) slot = 0;                      /* clamp first ... */
+            int64_t row = layer_base + slot;             /* ... then add the layer base */
+            if (row < 0 || row >= num_pages * ps) return -1;
+            int64_t page = row / ps, off = row % ps;
+            for (int h = 0; h < Hkv; ++h) {
+                for (int pass = 0; pass < 2; ++pass) {
+                    const uint16_t *src = pass ? v_new : k_new;
+                    const int64_t *ss = pass ? vn_stride : kn_stride;
+                    const int64_t *cs = pass ? v_stride : k_stride;
+                    int D = pass ? Dv : Dk;
+                    float sc = pass ? v_scale : k_scale;
+                    for (int d = 0; d < D; ++d) {
+                        uint16_t bits = src[b * ss[0] + t * ss[1] + h * ss[2] + d * ss[3]];
+                        int64_t at = page * cs[0] + off * cs[1] + (int64_t)h * cs[2] + (int64_t)d * cs[3];
+                        if (kv8) {
+                            float x = (float)bf16_to_double(bits);
+                            ((uint8_t *)(pass ? v_cache : k_cache))[at] = oracle_e4m3_from_float(x / sc);
+                        } else {
+                            ((uint16_t *)(pass ? v_cache : k_cache))[at] = bits;
+                        }
+                    }
+                }
+            }
+        }
+    }
+    return 0;
+}

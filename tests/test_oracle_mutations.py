@@ -29,6 +29,9 @@ MUTATIONS = {
     "fp8_value_scale_dropped": ("out[d] += p * (v_scale * oracle_e4m3_to_double", "out[d] += p * (oracle_e4m3_to_double"),
     "fp8_exponent_bias_off": ("else v = ldexp(1.0 + m / 8.0, e - 7);", "else v = ldexp(1.0 + m / 8.0, e - 8);"),
     "window_off_by_one": ("first = visible - 1 - J->window_left;", "first = visible - J->window_left;"),
+    "append_clamp_after_base": ("if (slot < 0) slot = 0;                      /* clamp first ... */\n            int64_t row = layer_base + slot;",
+                                "int64_t row = layer_base + slot;\n            if (row < 0) row = 0;"),
+    "append_fp8_scale_multiplied": ("oracle_e4m3_from_float(x / sc)", "oracle_e4m3_from_float(x * sc)"),
 }
 
 PIN_CHECKS = [
@@ -43,6 +46,8 @@ PIN_CHECKS = [
     lambda: pins.test_fp8_kv_decode_matches_sdpa_on_dequantized_copy(1, (5, 1, 13)),
     lambda: pins.test_window_matches_sdpa_on_dense_copy(2, (9, 30, 2), 4, 7),
     pins.test_window_zero_sees_own_position_only,
+    pins.test_warmup_slot_is_clamped_before_the_layer_base,
+    lambda: pins.test_append_changes_only_the_addressed_rows(True),
 ]
 
 
@@ -64,7 +69,7 @@ def test_pins_catch_mutant(tmp_path, monkeypatch, name):
     real = oracle._lib
     mutant = ctypes.CDLL(lib_path)
     for fn in ("oracle_paged_decode", "oracle_paged_decode_kv8", "oracle_paged_decode_window", "oracle_e4m3_to_double",
-               "oracle_varlen_prefill"):
+               "oracle_varlen_prefill", "oracle_e4m3_from_float", "oracle_kv_append"):
         getattr(mutant, fn).restype = getattr(real, fn).restype
         getattr(mutant, fn).argtypes = getattr(real, fn).argtypes
     monkeypatch.setattr(oracle, "_lib", mutant)

@@ -649,3 +649,103 @@ def test_window_never_reads_pages_before_it():
     o1, l1 = oracle.paged_decode(inp["q"], kc, vc, bt, inp["seq_lens"], inp["scale"], window_left=W)
     np.testing.assert_array_equal(o0, o1)
     np.testing.assert_array_equal(l0, l1)
+
+
+# ----------------------------------------------------------------- KV append
+# "Writing Page Attention with PyPTO", section 4.3: row (b, t) goes to cache
+# token row layer_base + max(slot, 0); a cache canary shows only those rows
+# change (section 10.2).
+
+def test_e4m3_encoding_round_trips_every_code_and_matches_torch():
+    for code in range(256):
+        if (code & 0x7F) == 0x7F:
+            continue                                  # NaN patterns
+        x = oracle.e4m3_to_double(code)
+        assert oracle.e4m3_from_float(x) == code, hex(code)
+    g = torch.Generator().manual_seed(3)
+    xs = torch.cat([torch.randn(4000, generator=g) * 40, torch.randn(1000, generator=g) * 0.01])
+    # midpoints between neighbouring codes: ties go to the even code
+    mids = [(oracle.e4m3_to_double(c) + oracle.e4m3_to_double(c + 1)) / 2 for c in range(0, 0x7E)]
+    xs = torch.cat([xs, torch.tensor(mids, dtype=torch.float32), -torch.tensor(mids, dtype=torch.float32)])
+    ref = xs.to(torch.float8_e4m3fn).view(torch.uint8)
+    for x, r in zip(xs.tolist(), ref.tolist()):
+        assert oracle.e4m3_from_float(x) == r, x
+    for x, code in ((448.0, 0x7E), (460.0, 0x7E), (1e30, 0x7E), (float("inf"), 0x7E), (-1e30, 0xFE)):
+        assert oracle.e4m3_from_float(x) == code
+
+
+def _append_case(q_len=2, fp8=False, seed=5):
+    wl, inp = tiny_decode(batch=3, q_len=q_len, hq=8, hkv=2, d=32, ps=4, lens=(7, 12, 5), seed=seed)
+    g = torch.Generator().manual_seed(seed + 100)
+    k_new = torch.randn(3, q_len, 2, 32, generator=g).to(torch.bfloat16)
+    v_new = torch.randn(3, q_len, 2, 32, generator=g).to(torch.bfloat16)
+    kc, vc = inp["k_cache"], inp["v_cache"]
+    if fp8:
+        kc = (kc.float().nan_to_num(0.0) / 0.05).clamp(-448, 448).to(torch.float8_e4m3fn)
+        vc = (vc.float().nan_to_num(0.0) / 0.05).clamp(-448, 448).to(torch.float8_e4m3fn)
+    return wl, inp, k_new, v_new, kc, vc
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_append_changes_only_the_addressed_rows(fp8):
+    wl, inp, k_new, v_new, kc, vc = _append_case(fp8=fp8)
+    ps, P = kc.shape[1], kc.shape[0]
+    slots = torch.tensor([3, 17, 20, 9, 30, 1], dtype=torch.int32)
+    kc2, vc2 = oracle.kv_append(k_new, v_new, slots, 4, kc, vc, k_scale=0.05, v_scale=0.05)
+    raw = (lambda t: t.view(torch.uint8)) if fp8 else (lambda t: t.view(torch.int16))
+    changed = (raw(kc2) != raw(kc)).flatten(2).any(-1) | (raw(vc2) != raw(vc)).flatten(2).any(-1)
+    rows = {int(4 + s) for s in slots}
+    for page in range(P):
+        for off in range(ps):
+            if page * ps + off not in rows:
+                assert not changed[page, off].any(), (page, off)
+    for i, s in enumerate(slots.tolist()):
+        b, t = divmod(i, wl.q_len)
+        page, off = divmod(4 + s, ps)
+        if fp8:
+            want_k = (k_new[b, t].float() / 0.05).to(torch.float8_e4m3fn).view(torch.uint8)
+            assert torch.equal(kc2[page, off].view(torch.uint8), want_k)
+        else:
+            assert torch.equal(kc2[page, off], k_new[b, t])
+            assert torch.equal(vc2[page, off], v_new[b, t])
+
+
+def test_warmup_slot_is_clamped_before_the_layer_base():
+    """Slot -1 with a nonzero layer base writes the layer's row 0, never the
+    previous layer's last row (section 4.3 and the test note of section 10.2)."""
+    wl, inp, k_new, v_new, kc, vc = _append_case(q_len=1)
+    base = 8
+    slots = torch.tensor([-1, 5, -1], dtype=torch.int32)
+    kc2, vc2 = oracle.kv_append(k_new, v_new, slots, base, kc, vc)
+    ps = kc.shape[1]
+    prev_page, prev_off = divmod(base - 1, ps)
+    assert torch.equal(kc2[prev_page, prev_off].view(torch.int16), kc[prev_page, prev_off].view(torch.int16))
+    page, off = divmod(base, ps)
+    assert torch.equal(kc2[page, off], k_new[2, 0])     # the last of the two -1 writers
+    page, off = divmod(base + 5, ps)
+    assert torch.equal(vc2[page, off], v_new[1, 0])
+
+
+def test_append_then_decode_matches_sdpa_with_the_new_keys():
+    """New tokens appended at each row's last q_len positions are the keys the
+    decode then attends to: equal to SDPA on the dense copy with those rows."""
+    wl, inp, k_new, v_new, kc, vc = _append_case(q_len=2, seed=9)
+    ps = kc.shape[1]
+    lens = inp["seq_lens"]
+    slots = []
+    for b in range(wl.batch):
+        for t in range(wl.q_len):
+            pos = int(lens[b]) - wl.q_len + t
+            slots.append(int(inp["block_table"][b, pos // ps]) * ps + pos % ps)
+    kc2, vc2 = oracle.kv_append(k_new, v_new, torch.tensor(slots, dtype=torch.int32), 0, kc, vc)
+    inp2 = dict(inp)
+    inp2["k_cache"], inp2["v_cache"] = kc2, vc2
+    out, lse = oracle.paged_decode(inp2["q"], kc2, vc2, inp["block_table"], lens, inp["scale"])
+    for b in range(wl.batch):
+        ref_o, ref_l = sdpa_decode_reference(inp2, b)
+        k_dense, _ = dense_kv(inp2, b)
+        n = int(lens[b])
+        assert torch.equal(k_dense[n - wl.q_len:], k_new[b])
+        rows = slice(b * wl.q_len * wl.num_q_heads, (b + 1) * wl.q_len * wl.num_q_heads)
+        np.testing.assert_allclose(out[rows], ref_o, atol=1e-12)
+        np.testing.assert_allclose(lse[rows], ref_l, atol=1e-12)
