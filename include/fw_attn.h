@@ -193,6 +193,65 @@ fw_status_t fw_paged_decode_window(const fw_tensor_t *q, const fw_tensor_t *k_ca
                                    fw_stream_t stream);
 
 /*
+ * KV-cache append ("Writing Page Attention with PyPTO", sections 4.2-4.3).
+ *
+ *   k_new, v_new  [B, q_len, Hkv, D]   BF16, last dim contiguous, strides
+ *                                      multiples of 8 elements, 16-byte aligned;
+ *                                      v_new may be NULL together with v_cache
+ *                                      (a latent cache whose values are a view
+ *                                      of its keys)
+ *   slot_mapping  [B * q_len] or [B, q_len]  I32, contiguous; the token row of
+ *                                      each new token inside its layer; -1 marks
+ *                                      a warm-up token
+ *   layer_base_rows   first token row of the layer in the (possibly packed
+ *                     multi-layer) cache, 0 <= layer_base_rows < pages * ps
+ *   k_cache, v_cache  [pages, ps, Hkv, D]  BF16 or FP8_E4M3 (both the same);
+ *                     written
+ *   k_scale, v_scale  FP8 caches: the stored code is E4M3(x / scale) -- IEEE
+ *                     single-precision division, nearest with ties to even,
+ *                     finite overflow saturating to +-448; 1 for BF16 caches
+ *                     (which take the BF16 bits unchanged).
+ *
+ * Token (b, t), KV head h goes to token row
+ *   r = layer_base_rows + max(slot_mapping[b * q_len + t], 0),
+ * page r / ps, slot r % ps: the warm-up slot -1 is clamped to 0 before the
+ * layer base is added, so a layer never writes the previous layer's last row.
+ * Nothing else in the caches changes.  Tokens sharing a row (repeated
+ * warm-up slots) race: each 16-byte group of that row (8 BF16 or 8 E4M3
+ * values of one head) ends up holding one of theirs.  A row at
+ * or past pages * ps records FW_ERR_INVALID_ARG in the device status word
+ * and is skipped.  One launch; no workspace.
+ */
+fw_status_t fw_kv_append(const fw_tensor_t *k_new, const fw_tensor_t *v_new, const fw_tensor_t *slot_mapping,
+                         int64_t layer_base_rows, fw_tensor_t *k_cache, fw_tensor_t *v_cache, float k_scale,
+                         float v_scale, fw_stream_t stream);
+
+/*
+ * Append the new tokens, then decode: fw_kv_append followed by
+ * fw_paged_decode_window on the layer, with the append folded into the
+ * decode's plan launch (no extra launch; the attention launch starts after
+ * it, so it reads the new rows).
+ *
+ *   k_cache, v_cache  the (packed) caches of fw_kv_append; the attention reads
+ *                     the layer's pages, pages layer_base_rows / ps onward, so
+ *                     block_table entries count pages from the layer's first
+ *                     page and layer_base_rows must be a multiple of ps
+ *   q, block_table, seq_lens, scale, k_scale, v_scale, window_left, out, lse:
+ *                     as fw_paged_decode_window (seq_lens include the new
+ *                     tokens, which normally occupy each row's last q_len
+ *                     positions)
+ *
+ * Supported: the grouped-query layouts (BF16 Dk = Dv in {128, 256}, FP8 128);
+ * the latent layout returns FW_ERR_UNSUPPORTED (append it with fw_kv_append).
+ */
+fw_status_t fw_paged_decode_append(const fw_tensor_t *q, const fw_tensor_t *k_new, const fw_tensor_t *v_new,
+                                   const fw_tensor_t *slot_mapping, int64_t layer_base_rows,
+                                   fw_tensor_t *k_cache, fw_tensor_t *v_cache,
+                                   const fw_tensor_t *block_table, const fw_tensor_t *seq_lens, float scale,
+                                   float k_scale, float v_scale, int32_t window_left,
+                                   fw_tensor_t *out, fw_tensor_t *lse, fw_stream_t stream);
+
+/*
  * Workspace bytes fw_paged_decode needs for these shapes (data pointers are
  * not read).  Writes the size to *bytes.  It holds the tile prefix table
  * (B + 3 int32) and rows * max_pieces * (Dv + 1) * 4 bytes of partials, with

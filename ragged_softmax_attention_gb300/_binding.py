@@ -68,6 +68,11 @@ def load_library(path: Optional[str] = None):
     lib.fw_paged_decode_window.restype = ctypes.c_int
     lib.fw_paged_decode_window.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                            ctypes.c_int32, P, P, ctypes.c_void_p]
+    lib.fw_kv_append.restype = ctypes.c_int
+    lib.fw_kv_append.argtypes = [P, P, P, ctypes.c_int64, P, P, ctypes.c_float, ctypes.c_float, ctypes.c_void_p]
+    lib.fw_paged_decode_append.restype = ctypes.c_int
+    lib.fw_paged_decode_append.argtypes = [P, P, P, P, ctypes.c_int64, P, P, P, P, ctypes.c_float, ctypes.c_float,
+                                           ctypes.c_float, ctypes.c_int32, P, P, ctypes.c_void_p]
     lib.fw_paged_decode_fp8.restype = ctypes.c_int
     lib.fw_paged_decode_fp8.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_float, ctypes.c_float, P, P,
                                         ctypes.c_void_p]
@@ -180,6 +185,40 @@ def paged_decode_window(q, k_cache, v_cache, block_table, seq_lens, scale, windo
     _check(lib.fw_paged_decode_window(*[_ref(a) for a in args], ctypes.c_float(scale), ctypes.c_float(k_scale),
                                       ctypes.c_float(v_scale), ctypes.c_int32(window_left), _ref(fo), _ref(fl),
                                       _stream_handle(stream)))
+    return out, lse
+
+
+def kv_append(k_new, v_new, slot_mapping, layer_base_rows, k_cache, v_cache, k_scale=1.0, v_scale=1.0, stream=None):
+    """fw_kv_append: token (b, t) of k_new / v_new [B, q_len, Hkv, D] (bf16) goes
+    to cache token row layer_base_rows + max(slot_mapping[b * q_len + t], 0) of
+    k_cache / v_cache [pages, ps, Hkv, D] (bf16, or float8_e4m3fn storing
+    E4M3(x / scale)); the caches are written in place.  v_new and v_cache may
+    both be None."""
+    lib = load_library()
+    t = [as_fw_tensor(x) if x is not None else None for x in (k_new, v_new, slot_mapping, k_cache, v_cache)]
+    _check(lib.fw_kv_append(_ref(t[0]), _ref(t[1]), _ref(t[2]), ctypes.c_int64(layer_base_rows), _ref(t[3]),
+                            _ref(t[4]), ctypes.c_float(k_scale), ctypes.c_float(v_scale), _stream_handle(stream)))
+
+
+def paged_decode_append(q, k_new, v_new, slot_mapping, layer_base_rows, k_cache, v_cache, block_table, seq_lens,
+                        scale, k_scale=1.0, v_scale=1.0, window_left=-1, out=None, lse=None, return_lse=True,
+                        stream=None):
+    """fw_paged_decode_append: kv_append into the (packed) caches, then the
+    decode of the layer whose pages start at layer_base_rows / ps (block_table
+    counts from there).  Returns (out, lse)."""
+    lib = load_library()
+    B, q_len, Hq, _ = q.shape
+    Dv = v_cache.shape[3]
+    if out is None:
+        out = torch.empty((B, q_len, Hq, Dv), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, q_len, Hq), dtype=torch.float32, device=q.device)
+    t = [as_fw_tensor(x) for x in (q, k_new, v_new, slot_mapping, k_cache, v_cache, block_table, seq_lens)]
+    fo, fl = as_fw_tensor(out), as_fw_tensor(lse)
+    _check(lib.fw_paged_decode_append(_ref(t[0]), _ref(t[1]), _ref(t[2]), _ref(t[3]), ctypes.c_int64(layer_base_rows),
+                                      _ref(t[4]), _ref(t[5]), _ref(t[6]), _ref(t[7]), ctypes.c_float(scale),
+                                      ctypes.c_float(k_scale), ctypes.c_float(v_scale), ctypes.c_int32(window_left),
+                                      _ref(fo), _ref(fl), _stream_handle(stream)))
     return out, lse
 
 

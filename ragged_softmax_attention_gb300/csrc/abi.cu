@@ -403,6 +403,88 @@ fw_status_t fw_paged_decode_workspace_size(const fw_tensor_t *q, const fw_tensor
     return ok();
 }
 
+// Host side of a KV-cache append: the new rows, their slots, the layer base.
+struct AppendArgs {
+    const fw_tensor_t *k_new, *v_new, *slot_mapping;
+    int64_t layer_base_rows;
+};
+
+// Validates an append into [pages, ps, Hkv, D] caches and fills the kernel's
+// parameters ("Writing Page Attention with PyPTO", section 4.3).
+static fw_status_t build_append(const AppendArgs &aa, const fw_tensor_t *k_cache, const fw_tensor_t *v_cache,
+                                float k_scale, float v_scale, fw::AppendParams *ap) {
+    if (!k_cache) return fail(FW_ERR_INVALID_ARG, "k_cache is NULL");
+    const bool kv8 = k_cache->dtype == FW_FP8_E4M3;
+    if (!kv8 && k_cache->dtype != FW_BF16) return fail(FW_ERR_INVALID_ARG, "caches must be BF16 or FP8_E4M3");
+    if (fw_status_t s = check_tensor(k_cache, "k_cache", 4, k_cache->dtype)) return s;
+    if (fw_status_t s = check_tensor(aa.k_new, "k_new", 4, FW_BF16)) return s;
+    if ((aa.v_new == nullptr) != (v_cache == nullptr))
+        return fail(FW_ERR_INVALID_ARG, "v_new and v_cache go together (both or neither)");
+    if (v_cache) {
+        if (fw_status_t s = check_tensor(v_cache, "v_cache", 4, k_cache->dtype)) return s;
+        if (fw_status_t s = check_tensor(aa.v_new, "v_new", 4, FW_BF16)) return s;
+    }
+    const fw_tensor_t *sm = aa.slot_mapping;
+    if (!sm || sm->dtype != FW_I32 || sm->ndim < 1 || sm->ndim > 2)
+        return fail(FW_ERR_INVALID_ARG, "slot_mapping must be an I32 [B * q_len] or [B, q_len] tensor");
+    const int64_t B = aa.k_new->shape[0], q_len = aa.k_new->shape[1], Hkv = aa.k_new->shape[2];
+    const int64_t Dk = aa.k_new->shape[3];
+    const int64_t P = k_cache->shape[0], ps = k_cache->shape[1];
+    const int64_t sm_n = sm->ndim == 1 ? sm->shape[0] : sm->shape[0] * sm->shape[1];
+    const bool sm_contig = sm->ndim == 1 ? (sm->shape[0] <= 1 || sm->stride[0] == 1)
+                                         : ((sm->shape[1] <= 1 || sm->stride[1] == 1) &&
+                                            (sm->shape[0] <= 1 || sm->stride[0] == sm->shape[1]));
+    if (sm_n != B * q_len || !sm_contig || (sm_n > 0 && !sm->data))
+        return fail(FW_ERR_INVALID_ARG, "slot_mapping must hold B * q_len contiguous entries");
+    if (k_cache->shape[2] != Hkv || k_cache->shape[3] != Dk)
+        return fail(FW_ERR_INVALID_ARG, "k_new [B, q_len, Hkv, D] does not match k_cache [pages, ps, Hkv, D]");
+    int64_t Dv = 0;
+    if (v_cache) {
+        Dv = aa.v_new->shape[3];
+        if (aa.v_new->shape[0] != B || aa.v_new->shape[1] != q_len || aa.v_new->shape[2] != Hkv ||
+            v_cache->shape[0] != P || v_cache->shape[1] != ps || v_cache->shape[2] != Hkv || v_cache->shape[3] != Dv)
+            return fail(FW_ERR_INVALID_ARG, "v_new / v_cache shapes do not match k_new / k_cache");
+    }
+    if (Dk < 8 || Dk % 8 || (v_cache && (Dv < 8 || Dv % 8)))
+        return fail(FW_ERR_UNSUPPORTED, "appended head dims must be positive multiples of 8");
+    if (P < 1 || ps < 1) return fail(FW_ERR_INVALID_ARG, "empty cache");
+    if (aa.layer_base_rows < 0 || aa.layer_base_rows >= P * ps)
+        return fail(FW_ERR_INVALID_ARG, "layer_base_rows %lld outside the cache's %lld token rows",
+                    (long long)aa.layer_base_rows, (long long)(P * ps));
+    if (kv8 && !(std::isfinite(k_scale) && std::isfinite(v_scale) && k_scale > 0.f && v_scale > 0.f))
+        return fail(FW_ERR_INVALID_ARG, "k_scale and v_scale must be finite and positive");
+    if (!kv8 && (k_scale != 1.f || v_scale != 1.f))
+        return fail(FW_ERR_INVALID_ARG, "k_scale and v_scale must be 1 for BF16 caches");
+    if (B * q_len > 0) {
+        if (fw_status_t s = check_tma_layout(aa.k_new, "k_new")) return s;
+        if (fw_status_t s = check_tma_layout(k_cache, "k_cache")) return s;
+        if (v_cache) {
+            if (fw_status_t s = check_tma_layout(aa.v_new, "v_new")) return s;
+            if (fw_status_t s = check_tma_layout(v_cache, "v_cache")) return s;
+        }
+    }
+    fw::AppendParams a{};
+    a.rows = B * q_len * Hkv;
+    a.q_len = (int)q_len; a.Hkv = (int)Hkv; a.Dk = (int)Dk; a.Dv = (int)Dv; a.ps = (int)ps;
+    a.kv8 = kv8 ? 1 : 0;
+    a.k_scale = k_scale; a.v_scale = v_scale;
+    a.k_new = static_cast<const uint16_t *>(aa.k_new->data);
+    a.v_new = v_cache ? static_cast<const uint16_t *>(aa.v_new->data) : nullptr;
+    for (int i = 0; i < 3; ++i) {
+        a.kn_stride[i] = aa.k_new->stride[i];
+        a.vn_stride[i] = v_cache ? aa.v_new->stride[i] : 0;
+        a.kc_stride[i] = k_cache->stride[i];
+        a.vc_stride[i] = v_cache ? v_cache->stride[i] : 0;
+    }
+    a.slot_mapping = static_cast<const int32_t *>(sm->data);
+    a.layer_base = aa.layer_base_rows;
+    a.cache_rows = P * ps;
+    a.k_cache = k_cache->data;
+    a.v_cache = v_cache ? v_cache->data : nullptr;
+    *ap = a;
+    return FW_OK;
+}
+
 // Shared body of the decode entry points.  `fixed_ws` selects where the
 // scratch comes from: nullptr = the workspace fw_set_workspace() set or the
 // internal buffer (fw_paged_decode); otherwise that device range of
@@ -412,8 +494,28 @@ static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_
                                      fw_tensor_t *out, fw_tensor_t *lse, fw_stream_t stream_,
                                      void *(*fixed_ws)(DeviceState *, fw_status_t *), size_t fixed_bytes,
                                      bool kv8 = false, float k_scale = 1.f, float v_scale = 1.f,
-                                     int32_t window_left = -1, bool any_cache = false) {
+                                     int32_t window_left = -1, bool any_cache = false,
+                                     const AppendArgs *append = nullptr) {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    // A fused append writes the packed cache at layer_base + max(slot, 0); the
+    // attention then reads the layer's pages, a view from layer_base on.
+    fw::AppendParams app{};
+    fw_tensor_t k_view, v_view;
+    if (append) {
+        if (fw_status_t s = build_append(*append, k_cache, v_cache, k_scale, v_scale, &app)) return s;
+        if (append->layer_base_rows % k_cache->shape[1] != 0)
+            return fail(FW_ERR_INVALID_ARG, "layer_base_rows must be a multiple of the page size");
+        const int64_t first_page = append->layer_base_rows / k_cache->shape[1];
+        const int64_t esz = k_cache->dtype == FW_FP8_E4M3 ? 1 : 2;
+        k_view = *k_cache;
+        v_view = *v_cache;
+        k_view.data = static_cast<char *>(k_cache->data) + first_page * k_cache->stride[0] * esz;
+        v_view.data = static_cast<char *>(v_cache->data) + first_page * v_cache->stride[0] * esz;
+        k_view.shape[0] -= first_page;
+        v_view.shape[0] -= first_page;
+        k_cache = &k_view;
+        v_cache = &v_view;
+    }
     if (fw_status_t s = decode_shapes(q, k_cache, v_cache, block_table)) return s;
     if (any_cache) kv8 = k_cache->dtype == FW_FP8_E4M3;
     if (kv8 != (k_cache->dtype == FW_FP8_E4M3))
@@ -441,6 +543,9 @@ static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_
     const bool latent = !kv8 && (Dk == 576 && Dv == 512);
     if (latent && window_left >= 0)
         return fail(FW_ERR_UNSUPPORTED, "sliding windows are served for Dk = Dv in {128, 256} (BF16) and 128 (FP8)");
+    if (latent && append)
+        return fail(FW_ERR_UNSUPPORTED, "the fused append serves the grouped-query layouts (append latent rows "
+                    "with fw_kv_append)");
     if (kv8 && !(Dk == 128 && Dv == 128))
         return fail(FW_ERR_UNSUPPORTED, "FP8 decode head dims (Dk=%lld, Dv=%lld): supported Dk = Dv = 128",
                     (long long)Dk, (long long)Dv);
@@ -499,6 +604,7 @@ static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_
     p.grid = pl.grid;
     p.Dv = (int)Dv;
     p.window_left = window_left;
+    p.app = app;
     p.block_table = static_cast<const int32_t *>(block_table->data);
     p.bt_stride = block_table->stride[0];
     p.seq_lens = static_cast<const int32_t *>(seq_lens->data);
@@ -578,6 +684,34 @@ fw_status_t fw_paged_decode_fp8(const fw_tensor_t *q, const fw_tensor_t *k_cache
                                 fw_stream_t stream) {
     return paged_decode_impl(q, k_cache, v_cache, block_table, seq_lens, scale, out, lse, stream, nullptr, 0,
                              true, k_scale, v_scale);
+}
+
+fw_status_t fw_paged_decode_append(const fw_tensor_t *q, const fw_tensor_t *k_new, const fw_tensor_t *v_new,
+                                   const fw_tensor_t *slot_mapping, int64_t layer_base_rows, fw_tensor_t *k_cache,
+                                   fw_tensor_t *v_cache, const fw_tensor_t *block_table,
+                                   const fw_tensor_t *seq_lens, float scale, float k_scale, float v_scale,
+                                   int32_t window_left, fw_tensor_t *out, fw_tensor_t *lse, fw_stream_t stream) {
+    if (!k_cache || !v_cache || !k_new || !v_new) return fail(FW_ERR_INVALID_ARG, "caches and new rows are required");
+    const AppendArgs aa{k_new, v_new, slot_mapping, layer_base_rows};
+    return paged_decode_impl(q, k_cache, v_cache, block_table, seq_lens, scale, out, lse, stream, nullptr, 0,
+                             false, k_scale, v_scale, window_left, true, &aa);
+}
+
+fw_status_t fw_kv_append(const fw_tensor_t *k_new, const fw_tensor_t *v_new, const fw_tensor_t *slot_mapping,
+                         int64_t layer_base_rows, fw_tensor_t *k_cache, fw_tensor_t *v_cache, float k_scale,
+                         float v_scale, fw_stream_t stream_) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    const AppendArgs aa{k_new, v_new, slot_mapping, layer_base_rows};
+    fw::AppendParams app{};
+    if (fw_status_t s = build_append(aa, k_cache, v_cache, k_scale, v_scale, &app)) return s;
+    if (app.rows == 0) return ok();
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState *d = nullptr;
+    if (fw_status_t s = device_state(&d)) return s;
+    cudaError_t e = fw::launch_kv_append(app, d->status, stream);
+    if (e != cudaSuccess) return fail(FW_ERR_CUDA, "append launch: %s", cudaGetErrorString(e));
+    g_launches.fetch_add(1);
+    return ok();
 }
 
 fw_status_t fw_paged_decode_window(const fw_tensor_t *q, const fw_tensor_t *k_cache, const fw_tensor_t *v_cache,

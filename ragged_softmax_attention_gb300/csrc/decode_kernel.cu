@@ -31,6 +31,7 @@
 // s_full/s_free, p_full/p_free, pv_done -- the READY events of PyPTO
 // section 8.3 with the double-buffered S and P slots playing its ring.
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include "decode_common.cuh"
 #include "fw_internal.h"
@@ -495,6 +496,70 @@ cudaError_t launch_t(const DecodeParams &p, const CUtensorMap &tq, const CUtenso
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------- append
+//
+// One warp per (b, t, kv head) row: 16-byte loads of eight BF16 values,
+// stored as they are or as eight E4M3 codes of x / scale (IEEE division,
+// round to nearest even, saturating: the conversion instruction's
+// satfinite form).  A slot whose row falls outside the cache records
+// FW_ERR_INVALID_ARG and writes nothing.
+
+__device__ void append_rows(const AppendParams &a, int block, int nblocks, int *status) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wpb = blockDim.x >> 5;
+    for (int64_t r = (int64_t)block * wpb + warp; r < a.rows; r += (int64_t)nblocks * wpb) {
+        const int h = (int)(r % a.Hkv);
+        const int64_t bt = r / a.Hkv;                    // b * q_len + t
+        const int t = (int)(bt % a.q_len);
+        const int64_t b = bt / a.q_len;
+        int64_t slot = __ldg(a.slot_mapping + bt);
+        if (slot < 0) slot = 0;                          // clamp before adding the layer base
+        const int64_t row = a.layer_base + slot;
+        if (row >= a.cache_rows) {
+            if (lane == 0) record_error(status, 1 /* FW_ERR_INVALID_ARG */);
+            continue;
+        }
+        const int64_t page = row / a.ps, off = row % a.ps;
+#pragma unroll 1
+        for (int pass = 0; pass < 2; ++pass) {
+            const uint16_t *src = pass ? a.v_new : a.k_new;
+            if (!src) break;
+            const int64_t *ss = pass ? a.vn_stride : a.kn_stride;
+            const int64_t *cs = pass ? a.vc_stride : a.kc_stride;
+            const int D = pass ? a.Dv : a.Dk;
+            const float sc = pass ? a.v_scale : a.k_scale;
+            const uint16_t *srow = src + b * ss[0] + t * ss[1] + h * ss[2];
+            const int64_t dst = page * cs[0] + off * cs[1] + h * cs[2];
+            for (int d = lane * 8; d < D; d += 256) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(srow + d);
+                if (a.kv8) {
+                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                    uint32_t out[2];
+#pragma unroll
+                    for (int e = 0; e < 4; e += 2) {
+                        const float x0 = __fdiv_rn(__uint_as_float(w[e] << 16), sc);
+                        const float x1 = __fdiv_rn(__uint_as_float(w[e] & 0xffff0000u), sc);
+                        const float x2 = __fdiv_rn(__uint_as_float(w[e + 1] << 16), sc);
+                        const float x3 = __fdiv_rn(__uint_as_float(w[e + 1] & 0xffff0000u), sc);
+                        const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
+                        const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(x2, x3), __NV_SATFINITE, __NV_E4M3);
+                        out[e >> 1] = lo | (hi << 16);
+                    }
+                    uint8_t *base = static_cast<uint8_t *>(pass ? a.v_cache : a.k_cache);
+                    *reinterpret_cast<uint2 *>(base + dst + d) = make_uint2(out[0], out[1]);
+                } else {
+                    uint16_t *base = static_cast<uint16_t *>(pass ? a.v_cache : a.k_cache);
+                    *reinterpret_cast<uint4 *>(base + dst + d) = v;
+                }
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256) kv_append_kernel(const __grid_constant__ AppendParams a, int *status) {
+    append_rows(a, blockIdx.x, gridDim.x, status);
+}
+
 // ------------------------------------------------------------------- plan
 //
 // One block: exclusive prefix PB[b] of the KV tiles each batch row puts in
@@ -503,6 +568,10 @@ cudaError_t launch_t(const DecodeParams &p, const CUtensorMap &tq, const CUtenso
 // T and the range span; rows with no keys get their zero output and -inf LSE
 // here, since no range ever covers them.
 __global__ void __launch_bounds__(1024) decode_plan_kernel(const __grid_constant__ DecodeParams p) {
+    if (blockIdx.x > 0) {                            // the launch's extra blocks append the new tokens
+        append_rows(p.app, blockIdx.x - 1, gridDim.x - 1, p.status);
+        return;
+    }
     __shared__ int warp_sums[32];
     __shared__ int carry_s;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -631,8 +700,23 @@ size_t decode_smem_bytes(int head_dim, int rows) {
     return rows == 16 ? DecodeCfg<256, 16>::kSmemBytes : DecodeCfg<256, 32>::kSmemBytes;
 }
 
+// Blocks of 32 warps that cover the append rows (at most 64 blocks; each
+// warp walks rows with the grid's stride).
+static unsigned append_blocks(const AppendParams &a, int warps_per_block) {
+    if (a.rows <= 0) return 0;
+    const int64_t b = (a.rows + warps_per_block - 1) / warps_per_block;
+    return (unsigned)(b < 64 ? b : 64);
+}
+
 cudaError_t launch_decode_plan(const DecodeParams &p, cudaStream_t stream) {
-    decode_plan_kernel<<<1, 1024, 0, stream>>>(p);
+    decode_plan_kernel<<<1 + append_blocks(p.app, 32), 1024, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_kv_append(const AppendParams &a, int *status, cudaStream_t stream) {
+    const unsigned grid = append_blocks(a, 8);
+    if (grid == 0) return cudaSuccess;
+    kv_append_kernel<<<grid, 256, 0, stream>>>(a, status);
     return cudaGetLastError();
 }
 

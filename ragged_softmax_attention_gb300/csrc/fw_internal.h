@@ -23,6 +23,22 @@ constexpr int kLatentRows = 64;       // latent-head decode: query heads per CTA
 // [r * span, (r + 1) * span) for r = c, c + grid, ...; the part of a unit
 // inside one range is a "piece" and writes a split-KV partial unless the unit
 // fits in a single range.
+// KV-cache append ("Writing Page Attention with PyPTO", section 4.3): row
+// (b, t, kv head) of the new keys/values goes to cache token row
+// layer_base + max(slot_mapping[b * q_len + t], 0).  rows = 0: nothing.
+struct AppendParams {
+    int64_t rows;                              // B * q_len * Hkv
+    int q_len, Hkv, Dk, Dv, ps;
+    int kv8;                                   // 1: E4M3 caches, code of x / scale
+    float k_scale, v_scale;
+    const uint16_t *k_new, *v_new;             // [B, q_len, Hkv, D] bf16; v_new may be null
+    int64_t kn_stride[3], vn_stride[3];        // elements (b, t, head); last dim contiguous
+    const int32_t *slot_mapping;               // [B * q_len]
+    int64_t layer_base, cache_rows;            // token rows; cache_rows = pages * ps
+    void *k_cache, *v_cache;                   // [pages, ps, Hkv, D]
+    int64_t kc_stride[3], vc_stride[3];        // elements (page, slot, head)
+};
+
 struct DecodeParams {
     int B, q_len, Hq, Hkv, G, ps, max_pages, num_pages;
     int head_mode;        // 0: a unit holds whole head groups for tokens_per_unit tokens;
@@ -38,6 +54,7 @@ struct DecodeParams {
                           // c / R, c / R + grid / R, ...), so they read the same keys together
     int Dv;
     int window_left;      // < 0: none; else token t sees keys max(0, n - q_len + t - W) .. n - q_len + t
+    AppendParams app;     // appended by the plan launch's extra blocks before the attention reads
     int32_t *plan;        // [0] = T, [1] = span, [2 .. 2 + B] = PB
     const int32_t *block_table; int64_t bt_stride;
     const int32_t *seq_lens;
@@ -77,6 +94,8 @@ cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &tm_q, const 
 size_t decode_smem_bytes(int head_dim, int rows);
 cudaError_t launch_decode_plan(const DecodeParams &p, cudaStream_t stream);
 cudaError_t launch_decode_combine(const DecodeParams &p, int head_dim_v, cudaStream_t stream);
+// Standalone KV-cache append (the fused form runs inside launch_decode_plan).
+cudaError_t launch_kv_append(const AppendParams &a, int *status, cudaStream_t stream);
 
 // Latent-head decode (Dk = 576, Dv = 512, row groups of 64 query heads):
 // plan kernel + attention kernel + combine kernel, in stream order
