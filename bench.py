@@ -455,6 +455,48 @@ def bench_decode_window(fw, torch, steps, warmup, device, peaks, fp8=False, wind
                          "kernel_ms_per_launch": round(per, 4)}}
 
 
+def bench_decode_append(fw, torch, steps, warmup, device, peaks):
+    """The Qwen3-14B-shaped decode with each row's new token appended in the
+    same call (fw_paged_decode_append, the append folded into the plan
+    launch): same metric as the plain decode line, so the difference is the
+    append's cost."""
+    from ragged_softmax_attention_gb300.workloads import WORKLOADS, make_decode_inputs
+    wl = WORKLOADS[DECODE_WL]
+    d = make_decode_inputs(wl, device)
+    lens = d["seq_lens"].long().cpu()
+    bt = d["block_table"].cpu()
+    ps = wl.page_size
+    slots = torch.tensor([int(bt[b, (int(lens[b]) - 1) // ps]) * ps + (int(lens[b]) - 1) % ps
+                          for b in range(wl.batch)], dtype=torch.int32, device=device)
+    g = torch.Generator(device="cpu").manual_seed(17)
+    k_new = torch.randn(wl.batch, 1, wl.num_kv_heads, wl.head_dim_qk, generator=g).to(torch.bfloat16).to(device)
+    v_new = torch.randn(wl.batch, 1, wl.num_kv_heads, wl.head_dim_v, generator=g).to(torch.bfloat16).to(device)
+    kv = int(lens.sum()) * wl.num_kv_heads * (wl.head_dim_qk + wl.head_dim_v) * 2
+    args = (d["q"], k_new, v_new, slots, 0, d["k_cache"], d["v_cache"], d["block_table"], d["seq_lens"], d["scale"])
+    out, lse = fw.paged_decode_append(*args)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, warmup)):
+        fw.paged_decode_append(*args, out=out, lse=lse)
+    torch.cuda.synchronize()
+    n = max(3, min(steps, 100))
+    l0 = fw.launch_count()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(n):
+        fw.paged_decode_append(*args, out=out, lse=lse)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(stop) / n
+    if fw.device_status() != 0:
+        raise RuntimeError("device status nonzero during the append + decode benchmark")
+    appended = wl.batch * wl.num_kv_heads * (wl.head_dim_qk + wl.head_dim_v) * 2
+    return {"workload": DECODE_WL + ", new token appended in the call", "value": round(kv / (ms * 1e-3) / 1e9, 1),
+            "unit": "GB/s", "ms_per_step": round(ms, 4), "steps": n, "kv_bytes_per_step": kv,
+            "appended_bytes_per_step": appended, "gpu_launches": fw.launch_count() - l0}
+
+
 # ------------------------------------------------------- latent decode
 
 def latent_work(lens, wl):
@@ -601,8 +643,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--only", choices=["all", "decode", "decode_fp8", "decode_window", "prefill", "prefill256",
-                                       "latent"],
+    ap.add_argument("--only", choices=["all", "decode", "decode_fp8", "decode_window", "decode_append", "prefill",
+                                       "prefill256", "latent"],
                     default="all",
                     help="profiling runs: time one path only")
     ap.add_argument("--decode-batch", type=int, default=0,
@@ -652,6 +694,11 @@ def main():
         if rank == 0:
             print(json.dumps({"decode_window": w16, "decode_fp8_window": w8}), flush=True)
         return 0
+    if args.only == "decode_append":
+        app = bench_decode_append(fw, torch, args.steps, args.warmup, device, peaks)
+        if rank == 0:
+            print(json.dumps({"decode_append": app}), flush=True)
+        return 0
     if args.only == "latent":
         lat = bench_latent(fw, torch, args.steps, args.warmup, device, peaks, batch=args.latent_batch or None)
         if rank == 0:
@@ -668,6 +715,7 @@ def main():
            bench_decode_window(fw, torch, args.steps, args.warmup, device, peaks, fp8=False))
     w8 = (None if args.only == "decode" else
           bench_decode_window(fw, torch, args.steps, args.warmup, device, peaks, fp8=True))
+    app = None if args.only == "decode" else bench_decode_append(fw, torch, args.steps, args.warmup, device, peaks)
     elapsed_ms, e2e_ms = max_over_ranks(pg, [dec["elapsed_ms"], dec["e2e_ms"]], device)
     value = whole_job_rate(dec["kv_bytes"], args.steps, world, elapsed_ms)
     e2e_value = whole_job_rate(dec["kv_bytes"], 1, world, e2e_ms)
@@ -685,7 +733,7 @@ def main():
                     "d2h_bytes_per_step": dec["d2h"], "steps": dec["e2e_steps"],
                     "note": "inputs (incl. the KV cache) copied from pinned host memory every step"},
             "prefill": pre, "prefill_hd256": pre256, "latent_decode": lat, "decode_fp8": f8,
-            "decode_window": w16, "decode_fp8_window": w8}
+            "decode_window": w16, "decode_fp8_window": w8, "decode_append": app}
     if world == 1 and not args.no_cpu_baseline and not args.decode_batch:
         try:
             line["cpu_baseline"] = cpu_baseline(torch, dec["inputs"], dec["wl"])
