@@ -194,17 +194,21 @@ fw_status_t plan_decode(int32_t B, int32_t q_len, int32_t Hq, int32_t Hkv, int32
     p.group = G;
     const bool latent = (Dv == 512);
     if (latent) {
-        // Latent heads (Dk = 576, Dv = 512): 64 query heads of one token per
-        // CTA; the q_len * G / 64 row groups of a unit share its tile ranges
-        // and ride on the CTA index.
+        // Latent heads (Dk = 576, Dv = 512): a row group is 128 query heads of
+        // one token on a CTA pair when the group size allows, else 64 on one
+        // CTA; the q_len * G / rows row groups of a unit share its tile ranges
+        // and ride on the worker (pair or CTA) index.
         if (G % fw::kLatentRows != 0)
             return fail(FW_ERR_UNSUPPORTED, "latent decode needs the query heads per KV head (%d) to be a "
                         "multiple of %d", G, fw::kLatentRows);
+        const int rows = G % fw::kLatentPairRows == 0 ? fw::kLatentPairRows : fw::kLatentRows;
         p.tokens_per_unit = 1;
-        p.heads_per_unit = fw::kLatentRows;
-        p.rows_per_unit = fw::kLatentRows;
-        p.row_groups = q_len * (G / fw::kLatentRows);
-        if (p.row_groups > num_sms) return fail(FW_ERR_UNSUPPORTED, "more row groups than SMs");
+        p.heads_per_unit = rows;
+        p.rows_per_unit = rows;
+        p.row_groups = q_len * (G / rows);
+        const int ctas_per_group = rows == fw::kLatentPairRows ? 2 : 1;
+        if ((int64_t)p.row_groups * ctas_per_group > num_sms)
+            return fail(FW_ERR_UNSUPPORTED, "more row groups than SMs");
     } else
     // Fold query tokens next to the heads of a KV group: the largest F that
     // divides q_len with G * F within the 32-row N budget ("TokenSpeed-MLA
@@ -242,8 +246,10 @@ fw_status_t plan_decode(int32_t B, int32_t q_len, int32_t Hq, int32_t Hkv, int32
     int64_t grid = num_sms;
     if (g_opt_max_ctas > 0 && grid > g_opt_max_ctas) grid = g_opt_max_ctas;
     if (latent) {
-        grid = grid / p.row_groups * p.row_groups;         // whole groups of row-group CTAs
-        if (grid < p.row_groups) grid = p.row_groups;
+        // whole groups of row-group workers (a worker is a CTA pair at 128 rows)
+        const int64_t per = (int64_t)p.row_groups * (p.rows_per_unit == fw::kLatentPairRows ? 2 : 1);
+        grid = grid / per * per;
+        if (grid < per) grid = per;
     }
     p.grid = (int32_t)(grid > 0 ? grid : 1);
     *pl = p;
@@ -619,6 +625,15 @@ static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_
     p.plan = reinterpret_cast<int32_t *>(wsb);
     p.ws_o = reinterpret_cast<float *>(wsb + plan_bytes);
     p.ws_lse = reinterpret_cast<float *>(wsb + plan_bytes + o_bytes);
+    if (latent) {
+        // Whole key pages, as the latent kernels' L2 prefetch reads them:
+        // from a page's first element to its last, rounded down to 16 bytes
+        // (TMA layouts keep pages 16-byte aligned).
+        const int64_t last = (ps - 1) * k_cache->stride[1] + (Hkv - 1) * k_cache->stride[2] + Dk;
+        p.k_bytes = static_cast<const uint8_t *>(k_cache->data);
+        p.k_page_stride = k_cache->stride[0] * 2;
+        p.k_page_span = last * 2 <= (1LL << 20) ? (uint32_t)(last * 2 / 16 * 16) : 0u;
+    }
     p.scale_log2 = scale * (kv8 ? k_scale : 1.f) * 1.4426950408889634f;
     p.out_scale = kv8 ? v_scale : 1.f;
     p.timeout_ns = (uint64_t)g_opt_timeout_ms * 1000000ull;
@@ -626,7 +641,9 @@ static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_
 
     CUtensorMap tq, tk, tv;
     {
-        const uint32_t box_h = p.head_mode == 0 ? (uint32_t)pl.group : (uint32_t)pl.heads_per_unit;
+        // Latent heads: each CTA loads 64 query rows (a pair splits its 128).
+        const uint32_t box_h = p.head_mode == 0 ? (uint32_t)pl.group
+                             : latent ? (uint32_t)fw::kLatentRows : (uint32_t)pl.heads_per_unit;
         const uint32_t box_t = p.head_mode == 0 ? (uint32_t)pl.tokens_per_unit : 1u;
         const uint64_t dims[4] = {(uint64_t)Dk, (uint64_t)Hq, (uint64_t)q_len, (uint64_t)B};
         const uint64_t strides[3] = {(uint64_t)q->stride[2] * 2, (uint64_t)q->stride[1] * 2, (uint64_t)q->stride[0] * 2};
@@ -664,7 +681,9 @@ static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_
     if (g_opt_timing) { ev0 = pooled_event(); ev1 = pooled_event(); }
     int launched = 0;
     cudaError_t e = kv8 ? fw::launch_decode_fp8(p, tq, tk, tv, stream, ev0, ev1, &launched)
-                  : latent ? fw::launch_latent_decode(p, tq, tk, tv, stream, ev0, ev1, &launched)
+                  : latent ? (pl.rows_per_unit == fw::kLatentPairRows
+                                  ? fw::launch_latent_pair_decode(p, tq, tk, tv, stream, ev0, ev1, &launched)
+                                  : fw::launch_latent_decode(p, tq, tk, tv, stream, ev0, ev1, &launched))
                            : fw::launch_decode(p, tq, tk, tv, (int)Dk, stream, ev0, ev1, &launched);
     g_launches.fetch_add(launched);
     if (e != cudaSuccess) return fail(FW_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));

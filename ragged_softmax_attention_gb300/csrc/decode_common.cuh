@@ -94,6 +94,72 @@ struct PieceIter {
     }
 };
 
+// Latent-head decode: one piece is a (batch row, KV head) unit's tiles inside
+// one tile range, for one row group (token t, heads h0 .. h0 + rows).
+struct LatentPiece {
+    int b, g, t, h0, n, k_begin, k_end, ntiles, k;
+    bool single;
+};
+
+// Walks the pieces of worker `idx` of `count` (a CTA, or a CTA pair): tile
+// ranges idx / R, idx / R + count / R, ... over the units laid end to end in
+// tile order, for row group idx % R (R = range_groups), so the R workers that
+// read the same keys run side by side.  Every role runs its own copy and
+// sees the same sequence.
+struct LatentIter {
+    int T, span, range, step, pos, end, b, rg;
+
+    __device__ void init(const DecodeParams &p, int idx, int count) {
+        T = __ldg(p.plan + 0);
+        span = max(1, __ldg(p.plan + 1));
+        step = max(1, count / p.range_groups);
+        range = idx / p.range_groups;
+        rg = idx % p.range_groups;
+        open_range();
+    }
+    __device__ void open_range() {
+        const long long lo = (long long)range * span;
+        pos = lo < T ? (int)lo : T;
+        end = (int)min((long long)T, lo + span);
+        b = -1;
+    }
+    __device__ bool next(const DecodeParams &p, LatentPiece &x) {
+        const int32_t *PB = p.plan + 2;
+        while (pos >= end) {
+            range += step;
+            if ((long long)range * span >= T) return false;
+            open_range();
+        }
+        if (b < 0 || pos >= __ldg(PB + b + 1)) {
+            int lo = 0, hi = p.B - 1;              // largest b with PB[b] <= pos
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (__ldg(PB + mid) <= pos) lo = mid; else hi = mid - 1;
+            }
+            b = lo;
+        }
+        const int pb0 = __ldg(PB + b);
+        const int tb = (__ldg(PB + b + 1) - pb0) / p.units_per_row;
+        const int off = pos - pb0;
+        const int u = off / tb;
+        const int tl = off - u * tb;
+        const int th = min(tb, tl + (end - pos));
+        const int pstart = pb0 + u * tb;
+        x.b = b;
+        x.g = u;
+        x.t = rg / p.head_chunks;
+        x.h0 = u * p.G + (rg % p.head_chunks) * p.rows;
+        x.n = clamp_len(p, __ldg(p.seq_lens + b));
+        x.k_begin = tl * kKvTile;
+        x.k_end = min(x.n, th * kKvTile);
+        x.ntiles = th - tl;
+        x.k = (pstart + tl) / span - pstart / span;
+        x.single = ((pstart + tb - 1) / span == pstart / span);
+        pos += th - tl;
+        return true;
+    }
+};
+
 // Query row r of unit x -> (token t, head h); false if the row is padding.
 __device__ __forceinline__ bool unit_row(const DecodeParams &p, const Unit &x, int r, int &t, int &h) {
     if (p.head_mode == 0) {

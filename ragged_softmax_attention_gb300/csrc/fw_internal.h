@@ -12,7 +12,8 @@ constexpr int kSoftmaxStartWarp = 2;  // decode: warps 2..5 run the softmax / ep
 
 constexpr int kDecodeMinSpan = 8;     // decode: fewest KV tiles one CTA range holds (auto mode)
 constexpr int kLatentMinSpan = 32;    // latent-head decode: the same, for its heavier tiles
-constexpr int kLatentRows = 64;       // latent-head decode: query heads per CTA (MMA N)
+constexpr int kLatentRows = 64;       // latent-head decode: query heads per CTA (MMA N of one CTA)
+constexpr int kLatentPairRows = 128;  // latent-head decode on CTA pairs: query heads per pair
 
 // One decode launch, fully resolved on the host.
 //
@@ -62,6 +63,9 @@ struct DecodeParams {
     float *lse; int64_t lse_stride[3];         // [B, q_len, Hq] or nullptr
     float *ws_o;                               // [B*q_len*Hq, max_pieces, Dv]
     float *ws_lse;                             // [B*q_len*Hq, max_pieces] (log2 units)
+    const uint8_t *k_bytes;                    // key cache base, for L2 prefetches of whole pages
+    int64_t k_page_stride;                     // bytes between pages
+    uint32_t k_page_span;                      // bytes of one page to prefetch (multiple of 16), 0 = none
     float scale_log2;                          // scale * log2(e) (times k_scale for an FP8 cache)
     float out_scale;                           // v_scale for an FP8 cache, else 1
     uint64_t timeout_ns;
@@ -103,6 +107,12 @@ cudaError_t launch_latent_decode(const DecodeParams &p, const CUtensorMap &tm_q,
                                  const CUtensorMap &tm_v, cudaStream_t stream, cudaEvent_t timing_start,
                                  cudaEvent_t timing_stop, int *launches);
 size_t latent_decode_smem_bytes();
+
+// The same on CTA pairs (row groups of 128 query heads, cta_group::2 MMAs)
+cudaError_t launch_latent_pair_decode(const DecodeParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                                      const CUtensorMap &tm_v, cudaStream_t stream, cudaEvent_t timing_start,
+                                      cudaEvent_t timing_stop, int *launches);
+size_t latent_pair_decode_smem_bytes();
 
 // Decode over an FP8 E4M3 KV cache (Dk = Dv = 128): plan + attention + combine
 cudaError_t launch_decode_fp8(const DecodeParams &p, const CUtensorMap &tm_q, const CUtensorMap &tm_k,

@@ -41,6 +41,7 @@
 
 #include "fw_internal.h"
 #include "fw_ptx.cuh"
+#include "decode_common.cuh"
 
 namespace fw {
 
@@ -115,69 +116,6 @@ __device__ __forceinline__ int clamp_len(const DecodeParams &p, int n) {
     const int cap = p.max_pages * p.ps;
     return n < 0 ? 0 : (n > cap ? cap : n);
 }
-
-struct LatPiece {             // one piece: a unit's tiles inside one tile range
-    int b, g, t, h0, n, k_begin, k_end, ntiles, k;
-    bool single;
-};
-
-// Walks this CTA's pieces: ranges blockIdx / R, blockIdx / R + grid / R, ...
-// over the (batch row, KV head) units laid end to end in tile order; the row
-// group (token, block of 64 heads) is blockIdx % R.  Every role runs its own
-// copy and sees the same sequence.
-struct LatIter {
-    int T, span, range, step, pos, end, b, rg;
-
-    __device__ void init(const DecodeParams &p) {
-        T = __ldg(p.plan + 0);
-        span = max(1, __ldg(p.plan + 1));
-        step = max(1, (int)gridDim.x / p.range_groups);
-        range = (int)blockIdx.x / p.range_groups;
-        rg = (int)blockIdx.x % p.range_groups;
-        open_range();
-    }
-    __device__ void open_range() {
-        const long long lo = (long long)range * span;
-        pos = lo < T ? (int)lo : T;
-        end = (int)min((long long)T, lo + span);
-        b = -1;
-    }
-    __device__ bool next(const DecodeParams &p, LatPiece &x) {
-        const int32_t *PB = p.plan + 2;
-        while (pos >= end) {
-            range += step;
-            if ((long long)range * span >= T) return false;
-            open_range();
-        }
-        if (b < 0 || pos >= __ldg(PB + b + 1)) {
-            int lo = 0, hi = p.B - 1;              // largest b with PB[b] <= pos
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (__ldg(PB + mid) <= pos) lo = mid; else hi = mid - 1;
-            }
-            b = lo;
-        }
-        const int pb0 = __ldg(PB + b);
-        const int tb = (__ldg(PB + b + 1) - pb0) / p.units_per_row;
-        const int off = pos - pb0;
-        const int u = off / tb;
-        const int tl = off - u * tb;
-        const int th = min(tb, tl + (end - pos));
-        const int pstart = pb0 + u * tb;
-        x.b = b;
-        x.g = u;
-        x.t = rg / p.head_chunks;
-        x.h0 = u * p.G + (rg % p.head_chunks) * kRows;
-        x.n = clamp_len(p, __ldg(p.seq_lens + b));
-        x.k_begin = tl * kKvTile;
-        x.k_end = min(x.n, th * kKvTile);
-        x.ntiles = th - tl;
-        x.k = (pstart + tl) / span - pstart / span;
-        x.single = ((pstart + tb - 1) / span == pstart / span);
-        pos += th - tl;
-        return true;
-    }
-};
 
 __global__ void __launch_bounds__(192, 1)
 latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tm_q,
@@ -290,9 +228,9 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
         };
         bool ok = true;
         int pb = -1, pg = 0, pts = 0, pend_end = 0, pphys = 0;   // the tile whose PV is still to be fed
-        LatIter it;
-        it.init(p);
-        LatPiece x;
+        dec::LatentIter it;
+        it.init(p, blockIdx.x, gridDim.x);
+        dec::LatentPiece x;
         while (ok && it.next(p, x)) {
             if (!warp_wait(q_empty, (nq & 1) ^ 1, wc, lane)) { ok = false; break; }
             if (lane == 0) {
@@ -375,9 +313,9 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
                 return true;
             };
             bool ok = true, pend = false, pend_first = false;
-            LatIter it;
-            it.init(p);
-            LatPiece x;
+            dec::LatentIter it;
+            it.init(p, blockIdx.x, gridDim.x);
+            dec::LatentPiece x;
             while (ok && it.next(p, x)) {
                 if (!mbar_wait(q_full, nq & 1, wc)) { ok = false; break; }
                 tc_fence_after();
@@ -427,9 +365,9 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
         auto red4 = [&](int r) {
             return fmaxf(fmaxf(red[r], red[kRows + r]), fmaxf(red[2 * kRows + r], red[3 * kRows + r]));
         };
-        LatIter it;
-        it.init(p);
-        LatPiece x;
+        dec::LatentIter it;
+        it.init(p, blockIdx.x, gridDim.x);
+        dec::LatentPiece x;
         while (it.next(p, x)) {
             const int lim = min(x.n, x.n - p.q_len + x.t + 1);   // keys the piece's token sees
             float l_part[kRows];

@@ -30,6 +30,7 @@
 
 #include "fw_internal.h"
 #include "fw_ptx.cuh"
+#include "fw_pair.cuh"
 
 namespace fw {
 namespace {
@@ -595,88 +596,6 @@ constexpr int kPairSmemBytes = kPairOffMisc + 16 + 1024;
 static_assert(kPairSmemBytes <= 232448, "shared memory budget of one CTA exceeded");
 constexpr uint32_t kPairIdescQK = idesc_bf16_f32(256, 128, false, false);
 constexpr uint32_t kPairIdescPV = idesc_bf16_f32(256, 256, false, true);
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Address of this CTA's shared variable `p` in the shared memory of cluster CTA `cta`.
-__device__ __forceinline__ uint32_t cluster_addr(const void *p, uint32_t cta) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(cta));
-    return r;
-}
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(bar_cluster_addr) : "memory");
-}
-// TMA tile load into this CTA's shared memory whose completion is counted on
-// an mbarrier of either CTA of the pair.
-__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void *tmap, uint32_t bar_cluster_addr,
-                                                 int32_t c0, int32_t c1, int32_t c2) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5}], [%2];"
-        :: "r"(dst), "l"(tmap), "r"(bar_cluster_addr), "r"(c0), "r"(c1), "r"(c2) : "memory");
-}
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
-                 :: "r"(smem_u32(dst)), "r"(ncols) : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish_pair() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
-}
-__device__ __forceinline__ void mma_pair_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-                 :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
-}
-__device__ __forceinline__ void mma_pair_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-                 :: "r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc) : "memory");
-}
-// Arrive on the mbarrier at this offset in both CTAs of the pair once all
-// MMAs issued so far have completed.
-__device__ __forceinline__ void mma_commit_pair(uint64_t *bar) {
-    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-                 :: "r"(smem_u32(bar)), "h"((uint16_t)3) : "memory");
-}
-
-// Bounded wait (as mbar_wait) whose acquire reaches cluster scope: for
-// barriers that threads of the other CTA of the pair arrive on.
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, const WaitCtx &w) {
-    const uint32_t a = smem_u32(bar);
-    auto try_once = [&]() {
-        uint32_t ok;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(ok) : "r"(a), "r"(parity) : "memory");
-        return ok != 0;
-    };
-    if (try_once()) return true;
-    if (*w.abort_flag) return false;
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (try_once()) return true;
-        if ((it & 255u) == 0) {
-            if (*w.abort_flag) return false;
-            if (global_timer_ns() - t0 > w.timeout_ns) {
-                record_error(w.status, 5 /* FW_ERR_DEVICE_TIMEOUT */);
-                *w.abort_flag = 1;
-                return false;
-            }
-        }
-    }
-}
 
 // Snake over the cost-sorted list, one entry per CTA pair.
 __device__ __forceinline__ int pair_snake_index(int k) {

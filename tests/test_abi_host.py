@@ -78,13 +78,17 @@ def test_planner_wide_groups_are_chunked(fwlib):
 @pytest.mark.parametrize("q_len,hq,hkv,sms,grid", [(4, 128, 1, 152, 152), (3, 128, 1, 152, 150),
                                                     (1, 64, 1, 152, 152), (2, 128, 2, 148, 148)])
 def test_planner_latent_row_groups_ride_on_the_grid(fwlib, q_len, hq, hkv, sms, grid):
-    """Latent heads (Dv 512): 64 heads of one token per CTA; the row groups of a
-    unit are q_len * G / 64 consecutive CTAs, so the grid is a whole multiple."""
+    """Latent heads (Dv 512): a row group is 128 heads of one token on a CTA
+    pair when the group holds a multiple of 128 heads, else 64 heads on one
+    CTA; the row groups of a unit are consecutive workers, so the grid is a
+    whole multiple of them (two CTAs per pair)."""
     p = fwlib.plan_decode(32, q_len, hq, hkv, 512, 81920, num_sms=sms)
     G = hq // hkv
-    assert p["heads_per_unit"] == 64 and p["rows_per_unit"] == 64 and p["tokens_per_unit"] == 1
-    assert p["row_groups"] == q_len * G // 64
-    assert p["grid"] == grid and p["grid"] % p["row_groups"] == 0
+    rows = 128 if G % 128 == 0 else 64
+    assert p["heads_per_unit"] == rows and p["rows_per_unit"] == rows and p["tokens_per_unit"] == 1
+    assert p["row_groups"] == q_len * G // rows
+    per = p["row_groups"] * (2 if rows == 128 else 1)
+    assert p["grid"] == grid and p["grid"] % per == 0
     assert p["min_span_tiles"] == 32
     assert p["max_pieces"] == -(-640 // 32) + 1
 
