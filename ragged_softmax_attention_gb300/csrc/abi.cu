@@ -625,15 +625,6 @@ static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_
     p.plan = reinterpret_cast<int32_t *>(wsb);
     p.ws_o = reinterpret_cast<float *>(wsb + plan_bytes);
     p.ws_lse = reinterpret_cast<float *>(wsb + plan_bytes + o_bytes);
-    if (latent) {
-        // Whole key pages, as the latent kernels' L2 prefetch reads them:
-        // from a page's first element to its last, rounded down to 16 bytes
-        // (TMA layouts keep pages 16-byte aligned).
-        const int64_t last = (ps - 1) * k_cache->stride[1] + (Hkv - 1) * k_cache->stride[2] + Dk;
-        p.k_bytes = static_cast<const uint8_t *>(k_cache->data);
-        p.k_page_stride = k_cache->stride[0] * 2;
-        p.k_page_span = last * 2 <= (1LL << 20) ? (uint32_t)(last * 2 / 16 * 16) : 0u;
-    }
     p.scale_log2 = scale * (kv8 ? k_scale : 1.f) * 1.4426950408889634f;
     p.out_scale = kv8 ? v_scale : 1.f;
     p.timeout_ns = (uint64_t)g_opt_timeout_ms * 1000000ull;

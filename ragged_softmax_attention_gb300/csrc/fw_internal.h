@@ -63,9 +63,6 @@ struct DecodeParams {
     float *lse; int64_t lse_stride[3];         // [B, q_len, Hq] or nullptr
     float *ws_o;                               // [B*q_len*Hq, max_pieces, Dv]
     float *ws_lse;                             // [B*q_len*Hq, max_pieces] (log2 units)
-    const uint8_t *k_bytes;                    // key cache base, for L2 prefetches of whole pages
-    int64_t k_page_stride;                     // bytes between pages
-    uint32_t k_page_span;                      // bytes of one page to prefetch (multiple of 16), 0 = none
     float scale_log2;                          // scale * log2(e) (times k_scale for an FP8 cache)
     float out_scale;                           // v_scale for an FP8 cache, else 1
     uint64_t timeout_ns;

@@ -128,11 +128,19 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
 __device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
 }
-// Hint: bring `bytes` (a multiple of 16) of global memory at a 16-byte
-// aligned address into L2.
-__device__ __forceinline__ void l2_prefetch_bulk(const void *ptr, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(reinterpret_cast<uint64_t>(ptr)), "r"(bytes)
-                 : "memory");
+// Asynchronous 4-byte store into the shared memory of a CTA of the cluster
+// whose completion is counted (4 bytes) on an mbarrier of that same CTA: the
+// receiver arms the barrier with the bytes it expects and its wait makes the
+// value visible, so the sender needs no release.
+__device__ __forceinline__ void st_async_u32(uint32_t addr_cluster, uint32_t v, uint32_t bar_cluster_addr) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];"
+                 :: "r"(addr_cluster), "r"(v), "r"(bar_cluster_addr) : "memory");
+}
+// The same for 16 bytes (four 32-bit words).
+__device__ __forceinline__ void st_async_v4(uint32_t addr_cluster, uint32_t x, uint32_t y, uint32_t z, uint32_t w,
+                                            uint32_t bar_cluster_addr) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+                 :: "r"(addr_cluster), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar_cluster_addr) : "memory");
 }
 // Make generic-proxy writes to any CTA's shared memory of the cluster
 // visible to the async proxy (tensor core operand reads).

@@ -58,7 +58,6 @@ constexpr int kRowsCta = 64;                           // query rows each CTA lo
 constexpr int kKeysCta = kKvTile;                      // keys of a step in one CTA (half of MMA M)
 constexpr int kStepKeys = 2 * kKeysCta;
 constexpr int kSlots = 3;
-constexpr int kPrefetchSteps = 2;                      // L2 prefetch distance, in steps
 constexpr int kHalfBytes = kKeysCta * 128;             // 128 keys x 64 columns, 128-byte swizzle
 constexpr int kSlotBytes = 2 * kHalfBytes;             // 128 keys x 128 columns
 constexpr int kQChunkBytes = kRowsCta * 128;           // 64 rows x 64 columns
@@ -69,7 +68,8 @@ constexpr int kOffP = kOffQ + kQBytes;
 constexpr int kOffRing = kOffP + kPBytes;
 constexpr int kOffRot = kOffRing + kSlots * kSlotBytes;
 constexpr int kOffBar = kOffRot + kHalfBytes;
-constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 1 + 1 + 2 + 1 + 1;
+constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 1 + 1 + 2 + 1 + 2 + 1;
+constexpr int kThreads = 352;                          // 11 warps: see the roles below
 constexpr int kOffX = kOffBar + ((kNumBars * 8 + 127) / 128) * 128;
 constexpr int kOffRed = kOffX + (2 * 128 + 32) * 4;    // xr[2][128] from the partner, xf[2] + pad
 constexpr int kOffMisc = kOffRed + 6 * 128 * 4;        // red[4][128], anchors[128], factors[128]
@@ -101,7 +101,7 @@ __device__ __forceinline__ bool named_bar_any(uint32_t id, uint32_t count, bool 
     return r != 0;
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
     extern __shared__ uint8_t smem_raw[];
@@ -119,11 +119,12 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
     uint64_t *q_empty = q_full + 1;                // [1]
     uint64_t *s_full = q_empty + 1;                // [2]
     uint64_t *s_free = s_full + 2;                 // [2], CTA 0's count both CTAs' softmax warps
-    uint64_t *p_full = s_free + 2;                 // [1], CTA 0's count one arrival per CTA
+    uint64_t *p_full = s_free + 2;                 // [1], CTA 0's: one arrival per CTA once its P^T is whole
     uint64_t *pv_done = p_full + 1;                // [1]: PV j landed (frees both CTAs' P^T)
     uint64_t *xbar = pv_done + 1;                  // [2]: the partner's part of an exchange arrived
     uint64_t *drain = xbar + 2;                    // [1]
-    uint64_t *tail_bar = drain + 1;                // [1]: own landing of a value chunk with a tail
+    uint64_t *tail_bar = drain + 1;                // [2]: a producer warp's landing of a value chunk with a tail
+    uint64_t *p_tx = tail_bar + 2;                 // [1]: the partner's P^T rows landed in this CTA
     float *xr = reinterpret_cast<float *>(smem + kOffX);           // [2][128] written by the partner
     uint32_t *xf = reinterpret_cast<uint32_t *>(xr + 2 * 128);     // [2] partner's flag
     float *red = reinterpret_cast<float *>(smem + kOffRed);        // [4][128] per-quadrant row partials
@@ -148,7 +149,9 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
         mbar_init(p_full, 2);
         mbar_init(pv_done, 1);
         mbar_init(drain, 1);
-        mbar_init(tail_bar, 1);
+        mbar_init(&tail_bar[0], 1);
+        mbar_init(&tail_bar[1], 1);
+        mbar_init(p_tx, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -163,8 +166,15 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
     const uint32_t tmem = *tmem_slot;
     const WaitCtx wc{p.status, p.timeout_ns, abort_flag};
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
+    if (warp == 0 || warp == 10) {
+        // ------------------------------------------------------------ producers
+        // Two warps walk the same item sequence; warp 0 (pw 0) copies the ring
+        // items of even index, Q and the rotary chunks, warp 10 (pw 1) the
+        // ring items of odd index.  (An L2 prefetch of the pages a few steps
+        // ahead made the call ~12% slower: the four row-group pairs of a
+        // request already walk its keys side by side.)
+        const int pw = warp == 0 ? 0 : 1;
+        uint64_t *my_tail = &tail_bar[pw];
         uint32_t m = 0, nq = 0, nr = 0, ntail = 0;
         const int box_rows = p.ps < kKeysCta ? p.ps : kKeysCta;
         // Pages holding keys [ks, ks + 128) below k_end; lane l < that count
@@ -203,14 +213,14 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
                 return true;
             }
             if (np > 0) {
-                if (lane == 0) mbar_arrive_expect_tx(tail_bar, bytes);
+                if (lane == 0) mbar_arrive_expect_tx(my_tail, bytes);
                 __syncwarp();
                 if (lane < np)
                     for (int c = 0; c < ncb; ++c)
-                        tma_load_4d(smem_u32(dst + c * kHalfBytes + lane * box_rows * 128), tm, tail_bar,
+                        tma_load_4d(smem_u32(dst + c * kHalfBytes + lane * box_rows * 128), tm, my_tail,
                                     col0 + c * 64, g, slot0, phys);
-                if (!dec::warp_wait(tail_bar, ntail & 1, wc, lane)) {
-                    if (lane == 0) mbar_wait_drain(tail_bar, ntail & 1, wc);
+                if (!dec::warp_wait(my_tail, ntail & 1, wc, lane)) {
+                    if (lane == 0) mbar_wait_drain(my_tail, ntail & 1, wc);
                     __syncwarp();
                     return false;
                 }
@@ -234,14 +244,14 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
         int pg = 0, pts = 0, pend_end = 0, pph0 = 0, pph1 = 0;   // the step whose PV is still to be fed
         // This CTA's value columns of both key halves of the pending step.
         auto feed_pv = [&]() -> bool {
-            for (int v = 0; v < 4; ++v) {
+            for (int v = 0; v < 4; ++v, ++m) {
+                if ((int)(m & 1) != pw) continue;
                 const int dh = v >> 1, kh = v & 1;
                 const uint32_t sl = m % kSlots;
                 if (!dec::warp_wait(&slot_empty[sl], ((m / kSlots) & 1) ^ 1, wc, lane)) return false;
                 if (!fill(&slot_full[sl], sRing + sl * kSlotBytes, &tm_v, pg, dh * 256 + (int)rank * 128, 2,
                           pts + kh * kKeysCta, pend_end, kh ? pph1 : pph0, true))
                     return false;
-                ++m;
             }
             return true;
         };
@@ -249,8 +259,8 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
         it.init(p, pair, npairs);
         dec::LatentPiece x;
         while (ok && it.next(p, x)) {
-            if (!dec::warp_wait(q_empty, (nq & 1) ^ 1, wc, lane)) { ok = false; break; }
-            if (lane == 0) {
+            if (pw == 0 && !dec::warp_wait(q_empty, (nq & 1) ^ 1, wc, lane)) { ok = false; break; }
+            if (pw == 0 && lane == 0) {
                 const uint32_t q_full0 = cluster_addr(q_full, 0);
                 mbar_arrive_expect_tx_relaxed_cluster(q_full0, (uint32_t)kQBytes);
                 for (int c = 0; c < kDk / 64; ++c)
@@ -261,20 +271,8 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
             ++nq;
             const int nsteps = (x.ntiles + 1) >> 1;
             int ph0 = lookup(x.b, x.k_begin, x.k_end), ph1 = lookup(x.b, x.k_begin + kKeysCta, x.k_end);
-            // Pages of this CTA's half of step s into L2 (the four pairs of a
-            // request's row groups all ask; L2 merges them), kPrefetchSteps
-            // ahead of the copies into shared memory.
-            auto prefetch_step = [&](int s) {
-                if (p.k_page_span == 0 || s >= nsteps) return;
-                const int ks = x.k_begin + s * kStepKeys + (int)rank * kKeysCta;
-                const int phys = lookup(x.b, ks, x.k_end);
-                if (lane < npages_of(ks, x.k_end))
-                    l2_prefetch_bulk(p.k_bytes + (int64_t)phys * p.k_page_stride, p.k_page_span);
-            };
-            for (int s = 0; s < kPrefetchSteps; ++s) prefetch_step(s);
             for (int s = 0; s < nsteps && ok; ++s) {
                 const int ts = x.k_begin + s * kStepKeys;
-                prefetch_step(s + kPrefetchSteps);
                 const int c0 = ph0, c1 = ph1;
                 if (s + 1 < nsteps) {
                     ph0 = lookup(x.b, ts + kStepKeys, x.k_end);
@@ -282,16 +280,18 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
                 }
                 const int own_ks = ts + (int)rank * kKeysCta;
                 const int own_ph = rank ? c1 : c0;
-                for (int c = 0; c < 4 && ok; ++c) {
+                for (int c = 0; c < 4 && ok; ++c, ++m) {
+                    if ((int)(m & 1) != pw) continue;
                     const uint32_t sl = m % kSlots;
                     if (!dec::warp_wait(&slot_empty[sl], ((m / kSlots) & 1) ^ 1, wc, lane)) { ok = false; break; }
                     ok = fill(&slot_full[sl], sRing + sl * kSlotBytes, &tm_k, x.g, c * 128, 2, own_ks, x.k_end,
                               own_ph, false);
-                    ++m;
                 }
                 if (!ok) break;
-                if (!dec::warp_wait(rot_empty, (nr & 1) ^ 1, wc, lane)) { ok = false; break; }
-                ok = fill(rot_full, sRot, &tm_k, x.g, 512, 1, own_ks, x.k_end, own_ph, false);
+                if (pw == 0) {
+                    if (!dec::warp_wait(rot_empty, (nr & 1) ^ 1, wc, lane)) { ok = false; break; }
+                    ok = fill(rot_full, sRot, &tm_k, x.g, 512, 1, own_ks, x.k_end, own_ph, false);
+                }
                 ++nr;
                 if (ok && pend) ok = feed_pv();
                 pend = true; pg = x.g; pts = ts; pend_end = x.k_end; pph0 = c0; pph1 = c1;
@@ -301,7 +301,7 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
         // CTA 0's full barriers complete only once both CTAs' copies have
         // landed; CTA 0 drains them here, before the pair's final cluster
         // barrier, so neither CTA leaves with a copy in flight.
-        if (rank == 0 && lane == 0) {
+        if (rank == 0 && pw == 0 && lane == 0) {
             for (uint32_t k = 0; k < (uint32_t)kSlots && k < m; ++k) {
                 const uint32_t j = m - 1 - k;
                 mbar_wait_drain(&slot_full[j % kSlots], (j / kSlots) & 1, wc);
@@ -422,9 +422,10 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
         // xr[xc & 1].  Advances xc.
         auto exchange_rows = [&](float own) {
             const uint32_t par = xc & 1;
-            if (tsw < 128) st_cluster_f32(cluster_addr(&xr[par * 128 + tsw], peer), own);
-            named_bar_sync(1, 256);
-            if (tsw == 0) mbar_arrive_cluster(cluster_addr(&xbar[par], peer));   // releases all 128 stores
+            if (tsw == 0) mbar_arrive_expect_tx(&xbar[par], 128 * 4);        // the partner's 128 values
+            if (tsw < 128)
+                st_async_u32(cluster_addr(&xr[par * 128 + tsw], peer), __float_as_uint(own),
+                             cluster_addr(&xbar[par], peer));
             xwait(xc);
             ++xc;
             return par;
@@ -495,8 +496,8 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
                     const bool mine = named_bar_any(1, 256, vis && xmax > kAnchorSlack);
                     const uint32_t par = xc & 1;
                     if (tsw == 0) {
-                        st_cluster_u32(cluster_addr(&xf[par], peer), mine ? 1u : 0u);
-                        mbar_arrive_cluster(cluster_addr(&xbar[par], peer));
+                        mbar_arrive_expect_tx(&xbar[par], 4);                   // the partner's verdict
+                        st_async_u32(cluster_addr(&xf[par], peer), mine ? 1u : 0u, cluster_addr(&xbar[par], peer));
                     }
                     xwait(xc);
                     ++xc;
@@ -537,23 +538,15 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
                         tmem_wait_st();
                     }
                 }
-                // Both CTAs' P^T buffers are free once the previous PV has
-                // landed (it ran while this step's check was made).
-                mbar_wait(pv_done, (jt & 1) ^ 1, wc);
                 // P^T row of this key for the warp's 64 query rows, packed in
-                // pairs and stored 16 rows (two 16-byte units) at a time into
-                // the CTA that holds the row half; the row sums take the FP32
-                // probabilities.
-                const int krow = (int)rank * kKeysCta + key;
-                const bool local = half == (int)rank;
-                uint8_t *prow = sP + krow * 128;
-                const uint32_t prow_c = cluster_addr(prow, (uint32_t)half);
+                // pairs (the row sums take the FP32 probabilities), computed
+                // while the previous PV may still run.
+                uint32_t pk[kRowsCta / 2];
 #pragma unroll
                 for (int c = 0; c < kRowsCta; c += 16) {
                     float s16[16];
                     tmem_ld16(sa + c, s16);
                     tmem_wait_ld();
-                    uint32_t pk[8];
 #pragma unroll
                     for (int k = 0; k < 16; k += 4) {
                         const float4 a = *reinterpret_cast<const float4 *>(anchor_s + row_base + c + k);
@@ -563,26 +556,46 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
                         const float p3 = vis ? ex2_approx(fmaf(s16[k + 3], c2, -a.w)) : 0.f;
                         const int li = (c + k) >> 5, lj = (c + k) & 31;
                         lp[li][lj] += p0; lp[li][lj + 1] += p1; lp[li][lj + 2] += p2; lp[li][lj + 3] += p3;
-                        pk[k >> 1] = pack_bf16x2(p0, p1);
-                        pk[(k >> 1) + 1] = pack_bf16x2(p2, p3);
-                    }
-#pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        const uint32_t off = (uint32_t)((((c >> 3) + i) ^ (krow & 7)) << 4);
-                        if (local)
-                            *reinterpret_cast<uint4 *>(prow + off) =
-                                make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-                        else
-                            st_cluster_v4(prow_c + off, pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                        pk[(c + k) >> 1] = pack_bf16x2(p0, p1);
+                        pk[((c + k) >> 1) + 1] = pack_bf16x2(p2, p3);
                     }
                 }
                 tc_fence_before();
-                if (local) fence_proxy_async_smem(); else fence_proxy_async_cluster();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_relaxed_cluster(cluster_addr(&s_free[sb], 0));
-                // One release per CTA publishes all eight warps' P^T rows.
+                // Both CTAs' P^T buffers are free once the previous PV has landed.
+                mbar_wait(pv_done, (jt & 1) ^ 1, wc);
+                // Into the CTA that holds the warp's row half (128-byte swizzle):
+                // plain stores here, asynchronous ones into the partner, whose
+                // p_tx counts their bytes.
+                const int krow = (int)rank * kKeysCta + key;
+                if (half == (int)rank) {
+                    uint8_t *prow = sP + krow * 128;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        *reinterpret_cast<uint4 *>(prow + ((u ^ (krow & 7)) << 4)) =
+                            make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                    fence_proxy_async_smem();
+                } else {
+                    const uint32_t prow = cluster_addr(sP + krow * 128, peer);
+                    const uint32_t ptx = cluster_addr(p_tx, peer);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        st_async_v4(prow + ((u ^ (krow & 7)) << 4), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2],
+                                    pk[4 * u + 3], ptx);
+                }
                 named_bar_sync(1, 256);
-                if (tsw == 0) mbar_arrive_cluster(cluster_addr(p_full, 0));
+                // This CTA's P^T is whole once its own warps' stores are done
+                // (the barrier) and the partner's 16 KB have landed (p_tx);
+                // one thread makes them visible to the tensor core and tells
+                // the MMA issuer.
+                if (tsw == 0) {
+                    mbar_arrive_expect_tx(p_tx, kKeysCta * 128);
+                    mbar_wait_cluster(p_tx, jt & 1, wc);
+                    fence_proxy_async_smem();
+                    if (rank == 0) mbar_arrive(p_full);
+                    else mbar_arrive_cluster(cluster_addr(p_full, 0));
+                }
             }
             // ------------------------------------------------------ epilogue
             // Row sums over both CTAs' keys: red[q4][row] per warp, thread
@@ -669,7 +682,7 @@ cudaError_t launch_latent_pair_decode(const DecodeParams &p, const CUtensorMap &
     if (e != cudaSuccess) return e;
     ++*launches;
     if (timing_start) cudaEventRecord(timing_start, stream);
-    latent_pair_decode_kernel<<<p.grid, 320, kSmemBytes, stream>>>(p, tq, tk, tv);
+    latent_pair_decode_kernel<<<p.grid, kThreads, kSmemBytes, stream>>>(p, tq, tk, tv);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     ++*launches;
