@@ -184,12 +184,11 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
             if (p.ps >= kKeysCta) return 1;
             return min(kKeysCta / p.ps, ceil_div_i(k_end - ks, p.ps));
         };
+        // The load is issued a step before the page is copied; its range
+        // check waits until then (in fill), so the walk never stalls on it.
         auto lookup = [&](int b, int ks, int k_end) -> int {
             int phys = 0;
-            if (lane < npages_of(ks, k_end)) {
-                phys = __ldg(p.block_table + (int64_t)b * p.bt_stride + ks / p.ps + lane);
-                if ((unsigned)phys >= (unsigned)p.num_pages) { record_error(p.status, 1); phys = 0; }
-            }
+            if (lane < npages_of(ks, k_end)) phys = __ldg(p.block_table + (int64_t)b * p.bt_stride + ks / p.ps + lane);
             return phys;
         };
         // Keys [ks, ks + 128) below k_end, `ncb` 64-column blocks from column
@@ -202,6 +201,7 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
             const int np = npages_of(ks, k_end);
             const int slot0 = p.ps >= kKeysCta ? ks % p.ps : 0;
             const uint32_t full0 = cluster_addr(full, 0);
+            if (lane < np && (unsigned)phys >= (unsigned)p.num_pages) { record_error(p.status, 1); phys = 0; }
             const uint32_t bytes = (uint32_t)(np * box_rows * 128 * ncb);
             if (!(zero_tail && ks + kKeysCta > k_end)) {
                 if (lane == 0) mbar_arrive_expect_tx_relaxed_cluster(full0, bytes);
