@@ -510,6 +510,11 @@ def latent_work(lens, wl):
     return flops, kv
 
 
+# 128 query heads per KV head: the CTA-pair kernel serves the latent workload.
+LATENT_KERNEL = "latent_pair_decode_kernel"
+LATENT_SOURCES = ["latent_pair_kernel.cu", "fw_pair.cuh", "fw_ptx.cuh", "decode_common.cuh", "abi.cu"]
+
+
 def bench_latent(fw, torch, steps, warmup, device, peaks, batch=None):
     import dataclasses
     from ragged_softmax_attention_gb300.workloads import WORKLOADS, make_decode_inputs
@@ -551,11 +556,11 @@ def bench_latent(fw, torch, steps, warmup, device, peaks, batch=None):
                        "num_kv_heads": wl.num_kv_heads, "head_dim_qk": wl.head_dim_qk,
                        "head_dim_v": wl.head_dim_v, "page_size": wl.page_size, "seq_lens": "81920 each",
                        "scale": wl.scale, "v": "first 512 columns of the key cache"},
-            "roofline": {"kernel": "latent_decode_kernel", "bound": "tensor", "achieved": round(ach, 1),
+            "roofline": {"kernel": LATENT_KERNEL, "bound": "tensor", "achieved": round(ach, 1),
                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": round(ach / peaks["bf16_tflops"], 4),
                          "frac_of_sustained": round(ach / peaks["bf16_tflops_sustained"], 4),
-                         "traffic": ncu_traffic("latent_decode_ncu.json", ["latent_kernel.cu", "fw_ptx.cuh", "abi.cu"],
+                         "traffic": ncu_traffic("latent_pair_decode_ncu.json", LATENT_SOURCES,
                                                 sum(lens)), "peak_source": peaks["source"], "kernel_ms_per_launch": round(per, 4)}}
 
 
