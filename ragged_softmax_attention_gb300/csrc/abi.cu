@@ -194,18 +194,26 @@ fw_status_t plan_decode(int32_t B, int32_t q_len, int32_t Hq, int32_t Hkv, int32
     p.group = G;
     const bool latent = (Dv == 512);
     if (latent) {
-        // Latent heads (Dk = 576, Dv = 512): a row group is 128 query heads of
-        // one token on a CTA pair when the group size allows, else 64 on one
-        // CTA; the q_len * G / rows row groups of a unit share its tile ranges
-        // and ride on the worker (pair or CTA) index.
-        if (G % fw::kLatentRows != 0)
-            return fail(FW_ERR_UNSUPPORTED, "latent decode needs the query heads per KV head (%d) to be a "
-                        "multiple of %d", G, fw::kLatentRows);
-        const int rows = G % fw::kLatentPairRows == 0 ? fw::kLatentPairRows : fw::kLatentRows;
+        // Latent heads (Dk = 576, Dv = 512): a row group is `rows` consecutive
+        // query rows of a (batch row, KV head) unit -- 128 on a CTA pair, 64
+        // on one CTA -- whose q_len * G / rows row groups share its tile
+        // ranges and ride on the worker (pair or CTA) index.  With one KV head
+        // the rows are packed (token, head) rows t * G + h ("TokenSpeed-MLA
+        // 2.0.1", packed-query paragraph): ceil(q_len * G / rows) groups, only
+        // the last one padded.  With several KV heads a group holds one
+        // token's heads, so G must be a multiple of 64.
+        int rows;
+        if (Hkv == 1)
+            rows = (int64_t)q_len * G >= fw::kLatentPairRows ? fw::kLatentPairRows : fw::kLatentRows;
+        else if (G % fw::kLatentRows == 0)
+            rows = G % fw::kLatentPairRows == 0 ? fw::kLatentPairRows : fw::kLatentRows;
+        else
+            return fail(FW_ERR_UNSUPPORTED, "latent decode with several KV heads needs the query heads per KV "
+                        "head (%d) to be a multiple of %d", G, fw::kLatentRows);
         p.tokens_per_unit = 1;
         p.heads_per_unit = rows;
         p.rows_per_unit = rows;
-        p.row_groups = q_len * (G / rows);
+        p.row_groups = (int32_t)(((int64_t)q_len * G + rows - 1) / rows);
         const int ctas_per_group = rows == fw::kLatentPairRows ? 2 : 1;
         if ((int64_t)p.row_groups * ctas_per_group > num_sms)
             return fail(FW_ERR_UNSUPPORTED, "more row groups than SMs");
@@ -609,6 +617,12 @@ static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_
     p.max_pieces = pl.max_pieces;
     p.grid = pl.grid;
     p.Dv = (int)Dv;
+    // Packed latent rows: row groups straddle tokens, so q is read through
+    // its flattened (token, head) axis, which must then be one stride.
+    p.packed = latent && Hkv == 1 && pl.group % pl.rows_per_unit != 0;
+    if (p.packed && q_len > 1 && q->stride[1] != Hq * q->stride[2])
+        return fail(FW_ERR_UNSUPPORTED, "packed latent query rows need q contiguous over (token, head): "
+                    "stride[1] = %lld, expected %lld", (long long)q->stride[1], (long long)(Hq * q->stride[2]));
     p.window_left = window_left;
     p.app = app;
     p.block_table = static_cast<const int32_t *>(block_table->data);
@@ -631,7 +645,14 @@ static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_
     p.status = d->status;
 
     CUtensorMap tq, tk, tv;
-    {
+    if (p.packed) {
+        // Packed latent rows: [B][q_len * Hq rows][Dk], 64 rows per box (a
+        // pair's CTAs load one box each); rows past the end read as zeros.
+        const uint64_t dims[3] = {(uint64_t)Dk, (uint64_t)(q_len * Hq), (uint64_t)B};
+        const uint64_t strides[2] = {(uint64_t)q->stride[2] * 2, (uint64_t)q->stride[0] * 2};
+        const uint32_t box[3] = {64, (uint32_t)fw::kLatentRows, 1};
+        if (fw_status_t s = encode_bf16(&tq, q->data, 3, dims, strides, box, "q")) return s;
+    } else {
         // Latent heads: each CTA loads 64 query rows (a pair splits its 128).
         const uint32_t box_h = p.head_mode == 0 ? (uint32_t)pl.group
                              : latent ? (uint32_t)fw::kLatentRows : (uint32_t)pl.heads_per_unit;

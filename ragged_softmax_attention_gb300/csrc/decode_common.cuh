@@ -95,9 +95,11 @@ struct PieceIter {
 };
 
 // Latent-head decode: one piece is a (batch row, KV head) unit's tiles inside
-// one tile range, for one row group (token t, heads h0 .. h0 + rows).
+// one tile range, for one row group: packed rows row0 .. row0 + rows of the
+// unit, packed row i being token i / G, head g * G + i % G (when G is a
+// multiple of `rows` a group is one token's heads h0 .. h0 + rows).
 struct LatentPiece {
-    int b, g, t, h0, n, k_begin, k_end, ntiles, k;
+    int b, g, t, h0, row0, n, k_begin, k_end, ntiles, k;
     bool single;
 };
 
@@ -147,8 +149,9 @@ struct LatentIter {
         const int pstart = pb0 + u * tb;
         x.b = b;
         x.g = u;
-        x.t = rg / p.head_chunks;
-        x.h0 = u * p.G + (rg % p.head_chunks) * p.rows;
+        x.row0 = rg * p.rows;
+        x.t = x.row0 / p.G;
+        x.h0 = u * p.G + x.row0 % p.G;
         x.n = clamp_len(p, __ldg(p.seq_lens + b));
         x.k_begin = tl * kKvTile;
         x.k_end = min(x.n, th * kKvTile);

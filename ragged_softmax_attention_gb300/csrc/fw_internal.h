@@ -54,6 +54,10 @@ struct DecodeParams {
                           // a unit ride on the CTA index (CTA c runs row group c % R over ranges
                           // c / R, c / R + grid / R, ...), so they read the same keys together
     int Dv;
+    int packed;           // latent heads: 1 when q rows are read through the flattened (token, head)
+                          // axis (one KV head, q contiguous over it): a row group is `rows` consecutive
+                          // packed rows t * Hq + h and may straddle tokens ("TokenSpeed-MLA 2.0.1",
+                          // packed-query paragraph); 0: one token's heads per row group
     int window_left;      // < 0: none; else token t sees keys max(0, n - q_len + t - W) .. n - q_len + t
     AppendParams app;     // appended by the plan launch's extra blocks before the attention reads
     int32_t *plan;        // [0] = T, [1] = span, [2 .. 2 + B] = PB

@@ -66,7 +66,7 @@ constexpr int kOffP = kOffRing + kSlots * kSlotBytes;
 constexpr int kOffBar = kOffP + kPBytes;
 constexpr int kNumBars = 2 * kSlots + 2 + 2 + 1 + 1 + 1 + 1 + 1 + 1;
 constexpr int kOffRed = kOffBar + ((kNumBars * 8 + 127) / 128) * 128;
-constexpr int kOffMisc = kOffRed + 6 * kRows * 4;       // [4][64] partials + [64] anchors + [64] factors
+constexpr int kOffMisc = kOffRed + 7 * kRows * 4;       // [4][64] partials + [64] anchors, factors, limits
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;        // + alignment slack
 static_assert(kOffRing % 1024 == 0 && kOffP % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA exceeded");
@@ -117,6 +117,9 @@ __device__ __forceinline__ int clamp_len(const DecodeParams &p, int n) {
     return n < 0 ? 0 : (n > cap ? cap : n);
 }
 
+// kPacked: row groups may straddle tokens (packed rows), so visibility is
+// per row; otherwise every row of a group is one token's and shares it.
+template <bool kPacked>
 __global__ void __launch_bounds__(192, 1)
 latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
@@ -139,6 +142,7 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
     float *red = reinterpret_cast<float *>(smem + kOffRed);        // [4][64] per-warp row partials
     float *anchor_s = red + 4 * kRows;                             // [64] row anchors
     float *alpha_s = anchor_s + kRows;                             // [64] rescale factors / 1 / L
+    int *lim_s = reinterpret_cast<int *>(alpha_s + kRows);         // [64] keys each row sees in the piece
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
 
@@ -235,8 +239,12 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
             if (!warp_wait(q_empty, (nq & 1) ^ 1, wc, lane)) { ok = false; break; }
             if (lane == 0) {
                 mbar_arrive_expect_tx(q_full, (uint32_t)kQBytes);
-                for (int c = 0; c < kDk / 64; ++c)
-                    tma_load_4d(smem_u32(sQ + c * kQChunkBytes), &tm_q, q_full, c * 64, x.h0, x.t, x.b);
+                for (int c = 0; c < kDk / 64; ++c) {
+                    if (kPacked)       // rows past the last (token, head) read as zeros
+                        tma_load_3d(smem_u32(sQ + c * kQChunkBytes), &tm_q, q_full, c * 64, x.row0, x.b);
+                    else
+                        tma_load_4d(smem_u32(sQ + c * kQChunkBytes), &tm_q, q_full, c * 64, x.h0, x.t, x.b);
+                }
             }
             __syncwarp();
             ++nq;
@@ -348,7 +356,7 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
         // Scaled, masked row maxima of the S^T buffer at `sa`: every warp
         // reduces over its 32 keys into red[q4][r]; after the barrier thread
         // r < 64 may combine row r.
-        auto row_max_partials = [&](uint32_t sa, bool vis) {
+        auto row_max_partials = [&](uint32_t sa, int tok, bool uni, bool vis) {
 #pragma unroll
             for (int c = 0; c < kRows; c += 16) {
                 float s16[16];
@@ -356,7 +364,7 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
                 tmem_wait_ld();
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
-                    const float v = warp_max(vis ? s16[k] * c2 : kNegInf);
+                    const float v = warp_max((uni ? vis : tok < lim_s[c + k]) ? s16[k] * c2 : kNegInf);
                     if (lane == 0) red[q4 * kRows + c + k] = v;
                 }
             }
@@ -369,13 +377,28 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
         it.init(p, blockIdx.x, gridDim.x);
         dec::LatentPiece x;
         while (it.next(p, x)) {
-            const int lim = min(x.n, x.n - p.q_len + x.t + 1);   // keys the piece's token sees
+            // lim_s[r]: keys row r sees in the piece (its token's causal
+            // bound); 0 for a padding row past the last packed row.  Rows of
+            // one group may belong to different tokens.
+            if (key < kRows) {
+                const int gr = x.row0 + key;
+                lim_s[key] = gr < p.q_len * p.G ? min(x.k_end, x.n - p.q_len + gr / p.G + 1) : 0;
+            }
+            named_bar_sync(1, 128);
+            // A key below every row's limit is visible to all rows, one at or
+            // above every limit to none: one test then serves the row set
+            // (always, unless the rows straddle a token boundary near it).
+            int lim_lo = lim_s[0], lim_hi = lim_lo;
+            for (int r = 1; r < kRows; ++r) {
+                lim_lo = min(lim_lo, lim_s[r]);
+                lim_hi = max(lim_hi, lim_s[r]);
+            }
             float l_part[kRows];
 #pragma unroll
             for (int r = 0; r < kRows; ++r) l_part[r] = 0.f;
             for (int i = 0; i < x.ntiles; ++i, ++jt) {
                 const int tok = x.k_begin + i * kKvTile + key;
-                const bool vis = tok < lim;
+                const bool vis = tok < lim_lo, uni = !kPacked || vis || tok >= lim_hi;
                 const uint32_t sb = jt & 1;
                 mbar_wait(&s_full[sb], (jt >> 1) & 1, wc);
                 tc_fence_after();
@@ -384,7 +407,7 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
                     // anchor_s[r]: row r's exponent offset, its max over this
                     // first tile (0 for a row that sees no key here, and hence
                     // none later in the piece).
-                    row_max_partials(sa, vis);
+                    row_max_partials(sa, tok, uni, vis);
                     if (key < kRows) {
                         const float m = red4(key);
                         anchor_s[key] = m == kNegInf ? 0.f : m;
@@ -395,7 +418,7 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
                 // raise any row to (a max-only pass; on a piece's first tile the
                 // anchors are this tile's maxima and nothing can exceed them).
                 float xmax = kNegInf;
-                if (i > 0) {
+                if (i > 0) {   // all lanes: tcgen05.ld is warp-collective
 #pragma unroll
                     for (int c = 0; c < kRows; c += 16) {
                         float s16[16];
@@ -404,17 +427,23 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
 #pragma unroll
                         for (int k = 0; k < 16; k += 4) {
                             const float4 a = *reinterpret_cast<const float4 *>(anchor_s + c + k);
-                            xmax = fmaxf(xmax, fmaxf(fmaxf(fmaf(s16[k], c2, -a.x), fmaf(s16[k + 1], c2, -a.y)),
-                                                     fmaxf(fmaf(s16[k + 2], c2, -a.z), fmaf(s16[k + 3], c2, -a.w))));
+                            float e0 = fmaf(s16[k], c2, -a.x), e1 = fmaf(s16[k + 1], c2, -a.y);
+                            float e2 = fmaf(s16[k + 2], c2, -a.z), e3 = fmaf(s16[k + 3], c2, -a.w);
+                            if (!uni) {            // rows of two tokens meet near this key
+                                const int4 L = *reinterpret_cast<const int4 *>(lim_s + c + k);
+                                e0 = tok < L.x ? e0 : kNegInf; e1 = tok < L.y ? e1 : kNegInf;
+                                e2 = tok < L.z ? e2 : kNegInf; e3 = tok < L.w ? e3 : kNegInf;
+                            }
+                            xmax = fmaxf(xmax, fmaxf(fmaxf(e0, e1), fmaxf(e2, e3)));
                         }
                     }
-                    if (!vis) xmax = kNegInf;
+                    if (uni && !vis) xmax = kNegInf;
                 }
                 if (named_bar_any(1, 128, xmax > kAnchorSlack)) {
                     // Some score rose more than kAnchorSlack above its anchor:
                     // move those anchors to this tile's row max and rescale l
                     // and O^T (once the previous PV has landed).
-                    row_max_partials(sa, vis);
+                    row_max_partials(sa, tok, uni, vis);
                     if (key < kRows) {
                         const float mx = red4(key);
                         float a = 1.f;
@@ -455,10 +484,17 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
 #pragma unroll
                     for (int k = 0; k < 16; k += 4) {
                         const float4 a = *reinterpret_cast<const float4 *>(anchor_s + c + k);
-                        const float p0 = vis ? ex2_approx(fmaf(s16[k], c2, -a.x)) : 0.f;
-                        const float p1 = vis ? ex2_approx(fmaf(s16[k + 1], c2, -a.y)) : 0.f;
-                        const float p2 = vis ? ex2_approx(fmaf(s16[k + 2], c2, -a.z)) : 0.f;
-                        const float p3 = vis ? ex2_approx(fmaf(s16[k + 3], c2, -a.w)) : 0.f;
+                        float p0 = ex2_approx(fmaf(s16[k], c2, -a.x)), p1 = ex2_approx(fmaf(s16[k + 1], c2, -a.y));
+                        float p2 = ex2_approx(fmaf(s16[k + 2], c2, -a.z)), p3 = ex2_approx(fmaf(s16[k + 3], c2, -a.w));
+                        // Masking by selection (an invisible key's score may be
+                        // anything); per row only when two tokens meet near the key.
+                        if (kPacked && !uni) {
+                            const int4 L = *reinterpret_cast<const int4 *>(lim_s + c + k);
+                            p0 = tok < L.x ? p0 : 0.f; p1 = tok < L.y ? p1 : 0.f;
+                            p2 = tok < L.z ? p2 : 0.f; p3 = tok < L.w ? p3 : 0.f;
+                        } else {
+                            p0 = vis ? p0 : 0.f; p1 = vis ? p1 : 0.f; p2 = vis ? p2 : 0.f; p3 = vis ? p3 : 0.f;
+                        }
                         l_part[c + k] += p0;
                         l_part[c + k + 1] += p1;
                         l_part[c + k + 2] += p2;
@@ -488,28 +524,33 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
                 if (lane == 0) red[q4 * kRows + r] = v;
             }
             named_bar_sync(1, 128);
-            const int64_t row0 = ((int64_t)x.b * p.q_len + x.t) * p.Hq + x.h0;
+            // Packed row gr of the unit is token gr / G, head g * G + gr % G;
+            // rows past q_len * G are padding and write nothing.
+            const int qG = p.q_len * p.G;
+            const int64_t wrow_b = (int64_t)x.b * p.q_len * p.Hq;      // workspace row of (b, 0, 0)
             if (key < kRows) {
                 const float L = (red[key] + red[kRows + key]) + (red[2 * kRows + key] + red[3 * kRows + key]);
                 alpha_s[key] = L > 0.f ? 1.f / L : 0.f;
                 const float lse2 = L > 0.f ? anchor_s[key] + __log2f(L) : kNegInf;
-                if (x.single) {
-                    if (p.lse)
-                        p.lse[x.b * p.lse_stride[0] + x.t * p.lse_stride[1] + (x.h0 + key) * p.lse_stride[2]] =
-                            lse2 * 0.69314718055994531f;
-                } else {
-                    p.ws_lse[(row0 + key) * p.max_pieces + x.k] = lse2;
+                const int gr = x.row0 + key;
+                if (gr < qG) {
+                    const int t = gr / p.G, h = x.g * p.G + gr % p.G;
+                    if (x.single) {
+                        if (p.lse)
+                            p.lse[x.b * p.lse_stride[0] + t * p.lse_stride[1] + h * p.lse_stride[2]] =
+                                lse2 * 0.69314718055994531f;
+                    } else {
+                        p.ws_lse[(wrow_b + (int64_t)t * p.Hq + h) * p.max_pieces + x.k] = lse2;
+                    }
                 }
             }
             named_bar_sync(1, 128);
             mbar_wait(pv_done, (jt - 1) & 1, wc);
             tc_fence_after();
-            // Thread = value column c * 128 + key; rows walk with a running
-            // offset (a warp stores 32 consecutive columns of one row at a time).
-            __nv_bfloat16 *obase = reinterpret_cast<__nv_bfloat16 *>(p.out) + x.b * p.out_stride[0] +
-                                   x.t * p.out_stride[1] + x.h0 * p.out_stride[2] + key;
-            float *wbase = p.ws_o + (row0 * p.max_pieces + x.k) * kDv + key;
-            const int64_t ostep = p.out_stride[2], wstep = (int64_t)p.max_pieces * kDv;
+            // Thread = value column c * 128 + key; a warp stores 32 consecutive
+            // columns of one row at a time.
+            __nv_bfloat16 *obase = reinterpret_cast<__nv_bfloat16 *>(p.out) + x.b * p.out_stride[0] + key;
+            float *wbase = p.ws_o + key;
 #pragma unroll 1
             for (int c = 0; c < kPvChunks; ++c) {
 #pragma unroll 1
@@ -517,14 +558,19 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
                     float o[16];
                     tmem_ld16(tmem + lane_off + kColO + c * kRows + r0, o);
                     tmem_wait_ld();
-                    if (x.single) {
-                        __nv_bfloat16 *op = obase + r0 * ostep + c * 128;
+                    const int gr0 = x.row0 + r0;
+                    int t = gr0 / p.G, hl = gr0 % p.G;
 #pragma unroll
-                        for (int k = 0; k < 16; ++k, op += ostep) *op = __float2bfloat16_rn(o[k] * alpha_s[r0 + k]);
-                    } else {
-                        float *wp = wbase + r0 * wstep + c * 128;
-#pragma unroll
-                        for (int k = 0; k < 16; ++k, wp += wstep) *wp = o[k] * alpha_s[r0 + k];
+                    for (int k = 0; k < 16; ++k) {
+                        if (gr0 + k < qG) {
+                            const int h = x.g * p.G + hl;
+                            const float v = o[k] * alpha_s[r0 + k];
+                            if (x.single)
+                                obase[t * p.out_stride[1] + h * p.out_stride[2] + c * 128] = __float2bfloat16_rn(v);
+                            else
+                                wbase[((wrow_b + (int64_t)t * p.Hq + h) * p.max_pieces + x.k) * kDv + c * 128] = v;
+                        }
+                        if (++hl == p.G) { hl = 0; ++t; }
                     }
                 }
             }
@@ -549,8 +595,11 @@ cudaError_t launch_latent_decode(const DecodeParams &p, const CUtensorMap &tq, c
     *launches = 0;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(latent_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(latent_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(latent_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kSmemBytes);
         if (e != cudaSuccess) return e;
         configured = true;
     }
@@ -558,7 +607,8 @@ cudaError_t launch_latent_decode(const DecodeParams &p, const CUtensorMap &tq, c
     if (e != cudaSuccess) return e;
     ++*launches;
     if (timing_start) cudaEventRecord(timing_start, stream);
-    latent_decode_kernel<<<p.grid, 192, kSmemBytes, stream>>>(p, tq, tk, tv);
+    if (p.packed) latent_decode_kernel<true><<<p.grid, 192, kSmemBytes, stream>>>(p, tq, tk, tv);
+    else latent_decode_kernel<false><<<p.grid, 192, kSmemBytes, stream>>>(p, tq, tk, tv);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     ++*launches;

@@ -72,7 +72,7 @@ constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 1 + 1 + 2 + 1 + 2 + 1;
 constexpr int kThreads = 352;                          // 11 warps: see the roles below
 constexpr int kOffX = kOffBar + ((kNumBars * 8 + 127) / 128) * 128;
 constexpr int kOffRed = kOffX + (2 * 128 + 32) * 4;    // xr[2][128] from the partner, xf[2] + pad
-constexpr int kOffMisc = kOffRed + 6 * 128 * 4;        // red[4][128], anchors[128], factors[128]
+constexpr int kOffMisc = kOffRed + 7 * 128 * 4;        // red[4][128], anchors[128], factors[128], limits[128]
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;       // + alignment slack
 static_assert(kOffP % 1024 == 0 && kOffRing % 1024 == 0 && kOffRot % 1024 == 0,
               "swizzled tiles need 1024-byte alignment");
@@ -101,6 +101,9 @@ __device__ __forceinline__ bool named_bar_any(uint32_t id, uint32_t count, bool 
     return r != 0;
 }
 
+// kPacked: row groups may straddle tokens (packed rows), so visibility is
+// per row; otherwise every row of a group is one token's and shares it.
+template <bool kPacked>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
@@ -130,6 +133,7 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
     float *red = reinterpret_cast<float *>(smem + kOffRed);        // [4][128] per-quadrant row partials
     float *anchor_s = red + 4 * 128;                               // [128] row anchors
     float *alpha_s = anchor_s + 128;                               // [128] rescale factors / 1 / L
+    int *lim_s = reinterpret_cast<int *>(alpha_s + 128);           // [128] keys each row sees in the piece
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
 
@@ -263,9 +267,14 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
             if (pw == 0 && lane == 0) {
                 const uint32_t q_full0 = cluster_addr(q_full, 0);
                 mbar_arrive_expect_tx_relaxed_cluster(q_full0, (uint32_t)kQBytes);
-                for (int c = 0; c < kDk / 64; ++c)
-                    tma_load_4d_pair(smem_u32(sQ + c * kQChunkBytes), &tm_q, q_full0, c * 64,
-                                     x.h0 + (int)rank * kRowsCta, x.t, x.b);
+                for (int c = 0; c < kDk / 64; ++c) {
+                    if (kPacked)       // rows past the last (token, head) read as zeros
+                        tma_load_3d_pair(smem_u32(sQ + c * kQChunkBytes), &tm_q, q_full0, c * 64,
+                                         x.row0 + (int)rank * kRowsCta, x.b);
+                    else
+                        tma_load_4d_pair(smem_u32(sQ + c * kQChunkBytes), &tm_q, q_full0, c * 64,
+                                         x.h0 + (int)rank * kRowsCta, x.t, x.b);
+                }
             }
             __syncwarp();
             ++nq;
@@ -433,14 +442,15 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
         // Per-row maxima of the scaled, masked scores of S^T at `sa` over this
         // CTA's keys: red[q4][row] per warp, then thread tsw < 128 combines row
         // tsw; returns it (other threads: -inf).
-        auto rows_max_own = [&](uint32_t sa, bool vis) -> float {
+        auto rows_max_own = [&](uint32_t sa, int tok, bool uni, bool vis) -> float {
 #pragma unroll
             for (int c = 0; c < kRowsCta; c += 16) {
                 float v[16];
                 tmem_ld16(sa + c, v);
                 tmem_wait_ld();
 #pragma unroll
-                for (int k = 0; k < 16; ++k) v[k] = vis ? v[k] * c2 : kNegInf;
+                for (int k = 0; k < 16; ++k)
+                    v[k] = (uni ? vis : tok < lim_s[row_base + c + k]) ? v[k] * c2 : kNegInf;
                 dec::warp_rows_reduce<16, true>(v, lane, red + q4 * 128 + row_base + c);
             }
             named_bar_sync(1, 256);
@@ -451,17 +461,32 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
         it.init(p, pair, npairs);
         dec::LatentPiece x;
         while (it.next(p, x)) {
-            // Keys the piece's token sees: its causal bound, and no key past
-            // the piece (a step's second half may lie beyond a piece that
-            // holds an odd number of tiles; those keys belong to the next).
-            const int lim = min(x.k_end, x.n - p.q_len + x.t + 1);
+            // lim_s[r]: keys row r sees in the piece -- its token's causal
+            // bound, and no key past the piece (a step's second half may lie
+            // beyond a piece that holds an odd number of tiles; those keys
+            // belong to the next); 0 for a padding row past the last packed
+            // row.  Rows of one group may belong to different tokens.
+            if (tsw < 128) {
+                const int gr = x.row0 + tsw;
+                lim_s[tsw] = gr < p.q_len * p.G ? min(x.k_end, x.n - p.q_len + gr / p.G + 1) : 0;
+            }
+            named_bar_sync(1, 256);
+            // A key below every limit of the warp's 64 rows is visible to all
+            // of them, one at or above every limit to none: then one test
+            // serves the whole row set (always, unless the rows straddle a
+            // token boundary near this key).
+            int lim_lo = lim_s[row_base], lim_hi = lim_lo;
+            for (int r = 1; r < kRowsCta; ++r) {
+                lim_lo = min(lim_lo, lim_s[row_base + r]);
+                lim_hi = max(lim_hi, lim_s[row_base + r]);
+            }
             const int nsteps = (x.ntiles + 1) >> 1;
             float lp[2][32];
 #pragma unroll
             for (int r = 0; r < 32; ++r) { lp[0][r] = 0.f; lp[1][r] = 0.f; }
             for (int s = 0; s < nsteps; ++s, ++jt) {
                 const int tok = x.k_begin + s * kStepKeys + (int)rank * kKeysCta + key;
-                const bool vis = tok < lim;
+                const bool vis = tok < lim_lo, uni = !kPacked || vis || tok >= lim_hi;
                 const uint32_t sb = jt & 1;
                 mbar_wait(&s_full[sb], (jt >> 1) & 1, wc);
                 tc_fence_after();
@@ -470,7 +495,7 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
                     // anchor_s[r]: row r's max over the piece's first step, both
                     // CTAs' keys (0 for a row that sees no key here, and hence
                     // none later in the piece).
-                    const float own = rows_max_own(sa, vis);
+                    const float own = rows_max_own(sa, tok, uni, vis);
                     const uint32_t par = exchange_rows(own);
                     if (tsw < 128) {
                         const float mx = fmaxf(own, xr[par * 128 + tsw]);
@@ -480,6 +505,8 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
                 } else {
                     // The check: the largest exponent this step would raise any
                     // row to, on either CTA.
+                    // (tcgen05.ld is warp-collective: every lane loads, and a
+                    // lane whose key no row sees discards what it loaded.)
                     float xmax = kNegInf;
 #pragma unroll
                     for (int c = 0; c < kRowsCta; c += 16) {
@@ -489,11 +516,18 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
 #pragma unroll
                         for (int k = 0; k < 16; k += 4) {
                             const float4 a = *reinterpret_cast<const float4 *>(anchor_s + row_base + c + k);
-                            xmax = fmaxf(xmax, fmaxf(fmaxf(fmaf(s16[k], c2, -a.x), fmaf(s16[k + 1], c2, -a.y)),
-                                                     fmaxf(fmaf(s16[k + 2], c2, -a.z), fmaf(s16[k + 3], c2, -a.w))));
+                            float e0 = fmaf(s16[k], c2, -a.x), e1 = fmaf(s16[k + 1], c2, -a.y);
+                            float e2 = fmaf(s16[k + 2], c2, -a.z), e3 = fmaf(s16[k + 3], c2, -a.w);
+                            if (!uni) {            // rows of two tokens meet near this key
+                                const int4 L = *reinterpret_cast<const int4 *>(lim_s + row_base + c + k);
+                                e0 = tok < L.x ? e0 : kNegInf; e1 = tok < L.y ? e1 : kNegInf;
+                                e2 = tok < L.z ? e2 : kNegInf; e3 = tok < L.w ? e3 : kNegInf;
+                            }
+                            xmax = fmaxf(xmax, fmaxf(fmaxf(e0, e1), fmaxf(e2, e3)));
                         }
                     }
-                    const bool mine = named_bar_any(1, 256, vis && xmax > kAnchorSlack);
+                    if (uni && !vis) xmax = kNegInf;
+                    const bool mine = named_bar_any(1, 256, xmax > kAnchorSlack);
                     const uint32_t par = xc & 1;
                     if (tsw == 0) {
                         mbar_arrive_expect_tx(&xbar[par], 4);                   // the partner's verdict
@@ -505,7 +539,7 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
                         // Some score rose more than kAnchorSlack above its anchor:
                         // move those anchors to this step's row max and rescale l
                         // and O^T (once the previous PV has landed).
-                        const float own = rows_max_own(sa, vis);
+                        const float own = rows_max_own(sa, tok, uni, vis);
                         const uint32_t par2 = exchange_rows(own);
                         if (tsw < 128) {
                             const float mx = fmaxf(own, xr[par2 * 128 + tsw]);
@@ -550,10 +584,17 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
 #pragma unroll
                     for (int k = 0; k < 16; k += 4) {
                         const float4 a = *reinterpret_cast<const float4 *>(anchor_s + row_base + c + k);
-                        const float p0 = vis ? ex2_approx(fmaf(s16[k], c2, -a.x)) : 0.f;
-                        const float p1 = vis ? ex2_approx(fmaf(s16[k + 1], c2, -a.y)) : 0.f;
-                        const float p2 = vis ? ex2_approx(fmaf(s16[k + 2], c2, -a.z)) : 0.f;
-                        const float p3 = vis ? ex2_approx(fmaf(s16[k + 3], c2, -a.w)) : 0.f;
+                        float p0 = ex2_approx(fmaf(s16[k], c2, -a.x)), p1 = ex2_approx(fmaf(s16[k + 1], c2, -a.y));
+                        float p2 = ex2_approx(fmaf(s16[k + 2], c2, -a.z)), p3 = ex2_approx(fmaf(s16[k + 3], c2, -a.w));
+                        // Masking by selection (an invisible key's score may be
+                        // anything); per row only when two tokens meet near the key.
+                        if (kPacked && !uni) {
+                            const int4 L = *reinterpret_cast<const int4 *>(lim_s + row_base + c + k);
+                            p0 = tok < L.x ? p0 : 0.f; p1 = tok < L.y ? p1 : 0.f;
+                            p2 = tok < L.z ? p2 : 0.f; p3 = tok < L.w ? p3 : 0.f;
+                        } else {
+                            p0 = vis ? p0 : 0.f; p1 = vis ? p1 : 0.f; p2 = vis ? p2 : 0.f; p3 = vis ? p3 : 0.f;
+                        }
                         const int li = (c + k) >> 5, lj = (c + k) & 31;
                         lp[li][lj] += p0; lp[li][lj + 1] += p1; lp[li][lj + 2] += p2; lp[li][lj + 3] += p3;
                         pk[(c + k) >> 1] = pack_bf16x2(p0, p1);
@@ -606,31 +647,34 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
             named_bar_sync(1, 256);
             const float own = tsw < 128 ? (red[tsw] + red[128 + tsw]) + (red[256 + tsw] + red[384 + tsw]) : 0.f;
             const uint32_t par = exchange_rows(own);
-            const int64_t row0 = ((int64_t)x.b * p.q_len + x.t) * p.Hq + x.h0;
+            // Packed row gr of the unit is token gr / G, head g * G + gr % G;
+            // rows past q_len * G are padding and write nothing.
+            const int qG = p.q_len * p.G;
+            const int64_t wrow_b = (int64_t)x.b * p.q_len * p.Hq;      // workspace row of (b, 0, 0)
             if (tsw < 128) {
                 const float L = own + xr[par * 128 + tsw];
                 alpha_s[tsw] = L > 0.f ? 1.f / L : 0.f;
                 const float lse2 = L > 0.f ? anchor_s[tsw] + __log2f(L) : kNegInf;
-                if (rank == 0) {
+                const int gr = x.row0 + tsw;
+                if (rank == 0 && gr < qG) {
+                    const int t = gr / p.G, h = x.g * p.G + gr % p.G;
                     if (x.single) {
                         if (p.lse)
-                            p.lse[x.b * p.lse_stride[0] + x.t * p.lse_stride[1] + (x.h0 + tsw) * p.lse_stride[2]] =
+                            p.lse[x.b * p.lse_stride[0] + t * p.lse_stride[1] + h * p.lse_stride[2]] =
                                 lse2 * 0.69314718055994531f;
                     } else {
-                        p.ws_lse[(row0 + tsw) * p.max_pieces + x.k] = lse2;
+                        p.ws_lse[(wrow_b + (int64_t)t * p.Hq + h) * p.max_pieces + x.k] = lse2;
                     }
                 }
             }
             named_bar_sync(1, 256);
             mbar_wait(pv_done, (jt - 1) & 1, wc);
             tc_fence_after();
-            // Thread = value column dh * 256 + rank * 128 + key; rows walk with
-            // a running offset (a warp stores 32 consecutive columns of a row).
+            // Thread = value column dh * 256 + rank * 128 + key; a warp stores
+            // 32 consecutive columns of one row at a time.
             const int col = (int)rank * 128 + key;
-            __nv_bfloat16 *obase = reinterpret_cast<__nv_bfloat16 *>(p.out) + x.b * p.out_stride[0] +
-                                   x.t * p.out_stride[1] + (x.h0 + row_base) * p.out_stride[2] + col;
-            float *wbase = p.ws_o + ((row0 + row_base) * p.max_pieces + x.k) * kDv + col;
-            const int64_t ostep = p.out_stride[2], wstep = (int64_t)p.max_pieces * kDv;
+            __nv_bfloat16 *obase = reinterpret_cast<__nv_bfloat16 *>(p.out) + x.b * p.out_stride[0] + col;
+            float *wbase = p.ws_o + col;
 #pragma unroll 1
             for (int dh = 0; dh < 2; ++dh) {
 #pragma unroll 1
@@ -638,15 +682,19 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
                     float o[16];
                     tmem_ld16(tmem + lane_off + kColO + dh * 128 + row_base + r0, o);
                     tmem_wait_ld();
-                    if (x.single) {
-                        __nv_bfloat16 *op = obase + r0 * ostep + dh * 256;
+                    const int gr0 = x.row0 + row_base + r0;
+                    int t = gr0 / p.G, hl = gr0 % p.G;
 #pragma unroll
-                        for (int k = 0; k < 16; ++k, op += ostep)
-                            *op = __float2bfloat16_rn(o[k] * alpha_s[row_base + r0 + k]);
-                    } else {
-                        float *wp = wbase + r0 * wstep + dh * 256;
-#pragma unroll
-                        for (int k = 0; k < 16; ++k, wp += wstep) *wp = o[k] * alpha_s[row_base + r0 + k];
+                    for (int k = 0; k < 16; ++k) {
+                        if (gr0 + k < qG) {
+                            const int h = x.g * p.G + hl;
+                            const float v = o[k] * alpha_s[row_base + r0 + k];
+                            if (x.single)
+                                obase[t * p.out_stride[1] + h * p.out_stride[2] + dh * 256] = __float2bfloat16_rn(v);
+                            else
+                                wbase[((wrow_b + (int64_t)t * p.Hq + h) * p.max_pieces + x.k) * kDv + dh * 256] = v;
+                        }
+                        if (++hl == p.G) { hl = 0; ++t; }
                     }
                 }
             }
@@ -673,8 +721,11 @@ cudaError_t launch_latent_pair_decode(const DecodeParams &p, const CUtensorMap &
     if (p.grid % 2 != 0) return cudaErrorInvalidValue;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(latent_pair_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(latent_pair_decode_kernel<false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(latent_pair_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kSmemBytes);
         if (e != cudaSuccess) return e;
         configured = true;
     }
@@ -682,7 +733,8 @@ cudaError_t launch_latent_pair_decode(const DecodeParams &p, const CUtensorMap &
     if (e != cudaSuccess) return e;
     ++*launches;
     if (timing_start) cudaEventRecord(timing_start, stream);
-    latent_pair_decode_kernel<<<p.grid, kThreads, kSmemBytes, stream>>>(p, tq, tk, tv);
+    if (p.packed) latent_pair_decode_kernel<true><<<p.grid, kThreads, kSmemBytes, stream>>>(p, tq, tk, tv);
+    else latent_pair_decode_kernel<false><<<p.grid, kThreads, kSmemBytes, stream>>>(p, tq, tk, tv);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     ++*launches;

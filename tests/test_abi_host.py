@@ -94,8 +94,25 @@ def test_planner_latent_row_groups_ride_on_the_grid(fwlib, q_len, hq, hkv, sms, 
 
 
 def test_planner_latent_rejects_partial_head_blocks(fwlib):
+    """Several KV heads: a row group holds one token's heads, so 48 heads per
+    KV head (not a multiple of 64) cannot be served."""
     with pytest.raises(fwlib.FwError):
-        fwlib.plan_decode(2, 1, 96, 1, 512, 4096, num_sms=152)
+        fwlib.plan_decode(2, 1, 96, 2, 512, 4096, num_sms=152)
+
+
+@pytest.mark.parametrize("hq,q_len", [(96, 4), (96, 8), (128, 4), (64, 2), (48, 3), (16, 4), (16, 1), (32, 3)])
+def test_planner_latent_packed_rows(fwlib, hq, q_len):
+    """One KV head: query rows are packed as token * H + head ("TokenSpeed-MLA
+    2.0.1", packed-query paragraph).  At 128 or more rows the groups are the
+    pages' 128-row query tiles, ceil(H * q_len / 128) of them (H96/Sq4 -> 3,
+    H96/Sq8 -> 6), on CTA pairs; fewer rows make 64-row groups on one CTA."""
+    p = fwlib.plan_decode(4, q_len, hq, 1, 512, 8192, num_sms=152)
+    if hq * q_len >= 128:
+        assert p["rows_per_unit"] == 128
+        assert p["row_groups"] == planning.packed_q_tiles(hq, q_len)
+        assert p["grid"] % (2 * p["row_groups"]) == 0
+    else:
+        assert p["rows_per_unit"] == 64 and p["row_groups"] == -(-hq * q_len // 64)
 
 
 def test_planner_workspace_matches_pages_formula(fwlib):

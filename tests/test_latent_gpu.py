@@ -5,7 +5,8 @@ The layout of "TokenSpeed-MLA 2.0.1" (decode): one KV head whose 576-wide rows
 are the keys and whose first 512 columns are the values, 128 query heads, up
 to four query tokens with bottom-right causal rows.  Covers ragged lengths
 around tile and page boundaries (NaN-poisoned slots past each row's end),
-rows that see no key, q_len 1-4, 64-head groups and two KV heads, page sizes
+rows that see no key, q_len 1-4, 64-head groups and two KV heads, packed
+(token, head) rows for head counts that are not a multiple of 64, page sizes
 16-256, forced split-KV chunking, score scales large enough to move the
 static anchors, a separate (non-aliased) value cache, and the full-size
 workload on sampled rows.
@@ -98,6 +99,22 @@ def test_scales_that_move_the_anchor(fw, scale):
     run_case(fw, wl_latent([2000, 1300], q_len=2, scale=scale, seed=23))
 
 
+@pytest.mark.parametrize("hq,q_len", [(16, 4), (16, 1), (96, 4), (64, 2), (48, 3), (32, 4)])
+def test_packed_query_rows(fw, hq, q_len):
+    """Head counts that are not a multiple of the row group: rows packed as
+    token * H + head, so a row group straddles tokens (each row keeps its own
+    causal bound) and the last group is padded.  Short rows (1-5 keys) make
+    whole tokens see nothing."""
+    run_case(fw, wl_latent([1, 3, 5, 130, 700], q_len=q_len, hq=hq, seed=27))
+
+
+@pytest.mark.parametrize("chunk", [128, 1024])
+def test_packed_query_rows_with_splits(fw, chunk):
+    """Packed rows (H96, q_len 4: three 128-row groups) with many split-KV
+    pieces merged by the combine kernel."""
+    run_case(fw, wl_latent([3000, 257, 1800], q_len=4, hq=96, seed=29), chunk=chunk)
+
+
 def test_separate_value_cache(fw):
     """Dv = 512 values from their own cache instead of a view of the keys."""
     run_case(fw, wl_latent([333, 1200], q_len=2, aliased=False, seed=25))
@@ -134,7 +151,7 @@ def test_invalid_latent_shapes_launch_nothing(fw):
     wl = wl_latent([100], hq=128)
     d = to_device(make_decode_inputs(wl, "cpu"))
     before = fw.launch_count()
-    with pytest.raises(fw.FwError):                     # 96 heads: not a multiple of 64
+    with pytest.raises(fw.FwError):                     # 96 of 128 heads: q not one stride over (token, head)
         fw.paged_decode(d["q"][:, :, :96], d["k_cache"], d["k_cache"][..., :512], d["block_table"],
                         d["seq_lens"], 0.1)
     with pytest.raises(fw.FwError):                     # Dv 512 with Dk 512: not the latent layout
