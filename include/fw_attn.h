@@ -181,10 +181,10 @@ fw_status_t fw_paged_decode_fp8(const fw_tensor_t *q, const fw_tensor_t *k_cache
  * the work scales with the window, not the row.  Block-table entries of pages
  * wholly before key max(0, n - q_len - W) are never read and those pages are
  * never loaded: a cache may drop pages that left the window.  Supported: the
- * grouped-query layouts of fw_paged_decode (Dk = Dv in {128, 256}) and of
- * fw_paged_decode_fp8; the latent layout (Dk 576, Dv 512) returns
- * FW_ERR_UNSUPPORTED when W >= 0.  FW_ERR_INVALID_ARG for W < -1 or BF16
- * caches with scales other than 1.  Same workspace as fw_paged_decode.
+ * layouts of fw_paged_decode (Dk = Dv in {128, 256}, and the latent Dk 576 /
+ * Dv 512, where TokenSpeed defines window_left) and of fw_paged_decode_fp8.
+ * FW_ERR_INVALID_ARG for W < -1 or BF16 caches with scales other than 1.
+ * Same workspace as fw_paged_decode.
  */
 fw_status_t fw_paged_decode_window(const fw_tensor_t *q, const fw_tensor_t *k_cache,
                                    const fw_tensor_t *v_cache, const fw_tensor_t *block_table,

@@ -555,8 +555,6 @@ static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_
         return fail(FW_ERR_INVALID_ARG, "lse must be [B, q_len, Hq]");
     if (!std::isfinite(scale)) return fail(FW_ERR_INVALID_ARG, "scale must be finite");
     const bool latent = !kv8 && (Dk == 576 && Dv == 512);
-    if (latent && window_left >= 0)
-        return fail(FW_ERR_UNSUPPORTED, "sliding windows are served for Dk = Dv in {128, 256} (BF16) and 128 (FP8)");
     if (latent && append)
         return fail(FW_ERR_UNSUPPORTED, "the fused append serves the grouped-query layouts (append latent rows "
                     "with fw_kv_append)");

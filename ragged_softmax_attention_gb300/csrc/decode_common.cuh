@@ -99,7 +99,7 @@ struct PieceIter {
 // unit, packed row i being token i / G, head g * G + i % G (when G is a
 // multiple of `rows` a group is one token's heads h0 .. h0 + rows).
 struct LatentPiece {
-    int b, g, t, h0, row0, n, k_begin, k_end, ntiles, k;
+    int b, g, t, h0, row0, n, lo, k_begin, k_end, ntiles, k;   // lo: first key any row may see
     bool single;
 };
 
@@ -153,8 +153,10 @@ struct LatentIter {
         x.t = x.row0 / p.G;
         x.h0 = u * p.G + x.row0 % p.G;
         x.n = clamp_len(p, __ldg(p.seq_lens + b));
-        x.k_begin = tl * kKvTile;
-        x.k_end = min(x.n, th * kKvTile);
+        x.lo = window_first_key(p, x.n);
+        const int t0 = x.lo / kKvTile;               // the walk starts at the window's first tile
+        x.k_begin = (t0 + tl) * kKvTile;
+        x.k_end = min(x.n, (t0 + th) * kKvTile);
         x.ntiles = th - tl;
         x.k = (pstart + tl) / span - pstart / span;
         x.single = ((pstart + tb - 1) / span == pstart / span);

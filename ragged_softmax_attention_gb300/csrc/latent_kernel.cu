@@ -66,7 +66,7 @@ constexpr int kOffP = kOffRing + kSlots * kSlotBytes;
 constexpr int kOffBar = kOffP + kPBytes;
 constexpr int kNumBars = 2 * kSlots + 2 + 2 + 1 + 1 + 1 + 1 + 1 + 1;
 constexpr int kOffRed = kOffBar + ((kNumBars * 8 + 127) / 128) * 128;
-constexpr int kOffMisc = kOffRed + 7 * kRows * 4;       // [4][64] partials + [64] anchors, factors, limits
+constexpr int kOffMisc = kOffRed + 8 * kRows * 4;       // [4][64] partials + [64] anchors, factors, upper/lower limits
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;        // + alignment slack
 static_assert(kOffRing % 1024 == 0 && kOffP % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA exceeded");
@@ -142,7 +142,8 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
     float *red = reinterpret_cast<float *>(smem + kOffRed);        // [4][64] per-warp row partials
     float *anchor_s = red + 4 * kRows;                             // [64] row anchors
     float *alpha_s = anchor_s + kRows;                             // [64] rescale factors / 1 / L
-    int *lim_s = reinterpret_cast<int *>(alpha_s + kRows);         // [64] keys each row sees in the piece
+    int *lim_s = reinterpret_cast<int *>(alpha_s + kRows);         // [64] end of the keys each row sees
+    int *lo_s = lim_s + kRows;                                     // [64] first key each row sees
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
 
@@ -183,28 +184,35 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
         // Physical pages of the 128-key tile at key ts of row b: lane l holds
         // the tile's l-th page (l < pages in the tile).  Read one tile ahead
         // of use, so no chunk load waits on the block table.
-        auto tile_pages = [&](int b, int ts, int k_end) {
+        // Leading pages of the tile at ts wholly before k_lo (the first key
+        // of a sliding window) are never looked up nor loaded.
+        auto skip_of = [&](int ts, int k_lo) { return p.ps >= kKvTile ? 0 : max(0, k_lo / p.ps - ts / p.ps); };
+        auto tile_pages = [&](int b, int ts, int k_end, int k_lo) {
             int npages = 1;
             if (p.ps < kKvTile) npages = min(kKvTile / p.ps, ceil_div_i(k_end - ts, p.ps));
             int phys = 0;
-            if (lane < npages) phys = __ldg(p.block_table + (int64_t)b * p.bt_stride + ts / p.ps + lane);
+            if (lane >= skip_of(ts, k_lo) && lane < npages)
+                phys = __ldg(p.block_table + (int64_t)b * p.bt_stride + ts / p.ps + lane);
             return phys;
         };
-        auto load_chunk = [&](int g, int ts, int k_end, int phys, const CUtensorMap *tm, int c, bool zero_tail) -> bool {
+        auto load_chunk = [&](int g, int ts, int k_end, int k_lo, int phys, const CUtensorMap *tm, int c,
+                              bool zero_tail) -> bool {
             const uint32_t s = m % kSlots;
             if (!warp_wait(&slot_empty[s], ((m / kSlots) & 1) ^ 1, wc, lane)) return false;
             const int halves = c < 4 ? 2 : 1;
             int npages = 1, slot0 = 0;
             if (p.ps < kKvTile) npages = min(kKvTile / p.ps, ceil_div_i(k_end - ts, p.ps));
             else slot0 = ts % p.ps;
-            if (lane < npages && (unsigned)phys >= (unsigned)p.num_pages) { record_error(p.status, 1); phys = 0; }
-            const bool zero = zero_tail && ts + kKvTile > k_end;
+            const int skip = min(npages, skip_of(ts, k_lo));
+            const bool load = lane >= skip && lane < npages;
+            if (load && (unsigned)phys >= (unsigned)p.num_pages) { record_error(p.status, 1); phys = 0; }
+            const bool zero = zero_tail && (ts + kKvTile > k_end || skip > 0);
             uint64_t *bar = zero ? tail_bar : &slot_full[s];
-            const uint32_t bytes = (uint32_t)(npages * box_rows * 128 * halves);
+            const uint32_t bytes = (uint32_t)((npages - skip) * box_rows * 128 * halves);
             uint8_t *dst = sRing + s * kSlotBytes;
             if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
             __syncwarp();
-            if (lane < npages) {
+            if (load) {
                 for (int h = 0; h < halves; ++h)
                     tma_load_4d(smem_u32(dst + h * kHalfBytes + lane * box_rows * 128), tm, bar,
                                 c * 128 + h * 64, g, slot0, phys);
@@ -217,9 +225,15 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
                     return false;
                 }
                 ++ntail;
-                const int r0 = k_end - ts;
+                // Rows at or past k_end, and rows of pages skipped before the window.
+                const int r0 = min(kKvTile, k_end - ts), rh = skip * p.ps;
                 for (int idx = lane; idx < (kKvTile - r0) * 16; idx += 32) {
                     const int row = r0 + (idx >> 4);
+                    const int h = (idx >> 3) & 1;
+                    reinterpret_cast<uint4 *>(dst + h * kHalfBytes + row * 128)[idx & 7] = make_uint4(0, 0, 0, 0);
+                }
+                for (int idx = lane; idx < min(rh, r0) * 16; idx += 32) {
+                    const int row = idx >> 4;
                     const int h = (idx >> 3) & 1;
                     reinterpret_cast<uint4 *>(dst + h * kHalfBytes + row * 128)[idx & 7] = make_uint4(0, 0, 0, 0);
                 }
@@ -231,7 +245,7 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
             return true;
         };
         bool ok = true;
-        int pb = -1, pg = 0, pts = 0, pend_end = 0, pphys = 0;   // the tile whose PV is still to be fed
+        int pb = -1, pg = 0, pts = 0, pend_end = 0, pend_lo = 0, pphys = 0;   // the tile whose PV is still to be fed
         dec::LatentIter it;
         it.init(p, blockIdx.x, gridDim.x);
         dec::LatentPiece x;
@@ -248,20 +262,22 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
             }
             __syncwarp();
             ++nq;
-            int nphys = tile_pages(x.b, x.k_begin, x.k_end);
+            int nphys = tile_pages(x.b, x.k_begin, x.k_end, x.lo);
             for (int i = 0; i < x.ntiles && ok; ++i) {
                 const int ts = x.k_begin + i * kKvTile;
                 const int phys = nphys;
-                if (i + 1 < x.ntiles) nphys = tile_pages(x.b, ts + kKvTile, x.k_end);
-                for (int c = 0; c < kQkChunks && ok; ++c) ok = load_chunk(x.g, ts, x.k_end, phys, &tm_k, c, false);
+                if (i + 1 < x.ntiles) nphys = tile_pages(x.b, ts + kKvTile, x.k_end, x.lo);
+                for (int c = 0; c < kQkChunks && ok; ++c)
+                    ok = load_chunk(x.g, ts, x.k_end, x.lo, phys, &tm_k, c, false);
                 if (pb >= 0)
                     for (int c = 0; c < kPvChunks && ok; ++c)
-                        ok = load_chunk(pg, pts, pend_end, pphys, &tm_v, c, true);
-                pb = x.b; pg = x.g; pts = ts; pend_end = x.k_end; pphys = phys;
+                        ok = load_chunk(pg, pts, pend_end, pend_lo, pphys, &tm_v, c, true);
+                pb = x.b; pg = x.g; pts = ts; pend_end = x.k_end; pend_lo = x.lo; pphys = phys;
             }
         }
         if (ok && pb >= 0)
-            for (int c = 0; c < kPvChunks && ok; ++c) ok = load_chunk(pg, pts, pend_end, pphys, &tm_v, c, true);
+            for (int c = 0; c < kPvChunks && ok; ++c)
+                ok = load_chunk(pg, pts, pend_end, pend_lo, pphys, &tm_v, c, true);
         // Do not leave the CTA while copies it issued may still land.
         if (lane == 0) {
             for (uint32_t k = 0; k < (uint32_t)kSlots && k < m; ++k) {
@@ -364,7 +380,8 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
                 tmem_wait_ld();
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
-                    const float v = warp_max((uni ? vis : tok < lim_s[c + k]) ? s16[k] * c2 : kNegInf);
+                    const float v =
+                        warp_max((uni ? vis : (tok >= lo_s[c + k] && tok < lim_s[c + k])) ? s16[k] * c2 : kNegInf);
                     if (lane == 0) red[q4 * kRows + c + k] = v;
                 }
             }
@@ -377,28 +394,35 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
         it.init(p, blockIdx.x, gridDim.x);
         dec::LatentPiece x;
         while (it.next(p, x)) {
-            // lim_s[r]: keys row r sees in the piece (its token's causal
-            // bound); 0 for a padding row past the last packed row.  Rows of
-            // one group may belong to different tokens.
+            // Row r sees keys lo_s[r] .. lim_s[r] - 1: from its window's first
+            // key (0 without a window) to its token's causal bound; nothing
+            // for a padding row past the last packed row.  Rows of one group
+            // may belong to different tokens.
             if (key < kRows) {
                 const int gr = x.row0 + key;
-                lim_s[key] = gr < p.q_len * p.G ? min(x.k_end, x.n - p.q_len + gr / p.G + 1) : 0;
+                const int pos = x.n - p.q_len + gr / p.G;             // the row's own key position
+                const bool real = gr < p.q_len * p.G;
+                lim_s[key] = real ? min(x.k_end, pos + 1) : 0;
+                lo_s[key] = real && p.window_left >= 0 ? max(0, pos - p.window_left) : 0;
             }
             named_bar_sync(1, 128);
-            // A key below every row's limit is visible to all rows, one at or
-            // above every limit to none: one test then serves the row set
+            // A key inside every row's range is visible to all rows, one
+            // outside all of them to none: one test then serves the row set
             // (always, unless the rows straddle a token boundary near it).
-            int lim_lo = lim_s[0], lim_hi = lim_lo;
+            int hi_min = lim_s[0], hi_max = hi_min, lo_min = lo_s[0], lo_max = lo_min;
             for (int r = 1; r < kRows; ++r) {
-                lim_lo = min(lim_lo, lim_s[r]);
-                lim_hi = max(lim_hi, lim_s[r]);
+                hi_min = min(hi_min, lim_s[r]);
+                hi_max = max(hi_max, lim_s[r]);
+                lo_min = min(lo_min, lo_s[r]);
+                lo_max = max(lo_max, lo_s[r]);
             }
             float l_part[kRows];
 #pragma unroll
             for (int r = 0; r < kRows; ++r) l_part[r] = 0.f;
             for (int i = 0; i < x.ntiles; ++i, ++jt) {
                 const int tok = x.k_begin + i * kKvTile + key;
-                const bool vis = tok < lim_lo, uni = !kPacked || vis || tok >= lim_hi;
+                const bool vis = tok >= lo_max && tok < hi_min;
+                const bool uni = !kPacked || vis || tok < lo_min || tok >= hi_max;
                 const uint32_t sb = jt & 1;
                 mbar_wait(&s_full[sb], (jt >> 1) & 1, wc);
                 tc_fence_after();
@@ -431,8 +455,9 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
                             float e2 = fmaf(s16[k + 2], c2, -a.z), e3 = fmaf(s16[k + 3], c2, -a.w);
                             if (!uni) {            // rows of two tokens meet near this key
                                 const int4 L = *reinterpret_cast<const int4 *>(lim_s + c + k);
-                                e0 = tok < L.x ? e0 : kNegInf; e1 = tok < L.y ? e1 : kNegInf;
-                                e2 = tok < L.z ? e2 : kNegInf; e3 = tok < L.w ? e3 : kNegInf;
+                                const int4 F = *reinterpret_cast<const int4 *>(lo_s + c + k);
+                                e0 = tok >= F.x && tok < L.x ? e0 : kNegInf; e1 = tok >= F.y && tok < L.y ? e1 : kNegInf;
+                                e2 = tok >= F.z && tok < L.z ? e2 : kNegInf; e3 = tok >= F.w && tok < L.w ? e3 : kNegInf;
                             }
                             xmax = fmaxf(xmax, fmaxf(fmaxf(e0, e1), fmaxf(e2, e3)));
                         }
@@ -490,8 +515,9 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
                         // anything); per row only when two tokens meet near the key.
                         if (kPacked && !uni) {
                             const int4 L = *reinterpret_cast<const int4 *>(lim_s + c + k);
-                            p0 = tok < L.x ? p0 : 0.f; p1 = tok < L.y ? p1 : 0.f;
-                            p2 = tok < L.z ? p2 : 0.f; p3 = tok < L.w ? p3 : 0.f;
+                            const int4 F = *reinterpret_cast<const int4 *>(lo_s + c + k);
+                            p0 = tok >= F.x && tok < L.x ? p0 : 0.f; p1 = tok >= F.y && tok < L.y ? p1 : 0.f;
+                            p2 = tok >= F.z && tok < L.z ? p2 : 0.f; p3 = tok >= F.w && tok < L.w ? p3 : 0.f;
                         } else {
                             p0 = vis ? p0 : 0.f; p1 = vis ? p1 : 0.f; p2 = vis ? p2 : 0.f; p3 = vis ? p3 : 0.f;
                         }

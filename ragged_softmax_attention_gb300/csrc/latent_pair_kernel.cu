@@ -72,7 +72,7 @@ constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 1 + 1 + 2 + 1 + 2 + 1;
 constexpr int kThreads = 352;                          // 11 warps: see the roles below
 constexpr int kOffX = kOffBar + ((kNumBars * 8 + 127) / 128) * 128;
 constexpr int kOffRed = kOffX + (2 * 128 + 32) * 4;    // xr[2][128] from the partner, xf[2] + pad
-constexpr int kOffMisc = kOffRed + 7 * 128 * 4;        // red[4][128], anchors[128], factors[128], limits[128]
+constexpr int kOffMisc = kOffRed + 8 * 128 * 4;        // red[4][128], anchors, factors, upper and lower limits
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;       // + alignment slack
 static_assert(kOffP % 1024 == 0 && kOffRing % 1024 == 0 && kOffRot % 1024 == 0,
               "swizzled tiles need 1024-byte alignment");
@@ -133,7 +133,8 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
     float *red = reinterpret_cast<float *>(smem + kOffRed);        // [4][128] per-quadrant row partials
     float *anchor_s = red + 4 * 128;                               // [128] row anchors
     float *alpha_s = anchor_s + 128;                               // [128] rescale factors / 1 / L
-    int *lim_s = reinterpret_cast<int *>(alpha_s + 128);           // [128] keys each row sees in the piece
+    int *lim_s = reinterpret_cast<int *>(alpha_s + 128);           // [128] end of the keys each row sees
+    int *lo_s = lim_s + 128;                                       // [128] first key each row sees
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
 
@@ -188,11 +189,17 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
             if (p.ps >= kKeysCta) return 1;
             return min(kKeysCta / p.ps, ceil_div_i(k_end - ks, p.ps));
         };
+        // Leading pages of keys [ks, ks + 128) wholly before k_lo (the first
+        // key of a sliding window): never looked up nor loaded.
+        auto skip_of = [&](int ks, int k_lo) -> int {
+            return p.ps >= kKeysCta ? 0 : max(0, k_lo / p.ps - ks / p.ps);
+        };
         // The load is issued a step before the page is copied; its range
         // check waits until then (in fill), so the walk never stalls on it.
-        auto lookup = [&](int b, int ks, int k_end) -> int {
+        auto lookup = [&](int b, int ks, int k_end, int k_lo) -> int {
             int phys = 0;
-            if (lane < npages_of(ks, k_end)) phys = __ldg(p.block_table + (int64_t)b * p.bt_stride + ks / p.ps + lane);
+            if (lane >= skip_of(ks, k_lo) && lane < npages_of(ks, k_end))
+                phys = __ldg(p.block_table + (int64_t)b * p.bt_stride + ks / p.ps + lane);
             return phys;
         };
         // Keys [ks, ks + 128) below k_end, `ncb` 64-column blocks from column
@@ -201,25 +208,27 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
         // cleared first: their values may be anything, and a zero probability
         // times a NaN is still NaN.
         auto fill = [&](uint64_t *full, uint8_t *dst, const CUtensorMap *tm, int g, int col0, int ncb, int ks,
-                        int k_end, int phys, bool zero_tail) -> bool {
+                        int k_end, int k_lo, int phys, bool zero_tail) -> bool {
             const int np = npages_of(ks, k_end);
+            const int skip = min(np, skip_of(ks, k_lo));
+            const bool load = lane >= skip && lane < np;
             const int slot0 = p.ps >= kKeysCta ? ks % p.ps : 0;
             const uint32_t full0 = cluster_addr(full, 0);
-            if (lane < np && (unsigned)phys >= (unsigned)p.num_pages) { record_error(p.status, 1); phys = 0; }
-            const uint32_t bytes = (uint32_t)(np * box_rows * 128 * ncb);
-            if (!(zero_tail && ks + kKeysCta > k_end)) {
+            if (load && (unsigned)phys >= (unsigned)p.num_pages) { record_error(p.status, 1); phys = 0; }
+            const uint32_t bytes = (uint32_t)((np - skip) * box_rows * 128 * ncb);
+            if (!(zero_tail && (ks + kKeysCta > k_end || skip > 0))) {
                 if (lane == 0) mbar_arrive_expect_tx_relaxed_cluster(full0, bytes);
                 __syncwarp();
-                if (lane < np)
+                if (load)
                     for (int c = 0; c < ncb; ++c)
                         tma_load_4d_pair(smem_u32(dst + c * kHalfBytes + lane * box_rows * 128), tm, full0,
                                          col0 + c * 64, g, slot0, phys);
                 return true;
             }
-            if (np > 0) {
+            if (np > skip) {
                 if (lane == 0) mbar_arrive_expect_tx(my_tail, bytes);
                 __syncwarp();
-                if (lane < np)
+                if (load)
                     for (int c = 0; c < ncb; ++c)
                         tma_load_4d(smem_u32(dst + c * kHalfBytes + lane * box_rows * 128), tm, my_tail,
                                     col0 + c * 64, g, slot0, phys);
@@ -230,9 +239,15 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
                 }
                 ++ntail;
             }
-            const int r0 = max(0, k_end - ks);
+            // Rows of pages skipped before the window, and rows at or past k_end.
+            const int r0 = max(0, k_end - ks), rh = skip * p.ps;
             for (int idx = lane; idx < (kKeysCta - r0) * 8 * ncb; idx += 32) {
                 const int row = r0 + idx / (8 * ncb);
+                const int rem = idx % (8 * ncb);
+                reinterpret_cast<uint4 *>(dst + (rem >> 3) * kHalfBytes + row * 128)[rem & 7] = make_uint4(0, 0, 0, 0);
+            }
+            for (int idx = lane; idx < min(rh, r0) * 8 * ncb; idx += 32) {
+                const int row = idx / (8 * ncb);
                 const int rem = idx % (8 * ncb);
                 reinterpret_cast<uint4 *>(dst + (rem >> 3) * kHalfBytes + row * 128)[rem & 7] = make_uint4(0, 0, 0, 0);
             }
@@ -245,7 +260,7 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
             return true;
         };
         bool ok = true, pend = false;
-        int pg = 0, pts = 0, pend_end = 0, pph0 = 0, pph1 = 0;   // the step whose PV is still to be fed
+        int pg = 0, pts = 0, pend_end = 0, pend_lo = 0, pph0 = 0, pph1 = 0;   // the step whose PV is still to be fed
         // This CTA's value columns of both key halves of the pending step.
         auto feed_pv = [&]() -> bool {
             for (int v = 0; v < 4; ++v, ++m) {
@@ -254,7 +269,7 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
                 const uint32_t sl = m % kSlots;
                 if (!dec::warp_wait(&slot_empty[sl], ((m / kSlots) & 1) ^ 1, wc, lane)) return false;
                 if (!fill(&slot_full[sl], sRing + sl * kSlotBytes, &tm_v, pg, dh * 256 + (int)rank * 128, 2,
-                          pts + kh * kKeysCta, pend_end, kh ? pph1 : pph0, true))
+                          pts + kh * kKeysCta, pend_end, pend_lo, kh ? pph1 : pph0, true))
                     return false;
             }
             return true;
@@ -279,13 +294,13 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
             __syncwarp();
             ++nq;
             const int nsteps = (x.ntiles + 1) >> 1;
-            int ph0 = lookup(x.b, x.k_begin, x.k_end), ph1 = lookup(x.b, x.k_begin + kKeysCta, x.k_end);
+            int ph0 = lookup(x.b, x.k_begin, x.k_end, x.lo), ph1 = lookup(x.b, x.k_begin + kKeysCta, x.k_end, x.lo);
             for (int s = 0; s < nsteps && ok; ++s) {
                 const int ts = x.k_begin + s * kStepKeys;
                 const int c0 = ph0, c1 = ph1;
                 if (s + 1 < nsteps) {
-                    ph0 = lookup(x.b, ts + kStepKeys, x.k_end);
-                    ph1 = lookup(x.b, ts + kStepKeys + kKeysCta, x.k_end);
+                    ph0 = lookup(x.b, ts + kStepKeys, x.k_end, x.lo);
+                    ph1 = lookup(x.b, ts + kStepKeys + kKeysCta, x.k_end, x.lo);
                 }
                 const int own_ks = ts + (int)rank * kKeysCta;
                 const int own_ph = rank ? c1 : c0;
@@ -294,16 +309,16 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
                     const uint32_t sl = m % kSlots;
                     if (!dec::warp_wait(&slot_empty[sl], ((m / kSlots) & 1) ^ 1, wc, lane)) { ok = false; break; }
                     ok = fill(&slot_full[sl], sRing + sl * kSlotBytes, &tm_k, x.g, c * 128, 2, own_ks, x.k_end,
-                              own_ph, false);
+                              x.lo, own_ph, false);
                 }
                 if (!ok) break;
                 if (pw == 0) {
                     if (!dec::warp_wait(rot_empty, (nr & 1) ^ 1, wc, lane)) { ok = false; break; }
-                    ok = fill(rot_full, sRot, &tm_k, x.g, 512, 1, own_ks, x.k_end, own_ph, false);
+                    ok = fill(rot_full, sRot, &tm_k, x.g, 512, 1, own_ks, x.k_end, x.lo, own_ph, false);
                 }
                 ++nr;
                 if (ok && pend) ok = feed_pv();
-                pend = true; pg = x.g; pts = ts; pend_end = x.k_end; pph0 = c0; pph1 = c1;
+                pend = true; pg = x.g; pts = ts; pend_end = x.k_end; pend_lo = x.lo; pph0 = c0; pph1 = c1;
             }
         }
         if (ok && pend) ok = feed_pv();
@@ -450,7 +465,8 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
                 tmem_wait_ld();
 #pragma unroll
                 for (int k = 0; k < 16; ++k)
-                    v[k] = (uni ? vis : tok < lim_s[row_base + c + k]) ? v[k] * c2 : kNegInf;
+                    v[k] = (uni ? vis : (tok >= lo_s[row_base + c + k] && tok < lim_s[row_base + c + k])) ? v[k] * c2
+                                                                                                    : kNegInf;
                 dec::warp_rows_reduce<16, true>(v, lane, red + q4 * 128 + row_base + c);
             }
             named_bar_sync(1, 256);
@@ -461,24 +477,30 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
         it.init(p, pair, npairs);
         dec::LatentPiece x;
         while (it.next(p, x)) {
-            // lim_s[r]: keys row r sees in the piece -- its token's causal
+            // Row r sees keys lo_s[r] .. lim_s[r] - 1 of the piece: from its
+            // window's first key (0 without a window) to its token's causal
             // bound, and no key past the piece (a step's second half may lie
             // beyond a piece that holds an odd number of tiles; those keys
-            // belong to the next); 0 for a padding row past the last packed
-            // row.  Rows of one group may belong to different tokens.
+            // belong to the next); nothing for a padding row past the last
+            // packed row.  Rows of one group may belong to different tokens.
             if (tsw < 128) {
                 const int gr = x.row0 + tsw;
-                lim_s[tsw] = gr < p.q_len * p.G ? min(x.k_end, x.n - p.q_len + gr / p.G + 1) : 0;
+                const int pos = x.n - p.q_len + gr / p.G;             // the row's own key position
+                const bool real = gr < p.q_len * p.G;
+                lim_s[tsw] = real ? min(x.k_end, pos + 1) : 0;
+                lo_s[tsw] = real && p.window_left >= 0 ? max(0, pos - p.window_left) : 0;
             }
             named_bar_sync(1, 256);
-            // A key below every limit of the warp's 64 rows is visible to all
-            // of them, one at or above every limit to none: then one test
-            // serves the whole row set (always, unless the rows straddle a
-            // token boundary near this key).
-            int lim_lo = lim_s[row_base], lim_hi = lim_lo;
+            // A key inside every row's range is visible to all of the warp's 64
+            // rows, one outside all of them to none: then one test serves the
+            // whole row set (always, unless the rows straddle a token boundary
+            // near this key).
+            int hi_min = lim_s[row_base], hi_max = hi_min, lo_min = lo_s[row_base], lo_max = lo_min;
             for (int r = 1; r < kRowsCta; ++r) {
-                lim_lo = min(lim_lo, lim_s[row_base + r]);
-                lim_hi = max(lim_hi, lim_s[row_base + r]);
+                hi_min = min(hi_min, lim_s[row_base + r]);
+                hi_max = max(hi_max, lim_s[row_base + r]);
+                lo_min = min(lo_min, lo_s[row_base + r]);
+                lo_max = max(lo_max, lo_s[row_base + r]);
             }
             const int nsteps = (x.ntiles + 1) >> 1;
             float lp[2][32];
@@ -486,7 +508,8 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
             for (int r = 0; r < 32; ++r) { lp[0][r] = 0.f; lp[1][r] = 0.f; }
             for (int s = 0; s < nsteps; ++s, ++jt) {
                 const int tok = x.k_begin + s * kStepKeys + (int)rank * kKeysCta + key;
-                const bool vis = tok < lim_lo, uni = !kPacked || vis || tok >= lim_hi;
+                const bool vis = tok >= lo_max && tok < hi_min;
+                const bool uni = !kPacked || vis || tok < lo_min || tok >= hi_max;
                 const uint32_t sb = jt & 1;
                 mbar_wait(&s_full[sb], (jt >> 1) & 1, wc);
                 tc_fence_after();
@@ -520,8 +543,9 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
                             float e2 = fmaf(s16[k + 2], c2, -a.z), e3 = fmaf(s16[k + 3], c2, -a.w);
                             if (!uni) {            // rows of two tokens meet near this key
                                 const int4 L = *reinterpret_cast<const int4 *>(lim_s + row_base + c + k);
-                                e0 = tok < L.x ? e0 : kNegInf; e1 = tok < L.y ? e1 : kNegInf;
-                                e2 = tok < L.z ? e2 : kNegInf; e3 = tok < L.w ? e3 : kNegInf;
+                                const int4 F = *reinterpret_cast<const int4 *>(lo_s + row_base + c + k);
+                                e0 = tok >= F.x && tok < L.x ? e0 : kNegInf; e1 = tok >= F.y && tok < L.y ? e1 : kNegInf;
+                                e2 = tok >= F.z && tok < L.z ? e2 : kNegInf; e3 = tok >= F.w && tok < L.w ? e3 : kNegInf;
                             }
                             xmax = fmaxf(xmax, fmaxf(fmaxf(e0, e1), fmaxf(e2, e3)));
                         }
@@ -590,8 +614,9 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
                         // anything); per row only when two tokens meet near the key.
                         if (kPacked && !uni) {
                             const int4 L = *reinterpret_cast<const int4 *>(lim_s + row_base + c + k);
-                            p0 = tok < L.x ? p0 : 0.f; p1 = tok < L.y ? p1 : 0.f;
-                            p2 = tok < L.z ? p2 : 0.f; p3 = tok < L.w ? p3 : 0.f;
+                            const int4 F = *reinterpret_cast<const int4 *>(lo_s + row_base + c + k);
+                            p0 = tok >= F.x && tok < L.x ? p0 : 0.f; p1 = tok >= F.y && tok < L.y ? p1 : 0.f;
+                            p2 = tok >= F.z && tok < L.z ? p2 : 0.f; p3 = tok >= F.w && tok < L.w ? p3 : 0.f;
                         } else {
                             p0 = vis ? p0 : 0.f; p1 = vis ? p1 : 0.f; p2 = vis ? p2 : 0.f; p3 = vis ? p3 : 0.f;
                         }

@@ -136,12 +136,6 @@ def test_invalid_window_arguments_launch_nothing(fw):
         fw.paged_decode_window(*args, -2)
     with pytest.raises(fw.FwError):                       # scales apply to FP8 caches only
         fw.paged_decode_window(*args, 10, k_scale=2.0)
-    lat = DecodeWorkload("lat", batch=1, q_len=1, num_q_heads=64, num_kv_heads=1, head_dim_qk=576,
-                         head_dim_v=512, page_size=64, scale=0.07, seq_lens=(200,), latent=True, value_seed=3)
-    dl = to_device(make_decode_inputs(lat, "cpu"))
-    with pytest.raises(fw.FwError):                       # latent layout: no window
-        fw.paged_decode_window(dl["q"], dl["k_cache"], dl["k_cache"][..., :512], dl["block_table"],
-                               dl["seq_lens"], 0.07, 10)
     assert fw.launch_count() == before
 
 

@@ -6,7 +6,8 @@ are the keys and whose first 512 columns are the values, 128 query heads, up
 to four query tokens with bottom-right causal rows.  Covers ragged lengths
 around tile and page boundaries (NaN-poisoned slots past each row's end),
 rows that see no key, q_len 1-4, 64-head groups and two KV heads, packed
-(token, head) rows for head counts that are not a multiple of 64, page sizes
+(token, head) rows for head counts that are not a multiple of 64, sliding
+windows with evicted pages, page sizes
 16-256, forced split-KV chunking, score scales large enough to move the
 static anchors, a separate (non-aliased) value cache, and the full-size
 workload on sampled rows.
@@ -20,6 +21,7 @@ import torch
 import oracle
 from ragged_softmax_attention_gb300.workloads import WORKLOADS, DecodeWorkload, make_decode_inputs
 from tests.gpu_common import built_library, compare, to_device
+from tests.test_decode_window_gpu import evict_before_window
 
 pytestmark = pytest.mark.gpu
 
@@ -113,6 +115,46 @@ def test_packed_query_rows_with_splits(fw, chunk):
     """Packed rows (H96, q_len 4: three 128-row groups) with many split-KV
     pieces merged by the combine kernel."""
     run_case(fw, wl_latent([3000, 257, 1800], q_len=4, hq=96, seed=29), chunk=chunk)
+
+
+def run_window_case(fw, wl, window, chunk=0):
+    """Sliding window ("TokenSpeed-MLA 2.0.1", window_left, defined there for
+    this layout); pages wholly before a row's window are evicted (NaN, table
+    entry -1), so touching one shows up as NaN or a bad-page status."""
+    inp = evict_before_window(make_decode_inputs(wl, "cpu"), wl, window)
+    ref_o, ref_l = oracle.paged_decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"],
+                                       inp["seq_lens"], inp["scale"], window_left=window)
+    d = to_device(inp)
+    if wl.latent:
+        d["v_cache"] = d["k_cache"][..., :512]
+    fw.set_option(fw.FW_OPT_DECODE_CHUNK_TOKENS, chunk)
+    try:
+        out, lse = fw.paged_decode_window(d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["seq_lens"],
+                                          d["scale"], window)
+        torch.cuda.synchronize()
+    finally:
+        fw.set_option(fw.FW_OPT_DECODE_CHUNK_TOKENS, 0)
+    assert fw.device_status() == 0
+    return compare(out, lse, ref_o, ref_l, what=f"latent window {window} {wl.seq_lens} q_len={wl.q_len} H={wl.num_q_heads}")
+
+
+@pytest.mark.parametrize("window", [0, 1, 100, 127, 128, 129, 300, 5000])
+def test_window_sizes(fw, window):
+    """CTA pairs, 128 heads, q_len 4: each token's window starts one key later."""
+    run_window_case(fw, wl_latent([1, 5, 130, 700, 2000], q_len=4), window)
+
+
+@pytest.mark.parametrize("hq,hkv,q_len,ps,window", [(96, 1, 4, 16, 100), (16, 1, 4, 32, 50), (128, 2, 2, 32, 129),
+                                                    (48, 1, 3, 64, 200)])
+def test_window_packed_rows_and_one_cta(fw, hq, hkv, q_len, ps, window):
+    """Packed rows (a group's rows have different windows), the one-CTA kernel,
+    and pages smaller than a tile (leading pages of the first tile skipped)."""
+    run_window_case(fw, wl_latent([3, 129, 777, 1500], q_len=q_len, hq=hq, hkv=hkv, ps=ps, seed=31), window)
+
+
+def test_window_with_splits(fw):
+    """A 1000-key window over long rows, cut into many split-KV pieces."""
+    run_window_case(fw, wl_latent([4000, 2600, 1100], q_len=2, seed=33), 1000, chunk=512)
 
 
 def test_separate_value_cache(fw):
