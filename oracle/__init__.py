@@ -53,6 +53,9 @@ def _load():
         lib.oracle_paged_decode_window.restype = I
         lib.oracle_paged_decode_window.argtypes = [P, P, P, P, P, P, I, D, D, I, P, L, P, I, I, I, I, I, I, I, I, I,
                                                    D, P, L, P, P, I]
+        lib.oracle_paged_decode_masked.restype = I
+        lib.oracle_paged_decode_masked.argtypes = [P, P, P, P, P, P, I, D, D, I, I, P, L, P, I, I, I, I, I, I, I,
+                                                   I, I, D, P, L, P, P, I]
         lib.oracle_e4m3_from_float.restype = ctypes.c_uint8
         lib.oracle_e4m3_from_float.argtypes = [ctypes.c_float]
         lib.oracle_kv_append.restype = I
@@ -96,7 +99,7 @@ def e4m3_to_double(byte: int) -> float:
 
 
 def paged_decode(q, k_cache, v_cache, block_table, seq_lens, scale, rows=None, threads=None,
-                 k_scale=1.0, v_scale=1.0, window_left=-1):
+                 k_scale=1.0, v_scale=1.0, window_left=-1, causal=True):
     """Softmax attention of every (b, t, h) query row over its paged keys.
 
     q [B, q_len, Hq, Dk], k_cache [P, ps, Hkv, Dk], v_cache [P, ps, Hkv, Dv]
@@ -106,6 +109,8 @@ def paged_decode(q, k_cache, v_cache, block_table, seq_lens, scale, rows=None, t
     compute; default all.  window_left >= 0: sliding window, token t sees keys
     max(0, n - q_len + t - window_left) .. n - q_len + t ("TokenSpeed-MLA
     2.0.1", window_left); block-table entries of keys before it are not read.
+    causal=False: every token sees all n keys (TokenSpeed's non-causal
+    decode), a window still starting at max(0, n - q_len + t - window_left).
     Returns (out [n_rows, Dv] float64, lse [n_rows] float64, natural log).
     """
     lib = _load()
@@ -133,7 +138,16 @@ def paged_decode(q, k_cache, v_cache, block_table, seq_lens, scale, rows=None, t
     out = np.zeros((n, Dv), dtype=np.float64)
     lse = np.zeros((n,), dtype=np.float64)
     qs, ks, vs = _strides(q), _strides(k_cache), _strides(v_cache)
-    if window_left is not None and int(window_left) >= 0:
+    if not causal:
+        rc = lib.oracle_paged_decode_masked(
+            q.data_ptr(), qs.ctypes.data, k_cache.data_ptr(), ks.ctypes.data,
+            v_cache.data_ptr(), vs.ctypes.data, int(kv8), float(k_scale), float(v_scale), 0,
+            int(window_left if window_left is not None else -1),
+            bt.ctypes.data, bt.shape[1], sl.ctypes.data,
+            B, q_len, Hq, Hkv, Dk, Dv, ps, P, bt.shape[1], float(scale),
+            rows_arr.ctypes.data, n, out.ctypes.data, lse.ctypes.data,
+            int(threads or default_threads()))
+    elif window_left is not None and int(window_left) >= 0:
         rc = lib.oracle_paged_decode_window(
             q.data_ptr(), qs.ctypes.data, k_cache.data_ptr(), ks.ctypes.data,
             v_cache.data_ptr(), vs.ctypes.data, int(kv8), float(k_scale), float(v_scale), int(window_left),

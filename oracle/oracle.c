@@ -32,6 +32,13 @@
  *   W positions before it.  Keys before the window are not gathered at all, so
  *   their block-table entries are never read.  W < 0: no window.
  *
+ * Causal or not (oracle_paged_decode_masked; "TokenSpeed-MLA 2.0.1":
+ *   causal_mask supports causal and non-causal decode, and window_left bounds
+ *   row i's history to keys from max(0, K - q_len - window_left + i) up to
+ *   its bound): token t's own position is pos = n - q_len + t; causal, it sees
+ *   keys up to pos, otherwise all n; a window of W starts at max(0, pos - W)
+ *   either way.
+ *
  * Varlen prefill ("TokenSpeed-MLA 2.0.1", capability summary: ragged varlen
  * prefill without padding, Q and KV packs described by separate cumulative
  * sequence lengths, causal or not):
@@ -144,6 +151,7 @@ typedef struct {
     const void *v; const int64_t *vs;            /* [P, ps, Hkv, Dv]   */
     int kv8; double k_scale, v_scale;
     int window_left;                             /* < 0: none */
+    int causal;                                  /* 0: every token sees all n keys */
     const int32_t *bt; int64_t bt_stride;        /* [B, max_pages]     */
     const int32_t *seq_lens;                     /* [B]                */
     int B, q_len, Hq, Hkv, Dk, Dv, ps, num_pages, max_pages;
@@ -171,14 +179,16 @@ static void *decode_worker(void *arg) {
         int b = (int)(row / ((int64_t)J->Hq * J->q_len));
         int g = h / G;                                   /* consecutive heads share a KV head */
         int64_t n = J->seq_lens[b];
-        int64_t visible = n - J->q_len + t + 1;          /* bottom-right causal for q_len > 1 */
+        int64_t pos = n - J->q_len + t;                  /* the token's own key position */
+        int64_t visible = J->causal ? pos + 1 : n;       /* bottom-right causal for q_len > 1 */
         if (visible > n) visible = n;
         if (visible < 0) visible = 0;
         if (n > cap) { J->status = -1; break; }
         int64_t first = 0;                               /* sliding window: keys first .. visible - 1 */
-        if (J->window_left >= 0 && visible > 0) {
-            first = visible - 1 - J->window_left;
+        if (J->window_left >= 0) {
+            first = pos - J->window_left;
             if (first < 0) first = 0;
+            if (first > visible) first = visible;
         }
         for (int64_t j = first; j < visible; ++j) {
             int32_t page = J->bt[(int64_t)b * J->bt_stride + j / J->ps];
@@ -205,7 +215,7 @@ done:
 static int paged_decode_any(const uint16_t *q, const int64_t *q_stride,
                             const void *k_cache, const int64_t *k_stride,
                             const void *v_cache, const int64_t *v_stride,
-                            int kv8, double k_scale, double v_scale, int window_left,
+                            int kv8, double k_scale, double v_scale, int causal, int window_left,
                             const int32_t *block_table, int64_t bt_stride,
                             const int32_t *seq_lens,
                             int B, int q_len, int Hq, int Hkv, int Dk, int Dv,
@@ -221,7 +231,7 @@ static int paged_decode_any(const uint16_t *q, const int64_t *q_stride,
     for (int w = 0; w < n_threads; ++w) {
         decode_job *J = &jobs[w];
         J->q = q; J->qs = q_stride; J->k = k_cache; J->ks = k_stride; J->v = v_cache; J->vs = v_stride;
-        J->kv8 = kv8; J->k_scale = k_scale; J->v_scale = v_scale; J->window_left = window_left;
+        J->kv8 = kv8; J->k_scale = k_scale; J->v_scale = v_scale; J->window_left = window_left; J->causal = causal;
         J->bt = block_table; J->bt_stride = bt_stride; J->seq_lens = seq_lens;
         J->B = B; J->q_len = q_len; J->Hq = Hq; J->Hkv = Hkv; J->Dk = Dk; J->Dv = Dv;
         J->ps = page_size; J->num_pages = num_pages; J->max_pages = max_pages; J->scale = scale;
@@ -247,7 +257,7 @@ int oracle_paged_decode(const uint16_t *q, const int64_t *q_stride,
                         int page_size, int num_pages, int max_pages, double scale,
                         const int64_t *rows, int64_t n_rows,
                         double *out, double *lse, int n_threads) {
-    return paged_decode_any(q, q_stride, k_cache, k_stride, v_cache, v_stride, 0, 1.0, 1.0, -1, block_table,
+    return paged_decode_any(q, q_stride, k_cache, k_stride, v_cache, v_stride, 0, 1.0, 1.0, 1, -1, block_table,
                             bt_stride, seq_lens, B, q_len, Hq, Hkv, Dk, Dv, page_size, num_pages, max_pages,
                             scale, rows, n_rows, out, lse, n_threads);
 }
@@ -262,7 +272,7 @@ int oracle_paged_decode_kv8(const uint16_t *q, const int64_t *q_stride,
                             int page_size, int num_pages, int max_pages, double scale,
                             const int64_t *rows, int64_t n_rows,
                             double *out, double *lse, int n_threads) {
-    return paged_decode_any(q, q_stride, k_cache, k_stride, v_cache, v_stride, 1, k_scale, v_scale, -1, block_table,
+    return paged_decode_any(q, q_stride, k_cache, k_stride, v_cache, v_stride, 1, k_scale, v_scale, 1, -1, block_table,
                             bt_stride, seq_lens, B, q_len, Hq, Hkv, Dk, Dv, page_size, num_pages, max_pages,
                             scale, rows, n_rows, out, lse, n_threads);
 }
@@ -278,9 +288,25 @@ int oracle_paged_decode_window(const uint16_t *q, const int64_t *q_stride,
                                int page_size, int num_pages, int max_pages, double scale,
                                const int64_t *rows, int64_t n_rows,
                                double *out, double *lse, int n_threads) {
-    return paged_decode_any(q, q_stride, k_cache, k_stride, v_cache, v_stride, kv8, k_scale, v_scale, window_left,
+    return paged_decode_any(q, q_stride, k_cache, k_stride, v_cache, v_stride, kv8, k_scale, v_scale, 1, window_left,
                             block_table, bt_stride, seq_lens, B, q_len, Hq, Hkv, Dk, Dv, page_size, num_pages,
                             max_pages, scale, rows, n_rows, out, lse, n_threads);
+}
+
+/* Either cache type, causal or not, and a sliding window (W < 0: none). */
+int oracle_paged_decode_masked(const uint16_t *q, const int64_t *q_stride,
+                               const void *k_cache, const int64_t *k_stride,
+                               const void *v_cache, const int64_t *v_stride,
+                               int kv8, double k_scale, double v_scale, int causal, int window_left,
+                               const int32_t *block_table, int64_t bt_stride,
+                               const int32_t *seq_lens,
+                               int B, int q_len, int Hq, int Hkv, int Dk, int Dv,
+                               int page_size, int num_pages, int max_pages, double scale,
+                               const int64_t *rows, int64_t n_rows,
+                               double *out, double *lse, int n_threads) {
+    return paged_decode_any(q, q_stride, k_cache, k_stride, v_cache, v_stride, kv8, k_scale, v_scale, causal,
+                            window_left, block_table, bt_stride, seq_lens, B, q_len, Hq, Hkv, Dk, Dv, page_size,
+                            num_pages, max_pages, scale, rows, n_rows, out, lse, n_threads);
 }
 
 /* ----------------------------------------------------------------- prefill */

@@ -19,7 +19,8 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 MUTATIONS = {
     "interleaved_gqa": ("int g = h / G;", "int g = h % J->Hkv;"),
     "scale_dropped": ("s[j] = scale * acc;", "s[j] = acc;"),
-    "causal_off_by_one": ("int64_t visible = n - J->q_len + t + 1;", "int64_t visible = n - J->q_len + t;"),
+    "causal_off_by_one": ("int64_t visible = J->causal ? pos + 1 : n;", "int64_t visible = J->causal ? pos : n;"),
+    "noncausal_flag_ignored": ("int64_t visible = J->causal ? pos + 1 : n;", "int64_t visible = pos + 1;"),
     "page_slot_shift": ("int64_t slot = j % J->ps;", "int64_t slot = (j + 1) % J->ps;"),
     "lse_without_max": ("*lse = m + log(l);", "*lse = log(l);"),
     "prefill_top_left_causal": ("visible = r + Lk - Lq + 1;", "visible = r + 1;"),
@@ -28,7 +29,7 @@ MUTATIONS = {
     "missing_normalisation": ("for (int d = 0; d < dv; ++d) out[d] /= l;", ""),
     "fp8_value_scale_dropped": ("out[d] += p * (v_scale * oracle_e4m3_to_double", "out[d] += p * (oracle_e4m3_to_double"),
     "fp8_exponent_bias_off": ("else v = ldexp(1.0 + m / 8.0, e - 7);", "else v = ldexp(1.0 + m / 8.0, e - 8);"),
-    "window_off_by_one": ("first = visible - 1 - J->window_left;", "first = visible - J->window_left;"),
+    "window_off_by_one": ("first = pos - J->window_left;", "first = pos + 1 - J->window_left;"),
     "append_clamp_after_base": ("if (slot < 0) slot = 0;                      /* clamp first ... */\n            int64_t row = layer_base + slot;",
                                 "int64_t row = layer_base + slot;\n            if (row < 0) row = 0;"),
     "append_fp8_scale_multiplied": ("oracle_e4m3_from_float(x / sc)", "oracle_e4m3_from_float(x * sc)"),
@@ -46,6 +47,7 @@ PIN_CHECKS = [
     lambda: pins.test_fp8_kv_decode_matches_sdpa_on_dequantized_copy(1, (5, 1, 13)),
     lambda: pins.test_window_matches_sdpa_on_dense_copy(2, (9, 30, 2), 4, 7),
     pins.test_window_zero_sees_own_position_only,
+    lambda: pins.test_noncausal_decode_matches_masked_sdpa(-1),
     pins.test_warmup_slot_is_clamped_before_the_layer_base,
     lambda: pins.test_append_changes_only_the_addressed_rows(True),
 ]
@@ -68,8 +70,9 @@ def test_pins_catch_mutant(tmp_path, monkeypatch, name):
     oracle._load()                                   # fetch argtypes from the real library
     real = oracle._lib
     mutant = ctypes.CDLL(lib_path)
-    for fn in ("oracle_paged_decode", "oracle_paged_decode_kv8", "oracle_paged_decode_window", "oracle_e4m3_to_double",
-               "oracle_varlen_prefill", "oracle_e4m3_from_float", "oracle_kv_append"):
+    for fn in ("oracle_paged_decode", "oracle_paged_decode_kv8", "oracle_paged_decode_window",
+               "oracle_paged_decode_masked", "oracle_e4m3_to_double", "oracle_varlen_prefill",
+               "oracle_e4m3_from_float", "oracle_kv_append"):
         getattr(mutant, fn).restype = getattr(real, fn).restype
         getattr(mutant, fn).argtypes = getattr(real, fn).argtypes
     monkeypatch.setattr(oracle, "_lib", mutant)

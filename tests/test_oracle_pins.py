@@ -310,6 +310,73 @@ def test_decode_equals_prefill_over_identity_pages():
         np.testing.assert_array_equal(dec_l[b * 12:(b + 1) * 12], l)
 
 
+def sdpa_masked_reference(inp, b, causal, window):
+    """float64 SDPA over a dense gathered copy with an explicit boolean mask:
+    token t's own position is pos = n - q_len + t; causal, it sees keys up to
+    pos, otherwise all n; a window W starts the range at max(0, pos - W)."""
+    q = inp["q"][b].double()
+    k, v = dense_kv(inp, b)
+    q_len, hq, _ = q.shape
+    n, hkv = k.shape[0], k.shape[1]
+    k = k.double().repeat_interleave(hq // hkv, dim=1)
+    v = v.double().repeat_interleave(hq // hkv, dim=1)
+    mask = torch.zeros(q_len, n, dtype=torch.bool)
+    for t in range(q_len):
+        pos = n - q_len + t
+        hi = min(n, pos + 1) if causal else n
+        lo = max(0, pos - window) if window >= 0 else 0
+        mask[t, lo:max(lo, hi)] = True
+    scores = torch.einsum("thd,nhd->htn", q, k) * inp["scale"]
+    scores = scores.masked_fill(~mask, float("-inf"))
+    lse = torch.logsumexp(scores, dim=-1)
+    p = torch.softmax(scores, dim=-1).nan_to_num(0.0)
+    out = torch.einsum("htn,nhd->thd", p, v)
+    return out.reshape(q_len * hq, -1).numpy(), lse.transpose(0, 1).reshape(-1).numpy()
+
+
+@pytest.mark.parametrize("window", [-1, 0, 3, 7])
+def test_noncausal_decode_matches_masked_sdpa(window):
+    """TokenSpeed's non-causal decode: every token sees all n keys (a window
+    still starts at its own position minus W); float64 reference built from
+    the mask definition, GQA by repeat_interleave."""
+    wl, inp = tiny_decode(q_len=3, lens=(9, 2, 14), hq=4, hkv=2, ps=4)
+    out, lse = oracle.paged_decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"],
+                                   inp["seq_lens"], inp["scale"], window_left=window, causal=False)
+    for b in range(3):
+        ref_o, ref_l = sdpa_masked_reference(inp, b, causal=False, window=window)
+        np.testing.assert_allclose(out[b * 12:(b + 1) * 12], ref_o, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse[b * 12:(b + 1) * 12], ref_l, rtol=0, atol=1e-12)
+    # the same mask builder reproduces the causal oracle (guards the builder itself)
+    out_c, _ = oracle.paged_decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"],
+                                   inp["seq_lens"], inp["scale"], window_left=window)
+    ref_c, _ = sdpa_masked_reference(inp, 0, causal=True, window=window)
+    np.testing.assert_allclose(out_c[:12], ref_c, rtol=0, atol=1e-12)
+
+
+def test_noncausal_decode_equals_noncausal_prefill_over_identity_pages():
+    """Non-causal prefill with Lq = q_len over n keys equals non-causal paged decode."""
+    wl, inp = tiny_decode(q_len=3, lens=(9, 5, 12), ps=4, mapping="identity", hq=4, hkv=2)
+    dec_o, dec_l = oracle.paged_decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"],
+                                       inp["seq_lens"], inp["scale"], causal=False)
+    for b in range(3):
+        k, v = dense_kv(inp, b)
+        cq = torch.tensor([0, 3], dtype=torch.int32)
+        ck = torch.tensor([0, k.shape[0]], dtype=torch.int32)
+        o, l = oracle.varlen_prefill(inp["q"][b], k, v, cq, ck, False, inp["scale"])
+        np.testing.assert_array_equal(dec_o[b * 12:(b + 1) * 12], o)
+        np.testing.assert_array_equal(dec_l[b * 12:(b + 1) * 12], l)
+
+
+def test_noncausal_equals_causal_at_one_token():
+    wl, inp = tiny_decode(q_len=1, lens=(9, 1, 6))
+    a = oracle.paged_decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"], inp["seq_lens"],
+                            inp["scale"], causal=False)
+    c = oracle.paged_decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"], inp["seq_lens"],
+                            inp["scale"])
+    np.testing.assert_array_equal(a[0], c[0])
+    np.testing.assert_array_equal(a[1], c[1])
+
+
 def test_latent_value_prefix_view():
     """V as the first Dv columns of the K rows (TokenSpeed decode, one KV cache)."""
     wl, inp = tiny_decode(hq=4, hkv=1, d=24, dv=16, lens=(7, 3, 9), latent=True)
