@@ -193,6 +193,29 @@ fw_status_t fw_paged_decode_window(const fw_tensor_t *q, const fw_tensor_t *k_ca
                                    fw_stream_t stream);
 
 /*
+ * fw_paged_decode_masked -- decode, causal or not ("TokenSpeed-MLA 2.0.1", MLA
+ * decode: causal_mask supports causal and non-causal execution; window_left
+ * bounds row i's history to start at max(0, K - q_len - window_left + i)).
+ *
+ *   causal       1: query token t of a row with n keys sees keys up to its own
+ *                position n - q_len + t (as fw_paged_decode); 0: every token
+ *                sees all n keys.  With q_len = 1 both are the same.
+ *   window_left  -1: none; W >= 0: the keys a token sees start at
+ *                max(0, n - q_len + t - W), causal or not.
+ *   other arguments   as fw_paged_decode_window (BF16 or FP8_E4M3 caches,
+ *                the scales applying to FP8 ones).
+ *
+ * Errors as fw_paged_decode_window; FW_ERR_UNSUPPORTED for a non-causal
+ * sliding window on the grouped-query layouts with q_len > 1 (served for the
+ * latent layout).  Same workspace as fw_paged_decode.
+ */
+fw_status_t fw_paged_decode_masked(const fw_tensor_t *q, const fw_tensor_t *k_cache,
+                                   const fw_tensor_t *v_cache, const fw_tensor_t *block_table,
+                                   const fw_tensor_t *seq_lens, float scale, int32_t causal,
+                                   int32_t window_left, float k_scale, float v_scale,
+                                   fw_tensor_t *out, fw_tensor_t *lse, fw_stream_t stream);
+
+/*
  * KV-cache append ("Writing Page Attention with PyPTO", sections 4.2-4.3).
  *
  *   k_new, v_new  [B, q_len, Hkv, D]   BF16, last dim contiguous, strides

@@ -7,7 +7,7 @@ it has not been built (``ragged_softmax_attention_gb300.build.build()``).
 """
 from ._binding import (FwError, device_status, kernel_timing_read, launch_count, load_library,  # noqa: F401
                        kv_append, paged_decode, paged_decode_append, paged_decode_fp8, paged_decode_noalloc,
-                       paged_decode_window, paged_decode_workspace_size, plan_decode,
+                       paged_decode_masked, paged_decode_window, paged_decode_workspace_size, plan_decode,
                        set_option,
                        set_workspace, varlen_prefill)
 from ._binding import (FW_OPT_DECODE_CHUNK_TOKENS, FW_OPT_KERNEL_TIMING, FW_OPT_MAX_CTAS,  # noqa: F401

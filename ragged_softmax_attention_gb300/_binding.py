@@ -68,6 +68,9 @@ def load_library(path: Optional[str] = None):
     lib.fw_paged_decode_window.restype = ctypes.c_int
     lib.fw_paged_decode_window.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                            ctypes.c_int32, P, P, ctypes.c_void_p]
+    lib.fw_paged_decode_masked.restype = ctypes.c_int
+    lib.fw_paged_decode_masked.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_int32, ctypes.c_int32,
+                                           ctypes.c_float, ctypes.c_float, P, P, ctypes.c_void_p]
     lib.fw_kv_append.restype = ctypes.c_int
     lib.fw_kv_append.argtypes = [P, P, P, ctypes.c_int64, P, P, ctypes.c_float, ctypes.c_float, ctypes.c_void_p]
     lib.fw_paged_decode_append.restype = ctypes.c_int
@@ -185,6 +188,27 @@ def paged_decode_window(q, k_cache, v_cache, block_table, seq_lens, scale, windo
     _check(lib.fw_paged_decode_window(*[_ref(a) for a in args], ctypes.c_float(scale), ctypes.c_float(k_scale),
                                       ctypes.c_float(v_scale), ctypes.c_int32(window_left), _ref(fo), _ref(fl),
                                       _stream_handle(stream)))
+    return out, lse
+
+
+def paged_decode_masked(q, k_cache, v_cache, block_table, seq_lens, scale, causal=True, window_left=-1, k_scale=1.0,
+                        v_scale=1.0, out=None, lse=None, return_lse=True, stream=None):
+    """fw_paged_decode_masked: causal=True, token t of row b sees keys up to
+    n - q_len + t; causal=False, all n keys; a window_left >= 0 starts either
+    range at max(0, n - q_len + t - window_left).  BF16 or FP8 E4M3 caches.
+    Returns (out [B, q_len, Hq, Dv] bf16, lse [B, q_len, Hq] f32 or None)."""
+    lib = load_library()
+    B, q_len, Hq, _ = q.shape
+    Dv = v_cache.shape[3]
+    if out is None:
+        out = torch.empty((B, q_len, Hq, Dv), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, q_len, Hq), dtype=torch.float32, device=q.device)
+    args = [as_fw_tensor(x) for x in (q, k_cache, v_cache, block_table, seq_lens)]
+    fo, fl = as_fw_tensor(out), as_fw_tensor(lse)
+    _check(lib.fw_paged_decode_masked(*[_ref(a) for a in args], ctypes.c_float(scale), ctypes.c_int32(1 if causal else 0),
+                                      ctypes.c_int32(window_left), ctypes.c_float(k_scale), ctypes.c_float(v_scale),
+                                      _ref(fo), _ref(fl), _stream_handle(stream)))
     return out, lse
 
 

@@ -509,7 +509,7 @@ static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_
                                      void *(*fixed_ws)(DeviceState *, fw_status_t *), size_t fixed_bytes,
                                      bool kv8 = false, float k_scale = 1.f, float v_scale = 1.f,
                                      int32_t window_left = -1, bool any_cache = false,
-                                     const AppendArgs *append = nullptr) {
+                                     const AppendArgs *append = nullptr, bool causal = true) {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     // A fused append writes the packed cache at layer_base + max(slot, 0); the
     // attention then reads the layer's pages, a view from layer_base on.
@@ -555,6 +555,11 @@ static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_
         return fail(FW_ERR_INVALID_ARG, "lse must be [B, q_len, Hq]");
     if (!std::isfinite(scale)) return fail(FW_ERR_INVALID_ARG, "scale must be finite");
     const bool latent = !kv8 && (Dk == 576 && Dv == 512);
+    // The grouped-query kernels anchor a row's window at its causal bound;
+    // the latent ones keep both bounds per row.
+    if (!causal && window_left >= 0 && !latent && q_len > 1)
+        return fail(FW_ERR_UNSUPPORTED, "non-causal decode with a sliding window is served for the latent layout "
+                    "(or q_len = 1)");
     if (latent && append)
         return fail(FW_ERR_UNSUPPORTED, "the fused append serves the grouped-query layouts (append latent rows "
                     "with fw_kv_append)");
@@ -622,6 +627,7 @@ static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_
         return fail(FW_ERR_UNSUPPORTED, "packed latent query rows need q contiguous over (token, head): "
                     "stride[1] = %lld, expected %lld", (long long)q->stride[1], (long long)(Hq * q->stride[2]));
     p.window_left = window_left;
+    p.causal = causal ? 1 : 0;
     p.app = app;
     p.block_table = static_cast<const int32_t *>(block_table->data);
     p.bt_stride = block_table->stride[0];
@@ -749,6 +755,14 @@ fw_status_t fw_paged_decode_window(const fw_tensor_t *q, const fw_tensor_t *k_ca
                                    fw_tensor_t *lse, fw_stream_t stream) {
     return paged_decode_impl(q, k_cache, v_cache, block_table, seq_lens, scale, out, lse, stream, nullptr, 0,
                              false, k_scale, v_scale, window_left, true);
+}
+
+fw_status_t fw_paged_decode_masked(const fw_tensor_t *q, const fw_tensor_t *k_cache, const fw_tensor_t *v_cache,
+                                   const fw_tensor_t *block_table, const fw_tensor_t *seq_lens, float scale,
+                                   int32_t causal, int32_t window_left, float k_scale, float v_scale,
+                                   fw_tensor_t *out, fw_tensor_t *lse, fw_stream_t stream) {
+    return paged_decode_impl(q, k_cache, v_cache, block_table, seq_lens, scale, out, lse, stream, nullptr, 0,
+                             false, k_scale, v_scale, window_left, true, nullptr, causal != 0);
 }
 
 // ----------------------------------------------------- decode without allocation

@@ -382,7 +382,7 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
             for (int r = 0; r < RH; ++r) {
                 int t, h;
                 const bool ok = unit_row(p, x, r0 + r, t, h);
-                lim[r] = ok ? min(x.n, x.n - p.q_len + t + 1) : 0;
+                lim[r] = ok ? (p.causal ? min(x.n, x.n - p.q_len + t + 1) : x.n) : 0;
                 if (ok) nrows = r + 1;
                 rs[r] = p.scale_log2 * __int_as_float((127 - q_exp[qs * NQ + r0 + r]) << 23);
             }

@@ -312,7 +312,7 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
             for (int r = 0; r < NQ; ++r) {
                 int t, h;
                 const bool ok = unit_row(p, x, r, t, h);
-                lim[r] = ok ? min(x.n, x.n - p.q_len + t + 1) : 0;
+                lim[r] = ok ? (p.causal ? min(x.n, x.n - p.q_len + t + 1) : x.n) : 0;
                 if (ok) nrows = r + 1;
             }
             // Sliding window: a row with visible-key bound lim sees keys

@@ -59,6 +59,7 @@ struct DecodeParams {
                           // packed rows t * Hq + h and may straddle tokens ("TokenSpeed-MLA 2.0.1",
                           // packed-query paragraph); 0: one token's heads per row group
     int window_left;      // < 0: none; else token t sees keys max(0, n - q_len + t - W) .. n - q_len + t
+    int causal;           // 1: token t sees keys up to its own position n - q_len + t; 0: all n keys
     AppendParams app;     // appended by the plan launch's extra blocks before the attention reads
     int32_t *plan;        // [0] = T, [1] = span, [2 .. 2 + B] = PB
     const int32_t *block_table; int64_t bt_stride;

@@ -487,7 +487,7 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
                 const int gr = x.row0 + tsw;
                 const int pos = x.n - p.q_len + gr / p.G;             // the row's own key position
                 const bool real = gr < p.q_len * p.G;
-                lim_s[tsw] = real ? min(x.k_end, pos + 1) : 0;
+                lim_s[tsw] = real ? min(x.k_end, p.causal ? pos + 1 : x.n) : 0;
                 lo_s[tsw] = real && p.window_left >= 0 ? max(0, pos - p.window_left) : 0;
             }
             named_bar_sync(1, 256);
