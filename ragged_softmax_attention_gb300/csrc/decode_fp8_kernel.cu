@@ -165,6 +165,7 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();                                    // the plan (and appended rows) of this call are written
     const WaitCtx wc{p.status, p.timeout_ns, abort_flag};
 
     if (warp == 0) {
@@ -564,6 +565,7 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
+    pdl_launch_dependents();                       // the combine kernel may launch
 }
 
 template <int NQ, int R>
@@ -577,7 +579,9 @@ cudaError_t launch_fp8_t(const DecodeParams &p, const CUtensorMap &tq, const CUt
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    paged_decode_fp8_kernel<NQ, R><<<p.grid, 320, C::kSmemBytes, stream>>>(p, tq, tk, tv);
+    cudaError_t le = launch_after_previous(paged_decode_fp8_kernel<NQ, R>, dim3(p.grid), dim3(320), C::kSmemBytes,
+                                           stream, p, tq, tk, tv);
+    if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
 

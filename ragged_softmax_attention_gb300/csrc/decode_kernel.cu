@@ -131,6 +131,7 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();                                    // the plan (and appended rows) of this call are written
     const WaitCtx wc{p.status, p.timeout_ns, abort_flag};
 
     if (warp == 0) {
@@ -479,6 +480,7 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
+    pdl_launch_dependents();                       // the combine kernel may launch
 }
 
 template <int D, int NQ>
@@ -492,7 +494,9 @@ cudaError_t launch_t(const DecodeParams &p, const CUtensorMap &tq, const CUtenso
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    paged_decode_kernel<D, NQ><<<p.grid, 192, C::kSmemBytes, stream>>>(p, tq, tk, tv);
+    cudaError_t le = launch_after_previous(paged_decode_kernel<D, NQ>, dim3(p.grid), dim3(192), C::kSmemBytes,
+                                           stream, p, tq, tk, tv);
+    if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
 
@@ -568,6 +572,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const __grid_constant__ 
 // T and the range span; rows with no keys get their zero output and -inf LSE
 // here, since no range ever covers them.
 __global__ void __launch_bounds__(1024) decode_plan_kernel(const __grid_constant__ DecodeParams p) {
+    pdl_launch_dependents();                         // the attention kernel waits for this grid to finish
     if (blockIdx.x > 0) {                            // the launch's extra blocks append the new tokens
         append_rows(p.app, blockIdx.x - 1, gridDim.x - 1, p.status);
         return;
@@ -639,6 +644,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const __grid_constant
 
 template <int D>
 __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ DecodeParams p) {
+    pdl_wait();                                      // the attention kernel's partials are written
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int64_t rows = (int64_t)p.B * p.q_len * p.Hq;
@@ -723,11 +729,10 @@ cudaError_t launch_kv_append(const AppendParams &a, int *status, cudaStream_t st
 cudaError_t launch_decode_combine(const DecodeParams &p, int head_dim_v, cudaStream_t stream) {
     const int64_t rows = (int64_t)p.B * p.q_len * p.Hq;
     const unsigned grid = (unsigned)((rows + 3) / 4);
-    if (head_dim_v == 128) combine_kernel<128><<<grid, 128, 0, stream>>>(p);
-    else if (head_dim_v == 256) combine_kernel<256><<<grid, 128, 0, stream>>>(p);
-    else if (head_dim_v == 512) combine_kernel<512><<<grid, 128, 0, stream>>>(p);
-    else return cudaErrorInvalidValue;
-    return cudaGetLastError();
+    if (head_dim_v == 128) return launch_after_previous(combine_kernel<128>, dim3(grid), dim3(128), 0, stream, p);
+    if (head_dim_v == 256) return launch_after_previous(combine_kernel<256>, dim3(grid), dim3(128), 0, stream, p);
+    if (head_dim_v == 512) return launch_after_previous(combine_kernel<512>, dim3(grid), dim3(128), 0, stream, p);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &tq, const CUtensorMap &tk,

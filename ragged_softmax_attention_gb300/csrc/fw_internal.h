@@ -7,6 +7,25 @@
 
 namespace fw {
 
+// Launches `kernel` so that it may start while the previous kernel in the
+// stream still runs (programmatic stream serialization); the kernel calls
+// pdl_wait() before it reads anything that kernel wrote.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_after_previous(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                         cudaStream_t stream, const Args &...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 constexpr int kKvTile = 128;          // keys per KV tile (MMA M extent in decode, N in prefill)
 constexpr int kSoftmaxStartWarp = 2;  // decode: warps 2..5 run the softmax / epilogue
 

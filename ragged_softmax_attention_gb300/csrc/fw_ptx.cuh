@@ -131,6 +131,17 @@ __device__ __forceinline__ void fence_barrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// ------------------------------------------------ programmatic dependent launch
+//
+// A kernel launched with programmatic stream serialization may start while
+// the kernel before it in the stream still runs.  pdl_wait blocks until that
+// kernel has completed and its memory operations are visible (a no-op for a
+// kernel launched the ordinary way); pdl_launch_dependents lets the next
+// such kernel start before this one ends.
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ----------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {

@@ -170,6 +170,7 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();                                    // the plan (and appended rows) of this call are written
     const WaitCtx wc{p.status, p.timeout_ns, abort_flag};
 
     if (warp == 0) {
@@ -609,6 +610,7 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    pdl_launch_dependents();                       // the combine kernel may launch
 }
 
 }  // namespace
@@ -633,8 +635,9 @@ cudaError_t launch_latent_decode(const DecodeParams &p, const CUtensorMap &tq, c
     if (e != cudaSuccess) return e;
     ++*launches;
     if (timing_start) cudaEventRecord(timing_start, stream);
-    if (p.packed) latent_decode_kernel<true><<<p.grid, 192, kSmemBytes, stream>>>(p, tq, tk, tv);
-    else latent_decode_kernel<false><<<p.grid, 192, kSmemBytes, stream>>>(p, tq, tk, tv);
+    e = launch_after_previous(p.packed ? latent_decode_kernel<true> : latent_decode_kernel<false>, dim3(p.grid),
+                              dim3(192), kSmemBytes, stream, p, tq, tk, tv);
+    if (e != cudaSuccess) return e;
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     ++*launches;

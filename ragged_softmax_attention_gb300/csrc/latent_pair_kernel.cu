@@ -169,6 +169,7 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
     cluster_sync_all();                            // both CTAs' barriers exist before any remote use
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();                                    // the plan (and appended rows) of this call are written
     const WaitCtx wc{p.status, p.timeout_ns, abort_flag};
 
     if (warp == 0 || warp == 10) {
@@ -733,6 +734,7 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
     cluster_sync_all();                            // no MMA, copy, store or arrive of the pair is left
     tc_fence_after();
     if (warp == 1) tmem_dealloc_pair(tmem, 512);
+    pdl_launch_dependents();                       // the combine kernel may launch
 }
 
 }  // namespace
@@ -758,8 +760,9 @@ cudaError_t launch_latent_pair_decode(const DecodeParams &p, const CUtensorMap &
     if (e != cudaSuccess) return e;
     ++*launches;
     if (timing_start) cudaEventRecord(timing_start, stream);
-    if (p.packed) latent_pair_decode_kernel<true><<<p.grid, kThreads, kSmemBytes, stream>>>(p, tq, tk, tv);
-    else latent_pair_decode_kernel<false><<<p.grid, kThreads, kSmemBytes, stream>>>(p, tq, tk, tv);
+    e = launch_after_previous(p.packed ? latent_pair_decode_kernel<true> : latent_pair_decode_kernel<false>,
+                              dim3(p.grid), dim3(kThreads), kSmemBytes, stream, p, tq, tk, tv);
+    if (e != cudaSuccess) return e;
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     ++*launches;

@@ -190,7 +190,6 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int count = __ldg(p.plan + 0);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kSlots; ++i) { mbar_init(&slot_full[i], 1); mbar_init(&slot_empty[i], NQ); }
@@ -211,6 +210,8 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();                                    // the plan of this call is written
+    const int count = p.plan[0];                   // (read only after the wait)
     const WaitCtx wc{p.status, p.timeout_ns, abort_flag};
 
     if (warp < 4) {
@@ -626,7 +627,6 @@ varlen_prefill_pair_kernel(const __grid_constant__ PrefillParams p, const __grid
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank();
-    const int count = __ldg(p.plan + 0);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kPairSlots; ++i) { mbar_init(&slot_full[i], 1); mbar_init(&slot_empty[i], 1); }
@@ -646,6 +646,8 @@ varlen_prefill_pair_kernel(const __grid_constant__ PrefillParams p, const __grid
     cluster_sync_all();                                  // both CTAs' barriers exist before any remote use
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();                                    // the plan of this call is written
+    const int count = p.plan[0];                   // (read only after the wait)
     const WaitCtx wc{p.status, p.timeout_ns, abort_flag};
 
     if (warp == 0) {
@@ -951,6 +953,7 @@ varlen_prefill_pair_kernel(const __grid_constant__ PrefillParams p, const __grid
 // Sequences whose cumulative lengths reach past the packed tensors are left
 // out and reported in the status word.
 __global__ void __launch_bounds__(1024) prefill_plan_kernel(const __grid_constant__ PrefillParams p, int num_q) {
+    pdl_launch_dependents();                         // the attention kernel waits for this grid to finish
     __shared__ int warp_sums[32];
     __shared__ int carry_s;
     __shared__ int bins[kCostBins];
@@ -1072,7 +1075,9 @@ cudaError_t launch_tiles(const PrefillParams &p, const CUtensorMap &tq, const CU
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    varlen_prefill_kernel<<<p.grid, C::kThreads, C::kSmemBytes, stream>>>(p, tq, tk, tv);
+    cudaError_t le = launch_after_previous(varlen_prefill_kernel, dim3(p.grid), dim3(C::kThreads), C::kSmemBytes,
+                                           stream, p, tq, tk, tv);
+    if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
 
@@ -1085,7 +1090,9 @@ cudaError_t launch_pair(const PrefillParams &p, const CUtensorMap &tq, const CUt
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    varlen_prefill_pair_kernel<<<p.grid & ~1, 256, kPairSmemBytes, stream>>>(p, tq, tk, tv);
+    cudaError_t le = launch_after_previous(varlen_prefill_pair_kernel, dim3(p.grid & ~1), dim3(256), kPairSmemBytes,
+                                           stream, p, tq, tk, tv);
+    if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
 
