@@ -331,7 +331,7 @@ def bench_prefill(fw, torch, steps, warmup, device, peaks, name=None):
     per = kms / max(1, kn)
     ach = flops / (per * 1e-3) / 1e12
     profile = {PREFILL_WL: "varlen_prefill_gqa_ncu.json", PREFILL_HD256_WL: "varlen_prefill_hd256_ncu.json"}[name]
-    traffic = ncu_traffic(profile, ["prefill_kernel.cu", "fw_ptx.cuh", "abi.cu"], flops)
+    traffic = ncu_traffic(profile, ["prefill_kernel.cu", "fw_pair.cuh", "fw_ptx.cuh", "abi.cu"], flops)
     return {"workload": name, "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 4), "steps": n, "flops_per_step": flops,
             "gpu_launches": fw.launch_count() - l0,
