@@ -185,26 +185,29 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
         // Physical pages of the 128-key tile at key ts of row b: lane l holds
         // the tile's l-th page (l < pages in the tile).  Read one tile ahead
         // of use, so no chunk load waits on the block table.
-        // Leading pages of the tile at ts wholly before k_lo (the first key
-        // of a sliding window) are never looked up nor loaded.
-        auto skip_of = [&](int ts, int k_lo) { return p.ps >= kKvTile ? 0 : max(0, k_lo / p.ps - ts / p.ps); };
-        auto tile_pages = [&](int b, int ts, int k_end, int k_lo) {
+        // Pages below a tile are powers of two: shifts instead of divisions.
+        const int ps_shift = __ffs(p.ps) - 1;
+        // Leading pages of the tile at ts wholly before the page holding the
+        // window's first key (lo_page) are never looked up nor loaded.
+        auto skip_of = [&](int ts, int lo_page) { return p.ps >= kKvTile ? 0 : max(0, lo_page - (ts >> ps_shift)); };
+        auto tile_pages = [&](int b, int ts, int k_end, int lo_page) {
             int npages = 1;
-            if (p.ps < kKvTile) npages = min(kKvTile / p.ps, ceil_div_i(k_end - ts, p.ps));
+            if (p.ps < kKvTile) npages = min(kKvTile >> ps_shift, (k_end - ts + p.ps - 1) >> ps_shift);
             int phys = 0;
-            if (lane >= skip_of(ts, k_lo) && lane < npages)
-                phys = __ldg(p.block_table + (int64_t)b * p.bt_stride + ts / p.ps + lane);
+            if (lane >= skip_of(ts, lo_page) && lane < npages)
+                phys = __ldg(p.block_table + (int64_t)b * p.bt_stride + (p.ps < kKvTile ? ts >> ps_shift : ts / p.ps) +
+                             lane);
             return phys;
         };
-        auto load_chunk = [&](int g, int ts, int k_end, int k_lo, int phys, const CUtensorMap *tm, int c,
+        auto load_chunk = [&](int g, int ts, int k_end, int lo_page, int phys, const CUtensorMap *tm, int c,
                               bool zero_tail) -> bool {
             const uint32_t s = m % kSlots;
             if (!warp_wait(&slot_empty[s], ((m / kSlots) & 1) ^ 1, wc, lane)) return false;
             const int halves = c < 4 ? 2 : 1;
             int npages = 1, slot0 = 0;
-            if (p.ps < kKvTile) npages = min(kKvTile / p.ps, ceil_div_i(k_end - ts, p.ps));
+            if (p.ps < kKvTile) npages = min(kKvTile >> ps_shift, (k_end - ts + p.ps - 1) >> ps_shift);
             else slot0 = ts % p.ps;
-            const int skip = min(npages, skip_of(ts, k_lo));
+            const int skip = min(npages, skip_of(ts, lo_page));
             const bool load = lane >= skip && lane < npages;
             if (load && (unsigned)phys >= (unsigned)p.num_pages) { record_error(p.status, 1); phys = 0; }
             const bool zero = zero_tail && (ts + kKvTile > k_end || skip > 0);
@@ -263,17 +266,18 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
             }
             __syncwarp();
             ++nq;
-            int nphys = tile_pages(x.b, x.k_begin, x.k_end, x.lo);
+            const int lo_page = x.lo / p.ps;
+            int nphys = tile_pages(x.b, x.k_begin, x.k_end, lo_page);
             for (int i = 0; i < x.ntiles && ok; ++i) {
                 const int ts = x.k_begin + i * kKvTile;
                 const int phys = nphys;
-                if (i + 1 < x.ntiles) nphys = tile_pages(x.b, ts + kKvTile, x.k_end, x.lo);
+                if (i + 1 < x.ntiles) nphys = tile_pages(x.b, ts + kKvTile, x.k_end, lo_page);
                 for (int c = 0; c < kQkChunks && ok; ++c)
-                    ok = load_chunk(x.g, ts, x.k_end, x.lo, phys, &tm_k, c, false);
+                    ok = load_chunk(x.g, ts, x.k_end, lo_page, phys, &tm_k, c, false);
                 if (pb >= 0)
                     for (int c = 0; c < kPvChunks && ok; ++c)
                         ok = load_chunk(pg, pts, pend_end, pend_lo, pphys, &tm_v, c, true);
-                pb = x.b; pg = x.g; pts = ts; pend_end = x.k_end; pend_lo = x.lo; pphys = phys;
+                pb = x.b; pg = x.g; pts = ts; pend_end = x.k_end; pend_lo = lo_page; pphys = phys;
             }
         }
         if (ok && pb >= 0)
@@ -635,9 +639,10 @@ cudaError_t launch_latent_decode(const DecodeParams &p, const CUtensorMap &tq, c
     if (e != cudaSuccess) return e;
     ++*launches;
     if (timing_start) cudaEventRecord(timing_start, stream);
-    e = launch_after_previous(p.packed ? latent_decode_kernel<true> : latent_decode_kernel<false>, dim3(p.grid),
-                              dim3(192), kSmemBytes, stream, p, tq, tk, tv);
-    if (e != cudaSuccess) return e;
+    // An ordinary launch, as for the CTA-pair kernel (programmatic
+    // serialization under the plan kernel measured slower there).
+    if (p.packed) latent_decode_kernel<true><<<p.grid, 192, kSmemBytes, stream>>>(p, tq, tk, tv);
+    else latent_decode_kernel<false><<<p.grid, 192, kSmemBytes, stream>>>(p, tq, tk, tv);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     ++*launches;

@@ -185,22 +185,26 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
         const int box_rows = p.ps < kKeysCta ? p.ps : kKeysCta;
         // Pages holding keys [ks, ks + 128) below k_end; lane l < that count
         // gets the l-th one's physical page (read one step ahead of use).
+        // Pages below a half are powers of two: shifts instead of divisions.
+        const int ps_shift = __ffs(p.ps) - 1;
         auto npages_of = [&](int ks, int k_end) -> int {
             if (ks >= k_end) return 0;
             if (p.ps >= kKeysCta) return 1;
-            return min(kKeysCta / p.ps, ceil_div_i(k_end - ks, p.ps));
+            return min(kKeysCta >> ps_shift, (k_end - ks + p.ps - 1) >> ps_shift);
         };
-        // Leading pages of keys [ks, ks + 128) wholly before k_lo (the first
-        // key of a sliding window): never looked up nor loaded.
-        auto skip_of = [&](int ks, int k_lo) -> int {
-            return p.ps >= kKeysCta ? 0 : max(0, k_lo / p.ps - ks / p.ps);
+        // Logical page of key ks.
+        auto page_of = [&](int ks) { return p.ps < kKeysCta ? ks >> ps_shift : ks / p.ps; };
+        // Leading pages of keys [ks, ks + 128) wholly before the page holding
+        // the window's first key (lo_page): never looked up nor loaded.
+        auto skip_of = [&](int ks, int lo_page) -> int {
+            return p.ps >= kKeysCta ? 0 : max(0, lo_page - (ks >> ps_shift));
         };
         // The load is issued a step before the page is copied; its range
         // check waits until then (in fill), so the walk never stalls on it.
-        auto lookup = [&](int b, int ks, int k_end, int k_lo) -> int {
+        auto lookup = [&](int b, int ks, int k_end, int lo_page) -> int {
             int phys = 0;
-            if (lane >= skip_of(ks, k_lo) && lane < npages_of(ks, k_end))
-                phys = __ldg(p.block_table + (int64_t)b * p.bt_stride + ks / p.ps + lane);
+            if (lane >= skip_of(ks, lo_page) && lane < npages_of(ks, k_end))
+                phys = __ldg(p.block_table + (int64_t)b * p.bt_stride + page_of(ks) + lane);
             return phys;
         };
         // Keys [ks, ks + 128) below k_end, `ncb` 64-column blocks from column
@@ -209,9 +213,9 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
         // cleared first: their values may be anything, and a zero probability
         // times a NaN is still NaN.
         auto fill = [&](uint64_t *full, uint8_t *dst, const CUtensorMap *tm, int g, int col0, int ncb, int ks,
-                        int k_end, int k_lo, int phys, bool zero_tail) -> bool {
+                        int k_end, int lo_page, int phys, bool zero_tail) -> bool {
             const int np = npages_of(ks, k_end);
-            const int skip = min(np, skip_of(ks, k_lo));
+            const int skip = min(np, skip_of(ks, lo_page));
             const bool load = lane >= skip && lane < np;
             const int slot0 = p.ps >= kKeysCta ? ks % p.ps : 0;
             const uint32_t full0 = cluster_addr(full, 0);
@@ -262,6 +266,7 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
         };
         bool ok = true, pend = false;
         int pg = 0, pts = 0, pend_end = 0, pend_lo = 0, pph0 = 0, pph1 = 0;   // the step whose PV is still to be fed
+        int lo_page = 0;                                                        // page of the piece's first key
         // This CTA's value columns of both key halves of the pending step.
         auto feed_pv = [&]() -> bool {
             for (int v = 0; v < 4; ++v, ++m) {
@@ -295,13 +300,14 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
             __syncwarp();
             ++nq;
             const int nsteps = (x.ntiles + 1) >> 1;
-            int ph0 = lookup(x.b, x.k_begin, x.k_end, x.lo), ph1 = lookup(x.b, x.k_begin + kKeysCta, x.k_end, x.lo);
+            lo_page = x.lo / p.ps;
+            int ph0 = lookup(x.b, x.k_begin, x.k_end, lo_page), ph1 = lookup(x.b, x.k_begin + kKeysCta, x.k_end, lo_page);
             for (int s = 0; s < nsteps && ok; ++s) {
                 const int ts = x.k_begin + s * kStepKeys;
                 const int c0 = ph0, c1 = ph1;
                 if (s + 1 < nsteps) {
-                    ph0 = lookup(x.b, ts + kStepKeys, x.k_end, x.lo);
-                    ph1 = lookup(x.b, ts + kStepKeys + kKeysCta, x.k_end, x.lo);
+                    ph0 = lookup(x.b, ts + kStepKeys, x.k_end, lo_page);
+                    ph1 = lookup(x.b, ts + kStepKeys + kKeysCta, x.k_end, lo_page);
                 }
                 const int own_ks = ts + (int)rank * kKeysCta;
                 const int own_ph = rank ? c1 : c0;
@@ -310,16 +316,16 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
                     const uint32_t sl = m % kSlots;
                     if (!dec::warp_wait(&slot_empty[sl], ((m / kSlots) & 1) ^ 1, wc, lane)) { ok = false; break; }
                     ok = fill(&slot_full[sl], sRing + sl * kSlotBytes, &tm_k, x.g, c * 128, 2, own_ks, x.k_end,
-                              x.lo, own_ph, false);
+                              lo_page, own_ph, false);
                 }
                 if (!ok) break;
                 if (pw == 0) {
                     if (!dec::warp_wait(rot_empty, (nr & 1) ^ 1, wc, lane)) { ok = false; break; }
-                    ok = fill(rot_full, sRot, &tm_k, x.g, 512, 1, own_ks, x.k_end, x.lo, own_ph, false);
+                    ok = fill(rot_full, sRot, &tm_k, x.g, 512, 1, own_ks, x.k_end, lo_page, own_ph, false);
                 }
                 ++nr;
                 if (ok && pend) ok = feed_pv();
-                pend = true; pg = x.g; pts = ts; pend_end = x.k_end; pend_lo = x.lo; pph0 = c0; pph1 = c1;
+                pend = true; pg = x.g; pts = ts; pend_end = x.k_end; pend_lo = lo_page; pph0 = c0; pph1 = c1;
             }
         }
         if (ok && pend) ok = feed_pv();
@@ -760,9 +766,10 @@ cudaError_t launch_latent_pair_decode(const DecodeParams &p, const CUtensorMap &
     if (e != cudaSuccess) return e;
     ++*launches;
     if (timing_start) cudaEventRecord(timing_start, stream);
-    e = launch_after_previous(p.packed ? latent_pair_decode_kernel<true> : latent_pair_decode_kernel<false>,
-                              dim3(p.grid), dim3(kThreads), kSmemBytes, stream, p, tq, tk, tv);
-    if (e != cudaSuccess) return e;
+    // An ordinary launch: starting under the plan kernel (programmatic
+    // serialization) measured ~2% slower for this kernel.
+    if (p.packed) latent_pair_decode_kernel<true><<<p.grid, kThreads, kSmemBytes, stream>>>(p, tq, tk, tv);
+    else latent_pair_decode_kernel<false><<<p.grid, kThreads, kSmemBytes, stream>>>(p, tq, tk, tv);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     ++*launches;
