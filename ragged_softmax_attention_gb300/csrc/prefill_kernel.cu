@@ -301,8 +301,11 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                                 (first && kk == 0) ? 0u : 1u);
                 }
             };
-            auto commit_pv = [&]() {
-                mma_commit(&pv_done[x]);
+            // pv_done completes once per unit, after the tile's last PV (the
+            // epilogue's wait): within the unit, S_{j+1} landing already
+            // implies PV_j complete (the same thread's earlier MMAs).
+            auto commit_pv = [&](bool last) {
+                if (last) mma_commit(&pv_done[x]);
                 ++pv_cnt;
             };
             // Each issuing thread releases every ring position of the unit
@@ -378,7 +381,7 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                         // empty pipe.
                         mbar_arrive(&issued[x]);
                         if (next_mine) push_qk(rk);
-                        commit_pv();
+                        commit_pv(j == n - 1);
                         release_tile(rv);
                         if (next_mine) { commit_qk(); release_tile(rk); }
                     } else if (!release_unused(rv)) {
@@ -409,8 +412,8 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
         const int row = q4 * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         const bool scale_pos = p.scale_log2 >= 0.f;
-        uint32_t s_cnt = 0, pv_cnt = 0;
-        // Completion of this tile's PV number i.
+        uint32_t s_cnt = 0, pv_units = 0;
+        // Completion of the last PV of this tile's unit number i.
         auto wait_pv = [&](uint32_t i) {
             mbar_wait(&pv_done[x], i & 1u, wc);
             tc_fence_after();
@@ -484,9 +487,9 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                     }
                     return ((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]));
                 };
-                // P overwrites the tile's only S buffer, which the previous PV
-                // reads, so that PV must have landed first.
-                if (j > 0) wait_pv(pv_cnt + j - 1);
+                // P overwrites the tile's only S buffer, which PV_{j-1} reads:
+                // that PV has landed, since the same thread issued it before
+                // QK_j, whose completion s_full reported.
                 // Static anchor ("Flywheel Attention", section 3.1 and appendix
                 // A): a row's anchor is the max of the first tile in which it sees
                 // a key and does not move on the fast path, so the exponent pass
@@ -532,7 +535,7 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
             __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(p.out) +
                                   (int64_t)(u.s.q0 + q_row) * p.out_stride[0] + (int64_t)u.h * p.out_stride[1];
             if (nkv > 0) {
-                wait_pv(pv_cnt + nkv - 1);
+                wait_pv(pv_units++);
                 const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
@@ -558,7 +561,6 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
             if (row_valid && p.lse)
                 p.lse[(int64_t)(u.s.q0 + q_row) * p.lse_stride[0] + (int64_t)u.h * p.lse_stride[1]] =
                     l_sum > 0.f ? (m_ref + __log2f(l_sum)) * 0.69314718055994531f : kNegInf;
-            pv_cnt += nkv;
         }
     }
 
