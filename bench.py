@@ -290,9 +290,17 @@ def prefill_flops(cu_q, cu_k, hq, dk, dv, causal):
     return total * hq * 2 * (dk + dv)
 
 
-def bench_prefill(fw, torch, steps, warmup, device, peaks, name=None):
-    from ragged_softmax_attention_gb300.workloads import WORKLOADS, make_prefill_inputs
+def bench_prefill(fw, torch, steps, warmup, device, peaks, name=None, softmax="static"):
     name = name or PREFILL_WL
+    fw.set_option(fw.FW_OPT_PREFILL_SOFTMAX, 1 if softmax == "online" else 0)
+    try:
+        return _bench_prefill(fw, torch, steps, warmup, device, peaks, name, softmax)
+    finally:
+        fw.set_option(fw.FW_OPT_PREFILL_SOFTMAX, 0)
+
+
+def _bench_prefill(fw, torch, steps, warmup, device, peaks, name, softmax):
+    from ragged_softmax_attention_gb300.workloads import WORKLOADS, make_prefill_inputs
     wl = WORKLOADS[name]
     d = make_prefill_inputs(wl, device)
     cu_q = d["cu_seqlens_q"].cpu().tolist()
@@ -338,7 +346,9 @@ def bench_prefill(fw, torch, steps, warmup, device, peaks, name=None):
             "config": {"num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads, "num_kv_heads": wl.num_kv_heads,
                        "head_dim": wl.head_dim_qk, "causal": wl.causal, "total_tokens": cu_q[-1],
                        "seq_len_range": list(wl.seq_len_range) if wl.seq_len_range else None,
-                       "seq_lens": list(wl.seq_lens) if wl.seq_lens else None, "scale": wl.scale},
+                       "seq_lens": list(wl.seq_lens) if wl.seq_lens else None, "scale": wl.scale,
+                       "softmax": "static anchor, check and replay" if softmax == "static"
+                       else "online, conditional rescale (8 log2 units)"},
             "roofline": {"kernel": "varlen_prefill_kernel" if wl.head_dim_qk == 128 else "varlen_prefill_pair_kernel", "bound": "tensor", "achieved": round(ach, 1),
                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": round(ach / peaks["bf16_tflops"], 4),
@@ -656,6 +666,8 @@ def main():
                     help="profiling runs: a prefix of the decode batch (smaller capture)")
     ap.add_argument("--latent-batch", type=int, default=0,
                     help="profiling runs: a prefix of the latent decode batch (smaller capture)")
+    ap.add_argument("--prefill-softmax", choices=["static", "online"], default="static",
+                    help="with --only prefill/prefill256: the prefill softmax mode to time")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -684,7 +696,8 @@ def main():
     if args.only in ("prefill", "prefill256"):
         key = "prefill" if args.only == "prefill" else "prefill_hd256"
         pre = bench_prefill(fw, torch, args.steps, args.warmup, device, peaks,
-                            name=PREFILL_WL if args.only == "prefill" else PREFILL_HD256_WL)
+                            name=PREFILL_WL if args.only == "prefill" else PREFILL_HD256_WL,
+                            softmax=args.prefill_softmax)
         if rank == 0:
             print(json.dumps({key: pre}), flush=True)
         return 0

@@ -333,7 +333,12 @@ typedef enum {
     FW_OPT_DECODE_CHUNK_TOKENS = 0, /* force the keys per CTA range (multiple of 128; 0 = auto) */
     FW_OPT_WAIT_TIMEOUT_MS = 1,     /* device wait limit before giving up (default 2000) */
     FW_OPT_KERNEL_TIMING = 2,       /* 1: record CUDA events around each attention kernel */
-    FW_OPT_MAX_CTAS = 3             /* cap on persistent CTAs (0 = one per SM) */
+    FW_OPT_MAX_CTAS = 3,            /* cap on persistent CTAs (0 = one per SM) */
+    FW_OPT_PREFILL_SOFTMAX = 4      /* prefill softmax: 0 = static anchor with a check and replay
+                                       ("Flywheel Attention", section 3.1, default); 1 = online
+                                       softmax with a conditional rescale (the base moves when a
+                                       row max rises more than 8 log2 units).  Same result up to
+                                       rounding; kept for comparison. */
 } fw_option_t;
 
 fw_status_t fw_set_option(int32_t option, int64_t value);

@@ -11,4 +11,4 @@ from ._binding import (FwError, device_status, kernel_timing_read, launch_count,
                        set_option,
                        set_workspace, varlen_prefill)
 from ._binding import (FW_OPT_DECODE_CHUNK_TOKENS, FW_OPT_KERNEL_TIMING, FW_OPT_MAX_CTAS,  # noqa: F401
-                       FW_OPT_WAIT_TIMEOUT_MS)
+                       FW_OPT_PREFILL_SOFTMAX, FW_OPT_WAIT_TIMEOUT_MS)

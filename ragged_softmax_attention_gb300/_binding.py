@@ -21,6 +21,7 @@ STATUS_NAMES = {0: "FW_OK", 1: "FW_ERR_INVALID_ARG", 2: "FW_ERR_UNSUPPORTED", 3:
                 4: "FW_ERR_CUDA", 5: "FW_ERR_DEVICE_TIMEOUT"}
 FW_BF16, FW_F32, FW_I32, FW_FP8_E4M3 = 0, 1, 2, 3
 FW_OPT_DECODE_CHUNK_TOKENS, FW_OPT_WAIT_TIMEOUT_MS, FW_OPT_KERNEL_TIMING, FW_OPT_MAX_CTAS = 0, 1, 2, 3
+FW_OPT_PREFILL_SOFTMAX = 4
 
 _DTYPES = {torch.bfloat16: FW_BF16, torch.float32: FW_F32, torch.int32: FW_I32,
            torch.float8_e4m3fn: FW_FP8_E4M3}

@@ -55,6 +55,7 @@ int64_t g_opt_chunk = 0;
 int64_t g_opt_timeout_ms = 2000;
 int64_t g_opt_timing = 0;
 int64_t g_opt_max_ctas = 0;
+int64_t g_opt_prefill_online = 0;
 
 struct TimedLaunch { cudaEvent_t a, b; };
 std::vector<TimedLaunch> g_timed;      // pending event pairs
@@ -313,6 +314,9 @@ fw_status_t fw_set_option(int32_t option, int64_t value) {
         case FW_OPT_MAX_CTAS:
             if (value < 0) return fail(FW_ERR_INVALID_ARG, "max CTAs must be >= 0");
             g_opt_max_ctas = value; return ok();
+        case FW_OPT_PREFILL_SOFTMAX:
+            if (value != 0 && value != 1) return fail(FW_ERR_INVALID_ARG, "prefill softmax mode must be 0 or 1");
+            g_opt_prefill_online = value; return ok();
         default: return fail(FW_ERR_INVALID_ARG, "unknown option %d", option);
     }
 }
@@ -852,6 +856,7 @@ fw_status_t fw_varlen_prefill(const fw_tensor_t *q, const fw_tensor_t *k, const 
     fw::PrefillParams p{};
     p.B = (int)B; p.Hq = (int)Hq; p.Hkv = (int)Hkv; p.G = (int)(Hq / Hkv); p.causal = causal ? 1 : 0;
     p.Dv = (int)Dv;
+    p.online = g_opt_prefill_online ? 1 : 0;
     p.total_q = total_q; p.total_k = total_k;
     p.cu_q = static_cast<const int32_t *>(cu_seqlens_q->data);
     p.cu_k = static_cast<const int32_t *>(cu_seqlens_k->data);

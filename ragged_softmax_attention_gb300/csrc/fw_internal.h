@@ -99,6 +99,7 @@ struct DecodeParams {
 // list, which balances the sums).
 struct PrefillParams {
     int B, Hq, Hkv, G, causal, Dv;
+    int online;           // 0: static anchor with check and replay; 1: online softmax, conditional rescale
     int64_t total_q, total_k;
     const int32_t *cu_q, *cu_k;
     void *out; int64_t out_stride[3];          // [total_q, Hq, Dv] bf16

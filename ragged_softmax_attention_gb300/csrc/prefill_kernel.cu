@@ -40,6 +40,10 @@ constexpr float kNegInf = -__builtin_huge_valf();
 // entry of O (|O| <= l * max|v|) far inside FP32 for |v| < 2^90; Flywheel's
 // appendix A derives its budget the same way, in natural-log units.
 constexpr float kAnchorBudget = 4294967296.0f;
+// Online mode: the base moves only when a row max rises more than this many
+// log2 units above it ("TokenSpeed-MLA 2.0.1" keeps its base for rises up to
+// 8 in split mode), so every p <= 2^8.
+constexpr float kRescaleSlack = 8.0f;
 constexpr int kQTile = 128;
 constexpr int kCostBins = 4096;
 
@@ -165,6 +169,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+template <bool kOnline>
 __global__ void __launch_bounds__(PrefillCfg::kThreads, 1)
 varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
@@ -494,36 +499,60 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                 // A): a row's anchor is the max of the first tile in which it sees
                 // a key and does not move on the fast path, so the exponent pass
                 // needs no running max.
-                if (m_ref == kNegInf) m_ref = row_max();
-                float tsum = write_p(m_ref);
-                // The check: every p <= l, so a running sum within the budget
-                // proves no score rose more than log2(budget) above the anchor
-                // (appendix A, claim 2).  A row that fails (or overflowed) replays
-                // the tile with the rescaling softmax: its anchor moves to the new
-                // max, l and O are rescaled, P is recomputed before the MMA sees it.
-                const bool over = !(l_sum + tsum <= kAnchorBudget);
-                if (__any_sync(0xffffffffu, over)) {
-                    float alpha = 1.f;
-                    if (over) {
-                        const float m_new = fmaxf(m_ref, row_max());
-                        alpha = ex2_approx(m_ref - m_new);
-                        l_sum *= alpha;
-                        m_ref = m_new;
+                // O *= alpha for this thread's row (warp-collective TMEM
+                // access; PV_{j-1} has landed, since S_j has).
+                auto rescale_o = [&](float alpha) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        float o[32];
+                        const uint32_t oa = tmem + lane_off + C::o_col(x) + c * 32;
+                        tmem_ld32(oa, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                        tmem_st32(oa, o);
                     }
-                    if (j > 0) {
-#pragma unroll
-                        for (int c = 0; c < D / 32; ++c) {
-                            float o[32];
-                            const uint32_t oa = tmem + lane_off + C::o_col(x) + c * 32;
-                            tmem_ld32(oa, o);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                            tmem_st32(oa, o);
+                    tmem_wait_st();
+                };
+                float tsum;
+                if constexpr (kOnline) {
+                    // Online softmax with a conditional rescale ("Flywheel
+                    // Attention", section 1): the tile's row max is taken every
+                    // tile, and the base moves to it (l and O rescaled) only when
+                    // it rose more than kRescaleSlack above the base.
+                    const float m_tile = row_max();
+                    const bool up = m_tile > m_ref + kRescaleSlack;
+                    if (__any_sync(0xffffffffu, up)) {
+                        float alpha = 1.f;
+                        if (up) {
+                            alpha = ex2_approx(m_ref - m_tile);    // 0 while the row had no base
+                            l_sum *= alpha;
+                            m_ref = m_tile;
                         }
-                        tmem_wait_st();
+                        if (j > 0) rescale_o(alpha);
                     }
-                    tsum = write_p(m_ref);         // all lanes: unchanged rows rewrite the same P
+                    tsum = write_p(m_ref);
+                } else {
+                    if (m_ref == kNegInf) m_ref = row_max();
+                    tsum = write_p(m_ref);
+                    // The check: every p <= l, so a running sum within the budget
+                    // proves no score rose more than log2(budget) above the anchor
+                    // (appendix A, claim 2).  A row that fails (or overflowed)
+                    // replays the tile with the rescaling softmax: its anchor moves
+                    // to the new max, l and O are rescaled, P is recomputed before
+                    // the MMA sees it.
+                    const bool over = !(l_sum + tsum <= kAnchorBudget);
+                    if (__any_sync(0xffffffffu, over)) {
+                        float alpha = 1.f;
+                        if (over) {
+                            const float m_new = fmaxf(m_ref, row_max());
+                            alpha = ex2_approx(m_ref - m_new);
+                            l_sum *= alpha;
+                            m_ref = m_new;
+                        }
+                        if (j > 0) rescale_o(alpha);
+                        tsum = write_p(m_ref);     // all lanes: unchanged rows rewrite the same P
+                    }
                 }
                 l_sum += tsum;
                 tmem_wait_st();
@@ -607,6 +636,7 @@ __device__ __forceinline__ int pair_snake_index(int k) {
     return k * nc + ((k & 1) ? (nc - 1 - c) : c);
 }
 
+template <bool kOnline>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
 varlen_prefill_pair_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tm_q,
                            const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
@@ -874,32 +904,58 @@ varlen_prefill_pair_kernel(const __grid_constant__ PrefillParams p, const __grid
                 };
                 // Static anchor and the running-sum check, as in the one-CTA
                 // kernel; P(j) goes to S buffer j & 1, which PV(j-1) does not read.
-                if (m_ref == kNegInf) m_ref = row_max();
-                float tsum = write_p(m_ref);
-                const bool over = !(l_sum + tsum <= kAnchorBudget);
-                if (__any_sync(0xffffffffu, over)) {
-                    float alpha = 1.f;
-                    if (over) {
-                        const float m_new = fmaxf(m_ref, row_max());
-                        alpha = ex2_approx(m_ref - m_new);
-                        l_sum *= alpha;
-                        m_ref = m_new;
+                // O *= alpha for this thread's row, once PV(j-1) has landed
+                // (warp-collective TMEM access).
+                auto rescale_o = [&](float alpha) {
+                    wait_pv(pv_cnt + j - 1);
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        float o[32];
+                        const uint32_t oa = tmem + lane_off + 256u + c * 32;
+                        tmem_ld32(oa, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                        tmem_st32(oa, o);
                     }
-                    if (j > 0) {
-                        wait_pv(pv_cnt + j - 1);
-#pragma unroll
-                        for (int c = 0; c < D / 32; ++c) {
-                            float o[32];
-                            const uint32_t oa = tmem + lane_off + 256u + c * 32;
-                            tmem_ld32(oa, o);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                            tmem_st32(oa, o);
+                    tmem_wait_st();
+                };
+                float tsum;
+                if constexpr (kOnline) {
+                    // Online softmax with a conditional rescale, as in the one-CTA kernel.
+                    const float m_tile = row_max();
+                    const bool up = m_tile > m_ref + kRescaleSlack;
+                    if (__any_sync(0xffffffffu, up)) {
+                        float alpha = 1.f;
+                        if (up) {
+                            alpha = ex2_approx(m_ref - m_tile);    // 0 while the row had no base
+                            l_sum *= alpha;
+                            m_ref = m_tile;
                         }
-                        tmem_wait_st();
+                        if (j > 0) rescale_o(alpha);
                     }
                     tsum = write_p(m_ref);
+                } else {
+                    if (m_ref == kNegInf) m_ref = row_max();
+                    tsum = write_p(m_ref);
+                    // The check: every p <= l, so a running sum within the budget
+                    // proves no score rose more than log2(budget) above the anchor
+                    // (appendix A, claim 2).  A row that fails (or overflowed)
+                    // replays the tile with the rescaling softmax: its anchor moves
+                    // to the new max, l and O are rescaled, P is recomputed before
+                    // the MMA sees it.
+                    const bool over = !(l_sum + tsum <= kAnchorBudget);
+                    if (__any_sync(0xffffffffu, over)) {
+                        float alpha = 1.f;
+                        if (over) {
+                            const float m_new = fmaxf(m_ref, row_max());
+                            alpha = ex2_approx(m_ref - m_new);
+                            l_sum *= alpha;
+                            m_ref = m_new;
+                        }
+                        if (j > 0) rescale_o(alpha);
+                        tsum = write_p(m_ref);     // all lanes: unchanged rows rewrite the same P
+                    }
                 }
                 l_sum += tsum;
                 tmem_wait_st();
@@ -1077,33 +1133,35 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const __grid_constan
     }
 }
 
+template <bool kOnline>
 cudaError_t launch_tiles(const PrefillParams &p, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                          cudaStream_t stream) {
     using C = PrefillCfg;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(varlen_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(varlen_prefill_kernel<kOnline>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    cudaError_t le = launch_after_previous(varlen_prefill_kernel, dim3(p.grid), dim3(C::kThreads), C::kSmemBytes,
-                                           stream, p, tq, tk, tv);
+    cudaError_t le = launch_after_previous(varlen_prefill_kernel<kOnline>, dim3(p.grid), dim3(C::kThreads),
+                                           C::kSmemBytes, stream, p, tq, tk, tv);
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
 
+template <bool kOnline>
 cudaError_t launch_pair(const PrefillParams &p, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                         cudaStream_t stream) {
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(varlen_prefill_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kPairSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(varlen_prefill_pair_kernel<kOnline>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    cudaError_t le = launch_after_previous(varlen_prefill_pair_kernel, dim3(p.grid & ~1), dim3(256), kPairSmemBytes,
-                                           stream, p, tq, tk, tv);
+    cudaError_t le = launch_after_previous(varlen_prefill_pair_kernel<kOnline>, dim3(p.grid & ~1), dim3(256),
+                                           kPairSmemBytes, stream, p, tq, tk, tv);
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
@@ -1119,8 +1177,8 @@ cudaError_t launch_prefill(const PrefillParams &p, const CUtensorMap &tq, const 
     if (e != cudaSuccess) return e;
     ++*launches;
     if (timing_start) cudaEventRecord(timing_start, stream);
-    if (head_dim == 128) e = launch_tiles(p, tq, tk, tv, stream);
-    else if (head_dim == 256) e = launch_pair(p, tq, tk, tv, stream);
+    if (head_dim == 128) e = p.online ? launch_tiles<true>(p, tq, tk, tv, stream) : launch_tiles<false>(p, tq, tk, tv, stream);
+    else if (head_dim == 256) e = p.online ? launch_pair<true>(p, tq, tk, tv, stream) : launch_pair<false>(p, tq, tk, tv, stream);
     else return cudaErrorInvalidValue;
     if (e != cudaSuccess) return e;
     ++*launches;

@@ -168,6 +168,15 @@ def test_forced_chunk_option(fwlib):
         fwlib.set_option(fwlib.FW_OPT_DECODE_CHUNK_TOKENS, 100)
 
 
+def test_prefill_softmax_option(fwlib):
+    """0 (static anchor) and 1 (online, conditional rescale) are the only modes."""
+    for mode in (1, 0):
+        fwlib.set_option(fwlib.FW_OPT_PREFILL_SOFTMAX, mode)
+    for bad in (-1, 2):
+        with pytest.raises(fwlib.FwError):
+            fwlib.set_option(fwlib.FW_OPT_PREFILL_SOFTMAX, bad)
+
+
 # ------------------------------------------------------- validation, no GPU
 
 def fake(shape, dtype, ptr=0x10000, strides=None):

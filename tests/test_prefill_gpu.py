@@ -140,6 +140,52 @@ def test_scale_extremes_exercise_anchor_replay(fw, scale, d):
     run_case(fw, wl, [300, 700, 129])
 
 
+@pytest.fixture
+def online(fw):
+    """The prefill in its online-softmax mode (conditional rescale) for one test."""
+    fw.set_option(fw.FW_OPT_PREFILL_SOFTMAX, 1)
+    yield fw
+    fw.set_option(fw.FW_OPT_PREFILL_SOFTMAX, 0)
+
+
+@pytest.mark.parametrize("d", [128, 256])
+@pytest.mark.parametrize("causal", [True, False])
+def test_online_mode_ragged_batch(online, d, causal):
+    """The conditional-rescale mode on ragged batches, empty and one-row sequences included."""
+    run_case(online, wl_prefill(d=d, causal=causal), [130, 1, 257, 64, 0, 400])
+
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_online_mode_different_packs(online, d):
+    run_case(online, wl_prefill(d=d), [100, 5, 300, 7], [500, 5, 300, 0])
+
+
+@pytest.mark.parametrize("scale", [2.0, -0.2])
+@pytest.mark.parametrize("d", [128, 256])
+def test_online_mode_rescales(online, scale, d):
+    """Scores spread over ~100 log2 units: row maxima rise tile after tile, so the
+    base moves often and l and O are rescaled in TMEM."""
+    wl = PrefillWorkload("s", num_seqs=0, num_q_heads=4, num_kv_heads=2, head_dim_qk=d, head_dim_v=d,
+                         causal=True, scale=scale, value_seed=41)
+    run_case(online, wl, [300, 700, 129])
+
+
+@pytest.mark.parametrize("name", ["varlen_gqa_prefill", "dense_causal_mha_hd256"])
+def test_online_mode_full_size_sampled_rows(online, name):
+    """Both softmax modes give the same result up to rounding at full size."""
+    wl = WORKLOADS[name]
+    d = make_prefill_inputs(wl, "cuda")
+    out, lse = online.varlen_prefill(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], wl.causal,
+                                     wl.scale)
+    torch.cuda.synchronize()
+    assert online.device_status() == 0
+    total = d["q"].shape[0] * wl.num_q_heads
+    rows = np.sort(np.random.default_rng(10).choice(total, size=512, replace=False))
+    ref_o, ref_l = oracle.varlen_prefill(d["q"].cpu(), d["k"].cpu(), d["v"].cpu(), d["cu_seqlens_q"].cpu(),
+                                         d["cu_seqlens_k"].cpu(), wl.causal, wl.scale, rows=rows)
+    compare(out.reshape(-1, out.shape[-1])[rows], lse.reshape(-1)[rows], ref_o, ref_l, name + " online")
+
+
 @pytest.mark.parametrize("name", ["varlen_gqa_prefill", "dense_causal_mha_hd256"])
 def test_repeated_launches_are_bitwise_identical(fw, name):
     """Every launch writes the same bytes: an accumulator read before its last
