@@ -46,16 +46,16 @@ def _load():
         D = ctypes.c_double
         lib.oracle_paged_decode.restype = I
         lib.oracle_paged_decode.argtypes = [P, P, P, P, P, P, P, L, P, I, I, I, I, I, I, I, I, I, D,
-                                            P, L, P, P, I]
+                                            P, L, P, P, P, I]
         lib.oracle_paged_decode_kv8.restype = I
         lib.oracle_paged_decode_kv8.argtypes = [P, P, P, P, P, P, D, D, P, L, P, I, I, I, I, I, I, I, I, I, D,
-                                                P, L, P, P, I]
+                                                P, L, P, P, P, I]
         lib.oracle_paged_decode_window.restype = I
         lib.oracle_paged_decode_window.argtypes = [P, P, P, P, P, P, I, D, D, I, P, L, P, I, I, I, I, I, I, I, I, I,
-                                                   D, P, L, P, P, I]
+                                                   D, P, L, P, P, P, I]
         lib.oracle_paged_decode_masked.restype = I
         lib.oracle_paged_decode_masked.argtypes = [P, P, P, P, P, P, I, D, D, I, I, P, L, P, I, I, I, I, I, I, I,
-                                                   I, I, D, P, L, P, P, I]
+                                                   I, I, D, P, L, P, P, P, I]
         lib.oracle_e4m3_from_float.restype = ctypes.c_uint8
         lib.oracle_e4m3_from_float.argtypes = [ctypes.c_float]
         lib.oracle_kv_append.restype = I
@@ -65,7 +65,7 @@ def _load():
         lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
         lib.oracle_varlen_prefill.restype = I
         lib.oracle_varlen_prefill.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, D,
-                                              P, L, P, P, I]
+                                              P, L, P, P, P, I]
         _lib = lib
     return _lib
 
@@ -99,7 +99,7 @@ def e4m3_to_double(byte: int) -> float:
 
 
 def paged_decode(q, k_cache, v_cache, block_table, seq_lens, scale, rows=None, threads=None,
-                 k_scale=1.0, v_scale=1.0, window_left=-1, causal=True):
+                 k_scale=1.0, v_scale=1.0, window_left=-1, causal=True, with_absv=False):
     """Softmax attention of every (b, t, h) query row over its paged keys.
 
     q [B, q_len, Hq, Dk], k_cache [P, ps, Hkv, Dk], v_cache [P, ps, Hkv, Dv]
@@ -111,7 +111,9 @@ def paged_decode(q, k_cache, v_cache, block_table, seq_lens, scale, rows=None, t
     2.0.1", window_left); block-table entries of keys before it are not read.
     causal=False: every token sees all n keys (TokenSpeed's non-causal
     decode), a window still starting at max(0, n - q_len + t - window_left).
-    Returns (out [n_rows, Dv] float64, lse [n_rows] float64, natural log).
+    Returns (out [n_rows, Dv] float64, lse [n_rows] float64, natural log);
+    with_absv=True adds absv [n_rows, Dv], the softmax-weighted mean of |v|
+    per output column (the scale of a kernel's rounding error, see oracle.c).
     """
     lib = _load()
     kv8 = k_cache.dtype == torch.float8_e4m3fn
@@ -137,6 +139,8 @@ def paged_decode(q, k_cache, v_cache, block_table, seq_lens, scale, rows=None, t
     n = rows_arr.size
     out = np.zeros((n, Dv), dtype=np.float64)
     lse = np.zeros((n,), dtype=np.float64)
+    absv = np.zeros((n, Dv), dtype=np.float64) if with_absv else None
+    ap = absv.ctypes.data if with_absv else None
     qs, ks, vs = _strides(q), _strides(k_cache), _strides(v_cache)
     if not causal:
         rc = lib.oracle_paged_decode_masked(
@@ -145,7 +149,7 @@ def paged_decode(q, k_cache, v_cache, block_table, seq_lens, scale, rows=None, t
             int(window_left if window_left is not None else -1),
             bt.ctypes.data, bt.shape[1], sl.ctypes.data,
             B, q_len, Hq, Hkv, Dk, Dv, ps, P, bt.shape[1], float(scale),
-            rows_arr.ctypes.data, n, out.ctypes.data, lse.ctypes.data,
+            rows_arr.ctypes.data, n, out.ctypes.data, lse.ctypes.data, ap,
             int(threads or default_threads()))
     elif window_left is not None and int(window_left) >= 0:
         rc = lib.oracle_paged_decode_window(
@@ -153,7 +157,7 @@ def paged_decode(q, k_cache, v_cache, block_table, seq_lens, scale, rows=None, t
             v_cache.data_ptr(), vs.ctypes.data, int(kv8), float(k_scale), float(v_scale), int(window_left),
             bt.ctypes.data, bt.shape[1], sl.ctypes.data,
             B, q_len, Hq, Hkv, Dk, Dv, ps, P, bt.shape[1], float(scale),
-            rows_arr.ctypes.data, n, out.ctypes.data, lse.ctypes.data,
+            rows_arr.ctypes.data, n, out.ctypes.data, lse.ctypes.data, ap,
             int(threads or default_threads()))
     elif kv8:
         rc = lib.oracle_paged_decode_kv8(
@@ -161,18 +165,18 @@ def paged_decode(q, k_cache, v_cache, block_table, seq_lens, scale, rows=None, t
             v_cache.data_ptr(), vs.ctypes.data, float(k_scale), float(v_scale),
             bt.ctypes.data, bt.shape[1], sl.ctypes.data,
             B, q_len, Hq, Hkv, Dk, Dv, ps, P, bt.shape[1], float(scale),
-            rows_arr.ctypes.data, n, out.ctypes.data, lse.ctypes.data,
+            rows_arr.ctypes.data, n, out.ctypes.data, lse.ctypes.data, ap,
             int(threads or default_threads()))
     else:
         rc = lib.oracle_paged_decode(
             q.data_ptr(), qs.ctypes.data, k_cache.data_ptr(), ks.ctypes.data,
             v_cache.data_ptr(), vs.ctypes.data, bt.ctypes.data, bt.shape[1], sl.ctypes.data,
             B, q_len, Hq, Hkv, Dk, Dv, ps, P, bt.shape[1], float(scale),
-            rows_arr.ctypes.data, n, out.ctypes.data, lse.ctypes.data,
+            rows_arr.ctypes.data, n, out.ctypes.data, lse.ctypes.data, ap,
             int(threads or default_threads()))
     if rc != 0:
         raise ValueError(f"oracle_paged_decode failed with code {rc}")
-    return out, lse
+    return (out, lse, absv) if with_absv else (out, lse)
 
 
 def e4m3_from_float(x: float) -> int:
@@ -211,12 +215,13 @@ def kv_append(k_new, v_new, slot_mapping, layer_base_rows, k_cache, v_cache, k_s
     return kc, vc
 
 
-def varlen_prefill(q, k, v, cu_seqlens_q, cu_seqlens_k, causal, scale, rows=None, threads=None):
+def varlen_prefill(q, k, v, cu_seqlens_q, cu_seqlens_k, causal, scale, rows=None, threads=None, with_absv=False):
     """Softmax attention of every packed query row over its own sequence's keys.
 
     q [total_q, Hq, Dk], k [total_k, Hkv, Dk], v [total_k, Hkv, Dv] bfloat16;
     cu_seqlens_q / cu_seqlens_k [B+1].  rows: optional flat ids token * Hq + h.
-    Returns (out [n_rows, Dv] float64, lse [n_rows] float64, natural log).
+    Returns (out [n_rows, Dv] float64, lse [n_rows] float64, natural log);
+    with_absv=True adds absv [n_rows, Dv] as in paged_decode.
     """
     lib = _load()
     q, k, v = _bf16(q), _bf16(k), _bf16(v)
@@ -234,12 +239,14 @@ def varlen_prefill(q, k, v, cu_seqlens_q, cu_seqlens_k, causal, scale, rows=None
     n = rows_arr.size
     out = np.zeros((n, Dv), dtype=np.float64)
     lse = np.zeros((n,), dtype=np.float64)
+    absv = np.zeros((n, Dv), dtype=np.float64) if with_absv else None
+    ap = absv.ctypes.data if with_absv else None
     qs, ks, vs = _strides(q), _strides(k), _strides(v)
     rc = lib.oracle_varlen_prefill(
         q.data_ptr(), qs.ctypes.data, k.data_ptr(), ks.ctypes.data, v.data_ptr(), vs.ctypes.data,
         cq.ctypes.data, ck.ctypes.data, B, Hq, Hkv, Dk, Dv, int(bool(causal)), float(scale),
-        rows_arr.ctypes.data, n, out.ctypes.data, lse.ctypes.data,
+        rows_arr.ctypes.data, n, out.ctypes.data, lse.ctypes.data, ap,
         int(threads or default_threads()))
     if rc != 0:
         raise ValueError(f"oracle_varlen_prefill failed with code {rc}")
-    return out, lse
+    return (out, lse, absv) if with_absv else (out, lse)

@@ -14,6 +14,15 @@
  *   l    = sum_j exp(s_j - m)
  *   out  = sum_j exp(s_j - m) v_j / l             (O = PV)
  *   lse  = m + ln l                               (natural-log log-sum-exp)
+ *   absv = sum_j exp(s_j - m) |v_j| / l           (optional output: the same
+ *                                                   weights on the magnitudes
+ *                                                   of the values)
+ *
+ * absv is not part of attention; it is the scale of the rounding error a
+ * kernel may make legitimately.  Rounding every weight exp(s_j - m) to a
+ * format with unit roundoff u before the PV product ("Writing Page Attention
+ * with PyPTO", section 6.3 casts P to BF16 for the matmul) moves each output
+ * column by at most about 2 u absv, whichever sum the kernel divides by.
  *
  * over the keys the row may see.  Rows with no visible key give out = 0 and
  * lse = -inf ("TokenSpeed-MLA 2.0.1", SM107 decode section: rows with no
@@ -88,9 +97,10 @@ static void attend_row(const uint16_t *q, int64_t q_dstride,
                        const uint16_t *const *krows, int64_t k_dstride,
                        const uint16_t *const *vrows, int64_t v_dstride,
                        int64_t nkeys, int dk, int dv, double scale,
-                       double *s /* scratch [nkeys] */, double *out, double *lse) {
+                       double *s /* scratch [nkeys] */, double *out, double *lse, double *absv) {
     if (nkeys <= 0) {
         for (int d = 0; d < dv; ++d) out[d] = 0.0;
+        if (absv) for (int d = 0; d < dv; ++d) absv[d] = 0.0;
         *lse = -INFINITY;
         return;
     }
@@ -104,12 +114,15 @@ static void attend_row(const uint16_t *q, int64_t q_dstride,
     }
     double l = 0.0;
     for (int d = 0; d < dv; ++d) out[d] = 0.0;
+    if (absv) for (int d = 0; d < dv; ++d) absv[d] = 0.0;
     for (int64_t j = 0; j < nkeys; ++j) {
         double p = exp(s[j] - m);
         l += p;
         for (int d = 0; d < dv; ++d) out[d] += p * bf16_to_double(vrows[j][d * v_dstride]);
+        if (absv) for (int d = 0; d < dv; ++d) absv[d] += p * fabs(bf16_to_double(vrows[j][d * v_dstride]));
     }
     for (int d = 0; d < dv; ++d) out[d] /= l;
+    if (absv) for (int d = 0; d < dv; ++d) absv[d] /= l;
     *lse = m + log(l);
 }
 
@@ -118,9 +131,10 @@ static void attend_row_kv8(const uint16_t *q, int64_t q_dstride,
                            const uint8_t *const *krows, int64_t k_dstride, double k_scale,
                            const uint8_t *const *vrows, int64_t v_dstride, double v_scale,
                            int64_t nkeys, int dk, int dv, double scale,
-                           double *s, double *out, double *lse) {
+                           double *s, double *out, double *lse, double *absv) {
     if (nkeys <= 0) {
         for (int d = 0; d < dv; ++d) out[d] = 0.0;
+        if (absv) for (int d = 0; d < dv; ++d) absv[d] = 0.0;
         *lse = -INFINITY;
         return;
     }
@@ -134,12 +148,17 @@ static void attend_row_kv8(const uint16_t *q, int64_t q_dstride,
     }
     double l = 0.0;
     for (int d = 0; d < dv; ++d) out[d] = 0.0;
+    if (absv) for (int d = 0; d < dv; ++d) absv[d] = 0.0;
     for (int64_t j = 0; j < nkeys; ++j) {
         double p = exp(s[j] - m);
         l += p;
         for (int d = 0; d < dv; ++d) out[d] += p * (v_scale * oracle_e4m3_to_double(vrows[j][d * v_dstride]));
+        if (absv)
+            for (int d = 0; d < dv; ++d)
+                absv[d] += p * fabs(v_scale * oracle_e4m3_to_double(vrows[j][d * v_dstride]));
     }
     for (int d = 0; d < dv; ++d) out[d] /= l;
+    if (absv) for (int d = 0; d < dv; ++d) absv[d] /= l;
     *lse = m + log(l);
 }
 
@@ -157,7 +176,7 @@ typedef struct {
     int B, q_len, Hq, Hkv, Dk, Dv, ps, num_pages, max_pages;
     double scale;
     const int64_t *rows; int64_t n_rows;
-    double *out, *lse;
+    double *out, *lse, *absv;                    /* absv may be NULL */
     int64_t begin, end;
     int status;
 } decode_job;
@@ -201,11 +220,12 @@ static void *decode_worker(void *arg) {
         if (J->kv8)
             attend_row_kv8(qrow, J->qs[3], (const uint8_t *const *)(kr + first), J->ks[3], J->k_scale,
                            (const uint8_t *const *)(vr + first), J->vs[3], J->v_scale, visible - first, J->Dk,
-                           J->Dv, J->scale, s, J->out + i * J->Dv, J->lse + i);
+                           J->Dv, J->scale, s, J->out + i * J->Dv, J->lse + i,
+                           J->absv ? J->absv + i * J->Dv : NULL);
         else
             attend_row(qrow, J->qs[3], (const uint16_t *const *)(kr + first), J->ks[3],
                        (const uint16_t *const *)(vr + first), J->vs[3], visible - first, J->Dk, J->Dv, J->scale, s,
-                       J->out + i * J->Dv, J->lse + i);
+                       J->out + i * J->Dv, J->lse + i, J->absv ? J->absv + i * J->Dv : NULL);
     }
 done:
     free(s); free(kr); free(vr);
@@ -221,7 +241,7 @@ static int paged_decode_any(const uint16_t *q, const int64_t *q_stride,
                             int B, int q_len, int Hq, int Hkv, int Dk, int Dv,
                             int page_size, int num_pages, int max_pages, double scale,
                             const int64_t *rows, int64_t n_rows,
-                            double *out, double *lse, int n_threads) {
+                            double *out, double *lse, double *absv, int n_threads) {
     if (Hkv <= 0 || Hq % Hkv != 0 || page_size <= 0) return -4;
     if (n_threads < 1) n_threads = 1;
     if (n_rows < n_threads) n_threads = (int)(n_rows > 0 ? n_rows : 1);
@@ -235,7 +255,7 @@ static int paged_decode_any(const uint16_t *q, const int64_t *q_stride,
         J->bt = block_table; J->bt_stride = bt_stride; J->seq_lens = seq_lens;
         J->B = B; J->q_len = q_len; J->Hq = Hq; J->Hkv = Hkv; J->Dk = Dk; J->Dv = Dv;
         J->ps = page_size; J->num_pages = num_pages; J->max_pages = max_pages; J->scale = scale;
-        J->rows = rows; J->n_rows = n_rows; J->out = out; J->lse = lse;
+        J->rows = rows; J->n_rows = n_rows; J->out = out; J->lse = lse; J->absv = absv;
         J->begin = n_rows * w / n_threads; J->end = n_rows * (w + 1) / n_threads;
         pthread_create(&tid[w], NULL, decode_worker, J);
     }
@@ -256,10 +276,10 @@ int oracle_paged_decode(const uint16_t *q, const int64_t *q_stride,
                         int B, int q_len, int Hq, int Hkv, int Dk, int Dv,
                         int page_size, int num_pages, int max_pages, double scale,
                         const int64_t *rows, int64_t n_rows,
-                        double *out, double *lse, int n_threads) {
+                        double *out, double *lse, double *absv, int n_threads) {
     return paged_decode_any(q, q_stride, k_cache, k_stride, v_cache, v_stride, 0, 1.0, 1.0, 1, -1, block_table,
                             bt_stride, seq_lens, B, q_len, Hq, Hkv, Dk, Dv, page_size, num_pages, max_pages,
-                            scale, rows, n_rows, out, lse, n_threads);
+                            scale, rows, n_rows, out, lse, absv, n_threads);
 }
 
 int oracle_paged_decode_kv8(const uint16_t *q, const int64_t *q_stride,
@@ -271,10 +291,10 @@ int oracle_paged_decode_kv8(const uint16_t *q, const int64_t *q_stride,
                             int B, int q_len, int Hq, int Hkv, int Dk, int Dv,
                             int page_size, int num_pages, int max_pages, double scale,
                             const int64_t *rows, int64_t n_rows,
-                            double *out, double *lse, int n_threads) {
+                            double *out, double *lse, double *absv, int n_threads) {
     return paged_decode_any(q, q_stride, k_cache, k_stride, v_cache, v_stride, 1, k_scale, v_scale, 1, -1, block_table,
                             bt_stride, seq_lens, B, q_len, Hq, Hkv, Dk, Dv, page_size, num_pages, max_pages,
-                            scale, rows, n_rows, out, lse, n_threads);
+                            scale, rows, n_rows, out, lse, absv, n_threads);
 }
 
 /* Either cache type (kv8 = 1: E4M3 bytes with scales) and a sliding window. */
@@ -287,10 +307,10 @@ int oracle_paged_decode_window(const uint16_t *q, const int64_t *q_stride,
                                int B, int q_len, int Hq, int Hkv, int Dk, int Dv,
                                int page_size, int num_pages, int max_pages, double scale,
                                const int64_t *rows, int64_t n_rows,
-                               double *out, double *lse, int n_threads) {
+                               double *out, double *lse, double *absv, int n_threads) {
     return paged_decode_any(q, q_stride, k_cache, k_stride, v_cache, v_stride, kv8, k_scale, v_scale, 1, window_left,
                             block_table, bt_stride, seq_lens, B, q_len, Hq, Hkv, Dk, Dv, page_size, num_pages,
-                            max_pages, scale, rows, n_rows, out, lse, n_threads);
+                            max_pages, scale, rows, n_rows, out, lse, absv, n_threads);
 }
 
 /* Either cache type, causal or not, and a sliding window (W < 0: none). */
@@ -303,10 +323,10 @@ int oracle_paged_decode_masked(const uint16_t *q, const int64_t *q_stride,
                                int B, int q_len, int Hq, int Hkv, int Dk, int Dv,
                                int page_size, int num_pages, int max_pages, double scale,
                                const int64_t *rows, int64_t n_rows,
-                               double *out, double *lse, int n_threads) {
+                               double *out, double *lse, double *absv, int n_threads) {
     return paged_decode_any(q, q_stride, k_cache, k_stride, v_cache, v_stride, kv8, k_scale, v_scale, causal,
                             window_left, block_table, bt_stride, seq_lens, B, q_len, Hq, Hkv, Dk, Dv, page_size,
-                            num_pages, max_pages, scale, rows, n_rows, out, lse, n_threads);
+                            num_pages, max_pages, scale, rows, n_rows, out, lse, absv, n_threads);
 }
 
 /* ----------------------------------------------------------------- prefill */
@@ -320,7 +340,7 @@ typedef struct {
     int64_t total_q, max_k;
     double scale;
     const int64_t *rows; int64_t n_rows;
-    double *out, *lse;
+    double *out, *lse, *absv;                    /* absv may be NULL */
     int64_t begin, end;
     int status;
 } prefill_job;
@@ -359,7 +379,7 @@ static void *prefill_worker(void *arg) {
         }
         const uint16_t *qrow = J->q + tok * J->qs[0] + (int64_t)h * J->qs[1];
         attend_row(qrow, J->qs[2], kr, J->ks[2], vr, J->vs[2], visible, J->Dk, J->Dv,
-                   J->scale, s, J->out + i * J->Dv, J->lse + i);
+                   J->scale, s, J->out + i * J->Dv, J->lse + i, J->absv ? J->absv + i * J->Dv : NULL);
     }
 done:
     free(s); free(kr); free(vr);
@@ -372,7 +392,7 @@ int oracle_varlen_prefill(const uint16_t *q, const int64_t *q_stride,
                           const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
                           int B, int Hq, int Hkv, int Dk, int Dv, int causal, double scale,
                           const int64_t *rows, int64_t n_rows,
-                          double *out, double *lse, int n_threads) {
+                          double *out, double *lse, double *absv, int n_threads) {
     if (Hkv <= 0 || Hq % Hkv != 0) return -4;
     int64_t max_k = 0;
     for (int b = 0; b < B; ++b) {
@@ -391,7 +411,7 @@ int oracle_varlen_prefill(const uint16_t *q, const int64_t *q_stride,
         J->cu_q = cu_seqlens_q; J->cu_k = cu_seqlens_k;
         J->B = B; J->Hq = Hq; J->Hkv = Hkv; J->Dk = Dk; J->Dv = Dv; J->causal = causal;
         J->total_q = cu_seqlens_q[B]; J->max_k = max_k; J->scale = scale;
-        J->rows = rows; J->n_rows = n_rows; J->out = out; J->lse = lse;
+        J->rows = rows; J->n_rows = n_rows; J->out = out; J->lse = lse; J->absv = absv;
         J->begin = n_rows * w / n_threads; J->end = n_rows * (w + 1) / n_threads;
         pthread_create(&tid[w], NULL, prefill_worker, J);
     }

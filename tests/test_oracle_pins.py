@@ -816,3 +816,73 @@ def test_append_then_decode_matches_sdpa_with_the_new_keys():
         rows = slice(b * wl.q_len * wl.num_q_heads, (b + 1) * wl.q_len * wl.num_q_heads)
         np.testing.assert_allclose(out[rows], ref_o, atol=1e-12)
         np.testing.assert_allclose(lse[rows], ref_l, atol=1e-12)
+
+
+# ------------------------------------------- the error-bound scale (absv)
+# absv = sum_j p_j |v_j| / l: the same softmax weights applied to |v|.  The
+# GPU tests scale their bound for rounding P to BF16 ("Writing Page Attention
+# with PyPTO", section 6.3) by it, so it is pinned like the output itself.
+
+@pytest.mark.parametrize("q_len,lens,ps,mapping", [
+    (1, (5, 1, 13), 4, "random"),
+    (3, (7, 9, 12), 4, "reverse"),
+])
+def test_absv_matches_sdpa_on_absolute_values(q_len, lens, ps, mapping):
+    wl, inp = tiny_decode(q_len=q_len, lens=lens, ps=ps, mapping=mapping)
+    out, lse, absv = oracle.paged_decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"],
+                                         inp["seq_lens"], inp["scale"], with_absv=True)
+    inp_abs = dict(inp, v_cache=inp["v_cache"].abs())
+    rows_per_b = q_len * wl.num_q_heads
+    for b in range(wl.batch):
+        ref_o, _ = sdpa_decode_reference(inp_abs, b)
+        np.testing.assert_allclose(absv[b * rows_per_b:(b + 1) * rows_per_b], ref_o, rtol=0, atol=1e-12)
+    # Asking for absv changes nothing else.
+    o2, l2 = oracle.paged_decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"],
+                                 inp["seq_lens"], inp["scale"])
+    assert np.array_equal(out, o2) and np.array_equal(lse, l2)
+    assert np.all(absv >= np.abs(out) - 1e-12)                  # |sum p v| <= sum p |v|
+
+
+def test_absv_closed_forms():
+    """Non-negative values: absv = out; one key: absv = |that value row|; a
+    row with no key: 0."""
+    wl, inp = tiny_decode(lens=(5, 1, 0))
+    inp_pos = dict(inp, v_cache=inp["v_cache"].abs())
+    out, _, absv = oracle.paged_decode(inp_pos["q"], inp_pos["k_cache"], inp_pos["v_cache"], inp["block_table"],
+                                       inp["seq_lens"], inp["scale"], with_absv=True)
+    fin = np.isfinite(out)
+    np.testing.assert_allclose(absv[fin], out[fin], rtol=0, atol=1e-12)
+    _, _, absv = oracle.paged_decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"],
+                                     inp["seq_lens"], inp["scale"], with_absv=True)
+    k, v = dense_kv(inp, 1)                                     # batch row 1 holds one key
+    hq, hkv = wl.num_q_heads, wl.num_kv_heads
+    for h in range(hq):
+        np.testing.assert_array_equal(absv[hq + h], v[0, h // (hq // hkv)].double().abs().numpy())
+    assert np.all(absv[2 * hq:] == 0.0)
+
+
+def test_absv_prefill_and_fp8_match_sdpa_on_absolute_values():
+    wl = PrefillWorkload("p", num_seqs=2, num_q_heads=4, num_kv_heads=2, head_dim_qk=16,
+                         head_dim_v=8, causal=True, scale=0.3, value_seed=5)
+    inp = make_prefill_inputs(wl, "cpu", [5, 9], [7, 9])
+    _, _, absv = oracle.varlen_prefill(inp["q"], inp["k"], inp["v"], inp["cu_seqlens_q"],
+                                       inp["cu_seqlens_k"], True, wl.scale, with_absv=True)
+    q = inp["q"][:5].double().transpose(0, 1)
+    k = inp["k"][:7].double().repeat_interleave(2, dim=1).transpose(0, 1)
+    v = inp["v"][:7].double().abs().repeat_interleave(2, dim=1).transpose(0, 1)
+    mask = torch.ones(5, 7, dtype=torch.bool).tril(diagonal=2)
+    ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=wl.scale)
+    np.testing.assert_allclose(absv[:20], ref.transpose(0, 1).reshape(20, -1).numpy(), rtol=0, atol=1e-12)
+
+    wl8, inp8 = tiny_decode_fp8()
+    _, _, absv8 = oracle.paged_decode(inp8["q"], inp8["k_cache"], inp8["v_cache"], inp8["block_table"],
+                                      inp8["seq_lens"], inp8["scale"], k_scale=inp8["k_scale"],
+                                      v_scale=inp8["v_scale"], with_absv=True)
+    hq, hkv = wl8.num_q_heads, wl8.num_kv_heads
+    for b in range(wl8.batch):
+        kk = _dequantized_dense(inp8, b, "k_cache", inp8["k_scale"]).repeat_interleave(hq // hkv, dim=1)
+        vv = _dequantized_dense(inp8, b, "v_cache", inp8["v_scale"]).abs().repeat_interleave(hq // hkv, dim=1)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            inp8["q"][b].double().transpose(0, 1), kk.transpose(0, 1), vv.transpose(0, 1), scale=inp8["scale"])
+        np.testing.assert_allclose(absv8[b * hq:(b + 1) * hq], ref.transpose(0, 1).reshape(hq, -1).numpy(),
+                                   rtol=0, atol=1e-12)
