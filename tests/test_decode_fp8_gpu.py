@@ -17,7 +17,7 @@ import torch
 
 import oracle
 from ragged_softmax_attention_gb300.workloads import WORKLOADS, DecodeWorkload, make_decode_inputs
-from tests.gpu_common import built_library, compare, to_device
+from tests.gpu_common import BF16_UNIT, FP16_UNIT, built_library, compare, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -40,8 +40,8 @@ def run_case(fw, wl, chunk=0, mapping="random", k_scale=None, v_scale=None):
     inp = make_decode_inputs(wl, "cpu", mapping=mapping)
     ks = inp["k_scale"] if k_scale is None else k_scale
     vs = inp["v_scale"] if v_scale is None else v_scale
-    ref_o, ref_l = oracle.paged_decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"],
-                                       inp["seq_lens"], inp["scale"], k_scale=ks, v_scale=vs)
+    ref_o, ref_l, ref_a = oracle.paged_decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"],
+                                              inp["seq_lens"], inp["scale"], k_scale=ks, v_scale=vs, with_absv=True)
     d = to_device(inp)
     fw.set_option(fw.FW_OPT_DECODE_CHUNK_TOKENS, chunk)
     try:
@@ -51,7 +51,7 @@ def run_case(fw, wl, chunk=0, mapping="random", k_scale=None, v_scale=None):
     finally:
         fw.set_option(fw.FW_OPT_DECODE_CHUNK_TOKENS, 0)
     assert fw.device_status() == 0
-    return compare(out, lse, ref_o, ref_l, what=f"fp8 {wl.seq_lens} q_len={wl.q_len} ps={wl.page_size}")
+    return compare(out, lse, ref_o, ref_l, what=f"fp8 {wl.seq_lens} q_len={wl.q_len} ps={wl.page_size}", absv=ref_a, p_unit=FP16_UNIT)
 
 
 def test_tiny_fp8_decode(fw):
@@ -132,9 +132,9 @@ def test_qwen3_14b_fp8_decode_full_size_sampled_rows(fw):
         v = d["v_cache"].view(torch.uint8)[pages.cuda()].cpu().view(torch.float8_e4m3fn)
         sub_bt = torch.arange(npg, dtype=torch.int32).unsqueeze(0)
         heads = torch.randperm(wl.num_q_heads, generator=g)[:4].tolist()
-        o_ref, l_ref = oracle.paged_decode(d["q"][b:b + 1].cpu(), k, v, sub_bt, lens[b:b + 1], wl.scale,
-                                           rows=heads, k_scale=d["k_scale"], v_scale=d["v_scale"])
-        compare(out[b, 0, heads], lse[b, 0, heads], o_ref, l_ref, f"b{b}")
+        o_ref, l_ref, a_ref = oracle.paged_decode(d["q"][b:b + 1].cpu(), k, v, sub_bt, lens[b:b + 1], wl.scale,
+                                                  rows=heads, k_scale=d["k_scale"], v_scale=d["v_scale"], with_absv=True)
+        compare(out[b, 0, heads], lse[b, 0, heads], o_ref, l_ref, f"b{b}", absv=a_ref, p_unit=FP16_UNIT)
 
 
 @pytest.mark.parametrize("chunk", [0, 512])

@@ -31,8 +31,8 @@ def fw():
 
 def run_case(fw, wl, lens=None, mapping="random", chunk=0, check_status=True):
     inp = make_decode_inputs(wl, "cpu", seq_lens=lens, mapping=mapping)
-    ref_o, ref_l = oracle.paged_decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"],
-                                       inp["seq_lens"], inp["scale"])
+    ref_o, ref_l, ref_a = oracle.paged_decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"],
+                                              inp["seq_lens"], inp["scale"], with_absv=True)
     d = to_device(inp)
     fw.set_option(fw.FW_OPT_DECODE_CHUNK_TOKENS, chunk)
     try:
@@ -43,7 +43,7 @@ def run_case(fw, wl, lens=None, mapping="random", chunk=0, check_status=True):
         fw.set_option(fw.FW_OPT_DECODE_CHUNK_TOKENS, 0)
     if check_status:
         assert fw.device_status() == 0
-    return compare(out, lse, ref_o, ref_l, what=wl.name), out, lse
+    return compare(out, lse, ref_o, ref_l, what=wl.name, absv=ref_a), out, lse
 
 
 def wl_decode(batch=3, q_len=1, hq=8, hkv=2, d=128, ps=16, lens=(37, 200, 5), seed=11, name="case"):
@@ -135,13 +135,13 @@ def test_output_guard_zones(fw):
 def test_lse_optional(fw):
     wl = wl_decode(batch=2, lens=(77, 5))
     inp = make_decode_inputs(wl, "cpu")
-    ref_o, _ = oracle.paged_decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"],
-                                   inp["seq_lens"], inp["scale"])
+    ref_o, _, ref_a = oracle.paged_decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"],
+                                          inp["seq_lens"], inp["scale"], with_absv=True)
     d = to_device(inp)
     out, lse = fw.paged_decode(d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["seq_lens"], d["scale"],
                                return_lse=False)
     assert lse is None
-    compare(out, None, ref_o, None, "no-lse")
+    compare(out, None, ref_o, None, "no-lse", absv=ref_a)
 
 
 def test_invalid_arguments_launch_nothing(fw):
@@ -179,9 +179,9 @@ def test_qwen3_14b_decode_full_size_sampled_rows(fw):
         v = d["v_cache"][pages.cuda()].cpu()
         sub_bt = torch.arange(npg, dtype=torch.int32).unsqueeze(0)
         heads = torch.randperm(wl.num_q_heads, generator=g)[:4].tolist()
-        o_ref, l_ref = oracle.paged_decode(d["q"][b:b + 1].cpu(), k, v, sub_bt, lens[b:b + 1], wl.scale,
-                                           rows=heads)
-        compare(out[b, 0, heads], lse[b, 0, heads], o_ref, l_ref, f"b{b}")
+        o_ref, l_ref, a_ref = oracle.paged_decode(d["q"][b:b + 1].cpu(), k, v, sub_bt, lens[b:b + 1], wl.scale,
+                                                  rows=heads, with_absv=True)
+        compare(out[b, 0, heads], lse[b, 0, heads], o_ref, l_ref, f"b{b}", absv=a_ref)
 
 
 @pytest.mark.parametrize("chunk", [0, 512])

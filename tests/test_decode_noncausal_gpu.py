@@ -16,7 +16,7 @@ import torch
 
 import oracle
 from ragged_softmax_attention_gb300.workloads import DecodeWorkload, make_decode_inputs
-from tests.gpu_common import built_library, compare, to_device
+from tests.gpu_common import BF16_UNIT, FP16_UNIT, built_library, compare, to_device
 from tests.test_decode_window_gpu import evict_before_window
 
 pytestmark = pytest.mark.gpu
@@ -43,9 +43,9 @@ def run_case(fw, wl, causal=False, window=-1, chunk=0):
     if window >= 0:
         inp = evict_before_window(inp, wl, window)
     ks, vs = (inp["k_scale"], inp["v_scale"]) if wl.kv_fp8 else (1.0, 1.0)
-    ref_o, ref_l = oracle.paged_decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"],
-                                       inp["seq_lens"], inp["scale"], k_scale=ks, v_scale=vs,
-                                       window_left=window, causal=causal)
+    ref_o, ref_l, ref_a = oracle.paged_decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"],
+                                              inp["seq_lens"], inp["scale"], k_scale=ks, v_scale=vs,
+                                              window_left=window, causal=causal, with_absv=True)
     d = to_device(inp)
     if wl.latent:
         d["v_cache"] = d["k_cache"][..., :wl.head_dim_v]
@@ -57,7 +57,8 @@ def run_case(fw, wl, causal=False, window=-1, chunk=0):
     finally:
         fw.set_option(fw.FW_OPT_DECODE_CHUNK_TOKENS, 0)
     assert fw.device_status() == 0
-    compare(out, lse, ref_o, ref_l, what=f"non-causal={not causal} window={window} {wl.seq_lens} q_len={wl.q_len}")
+    compare(out, lse, ref_o, ref_l, what=f"non-causal={not causal} window={window} {wl.seq_lens} q_len={wl.q_len}", absv=ref_a,
+            p_unit=FP16_UNIT if wl.kv_fp8 else BF16_UNIT)
     return d, out, lse
 
 

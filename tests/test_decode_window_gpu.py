@@ -17,7 +17,7 @@ import torch
 
 import oracle
 from ragged_softmax_attention_gb300.workloads import WORKLOADS, DecodeWorkload, make_decode_inputs
-from tests.gpu_common import built_library, compare, to_device
+from tests.gpu_common import BF16_UNIT, FP16_UNIT, built_library, compare, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -64,8 +64,8 @@ def run_case(fw, wl, window, chunk=0, evict=False, mapping="random"):
         inp = evict_before_window(inp, wl, window)
     ks = inp.get("k_scale", 1.0) if wl.kv_fp8 else 1.0
     vs = inp.get("v_scale", 1.0) if wl.kv_fp8 else 1.0
-    ref_o, ref_l = oracle.paged_decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"],
-                                       inp["seq_lens"], inp["scale"], k_scale=ks, v_scale=vs, window_left=window)
+    ref_o, ref_l, ref_a = oracle.paged_decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"],
+                                              inp["seq_lens"], inp["scale"], k_scale=ks, v_scale=vs, window_left=window, with_absv=True)
     d = to_device(inp)
     fw.set_option(fw.FW_OPT_DECODE_CHUNK_TOKENS, chunk)
     try:
@@ -76,7 +76,8 @@ def run_case(fw, wl, window, chunk=0, evict=False, mapping="random"):
         fw.set_option(fw.FW_OPT_DECODE_CHUNK_TOKENS, 0)
     assert fw.device_status() == 0
     return compare(out, lse, ref_o, ref_l,
-                   what=f"window {window} fp8={wl.kv_fp8} {wl.seq_lens} q_len={wl.q_len} ps={wl.page_size}")
+                   what=f"window {window} fp8={wl.kv_fp8} {wl.seq_lens} q_len={wl.q_len} ps={wl.page_size}", absv=ref_a,
+                   p_unit=FP16_UNIT if wl.kv_fp8 else BF16_UNIT)
 
 
 @pytest.mark.parametrize("fp8", [False, True])
@@ -166,9 +167,10 @@ def test_qwen3_14b_window_4096_full_size_sampled_rows(fw, fp8):
             v = d["v_cache"][pages.cuda()].cpu()
         sub_bt = torch.arange(npg, dtype=torch.int32).unsqueeze(0)
         heads = torch.randperm(wl.num_q_heads, generator=g)[:4].tolist()
-        o_ref, l_ref = oracle.paged_decode(d["q"][b:b + 1].cpu(), k, v, sub_bt, lens[b:b + 1], wl.scale,
-                                           rows=heads, k_scale=ks, v_scale=vs, window_left=W)
-        compare(out[b, 0, heads], lse[b, 0, heads], o_ref, l_ref, f"b{b}")
+        o_ref, l_ref, a_ref = oracle.paged_decode(d["q"][b:b + 1].cpu(), k, v, sub_bt, lens[b:b + 1], wl.scale,
+                                                  rows=heads, k_scale=ks, v_scale=vs, window_left=W, with_absv=True)
+        compare(out[b, 0, heads], lse[b, 0, heads], o_ref, l_ref, f"b{b}", absv=a_ref,
+                p_unit=FP16_UNIT if fp8 else BF16_UNIT)
 
 
 @pytest.mark.parametrize("fp8", [False, True])

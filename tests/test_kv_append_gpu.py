@@ -17,7 +17,7 @@ import torch
 
 import oracle
 from ragged_softmax_attention_gb300.workloads import WORKLOADS, DecodeWorkload, make_decode_inputs
-from tests.gpu_common import built_library, compare, to_device
+from tests.gpu_common import BF16_UNIT, FP16_UNIT, built_library, compare, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -178,8 +178,8 @@ def test_fused_append_then_decode(fw, fp8, window, q_len):
     ks, vs = (0.02, 0.02) if fp8 else (1.0, 1.0)
     ref_k, ref_v = oracle.kv_append(k_new, v_new, slots, base, kp, vp, k_scale=ks, v_scale=vs)
     P = inp["k_cache"].shape[0]
-    ref_o, ref_l = oracle.paged_decode(inp["q"], ref_k[P:], ref_v[P:], inp["block_table"], inp["seq_lens"],
-                                       inp["scale"], k_scale=ks, v_scale=vs, window_left=window)
+    ref_o, ref_l, ref_a = oracle.paged_decode(inp["q"], ref_k[P:], ref_v[P:], inp["block_table"], inp["seq_lens"],
+                                              inp["scale"], k_scale=ks, v_scale=vs, window_left=window, with_absv=True)
     dk, dv = kp.cuda(), vp.cuda()
     d = to_device(inp)
     out, lse = fw.paged_decode_append(d["q"], k_new.cuda(), v_new.cuda(), slots.cuda(), base, dk, dv,
@@ -189,7 +189,8 @@ def test_fused_append_then_decode(fw, fp8, window, q_len):
     assert fw.device_status() == 0
     assert torch.equal(raw(dk.cpu()), raw(ref_k))            # layer 0 untouched, layer 1 appended
     assert torch.equal(raw(dv.cpu()), raw(ref_v))
-    compare(out, lse, ref_o, ref_l, what=f"fused append fp8={fp8} window={window} q_len={q_len}")
+    compare(out, lse, ref_o, ref_l, what=f"fused append fp8={fp8} window={window} q_len={q_len}", absv=ref_a,
+            p_unit=FP16_UNIT if fp8 else BF16_UNIT)
 
 
 def test_fused_append_argument_checks_launch_nothing(fw):
@@ -239,5 +240,5 @@ def test_fused_append_full_size_qwen3(fw):
         v = d["v_cache"][pages.cuda()].cpu()
         sub_bt = torch.arange(npg, dtype=torch.int32).unsqueeze(0)
         heads = torch.randperm(wl.num_q_heads, generator=g)[:4].tolist()
-        o_ref, l_ref = oracle.paged_decode(d["q"][b:b + 1].cpu(), k, v, sub_bt, lens[b:b + 1], wl.scale, rows=heads)
-        compare(out[b, 0, heads], lse[b, 0, heads], o_ref, l_ref, f"b{b}")
+        o_ref, l_ref, a_ref = oracle.paged_decode(d["q"][b:b + 1].cpu(), k, v, sub_bt, lens[b:b + 1], wl.scale, rows=heads, with_absv=True)
+        compare(out[b, 0, heads], lse[b, 0, heads], o_ref, l_ref, f"b{b}", absv=a_ref)

@@ -42,8 +42,8 @@ def wl_latent(lens, q_len=4, hq=128, hkv=1, ps=64, scale=0.07216882, seed=21, al
 
 def run_case(fw, wl, chunk=0, mapping="random"):
     inp = make_decode_inputs(wl, "cpu", mapping=mapping)
-    ref_o, ref_l = oracle.paged_decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"],
-                                       inp["seq_lens"], inp["scale"])
+    ref_o, ref_l, ref_a = oracle.paged_decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"],
+                                              inp["seq_lens"], inp["scale"], with_absv=True)
     d = to_device(inp)
     if wl.latent:
         d["v_cache"] = d["k_cache"][..., :512]
@@ -55,7 +55,7 @@ def run_case(fw, wl, chunk=0, mapping="random"):
     finally:
         fw.set_option(fw.FW_OPT_DECODE_CHUNK_TOKENS, 0)
     assert fw.device_status() == 0
-    return compare(out, lse, ref_o, ref_l, what=f"latent {wl.seq_lens} q_len={wl.q_len} ps={wl.page_size}")
+    return compare(out, lse, ref_o, ref_l, what=f"latent {wl.seq_lens} q_len={wl.q_len} ps={wl.page_size}", absv=ref_a)
 
 
 def test_ragged_lengths_around_tiles_and_pages(fw):
@@ -98,7 +98,9 @@ def test_empty_rows(fw):
 def test_scales_that_move_the_anchor(fw, scale):
     """Scores spread over hundreds of log2 units: later tiles rise far above
     the first tile's maxima, so anchors move and O^T is rescaled in TMEM."""
+    fw.read_counters()                                   # reset
     run_case(fw, wl_latent([2000, 1300], q_len=2, scale=scale, seed=23))
+    assert fw.read_counters()["latent_rescales"] > 0, "no anchor moved"
 
 
 @pytest.mark.parametrize("hq,q_len", [(16, 4), (16, 1), (96, 4), (64, 2), (48, 3), (32, 4)])
@@ -122,8 +124,8 @@ def run_window_case(fw, wl, window, chunk=0):
     this layout); pages wholly before a row's window are evicted (NaN, table
     entry -1), so touching one shows up as NaN or a bad-page status."""
     inp = evict_before_window(make_decode_inputs(wl, "cpu"), wl, window)
-    ref_o, ref_l = oracle.paged_decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"],
-                                       inp["seq_lens"], inp["scale"], window_left=window)
+    ref_o, ref_l, ref_a = oracle.paged_decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_table"],
+                                              inp["seq_lens"], inp["scale"], window_left=window, with_absv=True)
     d = to_device(inp)
     if wl.latent:
         d["v_cache"] = d["k_cache"][..., :512]
@@ -135,7 +137,7 @@ def run_window_case(fw, wl, window, chunk=0):
     finally:
         fw.set_option(fw.FW_OPT_DECODE_CHUNK_TOKENS, 0)
     assert fw.device_status() == 0
-    return compare(out, lse, ref_o, ref_l, what=f"latent window {window} {wl.seq_lens} q_len={wl.q_len} H={wl.num_q_heads}")
+    return compare(out, lse, ref_o, ref_l, what=f"latent window {window} {wl.seq_lens} q_len={wl.q_len} H={wl.num_q_heads}", absv=ref_a)
 
 
 @pytest.mark.parametrize("window", [0, 1, 100, 127, 128, 129, 300, 5000])
@@ -184,9 +186,9 @@ def test_latent_workload_full_size_sampled_rows(fw):
         t = g.integers(0, wl.q_len, size=16)
         h = g.choice(wl.num_q_heads, size=16, replace=False)
         rows = (t * wl.num_q_heads + h).tolist()
-        o_ref, l_ref = oracle.paged_decode(d["q"][b:b + 1].cpu(), k, v, sub_bt, lens[b:b + 1], wl.scale, rows=rows)
+        o_ref, l_ref, a_ref = oracle.paged_decode(d["q"][b:b + 1].cpu(), k, v, sub_bt, lens[b:b + 1], wl.scale, rows=rows, with_absv=True)
         tt, hh = torch.as_tensor(t, device="cuda"), torch.as_tensor(h, device="cuda")
-        compare(out[b, tt, hh], lse[b, tt, hh], o_ref, l_ref, f"b{b}")
+        compare(out[b, tt, hh], lse[b, tt, hh], o_ref, l_ref, f"b{b}", absv=a_ref)
 
 
 def test_invalid_latent_shapes_launch_nothing(fw):

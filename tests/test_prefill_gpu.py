@@ -31,8 +31,8 @@ def wl_prefill(hq=8, hkv=2, d=128, causal=True, seed=31):
 
 def run_case(fw, wl, lq, lk=None, rows=None):
     inp = make_prefill_inputs(wl, "cpu", lq, lk)
-    ref_o, ref_l = oracle.varlen_prefill(inp["q"], inp["k"], inp["v"], inp["cu_seqlens_q"], inp["cu_seqlens_k"],
-                                         wl.causal, wl.scale, rows=rows)
+    ref_o, ref_l, ref_a = oracle.varlen_prefill(inp["q"], inp["k"], inp["v"], inp["cu_seqlens_q"], inp["cu_seqlens_k"],
+                                                wl.causal, wl.scale, rows=rows, with_absv=True)
     d = to_device(inp)
     out, lse = fw.varlen_prefill(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], wl.causal, wl.scale)
     torch.cuda.synchronize()
@@ -41,7 +41,7 @@ def run_case(fw, wl, lq, lk=None, rows=None):
     l_ = lse.reshape(-1)
     if rows is not None:
         o, l_ = o[rows], l_[rows]
-    return compare(o, l_, ref_o, ref_l, what=f"lq={lq} lk={lk}")
+    return compare(o, l_, ref_o, ref_l, what=f"lq={lq} lk={lk}", absv=ref_a)
 
 
 @pytest.mark.parametrize("L", [1, 2, 127, 128, 129, 255, 256, 257, 300, 511, 600])
@@ -89,9 +89,9 @@ def test_output_guard_and_lse_optional(fw):
                       out=out, return_lse=False)
     torch.cuda.synchronize()
     assert torch.all(big[0] == 3.0) and torch.all(big[171] == 3.0)
-    ref_o, _ = oracle.varlen_prefill(inp["q"].cpu(), inp["k"].cpu(), inp["v"].cpu(), inp["cu_seqlens_q"].cpu(),
-                                     inp["cu_seqlens_k"].cpu(), True, wl.scale)
-    compare(out.reshape(-1, 128), None, ref_o, None, "guard")
+    ref_o, _, ref_a = oracle.varlen_prefill(inp["q"].cpu(), inp["k"].cpu(), inp["v"].cpu(), inp["cu_seqlens_q"].cpu(),
+                                            inp["cu_seqlens_k"].cpu(), True, wl.scale, with_absv=True)
+    compare(out.reshape(-1, 128), None, ref_o, None, "guard", absv=ref_a)
 
 
 def test_invalid_prefill_arguments(fw):
@@ -119,9 +119,9 @@ def test_full_size_workloads_sampled_rows(fw, name):
     assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
     total = d["q"].shape[0] * wl.num_q_heads
     rows = np.sort(np.random.default_rng(9).choice(total, size=512, replace=False))
-    ref_o, ref_l = oracle.varlen_prefill(d["q"].cpu(), d["k"].cpu(), d["v"].cpu(), d["cu_seqlens_q"].cpu(),
-                                         d["cu_seqlens_k"].cpu(), wl.causal, wl.scale, rows=rows)
-    compare(out.reshape(-1, out.shape[-1])[rows], lse.reshape(-1)[rows], ref_o, ref_l, name)
+    ref_o, ref_l, ref_a = oracle.varlen_prefill(d["q"].cpu(), d["k"].cpu(), d["v"].cpu(), d["cu_seqlens_q"].cpu(),
+                                                d["cu_seqlens_k"].cpu(), wl.causal, wl.scale, rows=rows, with_absv=True)
+    compare(out.reshape(-1, out.shape[-1])[rows], lse.reshape(-1)[rows], ref_o, ref_l, name, absv=ref_a)
 
 
 def test_no_keys_at_all(fw):
@@ -129,15 +129,22 @@ def test_no_keys_at_all(fw):
     run_case(fw, wl_prefill(hq=4, hkv=2), [5, 130], [0, 0])
 
 
-@pytest.mark.parametrize("scale", [1.0, 2.0, -0.2])
+@pytest.mark.parametrize("scale", [1.0, 2.0, 4.0, -0.2])
 @pytest.mark.parametrize("d", [128, 256])
 def test_scale_extremes_exercise_anchor_replay(fw, scale, d):
     """Large scales spread scores over ~100 log2 units, so later tiles outgrow the
     first tile's anchor and the running-sum check replays them (Flywheel appendix
-    A); a negative scale exercises the sign-aware masking."""
+    A); a negative scale exercises the sign-aware masking.  The device counter
+    shows the replays ran: a float64 walk of the same check over these inputs
+    replays 234-1117 (row, tile) steps at scales 2 and 4 (5 and 63 at scale 1,
+    none at -0.2)."""
     wl = PrefillWorkload("s", num_seqs=0, num_q_heads=4, num_kv_heads=2, head_dim_qk=d, head_dim_v=d,
                          causal=True, scale=scale, value_seed=41)
+    fw.read_counters()                                   # reset
     run_case(fw, wl, [300, 700, 129])
+    replays = fw.read_counters()["prefill_replays"]
+    if abs(scale) >= 2.0:
+        assert replays > 0, "the static-anchor check never replayed a tile"
 
 
 @pytest.fixture
@@ -181,9 +188,9 @@ def test_online_mode_full_size_sampled_rows(online, name):
     assert online.device_status() == 0
     total = d["q"].shape[0] * wl.num_q_heads
     rows = np.sort(np.random.default_rng(10).choice(total, size=512, replace=False))
-    ref_o, ref_l = oracle.varlen_prefill(d["q"].cpu(), d["k"].cpu(), d["v"].cpu(), d["cu_seqlens_q"].cpu(),
-                                         d["cu_seqlens_k"].cpu(), wl.causal, wl.scale, rows=rows)
-    compare(out.reshape(-1, out.shape[-1])[rows], lse.reshape(-1)[rows], ref_o, ref_l, name + " online")
+    ref_o, ref_l, ref_a = oracle.varlen_prefill(d["q"].cpu(), d["k"].cpu(), d["v"].cpu(), d["cu_seqlens_q"].cpu(),
+                                                d["cu_seqlens_k"].cpu(), wl.causal, wl.scale, rows=rows, with_absv=True)
+    compare(out.reshape(-1, out.shape[-1])[rows], lse.reshape(-1)[rows], ref_o, ref_l, name + " online", absv=ref_a)
 
 
 @pytest.mark.parametrize("name", ["varlen_gqa_prefill", "dense_causal_mha_hd256"])
