@@ -125,7 +125,11 @@ fw_status_t fw_paged_decode(const fw_tensor_t *q, const fw_tensor_t *k_cache,
  * 64 MiB array in the library's device image, held by every GPU that loads
  * the library until the process exits.  Shapes whose scratch
  * (fw_decode_plan_t.workspace_bytes) exceeds 64 MiB return FW_ERR_WORKSPACE
- * and launch nothing.
+ * and launch nothing.  That size follows the block table's width
+ * (max_pages x page_size keys per row, the longest row the call could see),
+ * not the seq_lens values, which stay on the device: a caller with short
+ * rows in a wide table can pass a narrower view of the table (fewer
+ * columns, same row stride) to fit.
  *
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current); make that first call
@@ -325,6 +329,26 @@ fw_status_t fw_set_workspace(void *ptr, size_t bytes, fw_stream_t stream);
  */
 fw_status_t fw_get_device_status(fw_stream_t stream, int32_t *code);
 
+/*
+ * Device event counters, accumulated by every call on the current device
+ * since the last read.  Synchronises `stream`, copies the first n (1..4)
+ * counters into values[0..n-1] and resets all of them to zero.
+ *
+ *   FW_COUNTER_PREFILL_REPLAYS  (query row, KV tile) steps of the prefill
+ *       static-anchor softmax whose running-sum check failed, so the tile was
+ *       replayed with the rescaling form ("Flywheel Attention", section 3.1:
+ *       the check raises a flag and the block is recomputed, appendix A)
+ *   FW_COUNTER_LATENT_RESCALES  (query row, key step) steps of the latent-head
+ *       decode whose anchor moved because a score rose more than 64 log2 units
+ *       above it
+ */
+typedef enum {
+    FW_COUNTER_PREFILL_REPLAYS = 0,
+    FW_COUNTER_LATENT_RESCALES = 1
+} fw_counter_t;
+
+fw_status_t fw_read_counters(fw_stream_t stream, int64_t *values, int32_t n);
+
 /* Message for the last failing call on this host thread ("" if none). */
 const char *fw_last_error(void);
 
@@ -334,11 +358,17 @@ typedef enum {
     FW_OPT_WAIT_TIMEOUT_MS = 1,     /* device wait limit before giving up (default 2000) */
     FW_OPT_KERNEL_TIMING = 2,       /* 1: record CUDA events around each attention kernel */
     FW_OPT_MAX_CTAS = 3,            /* cap on persistent CTAs (0 = one per SM) */
-    FW_OPT_PREFILL_SOFTMAX = 4      /* prefill softmax: 0 = static anchor with a check and replay
+    FW_OPT_PREFILL_SOFTMAX = 4,     /* prefill softmax: 0 = static anchor with a check and replay
                                        ("Flywheel Attention", section 3.1, default); 1 = online
                                        softmax with a conditional rescale (the base moves when a
                                        row max rises more than 8 log2 units).  Same result up to
                                        rounding; kept for comparison. */
+    FW_OPT_TEST_STALL = 5           /* test hook, default 0.  1: the grouped-query decode kernel's
+                                       copy warp first waits on a barrier that nothing completes,
+                                       so that wait runs out after FW_OPT_WAIT_TIMEOUT_MS: the call
+                                       records FW_ERR_DEVICE_TIMEOUT (read by fw_get_device_status)
+                                       and its outputs are not valid.  Nothing is copied or
+                                       multiplied before the wait, so no work is left in flight. */
 } fw_option_t;
 
 fw_status_t fw_set_option(int32_t option, int64_t value);

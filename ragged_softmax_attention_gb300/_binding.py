@@ -21,7 +21,8 @@ STATUS_NAMES = {0: "FW_OK", 1: "FW_ERR_INVALID_ARG", 2: "FW_ERR_UNSUPPORTED", 3:
                 4: "FW_ERR_CUDA", 5: "FW_ERR_DEVICE_TIMEOUT"}
 FW_BF16, FW_F32, FW_I32, FW_FP8_E4M3 = 0, 1, 2, 3
 FW_OPT_DECODE_CHUNK_TOKENS, FW_OPT_WAIT_TIMEOUT_MS, FW_OPT_KERNEL_TIMING, FW_OPT_MAX_CTAS = 0, 1, 2, 3
-FW_OPT_PREFILL_SOFTMAX = 4
+FW_OPT_PREFILL_SOFTMAX, FW_OPT_TEST_STALL = 4, 5
+FW_COUNTER_PREFILL_REPLAYS, FW_COUNTER_LATENT_RESCALES = 0, 1
 
 _DTYPES = {torch.bfloat16: FW_BF16, torch.float32: FW_F32, torch.int32: FW_I32,
            torch.float8_e4m3fn: FW_FP8_E4M3}
@@ -94,6 +95,8 @@ def load_library(path: Optional[str] = None):
     lib.fw_set_option.argtypes = [ctypes.c_int32, ctypes.c_int64]
     lib.fw_kernel_timing_read.restype = S
     lib.fw_kernel_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64)]
+    lib.fw_read_counters.restype = S
+    lib.fw_read_counters.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int64), ctypes.c_int32]
     lib.fw_launch_count.restype = ctypes.c_int64
     lib.fw_launch_count.argtypes = []
     lib.fw_plan_decode.restype = S
@@ -313,6 +316,14 @@ def kernel_timing_read():
     n = ctypes.c_int64(0)
     _check(lib.fw_kernel_timing_read(ctypes.byref(ms), ctypes.byref(n)))
     return ms.value, n.value
+
+
+def read_counters(stream=None) -> dict:
+    """Device event counters since the last read (which resets them):
+    {"prefill_replays": ..., "latent_rescales": ...}."""
+    vals = (ctypes.c_int64 * 2)()
+    _check(load_library().fw_read_counters(_stream_handle(stream), vals, 2))
+    return {"prefill_replays": vals[FW_COUNTER_PREFILL_REPLAYS], "latent_rescales": vals[FW_COUNTER_LATENT_RESCALES]}
 
 
 def launch_count() -> int:

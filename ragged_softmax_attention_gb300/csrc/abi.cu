@@ -19,6 +19,7 @@
 namespace {
 
 __device__ int g_fw_status = 0;
+__device__ unsigned long long g_fw_counters[fw::kNumCounters];
 
 constexpr int kMaxDevices = 64;
 
@@ -41,6 +42,7 @@ struct DeviceState {
     bool init = false;
     int num_sms = 0;
     int *status = nullptr;          // device address of g_fw_status
+    unsigned long long *counters = nullptr;  // device address of g_fw_counters
     void *ws = nullptr;             // internal workspace
     size_t ws_bytes = 0;
     void *user_ws = nullptr;        // caller workspace
@@ -56,6 +58,7 @@ int64_t g_opt_timeout_ms = 2000;
 int64_t g_opt_timing = 0;
 int64_t g_opt_max_ctas = 0;
 int64_t g_opt_prefill_online = 0;
+int64_t g_opt_test_stall = 0;
 
 struct TimedLaunch { cudaEvent_t a, b; };
 std::vector<TimedLaunch> g_timed;      // pending event pairs
@@ -89,6 +92,8 @@ fw_status_t device_state(DeviceState **out) {
                         dev, major, minor);
         e = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.status), g_fw_status);
         if (e != cudaSuccess) return fail(FW_ERR_CUDA, "status word address: %s", cudaGetErrorString(e));
+        e = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.counters), g_fw_counters);
+        if (e != cudaSuccess) return fail(FW_ERR_CUDA, "counter address: %s", cudaGetErrorString(e));
         d.init = true;
     }
     *out = &d;
@@ -317,6 +322,7 @@ fw_status_t fw_set_option(int32_t option, int64_t value) {
         case FW_OPT_PREFILL_SOFTMAX:
             if (value != 0 && value != 1) return fail(FW_ERR_INVALID_ARG, "prefill softmax mode must be 0 or 1");
             g_opt_prefill_online = value; return ok();
+        case FW_OPT_TEST_STALL: g_opt_test_stall = value ? 1 : 0; return ok();
         default: return fail(FW_ERR_INVALID_ARG, "unknown option %d", option);
     }
 }
@@ -378,6 +384,23 @@ fw_status_t fw_get_device_status(fw_stream_t stream, int32_t *code) {
     const int zero = 0;
     cudaMemcpy(d->status, &zero, sizeof zero, cudaMemcpyHostToDevice);
     *code = v;
+    return ok();
+}
+
+fw_status_t fw_read_counters(fw_stream_t stream, int64_t *values, int32_t n) {
+    if (!values || n < 1 || n > fw::kNumCounters) return fail(FW_ERR_INVALID_ARG, "need 1 to %d counters", fw::kNumCounters);
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState *d = nullptr;
+    if (fw_status_t s = device_state(&d)) return s;
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(FW_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
+    unsigned long long v[fw::kNumCounters] = {};
+    e = cudaMemcpy(v, d->counters, sizeof v, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail(FW_ERR_CUDA, "counter read: %s", cudaGetErrorString(e));
+    const unsigned long long zero[fw::kNumCounters] = {};
+    e = cudaMemcpy(d->counters, zero, sizeof zero, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return fail(FW_ERR_CUDA, "counter reset: %s", cudaGetErrorString(e));
+    for (int i = 0; i < n; ++i) values[i] = (int64_t)v[i];
     return ok();
 }
 
@@ -651,6 +674,8 @@ static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_
     p.out_scale = kv8 ? v_scale : 1.f;
     p.timeout_ns = (uint64_t)g_opt_timeout_ms * 1000000ull;
     p.status = d->status;
+    p.counters = d->counters;
+    p.test_stall = g_opt_test_stall ? 1 : 0;
 
     CUtensorMap tq, tk, tv;
     if (p.packed) {
@@ -867,6 +892,7 @@ fw_status_t fw_varlen_prefill(const fw_tensor_t *q, const fw_tensor_t *k, const 
     p.scale_log2 = scale * 1.4426950408889634f;
     p.timeout_ns = (uint64_t)g_opt_timeout_ms * 1000000ull;
     p.status = d->status;
+    p.counters = d->counters;
     p.plan = static_cast<int32_t *>(ws);
     p.list = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + plan_bytes);
     p.list_capacity = capacity;

@@ -64,7 +64,7 @@ struct DecodeCfg {
     static constexpr int kOffQ = kOffV + kVStages * kTileBytes;
     static constexpr int kOffP = kOffQ + 2 * kQBytes;
     static constexpr int kOffBar = kOffP + 2 * kPBytes;
-    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + 2 + 2 + 2 + 1 + 1;
+    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + 2 + 2 + 2 + 1 + 1 + 1;
     static constexpr int kOffRedMax = kOffBar + kNumBars * 8;
     static constexpr int kOffRedSum = kOffRedMax + 2 * 4 * NQ * 4;
     static constexpr int kOffMisc = kOffRedSum + 4 * NQ * 4;
@@ -98,6 +98,7 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
     uint64_t *p_free = p_full + 2;
     uint64_t *pv_done = p_free + 2;
     uint64_t *drain = pv_done + 1;
+    uint64_t *never = drain + 1;                   // test hook: no thread ever arrives on it
     float *red_max = reinterpret_cast<float *>(smem + C::kOffRedMax);   // [2][4][NQ]
     float *red_sum = reinterpret_cast<float *>(smem + C::kOffRedSum);   // [4][NQ]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
@@ -116,6 +117,7 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
         }
         mbar_init(pv_done, 1);
         mbar_init(drain, 1);
+        mbar_init(never, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -140,6 +142,12 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
         const int box_rows = p.ps < kKvTile ? p.ps : kKvTile;
         const int pages_per_tile = p.ps < kKvTile ? kKvTile / p.ps : 1;
         const uint32_t q_rows = p.head_mode == 0 ? (uint32_t)(p.G * p.tokens_per_unit) : (uint32_t)p.rows;
+        // Test hook for the bounded waits: before anything is copied, wait on
+        // a barrier that nothing completes.  The wait runs out, records
+        // FW_ERR_DEVICE_TIMEOUT and raises the abort flag; the other roles'
+        // waits then return at once and the CTA winds down with no copy or
+        // MMA in flight.
+        if (p.test_stall && !warp_wait(never, 0, wc, lane)) goto producer_done;
         PieceIter it;
         it.init(p);
         Unit x;

@@ -27,6 +27,11 @@ inline cudaError_t launch_after_previous(void (*kernel)(KArgs...), dim3 grid, di
 }
 
 constexpr int kKvTile = 128;          // keys per KV tile (MMA M extent in decode, N in prefill)
+
+// Device event counters (the FW_COUNTER_* indices of the C ABI).
+constexpr int kCounterPrefillReplays = 0;   // (query row, KV tile) steps the static-anchor check replayed
+constexpr int kCounterLatentRescales = 1;   // (query row, key step) steps whose latent anchor moved
+constexpr int kNumCounters = 4;
 constexpr int kSoftmaxStartWarp = 2;  // decode: warps 2..5 run the softmax / epilogue
 
 constexpr int kDecodeMinSpan = 8;     // decode: fewest KV tiles one CTA range holds (auto mode)
@@ -91,6 +96,8 @@ struct DecodeParams {
     float out_scale;                           // v_scale for an FP8 cache, else 1
     uint64_t timeout_ns;
     int *status;                               // device status word
+    unsigned long long *counters;              // device event counters (FW_COUNTER_*)
+    int test_stall;                            // test hook: the producer first waits on a barrier nothing completes
 };
 
 // One varlen prefill launch.  The plan kernel lists the units (sequence,
@@ -107,6 +114,7 @@ struct PrefillParams {
     float scale_log2;
     uint64_t timeout_ns;
     int *status;
+    unsigned long long *counters;              // device event counters (FW_COUNTER_*)
     int32_t *plan;        // [0] = entries, [1] = pairs, [2 .. 2 + B] = pair prefix PP
     int32_t *list;        // entries pair_index * Hq + head, sorted by cost, longest first
     int64_t list_capacity;

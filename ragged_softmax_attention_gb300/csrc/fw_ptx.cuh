@@ -90,16 +90,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
 
 // Bounded wait that ignores the abort flag: used before leaving the CTA, to
 // let copies and MMAs already issued finish touching shared / tensor memory.
+// Its limit is at least kDrainTimeoutNs whatever the wait option says, so a
+// short limit for the other waits never lets a CTA leave (and free its
+// tensor memory) while work it issued is still in flight.
+constexpr uint64_t kDrainTimeoutNs = 2000000000ull;
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity, const WaitCtx &w) {
     const uint32_t a = smem_u32(bar);
+    const uint64_t limit = w.timeout_ns > kDrainTimeoutNs ? w.timeout_ns : kDrainTimeoutNs;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(a, parity)) return true;
-        if ((it & 255u) == 255u && global_timer_ns() - t0 > w.timeout_ns) {
+        if ((it & 255u) == 255u && global_timer_ns() - t0 > limit) {
             record_error(w.status, 5 /* FW_ERR_DEVICE_TIMEOUT */);
             return false;
         }
     }
+}
+
+// Adds n to event counter idx (no-op without a counter array).
+__device__ __forceinline__ void count_events(unsigned long long *counters, int idx, unsigned n) {
+    if (counters && n) atomicAdd(counters + idx, (unsigned long long)n);
 }
 
 // Re-split the registers of a warpgroup (all 4 warps execute it).  The sum

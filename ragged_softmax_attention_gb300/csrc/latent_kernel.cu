@@ -474,14 +474,17 @@ latent_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_consta
                     // move those anchors to this tile's row max and rescale l
                     // and O^T (once the previous PV has landed).
                     row_max_partials(sa, tok, uni, vis);
-                    if (key < kRows) {
+                    if (key < kRows) {                   // whole warps: q4 0-1
                         const float mx = red4(key);
                         float a = 1.f;
-                        if (mx > anchor_s[key] + kAnchorSlack) {
+                        const bool move = mx > anchor_s[key] + kAnchorSlack;
+                        if (move) {
                             a = ex2_approx(anchor_s[key] - mx);
                             anchor_s[key] = mx;
                         }
                         alpha_s[key] = a;
+                        const unsigned moved = __ballot_sync(0xffffffffu, move);
+                        if (lane == 0) count_events(p.counters, kCounterLatentRescales, __popc(moved));
                     }
                     named_bar_sync(1, 128);
 #pragma unroll

@@ -572,14 +572,17 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
                         // and O^T (once the previous PV has landed).
                         const float own = rows_max_own(sa, tok, uni, vis);
                         const uint32_t par2 = exchange_rows(own);
-                        if (tsw < 128) {
+                        if (tsw < 128) {                 // whole warps: sw 0-3
                             const float mx = fmaxf(own, xr[par2 * 128 + tsw]);
                             float a = 1.f;
-                            if (mx > anchor_s[tsw] + kAnchorSlack) {
+                            const bool move = mx > anchor_s[tsw] + kAnchorSlack;
+                            if (move) {
                                 a = ex2_approx(anchor_s[tsw] - mx);
                                 anchor_s[tsw] = mx;
                             }
                             alpha_s[tsw] = a;
+                            const unsigned moved = __ballot_sync(0xffffffffu, move);
+                            if (rank == 0 && lane == 0) count_events(p.counters, kCounterLatentRescales, __popc(moved));
                         }
                         named_bar_sync(1, 256);
 #pragma unroll

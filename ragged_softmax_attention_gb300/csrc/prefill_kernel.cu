@@ -542,7 +542,9 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                     // to the new max, l and O are rescaled, P is recomputed before
                     // the MMA sees it.
                     const bool over = !(l_sum + tsum <= kAnchorBudget);
-                    if (__any_sync(0xffffffffu, over)) {
+                    const unsigned replay = __ballot_sync(0xffffffffu, over);
+                    if (replay) {
+                        if (lane == 0) count_events(p.counters, kCounterPrefillReplays, __popc(replay));
                         float alpha = 1.f;
                         if (over) {
                             const float m_new = fmaxf(m_ref, row_max());
@@ -945,7 +947,9 @@ varlen_prefill_pair_kernel(const __grid_constant__ PrefillParams p, const __grid
                     // to the new max, l and O are rescaled, P is recomputed before
                     // the MMA sees it.
                     const bool over = !(l_sum + tsum <= kAnchorBudget);
-                    if (__any_sync(0xffffffffu, over)) {
+                    const unsigned replay = __ballot_sync(0xffffffffu, over);
+                    if (replay) {
+                        if (lane == 0) count_events(p.counters, kCounterPrefillReplays, __popc(replay));
                         float alpha = 1.f;
                         if (over) {
                             const float m_new = fmaxf(m_ref, row_max());
