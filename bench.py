@@ -168,6 +168,45 @@ def ncu_traffic(profile_name, sources, units):
     return per_unit * units
 
 
+def timed_calls(torch, stream, call, n):
+    """n back-to-back calls between CUDA events on `stream`, nvidia-smi clocks
+    sampled meanwhile; returns (ms per call, clock summary)."""
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        torch.cuda.synchronize()
+        start.record(stream)
+        for _ in range(n):
+            call()
+        stop.record(stream)
+        torch.cuda.synchronize()
+    return start.elapsed_time(stop) / n, clk.summary()
+
+
+def e2e_calls(torch, device, stream, dev_inputs, call, outputs, n):
+    """End to end through the public call: every step copies the call's inputs
+    from pinned host memory to the device, runs `call(inputs)` (which returns
+    its device outputs) and copies the outputs back to pinned host memory, all
+    inside the timed region.  Returns (ms per step, H2D bytes, D2H bytes)."""
+    host = {k: (v.cpu().pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in dev_inputs.items()}
+    dev = {k: (torch.empty_like(v, device=device) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+    outs_h = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outputs]
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if isinstance(v, torch.Tensor))
+    d2h = sum(o.numel() * o.element_size() for o in outs_h)
+
+    def step():
+        for k, v in host.items():
+            if isinstance(v, torch.Tensor):
+                dev[k].copy_(v, non_blocking=True)
+        for oh, od in zip(outs_h, call(dev)):
+            oh.copy_(od, non_blocking=True)
+
+    step()
+    ms, _ = timed_calls(torch, stream, step, n)
+    del dev, host
+    return ms, h2d, d2h
+
+
 # ----------------------------------------------------------------- decode
 
 def decode_work(inp, wl):
@@ -290,16 +329,17 @@ def prefill_flops(cu_q, cu_k, hq, dk, dv, causal):
     return total * hq * 2 * (dk + dv)
 
 
-def bench_prefill(fw, torch, steps, warmup, device, peaks, name=None, softmax="static"):
+def bench_prefill(fw, torch, steps, warmup, device, peaks, name=None, softmax="static", do_e2e=True,
+                  do_cpu=False):
     name = name or PREFILL_WL
     fw.set_option(fw.FW_OPT_PREFILL_SOFTMAX, 1 if softmax == "online" else 0)
     try:
-        return _bench_prefill(fw, torch, steps, warmup, device, peaks, name, softmax)
+        return _bench_prefill(fw, torch, steps, warmup, device, peaks, name, softmax, do_e2e, do_cpu)
     finally:
         fw.set_option(fw.FW_OPT_PREFILL_SOFTMAX, 0)
 
 
-def _bench_prefill(fw, torch, steps, warmup, device, peaks, name, softmax):
+def _bench_prefill(fw, torch, steps, warmup, device, peaks, name, softmax, do_e2e, do_cpu):
     from ragged_softmax_attention_gb300.workloads import WORKLOADS, make_prefill_inputs
     wl = WORKLOADS[name]
     d = make_prefill_inputs(wl, device)
@@ -321,28 +361,41 @@ def _bench_prefill(fw, torch, steps, warmup, device, peaks, name, softmax):
     torch.cuda.synchronize()
     fw.set_option(fw.FW_OPT_KERNEL_TIMING, 1)
     fw.kernel_timing_read()
+    fw.read_counters()
     n = max(3, min(steps, 50))
     l0 = fw.launch_count()
-    start = torch.cuda.Event(enable_timing=True)
-    stop = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for _ in range(n):
-        fw.varlen_prefill(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], wl.causal, wl.scale,
-                          out=out, lse=lse)
-    stop.record(stream)
-    torch.cuda.synchronize()
-    ms = start.elapsed_time(stop) / n
+    ms, clocks = timed_calls(torch, stream, lambda: fw.varlen_prefill(
+        d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], wl.causal, wl.scale, out=out, lse=lse), n)
+    launches = fw.launch_count() - l0
     kms, kn = fw.kernel_timing_read()
     fw.set_option(fw.FW_OPT_KERNEL_TIMING, 0)
+    replays = fw.read_counters()["prefill_replays"]
     if fw.device_status() != 0:
         raise RuntimeError("device status nonzero during the prefill benchmark")
     per = kms / max(1, kn)
+    e2e = None
+    if do_e2e:
+        e_ms, h2d, d2h = e2e_calls(
+            torch, device, stream, {k: d[k] for k in ("q", "k", "v", "cu_seqlens_q", "cu_seqlens_k")},
+            lambda x: fw.varlen_prefill(x["q"], x["k"], x["v"], x["cu_seqlens_q"], x["cu_seqlens_k"], wl.causal,
+                                        wl.scale, out=out, lse=lse), [out, lse], max(3, min(steps, 10)))
+        e2e = {"value": round(flops / (e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 4),
+               "note": "q, k, v and cu_seqlens copied from pinned host memory and out + lse copied back every "
+                       "step, through fw_varlen_prefill"}
+    cpu = None
+    if do_cpu:
+        try:
+            cpu = prefill_cpu_baseline(torch, d, wl)
+        except Exception as e:   # the baseline is context; report why it is missing
+            cpu = {"value": None, "unit": "TFLOP/s", "kind": "oracle", "error": str(e)}
     ach = flops / (per * 1e-3) / 1e12
     profile = {PREFILL_WL: "varlen_prefill_gqa_ncu.json", PREFILL_HD256_WL: "varlen_prefill_hd256_ncu.json"}[name]
     traffic = ncu_traffic(profile, ["prefill_kernel.cu", "fw_pair.cuh", "fw_ptx.cuh", "abi.cu"], flops)
     return {"workload": name, "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 4), "steps": n, "flops_per_step": flops,
-            "gpu_launches": fw.launch_count() - l0,
+            "gpu_launches": launches, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
+            "anchor_replays_per_call": round(replays / n, 2),
             "config": {"num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads, "num_kv_heads": wl.num_kv_heads,
                        "head_dim": wl.head_dim_qk, "causal": wl.causal, "total_tokens": cu_q[-1],
                        "seq_len_range": list(wl.seq_len_range) if wl.seq_len_range else None,
@@ -384,14 +437,7 @@ def bench_decode_fp8(fw, torch, steps, warmup, device, peaks, batch=None):
     fw.kernel_timing_read()
     n = max(3, min(steps, 100))
     l0 = fw.launch_count()
-    start = torch.cuda.Event(enable_timing=True)
-    stop = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for _ in range(n):
-        fw.paged_decode_fp8(*args, out=out, lse=lse)
-    stop.record(stream)
-    torch.cuda.synchronize()
-    ms = start.elapsed_time(stop) / n
+    ms, clocks = timed_calls(torch, stream, lambda: fw.paged_decode_fp8(*args, out=out, lse=lse), n)
     kms, kn = fw.kernel_timing_read()
     fw.set_option(fw.FW_OPT_KERNEL_TIMING, 0)
     if fw.device_status() != 0:
@@ -400,7 +446,7 @@ def bench_decode_fp8(fw, torch, steps, warmup, device, peaks, batch=None):
     ach = alg / (per * 1e-3) / 1e9
     return {"workload": DECODE_FP8_WL, "value": round(kv / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
             "kv_tokens_per_s": round(tokens / (ms * 1e-3), 1), "ms_per_step": round(ms, 4), "steps": n,
-            "kv_bytes_per_step": kv, "gpu_launches": fw.launch_count() - l0,
+            "kv_bytes_per_step": kv, "gpu_launches": fw.launch_count() - l0, "clocks": clocks,
             "config": {"batch": wl.batch, "q_len": wl.q_len, "num_q_heads": wl.num_q_heads,
                        "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim_qk, "page_size": wl.page_size,
                        "kv_dtype": "fp8_e4m3, one scale per cache", "total_kv_tokens": tokens},
@@ -440,14 +486,8 @@ def bench_decode_window(fw, torch, steps, warmup, device, peaks, fp8=False, wind
     fw.kernel_timing_read()
     n = max(3, min(steps, 100))
     l0 = fw.launch_count()
-    start = torch.cuda.Event(enable_timing=True)
-    stop = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for _ in range(n):
-        fw.paged_decode_window(*args, k_scale=ks, v_scale=vs, out=out, lse=lse)
-    stop.record(stream)
-    torch.cuda.synchronize()
-    ms = start.elapsed_time(stop) / n
+    ms, clocks = timed_calls(torch, stream, lambda: fw.paged_decode_window(*args, k_scale=ks, v_scale=vs, out=out,
+                                                                           lse=lse), n)
     kms, kn = fw.kernel_timing_read()
     fw.set_option(fw.FW_OPT_KERNEL_TIMING, 0)
     if fw.device_status() != 0:
@@ -459,6 +499,7 @@ def bench_decode_window(fw, torch, steps, warmup, device, peaks, fp8=False, wind
             "value": round(kv / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
             "kv_tokens_per_s": round(tokens / (ms * 1e-3), 1), "ms_per_step": round(ms, 4), "steps": n,
             "kv_bytes_per_step": kv, "window_kv_tokens": tokens, "gpu_launches": fw.launch_count() - l0,
+            "clocks": clocks,
             "roofline": {"kernel": kernel, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": None,
                          "peak_source": peaks["source"], "algorithmic_bytes_per_launch": alg,
@@ -491,20 +532,13 @@ def bench_decode_append(fw, torch, steps, warmup, device, peaks):
     torch.cuda.synchronize()
     n = max(3, min(steps, 100))
     l0 = fw.launch_count()
-    start = torch.cuda.Event(enable_timing=True)
-    stop = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for _ in range(n):
-        fw.paged_decode_append(*args, out=out, lse=lse)
-    stop.record(stream)
-    torch.cuda.synchronize()
-    ms = start.elapsed_time(stop) / n
+    ms, clocks = timed_calls(torch, stream, lambda: fw.paged_decode_append(*args, out=out, lse=lse), n)
     if fw.device_status() != 0:
         raise RuntimeError("device status nonzero during the append + decode benchmark")
     appended = wl.batch * wl.num_kv_heads * (wl.head_dim_qk + wl.head_dim_v) * 2
     return {"workload": DECODE_WL + ", new token appended in the call", "value": round(kv / (ms * 1e-3) / 1e9, 1),
             "unit": "GB/s", "ms_per_step": round(ms, 4), "steps": n, "kv_bytes_per_step": kv,
-            "appended_bytes_per_step": appended, "gpu_launches": fw.launch_count() - l0}
+            "appended_bytes_per_step": appended, "gpu_launches": fw.launch_count() - l0, "clocks": clocks}
 
 
 # ------------------------------------------------------- latent decode
@@ -525,7 +559,7 @@ LATENT_KERNEL = "latent_pair_decode_kernel"
 LATENT_SOURCES = ["latent_pair_kernel.cu", "fw_pair.cuh", "fw_ptx.cuh", "decode_common.cuh", "abi.cu"]
 
 
-def bench_latent(fw, torch, steps, warmup, device, peaks, batch=None):
+def bench_latent(fw, torch, steps, warmup, device, peaks, batch=None, do_e2e=True, do_cpu=False):
     import dataclasses
     from ragged_softmax_attention_gb300.workloads import WORKLOADS, make_decode_inputs
     wl = WORKLOADS[LATENT_WL]
@@ -543,25 +577,40 @@ def bench_latent(fw, torch, steps, warmup, device, peaks, batch=None):
     torch.cuda.synchronize()
     fw.set_option(fw.FW_OPT_KERNEL_TIMING, 1)
     fw.kernel_timing_read()
+    fw.read_counters()
     n = max(3, min(steps, 50))
     l0 = fw.launch_count()
-    start = torch.cuda.Event(enable_timing=True)
-    stop = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for _ in range(n):
-        fw.paged_decode(*args, out=out, lse=lse)
-    stop.record(stream)
-    torch.cuda.synchronize()
-    ms = start.elapsed_time(stop) / n
+    ms, clocks = timed_calls(torch, stream, lambda: fw.paged_decode(*args, out=out, lse=lse), n)
+    launches = fw.launch_count() - l0
     kms, kn = fw.kernel_timing_read()
     fw.set_option(fw.FW_OPT_KERNEL_TIMING, 0)
+    rescales = fw.read_counters()["latent_rescales"]
     if fw.device_status() != 0:
         raise RuntimeError("device status nonzero during the latent decode benchmark")
     per = kms / max(1, kn)
     ach = flops / (per * 1e-3) / 1e12
+    e2e = None
+    if do_e2e:
+        # The values are a view of the key cache: only the 576-wide cache crosses the link.
+        e_ms, h2d, d2h = e2e_calls(
+            torch, device, stream, {k: d[k] for k in ("q", "k_cache", "block_table", "seq_lens")},
+            lambda x: fw.paged_decode(x["q"], x["k_cache"], x["k_cache"][..., :wl.head_dim_v], x["block_table"],
+                                      x["seq_lens"], d["scale"], out=out, lse=lse), [out, lse], 3)
+        e2e = {"value": round(flops / (e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 4),
+               "note": "q, the key cache (values are its first 512 columns), block table and seq_lens copied "
+                       "from pinned host memory and out + lse copied back every step, through fw_paged_decode"}
+    cpu = None
+    if do_cpu:
+        try:
+            cpu = latent_cpu_baseline(torch, d, wl)
+        except Exception as e:   # the baseline is context; report why it is missing
+            cpu = {"value": None, "unit": "TFLOP/s", "kind": "oracle", "error": str(e)}
     return {"workload": LATENT_WL, "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "kv_gbs": round(kv / (ms * 1e-3) / 1e9, 1), "ms_per_step": round(ms, 4), "steps": n,
-            "flops_per_step": flops, "kv_bytes_per_step": kv, "gpu_launches": fw.launch_count() - l0,
+            "flops_per_step": flops, "kv_bytes_per_step": kv, "gpu_launches": launches,
+            "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
+            "anchor_rescales_per_call": round(rescales / n, 2),
             "config": {"batch": wl.batch, "q_len": wl.q_len, "num_q_heads": wl.num_q_heads,
                        "num_kv_heads": wl.num_kv_heads, "head_dim_qk": wl.head_dim_qk,
                        "head_dim_v": wl.head_dim_v, "page_size": wl.page_size, "seq_lens": "81920 each",
@@ -613,6 +662,78 @@ def cpu_baseline(torch, inp, wl, budget_s=12.0):
     return {"value": round(by / s / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": f"{n} batch rows in batch order ({n / wl.batch:.1f} passes over the {wl.batch}-row batch), "
                       f"all {wl.num_q_heads} query heads ({s:.1f} s of fp64 CPU work, {threads} threads)"}
+
+
+def prefill_cpu_baseline(torch, d, wl, budget_s=8.0):
+    """The oracle, as it stands, on the host cores over a fixed sample of the
+    prefill's (query row, head) units: evenly spaced rows of the flattened
+    [total_q, Hq] list, doubling the sample until about `budget_s` seconds of
+    oracle time.  The rate is the sample's algorithmic FLOPs over its time;
+    the whole workload's time is extrapolated from it."""
+    import numpy as np
+    import oracle
+    threads = max(1, os.cpu_count() or 1)
+    q, k, v = d["q"].cpu(), d["k"].cpu(), d["v"].cpu()
+    cq, ck = d["cu_seqlens_q"].cpu(), d["cu_seqlens_k"].cpu()
+    cql, ckl = cq.tolist(), ck.tolist()
+    total = q.shape[0] * wl.num_q_heads
+    seq_of = np.searchsorted(np.asarray(cql), np.arange(q.shape[0]), side="right") - 1
+
+    def row_flops(rows):
+        tok = rows // wl.num_q_heads
+        sq = seq_of[tok]
+        lq = np.asarray(cql)[sq + 1] - np.asarray(cql)[sq]
+        lk = np.asarray(ckl)[sq + 1] - np.asarray(ckl)[sq]
+        r = tok - np.asarray(cql)[sq]
+        vis = np.clip(r + lk - lq + 1, 0, lk) if wl.causal else lk
+        return int(vis.sum()) * 2 * (wl.head_dim_qk + wl.head_dim_v)
+
+    n = 1024
+    while True:
+        rows = np.linspace(0, total - 1, num=min(n, total)).astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.varlen_prefill(q, k, v, cq, ck, wl.causal, wl.scale, rows=rows, threads=threads)
+        sec = time.perf_counter() - t0
+        if sec >= budget_s / 2 or n >= total:
+            break
+        n *= 2
+    f = row_flops(rows)
+    rate = f / sec
+    whole = prefill_flops(cql, ckl, wl.num_q_heads, wl.head_dim_qk, wl.head_dim_v, wl.causal)
+    return {"value": round(rate / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{rows.size} evenly spaced (query row, head) units of {total} ({f / 1e9:.1f} GFLOP, "
+                      f"{sec:.1f} s of fp64 CPU work, {threads} threads)",
+            "extrapolated": True, "whole_workload_s": round(whole / rate, 1)}
+
+
+def latent_cpu_baseline(torch, d, wl, budget_s=8.0):
+    """The oracle, as it stands, on the host cores over whole requests (all
+    query tokens and heads) in batch order until about `budget_s` seconds of
+    oracle time; the rate is their algorithmic FLOPs over that time and the
+    whole workload's time is extrapolated from it."""
+    import oracle
+    threads = max(1, os.cpu_count() or 1)
+    lens = d["seq_lens"].cpu()
+    bt = d["block_table"].cpu()
+    f, sec, nb = 0, 0.0, 0
+    while sec < budget_s and nb < wl.batch:
+        b = nb
+        npg = -(-int(lens[b]) // wl.page_size)
+        pages = bt[b, :npg].long().to(d["k_cache"].device)
+        kc = d["k_cache"][pages].cpu()
+        sub_bt = torch.arange(npg, dtype=torch.int32).unsqueeze(0)
+        t0 = time.perf_counter()
+        oracle.paged_decode(d["q"][b:b + 1].cpu(), kc, kc[..., :wl.head_dim_v], sub_bt, lens[b:b + 1], wl.scale,
+                            threads=threads)
+        sec += time.perf_counter() - t0
+        f += latent_work([int(lens[b])], wl)[0]
+        nb += 1
+    rate = f / sec
+    whole = latent_work(lens.tolist(), wl)[0]
+    return {"value": round(rate / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{nb} of {wl.batch} requests, all {wl.q_len} tokens x {wl.num_q_heads} heads "
+                      f"({f / 1e9:.1f} GFLOP, {sec:.1f} s of fp64 CPU work, {threads} threads)",
+            "extrapolated": True, "whole_workload_s": round(whole / rate, 1)}
 
 
 def run_reference(args):
@@ -724,10 +845,15 @@ def main():
         return 0
     dec = bench_decode(fw, torch, args.steps, args.warmup, device, peaks, batch=args.decode_batch or None,
                        do_e2e=not args.no_e2e, barrier=(pg.barrier if pg else (lambda: None)))
-    pre = None if args.only == "decode" else bench_prefill(fw, torch, args.steps, args.warmup, device, peaks)
+    # CPU baselines on rank 0 of a single-GPU run only (they hold no GPU work).
+    do_cpu = world == 1 and not args.no_cpu_baseline and not args.decode_batch
+    pre = None if args.only == "decode" else bench_prefill(fw, torch, args.steps, args.warmup, device, peaks,
+                                                           do_e2e=not args.no_e2e, do_cpu=do_cpu)
     pre256 = (None if args.only == "decode" else
-              bench_prefill(fw, torch, args.steps, args.warmup, device, peaks, name=PREFILL_HD256_WL))
-    lat = None if args.only == "decode" else bench_latent(fw, torch, args.steps, args.warmup, device, peaks)
+              bench_prefill(fw, torch, args.steps, args.warmup, device, peaks, name=PREFILL_HD256_WL,
+                            do_e2e=not args.no_e2e, do_cpu=do_cpu))
+    lat = None if args.only == "decode" else bench_latent(fw, torch, args.steps, args.warmup, device, peaks,
+                                                         do_e2e=not args.no_e2e, do_cpu=do_cpu)
     f8 = None if args.only == "decode" else bench_decode_fp8(fw, torch, args.steps, args.warmup, device, peaks)
     w16 = (None if args.only == "decode" else
            bench_decode_window(fw, torch, args.steps, args.warmup, device, peaks, fp8=False))
@@ -752,7 +878,7 @@ def main():
                     "note": "inputs (incl. the KV cache) copied from pinned host memory every step"},
             "prefill": pre, "prefill_hd256": pre256, "latent_decode": lat, "decode_fp8": f8,
             "decode_window": w16, "decode_fp8_window": w8, "decode_append": app}
-    if world == 1 and not args.no_cpu_baseline and not args.decode_batch:
+    if do_cpu:
         try:
             line["cpu_baseline"] = cpu_baseline(torch, dec["inputs"], dec["wl"])
         except Exception as e:   # the baseline is context; report why it is missing
