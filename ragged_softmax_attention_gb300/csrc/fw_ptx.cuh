@@ -373,6 +373,24 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     return d;
 }
 
+// The same descriptor kept as two words, for MMA loops that step through a
+// tile: the start address is the low 14 bits of the low word (address / 16),
+// so adding offset / 16 to that word moves the descriptor by `offset` bytes
+// (no carry while the address stays below 256 KB).  One integer add per
+// operand instead of rebuilding it: at N = 128 a tcgen05.mma takes 64 cycles,
+// and an issuing thread that also rebuilds two descriptors per instruction
+// could not keep up (measured: 74 cycles per instruction).
+struct SDesc {
+    uint32_t lo, hi;
+};
+__device__ __forceinline__ SDesc sdesc_sw128_split(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    const uint64_t d = sdesc_sw128(saddr, lbo, sbo);
+    return SDesc{(uint32_t)d, (uint32_t)(d >> 32)};
+}
+__device__ __forceinline__ uint64_t sdesc_at(SDesc d, uint32_t byte_offset) {
+    return ((uint64_t)d.hi << 32) | (uint64_t)(d.lo + (byte_offset >> 4));
+}
+
 // Instruction descriptor, kind::f16 with BF16 A/B and FP32 accumulation.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bool a_mn_major,
                                                      bool b_mn_major) {

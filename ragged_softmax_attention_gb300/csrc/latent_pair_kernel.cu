@@ -345,36 +345,45 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
         // -------------------------------------------------- MMA (CTA 0 only)
         if (rank == 0 && lane == 0) {
             uint32_t m = 0, nq = 0, nr = 0, jt = 0, npv = 0;
-            const uint32_t q_base = smem_u32(sQ);
-            const uint32_t ring_base = smem_u32(sRing);
-            const uint32_t rot_base = smem_u32(sRot);
-            const uint32_t p_base = smem_u32(sP);
-            auto wait_slot = [&](uint32_t mm) {
-                return mbar_wait_cluster(&slot_full[mm % kSlots], (mm / kSlots) & 1, wc);
+            uint32_t si = 0, sph = 0;                  // ring slot of item m and its phase bit
+            // Descriptors at the tile bases; the loops add compile-time
+            // offsets (one integer add per operand and instruction).
+            const SDesc q_k = sdesc_sw128_split(smem_u32(sQ), 16, 1024);               // Q^T, K-major
+            const SDesc ring_k = sdesc_sw128_split(smem_u32(sRing), 16, 1024);          // key chunks, K-major
+            const SDesc ring_mn = sdesc_sw128_split(smem_u32(sRing), kHalfBytes, 1024); // value chunks, MN-major
+            const SDesc rot_k = sdesc_sw128_split(smem_u32(sRot), 16, 1024);
+            const SDesc p_mn = sdesc_sw128_split(smem_u32(sP), 8192, 1024);             // P^T, MN-major
+            // The slot of item m lands on the CTA-0 barrier; the copies are
+            // TMA transfers completing on it, so a CTA-scope acquire suffices.
+            auto wait_slot = [&]() { return mbar_wait(&slot_full[si], sph, wc); };
+            auto next_slot = [&]() {
+                ++m;
+                if (++si == (uint32_t)kSlots) { si = 0; sph ^= 1u; }
             };
             auto issue_qk = [&](bool last_of_piece) -> bool {
                 const uint32_t sb = jt & 1;
                 if (!mbar_wait_cluster(&s_free[sb], ((jt >> 1) & 1) ^ 1, wc)) return false;
+#pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
-                    if (!wait_slot(m)) return false;
+                    if (!wait_slot()) return false;
                     tc_fence_after();
-                    const uint32_t slot = ring_base + (m % kSlots) * kSlotBytes;
+                    const SDesc slot_k{ring_k.lo + si * (kSlotBytes >> 4), ring_k.hi};
+                    const SDesc q_c{q_k.lo + (uint32_t)c * (2 * kQChunkBytes >> 4), q_k.hi};
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t a = sdesc_sw128(slot + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
-                        const uint64_t b = sdesc_sw128(q_base + (2 * c + (kk >> 2)) * kQChunkBytes + (kk & 3) * 32,
-                                                       16, 1024);
+                        const uint64_t a = sdesc_at(slot_k, (kk >> 2) * kHalfBytes + (kk & 3) * 32);
+                        const uint64_t b = sdesc_at(q_c, (kk >> 2) * kQChunkBytes + (kk & 3) * 32);
                         mma_pair_ss(tmem + sb * 128, a, b, kIdescQK, (c > 0 || kk > 0) ? 1u : 0u);
                     }
-                    mma_commit_pair(&slot_empty[m % kSlots]);
-                    ++m;
+                    mma_commit_pair(&slot_empty[si]);
+                    next_slot();
                 }
-                if (!mbar_wait_cluster(rot_full, nr & 1, wc)) return false;
+                if (!mbar_wait(rot_full, nr & 1, wc)) return false;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t a = sdesc_sw128(rot_base + kk * 32, 16, 1024);
-                    const uint64_t b = sdesc_sw128(q_base + 8 * kQChunkBytes + kk * 32, 16, 1024);
+                    const uint64_t a = sdesc_at(rot_k, kk * 32);
+                    const uint64_t b = sdesc_at(q_k, 8 * kQChunkBytes + kk * 32);
                     mma_pair_ss(tmem + sb * 128, a, b, kIdescQK, 1u);
                 }
                 mma_commit_pair(rot_empty);
@@ -387,19 +396,22 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
             auto issue_pv = [&](bool first) -> bool {
                 if (!mbar_wait_cluster(p_full, npv & 1, wc)) return false;
                 tc_fence_after();
+#pragma unroll 1
                 for (int v = 0; v < 4; ++v) {
                     const int dh = v >> 1, kh = v & 1;
-                    if (!wait_slot(m)) return false;
+                    if (!wait_slot()) return false;
                     tc_fence_after();
-                    const uint32_t slot = ring_base + (m % kSlots) * kSlotBytes;
+                    const SDesc slot_mn{ring_mn.lo + si * (kSlotBytes >> 4), ring_mn.hi};
+                    const SDesc p_h{p_mn.lo + (uint32_t)kh * (kKeysCta * 128 >> 4), p_mn.hi};
+                    const uint32_t o_col = tmem + kColO + (uint32_t)dh * 128;
 #pragma unroll
                     for (int kk = 0; kk < kKeysCta / 16; ++kk) {
-                        const uint64_t a = sdesc_sw128(slot + kk * 16 * 128, kHalfBytes, 1024);
-                        const uint64_t b = sdesc_sw128(p_base + (kh * kKeysCta + kk * 16) * 128, 8192, 1024);
-                        mma_pair_ss(tmem + kColO + dh * 128, a, b, kIdescPV, (first && kh == 0 && kk == 0) ? 0u : 1u);
+                        const uint64_t a = sdesc_at(slot_mn, kk * 16 * 128);
+                        const uint64_t b = sdesc_at(p_h, kk * 16 * 128);
+                        mma_pair_ss(o_col, a, b, kIdescPV, (first && kh == 0 && kk == 0) ? 0u : 1u);
                     }
-                    mma_commit_pair(&slot_empty[m % kSlots]);
-                    ++m;
+                    mma_commit_pair(&slot_empty[si]);
+                    next_slot();
                 }
                 mma_commit_pair(pv_done);
                 ++npv;
@@ -410,7 +422,7 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
             it.init(p, pair, npairs);
             dec::LatentPiece x;
             while (ok && it.next(p, x)) {
-                if (!mbar_wait_cluster(q_full, nq & 1, wc)) { ok = false; break; }
+                if (!mbar_wait(q_full, nq & 1, wc)) { ok = false; break; }
                 tc_fence_after();
                 ++nq;
                 const int nsteps = (x.ntiles + 1) >> 1;
