@@ -279,14 +279,19 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
             // each step waits for everything first and commits afterwards.
             auto wait_tile = [&](uint32_t r) { return wait_slot(r); };
             auto release_tile = [&](uint32_t r) { mma_commit(&slot_empty[r % C::kSlots]); };
+            // Descriptors at the tile bases; the loops add compile-time offsets
+            // (one integer add per operand: at N = 128 an MMA takes 64 cycles,
+            // too few to rebuild two descriptors in the issuing thread).
+            const SDesc q_k = sdesc_sw128_split(smem_u32(sQ + x * C::kTileBytes), 16, 1024);
+            const SDesc ring_k = sdesc_sw128_split(smem_u32(sRing), 16, 1024);
+            const SDesc ring_v = sdesc_sw128_split(smem_u32(sRing), C::kChunkBytes, 1024);
             auto push_qk = [&](uint32_t r_k) {
                 const uint32_t sc = C::s_col(x);
-                const uint32_t q_base = smem_u32(sQ + x * C::kTileBytes);
-                const uint32_t k_base = smem_u32(sRing + (r_k % C::kSlots) * C::kSlotBytes);
+                const SDesc kd{ring_k.lo + (r_k % C::kSlots) * (C::kSlotBytes >> 4), ring_k.hi};
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t a = sdesc_sw128(q_base + (kk >> 2) * C::kChunkBytes + (kk & 3) * 32, 16, 1024);
-                    const uint64_t b = sdesc_sw128(k_base + (kk >> 2) * C::kChunkBytes + (kk & 3) * 32, 16, 1024);
+                    const uint64_t a = sdesc_at(q_k, (kk >> 2) * C::kChunkBytes + (kk & 3) * 32);
+                    const uint64_t b = sdesc_at(kd, (kk >> 2) * C::kChunkBytes + (kk & 3) * 32);
                     mma_bf16_ss(tmem + sc, a, b, C::kIdescQK, kk > 0 ? 1u : 0u);
                 }
             };
@@ -298,10 +303,10 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
             // (two BF16 per 32-bit column): A operand straight from TMEM.
             auto push_pv = [&](uint32_t r_v, bool first) {
                 const uint32_t p_col = C::s_col(x);
-                const uint32_t v_base = smem_u32(sRing + (r_v % C::kSlots) * C::kSlotBytes);
+                const SDesc vd{ring_v.lo + (r_v % C::kSlots) * (C::kSlotBytes >> 4), ring_v.hi};
 #pragma unroll
                 for (int kk = 0; kk < kKvTile / 16; ++kk) {
-                    const uint64_t b = sdesc_sw128(v_base + kk * 16 * 128, C::kChunkBytes, 1024);
+                    const uint64_t b = sdesc_at(vd, kk * 16 * 128);
                     mma_bf16_ts(tmem + C::o_col(x), tmem + p_col + kk * 8, b, C::kIdescPV,
                                 (first && kk == 0) ? 0u : 1u);
                 }
@@ -756,17 +761,20 @@ varlen_prefill_pair_kernel(const __grid_constant__ PrefillParams p, const __grid
         // -------------------------------------------------- MMA (CTA 0 only)
         if (rank == 0 && lane == 0) {
             uint32_t rp = 0, nu = 0, qk_cnt = 0, pv_cnt = 0;
-            const uint32_t q_base = smem_u32(sQ);
+            // Descriptors at the tile bases, stepped by compile-time offsets.
+            const SDesc q_k = sdesc_sw128_split(smem_u32(sQ), 16, 1024);
+            const SDesc ring_k = sdesc_sw128_split(smem_u32(sRing), 16, 1024);
+            const SDesc ring_v = sdesc_sw128_split(smem_u32(sRing), 128 * 128, 1024);
             auto wait_slot = [&](uint32_t r) {
                 return mbar_wait(&slot_full[r % kPairSlots], (r / kPairSlots) & 1, wc);
             };
             auto push_qk = [&](uint32_t r_k) {
                 const uint32_t sc = (qk_cnt & 1u) * 128u;
-                const uint32_t k_base = smem_u32(sRing + (r_k % kPairSlots) * kPairSlotBytes);
+                const SDesc kd{ring_k.lo + (r_k % kPairSlots) * (kPairSlotBytes >> 4), ring_k.hi};
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t a = sdesc_sw128(q_base + (kk >> 2) * 128 * 128 + (kk & 3) * 32, 16, 1024);
-                    const uint64_t b = sdesc_sw128(k_base + (kk >> 2) * 64 * 128 + (kk & 3) * 32, 16, 1024);
+                    const uint64_t a = sdesc_at(q_k, (kk >> 2) * 128 * 128 + (kk & 3) * 32);
+                    const uint64_t b = sdesc_at(kd, (kk >> 2) * 64 * 128 + (kk & 3) * 32);
                     mma_pair_ss(tmem + sc, a, b, kPairIdescQK, kk > 0 ? 1u : 0u);
                 }
             };
@@ -775,10 +783,10 @@ varlen_prefill_pair_kernel(const __grid_constant__ PrefillParams p, const __grid
             // per column, in each CTA's TMEM.
             auto push_pv = [&](uint32_t r_v, bool first) {
                 const uint32_t p_col = (pv_cnt & 1u) * 128u;
-                const uint32_t v_base = smem_u32(sRing + (r_v % kPairSlots) * kPairSlotBytes);
+                const SDesc vd{ring_v.lo + (r_v % kPairSlots) * (kPairSlotBytes >> 4), ring_v.hi};
 #pragma unroll
                 for (int kk = 0; kk < kKvTile / 16; ++kk) {
-                    const uint64_t b = sdesc_sw128(v_base + kk * 16 * 128, 128 * 128, 1024);
+                    const uint64_t b = sdesc_at(vd, kk * 16 * 128);
                     mma_pair_ts(tmem + 256u, tmem + p_col + kk * 8, b, kPairIdescPV, (first && kk == 0) ? 0u : 1u);
                 }
             };
