@@ -240,19 +240,24 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
         if (lane == 0) {
             int jt = 0, ju = 0, pend = -1;
             bool pend_first = false;
+            // Descriptors at the tile bases, stepped by one integer add per
+            // operand and instruction.
+            const SDesc ring_d = sdesc_sw128_split(smem_u32(ring), 16, 1024);
+            const SDesc p_d = sdesc_sw128_split(smem_u32(sP), 16, 1024);
+            const SDesc q_d = sdesc_sw128_split(smem_u32(sQ8), 16, 1024);
             auto issue_pv = [&](int jj, bool first) -> bool {
                 const int s = jj % S;
                 const int pb = jj & 1;
                 if (!mbar_wait(&v_full[s], (jj / S) & 1, wc)) return false;
                 if (!mbar_wait(&p_full[pb], (jj >> 1) & 1, wc)) return false;
                 tc_fence_after();
-                const uint32_t v_base = smem_u32(ring + s * C::kStageBytes + C::kTileBytes);
-                const uint32_t p_base = smem_u32(sP + pb * C::kPBytes);
+                const SDesc v_s{ring_d.lo + (uint32_t)(s * C::kStageBytes + C::kTileBytes) / 16u, ring_d.hi};
+                const SDesc p_s{p_d.lo + (uint32_t)(pb * C::kPBytes) / 16u, p_d.hi};
 #pragma unroll
                 for (int kk = 0; kk < kKvTile / 32; ++kk) {
                     // A = V^T, MN-major: 32 key rows of 128 bytes per step.
-                    const uint64_t a = sdesc_sw128(v_base + kk * 32 * 128, 16, 1024);
-                    const uint64_t b = sdesc_sw128(p_base + kk * 32, 16, 1024);
+                    const uint64_t a = sdesc_at(v_s, kk * 32 * 128);
+                    const uint64_t b = sdesc_at(p_s, kk * 32);
                     mma_f8_ss(tmem + C::kColO, a, b, C::kIdescPV, (first && kk == 0) ? 0u : 1u);
                 }
                 mma_commit(&kv_empty[s]);
@@ -277,12 +282,12 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                     if (!mbar_wait(&k_full[s], (jt / S) & 1, wc)) goto mma_done;
                     if (!mbar_wait(&s_free[sb], ((jt >> 1) & 1) ^ 1, wc)) goto mma_done;
                     tc_fence_after();
-                    const uint32_t k_base = smem_u32(ring + s * C::kStageBytes);
-                    const uint32_t q_base = smem_u32(sQ8 + qs * C::kQ8Bytes);
+                    const SDesc k_s{ring_d.lo + (uint32_t)(s * C::kStageBytes) / 16u, ring_d.hi};
+                    const SDesc q_s{q_d.lo + (uint32_t)(qs * C::kQ8Bytes) / 16u, q_d.hi};
 #pragma unroll
                     for (int kk = 0; kk < D / 32; ++kk) {
-                        const uint64_t a = sdesc_sw128(k_base + kk * 32, 16, 1024);
-                        const uint64_t b = sdesc_sw128(q_base + kk * 32, 16, 1024);
+                        const uint64_t a = sdesc_at(k_s, kk * 32);
+                        const uint64_t b = sdesc_at(q_s, kk * 32);
                         mma_f8_ss(tmem + C::kColS + sb * C::kSCols, a, b, C::kIdescQK, kk > 0 ? 1u : 0u);
                     }
                     mma_commit(&qk_done[sb]);

@@ -242,21 +242,26 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
         if (lane == 0) {
             int jt = 0, ju = 0, pend = -1;
             bool pend_first = false;
+            // Descriptors at the tile bases, stepped by one integer add per
+            // operand and instruction.
+            const SDesc v_d = sdesc_sw128_split(smem_u32(sV), C::kChunkBytes, 1024);
+            const SDesc k_d = sdesc_sw128_split(smem_u32(sK), 16, 1024);
+            const SDesc p_d = sdesc_sw128_split(smem_u32(sP), 16, 1024);
+            const SDesc q_d = sdesc_sw128_split(smem_u32(sQ), 16, 1024);
             auto issue_pv = [&](int jj, bool first) -> bool {
                 const int vs = jj % C::kVStages;
                 const int pb = jj & 1;
                 if (!mbar_wait(&v_full[vs], (jj / C::kVStages) & 1, wc)) return false;
                 if (!mbar_wait(&p_full[pb], (jj >> 1) & 1, wc)) return false;
                 tc_fence_after();
-                const uint32_t v_base = smem_u32(sV + vs * C::kTileBytes);
-                const uint32_t p_base = smem_u32(sP + pb * C::kPBytes);
+                const SDesc v_s{v_d.lo + (uint32_t)(vs * C::kTileBytes) / 16u, v_d.hi};
+                const SDesc p_s{p_d.lo + (uint32_t)(pb * C::kPBytes) / 16u, p_d.hi};
 #pragma unroll
                 for (int dvt = 0; dvt < C::kDvTiles; ++dvt) {
 #pragma unroll
                     for (int kk = 0; kk < kKvTile / 16; ++kk) {
-                        const uint64_t a = sdesc_sw128(v_base + (2 * dvt) * C::kChunkBytes + kk * 16 * 128,
-                                                       C::kChunkBytes, 1024);
-                        const uint64_t b = sdesc_sw128(p_base + (kk >> 2) * NQ * 128 + (kk & 3) * 32, 16, 1024);
+                        const uint64_t a = sdesc_at(v_s, (2 * dvt) * C::kChunkBytes + kk * 16 * 128);
+                        const uint64_t b = sdesc_at(p_s, (kk >> 2) * NQ * 128 + (kk & 3) * 32);
                         mma_bf16_ss(tmem + 2 * NQ + dvt * NQ, a, b, C::kIdescPV, (first && kk == 0) ? 0u : 1u);
                     }
                 }
@@ -277,12 +282,12 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
                     if (!mbar_wait(&k_full[ks], (jt / C::kKStages) & 1, wc)) goto mma_done;
                     if (!mbar_wait(&s_free[sb], ((jt >> 1) & 1) ^ 1, wc)) goto mma_done;
                     tc_fence_after();
-                    const uint32_t k_base = smem_u32(sK + ks * C::kTileBytes);
-                    const uint32_t q_base = smem_u32(sQ + qs * C::kQBytes);
+                    const SDesc k_s{k_d.lo + (uint32_t)(ks * C::kTileBytes) / 16u, k_d.hi};
+                    const SDesc q_s{q_d.lo + (uint32_t)(qs * C::kQBytes) / 16u, q_d.hi};
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t a = sdesc_sw128(k_base + (kk >> 2) * C::kChunkBytes + (kk & 3) * 32, 16, 1024);
-                        const uint64_t b = sdesc_sw128(q_base + (kk >> 2) * NQ * 128 + (kk & 3) * 32, 16, 1024);
+                        const uint64_t a = sdesc_at(k_s, (kk >> 2) * C::kChunkBytes + (kk & 3) * 32);
+                        const uint64_t b = sdesc_at(q_s, (kk >> 2) * NQ * 128 + (kk & 3) * 32);
                         mma_bf16_ss(tmem + sb * NQ, a, b, C::kIdescQK, kk > 0 ? 1u : 0u);
                     }
                     mma_commit(&k_empty[ks]);
