@@ -192,21 +192,40 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
             }
             __syncwarp();
             {
+                // Physical page numbers, 64 logical pages at a time in two
+                // 32-entry register windows (lane l holds page win + l and
+                // win + 32 + l), the next window fetched while the current one
+                // is in use: no tile waits on a block-table read (a read per tile
+                // on the copy warp's path measured as the bound of this kernel).
+                // Entries past the row's last page, or wholly before its window,
+                // are never read.
                 const int32_t *bt_row = p.block_table + (int64_t)x.b * p.bt_stride;
+                const int lp_end = ceil_div_i(x.k_end, p.ps);
+                const int lp_first = x.lo / p.ps;
+                int win = x.k_begin / p.ps;
+                auto bt_at = [&](int lp) { return (lp >= lp_first && lp < lp_end) ? __ldg(bt_row + lp) : 0; };
+                int cur = bt_at(win + lane);
+                int nxt = bt_at(win + 32 + lane);
                 for (int i = 0; i < x.ntiles; ++i, ++jt) {
                     const int ts = x.k_begin + i * kKvTile;
+                    const int lp0 = ts / p.ps;
                     const int slot0 = p.ps < kKvTile ? 0 : ts % p.ps;
                     int npages = 1;
                     if (p.ps < kKvTile) npages = min(pages_per_tile, ceil_div_i(x.k_end - ts, p.ps));
+                    if (lp0 >= win + 32) {
+                        win += 32;
+                        cur = nxt;
+                        nxt = bt_at(win + 32 + lane);
+                    }
                     // Leading pages wholly before the window are neither looked
                     // up nor loaded (their rows are masked, their V rows zeroed).
-                    const int skip = min(npages, max(0, x.lo / p.ps - ts / p.ps));
+                    const int skip = min(npages, max(0, lp_first - lp0));
                     const bool load = lane >= skip && lane < npages;
-                    int phys = 0;
-                    if (load) {
-                        phys = __ldg(bt_row + ts / p.ps + lane);
-                        if ((unsigned)phys >= (unsigned)p.num_pages) { record_error(p.status, 1); phys = 0; }
-                    }
+                    const int idx = lp0 + lane - win;          // < 64 for loading lanes (npages <= 16)
+                    const int from_cur = __shfl_sync(0xffffffffu, cur, idx & 31);
+                    const int from_nxt = __shfl_sync(0xffffffffu, nxt, idx & 31);
+                    int phys = idx < 32 ? from_cur : from_nxt;
+                    if (load && (unsigned)phys >= (unsigned)p.num_pages) { record_error(p.status, 1); phys = 0; }
                     const uint32_t bytes = (uint32_t)((npages - skip) * box_rows * 128);
                     const int s = jt % S;
                     if (!warp_wait(&kv_empty[s], ((jt / S) & 1) ^ 1, wc, lane)) goto producer_done;
