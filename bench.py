@@ -153,6 +153,14 @@ def source_sha(*names):
     return h.hexdigest()
 
 
+# Files whose bytes decide each profiled kernel and its launch: a committed ncu
+# summary counts only while their hash still matches.
+DECODE_SOURCES = ["decode_kernel.cu", "decode_common.cuh", "fw_ptx.cuh", "fw_internal.h", "abi.cu"]
+FP8_SOURCES = ["decode_fp8_kernel.cu", "decode_common.cuh", "fw_ptx.cuh", "fw_internal.h", "abi.cu"]
+PREFILL_SOURCES = ["prefill_kernel.cu", "fw_pair.cuh", "fw_ptx.cuh", "fw_internal.h", "abi.cu"]
+LATENT_SOURCES = ["latent_pair_kernel.cu", "fw_pair.cuh", "fw_ptx.cuh", "decode_common.cuh", "fw_internal.h", "abi.cu"]
+
+
 def ncu_traffic(profile_name, sources, units):
     """DRAM bytes per launch from a committed ncu summary, scaled to `units`
     of work; None when the kernel source changed since the capture."""
@@ -261,7 +269,7 @@ def bench_decode(fw, torch, steps, warmup, device, peaks, batch=None, do_e2e=Tru
         raise RuntimeError(f"device status {status} during the decode benchmark")
     per_launch_ms = kernel_ms / max(1, kernel_n)
     achieved = alg_bytes / (per_launch_ms * 1e-3) / 1e9
-    traffic = ncu_traffic("paged_decode_qwen3_14b_ncu.json", ["decode_kernel.cu", "decode_common.cuh", "fw_ptx.cuh", "abi.cu"],
+    traffic = ncu_traffic("paged_decode_qwen3_14b_ncu.json", DECODE_SOURCES,
                           tokens)
     roof = {"kernel": "paged_decode_kernel<128,16>", "bound": "hbm", "achieved": round(achieved, 1),
             "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
@@ -391,7 +399,7 @@ def _bench_prefill(fw, torch, steps, warmup, device, peaks, name, softmax, do_e2
             cpu = {"value": None, "unit": "TFLOP/s", "kind": "oracle", "error": str(e)}
     ach = flops / (per * 1e-3) / 1e12
     profile = {PREFILL_WL: "varlen_prefill_gqa_ncu.json", PREFILL_HD256_WL: "varlen_prefill_hd256_ncu.json"}[name]
-    traffic = ncu_traffic(profile, ["prefill_kernel.cu", "fw_pair.cuh", "fw_ptx.cuh", "abi.cu"], flops)
+    traffic = ncu_traffic(profile, PREFILL_SOURCES, flops)
     return {"workload": name, "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 4), "steps": n, "flops_per_step": flops,
             "gpu_launches": launches, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
@@ -452,8 +460,7 @@ def bench_decode_fp8(fw, torch, steps, warmup, device, peaks, batch=None):
                        "kv_dtype": "fp8_e4m3, one scale per cache", "total_kv_tokens": tokens},
             "roofline": {"kernel": "paged_decode_fp8_kernel<16,8>", "bound": "hbm", "achieved": round(ach, 1),
                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
-                         "traffic": ncu_traffic("paged_decode_fp8_ncu.json",
-                                                ["decode_fp8_kernel.cu", "decode_common.cuh", "fw_ptx.cuh", "abi.cu"], tokens),
+                         "traffic": ncu_traffic("paged_decode_fp8_ncu.json", FP8_SOURCES, tokens),
                          "peak_source": peaks["source"], "algorithmic_bytes_per_launch": alg,
                          "kernel_ms_per_launch": round(per, 4)}}
 
@@ -556,7 +563,6 @@ def latent_work(lens, wl):
 
 # 128 query heads per KV head: the CTA-pair kernel serves the latent workload.
 LATENT_KERNEL = "latent_pair_decode_kernel"
-LATENT_SOURCES = ["latent_pair_kernel.cu", "fw_pair.cuh", "fw_ptx.cuh", "decode_common.cuh", "abi.cu"]
 
 
 def bench_latent(fw, torch, steps, warmup, device, peaks, batch=None, do_e2e=True, do_cpu=False):
