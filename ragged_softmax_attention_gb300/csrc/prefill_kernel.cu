@@ -445,17 +445,20 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                 const uint32_t sa = tmem + lane_off + C::s_col(x);
                 const int key0 = j * kKvTile;
                 // The whole row of S in registers with one TMEM round trip.
-                float sv[kKvTile];
-#pragma unroll
-                for (int c = 0; c < kKvTile / 32; ++c) tmem_ld32(sa + c * 32, sv + c * 32);
-                tmem_wait_ld();
                 // Masked keys (past the causal limit or the sequence end) get the
                 // value that exponentiates to 0 for this scale's sign.
-                if (key0 + kKvTile > lim) {
+                float sv[kKvTile];
+                auto load_s = [&]() {
 #pragma unroll
-                    for (int i = 0; i < kKvTile; ++i)
-                        if (key0 + i >= lim) sv[i] = scale_pos ? kNegInf : -kNegInf;
-                }
+                    for (int c = 0; c < kKvTile / 32; ++c) tmem_ld32(sa + c * 32, sv + c * 32);
+                    tmem_wait_ld();
+                    if (key0 + kKvTile > lim) {
+#pragma unroll
+                        for (int i = 0; i < kKvTile; ++i)
+                            if (key0 + i >= lim) sv[i] = scale_pos ? kNegInf : -kNegInf;
+                    }
+                };
+                load_s();
                 // Scaled row max of this tile (-inf when every key is masked),
                 // 8 independent chains over the raw scores.
                 auto row_max = [&]() -> float {
@@ -475,27 +478,30 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                     return (ext == kNegInf || ext == -kNegInf) ? kNegInf : ext * p.scale_log2;
                 };
                 // P = 2^(s * scale * log2(e) - anchor) as BF16, packed two per
-                // 32-bit column over the first 64 columns of this tile's S buffer
-                // (its scores are already in registers); returns the tile's row
-                // sum (8 independent chains).  Warp-collective (TMEM stores).
-                auto write_p = [&](float anchor) -> float {
+                // 32-bit register; returns the tile's row sum (8 independent
+                // chains).  Each score dies as its probability is formed, so the
+                // rows of S and P never both sit in registers in full.
+                // store_p writes P over the first 64 columns of this tile's S
+                // buffer (warp-collective TMEM stores), after the check below.
+                uint32_t pk[kKvTile / 2];
+                auto exp_pass = [&](float anchor) -> float {
                     const float mu = (anchor == kNegInf) ? 0.f : anchor;
                     float a8[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) a8[i] = 0.f;
 #pragma unroll
-                    for (int c = 0; c < kKvTile / 32; ++c) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int i = 0; i < 32; i += 2) {
-                            const float p0 = ex2_approx(fmaf(sv[c * 32 + i], p.scale_log2, -mu));
-                            const float p1 = ex2_approx(fmaf(sv[c * 32 + i + 1], p.scale_log2, -mu));
-                            a8[(i >> 1) & 7] += p0 + p1;
-                            pk[i >> 1] = pack_bf16x2(p0, p1);
-                        }
-                        tmem_st16u(sa + c * 16, pk);
+                    for (int i = 0; i < kKvTile; i += 2) {
+                        const float p0 = ex2_approx(fmaf(sv[i], p.scale_log2, -mu));
+                        const float p1 = ex2_approx(fmaf(sv[i + 1], p.scale_log2, -mu));
+                        a8[(i >> 1) & 7] += p0 + p1;
+                        pk[i >> 1] = pack_bf16x2(p0, p1);
                     }
                     return ((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]));
+                };
+                auto store_p = [&]() {
+#pragma unroll
+                    for (int c = 0; c < kKvTile / 32; ++c)
+                        tmem_st16u(sa + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + c * 16));
                 };
                 // P overwrites the tile's only S buffer, which PV_{j-1} reads:
                 // that PV has landed, since the same thread issued it before
@@ -536,31 +542,38 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                         }
                         if (j > 0) rescale_o(alpha);
                     }
-                    tsum = write_p(m_ref);
+                    tsum = exp_pass(m_ref);
                 } else {
                     if (m_ref == kNegInf) m_ref = row_max();
-                    tsum = write_p(m_ref);
+                    tsum = exp_pass(m_ref);
                     // The check: every p <= l, so a running sum within the budget
                     // proves no score rose more than log2(budget) above the anchor
                     // (appendix A, claim 2).  A row that fails (or overflowed)
                     // replays the tile with the rescaling softmax: its anchor moves
                     // to the new max, l and O are rescaled, P is recomputed before
-                    // the MMA sees it.
+                    // the MMA sees it.  The scores come back from TMEM, which P
+                    // has not overwritten yet.
                     const bool over = !(l_sum + tsum <= kAnchorBudget);
                     const unsigned replay = __ballot_sync(0xffffffffu, over);
                     if (replay) {
                         if (lane == 0) count_events(p.counters, kCounterPrefillReplays, __popc(replay));
+                        // The scores are read twice so that they are not held in
+                        // registers across the O rescale.
+                        load_s();
+                        const float m_tile = row_max();
                         float alpha = 1.f;
                         if (over) {
-                            const float m_new = fmaxf(m_ref, row_max());
+                            const float m_new = fmaxf(m_ref, m_tile);
                             alpha = ex2_approx(m_ref - m_new);
                             l_sum *= alpha;
                             m_ref = m_new;
                         }
                         if (j > 0) rescale_o(alpha);
-                        tsum = write_p(m_ref);     // all lanes: unchanged rows rewrite the same P
+                        load_s();
+                        tsum = exp_pass(m_ref);    // all lanes: unchanged rows recompute the same P
                     }
                 }
+                store_p();
                 l_sum += tsum;
                 tmem_wait_st();
                 tc_fence_before();
@@ -869,14 +882,17 @@ varlen_prefill_pair_kernel(const __grid_constant__ PrefillParams p, const __grid
                 const uint32_t sa = tmem + lane_off + sb * 128u;
                 const int key0 = j * kKvTile;
                 float sv[kKvTile];
+                auto load_s = [&]() {
 #pragma unroll
-                for (int c = 0; c < kKvTile / 32; ++c) tmem_ld32(sa + c * 32, sv + c * 32);
-                tmem_wait_ld();
-                if (key0 + kKvTile > lim) {
+                    for (int c = 0; c < kKvTile / 32; ++c) tmem_ld32(sa + c * 32, sv + c * 32);
+                    tmem_wait_ld();
+                    if (key0 + kKvTile > lim) {
 #pragma unroll
-                    for (int i = 0; i < kKvTile; ++i)
-                        if (key0 + i >= lim) sv[i] = scale_pos ? kNegInf : -kNegInf;
-                }
+                        for (int i = 0; i < kKvTile; ++i)
+                            if (key0 + i >= lim) sv[i] = scale_pos ? kNegInf : -kNegInf;
+                    }
+                };
+                load_s();
                 auto row_max = [&]() -> float {
                     float e8[8];
 #pragma unroll
@@ -893,24 +909,25 @@ varlen_prefill_pair_kernel(const __grid_constant__ PrefillParams p, const __grid
                         : fminf(fminf(fminf(e8[0], e8[1]), fminf(e8[2], e8[3])), fminf(fminf(e8[4], e8[5]), fminf(e8[6], e8[7])));
                     return (ext == kNegInf || ext == -kNegInf) ? kNegInf : ext * p.scale_log2;
                 };
-                auto write_p = [&](float anchor) -> float {
+                uint32_t pk[kKvTile / 2];
+                auto exp_pass = [&](float anchor) -> float {
                     const float mu = (anchor == kNegInf) ? 0.f : anchor;
                     float a8[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) a8[i] = 0.f;
 #pragma unroll
-                    for (int c = 0; c < kKvTile / 32; ++c) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int i = 0; i < 32; i += 2) {
-                            const float p0 = ex2_approx(fmaf(sv[c * 32 + i], p.scale_log2, -mu));
-                            const float p1 = ex2_approx(fmaf(sv[c * 32 + i + 1], p.scale_log2, -mu));
-                            a8[(i >> 1) & 7] += p0 + p1;
-                            pk[i >> 1] = pack_bf16x2(p0, p1);
-                        }
-                        tmem_st16u(sa + c * 16, pk);
+                    for (int i = 0; i < kKvTile; i += 2) {
+                        const float p0 = ex2_approx(fmaf(sv[i], p.scale_log2, -mu));
+                        const float p1 = ex2_approx(fmaf(sv[i + 1], p.scale_log2, -mu));
+                        a8[(i >> 1) & 7] += p0 + p1;
+                        pk[i >> 1] = pack_bf16x2(p0, p1);
                     }
                     return ((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]));
+                };
+                auto store_p = [&]() {
+#pragma unroll
+                    for (int c = 0; c < kKvTile / 32; ++c)
+                        tmem_st16u(sa + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + c * 16));
                 };
                 // Static anchor and the running-sum check, as in the one-CTA
                 // kernel; P(j) goes to S buffer j & 1, which PV(j-1) does not read.
@@ -944,31 +961,38 @@ varlen_prefill_pair_kernel(const __grid_constant__ PrefillParams p, const __grid
                         }
                         if (j > 0) rescale_o(alpha);
                     }
-                    tsum = write_p(m_ref);
+                    tsum = exp_pass(m_ref);
                 } else {
                     if (m_ref == kNegInf) m_ref = row_max();
-                    tsum = write_p(m_ref);
+                    tsum = exp_pass(m_ref);
                     // The check: every p <= l, so a running sum within the budget
                     // proves no score rose more than log2(budget) above the anchor
                     // (appendix A, claim 2).  A row that fails (or overflowed)
                     // replays the tile with the rescaling softmax: its anchor moves
                     // to the new max, l and O are rescaled, P is recomputed before
-                    // the MMA sees it.
+                    // the MMA sees it.  The scores come back from TMEM, which P
+                    // has not overwritten yet.
                     const bool over = !(l_sum + tsum <= kAnchorBudget);
                     const unsigned replay = __ballot_sync(0xffffffffu, over);
                     if (replay) {
                         if (lane == 0) count_events(p.counters, kCounterPrefillReplays, __popc(replay));
+                        // The scores are read twice so that they are not held in
+                        // registers across the O rescale.
+                        load_s();
+                        const float m_tile = row_max();
                         float alpha = 1.f;
                         if (over) {
-                            const float m_new = fmaxf(m_ref, row_max());
+                            const float m_new = fmaxf(m_ref, m_tile);
                             alpha = ex2_approx(m_ref - m_new);
                             l_sum *= alpha;
                             m_ref = m_new;
                         }
                         if (j > 0) rescale_o(alpha);
-                        tsum = write_p(m_ref);     // all lanes: unchanged rows rewrite the same P
+                        load_s();
+                        tsum = exp_pass(m_ref);    // all lanes: unchanged rows recompute the same P
                     }
                 }
+                store_p();
                 l_sum += tsum;
                 tmem_wait_st();
                 tc_fence_before();
