@@ -59,7 +59,7 @@ struct PrefillCfg {
     static constexpr int kOffQ = 0;
     static constexpr int kOffRing = kOffQ + kNumQ * kTileBytes;
     static constexpr int kOffBar = kOffRing + kSlots * kSlotBytes;
-    static constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 2 + 2;
+    static constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 2 + 2 + 2 + 2;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA exceeded");
@@ -190,6 +190,8 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
     uint64_t *pv_done = p_full + 2;                  // [2]
     uint64_t *drain = pv_done + 2;                   // [2]
     uint64_t *issued = drain + 2;                    // [2]: step handoff between the two issuers
+    uint64_t *p_half = issued + 2;                   // [2]: first half of P (keys 0..63) written
+    uint64_t *pvh_done = p_half + 2;                 // [2]: the PV of that half complete
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
 
@@ -203,6 +205,7 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1); mbar_init(&p_full[i], 4); mbar_init(&pv_done[i], 1); mbar_init(&drain[i], 1);
             mbar_init(&issued[i], 1);
+            mbar_init(&p_half[i], 4); mbar_init(&pvh_done[i], 1);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -300,12 +303,15 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                 ++qk_cnt;
             };
             // P was written over the first 64 columns of this tile's S buffer
-            // (two BF16 per 32-bit column): A operand straight from TMEM.
-            auto push_pv = [&](uint32_t r_v, bool first) {
+            // (two BF16 per 32-bit column): A operand straight from TMEM.  The
+            // softmax hands it over in two halves of 64 keys, and each half's
+            // four MMAs go out as soon as it is there.
+            auto push_pv_half = [&](uint32_t r_v, int half, bool first) {
                 const uint32_t p_col = C::s_col(x);
                 const SDesc vd{ring_v.lo + (r_v % C::kSlots) * (C::kSlotBytes >> 4), ring_v.hi};
 #pragma unroll
-                for (int kk = 0; kk < kKvTile / 16; ++kk) {
+                for (int k4 = 0; k4 < kKvTile / 32; ++k4) {
+                    const int kk = half * (kKvTile / 32) + k4;
                     const uint64_t b = sdesc_at(vd, kk * 16 * 128);
                     mma_bf16_ts(tmem + C::o_col(x), tmem + p_col + kk * 8, b, C::kIdescPV,
                                 (first && kk == 0) ? 0u : 1u);
@@ -380,11 +386,15 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                         // need only older items consumed), so PV and QK go out back
                         // to back.
                         if (!wait_tile(rv) || (next_mine && !wait_tile(rk)) ||
-                            !mbar_wait(&p_full[x], pv_cnt & 1u, wc)) {
+                            !mbar_wait(&p_half[x], pv_cnt & 1u, wc)) {
                             ok = false; break;
                         }
                         tc_fence_after();
-                        push_pv(rv, j == 0);
+                        push_pv_half(rv, 0, j == 0);
+                        mma_commit(&pvh_done[x]);       // read only by a late replay
+                        if (!mbar_wait(&p_full[x], pv_cnt & 1u, wc)) { ok = false; break; }
+                        tc_fence_after();
+                        push_pv_half(rv, 1, false);
                         // Hand the turn over while this step's QK is still being
                         // pushed: the other issuer's waits then overlap that push,
                         // and its PV queues right behind it instead of after an
@@ -459,18 +469,18 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                     }
                 };
                 load_s();
-                // Scaled row max of this tile (-inf when every key is masked),
-                // 8 independent chains over the raw scores.
-                auto row_max = [&]() -> float {
+                // Scaled row max of keys [lo, 128) of this tile (-inf when every
+                // one is masked), 8 independent chains over the raw scores.
+                auto row_max = [&](int lo) -> float {
                     float e8[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) e8[i] = sv[i];
+                    for (int i = 0; i < 8; ++i) e8[i] = sv[lo + i];
                     if (scale_pos) {
 #pragma unroll
-                        for (int i = 8; i < kKvTile; ++i) e8[i & 7] = fmaxf(e8[i & 7], sv[i]);
+                        for (int i = lo + 8; i < kKvTile; ++i) e8[i & 7] = fmaxf(e8[i & 7], sv[i]);
                     } else {
 #pragma unroll
-                        for (int i = 8; i < kKvTile; ++i) e8[i & 7] = fminf(e8[i & 7], sv[i]);
+                        for (int i = lo + 8; i < kKvTile; ++i) e8[i & 7] = fminf(e8[i & 7], sv[i]);
                     }
                     const float ext = scale_pos
                         ? fmaxf(fmaxf(fmaxf(e8[0], e8[1]), fmaxf(e8[2], e8[3])), fmaxf(fmaxf(e8[4], e8[5]), fmaxf(e8[6], e8[7])))
@@ -478,40 +488,51 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                     return (ext == kNegInf || ext == -kNegInf) ? kNegInf : ext * p.scale_log2;
                 };
                 // P = 2^(s * scale * log2(e) - anchor) as BF16, packed two per
-                // 32-bit register; returns the tile's row sum (8 independent
-                // chains).  Each score dies as its probability is formed, so the
-                // rows of S and P never both sit in registers in full.
-                // store_p writes P over the first 64 columns of this tile's S
-                // buffer (warp-collective TMEM stores), after the check below.
+                // 32-bit register, for keys [64h, 64h + 64); returns their sum
+                // (8 independent chains).  Each score dies as its probability is
+                // formed, so the rows of S and P never both sit in registers in
+                // full.
                 uint32_t pk[kKvTile / 2];
-                auto exp_pass = [&](float anchor) -> float {
+                auto exp_half = [&](int h, float anchor) -> float {
                     const float mu = (anchor == kNegInf) ? 0.f : anchor;
                     float a8[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) a8[i] = 0.f;
 #pragma unroll
-                    for (int i = 0; i < kKvTile; i += 2) {
-                        const float p0 = ex2_approx(fmaf(sv[i], p.scale_log2, -mu));
-                        const float p1 = ex2_approx(fmaf(sv[i + 1], p.scale_log2, -mu));
+                    for (int i = 0; i < kKvTile / 2; i += 2) {
+                        const int k = h * (kKvTile / 2) + i;
+                        const float p0 = ex2_approx(fmaf(sv[k], p.scale_log2, -mu));
+                        const float p1 = ex2_approx(fmaf(sv[k + 1], p.scale_log2, -mu));
                         a8[(i >> 1) & 7] += p0 + p1;
-                        pk[i >> 1] = pack_bf16x2(p0, p1);
+                        pk[k >> 1] = pack_bf16x2(p0, p1);
                     }
                     return ((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]));
                 };
-                auto store_p = [&]() {
+                // Half h of P over columns [32h, 32h + 32) of this tile's S
+                // buffer, then handed to the MMA warp: p_half releases the PV of
+                // keys 0..63 while the exponent pass of keys 64..127 runs, p_full
+                // the rest (warp-collective TMEM stores).  P overwrites the
+                // tile's only S buffer, which PV_{j-1} reads: that PV has landed,
+                // since the same thread issued it before QK_j, whose completion
+                // s_full reported.
+                auto publish_half = [&](int h, bool store) {
+                    if (store) {
 #pragma unroll
-                    for (int c = 0; c < kKvTile / 32; ++c)
-                        tmem_st16u(sa + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + c * 16));
+                        for (int c = 0; c < 2; ++c)
+                            tmem_st16u(sa + h * 32 + c * 16,
+                                       *reinterpret_cast<const uint32_t(*)[16]>(pk + h * 32 + c * 16));
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(h == 0 ? &p_half[x] : &p_full[x]);
                 };
-                // P overwrites the tile's only S buffer, which PV_{j-1} reads:
-                // that PV has landed, since the same thread issued it before
-                // QK_j, whose completion s_full reported.
                 // Static anchor ("Flywheel Attention", section 3.1 and appendix
                 // A): a row's anchor is the max of the first tile in which it sees
                 // a key and does not move on the fast path, so the exponent pass
                 // needs no running max.
                 // O *= alpha for this thread's row (warp-collective TMEM
-                // access; PV_{j-1} has landed, since S_j has).
+                // access; the caller makes sure no PV into O is in flight).
                 auto rescale_o = [&](float alpha) {
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
@@ -525,13 +546,82 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                     }
                     tmem_wait_st();
                 };
-                float tsum;
+                // Slow path of the static anchor: half h of a tile whose check
+                // failed in some row (warp-collective).  It works straight from
+                // TMEM, 32 columns at a time in rolled loops, so that the hot
+                // path carries neither its code nor its registers.  Rows with
+                // `over` move their anchor to the max of the scores still in
+                // TMEM (keys [64h, 128): the first half's P has overwritten keys
+                // 0..63 once published), l is rescaled -- and for h = 1 also the
+                // first half's sum t0, whose P already went to the MMA -- O is
+                // rescaled (for h = 1 once that half's PV has landed), and P of
+                // keys [64h, 64h + 64) is recomputed and written over columns
+                // [32h, 32h + 32).  Returns the half's new sum.
+                auto replay_half = [&](int h, bool over, bool rescale, float &t0) -> float {
+                    float ext = scale_pos ? kNegInf : -kNegInf;
+#pragma unroll 1
+                    for (int c = 2 * h; c < 4; ++c) {
+                        float v[32];
+                        tmem_ld32(sa + c * 32, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (key0 + c * 32 + i < lim) ext = scale_pos ? fmaxf(ext, v[i]) : fminf(ext, v[i]);
+                    }
+                    const float m_tile = (ext == kNegInf || ext == -kNegInf) ? kNegInf : ext * p.scale_log2;
+                    float alpha = 1.f;
+                    if (over) {
+                        const float m_new = fmaxf(m_ref, m_tile);
+                        alpha = ex2_approx(m_ref - m_new);
+                        l_sum *= alpha;
+                        if (h == 1) t0 *= alpha;
+                        m_ref = m_new;
+                    }
+                    if (h == 1) {
+                        mbar_wait(&pvh_done[x], s_cnt & 1u, wc);
+                        tc_fence_after();
+                    }
+                    if (rescale) {
+#pragma unroll 1
+                        for (int c = 0; c < D / 32; ++c) {
+                            float o[32];
+                            const uint32_t oa = tmem + lane_off + C::o_col(x) + c * 32;
+                            tmem_ld32(oa, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                            tmem_st32(oa, o);
+                        }
+                        tmem_wait_st();
+                    }
+                    const float mu = (m_ref == kNegInf) ? 0.f : m_ref;
+                    float sum = 0.f;
+#pragma unroll 1
+                    for (int c = 2 * h; c < 2 * h + 2; ++c) {
+                        float v[32];
+                        uint32_t q[16];
+                        tmem_ld32(sa + c * 32, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            const bool in0 = key0 + c * 32 + i < lim, in1 = key0 + c * 32 + i + 1 < lim;
+                            const float p0 = in0 ? ex2_approx(fmaf(v[i], p.scale_log2, -mu)) : 0.f;
+                            const float p1 = in1 ? ex2_approx(fmaf(v[i + 1], p.scale_log2, -mu)) : 0.f;
+                            sum += p0 + p1;
+                            q[i >> 1] = pack_bf16x2(p0, p1);
+                        }
+                        tmem_st16u(sa + c * 16, q);
+                    }
+                    return sum;
+                };
+                float tsum0, tsum1;
                 if constexpr (kOnline) {
                     // Online softmax with a conditional rescale ("Flywheel
                     // Attention", section 1): the tile's row max is taken every
                     // tile, and the base moves to it (l and O rescaled) only when
-                    // it rose more than kRescaleSlack above the base.
-                    const float m_tile = row_max();
+                    // it rose more than kRescaleSlack above the base.  PV_{j-1}
+                    // has landed, since S_j has.
+                    const float m_tile = row_max(0);
                     const bool up = m_tile > m_ref + kRescaleSlack;
                     if (__any_sync(0xffffffffu, up)) {
                         float alpha = 1.f;
@@ -542,43 +632,44 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                         }
                         if (j > 0) rescale_o(alpha);
                     }
-                    tsum = exp_pass(m_ref);
+                    tsum0 = exp_half(0, m_ref);
+                    publish_half(0, true);
+                    tsum1 = exp_half(1, m_ref);
+                    publish_half(1, true);
                 } else {
-                    if (m_ref == kNegInf) m_ref = row_max();
-                    tsum = exp_pass(m_ref);
-                    // The check: every p <= l, so a running sum within the budget
-                    // proves no score rose more than log2(budget) above the anchor
-                    // (appendix A, claim 2).  A row that fails (or overflowed)
-                    // replays the tile with the rescaling softmax: its anchor moves
-                    // to the new max, l and O are rescaled, P is recomputed before
-                    // the MMA sees it.  The scores come back from TMEM, which P
-                    // has not overwritten yet.
-                    const bool over = !(l_sum + tsum <= kAnchorBudget);
-                    const unsigned replay = __ballot_sync(0xffffffffu, over);
+                    if (m_ref == kNegInf) m_ref = row_max(0);
+                    // The check, once per half before the MMA sees it: every p <=
+                    // l, so a running sum within the budget proves no score rose
+                    // more than log2(budget) above the anchor (appendix A, claim
+                    // 2).  A row that fails (or overflowed) replays that half with
+                    // the rescaling softmax (prefill_replay_half): its anchor
+                    // moves to the new max, l and O are rescaled, P is recomputed.
+                    tsum0 = exp_half(0, m_ref);
+                    bool over = !(l_sum + tsum0 <= kAnchorBudget);
+                    unsigned replay = __ballot_sync(0xffffffffu, over);
                     if (replay) {
+                        // Nothing of this tile has reached the MMA, and PV_{j-1}
+                        // has landed, since S_j has.
                         if (lane == 0) count_events(p.counters, kCounterPrefillReplays, __popc(replay));
-                        // The scores are read twice so that they are not held in
-                        // registers across the O rescale.
-                        load_s();
-                        const float m_tile = row_max();
-                        float alpha = 1.f;
-                        if (over) {
-                            const float m_new = fmaxf(m_ref, m_tile);
-                            alpha = ex2_approx(m_ref - m_new);
-                            l_sum *= alpha;
-                            m_ref = m_new;
-                        }
-                        if (j > 0) rescale_o(alpha);
-                        load_s();
-                        tsum = exp_pass(m_ref);    // all lanes: unchanged rows recompute the same P
+                        tsum0 = replay_half(0, over, j > 0, tsum0);
+                        publish_half(0, false);
+                    } else {
+                        publish_half(0, true);
+                    }
+                    tsum1 = exp_half(1, m_ref);
+                    over = !(l_sum + tsum0 + tsum1 <= kAnchorBudget);
+                    replay = __ballot_sync(0xffffffffu, over);
+                    if (replay) {
+                        // The first half went out with the old anchor: it is
+                        // rescaled in O once its PV has landed (pvh_done).
+                        if (lane == 0) count_events(p.counters, kCounterPrefillReplays, __popc(replay));
+                        tsum1 = replay_half(1, over, true, tsum0);
+                        publish_half(1, false);
+                    } else {
+                        publish_half(1, true);
                     }
                 }
-                store_p();
-                l_sum += tsum;
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&p_full[x]);
+                l_sum += tsum0 + tsum1;
             }
             // ------------------------------------------------------ epilogue
             __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(p.out) +

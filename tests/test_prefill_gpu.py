@@ -147,6 +147,34 @@ def test_scale_extremes_exercise_anchor_replay(fw, scale, d):
         assert replays > 0, "the static-anchor check never replayed a tile"
 
 
+@pytest.mark.parametrize("pos", [10, 100])
+@pytest.mark.parametrize("d", [128, 256])
+def test_anchor_replay_in_either_half_of_a_tile(fw, pos, d):
+    """One key of the second KV tile scores ~50 log2 units above everything else
+    for every query row (a shared direction in Q and a large K entry), so every
+    row's running-sum check fails on that tile, with the key in the first (pos
+    10) or the second (pos 100) half of the tile's 128 keys.  At head dim 128
+    the softmax hands P to the MMA in two halves of 64 keys, so a failure in the
+    second half comes after the first half's PV went out with the old anchor and
+    is repaired in O; both must match the oracle."""
+    wl = wl_prefill(hq=4, hkv=2, d=d, causal=False, seed=43)
+    inp = make_prefill_inputs(wl, "cpu", [256, 40])
+    inp["q"][:, :, 0] = 2.0
+    big = 128 + pos
+    inp["k"][big] = 0.0
+    inp["k"][big, :, 0] = 200.0 * math.sqrt(d / 128)   # the same score after the 1/sqrt(d) scale
+    ref_o, ref_l, ref_a = oracle.varlen_prefill(inp["q"], inp["k"], inp["v"], inp["cu_seqlens_q"], inp["cu_seqlens_k"],
+                                                wl.causal, wl.scale, with_absv=True)
+    dev = to_device(inp)
+    fw.read_counters()                                   # reset
+    out, lse = fw.varlen_prefill(dev["q"], dev["k"], dev["v"], dev["cu_seqlens_q"], dev["cu_seqlens_k"], wl.causal,
+                                 wl.scale)
+    torch.cuda.synchronize()
+    assert fw.device_status() == 0
+    assert fw.read_counters()["prefill_replays"] >= 256 * 4, "every row of the first sequence replays once"
+    compare(out.reshape(-1, out.shape[-1]), lse.reshape(-1), ref_o, ref_l, f"planted key at {pos}", absv=ref_a)
+
+
 @pytest.fixture
 def online(fw):
     """The prefill in its online-softmax mode (conditional rescale) for one test."""
