@@ -68,7 +68,23 @@ constexpr int kOffP = kOffQ + kQBytes;
 constexpr int kOffRing = kOffP + kPBytes;
 constexpr int kOffRot = kOffRing + kSlots * kSlotBytes;
 constexpr int kOffBar = kOffRot + kHalfBytes;
-constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 1 + 1 + 2 + 1 + 2 + 1;
+// mbarrier array: index of each group (every pointer derives from these, so
+// the count cannot drift from the layout)
+constexpr int kBarSlotFull = 0;                        // [kSlots], CTA 0's count both CTAs' copies
+constexpr int kBarSlotEmpty = kBarSlotFull + kSlots;   // [kSlots]
+constexpr int kBarRotFull = kBarSlotEmpty + kSlots;    // [1], CTA 0's
+constexpr int kBarRotEmpty = kBarRotFull + 1;          // [1]
+constexpr int kBarQFull = kBarRotEmpty + 1;            // [1], CTA 0's
+constexpr int kBarQEmpty = kBarQFull + 1;              // [1]
+constexpr int kBarSFull = kBarQEmpty + 1;              // [2]
+constexpr int kBarSFree = kBarSFull + 2;               // [2], CTA 0's count both CTAs' softmax warps
+constexpr int kBarPFull = kBarSFree + 2;               // [1], CTA 0's: one arrival per CTA once its P^T is whole
+constexpr int kBarPvDone = kBarPFull + 1;              // [1]: PV j landed (frees both CTAs' P^T)
+constexpr int kBarX = kBarPvDone + 1;                  // [2]: the partner's part of an exchange arrived
+constexpr int kBarDrain = kBarX + 2;                   // [1]
+constexpr int kBarTail = kBarDrain + 1;                // [2]: a producer warp's landing of a value chunk with a tail
+constexpr int kBarPTx = kBarTail + 2;                  // [1]: the partner's P^T rows landed in this CTA
+constexpr int kNumBars = kBarPTx + 1;
 constexpr int kThreads = 352;                          // 11 warps: see the roles below
 constexpr int kOffX = kOffBar + ((kNumBars * 8 + 127) / 128) * 128;
 constexpr int kOffRed = kOffX + (2 * 128 + 32) * 4;    // xr[2][128] from the partner, xf[2] + pad
@@ -114,20 +130,20 @@ latent_pair_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_c
     uint8_t *sRing = smem + kOffRing;
     uint8_t *sRot = smem + kOffRot;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
-    uint64_t *slot_full = bars;                    // CTA 0's count both CTAs' copies
-    uint64_t *slot_empty = slot_full + kSlots;
-    uint64_t *rot_full = slot_empty + kSlots;      // [1], CTA 0's
-    uint64_t *rot_empty = rot_full + 2;            // [1]
-    uint64_t *q_full = rot_empty + 2;              // [1], CTA 0's
-    uint64_t *q_empty = q_full + 1;                // [1]
-    uint64_t *s_full = q_empty + 1;                // [2]
-    uint64_t *s_free = s_full + 2;                 // [2], CTA 0's count both CTAs' softmax warps
-    uint64_t *p_full = s_free + 2;                 // [1], CTA 0's: one arrival per CTA once its P^T is whole
-    uint64_t *pv_done = p_full + 1;                // [1]: PV j landed (frees both CTAs' P^T)
-    uint64_t *xbar = pv_done + 1;                  // [2]: the partner's part of an exchange arrived
-    uint64_t *drain = xbar + 2;                    // [1]
-    uint64_t *tail_bar = drain + 1;                // [2]: a producer warp's landing of a value chunk with a tail
-    uint64_t *p_tx = tail_bar + 2;                 // [1]: the partner's P^T rows landed in this CTA
+    uint64_t *slot_full = bars + kBarSlotFull;
+    uint64_t *slot_empty = bars + kBarSlotEmpty;
+    uint64_t *rot_full = bars + kBarRotFull;
+    uint64_t *rot_empty = bars + kBarRotEmpty;
+    uint64_t *q_full = bars + kBarQFull;
+    uint64_t *q_empty = bars + kBarQEmpty;
+    uint64_t *s_full = bars + kBarSFull;
+    uint64_t *s_free = bars + kBarSFree;
+    uint64_t *p_full = bars + kBarPFull;
+    uint64_t *pv_done = bars + kBarPvDone;
+    uint64_t *xbar = bars + kBarX;
+    uint64_t *drain = bars + kBarDrain;
+    uint64_t *tail_bar = bars + kBarTail;
+    uint64_t *p_tx = bars + kBarPTx;
     float *xr = reinterpret_cast<float *>(smem + kOffX);           // [2][128] written by the partner
     uint32_t *xf = reinterpret_cast<uint32_t *>(xr + 2 * 128);     // [2] partner's flag
     float *red = reinterpret_cast<float *>(smem + kOffRed);        // [4][128] per-quadrant row partials

@@ -59,7 +59,20 @@ struct PrefillCfg {
     static constexpr int kOffQ = 0;
     static constexpr int kOffRing = kOffQ + kNumQ * kTileBytes;
     static constexpr int kOffBar = kOffRing + kSlots * kSlotBytes;
-    static constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 2 + 2 + 2 + 2;
+    // mbarrier array: index of each group (every pointer below derives from
+    // these, so the count cannot drift from the layout)
+    static constexpr int kBarSlotFull = 0;                      // [kSlots]
+    static constexpr int kBarSlotEmpty = kBarSlotFull + kSlots;  // [kSlots]
+    static constexpr int kBarQFull = kBarSlotEmpty + kSlots;     // [1]
+    static constexpr int kBarQEmpty = kBarQFull + 1;             // [1]
+    static constexpr int kBarSFull = kBarQEmpty + 1;             // [2] per query tile
+    static constexpr int kBarPFull = kBarSFull + 2;              // [2]
+    static constexpr int kBarPvDone = kBarPFull + 2;             // [2]
+    static constexpr int kBarDrain = kBarPvDone + 2;             // [2]
+    static constexpr int kBarIssued = kBarDrain + 2;             // [2]
+    static constexpr int kBarPHalf = kBarIssued + 2;             // [2]
+    static constexpr int kBarPvhDone = kBarPHalf + 2;            // [2]
+    static constexpr int kNumBars = kBarPvhDone + 2;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA exceeded");
@@ -181,17 +194,17 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
     uint8_t *sQ = smem + C::kOffQ;
     uint8_t *sRing = smem + C::kOffRing;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
-    uint64_t *slot_full = bars;
-    uint64_t *slot_empty = slot_full + C::kSlots;
-    uint64_t *q_full = slot_empty + C::kSlots;      // [1]
-    uint64_t *q_empty = q_full + 2;                  // [1]
-    uint64_t *s_full = q_empty + 2;                  // [2]
-    uint64_t *p_full = s_full + 2;                   // [2]
-    uint64_t *pv_done = p_full + 2;                  // [2]
-    uint64_t *drain = pv_done + 2;                   // [2]
-    uint64_t *issued = drain + 2;                    // [2]: step handoff between the two issuers
-    uint64_t *p_half = issued + 2;                   // [2]: first half of P (keys 0..63) written
-    uint64_t *pvh_done = p_half + 2;                 // [2]: the PV of that half complete
+    uint64_t *slot_full = bars + C::kBarSlotFull;
+    uint64_t *slot_empty = bars + C::kBarSlotEmpty;
+    uint64_t *q_full = bars + C::kBarQFull;
+    uint64_t *q_empty = bars + C::kBarQEmpty;
+    uint64_t *s_full = bars + C::kBarSFull;
+    uint64_t *p_full = bars + C::kBarPFull;
+    uint64_t *pv_done = bars + C::kBarPvDone;
+    uint64_t *drain = bars + C::kBarDrain;
+    uint64_t *issued = bars + C::kBarIssued;         // step handoff between the two issuers
+    uint64_t *p_half = bars + C::kBarPHalf;          // first half of P (keys 0..63) written
+    uint64_t *pvh_done = bars + C::kBarPvhDone;      // the PV of that half complete
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
 
@@ -734,7 +747,16 @@ constexpr int kPairSlotBytes = 32768;          // half a K tile (64 x 256) or ha
 constexpr int kPairQBytes = 128 * 256 * 2;
 constexpr int kPairOffRing = kPairQBytes;
 constexpr int kPairOffBar = kPairOffRing + kPairSlots * kPairSlotBytes;
-constexpr int kPairNumBars = 2 * kPairSlots + 2 + 2 + 2 + 2 + 2 + 2;
+// mbarrier array of the pair kernel, as above
+constexpr int kPairBarSlotFull = 0;                            // [kPairSlots]
+constexpr int kPairBarSlotEmpty = kPairBarSlotFull + kPairSlots;  // [kPairSlots]
+constexpr int kPairBarQFull = kPairBarSlotEmpty + kPairSlots;  // [1]
+constexpr int kPairBarQEmpty = kPairBarQFull + 1;              // [1]
+constexpr int kPairBarSFull = kPairBarQEmpty + 1;              // [2]
+constexpr int kPairBarPFull = kPairBarSFull + 2;               // [2]
+constexpr int kPairBarPvDone = kPairBarPFull + 2;              // [2]
+constexpr int kPairBarDrain = kPairBarPvDone + 2;              // [1]
+constexpr int kPairNumBars = kPairBarDrain + 1;
 constexpr int kPairOffMisc = kPairOffBar + kPairNumBars * 8;
 constexpr int kPairSmemBytes = kPairOffMisc + 16 + 1024;
 static_assert(kPairSmemBytes <= 232448, "shared memory budget of one CTA exceeded");
@@ -757,14 +779,14 @@ varlen_prefill_pair_kernel(const __grid_constant__ PrefillParams p, const __grid
     uint8_t *sQ = smem;
     uint8_t *sRing = smem + kPairOffRing;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kPairOffBar);
-    uint64_t *slot_full = bars;                          // CTA 0's count both CTAs' copies
-    uint64_t *slot_empty = slot_full + kPairSlots;
-    uint64_t *q_full = slot_empty + kPairSlots;          // [1], CTA 0's counts both Q tiles
-    uint64_t *q_empty = q_full + 2;                      // [1]
-    uint64_t *s_full = q_empty + 2;                      // [2]
-    uint64_t *p_full = s_full + 2;                       // [2], CTA 0's: its 4 warps + one arrival of CTA 1
-    uint64_t *pv_done = p_full + 2;                      // [2]
-    uint64_t *drain = pv_done + 2;                       // [1]: CTA 0's MMAs all complete
+    uint64_t *slot_full = bars + kPairBarSlotFull;       // CTA 0's count both CTAs' copies
+    uint64_t *slot_empty = bars + kPairBarSlotEmpty;
+    uint64_t *q_full = bars + kPairBarQFull;             // CTA 0's counts both Q tiles
+    uint64_t *q_empty = bars + kPairBarQEmpty;
+    uint64_t *s_full = bars + kPairBarSFull;
+    uint64_t *p_full = bars + kPairBarPFull;             // CTA 0's: its 4 warps + one arrival of CTA 1
+    uint64_t *pv_done = bars + kPairBarPvDone;
+    uint64_t *drain = bars + kPairBarDrain;              // CTA 0's MMAs all complete
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kPairOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kPairOffMisc + 4);
 
