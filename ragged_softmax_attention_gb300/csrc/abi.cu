@@ -245,7 +245,7 @@ fw_status_t plan_decode(int32_t B, int32_t q_len, int32_t Hq, int32_t Hkv, int32
     }
     p.num_units = (int64_t)B * Hkv * p.row_groups;
     const int64_t tiles_max = (max_kv_len + fw::kKvTile - 1) / fw::kKvTile;
-    if (p.num_units * (tiles_max > 0 ? tiles_max : 1) >= (1LL << 31))
+    if (p.num_units * ((tiles_max > 0 ? tiles_max : 1) + fw::kDecodePieceCostFp8) >= (1LL << 31))
         return fail(FW_ERR_UNSUPPORTED, "decode too large for 32-bit tile indices");
     int64_t span = g_opt_chunk > 0 ? (g_opt_chunk + fw::kKvTile - 1) / fw::kKvTile
                                    : (latent ? fw::kLatentMinSpan : fw::kDecodeMinSpan);
@@ -676,6 +676,7 @@ static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_
     p.status = d->status;
     p.counters = d->counters;
     p.test_stall = g_opt_test_stall ? 1 : 0;
+    p.piece_cost = latent ? 0 : kv8 ? fw::kDecodePieceCostFp8 : fw::kDecodePieceCostBf16;
 
     CUtensorMap tq, tk, tv;
     if (p.packed) {

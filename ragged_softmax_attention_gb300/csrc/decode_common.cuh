@@ -57,40 +57,50 @@ struct PieceIter {
     }
     __device__ bool next(const DecodeParams &p, Unit &x) {
         const int32_t *PB = p.plan + 2;
-        while (pos >= end) {
-            range += gridDim.x;
-            if ((long long)range * span >= T) return false;
-            open_range();
-        }
-        if (b < 0 || pos >= __ldg(PB + b + 1)) {
-            int lo = 0, hi = p.B - 1;              // largest b with PB[b] <= pos
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (__ldg(PB + mid) <= pos) lo = mid; else hi = mid - 1;
+        for (;;) {
+            while (pos >= end) {
+                range += gridDim.x;
+                if ((long long)range * span >= T) return false;
+                open_range();
             }
-            b = lo;
+            if (b < 0 || pos >= __ldg(PB + b + 1)) {
+                int lo = 0, hi = p.B - 1;              // largest b with PB[b] <= pos
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (__ldg(PB + mid) <= pos) lo = mid; else hi = mid - 1;
+                }
+                b = lo;
+            }
+            // Row b holds units_per_row units of vb slots: piece_cost empty
+            // ones, then the unit's tb tiles.
+            const int pb0 = __ldg(PB + b);
+            const int vb = (__ldg(PB + b + 1) - pb0) / p.units_per_row;
+            const int off = pos - pb0;
+            const int u = off / vb;
+            const int vl = off - u * vb;
+            if (vl < p.piece_cost) {                   // empty slots carry no tiles
+                pos += p.piece_cost - vl;
+                continue;
+            }
+            const int tb = vb - p.piece_cost;
+            const int tl = vl - p.piece_cost;
+            const int th = min(tb, tl + (end - pos));
+            const int pstart = pb0 + u * vb + p.piece_cost;   // the unit's first tile
+            x.b = b;
+            x.g = u / p.row_groups;
+            x.rg = u - x.g * p.row_groups;
+            x.n = clamp_len(p, __ldg(p.seq_lens + b));
+            x.lo = window_first_key(p, x.n);
+            const int t0 = x.lo / kKvTile;               // the walk starts at the window's first tile
+            x.k_begin = (t0 + tl) * kKvTile;
+            x.k_end = min(x.n, (t0 + th) * kKvTile);
+            x.ntiles = th - tl;
+            x.k = (pstart + tl) / span - pstart / span;
+            x.npieces = (pstart + tb - 1) / span - pstart / span + 1;
+            x.single = (x.npieces == 1);
+            pos += th - tl;
+            return true;
         }
-        const int pb0 = __ldg(PB + b);
-        const int tb = (__ldg(PB + b + 1) - pb0) / p.units_per_row;
-        const int off = pos - pb0;
-        const int u = off / tb;
-        const int tl = off - u * tb;
-        const int th = min(tb, tl + (end - pos));
-        const int pstart = pb0 + u * tb;
-        x.b = b;
-        x.g = u / p.row_groups;
-        x.rg = u - x.g * p.row_groups;
-        x.n = clamp_len(p, __ldg(p.seq_lens + b));
-        x.lo = window_first_key(p, x.n);
-        const int t0 = x.lo / kKvTile;               // the walk starts at the window's first tile
-        x.k_begin = (t0 + tl) * kKvTile;
-        x.k_end = min(x.n, (t0 + th) * kKvTile);
-        x.ntiles = th - tl;
-        x.k = (pstart + tl) / span - pstart / span;
-        x.npieces = (pstart + tb - 1) / span - pstart / span + 1;
-        x.single = (x.npieces == 1);
-        pos += th - tl;
-        return true;
     }
 };
 
@@ -127,41 +137,50 @@ struct LatentIter {
     }
     __device__ bool next(const DecodeParams &p, LatentPiece &x) {
         const int32_t *PB = p.plan + 2;
-        while (pos >= end) {
-            range += step;
-            if ((long long)range * span >= T) return false;
-            open_range();
-        }
-        if (b < 0 || pos >= __ldg(PB + b + 1)) {
-            int lo = 0, hi = p.B - 1;              // largest b with PB[b] <= pos
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (__ldg(PB + mid) <= pos) lo = mid; else hi = mid - 1;
+        for (;;) {
+            while (pos >= end) {
+                range += step;
+                if ((long long)range * span >= T) return false;
+                open_range();
             }
-            b = lo;
+            if (b < 0 || pos >= __ldg(PB + b + 1)) {
+                int lo = 0, hi = p.B - 1;              // largest b with PB[b] <= pos
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (__ldg(PB + mid) <= pos) lo = mid; else hi = mid - 1;
+                }
+                b = lo;
+            }
+            // As in PieceIter: units of vb slots, piece_cost empty ones first.
+            const int pb0 = __ldg(PB + b);
+            const int vb = (__ldg(PB + b + 1) - pb0) / p.units_per_row;
+            const int off = pos - pb0;
+            const int u = off / vb;
+            const int vl = off - u * vb;
+            if (vl < p.piece_cost) {
+                pos += p.piece_cost - vl;
+                continue;
+            }
+            const int tb = vb - p.piece_cost;
+            const int tl = vl - p.piece_cost;
+            const int th = min(tb, tl + (end - pos));
+            const int pstart = pb0 + u * vb + p.piece_cost;
+            x.b = b;
+            x.g = u;
+            x.row0 = rg * p.rows;
+            x.t = x.row0 / p.G;
+            x.h0 = u * p.G + x.row0 % p.G;
+            x.n = clamp_len(p, __ldg(p.seq_lens + b));
+            x.lo = window_first_key(p, x.n);
+            const int t0 = x.lo / kKvTile;               // the walk starts at the window's first tile
+            x.k_begin = (t0 + tl) * kKvTile;
+            x.k_end = min(x.n, (t0 + th) * kKvTile);
+            x.ntiles = th - tl;
+            x.k = (pstart + tl) / span - pstart / span;
+            x.single = ((pstart + tb - 1) / span == pstart / span);
+            pos += th - tl;
+            return true;
         }
-        const int pb0 = __ldg(PB + b);
-        const int tb = (__ldg(PB + b + 1) - pb0) / p.units_per_row;
-        const int off = pos - pb0;
-        const int u = off / tb;
-        const int tl = off - u * tb;
-        const int th = min(tb, tl + (end - pos));
-        const int pstart = pb0 + u * tb;
-        x.b = b;
-        x.g = u;
-        x.row0 = rg * p.rows;
-        x.t = x.row0 / p.G;
-        x.h0 = u * p.G + x.row0 % p.G;
-        x.n = clamp_len(p, __ldg(p.seq_lens + b));
-        x.lo = window_first_key(p, x.n);
-        const int t0 = x.lo / kKvTile;               // the walk starts at the window's first tile
-        x.k_begin = (t0 + tl) * kKvTile;
-        x.k_end = min(x.n, (t0 + th) * kKvTile);
-        x.ntiles = th - tl;
-        x.k = (pstart + tl) / span - pstart / span;
-        x.single = ((pstart + tb - 1) / span == pstart / span);
-        pos += th - tl;
-        return true;
     }
 };
 

@@ -599,7 +599,8 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const __grid_constant
     for (int base = 0; base < p.B; base += 1024) {
         const int b = base + tid;
         const int n = b < p.B ? clamp_len(p, __ldg(p.seq_lens + b)) : 0;
-        const int t = row_tiles(p, n) * p.units_per_row;
+        const int rt = row_tiles(p, n);
+        const int t = rt > 0 ? (p.piece_cost + rt) * p.units_per_row : 0;   // each unit: empty slots, then its tiles
         int incl = t;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -669,14 +670,15 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ De
     const int32_t *PB = p.plan + 2;
     const int span = max(1, __ldg(p.plan + 1));
     const int pb0 = __ldg(PB + b);
-    const int tb = (__ldg(PB + b + 1) - pb0) / p.units_per_row;
-    if (tb == 0) return;                             // empty row: written by the plan kernel
+    const int vb = (__ldg(PB + b + 1) - pb0) / p.units_per_row;   // slots per unit
+    if (vb == 0) return;                             // empty row: written by the plan kernel
+    const int tb = vb - p.piece_cost;
     const int g = h / p.G;
     // Row groups that ride on the CTA index share their unit's tile range.
     const int rg = p.range_groups > 1 ? 0
                  : p.head_mode == 0 ? t / p.tokens_per_unit
                                     : t * p.head_chunks + (h - g * p.G) / p.rows;
-    const int pstart = pb0 + (g * (p.range_groups > 1 ? 1 : p.row_groups) + rg) * tb;
+    const int pstart = pb0 + (g * (p.range_groups > 1 ? 1 : p.row_groups) + rg) * vb + p.piece_cost;
     const int npieces = (pstart + tb - 1) / span - pstart / span + 1;
     if (npieces <= 1) return;
     const float *lse_row = p.ws_lse + row * p.max_pieces;

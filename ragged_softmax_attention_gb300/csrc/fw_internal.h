@@ -36,6 +36,14 @@ constexpr int kSoftmaxStartWarp = 2;  // decode: warps 2..5 run the softmax / ep
 
 constexpr int kDecodeMinSpan = 8;     // decode: fewest KV tiles one CTA range holds (auto mode)
 constexpr int kLatentMinSpan = 32;    // latent-head decode: the same, for its heavier tiles
+// What starting a piece costs a decode CTA, in KV tiles of streaming (the
+// next unit's Q, the pipeline refill, the previous piece's epilogue): a
+// clock64 trace of the FP8 kernel puts a piece boundary at ~8,400 cycles
+// against ~1,425 per tile inside a piece.  The planned tile sequence gives
+// every unit this many empty slots before its tiles, so equal ranges of it
+// carry equal work, piece starts included.
+constexpr int kDecodePieceCostBf16 = 3;
+constexpr int kDecodePieceCostFp8 = 5;
 constexpr int kLatentRows = 64;       // latent-head decode: query heads per CTA (MMA N of one CTA)
 constexpr int kLatentPairRows = 128;  // latent-head decode on CTA pairs: query heads per pair
 
@@ -98,6 +106,7 @@ struct DecodeParams {
     int *status;                               // device status word
     unsigned long long *counters;              // device event counters (FW_COUNTER_*)
     int test_stall;                            // test hook: the producer first waits on a barrier nothing completes
+    int piece_cost;                            // empty slots before each unit's tiles in the planned sequence
 };
 
 // One varlen prefill launch.  The plan kernel lists the units (sequence,
