@@ -339,11 +339,14 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
         PieceIter it;
         it.init(p);
         Unit x;
-        while (it.next(p, x)) {
-            const int qs = ju & 1;
-            // ---- query terms: BF16 row * 2^e = hi + mid, both E4M3
-            mbar_wait(&q16_full[qs], (ju >> 1) & 1, wc);
-            mbar_wait(&q8_free[qs], ((ju >> 1) & 1) ^ 1, wc);
+        // ---- query terms of unit nu: BF16 row * 2^e = hi + mid, both E4M3.
+        // Built for the next unit before this unit's epilogue, so that the
+        // MMA warp can start the next unit's QK^T while the epilogue waits
+        // for the last PV and writes O.
+        auto build_q8 = [&](int nu) {
+            const int qs = nu & 1;
+            mbar_wait(&q16_full[qs], (nu >> 1) & 1, wc);
+            mbar_wait(&q8_free[qs], ((nu >> 1) & 1) ^ 1, wc);
             {
                 constexpr int TPR = kSoftmaxThreads / NQ;          // threads per query row
                 constexpr int EPT = D / TPR;                       // elements per thread (8 or 16)
@@ -399,7 +402,12 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) { mbar_arrive(&q16_free[qs]); mbar_arrive(&q8_full[qs]); }
-            named_bar_sync(3, kSoftmaxThreads);                   // q_exp of this unit visible
+            named_bar_sync(3, kSoftmaxThreads);                   // q_exp of unit nu visible
+        };
+        bool have = it.next(p, x);
+        if (have) build_q8(0);
+        while (have) {
+            const int qs = ju & 1;
             int lim[RH];
             float rs[RH];
             int nrows = 0;
@@ -520,6 +528,9 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[pb]);
             }
+            Unit nx;
+            const bool next_unit = it.next(p, nx);
+            if (next_unit) build_q8(ju + 1);
             // ------------------------------------------------------ epilogue
             {
                 warp_rows_reduce<RH, false>(l_part, lane, red_sum + q4 * R + r0);
@@ -582,6 +593,8 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                 named_bar_sync(1 + half, 128);
             }
             ++ju;
+            x = nx;
+            have = next_unit;
         }
     }
 

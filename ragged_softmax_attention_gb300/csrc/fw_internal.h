@@ -42,7 +42,7 @@ constexpr int kLatentMinSpan = 32;    // latent-head decode: the same, for its h
 // against ~1,425 per tile inside a piece.  The planned tile sequence gives
 // every unit this many empty slots before its tiles, so equal ranges of it
 // carry equal work, piece starts included.
-constexpr int kDecodePieceCostBf16 = 3;
+constexpr int kDecodePieceCostBf16 = 4;
 constexpr int kDecodePieceCostFp8 = 5;
 constexpr int kLatentRows = 64;       // latent-head decode: query heads per CTA (MMA N of one CTA)
 constexpr int kLatentPairRows = 128;  // latent-head decode on CTA pairs: query heads per pair
