@@ -117,7 +117,10 @@ struct LatentPiece {
 // ranges idx / R, idx / R + count / R, ... over the units laid end to end in
 // tile order, for row group idx % R (R = range_groups), so the R workers that
 // read the same keys run side by side.  Every role runs its own copy and
-// sees the same sequence.
+// sees the same sequence.  Latent plans carry no empty slots
+// (piece_cost = 0: the host never sets it for them), so a unit's slots are its
+// tiles; keeping that case out of this walk keeps the pair kernel's roles
+// within their registers.
 struct LatentIter {
     int T, span, range, step, pos, end, b, rg;
 
@@ -137,50 +140,41 @@ struct LatentIter {
     }
     __device__ bool next(const DecodeParams &p, LatentPiece &x) {
         const int32_t *PB = p.plan + 2;
-        for (;;) {
-            while (pos >= end) {
-                range += step;
-                if ((long long)range * span >= T) return false;
-                open_range();
-            }
-            if (b < 0 || pos >= __ldg(PB + b + 1)) {
-                int lo = 0, hi = p.B - 1;              // largest b with PB[b] <= pos
-                while (lo < hi) {
-                    const int mid = (lo + hi + 1) >> 1;
-                    if (__ldg(PB + mid) <= pos) lo = mid; else hi = mid - 1;
-                }
-                b = lo;
-            }
-            // As in PieceIter: units of vb slots, piece_cost empty ones first.
-            const int pb0 = __ldg(PB + b);
-            const int vb = (__ldg(PB + b + 1) - pb0) / p.units_per_row;
-            const int off = pos - pb0;
-            const int u = off / vb;
-            const int vl = off - u * vb;
-            if (vl < p.piece_cost) {
-                pos += p.piece_cost - vl;
-                continue;
-            }
-            const int tb = vb - p.piece_cost;
-            const int tl = vl - p.piece_cost;
-            const int th = min(tb, tl + (end - pos));
-            const int pstart = pb0 + u * vb + p.piece_cost;
-            x.b = b;
-            x.g = u;
-            x.row0 = rg * p.rows;
-            x.t = x.row0 / p.G;
-            x.h0 = u * p.G + x.row0 % p.G;
-            x.n = clamp_len(p, __ldg(p.seq_lens + b));
-            x.lo = window_first_key(p, x.n);
-            const int t0 = x.lo / kKvTile;               // the walk starts at the window's first tile
-            x.k_begin = (t0 + tl) * kKvTile;
-            x.k_end = min(x.n, (t0 + th) * kKvTile);
-            x.ntiles = th - tl;
-            x.k = (pstart + tl) / span - pstart / span;
-            x.single = ((pstart + tb - 1) / span == pstart / span);
-            pos += th - tl;
-            return true;
+        while (pos >= end) {
+            range += step;
+            if ((long long)range * span >= T) return false;
+            open_range();
         }
+        if (b < 0 || pos >= __ldg(PB + b + 1)) {
+            int lo = 0, hi = p.B - 1;              // largest b with PB[b] <= pos
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (__ldg(PB + mid) <= pos) lo = mid; else hi = mid - 1;
+            }
+            b = lo;
+        }
+        const int pb0 = __ldg(PB + b);
+        const int tb = (__ldg(PB + b + 1) - pb0) / p.units_per_row;
+        const int off = pos - pb0;
+        const int u = off / tb;
+        const int tl = off - u * tb;
+        const int th = min(tb, tl + (end - pos));
+        const int pstart = pb0 + u * tb;
+        x.b = b;
+        x.g = u;
+        x.row0 = rg * p.rows;
+        x.t = x.row0 / p.G;
+        x.h0 = u * p.G + x.row0 % p.G;
+        x.n = clamp_len(p, __ldg(p.seq_lens + b));
+        x.lo = window_first_key(p, x.n);
+        const int t0 = x.lo / kKvTile;               // the walk starts at the window's first tile
+        x.k_begin = (t0 + tl) * kKvTile;
+        x.k_end = min(x.n, (t0 + th) * kKvTile);
+        x.ntiles = th - tl;
+        x.k = (pstart + tl) / span - pstart / span;
+        x.single = ((pstart + tb - 1) / span == pstart / span);
+        pos += th - tl;
+        return true;
     }
 };
 
