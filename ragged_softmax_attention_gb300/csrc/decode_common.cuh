@@ -63,13 +63,18 @@ struct PieceIter {
                 if ((long long)range * span >= T) return false;
                 open_range();
             }
-            if (b < 0 || pos >= __ldg(PB + b + 1)) {
+            if (b < 0) {
                 int lo = 0, hi = p.B - 1;              // largest b with PB[b] <= pos
                 while (lo < hi) {
                     const int mid = (lo + hi + 1) >> 1;
                     if (__ldg(PB + mid) <= pos) lo = mid; else hi = mid - 1;
                 }
                 b = lo;
+            } else {
+                // Within a range the walk only moves forward, mostly into the
+                // next row: a scan costs one dependent load per row crossed,
+                // where a fresh binary search costs log2(B).
+                while (pos >= __ldg(PB + b + 1)) ++b;
             }
             // Row b holds units_per_row units of vb slots: piece_cost empty
             // ones, then the unit's tb tiles.

@@ -404,20 +404,65 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
             if (lane == 0) { mbar_arrive(&q16_free[qs]); mbar_arrive(&q8_full[qs]); }
             named_bar_sync(3, kSoftmaxThreads);                   // q_exp of unit nu visible
         };
-        bool have = it.next(p, x);
-        if (have) build_q8(0);
-        while (have) {
-            const int qs = ju & 1;
-            int lim[RH];
-            float rs[RH];
-            int nrows = 0;
+        // Token, head and visible-key bound of this warp's rows of a unit.
+        // Warps of up to 4 rows work them out for the next unit while the
+        // current one runs (with the next unit's descriptor, fetched then
+        // too), so a piece boundary waits on neither; wider warps, short of
+        // registers, work them out at the unit's start and again in its
+        // epilogue.
+        constexpr bool kKeepRows = RH <= 4;
+        constexpr int KR = kKeepRows ? RH : 1;
+        struct Rows {
+            int t[KR], h[KR], lim[RH];
+            unsigned ok;
+            int nrows;
+        };
+        auto rows_of = [&](const Unit &u, Rows &w) {
+            w.ok = 0;
+            w.nrows = 0;
 #pragma unroll
             for (int r = 0; r < RH; ++r) {
                 int t, h;
-                const bool ok = unit_row(p, x, r0 + r, t, h);
-                lim[r] = ok ? (p.causal ? min(x.n, x.n - p.q_len + t + 1) : x.n) : 0;
-                if (ok) nrows = r + 1;
+                const bool ok = unit_row(p, u, r0 + r, t, h);
+                if constexpr (kKeepRows) {
+                    w.t[r] = t;
+                    w.h[r] = h;
+                }
+                if (ok) { w.ok |= 1u << r; w.nrows = r + 1; }
+                w.lim[r] = ok ? (p.causal ? min(u.n, u.n - p.q_len + t + 1) : u.n) : 0;
+            }
+        };
+        bool have = it.next(p, x);
+        if (have) build_q8(0);
+        Rows cur, nxt;
+        if (have) rows_of(x, cur);
+        Unit nx;
+        while (have) {
+            const int qs = ju & 1;
+            if (!kKeepRows) rows_of(x, cur);
+            const int nrows = cur.nrows;
+            const unsigned row_ok = cur.ok;
+            int lim[RH];
+            float rs[RH];
+#pragma unroll
+            for (int r = 0; r < RH; ++r) {
+                lim[r] = cur.lim[r];
                 rs[r] = p.scale_log2 * __int_as_float((127 - q_exp[qs * NQ + r0 + r]) << 23);
+            }
+            auto row_of = [&](int r, int &t, int &h) -> bool {
+                if constexpr (kKeepRows) {
+                    t = cur.t[r];
+                    h = cur.h[r];
+                    return (row_ok >> r) & 1u;
+                } else {
+                    return unit_row(p, x, r0 + r, t, h);
+                }
+            };
+            // The next unit's descriptor (and rows), while this unit runs.
+            bool next_unit = false;
+            if constexpr (kKeepRows) {
+                next_unit = it.next(p, nx);
+                if (next_unit) rows_of(nx, nxt);
             }
             // Sliding window: a row with visible-key bound lim sees keys
             // lim - 1 - W .. lim - 1, i.e. lim - tok <= W + 1.
@@ -528,8 +573,7 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[pb]);
             }
-            Unit nx;
-            const bool next_unit = it.next(p, nx);
+            if constexpr (!kKeepRows) next_unit = it.next(p, nx);
             if (next_unit) build_q8(ju + 1);
             // ------------------------------------------------------ epilogue
             {
@@ -560,7 +604,7 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
 #pragma unroll
                 for (int r = 0; r < RH; ++r) {
                     int t, h;
-                    if (r >= nrows || !unit_row(p, x, r0 + r, t, h)) continue;
+                    if (r >= nrows || !row_of(r, t, h)) continue;
                     const float val = L[r] > 0.f ? o[r] / L[r] * p.out_scale : 0.f;
                     if (x.single) {
                         __nv_bfloat16 *op = reinterpret_cast<__nv_bfloat16 *>(p.out) + x.b * p.out_stride[0] +
@@ -571,14 +615,17 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                         p.ws_o[(row * p.max_pieces + x.k) * D + dv] = val;
                     }
                 }
-                if (q4 == 0 && lane < nrows) {
+                if (q4 == 0 && lane < nrows && ((row_ok >> lane) & 1u)) {
                     const int r = lane;
-                    int t, h;
-                    if (unit_row(p, x, r0 + r, t, h)) {
+                    {
+                        int t = 0, h = 0;
                         float lse2 = kNegInf;
 #pragma unroll
-                        for (int k = 0; k < RH; ++k)
-                            if (k == r && L[k] > 0.f) lse2 = m_ref[k] - kHeadroom + __log2f(L[k]);
+                        for (int k = 0; k < RH; ++k) {
+                            if (k != r) continue;
+                            row_of(k, t, h);
+                            if (L[k] > 0.f) lse2 = m_ref[k] - kHeadroom + __log2f(L[k]);
+                        }
                         if (x.single) {
                             if (p.lse)
                                 p.lse[x.b * p.lse_stride[0] + t * p.lse_stride[1] + h * p.lse_stride[2]] =
@@ -594,6 +641,7 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
             }
             ++ju;
             x = nx;
+            if (kKeepRows) cur = nxt;
             have = next_unit;
         }
     }
