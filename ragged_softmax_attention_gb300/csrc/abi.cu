@@ -874,7 +874,7 @@ fw_status_t fw_varlen_prefill(const fw_tensor_t *q, const fw_tensor_t *k, const 
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceState *d = nullptr;
     if (fw_status_t s = device_state(&d)) return s;
-    const int64_t plan_bytes = ((B + 3) * 4 + 255) / 256 * 256;
+    const int64_t plan_bytes = ((B + 4) * 4 + 255) / 256 * 256;
     const int64_t ws_bytes = plan_bytes + capacity * 4;
     void *ws = nullptr;
     if (fw_status_t s = get_workspace(d, (size_t)ws_bytes, stream, &ws)) return s;

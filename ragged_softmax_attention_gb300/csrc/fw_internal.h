@@ -124,7 +124,8 @@ struct PrefillParams {
     uint64_t timeout_ns;
     int *status;
     unsigned long long *counters;              // device event counters (FW_COUNTER_*)
-    int32_t *plan;        // [0] = entries, [1] = pairs, [2 .. 2 + B] = pair prefix PP
+    int32_t *plan;        // [0] = entries, [1] = pairs, [2 .. 2 + B] = pair prefix PP, [3 + B] = next entry
+                          // to hand out (head dim 128: CTAs take entries in list order as they free up)
     int32_t *list;        // entries pair_index * Hq + head, sorted by cost, longest first
     int64_t list_capacity;
     int grid;

@@ -72,17 +72,24 @@ struct PrefillCfg {
     static constexpr int kBarIssued = kBarDrain + 2;             // [2]
     static constexpr int kBarPHalf = kBarIssued + 2;             // [2]
     static constexpr int kBarPvhDone = kBarPHalf + 2;            // [2]
-    static constexpr int kNumBars = kBarPvhDone + 2;
-    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kSchedSlots = 4;                        // unit records in flight
+    static constexpr int kBarSchedFull = kBarPvhDone + 2;        // [kSchedSlots]
+    static constexpr int kBarSchedEmpty = kBarSchedFull + kSchedSlots;  // [kSchedSlots]
+    static constexpr int kNumBars = kBarSchedEmpty + kSchedSlots;
+    // Readers of a unit record: the two issuers and the eight softmax warps.
+    static constexpr int kSchedReaders = 2 + 8;
+    static constexpr int kOffSched = kOffBar + kNumBars * 8;
+    static constexpr int kOffMisc = kOffSched + 64 * kSchedSlots;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA exceeded");
     // warpgroup 0: producer (warp 0), MMA (warp 1), two idle warps; then one
     // softmax warpgroup per query tile
     static constexpr int kThreads = 128 + kNumQ * 128;
     // hd 128 launches 384 threads at 168 registers (64512 in all); the split
-    // below gives 128 x 72 + 256 x 216 = 64512 <= 64512.
-    static constexpr uint32_t kRegsControl = 72;
-    static constexpr uint32_t kRegsSoftmax = 216;
+    // below gives 128 x 80 + 256 x 208 = 63488 <= 64512.  (72 / 216 left
+    // the control warps, which also run the unit queue, short: 2.5% slower.)
+    static constexpr uint32_t kRegsControl = 80;
+    static constexpr uint32_t kRegsSoftmax = 208;
     static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= 384 * 168, "register split");
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kKvTile, false, false);
@@ -148,6 +155,7 @@ struct PUnit {
     int nkv[2];        // KV tiles each query tile walks
     int nmax;
 };
+static_assert(sizeof(PUnit) <= 64, "a unit record fills one 64-byte slot");
 
 __device__ __forceinline__ void decode_entry(const PrefillParams &p, int e, PUnit &u, int num_q) {
     const int32_t *PP = p.plan + 2;
@@ -205,6 +213,9 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
     uint64_t *issued = bars + C::kBarIssued;         // step handoff between the two issuers
     uint64_t *p_half = bars + C::kBarPHalf;          // first half of P (keys 0..63) written
     uint64_t *pvh_done = bars + C::kBarPvhDone;      // the PV of that half complete
+    uint64_t *sched_full = bars + C::kBarSchedFull;  // unit record k written by the producer
+    uint64_t *sched_empty = bars + C::kBarSchedEmpty;  // unit record k read by every role
+    PUnit *sched = reinterpret_cast<PUnit *>(smem + C::kOffSched);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
 
@@ -220,6 +231,9 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
             mbar_init(&issued[i], 1);
             mbar_init(&p_half[i], 4); mbar_init(&pvh_done[i], 1);
         }
+        for (int i = 0; i < C::kSchedSlots; ++i) {
+            mbar_init(&sched_full[i], 1); mbar_init(&sched_empty[i], C::kSchedReaders);
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -234,6 +248,18 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
     pdl_wait();                                    // the plan of this call is written
     const int count = p.plan[0];                   // (read only after the wait)
     const WaitCtx wc{p.status, p.timeout_ns, abort_flag};
+    // Units are handed out in list order (longest first) to whichever CTA
+    // frees up: the producer takes the next entry from the call's counter
+    // and publishes the decoded unit in shared memory for the other roles,
+    // who so never walk the list themselves.  A record with seq < 0 ends
+    // the CTA's work.  (A static snake over the list left CTAs finishing
+    // 2.06-2.23 ms apart on the varlen workload.)
+    // Readers copy the fields they use out of record k, then free it.
+    auto wait_unit = [&](int k) -> const PUnit * {
+        const int sl = k % C::kSchedSlots;
+        return mbar_wait(&sched_full[sl], (k / C::kSchedSlots) & 1, wc) ? &sched[sl] : nullptr;
+    };
+    auto free_unit = [&](int k) { mbar_arrive(&sched_empty[k % C::kSchedSlots]); };
 
     if (warp < 4) {
       setmaxnreg_dec<C::kRegsControl>();
@@ -243,10 +269,17 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
             uint32_t rp = 0, nu = 0, issued = 0;
             bool ok = true;
             for (int k = 0; ok; ++k, ++nu) {
-                const int idx = snake_index(k, p.grid);
-                if (idx >= count) break;
+                const int idx = atomicAdd(p.plan + 3 + p.B, 1);      // the call's next entry
                 PUnit u;
-                decode_entry(p, __ldg(p.list + idx), u, NQ);
+                if (idx < count) decode_entry(p, __ldg(p.list + idx), u, NQ);
+                else u.seq = -1;
+                {
+                    const int sl = k % C::kSchedSlots;
+                    if (!mbar_wait(&sched_empty[sl], ((k / C::kSchedSlots) & 1) ^ 1, wc)) break;
+                    sched[sl] = u;
+                    mbar_arrive(&sched_full[sl]);          // release: the record is visible to its readers
+                }
+                if (u.seq < 0) break;
                 if (!mbar_wait(q_empty, (nu & 1) ^ 1, wc)) break;
                 uint32_t bytes = 0;
                 for (int x = 0; x < NQ; ++x) if (u.tile[x] >= 0) bytes += C::kTileBytes;
@@ -357,20 +390,21 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
             uint32_t other = 0;                            // steps the other tile issued so far
             bool ok = true;
             for (int k = 0; ok; ++k) {
-                const int idx = snake_index(k, p.grid);
-                if (idx >= count) break;
-                PUnit u;
-                decode_entry(p, __ldg(p.list + idx), u, NQ);
+                const PUnit *ur = wait_unit(k);
+                const bool got = ur && ur->seq >= 0;
+                const int nmax = got ? ur->nmax : 0;
+                const int n = got ? ur->nkv[x] : 0;
+                const int n_other = got ? ur->nkv[1 - x] : 0;
+                free_unit(k);
+                if (!got) break;
                 if (!mbar_wait(q_full, nu & 1, wc)) break;
                 tc_fence_after();
                 const uint32_t r0 = rp;                       // K_j at r0 + 2j, V_j at r0 + 2j + 1
                 auto pos_k = [&](int j) { return r0 + 2u * (uint32_t)j; };
                 auto pos_v = [&](int j) { return r0 + 2u * (uint32_t)j + 1u; };
-                const int n = u.nkv[x];
-                const int n_other = u.nkv[1 - x];
                 constexpr int step = 1;                       // QK_{j+1} goes out with PV_j
                 // prologue: the first `step` QKs
-                for (int j = 0; j < step && j < u.nmax && ok; ++j) {
+                for (int j = 0; j < step && j < nmax && ok; ++j) {
                     const uint32_t rk = pos_k(j);
                     if (j < n) {
                         if (!wait_tile(rk)) { ok = false; break; }
@@ -382,10 +416,10 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                         ok = release_unused(rk);
                     }
                 }
-                for (int j = 0; j < u.nmax && ok; ++j) {
+                for (int j = 0; j < nmax && ok; ++j) {
                     const int jn = j + step;
                     const uint32_t rv = pos_v(j);
-                    const uint32_t rk = jn < u.nmax ? pos_k(jn) : 0u;
+                    const uint32_t rk = jn < nmax ? pos_k(jn) : 0u;
                     const bool mine = j < n, next_mine = jn < n;
                     if (mine) {
                         {
@@ -420,11 +454,11 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                     } else if (!release_unused(rv)) {
                         ok = false; break;
                     }
-                    if (jn < u.nmax && !next_mine && !release_unused(rk)) { ok = false; break; }
+                    if (jn < nmax && !next_mine && !release_unused(rk)) { ok = false; break; }
                 }
                 if (!ok) break;
                 other += n_other;
-                rp = r0 + (uint32_t)(2 * u.nmax);
+                rp = r0 + (uint32_t)(2 * nmax);
                 mma_commit(q_empty);
                 ++nu;
             }
@@ -451,16 +485,23 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
             mbar_wait(&pv_done[x], i & 1u, wc);
             tc_fence_after();
         };
+        // The softmax warps hold their unit's record until its epilogue, which
+        // reads the output row from it (fewer registers across the tile loop).
         for (int k = 0;; ++k) {
-            const int idx = snake_index(k, p.grid);
-            if (idx >= count) break;
-            PUnit u;
-            decode_entry(p, __ldg(p.list + idx), u, NQ);
-            if (u.tile[x] < 0) continue;
-            const int q_row = u.tile[x] * kQTile + row;          // row within the sequence
-            const bool row_valid = q_row < u.s.Lq;
-            const int lim = !p.causal ? u.s.Lk : max(0, min(u.s.Lk, q_row + u.s.Lk - u.s.Lq + 1));
-            const int nkv = u.nkv[x];
+            const PUnit *ur = wait_unit(k);
+            const bool got = ur && ur->seq >= 0;
+            const int tile = got ? ur->tile[x] : -1;
+            if (tile < 0) {
+                __syncwarp();
+                if (lane == 0) free_unit(k);
+                if (!got) break;
+                continue;
+            }
+            const int Lq = ur->s.Lq, Lk = ur->s.Lk;
+            const int nkv = ur->nkv[x];
+            const int q_row = tile * kQTile + row;               // row within the sequence
+            const bool row_valid = q_row < Lq;
+            const int lim = !p.causal ? Lk : max(0, min(Lk, q_row + Lk - Lq + 1));
             float m_ref = kNegInf, l_sum = 0.f;
             for (int j = 0; j < nkv; ++j, ++s_cnt) {
                 mbar_wait(&s_full[x], s_cnt & 1u, wc);
@@ -685,8 +726,11 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                 l_sum += tsum0 + tsum1;
             }
             // ------------------------------------------------------ epilogue
+            const int q0 = sched[k % C::kSchedSlots].s.q0, head = sched[k % C::kSchedSlots].h;
+            __syncwarp();
+            if (lane == 0) free_unit(k);
             __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(p.out) +
-                                  (int64_t)(u.s.q0 + q_row) * p.out_stride[0] + (int64_t)u.h * p.out_stride[1];
+                                  (int64_t)(q0 + q_row) * p.out_stride[0] + (int64_t)head * p.out_stride[1];
             if (nkv > 0) {
                 wait_pv(pv_units++);
                 const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
@@ -712,7 +756,7 @@ varlen_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_cons
                 for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4 *>(orow)[c] = make_uint4(0, 0, 0, 0);
             }
             if (row_valid && p.lse)
-                p.lse[(int64_t)(u.s.q0 + q_row) * p.lse_stride[0] + (int64_t)u.h * p.lse_stride[1]] =
+                p.lse[(int64_t)(q0 + q_row) * p.lse_stride[0] + (int64_t)head * p.lse_stride[1]] =
                     l_sum > 0.f ? (m_ref + __log2f(l_sum)) * 0.69314718055994531f : kNegInf;
         }
     }
@@ -1278,6 +1322,7 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const __grid_constan
     if (tid == 0) {
         p.plan[0] = (int64_t)NP * p.Hq <= p.list_capacity ? NP * p.Hq : 0;
         p.plan[1] = NP;
+        p.plan[3 + p.B] = 0;                         // the hd-128 kernel's next entry to hand out
         if ((int64_t)NP * p.Hq > p.list_capacity) record_error(p.status, 3);
     }
 }
