@@ -110,9 +110,11 @@ struct DecodeParams {
 };
 
 // One varlen prefill launch.  The plan kernel lists the units (sequence,
-// query head, pair of consecutive 128-row query tiles) longest first; CTA c
-// takes list entries c, 2*grid-1-c, 2*grid+c, ... (a snake over the sorted
-// list, which balances the sums).
+// query head, pair of consecutive 128-row query tiles) longest first.  At
+// head dim 128 the CTAs take list entries in order as they free up (a
+// counter in the plan); the CTA pairs at head dim 256 take entries c,
+// 2*pairs-1-c, 2*pairs+c, ... (a snake over the sorted list, which balances
+// the sums).
 struct PrefillParams {
     int B, Hq, Hkv, G, causal, Dv;
     int online;           // 0: static anchor with check and replay; 1: online softmax, conditional rescale

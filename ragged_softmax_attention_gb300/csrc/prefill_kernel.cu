@@ -180,11 +180,6 @@ __device__ __forceinline__ void decode_entry(const PrefillParams &p, int e, PUni
     }
 }
 
-// Static snake over the cost-sorted list: entry index of this CTA's k-th unit.
-__device__ __forceinline__ int snake_index(int k, int grid) {
-    return k * grid + ((k & 1) ? (grid - 1 - (int)blockIdx.x) : (int)blockIdx.x);
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
@@ -1210,7 +1205,8 @@ varlen_prefill_pair_kernel(const __grid_constant__ PrefillParams p, const __grid
 //
 // One block.  PP[i] = exclusive prefix of the unit pairs per sequence; each
 // (pair, head) entry goes into the list ordered by its KV-tile cost, largest
-// first (counting sort), so that the snake assignment balances the CTAs.
+// first (counting sort): handed out in that order as CTAs free up (head dim
+// 128) or in a snake over CTA pairs (head dim 256), it balances the CTAs.
 // Sequences whose cumulative lengths reach past the packed tensors are left
 // out and reported in the status word.
 __global__ void __launch_bounds__(1024) prefill_plan_kernel(const __grid_constant__ PrefillParams p, int num_q) {
