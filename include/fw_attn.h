@@ -390,11 +390,13 @@ int64_t fw_launch_count(void);
  * device.  Fields are written on success.
  *
  * Scheduling: the (batch row, KV head, row group) units are laid end to end
- * in the order of their 128-key tiles; each persistent CTA takes equal
- * contiguous tile ranges (span decided on the device from seq_lens, never
- * below min_span_tiles unless forced), so CTAs differ by at most one tile of
- * work.  A unit cut by range boundaries becomes pieces whose FP32 partials a
- * combine kernel merges.
+ * in the order of their 128-key tiles, each preceded by a few empty slots
+ * that stand for the cost of starting a piece (none for the latent layout);
+ * each persistent CTA takes equal contiguous ranges of that sequence (span
+ * decided on the device from seq_lens, never below min_span_tiles unless
+ * forced), so CTAs carry equal work, piece starts included.  A unit cut by
+ * range boundaries becomes pieces whose FP32 partials a combine kernel
+ * merges.
  */
 typedef struct {
     int32_t group;            /* G = Hq / Hkv */
