@@ -78,7 +78,7 @@ struct PrefillCfg {
     static constexpr int kNumBars = kBarSchedEmpty + kSchedSlots;
     // Readers of a unit record: the two issuers and the eight softmax warps.
     static constexpr int kSchedReaders = 2 + 8;
-    static constexpr int kOffSched = kOffBar + kNumBars * 8;
+    static constexpr int kOffSched = (kOffBar + kNumBars * 8 + 63) / 64 * 64;
     static constexpr int kOffMisc = kOffSched + 64 * kSchedSlots;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA exceeded");
@@ -148,14 +148,17 @@ __device__ __forceinline__ int tile_kv_tiles(const PrefillParams &p, const Seq &
 }
 
 // One unit of work: (sequence, head, pair of query tiles 2*pair and 2*pair+1).
-struct PUnit {
+// 64 bytes, 16-aligned: a unit record is copied whole into the queues, the
+// partner CTA's in four 16-byte stores.
+struct alignas(16) PUnit {
     int seq, h, g;
     Seq s;
     int tile[2];       // query tile index, -1 if absent
     int nkv[2];        // KV tiles each query tile walks
     int nmax;
+    int pad_[3];
 };
-static_assert(sizeof(PUnit) <= 64, "a unit record fills one 64-byte slot");
+static_assert(sizeof(PUnit) == 64, "a unit record fills one 64-byte slot");
 
 __device__ __forceinline__ void decode_entry(const PrefillParams &p, int e, PUnit &u, int num_q) {
     const int32_t *PP = p.plan + 2;
@@ -795,18 +798,21 @@ constexpr int kPairBarSFull = kPairBarQEmpty + 1;              // [2]
 constexpr int kPairBarPFull = kPairBarSFull + 2;               // [2]
 constexpr int kPairBarPvDone = kPairBarPFull + 2;              // [2]
 constexpr int kPairBarDrain = kPairBarPvDone + 2;              // [1]
-constexpr int kPairNumBars = kPairBarDrain + 1;
-constexpr int kPairOffMisc = kPairOffBar + kPairNumBars * 8;
+constexpr int kPairSchedSlots = 4;                             // unit records in flight
+constexpr int kPairBarSchedFull = kPairBarDrain + 1;           // [kPairSchedSlots], each CTA's own
+constexpr int kPairBarSchedEmpty = kPairBarSchedFull + kPairSchedSlots;  // [kPairSchedSlots], CTA 0's
+constexpr int kPairNumBars = kPairBarSchedEmpty + kPairSchedSlots;
+// Readers of a unit record that arrive on CTA 0's sched_empty: CTA 0's issuer
+// and four softmax warps, CTA 1's producer and (one arrival for) its softmax
+// warps.
+constexpr int kPairSchedReaders = 1 + 4 + 1 + 1;
+constexpr int kPairOffSched = (kPairOffBar + kPairNumBars * 8 + 63) / 64 * 64;   // 16-byte stores land here
+constexpr int kPairOffMisc = kPairOffSched + 64 * kPairSchedSlots;
 constexpr int kPairSmemBytes = kPairOffMisc + 16 + 1024;
 static_assert(kPairSmemBytes <= 232448, "shared memory budget of one CTA exceeded");
 constexpr uint32_t kPairIdescQK = idesc_bf16_f32(256, 128, false, false);
 constexpr uint32_t kPairIdescPV = idesc_bf16_f32(256, 256, false, true);
 
-// Snake over the cost-sorted list, one entry per CTA pair.
-__device__ __forceinline__ int pair_snake_index(int k) {
-    const int nc = (int)gridDim.x >> 1, c = (int)blockIdx.x >> 1;
-    return k * nc + ((k & 1) ? (nc - 1 - c) : c);
-}
 
 template <bool kOnline>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
@@ -826,6 +832,9 @@ varlen_prefill_pair_kernel(const __grid_constant__ PrefillParams p, const __grid
     uint64_t *p_full = bars + kPairBarPFull;             // CTA 0's: its 4 warps + one arrival of CTA 1
     uint64_t *pv_done = bars + kPairBarPvDone;
     uint64_t *drain = bars + kPairBarDrain;              // CTA 0's MMAs all complete
+    uint64_t *sched_full = bars + kPairBarSchedFull;     // unit record k in this CTA
+    uint64_t *sched_empty = bars + kPairBarSchedEmpty;   // CTA 0's: record k read in both CTAs
+    PUnit *sched = reinterpret_cast<PUnit *>(smem + kPairOffSched);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kPairOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kPairOffMisc + 4);
 
@@ -839,6 +848,9 @@ varlen_prefill_pair_kernel(const __grid_constant__ PrefillParams p, const __grid
         mbar_init(q_empty, 1);
         for (int i = 0; i < 2; ++i) { mbar_init(&s_full[i], 1); mbar_init(&p_full[i], 5); mbar_init(&pv_done[i], 1); }
         mbar_init(drain, 1);
+        for (int i = 0; i < kPairSchedSlots; ++i) {
+            mbar_init(&sched_full[i], 1); mbar_init(&sched_empty[i], kPairSchedReaders);
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -854,6 +866,20 @@ varlen_prefill_pair_kernel(const __grid_constant__ PrefillParams p, const __grid
     pdl_wait();                                    // the plan of this call is written
     const int count = p.plan[0];                   // (read only after the wait)
     const WaitCtx wc{p.status, p.timeout_ns, abort_flag};
+    // Units are handed out in list order to whichever pair frees up: CTA 0's
+    // producer takes the next entry from the call's counter, decodes it and
+    // writes the unit record into both CTAs' queues; every other role of
+    // the pair reads its own CTA's copy and frees it on CTA 0's barrier.  A
+    // record with seq < 0 ends the pair's work.
+    auto wait_unit = [&](int k) -> const PUnit * {
+        const int sl = k % kPairSchedSlots;
+        return mbar_wait_cluster(&sched_full[sl], (k / kPairSchedSlots) & 1, wc) ? &sched[sl] : nullptr;
+    };
+    auto free_unit = [&](int k) {
+        const int sl = k % kPairSchedSlots;
+        if (rank == 0) mbar_arrive(&sched_empty[sl]);
+        else mbar_arrive_cluster(cluster_addr(&sched_empty[sl], 0));
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -862,10 +888,28 @@ varlen_prefill_pair_kernel(const __grid_constant__ PrefillParams p, const __grid
             uint32_t rp = 0, nu = 0;
             bool ok = true;
             for (int k = 0; ok; ++k, ++nu) {
-                const int idx = pair_snake_index(k);
-                if (idx >= count) break;
                 PUnit u;
-                decode_entry(p, __ldg(p.list + idx), u, 2);
+                if (rank == 0) {
+                    const int idx = atomicAdd(p.plan + 3 + p.B, 1);    // the call's next entry
+                    if (idx < count) decode_entry(p, __ldg(p.list + idx), u, 2);
+                    else u.seq = -1;
+                    const int sl = k % kPairSchedSlots;
+                    if (!mbar_wait_cluster(&sched_empty[sl], ((k / kPairSchedSlots) & 1) ^ 1, wc)) break;
+                    sched[sl] = u;
+                    const uint4 *w = reinterpret_cast<const uint4 *>(&u);
+                    const uint32_t peer = cluster_addr(&sched[sl], 1);
+#pragma unroll
+                    for (int i = 0; i < (int)sizeof(PUnit) / 16; ++i)
+                        st_cluster_v4(peer + 16u * i, w[i].x, w[i].y, w[i].z, w[i].w);
+                    mbar_arrive(&sched_full[sl]);
+                    mbar_arrive_cluster(cluster_addr(&sched_full[sl], 1));   // release: the copy is visible
+                } else {
+                    const PUnit *ur = wait_unit(k);
+                    if (ur) u = *ur;
+                    else u.seq = -1;
+                    free_unit(k);
+                }
+                if (u.seq < 0) break;
                 if (!mbar_wait(q_empty, (nu & 1) ^ 1, wc)) break;
                 // A CTA whose tile does not exist loads its partner's rows
                 // (finite values; its outputs are never written).
@@ -958,14 +1002,14 @@ varlen_prefill_pair_kernel(const __grid_constant__ PrefillParams p, const __grid
             auto commit_pv = [&]() { mma_commit_pair(&pv_done[pv_cnt & 1u]); ++pv_cnt; };
             bool ok = true;
             for (int k = 0; ok; ++k) {
-                const int idx = pair_snake_index(k);
-                if (idx >= count) break;
-                PUnit u;
-                decode_entry(p, __ldg(p.list + idx), u, 2);
+                const PUnit *ur = wait_unit(k);
+                const bool got = ur && ur->seq >= 0;
+                const int n = got ? ur->nmax : 0;
+                free_unit(k);
+                if (!got) break;
                 if (!mbar_wait(q_full, nu & 1, wc)) break;
                 tc_fence_after();
                 const uint32_t r0 = rp;
-                const int n = u.nmax;
                 auto pos_k = [&](int j) { return r0 + (uint32_t)ring_pos_k(j, n); };
                 auto pos_v = [&](int j) { return r0 + (uint32_t)ring_pos_v(j, n); };
                 for (int j = 0; j < 2 && j < n && ok; ++j) {
@@ -1017,15 +1061,29 @@ varlen_prefill_pair_kernel(const __grid_constant__ PrefillParams p, const __grid
             tc_fence_after();
         };
         for (int k = 0;; ++k) {
-            const int idx = pair_snake_index(k);
-            if (idx >= count) break;
-            PUnit u;
-            decode_entry(p, __ldg(p.list + idx), u, 2);
-            const bool tile_ok = u.tile[rank] >= 0;
-            const int q_row = (tile_ok ? u.tile[rank] : u.tile[0]) * kQTile + row;
-            const bool row_valid = tile_ok && q_row < u.s.Lq;
-            const int lim = !p.causal ? u.s.Lk : max(0, min(u.s.Lk, q_row + u.s.Lk - u.s.Lq + 1));
-            const int n = u.nmax;
+            const PUnit *ur = wait_unit(k);
+            bool got = ur && ur->seq >= 0;
+            const int tile0 = got ? ur->tile[0] : 0, tile_r = got ? ur->tile[rank] : -1;
+            const int q0 = got ? ur->s.q0 : 0, Lq = got ? ur->s.Lq : 0, Lk = got ? ur->s.Lk : 0;
+            const int head = got ? ur->h : 0;
+            const int n = got ? ur->nmax : 0;
+            // CTA 0's warps free the record one by one; CTA 1's meet first and
+            // send one cluster-scope arrival.
+            __syncwarp();
+            if (rank == 0) {
+                if (lane == 0) free_unit(k);
+            } else {
+                named_bar_sync(2, 128);
+                if (warp == 4 && lane == 0) free_unit(k);
+                // After an abort (some wait ran out) all four warps leave
+                // together, so none is left alone at a named barrier.
+                if (*abort_flag) got = false;
+            }
+            if (!got) break;
+            const bool tile_ok = tile_r >= 0;
+            const int q_row = (tile_ok ? tile_r : tile0) * kQTile + row;
+            const bool row_valid = tile_ok && q_row < Lq;
+            const int lim = !p.causal ? Lk : max(0, min(Lk, q_row + Lk - Lq + 1));
             float m_ref = kNegInf, l_sum = 0.f;
             for (int j = 0; j < n; ++j, ++s_cnt) {
                 const uint32_t sb = s_cnt & 1u;
@@ -1162,7 +1220,7 @@ varlen_prefill_pair_kernel(const __grid_constant__ PrefillParams p, const __grid
             }
             // ------------------------------------------------------ epilogue
             __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(p.out) +
-                                  (int64_t)(u.s.q0 + q_row) * p.out_stride[0] + (int64_t)u.h * p.out_stride[1];
+                                  (int64_t)(q0 + q_row) * p.out_stride[0] + (int64_t)head * p.out_stride[1];
             if (n > 0) {
                 wait_pv(pv_cnt + n - 1);
                 const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
@@ -1188,7 +1246,7 @@ varlen_prefill_pair_kernel(const __grid_constant__ PrefillParams p, const __grid
                 for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4 *>(orow)[c] = make_uint4(0, 0, 0, 0);
             }
             if (row_valid && p.lse)
-                p.lse[(int64_t)(u.s.q0 + q_row) * p.lse_stride[0] + (int64_t)u.h * p.lse_stride[1]] =
+                p.lse[(int64_t)(q0 + q_row) * p.lse_stride[0] + (int64_t)head * p.lse_stride[1]] =
                     l_sum > 0.f ? (m_ref + __log2f(l_sum)) * 0.69314718055994531f : kNegInf;
             pv_cnt += n;
         }
