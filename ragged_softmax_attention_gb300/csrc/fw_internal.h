@@ -110,11 +110,9 @@ struct DecodeParams {
 };
 
 // One varlen prefill launch.  The plan kernel lists the units (sequence,
-// query head, pair of consecutive 128-row query tiles) longest first.  At
-// head dim 128 the CTAs take list entries in order as they free up (a
-// counter in the plan); the CTA pairs at head dim 256 take entries c,
-// 2*pairs-1-c, 2*pairs+c, ... (a snake over the sorted list, which balances
-// the sums).
+// query head, pair of consecutive 128-row query tiles) longest first; the
+// CTAs (CTA pairs at head dim 256) take list entries in that order as they
+// free up, from a counter in the plan.
 struct PrefillParams {
     int B, Hq, Hkv, G, causal, Dv;
     int online;           // 0: static anchor with check and replay; 1: online softmax, conditional rescale
@@ -127,7 +125,7 @@ struct PrefillParams {
     int *status;
     unsigned long long *counters;              // device event counters (FW_COUNTER_*)
     int32_t *plan;        // [0] = entries, [1] = pairs, [2 .. 2 + B] = pair prefix PP, [3 + B] = next entry
-                          // to hand out (head dim 128: CTAs take entries in list order as they free up)
+                          // to hand out (CTAs take entries in list order as they free up)
     int32_t *list;        // entries pair_index * Hq + head, sorted by cost, longest first
     int64_t list_capacity;
     int grid;

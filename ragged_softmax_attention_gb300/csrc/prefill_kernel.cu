@@ -1263,8 +1263,8 @@ varlen_prefill_pair_kernel(const __grid_constant__ PrefillParams p, const __grid
 //
 // One block.  PP[i] = exclusive prefix of the unit pairs per sequence; each
 // (pair, head) entry goes into the list ordered by its KV-tile cost, largest
-// first (counting sort): handed out in that order as CTAs free up (head dim
-// 128) or in a snake over CTA pairs (head dim 256), it balances the CTAs.
+// first (counting sort): handed out in that order as CTAs (or CTA pairs)
+// free up, it balances them.
 // Sequences whose cumulative lengths reach past the packed tensors are left
 // out and reported in the status word.
 __global__ void __launch_bounds__(1024) prefill_plan_kernel(const __grid_constant__ PrefillParams p, int num_q) {
@@ -1376,7 +1376,7 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const __grid_constan
     if (tid == 0) {
         p.plan[0] = (int64_t)NP * p.Hq <= p.list_capacity ? NP * p.Hq : 0;
         p.plan[1] = NP;
-        p.plan[3 + p.B] = 0;                         // the hd-128 kernel's next entry to hand out
+        p.plan[3 + p.B] = 0;                         // the attention kernel's next entry to hand out
         if ((int64_t)NP * p.Hq > p.list_capacity) record_error(p.status, 3);
     }
 }
