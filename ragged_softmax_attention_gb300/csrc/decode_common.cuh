@@ -35,12 +35,31 @@ __device__ __forceinline__ int row_tiles(const DecodeParams &p, int n) {
     return ceil_div_i(n, kKvTile) - window_first_key(p, n) / kKvTile;
 }
 
+// The per-row slot prefix PB[0..B] and the sequence lengths, copied into
+// shared memory once per CTA when the batch fits (else read in place): the
+// piece walk then finds the next unit without a global load, which at every
+// piece boundary cost the softmax warps ~2,000 cycles.  All threads of the
+// CTA call it, after the plan is visible.
+struct RowTables {
+    const int32_t *pb;
+    const int32_t *lens;
+};
+__device__ __forceinline__ RowTables cache_row_tables(const DecodeParams &p, int32_t *smem_rows, int cap) {
+    if (p.B + 1 + p.B > cap) return RowTables{p.plan + 2, p.seq_lens};
+    for (int i = threadIdx.x; i <= p.B; i += blockDim.x) smem_rows[i] = p.plan[2 + i];
+    for (int i = threadIdx.x; i < p.B; i += blockDim.x) smem_rows[p.B + 1 + i] = __ldg(p.seq_lens + i);
+    __syncthreads();
+    return RowTables{smem_rows, smem_rows + p.B + 1};
+}
+
 // Walks the pieces of this CTA's tile ranges; every role runs its own copy
 // and sees the same sequence.
 struct PieceIter {
     int T, span, range, pos, end, b;
+    RowTables rt;
 
-    __device__ void init(const DecodeParams &p) {
+    __device__ void init(const DecodeParams &p, RowTables tables) {
+        rt = tables;
         T = __ldg(p.plan + 0);
         span = max(1, __ldg(p.plan + 1));
         range = blockIdx.x;
@@ -56,7 +75,7 @@ struct PieceIter {
         b = -1;
     }
     __device__ bool next(const DecodeParams &p, Unit &x) {
-        const int32_t *PB = p.plan + 2;
+        const int32_t *PB = rt.pb;
         for (;;) {
             while (pos >= end) {
                 range += gridDim.x;
@@ -67,19 +86,19 @@ struct PieceIter {
                 int lo = 0, hi = p.B - 1;              // largest b with PB[b] <= pos
                 while (lo < hi) {
                     const int mid = (lo + hi + 1) >> 1;
-                    if (__ldg(PB + mid) <= pos) lo = mid; else hi = mid - 1;
+                    if (PB[mid] <= pos) lo = mid; else hi = mid - 1;
                 }
                 b = lo;
             } else {
                 // Within a range the walk only moves forward, mostly into the
                 // next row: a scan costs one dependent load per row crossed,
                 // where a fresh binary search costs log2(B).
-                while (pos >= __ldg(PB + b + 1)) ++b;
+                while (pos >= PB[b + 1]) ++b;
             }
             // Row b holds units_per_row units of vb slots: piece_cost empty
             // ones, then the unit's tb tiles.
-            const int pb0 = __ldg(PB + b);
-            const int vb = (__ldg(PB + b + 1) - pb0) / p.units_per_row;
+            const int pb0 = PB[b];
+            const int vb = (PB[b + 1] - pb0) / p.units_per_row;
             const int off = pos - pb0;
             const int u = off / vb;
             const int vl = off - u * vb;
@@ -94,7 +113,7 @@ struct PieceIter {
             x.b = b;
             x.g = u / p.row_groups;
             x.rg = u - x.g * p.row_groups;
-            x.n = clamp_len(p, __ldg(p.seq_lens + b));
+            x.n = clamp_len(p, rt.lens[b]);
             x.lo = window_first_key(p, x.n);
             const int t0 = x.lo / kKvTile;               // the walk starts at the window's first tile
             x.k_begin = (t0 + tl) * kKvTile;

@@ -90,7 +90,10 @@ struct F8Cfg {
     static constexpr int kOffRedSum = kOffRedMax + 2 * 4 * R * 4;
     static constexpr int kOffQExp = kOffRedSum + 4 * R * 4;
     static constexpr int kOffMisc = kOffQExp + 2 * NQ * 4;
-    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+    // The row tables (PB and the lengths) take what is left of the budget.
+    static constexpr int kOffRows = kOffMisc + 16;
+    static constexpr int kRowCap = (232448 - 1024 - kOffRows) / 4 > 4096 ? 4096 : (232448 - 1024 - kOffRows) / 4;
+    static constexpr int kSmemBytes = kOffRows + kRowCap * 4 + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA exceeded");
     static_assert(kRH % 4 == 0, "softmax rows per warp");
     // TMEM: two S^T buffers (Q terms side by side), then O^T (P terms side by side)
@@ -167,6 +170,7 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
     const uint32_t tmem = *tmem_slot;
     pdl_wait();                                    // the plan (and appended rows) of this call are written
     const WaitCtx wc{p.status, p.timeout_ns, abort_flag};
+    const RowTables rows = cache_row_tables(p, reinterpret_cast<int32_t *>(smem + C::kOffRows), C::kRowCap);
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -175,7 +179,7 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
         const int pages_per_tile = p.ps < kKvTile ? kKvTile / p.ps : 1;
         const uint32_t q_rows = p.head_mode == 0 ? (uint32_t)(p.G * p.tokens_per_unit) : (uint32_t)p.rows;
         PieceIter it;
-        it.init(p);
+        it.init(p, rows);
         Unit x;
         while (it.next(p, x)) {
             const int qs = ju & 1;
@@ -283,7 +287,7 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
                 return true;
             };
             PieceIter it;
-            it.init(p);
+            it.init(p, rows);
             Unit x;
             while (it.next(p, x)) {
                 const int qs = ju & 1;
@@ -337,7 +341,7 @@ paged_decode_fp8_kernel(const __grid_constant__ DecodeParams p, const __grid_con
         const int st = threadIdx.x - 64;                       // 0..255
         int jt = 0, ju = 0;
         PieceIter it;
-        it.init(p);
+        it.init(p, rows);
         Unit x;
         // ---- query terms of unit nu: BF16 row * 2^e = hi + mid, both E4M3.
         // Built for the next unit before this unit's epilogue, so that the

@@ -68,7 +68,10 @@ struct DecodeCfg {
     static constexpr int kOffRedMax = kOffBar + kNumBars * 8;
     static constexpr int kOffRedSum = kOffRedMax + 2 * 4 * NQ * 4;
     static constexpr int kOffMisc = kOffRedSum + 4 * NQ * 4;
-    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
+    // The row tables (PB and the lengths) take what is left of the budget.
+    static constexpr int kOffRows = kOffMisc + 16;
+    static constexpr int kRowCap = (232448 - 1024 - kOffRows) / 4 > 4096 ? 4096 : (232448 - 1024 - kOffRows) / 4;
+    static constexpr int kSmemBytes = kOffRows + kRowCap * 4 + 1024;   // + alignment slack
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA exceeded");
     static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, NQ, false, false);
     static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, NQ, true, false);
@@ -135,6 +138,7 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
     const uint32_t tmem = *tmem_slot;
     pdl_wait();                                    // the plan (and appended rows) of this call are written
     const WaitCtx wc{p.status, p.timeout_ns, abort_flag};
+    const RowTables rows = cache_row_tables(p, reinterpret_cast<int32_t *>(smem + C::kOffRows), C::kRowCap);
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -149,7 +153,7 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
         // MMA in flight.
         if (p.test_stall && !warp_wait(never, 0, wc, lane)) goto producer_done;
         PieceIter it;
-        it.init(p);
+        it.init(p, rows);
         Unit x;
         while (it.next(p, x)) {
             const int qs = ju & 1;
@@ -271,7 +275,7 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
                 return true;
             };
             PieceIter it;
-            it.init(p);
+            it.init(p, rows);
             Unit x;
             while (it.next(p, x)) {
                 const int qs = ju & 1;
@@ -317,7 +321,7 @@ paged_decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constan
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         int jt = 0;
         PieceIter it;
-        it.init(p);
+        it.init(p, rows);
         Unit x;
         while (it.next(p, x)) {
             int lim[NQ];
