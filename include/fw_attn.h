@@ -396,7 +396,11 @@ int64_t fw_launch_count(void);
  * decided on the device from seq_lens, never below min_span_tiles unless
  * forced), so CTAs carry equal work, piece starts included.  A unit cut by
  * range boundaries becomes pieces whose FP32 partials a combine kernel
- * merges.
+ * merges.  When the grid is a multiple of Hkv > 1 (grouped-query heads), the
+ * KV heads ride on the CTA index instead: the sequence holds the (batch row,
+ * row group) units, and CTA c walks the ranges c / Hkv, c / Hkv + grid / Hkv,
+ * ... for KV head c % Hkv, so the Hkv CTAs that read one token row's heads
+ * run side by side.
  */
 typedef struct {
     int32_t group;            /* G = Hq / Hkv */

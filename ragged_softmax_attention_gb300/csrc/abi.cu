@@ -642,6 +642,14 @@ static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_
     p.row_groups = pl.row_groups;
     p.units_per_row = latent ? (int)Hkv : (int)Hkv * pl.row_groups;
     p.range_groups = latent ? pl.row_groups : 1;
+    // Grouped-query heads: the KV heads ride on the CTA index when the grid
+    // holds whole groups of Hkv CTAs (same-box A/B at the Qwen3 shape: BF16
+    // decode 4.0 % and FP8 decode 3.5 % faster).
+    if (!latent && Hkv > 1 && pl.grid % Hkv == 0) {
+        p.head_ride = 1;
+        p.units_per_row = pl.row_groups;
+        p.range_groups = (int)Hkv;
+    }
     p.forced_span = g_opt_chunk > 0 ? pl.min_span_tiles : 0;
     p.min_span = pl.min_span_tiles;
     p.max_pieces = pl.max_pieces;
@@ -708,11 +716,15 @@ static fw_status_t paged_decode_impl(const fw_tensor_t *q, const fw_tensor_t *k_
         const uint32_t box[4] = {kv8 ? 128u : 64u, 1, rows_box, 1};
         // A 128-byte FP8 row is followed in memory by another head's row
         // unless the slots are 128 bytes apart (one KV head): promoting its
-        // fetch to 256 bytes would then pull that row through DRAM for another
-        // CTA that mostly comes too late (measured: 1.4x the algorithmic bytes
-        // with 8 KV heads).  BF16 rows of 256 bytes or more use both halves.
+        // fetch to 256 bytes pulls that row through DRAM for another CTA,
+        // which uses it from L2 when the heads ride on the CTA index (that
+        // CTA reads the same token rows at the same time) and mostly comes
+        // too late otherwise (measured: 1.4x the algorithmic bytes with 8 KV
+        // heads), so only riding heads get 256 bytes.  BF16 rows of 256 bytes
+        // or more use both halves.
         auto promo_for = [&](const fw_tensor_t *c) {
-            const bool narrow_row = kv8 && (uint64_t)Dk * esz == 128 && (uint64_t)c->stride[1] * esz != 128;
+            const bool narrow_row = kv8 && (uint64_t)Dk * esz == 128 && (uint64_t)c->stride[1] * esz != 128 &&
+                                    !p.head_ride;
             return narrow_row ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
         };
         if (fw_status_t s = encode_map(&tk, type, k_cache->data, 4, dk, sk, box, "k_cache", promo_for(k_cache)))

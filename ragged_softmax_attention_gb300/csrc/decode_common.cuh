@@ -53,16 +53,26 @@ __device__ __forceinline__ RowTables cache_row_tables(const DecodeParams &p, int
 }
 
 // Walks the pieces of this CTA's tile ranges; every role runs its own copy
-// and sees the same sequence.
+// and sees the same sequence.  With the KV heads riding on the CTA index
+// (head_ride) the CTA's head is fixed and the units of a row are its row
+// groups.
 struct PieceIter {
-    int T, span, range, pos, end, b;
+    int T, span, range, step, g_ride, pos, end, b;
     RowTables rt;
 
     __device__ void init(const DecodeParams &p, RowTables tables) {
         rt = tables;
         T = __ldg(p.plan + 0);
         span = max(1, __ldg(p.plan + 1));
-        range = blockIdx.x;
+        if (p.head_ride) {
+            range = blockIdx.x / p.Hkv;
+            step = gridDim.x / p.Hkv;
+            g_ride = blockIdx.x % p.Hkv;
+        } else {
+            range = blockIdx.x;
+            step = gridDim.x;
+            g_ride = 0;
+        }
         pos = 0;
         end = 0;
         b = -1;
@@ -78,7 +88,7 @@ struct PieceIter {
         const int32_t *PB = rt.pb;
         for (;;) {
             while (pos >= end) {
-                range += gridDim.x;
+                range += step;
                 if ((long long)range * span >= T) return false;
                 open_range();
             }
@@ -111,8 +121,13 @@ struct PieceIter {
             const int th = min(tb, tl + (end - pos));
             const int pstart = pb0 + u * vb + p.piece_cost;   // the unit's first tile
             x.b = b;
-            x.g = u / p.row_groups;
-            x.rg = u - x.g * p.row_groups;
+            if (p.head_ride) {
+                x.g = g_ride;
+                x.rg = u;
+            } else {
+                x.g = u / p.row_groups;
+                x.rg = u - x.g * p.row_groups;
+            }
             x.n = clamp_len(p, rt.lens[b]);
             x.lo = window_first_key(p, x.n);
             const int t0 = x.lo / kKvTile;               // the walk starts at the window's first tile

@@ -679,10 +679,12 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ De
     const int tb = vb - p.piece_cost;
     const int g = h / p.G;
     // Row groups that ride on the CTA index share their unit's tile range.
-    const int rg = p.range_groups > 1 ? 0
+    const int rg = (p.range_groups > 1 && !p.head_ride) ? 0
                  : p.head_mode == 0 ? t / p.tokens_per_unit
                                     : t * p.head_chunks + (h - g * p.G) / p.rows;
-    const int pstart = pb0 + (g * (p.range_groups > 1 ? 1 : p.row_groups) + rg) * vb + p.piece_cost;
+    // With the KV heads riding on the CTA index a row's units are its row groups.
+    const int unit = p.head_ride ? rg : g * (p.range_groups > 1 ? 1 : p.row_groups) + rg;
+    const int pstart = pb0 + unit * vb + p.piece_cost;
     const int npieces = (pstart + tb - 1) / span - pstart / span + 1;
     if (npieces <= 1) return;
     const float *lse_row = p.ws_lse + row * p.max_pieces;

@@ -55,7 +55,11 @@ constexpr int kLatentPairRows = 128;  // latent-head decode on CTA pairs: query 
 // total T and the range span.  CTA c then processes the global tile ranges
 // [r * span, (r + 1) * span) for r = c, c + grid, ...; the part of a unit
 // inside one range is a "piece" and writes a split-KV partial unless the unit
-// fits in a single range.
+// fits in a single range.  With head_ride the KV head leaves the unit: the
+// units are (batch row, row group), and CTA c takes KV head c % Hkv over the
+// ranges c / Hkv, c / Hkv + grid / Hkv, ...; the Hkv CTAs of one range then
+// read the heads of the same token rows at the same time (one DRAM row and,
+// for 128-byte FP8 rows, one 256-byte L2 fetch serve two of them).
 // KV-cache append ("Writing Page Attention with PyPTO", section 4.3): row
 // (b, t, kv head) of the new keys/values goes to cache token row
 // layer_base + max(slot_mapping[b * q_len + t], 0).  rows = 0: nothing.
@@ -107,6 +111,9 @@ struct DecodeParams {
     unsigned long long *counters;              // device event counters (FW_COUNTER_*)
     int test_stall;                            // test hook: the producer first waits on a barrier nothing completes
     int piece_cost;                            // empty slots before each unit's tiles in the planned sequence
+    int head_ride;        // 1: the KV heads ride on the CTA index (CTA c runs KV head c % Hkv over
+                          // ranges c / Hkv, c / Hkv + grid / Hkv, ... of the (batch row, row group)
+                          // units), so the Hkv CTAs reading one token row's heads run side by side
 };
 
 // One varlen prefill launch.  The plan kernel lists the units (sequence,

@@ -6,6 +6,8 @@ prefill's four-slot unit queue wraps round many times and its counter hands
 out every list entry, the hd-256 CTA pair walks the whole list alone, and the
 decode ranges (tiles plus the empty slots that stand for piece starts) are
 long and cross many unit boundaries, each a piece with its own partials.
+With 4 CTAs and 2 KV heads the heads ride on the CTA index: two CTA pairs,
+each pair walking the same ranges for the two heads.
 """
 import math
 
@@ -55,7 +57,7 @@ def test_prefill_with_few_ctas(fw, d, ctas, causal):
 
 
 @pytest.mark.parametrize("fp8", [False, True])
-@pytest.mark.parametrize("ctas", [1, 3])
+@pytest.mark.parametrize("ctas", [1, 3, 4])
 def test_decode_with_few_ctas(fw, fp8, ctas):
     lens = (37, 1, 900, 129, 0, 300, 2000, 5)
     wl = DecodeWorkload("few", batch=len(lens), q_len=1, num_q_heads=8, num_kv_heads=2, head_dim_qk=128,
